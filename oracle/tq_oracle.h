@@ -1,0 +1,123 @@
+/*
+ * tq_oracle.h -- plain, slow, double-precision CPU oracle for the TurboQuant
+ * KV-cache codec and the decode attention that reads its packed output.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library (kv_cache_vector_gb300/)
+ * includes, links or calls this code; only tests/, the smoke check and the
+ * CPU-baseline leg of bench.py do.  It shares no header, helper, table or
+ * constant generator with the CUDA path.
+ *
+ * Sources (page title, section):
+ *  [FS]  "TurboQuant KV Cache Compression -- Spec" (Foundry attention/spec.md):
+ *        As-Built Notes 1-2; Step 1 Random Orthogonal Rotation; Step 2
+ *        Lloyd-Max Scalar Quantization; Step 3 Packing; Codebook Generation;
+ *        Hadamard Transform Detail; Optimization: Fused dequant-dot.
+ *  [LS]  "TurboQuantEngine -- Specification" (larql turbo-quant-engine.md):
+ *        2.1 Accuracy contract; 2.2 Memory contract (4-byte norm per row).
+ *  [AC]  "CITATIONS" (Atlas feature/tq-plus-integration): N(0,1/d) codebook
+ *        note; Sparse V dequant.
+ *  [KS]  "Implementation specification: TurboAngle and TurboQuant-style KV
+ *        compression" (kvcompress): Core implementation contract; Required
+ *        invariants.
+ *
+ * Readings where the pages are silent or disagree (each is listed in the
+ * design notes of the repository):
+ *  - sign diagonal: s_i = -1 iff the top bit of the i-th splitmix64 output
+ *    (seeded with `seed`) is set; the pages say "random +-1 signs from a seed"
+ *    and name no generator.
+ *  - D is applied before H ([FS] As-Built Note 1), y = H (s . x) / sqrt(d).
+ *  - density of one rotated coordinate: (1-x^2)^((d-3)/2) on [-1,1], the exact
+ *    marginal of a uniform unit vector (the pages' "Beta(d/2,d/2) on [0,1]" is
+ *    this family after an affine change of variable, with a different shape
+ *    parameter; the exact marginal is taken).
+ *  - Lloyd iteration is run to convergence, not a fixed ~20 iterations.
+ *  - codebook values are stored as fp32 ([FS] Step 2 struct: float arrays),
+ *    and the bucket decision compares the fp32 coordinate with the fp32
+ *    boundaries: idx = #{ j : u >= beta_j } (what a binary search into
+ *    boundaries[] returns, ties going to the higher level).
+ *  - a zero row has u = 0, norm 0, and decodes to exact zeros.
+ *  - packing is a dense LSB-first bit stream, d*b/8 bytes per row
+ *    ([LS] 2.2 ceil(head_dim*bits/8); [FS] memory table K3 = 48 B per head).
+ *  - sparse-V: row t is dropped for head h iff exp(sigma_t - max_t sigma) <
+ *    threshold; dropped rows still count in the softmax denominator and
+ *    contribute a zero V row ([AC] Sparse V dequant).
+ */
+#ifndef TQ_ORACLE_H
+#define TQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* splitmix64 (Vigna): advance *state and return the next output. */
+uint64_t orc_splitmix64_next(uint64_t *state);
+
+/* s[i] in {-1,+1} for i < d, from the splitmix64 stream seeded with seed. */
+void orc_signs(uint64_t seed, int d, int8_t *s);
+
+/* In-place unnormalised Walsh-Hadamard butterfly (Sylvester order), d = 2^k.
+ * [FS] Hadamard Transform Detail. */
+void orc_fwht(double *v, int d);
+
+/* y = H (s . x) / sqrt(d)   ([FS] As-Built Note 1, Hadamard Transform Detail) */
+void orc_rotate(const int8_t *s, int d, const double *x, double *y);
+/* x = s . (H y) / sqrt(d)   (the inverse: H/sqrt(d) and D are self-inverse) */
+void orc_unrotate(const int8_t *s, int d, const double *y, double *x);
+
+/* Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d,
+ * 2^bits levels, bits in [1, 8], d >= 3.  Writes 2^bits centroids and
+ * 2^bits - 1 boundaries, ascending, in double.  Returns the number of Lloyd
+ * iterations, or -1 on bad arguments / no convergence.  [FS] Step 2,
+ * Codebook Generation. */
+int orc_codebook(int d, int bits, double *centroids, double *boundaries);
+
+/* Per-coordinate mean squared error E[(X - Q(X))^2] of a codebook under the
+ * coordinate density for dimension d (all cells, normalised density). */
+double orc_codebook_mse(int d, int bits, const double *centroids,
+                        const double *boundaries);
+
+/* Probability mass of the coordinate density on [a, b] (-1 <= a <= b <= 1). */
+double orc_density_mass(int d, double a, double b);
+
+/* Level index of the fp32 coordinate u: #{ j : u >= boundaries[j] }. */
+int orc_bucket(float u, int bits, const float *boundaries);
+
+/* Dense LSB-first bit packing of d indices of `bits` bits: d*bits/8 bytes. */
+void orc_pack(const uint8_t *idx, int d, int bits, uint8_t *out);
+void orc_unpack(const uint8_t *in, int d, int bits, uint8_t *idx);
+
+/* Encode n_rows rows of x (double; the caller converts fp32/bf16 exactly).
+ *  packed: [n_rows][d*bits/8], norms: [n_rows] fp32 (round to nearest of the
+ *  exact-in-double L2 norm).  u_out (optional, may be NULL): [n_rows][d], the
+ *  normalised rotated coordinate in double before the fp32 decision. */
+void orc_encode(const int8_t *s, int d, int bits, const float *boundaries,
+                const double *x, int64_t n_rows, uint8_t *packed, float *norms,
+                double *u_out);
+
+/* Decode: x_hat = norm * s . (H c_idx) / sqrt(d), in double. */
+void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
+                const uint8_t *packed, const float *norms, int64_t n_rows,
+                double *out);
+
+/* Decode attention in the unrotated domain (plain definition).
+ *  q:    [B][Hq][d] double
+ *  k_packed [B][Hkv][cap][d*kb/8], k_norm [B][Hkv][cap]; same for v.
+ *  Query head h reads KV head h / (Hq/Hkv).  Attends positions [0, ctx_len).
+ *  sigma_t = scale * q . k_hat_t;  p = exp(sigma - max) / sum exp(sigma - max)
+ *  o = sum_t p_t v_hat_t, where rows with exp(sigma_t - max) < sparse_thr
+ *  contribute zero (sparse_thr = 0: dense).
+ *  out: [B][Hq][d] double; kept (optional): [B][Hq] number of V rows used. */
+void orc_attention(const int8_t *s, int d, int B, int Hq, int Hkv, int64_t cap,
+                   int64_t ctx_len, int k_bits, const float *k_centroids,
+                   const uint8_t *k_packed, const float *k_norm, int v_bits,
+                   const float *v_centroids, const uint8_t *v_packed,
+                   const float *v_norm, const double *q, double scale,
+                   double sparse_thr, double *out, int64_t *kept);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_ORACLE_H */
