@@ -1,0 +1,179 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) TurboQuant KV-cache codec and the
+ * decode attention that reads its packed output.
+ *
+ * The method (page titles and sections it follows):
+ *  "TurboQuant KV Cache Compression -- Spec" (Foundry attention/spec.md):
+ *     Step 1 Random Orthogonal Rotation, As-Built Notes 1-2 (signs before the
+ *     Hadamard transform; L2-norm normalisation), Step 2 Lloyd-Max Scalar
+ *     Quantization, Step 3 Packing, Codebook Generation, Hadamard Transform
+ *     Detail, API (fa_tq_init / fa_tq_quantize / fa_tq_dequantize /
+ *     fa_tq_attention_cached), Optimization: Fused dequant-dot.
+ *  "TurboQuantEngine -- Specification" (larql): 2.2 Memory contract (fp32
+ *     norm + ceil(head_dim*bits/8) bytes per head and row), 6 P1 follow-ups
+ *     (incremental encode of the new row only).
+ *  "CITATIONS" (Atlas): Sparse V dequant; Asymmetric K/V dtype.
+ *
+ * Row codec.  For a row x of length d (a power of two, 8 <= d <= 256):
+ *   n = ||x||_2 (stored as fp32);  y = H (s . x) / sqrt(d)  with s the seeded
+ *   +-1 diagonal and H the Sylvester Hadamard matrix;  u = y / n (u = 0 when
+ *   n = 0);  idx_i = #{ j : u_i >= beta_j } over the 2^bits - 1 fp32
+ *   boundaries of the Lloyd-Max codebook of one coordinate of a uniform unit
+ *   vector in R^d;  the indices are packed as a dense LSB-first bit stream
+ *   (index i in stream bits [i*bits, i*bits+bits); stream bit k is bit k%8 of
+ *   byte k/8), d*bits/8 bytes per row.  Decode: x_hat = n * s . (H c_idx) /
+ *   sqrt(d).  The sign diagonal: s_i = -1 iff the top bit of the i-th output
+ *   of splitmix64 seeded with `seed` is set.
+ *
+ * Conventions for every call below:
+ *  - Device buffers are owned by the caller.  The library allocates only host
+ *    memory, and only in tq_plan_create.  No call allocates device memory.
+ *  - Hot calls (tq_encode, tq_decode, tq_append, tq_attn_decode) validate
+ *    their arguments on the host, return an error before launching anything
+ *    if they are wrong, and otherwise enqueue their kernels on `stream`
+ *    (asynchronous; a NULL stream is the legacy default stream).  A launch
+ *    failure is reported as TQ_ERR_CUDA (see tq_last_cuda_error); faults
+ *    during execution surface at the caller's next synchronisation.
+ *  - Pointers to device memory must be 16-byte aligned (TQ_ERR_ALIGNMENT).
+ *  - Kernels never trap; a kernel that gives up a bounded wait records it in
+ *    a device status word read by tq_device_status.
+ *  - Calls are thread-safe as long as plans are not destroyed while in use.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, without the CUDA headers. */
+typedef struct CUstream_st *tq_stream_t;
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, Hq % Hkv != 0 ... */
+    TQ_ERR_UNSUPPORTED = 2, /* d or bits or dtype outside the supported set   */
+    TQ_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned        */
+    TQ_ERR_RANGE = 4,       /* pos / ctx_len outside the cache capacity       */
+    TQ_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required     */
+    TQ_ERR_CUDA = 6,        /* a CUDA runtime call failed                      */
+    TQ_ERR_NOMEM = 7        /* host allocation failed                          */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1 } tq_dtype;
+
+/* Opaque plan: d, seed, sign diagonal and the fp32 codebooks for bits 2..4
+ * (the pages' fa_tq_state).  Host memory only. */
+typedef struct tq_plan tq_plan;
+
+/* One layer of a packed KV cache, caller-owned device memory:
+ *   k_packed [B][Hkv][cap][d*k_bits/8]   k_norm [B][Hkv][cap]  (fp32)
+ *   v_packed [B][Hkv][cap][d*v_bits/8]   v_norm [B][Hkv][cap]  (fp32)
+ * (the pages' per-token compressed entry: packed indices per head plus the
+ * stored norm, laid out per head and position as in their per-head
+ * [n_kv_head, max_seq, head_dim] cache). */
+typedef struct {
+    uint8_t *k_packed;
+    float *k_norm;
+    uint8_t *v_packed;
+    float *v_norm;
+    int64_t cap;
+} tq_cache_view;
+
+/* Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d
+ * (density proportional to (1-x^2)^((d-3)/2) on [-1,1]), 2^bits levels:
+ * "TurboQuant KV Cache Compression -- Spec", Step 2 and Codebook Generation
+ * (Lloyd iteration -- centroids are conditional means of their cells,
+ * boundaries are midpoints -- run to convergence).  Pure host function,
+ * deterministic.  d >= 3, 1 <= bits <= 4.
+ *   centroids:  2^bits doubles, ascending (caller-owned host memory)
+ *   boundaries: 2^bits - 1 doubles, ascending, middle one exactly 0
+ * Errors: TQ_ERR_INVALID_ARG (null), TQ_ERR_UNSUPPORTED (d or bits). */
+tq_status tq_codebook_init(int d, int bits, double *centroids, double *boundaries);
+
+/* Build a plan for head dimension d (power of two, 8..256) and sign seed
+ * (the pages' fa_tq_init(head_dim, config, seed)).  Computes the codebooks
+ * for bits 2, 3, 4 and the sign diagonal.  *out receives a host object that
+ * the caller releases with tq_plan_destroy. */
+tq_status tq_plan_create(int d, uint64_t seed, tq_plan **out);
+tq_status tq_plan_destroy(tq_plan *plan);
+
+/* Inspection helpers (host memory): the d signs (+1/-1) of the plan, and the
+ * fp32 codebook the kernels use for `bits` (2^bits centroids, 2^bits - 1
+ * boundaries). */
+tq_status tq_plan_signs(const tq_plan *plan, int8_t *signs);
+tq_status tq_plan_codebook(const tq_plan *plan, int bits, float *centroids, float *boundaries);
+
+/* Encode n_rows rows ("fa_tq_quantize" on a batch of rows).
+ *   x:      [n_rows][d] fp32 or bf16 (x_dtype), device, 16-byte aligned
+ *   packed: [n_rows][d*bits/8] bytes, device, 16-byte aligned
+ *   norms:  [n_rows] fp32, device
+ * bits in {2,3,4}.  n_rows = 0 is a no-op. */
+tq_status tq_encode(const tq_plan *plan, int bits, const void *x, tq_dtype x_dtype,
+                    int64_t n_rows, uint8_t *packed, float *norms, tq_stream_t stream);
+
+/* Decode n_rows rows ("fa_tq_dequantize"): y = n * s . (H c_idx) / sqrt(d).
+ *   packed: [n_rows][d*bits/8], norms: [n_rows] fp32 (device)
+ *   y:      [n_rows][d] fp32 or bf16 (y_dtype, round to nearest even), device */
+tq_status tq_decode(const tq_plan *plan, int bits, const uint8_t *packed, const float *norms,
+                    int64_t n_rows, void *y, tq_dtype y_dtype, tq_stream_t stream);
+
+/* Append n_new tokens of K and V into one layer of the cache at positions
+ * [pos, pos + n_new): the incremental encode of only the new rows
+ * ("TurboQuantEngine -- Specification", 6 P1 follow-ups, W3).  One launch
+ * encodes the K rows with k_bits and the V rows with v_bits.
+ *   k_new, v_new: [B][Hkv][n_new][d] fp32 or bf16 (dtype), device
+ * Errors: TQ_ERR_RANGE if pos < 0 or pos + n_new > cache.cap. */
+tq_status tq_append(const tq_plan *plan, int k_bits, int v_bits, const void *k_new,
+                    const void *v_new, tq_dtype dtype, int B, int Hkv, int64_t n_new,
+                    tq_cache_view cache, int64_t pos, tq_stream_t stream);
+
+/* Workspace bytes tq_attn_decode needs for these sizes on the current device
+ * (split-K partials).  0 for invalid sizes. */
+size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len);
+
+/* Decode attention over the packed cache, one query token per sequence
+ * ("TurboQuant KV Cache Compression -- Spec", fa_tq_attention_cached and
+ * Optimization: Fused dequant-dot; "CITATIONS", Sparse V dequant and
+ * Asymmetric K/V dtype).  For batch b and query head h (KV head
+ * g = h / (Hq/Hkv)), over positions t in [0, ctx_len):
+ *   sigma_t = scale * q . k_hat_t,  p = softmax(sigma),
+ *   out = sum_t p_t v_hat_t
+ * computed in the rotated domain: q is rotated once, scores are taken against
+ * the centroids, V is accumulated rotated and the output is rotated back
+ * once.  fp32 accumulation and softmax.
+ *   q:   [B][Hq][d] bf16, device
+ *   out: [B][Hq][d] fp32, device
+ *   sparse_v_threshold: 0 = dense.  Otherwise a V row is skipped (treated as
+ *     zero, still counted in the softmax denominator) when, for every head of
+ *     the GQA group, exp(sigma_t - m) < threshold, with m the running maximum
+ *     of that head at the time (m <= the global maximum, so the rows kept
+ *     include every row with exp(sigma_t - max) >= threshold).
+ *   workspace: device scratch of at least tq_attn_workspace_bytes(...) bytes;
+ *     no initial contents needed.
+ * Errors: TQ_ERR_RANGE if ctx_len < 1 or ctx_len > cache.cap;
+ *   TQ_ERR_INVALID_ARG if Hq % Hkv != 0; TQ_ERR_WORKSPACE. */
+tq_status tq_attn_decode(const tq_plan *plan, const void *q, int B, int Hq, int Hkv,
+                         tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                         float scale, float sparse_v_threshold, float *out, void *workspace,
+                         size_t workspace_bytes, tq_stream_t stream);
+
+/* Text for a status code (static storage). */
+const char *tq_status_string(tq_status status);
+
+/* The cudaError_t value behind the most recent TQ_ERR_CUDA of this thread. */
+int tq_last_cuda_error(void);
+
+/* Device status word of the current device: 0 if no kernel of this library
+ * has given up a bounded wait since the last reset (reset = 1 clears it).
+ * Synchronises the device. */
+tq_status tq_device_status(int reset, int *status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

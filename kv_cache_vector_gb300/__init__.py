@@ -1,0 +1,9 @@
+"""TurboQuant KV-cache codec and packed decode attention for GB300 (sm_103a).
+
+The compute lives in ``libtq.so`` (hand-written CUDA kernels behind a C ABI,
+declared in ``include/tq.h``); ``kv_cache_vector_gb300.abi`` is its thin
+Python binding.  Importing the package does not load the library; the first
+call does, and raises if it has not been built.
+"""
+from .abi import (Cache, Plan, TQError, tq_append, tq_attn_decode, tq_attn_workspace_bytes,  # noqa: F401
+                  tq_codebook_init, tq_decode, tq_device_status, tq_encode, tq_plan_create)

@@ -1,0 +1,404 @@
+// tq_api.cpp -- the C ABI: plan construction (codebooks, signs), argument
+// validation, and dispatch to the sm_103a kernels.  See include/tq.h.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <type_traits>
+
+#include "tq_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+tq_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return TQ_ERR_CUDA;
+}
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// A pointer the GPU cannot dereference (pageable host memory on a system
+// without pageable-memory access) is turned into an error instead of a fault.
+// Unknown answers are let through.
+bool device_accessible(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    if (a.type != cudaMemoryTypeUnregistered) return true;
+    int dev = 0, pageable = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return pageable != 0;
+}
+
+// ------------------------------------------------------------ signs
+
+// splitmix64 (S. Vigna): the state advances by the 64-bit golden-ratio
+// constant and each output is that state passed through two
+// xor-shift/multiply rounds and a final xor-shift.
+uint64_t splitmix64(uint64_t& st) {
+    st += 0x9E3779B97F4A7C15ULL;
+    uint64_t z = st;
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ULL;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBULL;
+    z ^= z >> 31;
+    return z;
+}
+
+// ---------------------------------------------------------- codebook
+//
+// One coordinate X of a uniform unit vector in R^d has density proportional
+// to (1 - x^2)^((d-3)/2) on [-1, 1].  With x = sin(t) the mass of [0, x] is
+// W_{d-2}(asin x), where W_n(T) = int_0^T cos^n is given in closed form by
+// the reduction W_n = cos^{n-1}(T) sin(T) / n + (n-1)/n W_{n-2}, W_0 = T,
+// W_1 = sin T; the first moment of [a, b] is
+// ((1-a^2)^{(d-1)/2} - (1-b^2)^{(d-1)/2}) / (d-1).
+
+double cos_power_integral(int n, double T) {
+    const double s = std::sin(T), c = std::cos(T);
+    double w = (n % 2 == 0) ? T : s;
+    double cpow = (n % 2 == 0) ? c : c * c;  // cos^{k-1} for the first k below
+    for (int k = (n % 2 == 0) ? 2 : 3; k <= n; k += 2) {
+        w = cpow * s / k + (double)(k - 1) / k * w;
+        cpow *= c * c;
+    }
+    return w;
+}
+
+struct HalfDensity {
+    int d;
+    double mass(double a, double b) const {  // 0 <= a <= b <= 1
+        return cos_power_integral(d - 2, std::asin(b)) - cos_power_integral(d - 2, std::asin(a));
+    }
+    double moment(double a, double b) const {
+        const double e = 0.5 * (d - 1);
+        return (std::pow(1.0 - a * a, e) - std::pow(1.0 - b * b, e)) / (double)(d - 1);
+    }
+};
+
+// Lloyd iteration on the positive half-line (the density is symmetric and
+// log-concave, so the optimum is symmetric and unique): centroids are
+// conditional means of their cells, interior boundaries midpoints of
+// neighbouring centroids.  Starts from cells evenly spread over
+// [0, 2.5/sqrt(d)] and runs until the centroids settle at rounding level.
+bool lloyd_half(int d, int bits, double* c, double* beta) {
+    const int H = (1 << bits) / 2;
+    HalfDensity f{d};
+    double w = 2.5 / std::sqrt((double)d);
+    if (w > 1.0) w = 1.0;
+    beta[0] = 0.0;
+    beta[H] = 1.0;
+    for (int k = 1; k < H; ++k) beta[k] = w * k / H;
+    double best = std::numeric_limits<double>::infinity();
+    int stall = 0;
+    for (int it = 0; it < 400000; ++it) {
+        double moved = 0.0, big = 0.0;
+        for (int k = 0; k < H; ++k) {
+            double ck = f.moment(beta[k], beta[k + 1]) / f.mass(beta[k], beta[k + 1]);
+            if (!std::isfinite(ck)) return false;
+            if (it > 0) moved = std::fmax(moved, std::fabs(ck - c[k]));
+            c[k] = ck;
+            big = std::fmax(big, std::fabs(ck));
+        }
+        for (int k = 1; k < H; ++k) beta[k] = 0.5 * (c[k - 1] + c[k]);
+        if (it == 0) continue;
+        if (moved <= 4e-15 * big) return true;
+        if (moved < 0.5 * best) {
+            best = moved;
+            stall = 0;
+        } else if (++stall > 500 && best <= 1e-12 * big) {
+            return true;
+        }
+    }
+    return false;
+}
+
+bool codebook(int d, int bits, double* cen, double* bnd) {
+    const int L = 1 << bits, H = L / 2;
+    double c[8], beta[9];
+    if (!lloyd_half(d, bits, c, beta)) return false;
+    for (int k = 0; k < H; ++k) {
+        cen[H + k] = c[k];
+        cen[H - 1 - k] = -c[k];
+    }
+    bnd[H - 1] = 0.0;
+    for (int k = 1; k < H; ++k) {
+        bnd[H - 1 + k] = beta[k];
+        bnd[H - 1 - k] = -beta[k];
+    }
+    return true;
+}
+
+// The encode kernels bucket through a table of cells of width 1/kLutScale;
+// it is exact when no closed cell holds two boundaries.
+bool lut_exact(const float* b32, int nb) {
+    for (int j = 0; j + 1 < nb; ++j) {
+        double gap = (double)b32[j + 1] - (double)b32[j];
+        if (gap <= 1.0 / tq::kLutScale + 1e-12) return false;
+    }
+    return true;
+}
+
+void fill_row_params(const tq::Plan& P, int bits, tq::RowParams& R) {
+    for (int i = 0; i < tq::kMaxD; ++i)
+        R.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
+    for (int i = 0; i < 16; ++i) {
+        R.cen[i] = P.c32[bits][i];
+        R.bnd[i] = P.b32[bits][i];
+    }
+    R.inv_sqrt_d = (float)(1.0 / std::sqrt((double)P.d));
+}
+
+template <int V>
+using IntC = std::integral_constant<int, V>;
+
+// Call f(IntC<d>) for the supported head dimensions.
+template <typename F>
+cudaError_t dispatch_d(int d, F&& f) {
+    switch (d) {
+        case 8: return f(IntC<8>{});
+        case 16: return f(IntC<16>{});
+        case 32: return f(IntC<32>{});
+        case 64: return f(IntC<64>{});
+        case 128: return f(IntC<128>{});
+        case 256: return f(IntC<256>{});
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename F>
+cudaError_t dispatch_attn_d(int d, F&& f) {
+    switch (d) {
+        case 32: return f(IntC<32>{});
+        case 64: return f(IntC<64>{});
+        case 128: return f(IntC<128>{});
+        case 256: return f(IntC<256>{});
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool valid_bits(int b) { return b >= 2 && b <= 4; }
+bool valid_dtype(tq_dtype t) { return t == TQ_F32 || t == TQ_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_codebook_init(int d, int bits, double* centroids, double* boundaries) {
+    if (!centroids || !boundaries) return TQ_ERR_INVALID_ARG;
+    if (d < 3 || d > 65536 || bits < 1 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    return codebook(d, bits, centroids, boundaries) ? TQ_OK : TQ_ERR_UNSUPPORTED;
+}
+
+tq_status tq_plan_create(int d, uint64_t seed, tq_plan** out) {
+    if (!out) return TQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!is_pow2(d) || d < 8 || d > tq::kMaxD) return TQ_ERR_UNSUPPORTED;
+    tq::Plan* P = new (std::nothrow) tq::Plan;
+    if (!P) return TQ_ERR_NOMEM;
+    std::memset(P, 0, sizeof(*P));
+    P->d = d;
+    P->seed = seed;
+    uint64_t st = seed;
+    for (int i = 0; i < d; ++i) P->signs[i] = (splitmix64(st) >> 63) ? -1 : 1;
+    for (int bits = 1; bits <= 4; ++bits) {
+        const int L = 1 << bits;
+        if (!codebook(d, bits, P->c64[bits], P->b64[bits])) {
+            delete P;
+            return TQ_ERR_UNSUPPORTED;
+        }
+        for (int i = 0; i < 16; ++i) {
+            P->c32[bits][i] = i < L ? (float)P->c64[bits][i] : 0.0f;
+            P->b32[bits][i] = i < L - 1 ? (float)P->b64[bits][i]
+                                        : std::numeric_limits<float>::infinity();
+        }
+        if (bits >= 2 && !lut_exact(P->b32[bits], L - 1)) {
+            delete P;
+            return TQ_ERR_UNSUPPORTED;
+        }
+    }
+    *out = reinterpret_cast<tq_plan*>(P);
+    return TQ_OK;
+}
+
+tq_status tq_plan_destroy(tq_plan* plan) {
+    delete reinterpret_cast<tq::Plan*>(plan);
+    return TQ_OK;
+}
+
+tq_status tq_plan_signs(const tq_plan* plan, int8_t* signs) {
+    if (!plan || !signs) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    std::memcpy(signs, P->signs, (size_t)P->d);
+    return TQ_OK;
+}
+
+tq_status tq_plan_codebook(const tq_plan* plan, int bits, float* centroids, float* boundaries) {
+    if (!plan || !centroids || !boundaries) return TQ_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    const int L = 1 << bits;
+    std::memcpy(centroids, P->c32[bits], sizeof(float) * L);
+    std::memcpy(boundaries, P->b32[bits], sizeof(float) * (L - 1));
+    return TQ_OK;
+}
+
+tq_status tq_encode(const tq_plan* plan, int bits, const void* x, tq_dtype x_dtype,
+                    int64_t n_rows, uint8_t* packed, float* norms, tq_stream_t stream) {
+    if (!plan || n_rows < 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_dtype(x_dtype)) return TQ_ERR_UNSUPPORTED;
+    if (n_rows == 0) return TQ_OK;
+    if (!x || !packed || !norms) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(packed) || !aligned4(norms)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(x) || !device_accessible(packed) || !device_accessible(norms))
+        return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    tq::RowParams R;
+    fill_row_params(*P, bits, R);
+    cudaError_t e = dispatch_d(P->d, [&](auto D) {
+        return tq::launch_encode_d<decltype(D)::value>(bits, x_dtype, x, n_rows, packed, norms, R,
+                                                       reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_decode(const tq_plan* plan, int bits, const uint8_t* packed, const float* norms,
+                    int64_t n_rows, void* y, tq_dtype y_dtype, tq_stream_t stream) {
+    if (!plan || n_rows < 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(bits) || !valid_dtype(y_dtype)) return TQ_ERR_UNSUPPORTED;
+    if (n_rows == 0) return TQ_OK;
+    if (!y || !packed || !norms) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(packed) || !aligned4(norms)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(y) || !device_accessible(packed) || !device_accessible(norms))
+        return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    tq::RowParams R;
+    fill_row_params(*P, bits, R);
+    cudaError_t e = dispatch_d(P->d, [&](auto D) {
+        return tq::launch_decode_d<decltype(D)::value>(bits, y_dtype, packed, norms, n_rows, y, R,
+                                                       reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_append(const tq_plan* plan, int k_bits, int v_bits, const void* k_new,
+                    const void* v_new, tq_dtype dtype, int B, int Hkv, int64_t n_new,
+                    tq_cache_view cache, int64_t pos, tq_stream_t stream) {
+    if (!plan || B < 0 || Hkv < 0 || n_new < 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits) || !valid_dtype(dtype))
+        return TQ_ERR_UNSUPPORTED;
+    if (pos < 0 || cache.cap < 0 || pos + n_new > cache.cap) return TQ_ERR_RANGE;
+    if ((int64_t)B * Hkv * n_new == 0) return TQ_OK;
+    if (!k_new || !v_new || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cache.k_packed) ||
+        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
+        return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(k_new) || !device_accessible(v_new) ||
+        !device_accessible(cache.k_packed) || !device_accessible(cache.v_packed) ||
+        !device_accessible(cache.k_norm) || !device_accessible(cache.v_norm))
+        return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    tq::RowParams PK, PV;
+    fill_row_params(*P, k_bits, PK);
+    fill_row_params(*P, v_bits, PV);
+    cudaError_t e = dispatch_d(P->d, [&](auto D) {
+        return tq::launch_append_d<decltype(D)::value>(k_bits, v_bits, dtype, k_new, v_new, B, Hkv,
+                                                       n_new, cache, pos, PK, PV,
+                                                       reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !is_pow2(d) ||
+        d > tq::kMaxD)
+        return 0;
+    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms());
+    return tq::attn_workspace_bytes(B, Hq, d, g);
+}
+
+tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                         tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                         float scale, float sparse_v_threshold, float* out, void* workspace,
+                         size_t workspace_bytes, tq_stream_t stream) {
+    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0) return TQ_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits)) return TQ_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 8) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (P->d < 32) return TQ_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale)) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
+        return TQ_ERR_INVALID_ARG;
+    if (ctx_len < 1 || ctx_len > cache.cap) return TQ_ERR_RANGE;
+    if (B == 0) return TQ_OK;
+    if (!q || !out || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
+        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
+        return TQ_ERR_ALIGNMENT;
+    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms());
+    size_t need = tq::attn_workspace_bytes(B, Hq, P->d, g);
+    if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(workspace) ||
+        !device_accessible(cache.k_packed) || !device_accessible(cache.v_packed) ||
+        !device_accessible(cache.k_norm) || !device_accessible(cache.v_norm))
+        return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    for (int i = 0; i < tq::kMaxD; ++i)
+        A.sgn[i] = (i < P->d && P->signs[i] < 0) ? 0x80000000u : 0u;
+    for (int i = 0; i < 16; ++i) {
+        A.kcen[i] = P->c32[k_bits][i];
+        A.vcen[i] = P->c32[v_bits][i];
+    }
+    A.inv_sqrt_d = (float)(1.0 / std::sqrt((double)P->d));
+    A.scale = scale;
+    A.sparse_thr = sparse_v_threshold;
+    cudaError_t e = dispatch_attn_d(P->d, [&](auto D) {
+        constexpr int d = decltype(D)::value;
+        auto st = reinterpret_cast<cudaStream_t>(stream);
+        switch (k_bits) {
+            case 2: return tq::launch_attn_dk<d, 2>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+            case 3: return tq::launch_attn_dk<d, 3>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+            default: return tq::launch_attn_dk<d, 4>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+        }
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+const char* tq_status_string(tq_status s) {
+    switch (s) {
+        case TQ_OK: return "ok";
+        case TQ_ERR_INVALID_ARG: return "invalid argument";
+        case TQ_ERR_UNSUPPORTED: return "unsupported head dimension, bit width or dtype";
+        case TQ_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case TQ_ERR_RANGE: return "position or context length outside the cache";
+        case TQ_ERR_WORKSPACE: return "workspace missing or too small";
+        case TQ_ERR_CUDA: return "CUDA runtime error";
+        case TQ_ERR_NOMEM: return "host allocation failed";
+    }
+    return "unknown status";
+}
+
+int tq_last_cuda_error(void) { return g_last_cuda_error; }
+
+tq_status tq_device_status(int reset, int* status_out) {
+    if (!status_out) return TQ_ERR_INVALID_ARG;
+    cudaError_t e = tq::read_device_status(reset, status_out);
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// tq_device.cuh -- device building blocks of the sm_103a row codec.
+//
+// A row of d elements is held by R = d/E threads (E <= 128 elements in
+// registers each; R = 2 only for d = 256).  The Walsh-Hadamard transform runs
+// as log2(E) register-only butterfly stages plus, for R = 2, one stage that
+// pairs the two threads through a shuffle ("TurboQuant KV Cache Compression
+// -- Spec", Hadamard Transform Detail: stages commute, so the cross-thread
+// stage can come last on encode and last on decode).
+//
+// Element layouts for R = 2 (E = 128, d = 256), thread part p in {0, 1}:
+//   "contiguous":  slot s <-> element p*E + s
+//   "split":       slot s <  E/2 <-> element p*E/2 + s
+//                  slot s >= E/2 <-> element E + p*E/2 + (s - E/2)
+// Encode loads contiguous and leaves split after the cross stage; decode
+// loads split and leaves contiguous.  The packed bit stream of a split part
+// is two contiguous runs of E/2 indices, so both sides stay vectorised.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+namespace dev {
+
+template <int D>
+struct RowShape {
+    static constexpr int R = (D > 128) ? 2 : 1;  // threads per row
+    static constexpr int E = D / R;              // elements per thread
+};
+
+// ------------------------------------------------------------- load + sign
+
+// v[s] = s_i * x_i for the thread's E elements starting at element `first`
+// (contiguous layout).  The sign is an xor of the fp32 sign bit with the
+// per-element mask from the parameter bank.
+template <int E>
+__device__ __forceinline__ void load_signed(const float* __restrict__ src, float (&v)[E],
+                                            const uint32_t* sgn) {
+    static_assert(E % 4 == 0 || E < 4, "vector width");
+    if constexpr (E >= 4) {
+        const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) {
+            uint4 w = __ldg(p + k);
+            v[4 * k + 0] = __uint_as_float(w.x ^ sgn[4 * k + 0]);
+            v[4 * k + 1] = __uint_as_float(w.y ^ sgn[4 * k + 1]);
+            v[4 * k + 2] = __uint_as_float(w.z ^ sgn[4 * k + 2]);
+            v[4 * k + 3] = __uint_as_float(w.w ^ sgn[4 * k + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < E; ++k) v[k] = __uint_as_float(__float_as_uint(src[k]) ^ sgn[k]);
+    }
+}
+
+// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+__device__ __forceinline__ float bf16lo(uint32_t w, uint32_t m) {
+    return __uint_as_float((w << 16) ^ m);
+}
+__device__ __forceinline__ float bf16hi(uint32_t w, uint32_t m) {
+    return __uint_as_float((w & 0xFFFF0000u) ^ m);
+}
+
+template <int E>
+__device__ __forceinline__ void load_signed(const __nv_bfloat16* __restrict__ src, float (&v)[E],
+                                            const uint32_t* sgn) {
+    static_assert(E % 8 == 0, "bf16 rows are loaded 16 bytes at a time");
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int k = 0; k < E / 8; ++k) {
+        uint4 w = __ldg(p + k);
+        const uint32_t* m = sgn + 8 * k;
+        v[8 * k + 0] = bf16lo(w.x, m[0]);
+        v[8 * k + 1] = bf16hi(w.x, m[1]);
+        v[8 * k + 2] = bf16lo(w.y, m[2]);
+        v[8 * k + 3] = bf16hi(w.y, m[3]);
+        v[8 * k + 4] = bf16lo(w.z, m[4]);
+        v[8 * k + 5] = bf16hi(w.z, m[5]);
+        v[8 * k + 6] = bf16lo(w.w, m[6]);
+        v[8 * k + 7] = bf16hi(w.w, m[7]);
+    }
+}
+
+// ------------------------------------------------------------------ FWHT
+
+// Unnormalised butterfly over the E registers: stages len = 1 .. E/2,
+// (a, b) -> (a + b, a - b).
+template <int E>
+__device__ __forceinline__ void fwht_reg(float (&v)[E]) {
+#pragma unroll
+    for (int len = 1; len < E; len <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; i += 2 * len) {
+#pragma unroll
+            for (int j = i; j < i + len; ++j) {
+                float a = v[j], b = v[j + len];
+                v[j] = a + b;
+                v[j + len] = a - b;
+            }
+        }
+    }
+}
+
+// The butterfly stage that pairs slot s of part 0 with slot s of part 1
+// (lanes l and l^1).  Part 0 computes both outputs of slots [0, E/2), part 1
+// those of slots [E/2, E); afterwards slot j (j < E/2) holds the part-0
+// output and slot E/2 + j the part-1 output of the slot it computed.
+template <int E>
+__device__ __forceinline__ void fwht_cross(float (&v)[E], int p) {
+    constexpr int H = E / 2;
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+        float send = p ? v[j] : v[H + j];
+        float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+        float a = p ? recv : v[j];
+        float b = p ? v[H + j] : recv;
+        v[j] = a + b;
+        v[H + j] = a - b;
+    }
+}
+
+// ------------------------------------------------------------- bucketing
+
+struct LutEntry {
+    int lo;     // #{ j : beta_j < cell_lo }
+    float thr;  // the one boundary inside the closed cell, or +inf
+};
+
+// Fill the bucketing table from the fp32 boundaries (every thread of the
+// block takes part; the caller synchronises).  Exact by construction: every
+// closed cell holds at most one boundary (checked on the host when the plan
+// is built), so for any w in cell g,
+//   #{ j : w >= beta_j } = lo_g + [w >= thr_g].
+__device__ __forceinline__ void build_lut(LutEntry* lut, const float* bnd, int nb) {
+    for (int g = threadIdx.x; g < kLutCells; g += blockDim.x) {
+        float lo = (float)(g - kLutCenter - 0.5) / (float)kLutScale;
+        float hi = (float)(g - kLutCenter + 0.5) / (float)kLutScale;
+        int cnt = 0;
+        float thr = __int_as_float(0x7F800000);
+        for (int j = 0; j < nb; ++j) {
+            float b = bnd[j];
+            if (b < lo) cnt += 1;
+            else if (b <= hi) thr = b;
+        }
+        lut[g].lo = cnt;
+        lut[g].thr = thr;
+    }
+}
+
+// Level index of w = y * inv (exact product), via the table.  The cell is
+// rint(w * kLutScale) + kLutCenter, read off the mantissa of a single FMA
+// with 1.5 * 2^23 (its unit in the last place is 1, so the FMA rounds the
+// exact product to the nearest integer); the compare is one FMA whose sign is
+// exact.  y * inv_s (inv_s = inv * kLutScale) equals w * kLutScale exactly.
+__device__ __forceinline__ int bucket_lut(const LutEntry* lut, float y, float inv, float inv_s) {
+    constexpr float kMagic = 12582912.0f + (float)kLutCenter;
+    float f = fmaf(y, inv_s, kMagic);
+    uint32_t g = __float_as_uint(f) & (uint32_t)(kLutCells - 1);
+    LutEntry e = lut[g];
+    float r = fmaf(y, inv, -e.thr);
+    return e.lo + (r >= 0.0f ? 1 : 0);
+}
+
+// Reference bucketing by binary search over the fp32 boundaries (used where
+// building the table would cost more than it saves: a few rows per launch).
+template <int BITS>
+__device__ __forceinline__ int bucket_search(const float* bnd, float y, float inv) {
+    int idx = 0;
+#pragma unroll
+    for (int step = (1 << BITS) / 2; step >= 1; step >>= 1) {
+        float r = fmaf(y, inv, -bnd[idx + step - 1]);
+        if (r >= 0.0f) idx += step;
+    }
+    return idx;
+}
+
+// --------------------------------------------------------------- packing
+
+// Pack N indices (N * BITS a multiple of 32) into N*BITS/32 words, dense
+// LSB-first.
+template <int N, int BITS>
+__device__ __forceinline__ void pack_words(const int* idx, uint32_t* w) {
+    constexpr int NW = N * BITS / 32;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) w[k] = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int pos = i * BITS;
+        const int wi = pos / 32, sh = pos % 32;
+        w[wi] |= (uint32_t)idx[i] << sh;
+        if (sh + BITS > 32) w[wi + 1] |= (uint32_t)idx[i] >> (32 - sh);
+    }
+}
+
+// Extract index i (compile-time) from a word array.
+template <int BITS>
+__device__ __forceinline__ int unpack_one(const uint32_t* w, int i) {
+    const int pos = i * BITS;
+    const int wi = pos / 32, sh = pos % 32;
+    uint32_t v = w[wi] >> sh;
+    if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
+    return (int)(v & ((1u << BITS) - 1));
+}
+
+// Store / load `bytes` bytes (compile-time) at a pointer aligned to the
+// largest power of two dividing `bytes` (at most 16).
+template <int BYTES>
+__device__ __forceinline__ void store_bytes(uint8_t* dst, const uint32_t* w) {
+    if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 16; ++k)
+            reinterpret_cast<uint4*>(dst)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 8; ++k)
+            reinterpret_cast<uint2*>(dst)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+    } else if constexpr (BYTES % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 4; ++k) reinterpret_cast<uint32_t*>(dst)[k] = w[k];
+    } else {
+#pragma unroll
+        for (int k = 0; k < BYTES; ++k) dst[k] = (uint8_t)(w[k / 4] >> (8 * (k % 4)));
+    }
+}
+
+template <int BYTES>
+__device__ __forceinline__ void load_bytes(const uint8_t* src, uint32_t* w) {
+    if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 16; ++k) {
+            uint4 q = __ldg(reinterpret_cast<const uint4*>(src) + k);
+            w[4 * k] = q.x; w[4 * k + 1] = q.y; w[4 * k + 2] = q.z; w[4 * k + 3] = q.w;
+        }
+    } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 8; ++k) {
+            uint2 q = __ldg(reinterpret_cast<const uint2*>(src) + k);
+            w[2 * k] = q.x; w[2 * k + 1] = q.y;
+        }
+    } else if constexpr (BYTES % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < BYTES / 4; ++k) w[k] = __ldg(reinterpret_cast<const uint32_t*>(src) + k);
+    } else {
+#pragma unroll
+        for (int k = 0; k < (BYTES + 3) / 4; ++k) w[k] = 0;
+#pragma unroll
+        for (int k = 0; k < BYTES; ++k) w[k / 4] |= (uint32_t)__ldg(src + k) << (8 * (k % 4));
+    }
+}
+
+}  // namespace dev
+}  // namespace tq

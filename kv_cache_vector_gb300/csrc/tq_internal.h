@@ -1,0 +1,85 @@
+// tq_internal.h -- declarations shared by the host entry points (tq_api.cpp)
+// and the kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+constexpr int kMaxD = 256;
+
+// Per-launch constants of the row codec, passed by value (they live in the
+// kernel-parameter constant bank, so uniform reads cost no instruction).
+struct RowParams {
+    uint32_t sgn[kMaxD];  // 0x80000000 where s_i = -1, else 0 (xor mask on fp32 bits)
+    float cen[16];        // fp32 centroids, ascending (2^bits used)
+    float bnd[16];        // fp32 boundaries, ascending (2^bits - 1 used), rest +inf
+    float inv_sqrt_d;
+};
+
+// Constants of the attention kernels.
+struct AttnParams {
+    uint32_t sgn[kMaxD];
+    float kcen[16];
+    float vcen[16];
+    float inv_sqrt_d;
+    float scale;       // softmax scale applied to q . k
+    float sparse_thr;  // 0 = dense
+};
+
+// Host plan (the public tq_plan).
+struct Plan {
+    int d;
+    uint64_t seed;
+    int8_t signs[kMaxD];
+    double c64[5][16], b64[5][16];  // index by bits (1..4)
+    float c32[5][16], b32[5][16];
+};
+
+// Bucketing lookup table geometry (encode): cell g covers the normalised
+// coordinate w with rint(w * kLutScale) = g - kLutCenter, i.e. the closed
+// interval [(g - kLutCenter - 0.5) / kLutScale, (g - kLutCenter + 0.5) / kLutScale].
+constexpr int kLutScale = 512;
+constexpr int kLutCenter = 1024;
+constexpr int kLutCells = 2048;  // covers w in [-2, 2); |w| <= 1 for finite rows
+
+// Launchers, one explicit instantiation per head dimension D (each kernel
+// file is compiled once per D, in parallel).  They validate nothing: the
+// caller (tq_api.cpp) has checked every argument.
+template <int D>
+cudaError_t launch_encode_d(int bits, tq_dtype dt, const void* x, int64_t n_rows, uint8_t* packed,
+                            float* norms, const RowParams& P, cudaStream_t s);
+template <int D>
+cudaError_t launch_decode_d(int bits, tq_dtype dt, const uint8_t* packed, const float* norms,
+                            int64_t n_rows, void* y, const RowParams& P, cudaStream_t s);
+template <int D>
+cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,
+                            const void* v_new, int B, int Hkv, int64_t n_new,
+                            const tq_cache_view& cache, int64_t pos, const RowParams& PK,
+                            const RowParams& PV, cudaStream_t s);
+
+struct AttnGeometry {
+    int n_splits;
+    int split_len;  // positions per split
+};
+AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int num_sms);
+size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
+template <int D, int KB>
+cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
+                           const tq_cache_view& cache, int64_t ctx_len, float* out, void* workspace,
+                           const AttnGeometry& g, const AttnParams& P, cudaStream_t s);
+
+// Shared launch helpers (tq_launch.cpp).
+int num_sms();
+int blocks_per_sm(const void* kernel, int block_threads, size_t dyn_smem);
+unsigned grid_for(const void* kernel, int block_threads, int64_t items);
+
+// Device status word (bounded waits that gave up).
+cudaError_t read_device_status(int reset, int* out);
+
+}  // namespace tq

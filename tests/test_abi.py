@@ -1,0 +1,141 @@
+"""CPU tests of the C ABI: the library loads and exports what include/tq.h
+declares; its host-side parts (codebook, signs, argument validation, the
+bucketing-table geometry) agree with the oracle and the header.  No kernel is
+launched here."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from kv_cache_vector_gb300 import abi
+from oracle import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kv_cache_vector_gb300 import build
+    build.build()
+    return abi.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    hdr = open(os.path.join(ROOT, "include", "tq.h")).read()
+    declared = set(re.findall(r"\b(tq_[a-z_0-9]+)\s*\(", hdr))
+    assert declared == set(abi.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("d", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_codebook_matches_oracle(L, d, bits):
+    """The library's codebook (closed-form cell masses) and the oracle's
+    (Gauss-Legendre) are independent computations of the same fixed point."""
+    c, b = abi.tq_codebook_init(d, bits)
+    oc, ob, _ = O.codebook(d, bits)
+    scale = 1.0 / math.sqrt(d)
+    assert np.max(np.abs(c - oc)) < 1e-12 * scale
+    assert np.max(np.abs(b - ob)) < 1e-12 * scale
+    assert np.array_equal(c.astype(np.float32), oc.astype(np.float32))
+    assert np.array_equal(b.astype(np.float32), ob.astype(np.float32))
+
+
+@pytest.mark.parametrize("seed", [0, 42, 2**63 + 5])
+@pytest.mark.parametrize("d", [8, 128, 256])
+def test_plan_signs_and_codebooks(L, seed, d):
+    p = abi.Plan(d, seed)
+    assert np.array_equal(p.signs(), O.signs(seed, d))
+    for bits in (2, 3, 4):
+        c, b = p.codebook(bits)
+        oc, ob = O.codebook_f32(d, bits)
+        assert np.array_equal(c, oc) and np.array_equal(b, ob)
+    p.close()
+
+
+def test_codebook_and_plan_argument_errors(L):
+    c = np.empty(16)
+    b = np.empty(15)
+    assert L.tq_codebook_init(2, 4, c.ctypes.data, b.ctypes.data) == 2
+    assert L.tq_codebook_init(128, 5, c.ctypes.data, b.ctypes.data) == 2
+    assert L.tq_codebook_init(128, 4, None, b.ctypes.data) == 1
+    h = ctypes.c_void_p()
+    for d in (0, 4, 96, 512):
+        assert L.tq_plan_create(d, 1, ctypes.byref(h)) == 2
+    assert L.tq_plan_create(128, 1, None) == 1
+    assert L.tq_status_string(0) == b"ok"
+
+
+def test_hot_call_validation_before_launch(L):
+    """Wrong arguments come back as status codes; none of these reaches CUDA."""
+    p = abi.Plan(128, 42)
+    h = p.handle
+    A = 1 << 20  # a 16-byte aligned address (never dereferenced)
+    s = None
+    assert L.tq_encode(None, 4, A, 1, 8, A, A, s) == 1
+    assert L.tq_encode(h, 5, A, 1, 8, A, A, s) == 2
+    assert L.tq_encode(h, 4, A, 7, 8, A, A, s) == 2
+    assert L.tq_encode(h, 4, A, 1, -1, A, A, s) == 1
+    assert L.tq_encode(h, 4, A, 1, 0, None, None, s) == 0   # empty: no-op
+    assert L.tq_encode(h, 4, None, 1, 8, A, A, s) == 1
+    assert L.tq_encode(h, 4, A + 8, 1, 8, A, A, s) == 3
+    assert L.tq_encode(h, 4, A, 1, 8, A + 4, A, s) == 3
+    assert L.tq_decode(h, 1, A, A, 8, A, 0, s) == 2
+    assert L.tq_decode(h, 4, A, A, 8, A + 2, 0, s) == 3
+    cv = abi.CacheView(A, A, A, A, 16)
+    assert L.tq_append(h, 4, 2, A, A, 1, 1, 2, 1, cv, 16, s) == 4      # pos == cap
+    assert L.tq_append(h, 4, 2, A, A, 1, 1, 2, 4, cv, 13, s) == 4      # runs past cap
+    assert L.tq_append(h, 4, 2, A, A, 1, 1, 2, 1, cv, -1, s) == 4
+    assert L.tq_append(h, 4, 9, A, A, 1, 1, 2, 1, cv, 0, s) == 2
+    f = ctypes.c_float
+    assert L.tq_attn_decode(h, A, 1, 6, 4, cv, 8, 4, 2, f(1.0), f(0.0), A, A, 1 << 20, s) == 1
+    assert L.tq_attn_decode(h, A, 1, 32, 2, cv, 8, 4, 2, f(1.0), f(0.0), A, A, 1 << 20, s) == 2
+    assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 0, 4, 2, f(1.0), f(0.0), A, A, 1 << 20, s) == 4
+    assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 17, 4, 2, f(1.0), f(0.0), A, A, 1 << 20, s) == 4
+    assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 8, 4, 2, f(1.0), f(-1.0), A, A, 1 << 20, s) == 1
+    assert L.tq_attn_workspace_bytes(1, 6, 4, 128, 8) == 0
+    p.close()
+
+
+def _emulate_table_bucket(bnd32: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """numpy restatement of the kernels' bucketing table: cell = rint(w*512)
+    (round half even, exact), lo = #{beta < cell_lo}, thr = the boundary in the
+    closed cell, idx = lo + [w >= thr]."""
+    S, C, N = 512, 1024, 2048
+    g = np.arange(N)
+    lo = ((g - C - 0.5) / S).astype(np.float32).astype(np.float64)
+    hi = ((g - C + 0.5) / S).astype(np.float32).astype(np.float64)
+    b = bnd32.astype(np.float64)
+    cnt = (b[None, :] < lo[:, None]).sum(1)
+    inside = (b[None, :] >= lo[:, None]) & (b[None, :] <= hi[:, None])
+    assert inside.sum(1).max() <= 1
+    thr = np.full(N, np.inf)
+    rows, cols = np.nonzero(inside)
+    thr[rows] = b[cols]
+    cell = (np.rint(w.astype(np.float64) * S).astype(np.int64) + C) & (N - 1)
+    return cnt[cell] + (w.astype(np.float64) >= thr[cell])
+
+
+@pytest.mark.parametrize("d", [8, 32, 128, 256])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_bucketing_table_is_exact(L, d, bits):
+    """The table the encode kernels build gives #{j : w >= beta_j} for every
+    fp32 w a finite row can produce (|w| <= |y_i| / (sqrt(d) n) <= 1, plus
+    rounding): checked on boundaries, their neighbours, cell edges and a dense
+    random sweep."""
+    p = abi.Plan(d, 1)
+    _, bnd = p.codebook(bits)
+    rng = np.random.default_rng(d + bits)
+    edges = ((np.arange(-530, 530) + 0.5) / 512).astype(np.float32)
+    w = np.concatenate([
+        bnd, np.nextafter(bnd, np.float32(-9)), np.nextafter(bnd, np.float32(9)),
+        edges, np.nextafter(edges, np.float32(-9)), np.nextafter(edges, np.float32(9)),
+        rng.normal(0, 1 / math.sqrt(d), 200000).astype(np.float32),
+        rng.uniform(-1, 1, 200000).astype(np.float32), np.array([0.0, -0.0, 1.0, -1.0], np.float32)])
+    want = np.searchsorted(bnd, w, side="right")
+    assert np.array_equal(_emulate_table_bucket(bnd, w), want)
+    p.close()
