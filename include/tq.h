@@ -161,6 +161,34 @@ tq_status tq_attn_decode(const tq_plan *plan, const void *q, int B, int Hq, int 
                          float scale, float sparse_v_threshold, float *out, void *workspace,
                          size_t workspace_bytes, tq_stream_t stream);
 
+/* Decode attention that allocates nothing, for callers that are not allowed
+ * to allocate device memory while they run -- a plugin inside a framework
+ * that owns every device allocation through its own memory planner, or a
+ * serving loop whose device memory is fixed up front so that no step can fail
+ * or stall on an allocation.  Such callers cannot hand tq_attn_decode a
+ * workspace.  This call computes exactly what tq_attn_decode computes, with
+ * the same kernels and arguments minus the workspace.  The pages have no
+ * counterpart of it.
+ *   Scratch: a fixed device array of 8 MiB inside the library (every GPU
+ *   that loads the library holds it until the process exits).  If the split-K
+ *   partials for these sizes need more than that (compare
+ *   tq_attn_workspace_bytes with 8388608), the call returns TQ_ERR_WORKSPACE
+ *   and launches nothing.  No part of the scratch needs to start at zero:
+ *   each call writes every partial before it reads it.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (with that device current) and caches it; make that first call before
+ *   any stream capture on that device.
+ *   All calls on a device share the one array: calls whose kernels overlap on
+ *   the GPU (different streams, or concurrent host threads) race and produce
+ *   wrong results.  Serialise them, e.g. on one stream.
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Errors: as tq_attn_decode, with TQ_ERR_WORKSPACE meaning "needs more than
+ * the 8 MiB array". */
+tq_status tq_attn_decode_noalloc(const tq_plan *plan, const void *q, int B, int Hq, int Hkv,
+                                 tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                                 float scale, float sparse_v_threshold, float *out,
+                                 tq_stream_t stream);
+
 /* Text for a status code (static storage). */
 const char *tq_status_string(tq_status status);
 

@@ -25,7 +25,8 @@ STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_E
 # every symbol include/tq.h declares
 EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_signs",
            "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes",
-           "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status")
+           "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
+           "tq_attn_decode_noalloc")
 
 
 class TQError(RuntimeError):
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
         ("tq_attn_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32, i64]),
         ("tq_attn_decode", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32, vp, vp,
                                  ctypes.c_size_t, vp]),
+        ("tq_attn_decode_noalloc", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32,
+                                         vp, vp]),
         ("tq_status_string", ctypes.c_char_p, [i32]),
         ("tq_last_cuda_error", i32, []),
         ("tq_device_status", i32, [i32, ctypes.POINTER(i32)]),
@@ -226,6 +229,27 @@ def tq_attn_decode(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scal
         plan.handle, q.data_ptr(), B, Hq, Hkv, cache.view(), ctx_len, cache.k_bits, cache.v_bits,
         ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(),
         workspace.data_ptr(), workspace.numel(), _stream(q)))
+    return out
+
+
+def tq_attn_decode_noalloc(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scale: float,
+                           sparse_v_threshold: float = 0.0,
+                           out: torch.Tensor | None = None) -> torch.Tensor:
+    """As tq_attn_decode, without a workspace: for callers that may not
+    allocate device memory while they run.  The library's fixed 8 MiB device
+    array holds the split-K partials; sizes that need more raise TQError
+    (TQ_ERR_WORKSPACE).  Calls that overlap on the GPU share that array and
+    race.  (This wrapper allocates `out` only when none is passed.)"""
+    B, Hq, d = q.shape
+    Hkv = cache.k_norm.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    _cuda(q, out)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    _check("tq_attn_decode_noalloc", lib().tq_attn_decode_noalloc(
+        plan.handle, q.data_ptr(), B, Hq, Hkv, cache.view(), ctx_len, cache.k_bits, cache.v_bits,
+        ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(), _stream(q)))
     return out
 
 

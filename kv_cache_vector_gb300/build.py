@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 # (source, specialisation macros TQ_UNIT_<name>)
 CODEC_DIMS = (8, 16, 32, 64, 128, 256)
 ATTN_DIMS = (32, 64, 128, 256)
-UNITS = ([("tq_api.cpp", {}), ("tq_launch.cu", {})]
+UNITS = ([("tq_api.cpp", {}), ("tq_launch.cu", {}), ("tq_noalloc.cu", {})]
          + [("tq_codec.cu", {"D": d}) for d in CODEC_DIMS]
          + [("tq_attn.cu", {"D": d, "KB": kb}) for d in ATTN_DIMS for kb in (2, 3, 4)])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -194,6 +194,8 @@ bool valid_dtype(tq_dtype t) { return t == TQ_F32 || t == TQ_BF16; }
 
 }  // namespace
 
+void tq::set_last_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 extern "C" {
 
 tq_status tq_codebook_init(int d, int bits, double* centroids, double* boundaries) {

@@ -79,6 +79,9 @@ int num_sms();
 int blocks_per_sm(const void* kernel, int block_threads, size_t dyn_smem);
 unsigned grid_for(const void* kernel, int block_threads, int64_t items);
 
+// Records the cudaError_t that tq_last_cuda_error reports for this thread.
+void set_last_cuda_error(cudaError_t e);
+
 // Device status word (bounded waits that gave up).
 cudaError_t read_device_status(int reset, int* out);
 
