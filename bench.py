@@ -42,7 +42,7 @@ def args_():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--small", action="store_true", help="1/32 of the codec rows, batch 4 attention")
+    ap.add_argument("--small", action="store_true", help="1/32 of the codec rows, batch 8 attention")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["encode", "decode", "attn", "append"], default=None,
@@ -55,8 +55,8 @@ class Workload:
         self.L, self.Hkv, self.B, self.T = 32, 8, 16, 8192
         self.ab, self.aHq, self.aHkv, self.ctx = 32, 32, 8, 32768
         self.kb, self.vb, self.akb, self.avb = 4, 2, 4, 3
-        if small:
-            self.L, self.ab = 1, 4
+        if small:  # profiling size: still larger than L2 (codec 256 MB, cache 252 MB)
+            self.L, self.ab = 1, 8
         self.rows = self.L * self.Hkv * self.B * self.T
 
     def describe(self):
@@ -188,13 +188,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest per-rank value (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank encodes and attends over its own batch (weak scaling)."""
+    return 1000 + rank
 
 
 # ------------------------------------------------------------- our arm
@@ -209,7 +216,7 @@ def make_state(W: Workload, rank: int):
     dev = torch.device("cuda")
     S = State()
     S.plan = abi.Plan(D, 42)
-    seed = 1000 + rank
+    seed = rank_seed(rank)
     S.seed = seed
     per = W.B * W.T
     S.K = torch.empty(W.rows, D, dtype=torch.bfloat16, device=dev)
@@ -348,6 +355,101 @@ def e2e_run(W, S, steps):
     return ms, h2d, d2h
 
 
+# ---------------------------------------------- the other two workloads
+
+def flush_l2(buf):
+    buf.add_(1)  # writes 2x the L2 size: nothing of the next input stays cached
+
+
+def time_events(fn, iters, flush=None):
+    import torch
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def extra_long_context(peak):
+    """Batch 1, 32 query / 8 KV heads, d 128, context 131072, K3/V2; keys
+    N(0,1) with 2 outlier channels x8, values N(0,1); dense and sparse-V
+    (threshold 1e-4); L2 flushed before every timed call."""
+    import torch
+    from kv_cache_vector_gb300 import abi, synth
+    B, Hq, Hkv, ctx, kb, vb = 1, 32, 8, 131072, 3, 2
+    plan = abi.Plan(D, 42)
+    cache = abi.Cache.empty(B, Hkv, ctx, D, kb, vb)
+    for h in range(Hkv):
+        k = synth.outlier_rows(3000, B * ctx, D, 2, stream=h, device="cuda")
+        v = synth.device_normal(3100 + h, (B * ctx, D))
+        p2, n2 = abi.tq_encode(plan, kb, k)
+        cache.k_packed[:, h] = p2.view(B, ctx, -1)
+        cache.k_norm[:, h] = n2.view(B, ctx)
+        p2, n2 = abi.tq_encode(plan, vb, v)
+        cache.v_packed[:, h] = p2.view(B, ctx, -1)
+        cache.v_norm[:, h] = n2.view(B, ctx)
+    q = synth.device_normal(5, (B, Hq, D))
+    out = torch.empty(B, Hq, D, device="cuda")
+    ws = torch.empty(abi.tq_attn_workspace_bytes(B, Hq, Hkv, D, ctx), dtype=torch.uint8, device="cuda")
+    buf = torch.empty(2 * 129 * 2 ** 20 // 4, device="cuda")
+    res = {}
+    nbytes = B * Hkv * ctx * (D * (kb + vb) // 8 + 8)
+    for name, thr in (("dense", 0.0), ("sparse_v_1e-4", 1e-4)):
+        f = lambda: abi.tq_attn_decode(plan, q, cache, ctx, 1.0 / math.sqrt(D), thr, out=out, workspace=ws)
+        for _ in range(5):
+            f()
+        ms = time_events(f, 50, lambda: flush_l2(buf))
+        res[name] = {"us": round(ms * 1e3, 2), "GBps_dense_bytes": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+    res["config"] = "B1 Hq32/Hkv8 d128 ctx131072 K3/V2, 2 outlier key channels x8, L2 flushed"
+    return res
+
+
+def extra_gemma(peak):
+    """34 layers x 4 KV heads x d 256 x 512 tokens bf16 N(0,1), K4/V4: window
+    encode GB/s (L2 flushed), then the append-only decode step: one tq_append
+    per layer (4 K + 4 V rows), the 34-layer step replayed from a CUDA graph."""
+    import torch
+    from kv_cache_vector_gb300 import abi, synth
+    L, Hkv, d, T, steps = 34, 4, 256, 512, 50
+    plan = abi.Plan(d, 42)
+    win = synth.device_normal(4000, (2, L * Hkv * T, d))
+    pk = torch.empty(L * Hkv * T, d // 2, dtype=torch.uint8, device="cuda")
+    nm = torch.empty(L * Hkv * T, device="cuda")
+    buf = torch.empty(2 * 129 * 2 ** 20 // 4, device="cuda")
+    f = lambda: (abi.tq_encode(plan, 4, win[0], pk, nm), abi.tq_encode(plan, 4, win[1], pk, nm))
+    for _ in range(3):
+        f()
+    ms = time_events(f, 20, lambda: flush_l2(buf))
+    wbytes = 2 * L * Hkv * T * (d * 2 + d // 2 + 4)
+    caches = [abi.Cache.empty(1, Hkv, T + steps, d, 4, 4) for _ in range(L)]
+    nk = synth.device_normal(4002, (L, 1, Hkv, 1, d))
+    nv = synth.device_normal(4003, (L, 1, Hkv, 1, d))
+    one = lambda: abi.tq_append(plan, caches[0], nk[0], nv[0], T)
+    for _ in range(3):
+        one()
+    append_ms = time_events(one, 50)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l in range(L):
+            abi.tq_append(plan, caches[l], nk[l], nv[l], T)
+    for _ in range(3):
+        g.replay()
+    step_ms = time_events(g.replay, 50)
+    return {"window_encode": {"ms": round(ms, 4), "GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
+                              "frac": round(wbytes / (ms * 1e-3) / 1e9 / peak, 4)},
+            "append_us_per_call": round(append_ms * 1e3, 2),
+            "append_step_us_34_layers_graph": round(step_ms * 1e3, 2),
+            "config": "34L x 4Hkv x d256 x 512 tokens bf16, K4/V4, then 1-token appends (B1)"}
+
+
 # ------------------------------------------------------- oracle timing
 
 def oracle_sample(W, budget_s: float):
@@ -465,11 +567,14 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic_for(dom)},
         "clocks": clk.summary(),
-        "gpu_launches": a.steps * (sum(1 for k in KERNELS if not a.only or k.startswith(a.only))
-                                   + (1 if (not a.only or a.only == "attn") else 0)),
+        # launches of this library's kernels per step: one per codec call and
+        # append; q rotation + split + combine for the attention
+        "gpu_launches": a.steps * sum({"attn": 3}.get(k, 1) for k in KERNELS
+                                      if not a.only or k.startswith(a.only)),
     }
     if not a.only:
         out["parity"] = parity_sample(W, S)
+
     if not a.no_e2e and not a.only:
         ems, h2d, d2h = e2e_run(W, S, min(a.steps, 3))
         out["e2e"] = {"value": round(step_bytes / (ems * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
@@ -478,6 +583,11 @@ def main():
         sec, sample = oracle_sample(W, 20.0)
         out["cpu_baseline"] = {"value": round(step_bytes / sec / 1e9, 6), "unit": "GB/s",
                                "cores": cpu_cores_used(), "kind": "oracle", "sample": sample}
+    if not a.only and not a.small:
+        del S
+        torch.cuda.empty_cache()
+        out["long_context"] = extra_long_context(peak)
+        out["gemma_cache"] = extra_gemma(peak)
     print(json.dumps(out))
     barrier(world)
 

@@ -328,7 +328,7 @@ size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !is_pow2(d) ||
         d > tq::kMaxD)
         return 0;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms());
+    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms(), d);
     return tq::attn_workspace_bytes(B, Hq, d, g);
 }
 
@@ -351,7 +351,7 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms());
+    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms(), P->d);
     size_t need = tq::attn_workspace_bytes(B, Hq, P->d, g);
     if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;

@@ -7,7 +7,15 @@
 // norm / sqrt(d) -> sign -> store.  Rows are independent ("TurboQuantEngine --
 // Specification", 7 Non-goals: each row encoded independently), so the grid
 // simply strides over rows.
+#include "tq_async.cuh"
 #include "tq_device.cuh"
+#include "tq_umma.cuh"
+
+// The d = 128 bf16 encode runs its Walsh-Hadamard transform on the tensor
+// cores (tcgen05) when this is 1, on CUDA cores (TMA-fed kernel) when 0.
+#ifndef TQ_ENCODE_TCGEN05
+#define TQ_ENCODE_TCGEN05 0
+#endif
 
 namespace tq {
 namespace dev {
@@ -220,20 +228,646 @@ __global__ void __launch_bounds__(kBlock) k_decode(const uint8_t* __restrict__ p
 
 }  // namespace dev
 
+namespace dev {
+
+// ------------------------------------------------- encode, TMA-fed (v2)
+//
+// Persistent, warp-specialised: warp 4 issues 2-D TMA loads of 128-row tiles
+// (128-byte boxes, 128-byte swizzle) into a ring of shared-memory stages;
+// warps 0-3 take one row per thread, read it conflict-free from the swizzled
+// stage, release the stage and encode the row in registers.  bf16 rows only.
+
+constexpr int kTmaRows = 128;
+constexpr int kTmaThreads = 160;
+
+template <int D>
+struct TmaEncodeShape {
+    static constexpr int kBoxes = D * 2 / 128;                       // 128-byte boxes per row
+    static constexpr int kStageBytes = kTmaRows * D * 2;
+    static constexpr int kStages = kStageBytes <= 16384 ? 6 : 3;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kLutCells * 8 + 2 * kStages * 8;
+};
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+k_encode_tma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* __restrict__ packed,
+             float* __restrict__ norms, int* status, const __grid_constant__ RowParams P) {
+    using S = TmaEncodeShape<D>;
+    constexpr int RB = D * BITS / 8;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle, by pointer arithmetic on
+    // the shared array (keeps every access below a shared-memory access).
+    unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    unsigned char* stages = base;
+    LutEntry* lut = reinterpret_cast<LutEntry*>(stages + S::kStages * S::kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(lut + kLutCells);
+    uint64_t* empty = full + S::kStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);
+        }
+        mbar_fence_init();
+    }
+    build_lut(lut, P.bnd, (1 << BITS) - 1);
+    __syncthreads();
+    const int64_t n_tiles = (n_rows + kTmaRows - 1) / kTmaRows;
+
+    if (warp == 4) {  // ---- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            int it = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int s = it % S::kStages;
+                const uint32_t k = it / S::kStages;
+                if (it >= S::kStages && !mbar_wait(&empty[s], (k - 1) & 1)) {
+                    report_timeout(status, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+#pragma unroll
+                for (int b = 0; b < S::kBoxes; ++b)
+                    tma_load_2d(stages + s * S::kStageBytes + b * kTmaRows * 128, &xmap, b * 64,
+                                (int)(tile * kTmaRows), &full[s]);
+            }
+            // Loads still in flight must land before this CTA may exit.
+            const int last = it;
+            for (int j = (last > S::kStages ? last - S::kStages : 0); j < last; ++j) {
+                if (!mbar_wait(&full[j % S::kStages], (j / S::kStages) & 1)) {
+                    report_timeout(status, 2);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- consumers: one row per thread
+    const int r = threadIdx.x;  // 0..127
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+        const int s = it % S::kStages;
+        if (!mbar_wait(&full[s], (it / S::kStages) & 1)) {
+            report_timeout(status, 3);
+            break;
+        }
+        float v[D];
+        const unsigned char* st = stages + s * S::kStageBytes;
+#pragma unroll
+        for (int b = 0; b < S::kBoxes; ++b) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 q = *reinterpret_cast<const uint4*>(
+                    st + b * kTmaRows * 128 + r * 128 + ((c ^ (r & 7)) << 4));
+                const uint32_t* m = P.sgn + b * 64 + c * 8;
+                float* o = v + b * 64 + c * 8;
+                o[0] = bf16lo(q.x, m[0]);
+                o[1] = bf16hi(q.x, m[1]);
+                o[2] = bf16lo(q.y, m[2]);
+                o[3] = bf16hi(q.y, m[3]);
+                o[4] = bf16lo(q.z, m[4]);
+                o[5] = bf16hi(q.z, m[5]);
+                o[6] = bf16lo(q.w, m[6]);
+                o[7] = bf16hi(q.w, m[7]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        F2 sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < D; i += 4) {
+            const F2 p0 = f2(v[i], v[i + 1]);
+            const F2 p1 = f2(v[i + 2], v[i + 3]);
+            sa = f2_fma(p0, p0, sa);
+            sb = f2_fma(p1, p1, sb);
+        }
+        float s0, s1, s2, s3;
+        f2_split(sa, s0, s1);
+        f2_split(sb, s2, s3);
+        const float ss = (s0 + s1) + (s2 + s3);
+        fwht_reg2<D>(v);
+        const float n = __fsqrt_rn(ss);
+        const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+        const float ks = inv * (float)kLutScale;
+        const F2 K2 = f2(ks, ks);
+        constexpr float kMagic = 12582912.0f + (float)kLutCenter;
+        const F2 M2 = f2(kMagic, kMagic);
+        constexpr int NW = D * BITS / 32;
+        uint32_t w[NW];
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = 0;
+#pragma unroll
+        for (int i = 0; i < D; i += 2) {
+            float fx, fy;
+            f2_split(f2_fma(f2(v[i], v[i + 1]), K2, M2), fx, fy);
+            const LutEntry e0 = lut[__float_as_uint(fx) & (kLutCells - 1)];
+            const LutEntry e1 = lut[__float_as_uint(fy) & (kLutCells - 1)];
+            const int id0 = e0.lo + (fmaf(v[i], inv, -e0.thr) >= 0.0f ? 1 : 0);
+            const int id1 = e1.lo + (fmaf(v[i + 1], inv, -e1.thr) >= 0.0f ? 1 : 0);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int id = h ? id1 : id0;
+                const int pos = (i + h) * BITS, wi = pos / 32, sh = pos % 32;
+                w[wi] += (uint32_t)id << sh;
+                if (sh + BITS > 32) w[wi + 1] += (uint32_t)id >> (32 - sh);
+            }
+        }
+        const int64_t row = tile * kTmaRows + r;
+        if (row < n_rows) {
+            store_bytes<RB>(packed + row * RB, w);
+            norms[row] = n;
+        }
+    }
+}
+
+// ------------------------------------------- encode on tcgen05 (d = 128)
+//
+// y = H (s . x) for a tile of 128 rows is one GEMM, Y = X (D H): X (128 x 128
+// bf16, TMA-loaded, K-major, 128-byte swizzle) times the constant +-1 matrix
+// D H (bf16, built once per CTA in shared memory) on the tensor cores, fp32
+// accumulation in tensor memory.  Warp roles: 0 = TMA producer, 1 = MMA
+// issuer (and tensor-memory owner), 2-9 = two epilogue warpgroups taking
+// alternate tiles; each epilogue thread reads its row from tensor memory
+// (32x32b loads), forms the norm, buckets through the exact table and packs.
+
+constexpr int kUmRows = 128;
+constexpr int kUmStages = 4;
+constexpr int kUmAcc = 4;             // tensor-memory accumulators of 128 columns
+constexpr int kUmThreads = 10 * 32;
+constexpr int kUmStageBytes = kUmRows * 128 * 2;
+constexpr int kUmSmemBytes = 1024 + kUmStages * kUmStageBytes + 128 * 128 * 2 + kLutCells * 8 +
+                             (2 * kUmStages + 2 * kUmAcc) * 8 + 16;
+
+template <int BITS>
+__global__ void __launch_bounds__(kUmThreads, 1)
+k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* __restrict__ packed,
+              float* __restrict__ norms, int* status, const __grid_constant__ RowParams P) {
+    constexpr int RB = 128 * BITS / 8;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    unsigned char* xs = base;                                   // stages of X
+    unsigned char* hb = xs + kUmStages * kUmStageBytes;         // D H, K-major
+    LutEntry* lut = reinterpret_cast<LutEntry*>(hb + 128 * 128 * 2);
+    uint64_t* full = reinterpret_cast<uint64_t*>(lut + kLutCells);
+    uint64_t* empty = full + kUmStages;
+    uint64_t* accf = empty + kUmStages;
+    uint64_t* acce = accf + kUmAcc;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(acce + kUmAcc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // B operand: element (n, k) = s_k * (-1)^popcount(n & k), stored like a
+    // TMA 128-byte-swizzled K-major tile (two 64-column halves of 16 KB).
+    for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
+        const int n = i >> 7, k = i & 127;
+        const bool neg = ((__popc(n & k) & 1) != 0) != (P.sgn[k] != 0u);
+        const int off = (k >> 6) * 16384 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
+        *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBF80u : 0x3F80u;
+    }
+    build_lut(lut, P.bnd, (1 << BITS) - 1);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kUmStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kUmAcc; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], 4);
+        }
+        mbar_fence_init();
+    }
+    fence_proxy_async_smem();
+    if (warp == 1) tmem_alloc<kUmAcc * 128>(slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const int64_t n_tiles = (n_rows + kUmRows - 1) / kUmRows;
+
+    if (warp == 0) {  // ---- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            int it = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int s = it % kUmStages;
+                if (it >= kUmStages && !mbar_wait(&empty[s], ((it / kUmStages) - 1) & 1)) {
+                    report_timeout(status, 11);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kUmStageBytes);
+                tma_load_2d(xs + s * kUmStageBytes, &xmap, 0, (int)(tile * kUmRows), &full[s]);
+                tma_load_2d(xs + s * kUmStageBytes + 16384, &xmap, 64, (int)(tile * kUmRows), &full[s]);
+            }
+            for (int j = (it > kUmStages ? it - kUmStages : 0); j < it; ++j)
+                if (!mbar_wait(&full[j % kUmStages], (j / kUmStages) & 1)) {
+                    report_timeout(status, 12);
+                    break;
+                }
+        }
+    } else if (warp == 1) {  // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16(128, 128, true);
+            const uint32_t xs_a = smem_addr(xs), hb_a = smem_addr(hb);
+            int it = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int s = it % kUmStages, a = it % kUmAcc;
+                if (!mbar_wait(&full[s], (it / kUmStages) & 1)) {
+                    report_timeout(status, 13);
+                    break;
+                }
+                if (it >= kUmAcc && !mbar_wait(&acce[a], ((it / kUmAcc) - 1) & 1)) {
+                    report_timeout(status, 14);
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_f16(tmem + a * 128, umma_desc_sw128(xs_a + s * kUmStageBytes + off),
+                             umma_desc_sw128(hb_a + off), idesc, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);
+                umma_commit(&accf[a]);
+            }
+            // the last accumulators must be complete before tensor memory is freed
+            for (int j = (it > kUmAcc ? it - kUmAcc : 0); j < it; ++j)
+                if (!mbar_wait(&accf[j % kUmAcc], (j / kUmAcc) & 1)) {
+                    report_timeout(status, 15);
+                    break;
+                }
+        }
+    } else {  // ---- epilogue: warps 2-5 take even tiles, 6-9 odd tiles
+        const int wg = (warp - 2) >> 2, q = warp & 3;
+        const int r = 32 * q + lane;
+        constexpr int NW = 128 * BITS / 32;
+        constexpr float kMagic = 12582912.0f + (float)kLutCenter;
+        const F2 M2 = f2(kMagic, kMagic);
+        int it = wg;
+        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < n_tiles;
+             tile += 2 * (int64_t)gridDim.x, it += 2) {
+            const int a = it % kUmAcc;
+            if (!mbar_wait(&accf[a], (it / kUmAcc) & 1)) {
+                report_timeout(status, 16);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + a * 128;
+            F2 sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t y[32];
+                tmem_ld32(ta + 32 * c, y);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const F2 p0 = f2(__uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+                    const F2 p1 = f2(__uint_as_float(y[i + 2]), __uint_as_float(y[i + 3]));
+                    sa = f2_fma(p0, p0, sa);
+                    sb = f2_fma(p1, p1, sb);
+                }
+            }
+            float s0, s1, s2, s3;
+            f2_split(sa, s0, s1);
+            f2_split(sb, s2, s3);
+            const float ss = (s0 + s1) + (s2 + s3);  // = d * ||x||^2
+            const float n = __fsqrt_rn(ss * (1.0f / 128.0f));
+            const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // w = y / sqrt(ss) = u
+            const float ks = inv * (float)kLutScale;
+            const F2 K2 = f2(ks, ks);
+            uint32_t w[NW];
+#pragma unroll
+            for (int k = 0; k < NW; ++k) w[k] = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t y[32];
+                tmem_ld32(ta + 32 * c, y);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float y0 = __uint_as_float(y[i]), y1 = __uint_as_float(y[i + 1]);
+                    float fx, fy;
+                    f2_split(f2_fma(f2(y0, y1), K2, M2), fx, fy);
+                    const LutEntry e0 = lut[__float_as_uint(fx) & (kLutCells - 1)];
+                    const LutEntry e1 = lut[__float_as_uint(fy) & (kLutCells - 1)];
+                    const int id0 = e0.lo + (fmaf(y0, inv, -e0.thr) >= 0.0f ? 1 : 0);
+                    const int id1 = e1.lo + (fmaf(y1, inv, -e1.thr) >= 0.0f ? 1 : 0);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int id = h ? id1 : id0;
+                        const int pos = (32 * c + i + h) * BITS, wi = pos / 32, sh = pos % 32;
+                        w[wi] += (uint32_t)id << sh;
+                        if (sh + BITS > 32) w[wi + 1] += (uint32_t)id >> (32 - sh);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[a]);
+            const int64_t row = tile * kUmRows + r;
+            if (row < n_rows) {
+                store_bytes<RB>(packed + row * RB, w);
+                norms[row] = n;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<kUmAcc * 128>(tmem);
+    }
+}
+
+// ------------------------------------------------------- decode (v2)
+//
+// One row per thread, d <= 128: the next row's packed words and norm are
+// loaded before the current row is transformed, so the load latency hides
+// behind a row of arithmetic.  Centroids come from a 16-entry shared table
+// (every entry in its own bank: conflict-free); field extraction produces the
+// table's byte offsets directly.
+
+template <int BITS, int D>
+__device__ __forceinline__ void centroids_of(const uint32_t* w, const float (&cen)[16], float (&v)[D]) {
+    const char* cb = reinterpret_cast<const char*>(cen);
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) {
+            const uint32_t lo = (w[k] << 2) & 0x3C3C3C3Cu;  // fields 0,2,4,6 times 4
+            const uint32_t hi = (w[k] >> 2) & 0x3C3C3C3Cu;  // fields 1,3,5,7 times 4
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[8 * k + 2 * j] = *reinterpret_cast<const float*>(cb + __byte_perm(lo, 0, 0x4440 + j));
+                v[8 * k + 2 * j + 1] = *reinterpret_cast<const float*>(cb + __byte_perm(hi, 0, 0x4440 + j));
+            }
+        }
+    } else if constexpr (BITS == 2) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t m[4] = {(w[k] << 2) & 0x0C0C0C0Cu, w[k] & 0x0C0C0C0Cu,
+                                   (w[k] >> 2) & 0x0C0C0C0Cu, (w[k] >> 4) & 0x0C0C0C0Cu};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int f = 0; f < 4; ++f)
+                    v[16 * k + 4 * j + f] = *reinterpret_cast<const float*>(cb + __byte_perm(m[f], 0, 0x4440 + j));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
+            uint32_t x;
+            if (sh + BITS <= 32) x = w[wi] >> sh;
+            else x = __funnelshift_r(w[wi], w[wi + 1], sh);
+            v[i] = *reinterpret_cast<const float*>(cb + ((x << 2) & 0x1Cu));
+        }
+    }
+}
+
+template <int D, int BITS, typename TO>
+__global__ void __launch_bounds__(128, 3) k_decode2(const uint8_t* __restrict__ packed,
+                                                 const float* __restrict__ norms, int64_t n_rows,
+                                                 TO* __restrict__ y, const __grid_constant__ RowParams P) {
+    __shared__ float cen_s[16];
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
+    __syncthreads();
+    constexpr int RB = D * BITS / 8, NW = RB / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // two rows in flight ahead of the one being transformed
+    uint32_t wa[NW], wb[NW];
+    float na = 0.f, nb = 0.f;
+    if (row < n_rows) {
+        load_bytes<RB>(packed + row * RB, wa);
+        na = __ldg(norms + row);
+    }
+    if (row + stride < n_rows) {
+        load_bytes<RB>(packed + (row + stride) * RB, wb);
+        nb = __ldg(norms + row + stride);
+    }
+    for (; row < n_rows; row += stride) {
+        uint32_t w[NW];
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            w[k] = wa[k];
+            wa[k] = wb[k];
+        }
+        const float norm = na;
+        na = nb;
+        const int64_t nxt = row + 2 * stride;
+        if (nxt < n_rows) {
+            load_bytes<RB>(packed + nxt * RB, wb);
+            nb = __ldg(norms + nxt);
+        }
+        float v[D];
+        centroids_of<BITS, D>(w, cen_s, v);
+        fwht_reg2<D>(v);
+        const float scs = norm * P.inv_sqrt_d;
+        const F2 sc = f2(scs, scs);
+        TO* out = y + row * D;
+        if constexpr (sizeof(TO) == 4) {
+#pragma unroll
+            for (int k = 0; k < D; k += 4) {
+                float ax, ay, bx, by;
+                f2_split(f2_mul(f2(v[k], v[k + 1]), sc), ax, ay);
+                f2_split(f2_mul(f2(v[k + 2], v[k + 3]), sc), bx, by);
+                float4 o;
+                o.x = __uint_as_float(__float_as_uint(ax) ^ P.sgn[k]);
+                o.y = __uint_as_float(__float_as_uint(ay) ^ P.sgn[k + 1]);
+                o.z = __uint_as_float(__float_as_uint(bx) ^ P.sgn[k + 2]);
+                o.w = __uint_as_float(__float_as_uint(by) ^ P.sgn[k + 3]);
+                reinterpret_cast<float4*>(out)[k / 4] = o;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < D; k += 8) {
+                uint32_t q[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    float ax, ay;
+                    f2_split(f2_mul(f2(v[k + 2 * m], v[k + 2 * m + 1]), sc), ax, ay);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(ax, ay);
+                    q[m] = *reinterpret_cast<uint32_t*>(&h) ^ ((P.sgn[k + 2 * m] >> 16) | P.sgn[k + 2 * m + 1]);
+                }
+                reinterpret_cast<uint4*>(out)[k / 8] = make_uint4(q[0], q[1], q[2], q[3]);
+            }
+        }
+    }
+}
+
+// --------------------------------------------- decode to bf16, d = 128 (v3)
+//
+// As k_decode2, with the output staged per warp: 32 rows of bf16 (8 KB) are
+// written thread-per-row into a 128-byte-swizzled shared buffer (conflict
+// free) and leave as two 2-D TMA stores, so global writes are whole lines.
+// Two buffers per warp; the packed rows of the next warp tile are loaded
+// before the current one is transformed.
+
+constexpr int kDec3Warps = 4;
+constexpr int kDec3Smem = kDec3Warps * 2 * 8192 + 1024;
+
+template <int BITS>
+__global__ void __launch_bounds__(32 * kDec3Warps, 3)
+k_decode3(const uint8_t* __restrict__ packed, const float* __restrict__ norms, int64_t n_rows,
+          const __grid_constant__ CUtensorMap ymap, const __grid_constant__ RowParams P) {
+    constexpr int D = 128, RB = D * BITS / 8, NW = RB / 4;
+    __shared__ float cen_s[16];
+    extern __shared__ __align__(1024) unsigned char dsm[];
+    unsigned char* base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* buf = base + warp * 2 * 8192;
+    const int64_t n_tiles = (n_rows + 31) / 32;
+    const int64_t wstride = (int64_t)gridDim.x * kDec3Warps;
+    int64_t tile = (int64_t)blockIdx.x * kDec3Warps + warp;
+    uint32_t wn[NW];
+    float nn = 0.f;
+    auto fetch = [&](int64_t tl) {
+        const int64_t row = tl * 32 + lane;
+        if (tl < n_tiles && row < n_rows) {
+            load_bytes<RB>(packed + row * RB, wn);
+            nn = __ldg(norms + row);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NW; ++k) wn[k] = 0;
+            nn = 0.f;
+        }
+    };
+    fetch(tile);
+    int it = 0;
+    for (; tile < n_tiles; tile += wstride, ++it) {
+        uint32_t w[NW];
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = wn[k];
+        const float norm = nn;
+        fetch(tile + wstride);
+        float v[D];
+        centroids_of<BITS, D>(w, cen_s, v);
+        fwht_reg2<D>(v);
+        const float scs = norm * P.inv_sqrt_d;
+        const F2 sc = f2(scs, scs);
+        unsigned char* b = buf + (it & 1) * 8192;
+        // the store that last read this buffer (two tiles ago) must be done
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = columns 8c .. 8c+7
+            uint32_t q[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int k = 8 * c + 2 * m;
+                float ax, ay;
+                f2_split(f2_mul(f2(v[k], v[k + 1]), sc), ax, ay);
+                __nv_bfloat162 h = __floats2bfloat162_rn(ax, ay);
+                q[m] = *reinterpret_cast<uint32_t*>(&h) ^ ((P.sgn[k] >> 16) | P.sgn[k + 1]);
+            }
+            const int half = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4*>(b + half * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                make_uint4(q[0], q[1], q[2], q[3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&ymap, 0, (int)(tile * 32), b);
+            tma_store_2d(&ymap, 64, (int)(tile * 32), b + 4096);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) bulk_wait<0>();
+}
+
+}  // namespace dev
+
 // ---------------------------------------------------------------- launchers
 
 namespace {
 
+template <int D, int BITS>
+cudaError_t enc_tma(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
+    using Sh = dev::TmaEncodeShape<D>;
+    CUtensorMap map;
+    cudaError_t e = make_rows_map(&map, x, 2, D, (uint64_t)n, dev::kTmaRows);
+    if (e != cudaSuccess) return e;
+    auto fn = dev::k_encode_tma<D, BITS>;
+    static int attr_dev_mask = 0;  // devices on which the smem opt-in was set
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(attr_dev_mask & (1 << dev))) {
+        e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_dev_mask |= 1 << dev;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)fn, dev::kTmaThreads, Sh::kSmemBytes) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    const int64_t tiles = (n + dev::kTmaRows - 1) / dev::kTmaRows;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (grid > tiles) grid = tiles;
+    fn<<<(unsigned)grid, dev::kTmaThreads, Sh::kSmemBytes, s>>>(map, n, pk, nm, status_word(), P);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t enc_umma(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
+    CUtensorMap map;
+    cudaError_t e = make_rows_map(&map, x, 2, 128, (uint64_t)n, dev::kUmRows);
+    if (e != cudaSuccess) return e;
+    auto fn = dev::k_encode_umma<BITS>;
+    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kUmSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (n + dev::kUmRows - 1) / dev::kUmRows;
+    int64_t grid = num_sms();
+    if (grid > tiles) grid = tiles;
+    fn<<<(unsigned)grid, dev::kUmThreads, dev::kUmSmemBytes, s>>>(map, n, pk, nm, status_word(), P);
+    return cudaGetLastError();
+}
+
 template <int D, int BITS, typename T>
 cudaError_t enc(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
+#if TQ_ENCODE_TCGEN05
+    if constexpr (D == 128 && sizeof(T) == 2) return enc_umma<BITS>(x, n, pk, nm, P, s);
+#endif
+    if constexpr ((D == 64 || D == 128) && sizeof(T) == 2) return enc_tma<D, BITS>(x, n, pk, nm, P, s);
     auto fn = dev::k_encode<D, BITS, T>;
     unsigned g = grid_for((const void*)fn, dev::kBlock, n * dev::RowShape<D>::R);
     fn<<<g, dev::kBlock, 0, s>>>(static_cast<const T*>(x), n, pk, nm, P);
     return cudaGetLastError();
 }
 
+template <int BITS>
+cudaError_t dec3(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
+    CUtensorMap map;
+    cudaError_t e = make_rows_map(&map, y, 2, 128, (uint64_t)n, 32);
+    if (e != cudaSuccess) return e;
+    auto fn = dev::k_decode3<BITS>;
+    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kDec3Smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)fn, 32 * dev::kDec3Warps, dev::kDec3Smem) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    const int64_t warp_tiles = (n + 31) / 32;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    const int64_t need = (warp_tiles + dev::kDec3Warps - 1) / dev::kDec3Warps;
+    if (grid > need) grid = need;
+    fn<<<(unsigned)grid, 32 * dev::kDec3Warps, dev::kDec3Smem, s>>>(pk, nm, n, map, P);
+    return cudaGetLastError();
+}
+
 template <int D, int BITS, typename TO>
 cudaError_t dec(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
+    if constexpr (D == 128 && sizeof(TO) == 2) return dec3<BITS>(pk, nm, n, y, P, s);
+    if constexpr (D == 64 || D == 128) {
+        auto fn2 = dev::k_decode2<D, BITS, TO>;
+        unsigned g = grid_for((const void*)fn2, 128, n);
+        fn2<<<g, 128, 0, s>>>(pk, nm, n, static_cast<TO*>(y), P);
+        return cudaGetLastError();
+    }
     auto fn = dev::k_decode<D, BITS, TO>;
     unsigned g = grid_for((const void*)fn, dev::kBlock, n * dev::RowShape<D>::R);
     fn<<<g, dev::kBlock, 0, s>>>(pk, nm, n, static_cast<TO*>(y), P);

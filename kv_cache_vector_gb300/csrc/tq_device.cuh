@@ -87,19 +87,80 @@ __device__ __forceinline__ void load_signed(const __nv_bfloat16* __restrict__ sr
 // ------------------------------------------------------------------ FWHT
 
 // Unnormalised butterfly over the E registers: stages len = 1 .. E/2,
-// (a, b) -> (a + b, a - b).
+// (a, b) -> (a + b, a - b).  Every loop has a constant trip count (stage st,
+// butterfly q; the pair is (i, i + 2^st) with i = q with a zero bit inserted
+// at position st), so full unrolling turns every index into a constant and
+// the row stays in registers.
 template <int E>
 __device__ __forceinline__ void fwht_reg(float (&v)[E]) {
 #pragma unroll
-    for (int len = 1; len < E; len <<= 1) {
+    for (int st = 0; (1 << st) < E; ++st) {
 #pragma unroll
-        for (int i = 0; i < E; i += 2 * len) {
+        for (int q = 0; q < E / 2; ++q) {
+            const int len = 1 << st;
+            const int i = ((q >> st) << (st + 1)) | (q & (len - 1));
+            const float a = v[i], b = v[i + len];
+            v[i] = a + b;
+            v[i + len] = a - b;
+        }
+    }
+}
+
+// Packed fp32x2 arithmetic on a register pair (inline PTX on .b64 operands;
+// the pair is packed and unpacked with mov, which register allocation folds).
+struct F2 {
+    unsigned long long r;
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 o;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(o.r) : "f"(lo), "f"(hi));
+    return o;
+}
+__device__ __forceinline__ void f2_split(F2 a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.r));
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    F2 o;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+    F2 o;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+    F2 o;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+    F2 o;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(o.r) : "l"(a.r), "l"(b.r), "l"(c.r));
+    return o;
+}
+
+// The same transform with packed fp32x2 arithmetic: stage len = 1 is scalar,
+// every later stage pairs registers (i, i+1) with (i+len, i+len+1), so one
+// instruction does two butterflies.  Same lane-op count, half the issue slots.
+template <int E>
+__device__ __forceinline__ void fwht_reg2(float (&v)[E]) {
 #pragma unroll
-            for (int j = i; j < i + len; ++j) {
-                float a = v[j], b = v[j + len];
-                v[j] = a + b;
-                v[j + len] = a - b;
-            }
+    for (int j = 0; j < E; j += 2) {
+        const float a = v[j], b = v[j + 1];
+        v[j] = a + b;
+        v[j + 1] = a - b;
+    }
+#pragma unroll
+    for (int st = 1; (1 << st) < E; ++st) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {  // q-th pair of butterflies of this stage
+            const int len = 1 << st;
+            const int i = (((2 * q) >> st) << (st + 1)) | ((2 * q) & (len - 1));
+            const F2 a = f2(v[i], v[i + 1]);
+            const F2 b = f2(v[i + len], v[i + len + 1]);
+            f2_split(f2_add(a, b), v[i], v[i + 1]);
+            f2_split(f2_sub(a, b), v[i + len], v[i + len + 1]);
         }
     }
 }

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tq.h"
@@ -44,9 +45,9 @@ struct Plan {
 // Bucketing lookup table geometry (encode): cell g covers the normalised
 // coordinate w with rint(w * kLutScale) = g - kLutCenter, i.e. the closed
 // interval [(g - kLutCenter - 0.5) / kLutScale, (g - kLutCenter + 0.5) / kLutScale].
-constexpr int kLutScale = 512;
-constexpr int kLutCenter = 1024;
-constexpr int kLutCells = 2048;  // covers w in [-2, 2); |w| <= 1 for finite rows
+constexpr int kLutScale = 256;
+constexpr int kLutCenter = 512;
+constexpr int kLutCells = 1024;  // covers w in [-2, 2); |w| <= 1 for finite rows
 
 // Launchers, one explicit instantiation per head dimension D (each kernel
 // file is compiled once per D, in parallel).  They validate nothing: the
@@ -65,10 +66,15 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
 
 struct AttnGeometry {
     int n_splits;
-    int split_len;  // positions per split
+    int split_len;    // positions per split
+    int parts;        // partials written per split (one per warp in the d = 128 kernel)
+    bool q16;         // the workspace starts with the rotated fp16 queries
 };
-AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int num_sms);
+AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
+inline size_t attn2_q16_bytes(int B, int Hq) {  // rotated queries, rounded to 256 B
+    return ((size_t)B * Hq * 128 * 2 + 255) / 256 * 256;
+}
 template <int D, int KB>
 cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
                            const tq_cache_view& cache, int64_t ctx_len, float* out, void* workspace,
@@ -78,6 +84,15 @@ cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
 int num_sms();
 int blocks_per_sm(const void* kernel, int block_threads, size_t dyn_smem);
 unsigned grid_for(const void* kernel, int block_threads, int64_t items);
+
+// Device address of the status word on the current device (kernels with
+// bounded waits write it when they give up); nullptr if unavailable.
+int* status_word();
+
+// 2-D TMA descriptor over rows: n_rows x d elements of `esize` bytes, boxes of
+// 128 bytes (inner) x box_rows rows, 128-byte swizzle, zero fill past the end.
+cudaError_t make_rows_map(CUtensorMap* map, const void* base, int esize, uint64_t d,
+                          uint64_t n_rows, uint32_t box_rows);
 
 // Records the cudaError_t that tq_last_cuda_error reports for this thread.
 void set_last_cuda_error(cudaError_t e);

@@ -3,6 +3,8 @@
 // word that kernels with bounded waits set when they give up.
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "tq_internal.h"
 
 namespace tq {
@@ -52,21 +54,86 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
     return (unsigned)(want < 1 ? 1 : want);
 }
 
-// Split-K geometry of the decode attention: the longest split (<= 512
-// positions) that still gives at least two CTAs per SM.
-AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int sms) {
+// Split-K geometry of the decode attention.  d = 128 (tensor-core kernel):
+// splits of 512 positions, four partials each (one per warp).  Otherwise the
+// longest split (<= 512 positions) that still gives two CTAs per SM.
+AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int sms, int d) {
     AttnGeometry g;
+    if (d == 128) {
+        g.split_len = 512;
+        g.n_splits = (int)((ctx_len + 511) / 512);
+        g.parts = 4;
+        g.q16 = true;
+        return g;
+    }
     int split = 512;
     const int64_t pairs = (int64_t)B * Hkv;
     const int64_t want = 2LL * (sms > 0 ? sms : 1);
     while (split > 64 && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
     g.split_len = split;
     g.n_splits = (int)((ctx_len + split - 1) / split);
+    g.parts = 1;
+    g.q16 = false;
     return g;
 }
 
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g) {
-    return sizeof(float) * (size_t)B * Hq * g.n_splits * (d + 2);
+    return (g.q16 ? attn2_q16_bytes(B, Hq) : 0) +
+           sizeof(float) * (size_t)B * Hq * g.n_splits * g.parts * (d + 2);
+}
+
+int* status_word() {
+    static std::mutex mu;
+    static int* ptr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, dev::g_status) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        ptr[dev] = static_cast<int*>(p);
+    }
+    return ptr[dev];
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+}  // namespace
+
+cudaError_t make_rows_map(CUtensorMap* map, const void* base, int esize, uint64_t d,
+                          uint64_t n_rows, uint32_t box_rows) {
+    auto fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t dims[2] = {d, n_rows};
+    cuuint64_t strides[1] = {d * (uint64_t)esize};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esize), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t read_device_status(int reset, int* out) {

@@ -102,10 +102,10 @@ def test_hot_call_validation_before_launch(L):
 
 
 def _emulate_table_bucket(bnd32: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """numpy restatement of the kernels' bucketing table: cell = rint(w*512)
+    """numpy restatement of the kernels' bucketing table: cell = rint(w*256)
     (round half even, exact), lo = #{beta < cell_lo}, thr = the boundary in the
     closed cell, idx = lo + [w >= thr]."""
-    S, C, N = 512, 1024, 2048
+    S, C, N = 256, 512, 1024
     g = np.arange(N)
     lo = ((g - C - 0.5) / S).astype(np.float32).astype(np.float64)
     hi = ((g - C + 0.5) / S).astype(np.float32).astype(np.float64)
@@ -130,7 +130,7 @@ def test_bucketing_table_is_exact(L, d, bits):
     p = abi.Plan(d, 1)
     _, bnd = p.codebook(bits)
     rng = np.random.default_rng(d + bits)
-    edges = ((np.arange(-530, 530) + 0.5) / 512).astype(np.float32)
+    edges = ((np.arange(-265, 265) + 0.5) / 256).astype(np.float32)
     w = np.concatenate([
         bnd, np.nextafter(bnd, np.float32(-9)), np.nextafter(bnd, np.float32(9)),
         edges, np.nextafter(edges, np.float32(-9)), np.nextafter(edges, np.float32(9)),
