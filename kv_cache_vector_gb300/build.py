@@ -45,6 +45,10 @@ def _deps():
 def _stale() -> bool:
     if not os.path.exists(OUT):
         return True
+    stamp = OUT + ".defines"
+    want = os.environ.get("TQ_NVCC_DEFINES", "")
+    if (open(stamp).read() if os.path.exists(stamp) else "") != want:
+        return True
     t = os.path.getmtime(OUT)
     return any(os.path.getmtime(f) > t for f in _deps())
 
@@ -57,6 +61,9 @@ def _compile(unit, verbose: bool) -> str:
            "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
     for k, v in defs.items():
         cmd.insert(1, f"-DTQ_UNIT_{k}={v}")
+    # implementation selectors, e.g. TQ_NVCC_DEFINES="TQ_ENCODE_TCGEN05=1"
+    for d in os.environ.get("TQ_NVCC_DEFINES", "").split():
+        cmd.insert(1, f"-D{d}")
     if src.endswith(".cu"):
         cmd[1:1] = ["-Xptxas", "-v"] if verbose else []
     else:
@@ -82,6 +89,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, OUT)
+    with open(OUT + ".defines", "w") as f:
+        f.write(os.environ.get("TQ_NVCC_DEFINES", ""))
     return OUT
 
 

@@ -161,6 +161,38 @@ void fill_row_params(const tq::Plan& P, int bits, tq::RowParams& R) {
     R.inv_sqrt_d = (float)(1.0 / std::sqrt((double)P.d));
 }
 
+// Nearest fp16 value of x (ties to even), for x inside the normal fp16 range:
+// 11 significant bits.
+double round_to_half(double x) {
+    int e = 0;
+    const double m = std::frexp(x, &e);  // x = m * 2^e, 0.5 <= |m| < 1
+    return std::ldexp(std::nearbyint(std::ldexp(m, 11)), e - 11);
+}
+
+// The d = 128 attention multiplies fp16 centroids on the tensor cores.  A
+// common scale s leaves the attention unchanged once 1/s is applied to the
+// result, and a good s brings every centroid of the width close to an fp16
+// value: s is the best of 2^14 evenly spaced candidates in [1, 2) for the
+// worst relative rounding error (centroids are symmetric, so the positive
+// half decides).
+void half_scale(const float* c, int L, float* s_out, float* h_out) {
+    double best = std::numeric_limits<double>::infinity(), best_s = 1.0;
+    for (int i = 0; i < (1 << 14); ++i) {
+        const double s = 1.0 + i / 16384.0;
+        double worst = 0.0;
+        for (int k = L / 2; k < L && worst < best; ++k) {
+            const double v = (double)c[k] * s;
+            worst = std::fmax(worst, std::fabs(round_to_half(v) - v) / std::fabs(v));
+        }
+        if (worst < best) {
+            best = worst;
+            best_s = s;
+        }
+    }
+    *s_out = (float)best_s;  // 15 significant bits: exact
+    for (int k = 0; k < 16; ++k) h_out[k] = k < L ? (float)round_to_half((double)c[k] * best_s) : 0.0f;
+}
+
 template <int V>
 using IntC = std::integral_constant<int, V>;
 
@@ -196,6 +228,25 @@ bool valid_dtype(tq_dtype t) { return t == TQ_F32 || t == TQ_BF16; }
 
 void tq::set_last_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
+void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, float sparse_thr,
+                          AttnParams& A) {
+    for (int i = 0; i < kMaxD; ++i) A.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
+    for (int i = 0; i < 16; ++i) {
+        A.kcen[i] = P.c32[k_bits][i];
+        A.vcen[i] = P.c32[v_bits][i];
+        A.kcen_h[i] = P.hcen[k_bits][i];
+        A.vcen_h[i] = P.hcen[v_bits][i];
+    }
+    const double sd = std::sqrt((double)P.d);
+    A.inv_sqrt_d = (float)(1.0 / sd);
+    A.scale = scale;
+    A.sparse_thr = sparse_thr;
+    const double ks = P.hscale[k_bits] > 0.0f ? P.hscale[k_bits] : 1.0;
+    const double vs = P.hscale[v_bits] > 0.0f ? P.hscale[v_bits] : 1.0;
+    A.q_mul = (float)((double)scale * 1.4426950408889634 / (sd * ks));
+    A.out_mul = (float)(1.0 / vs);
+}
+
 extern "C" {
 
 tq_status tq_codebook_init(int d, int bits, double* centroids, double* boundaries) {
@@ -230,6 +281,7 @@ tq_status tq_plan_create(int d, uint64_t seed, tq_plan** out) {
             delete P;
             return TQ_ERR_UNSUPPORTED;
         }
+        if (bits >= 2 && d == 128) half_scale(P->c32[bits], L, &P->hscale[bits], P->hcen[bits]);
     }
     *out = reinterpret_cast<tq_plan*>(P);
     return TQ_OK;
@@ -328,7 +380,7 @@ size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !is_pow2(d) ||
         d > tq::kMaxD)
         return 0;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms(), d);
+    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), d);
     return tq::attn_workspace_bytes(B, Hq, d, g);
 }
 
@@ -351,7 +403,7 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms(), P->d);
+    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d);
     size_t need = tq::attn_workspace_bytes(B, Hq, P->d, g);
     if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
@@ -360,15 +412,7 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
         !device_accessible(cache.k_norm) || !device_accessible(cache.v_norm))
         return TQ_ERR_INVALID_ARG;
     tq::AttnParams A;
-    for (int i = 0; i < tq::kMaxD; ++i)
-        A.sgn[i] = (i < P->d && P->signs[i] < 0) ? 0x80000000u : 0u;
-    for (int i = 0; i < 16; ++i) {
-        A.kcen[i] = P->c32[k_bits][i];
-        A.vcen[i] = P->c32[v_bits][i];
-    }
-    A.inv_sqrt_d = (float)(1.0 / std::sqrt((double)P->d));
-    A.scale = scale;
-    A.sparse_thr = sparse_v_threshold;
+    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
     cudaError_t e = dispatch_attn_d(P->d, [&](auto D) {
         constexpr int d = decltype(D)::value;
         auto st = reinterpret_cast<cudaStream_t>(stream);

@@ -13,6 +13,7 @@
 
 #include <cuda_fp16.h>
 
+#include "tq_async.cuh"
 #include "tq_device.cuh"
 
 namespace tq {
@@ -223,38 +224,83 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
     out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }
 
-// ============================================================ v2, d = 128
+// ============================================================ d = 128
 //
-// Tensor-core flash-decode (mma.sync m16n8k16, fp16 operands, fp32
-// accumulation).  Per warp and 16-position tile:
-//   S = Q K^T   rows = the G query heads of the group (padded to 16), columns =
-//               8 positions per MMA; A = q (rotated once, scaled by
-//               scale*log2(e), fp16, in registers), B = K centroids straight
-//               from a lane-replicated shared table.  The 128 contraction dims
-//               are permuted so that lane t reads one contiguous chunk (dims
-//               32t..32t+31) of each K row; q is loaded with the same
-//               permutation, and a dot product does not depend on the order.
-//   softmax     exp2 with a lazily updated running max (rescale only when the
-//               tile max exceeds it by more than kLazy, or at once when norms
-//               are large), fp32 denominators.
-//   O += P V    the S accumulators are exactly the A fragments of P (heads x
-//               positions); V rows are dequantised by the warp into a
-//               swizzled shared tile (16 x 128 fp16) and read with
-//               ldmatrix.trans; the V norm is folded into P.
-// Work items (batch, KV head, 512-position split) are spread over persistent
-// CTAs of 4 warps; each warp owns 128 positions and writes its own partial
-// (acc[128], m, l) with m in log2 units; a combine kernel merges them.
+// Tensor-core flash-decode (mma.sync m16n8k16: fp16 operands, fp32
+// accumulation) over chunks of 32 positions, processed as two sub-tiles of
+// 16 positions.
+//
+//   S^T = K Q~    A = K centroids of 16 positions (rows) x 16 dims, looked
+//                 up as pairs (two consecutive dims, fp16 x 2) in a lane-
+//                 replicated table; B = the rotated query, 8 columns = 4
+//                 query heads x (fp16 high part, fp16 low part).  The score
+//                 of a head is the sum of its two columns, so the query keeps
+//                 about 22 significant bits.  The 128 contraction dims are
+//                 permuted so that lane t reads dims 32t..32t+31 of a K row;
+//                 a dot product does not depend on the order.
+//   softmax       exp2 with a lazily updated running maximum (updated only
+//                 when a chunk's maximum exceeds it by more than kLazy, so
+//                 p <= 2^kLazy), fp32 denominators.
+//   O^T += V^T P  A = V centroids, 16 dims (rows) x 16 positions, from pair
+//                 lookups of four positions and byte permutes; B = p times the
+//                 V norm, 8 columns = 4 heads x (high, low part).  Row g of
+//                 m-tile mt is dim 16g + 2mt, row g + 8 is dim 16g + 2mt + 1,
+//                 so lane row g ends up holding dims 16g..16g+15.
+// The tables hold fp16 values of c * s, with the scale s chosen on the host
+// so that every centroid of the width is close to its fp16 value (worst
+// relative error about 1e-4 at 4 bits, 3e-5 at 3 bits); 1/s_k is folded into
+// the query and 1/s_v into the output.  Query heads go in groups of four:
+// NG = 1 for G <= 4, NG = 2 for G <= 8.
+//
+// Data movement: CTAs of kAttn3Warps warps take contiguous ranges of work
+// items (batch, KV head, segment of kAttn3Warps * warp_len positions); warp w
+// takes positions [w * warp_len, (w + 1) * warp_len) of each segment, in
+// chunks of 32.  A warp streams its own chunks through a 3-stage ring in
+// shared memory: one lane issues 1-D bulk copies (cp.async.bulk) of the
+// chunk's packed K and V rows, each lane copies the two norms of one
+// position (cp.async, 4 bytes), and one mbarrier per stage completes when
+// all of it has landed.  At the end of an item the warps merge their
+// partials through shared memory and write one partial (acc[128], m, l) per
+// query head; k_attn3_combine merges the items of a (batch, head).
 
-constexpr int kA2Warps = 4;
-constexpr int kA2Threads = 32 * kA2Warps;
-constexpr int kA2WarpPos = 128;
-constexpr int kA2Split = kA2Warps * kA2WarpPos;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLazy = 8.0f;  // log2 units: p <= 256 before a forced rescale
+constexpr int kA3Chunk = 32;
+constexpr int kA3MergeStride = 132;  // floats per (warp, head) row of the merge buffer
+constexpr float kLazy = 8.0f;        // log2 units
+// Shared memory is addressed by absolute shared-window address.  The pair
+// table starts at 128 KiB: entry e of lane l's column is at
+// kA3TableAt + e * 256 + 4 * l (K) or + 128 + 4 * l (V), so a lookup address
+// is (e << 8) | slot, one byte permute for a 4-bit pair.
+constexpr uint32_t kA3RingAt = 2048;
+constexpr uint32_t kA3TableAt = 131072;
+// Device status codes.
+constexpr int kA3StatusWait = 31;    // a ring stage did not complete within the bound
+constexpr int kA3StatusLayout = 32;  // dynamic shared memory starts above kA3RingAt
 
-template <int BITS>
-struct PairTable {  // (2*BITS)-bit index -> two fp16 centroids of consecutive dims
-    static constexpr int kEntries = 1 << (2 * BITS);
+// Warps and ring stages per CTA: 12 x 2 for up to four query heads per KV
+// head (about 160 registers a thread), 8 x 3 for up to eight (about 220).
+template <int NG>
+struct A3Shape {
+    static constexpr int kWarps = NG == 1 ? kAttn3WarpsG4 : kAttn3WarpsG8;
+    static constexpr int kStages = NG == 1 ? 2 : 3;
+    static constexpr int kThreads = 32 * kWarps;
+};
+
+template <int KB, int VB, int NG>
+struct A3Layout {
+    static constexpr int kWarps = A3Shape<NG>::kWarps, kStages = A3Shape<NG>::kStages;
+    static constexpr int kKRow = 16 * KB, kVRow = 16 * VB;  // bytes of a d = 128 row
+    static constexpr int kVOff = kA3Chunk * kKRow;
+    static constexpr int kKnOff = kA3Chunk * (kKRow + kVRow);
+    static constexpr int kVnOff = kKnOff + 4 * kA3Chunk;
+    static constexpr int kStage = kVnOff + 4 * kA3Chunk;
+    static constexpr int kEntries = 1 << (2 * (KB > VB ? KB : VB));
+    static constexpr int kHeads = 4 * NG;
+    static constexpr uint32_t kMergeAt = kA3TableAt + 256u * kEntries;
+    static constexpr uint32_t kBarAt = kMergeAt + 4u * kWarps * kHeads * kA3MergeStride;
+    static constexpr uint32_t kEnd = kBarAt + 8u * kWarps * kStages;
+    static_assert(kStage % 16 == 0, "stage alignment");
+    static_assert(kA3RingAt + kWarps * kStages * kStage <= kA3TableAt, "ring overlaps the table");
+    static_assert(kEnd <= 232448, "more than 227 KiB of shared memory");
 };
 
 __device__ __forceinline__ uint32_t h2u(float lo, float hi) {
@@ -268,251 +314,505 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// table[e * 32 + lane] = (c[e & m], c[e >> BITS]): one copy per lane, so a
-// warp's lookups never collide in a bank.
-template <int BITS>
-__device__ void fill_pair_table(uint32_t* t, const float* cen) {
-    constexpr int N = PairTable<BITS>::kEntries, M = (1 << BITS) - 1;
-    for (int i = threadIdx.x; i < N * 32; i += blockDim.x) {
-        const int e = i >> 5;
-        t[i] = h2u(cen[e & M], cen[(e >> BITS) & M]);
-    }
-}
-
-// Pair p of a bit stream held in words w: bits [p*2*BITS, p*2*BITS + 2*BITS).
-template <int BITS>
-__device__ __forceinline__ uint32_t pair_at(const uint32_t* w, int p) {
-    constexpr int PB = 2 * BITS;
-    const int pos = p * PB, wi = pos / 32, sh = pos % 32;
-    uint32_t x;
-    if (sh + PB <= 32) x = w[wi] >> sh;
-    else x = __funnelshift_r(w[wi], w[wi + 1], sh);
-    return x & ((1u << PB) - 1);
-}
-
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+// Table lookup (the table is written once, before the first barrier).
+__device__ __forceinline__ uint32_t lds_tab(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+// Loads of ring data: volatile, so that they stay after the stage's wait.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) { return __uint_as_float(lds_u32(addr)); }
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
+    return v;
 }
 
-template <int BYTES>
-__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t* w) {
-    load_bytes<BYTES>(p, w);
+// Lookup address of pair q (stream order) of a packed field held in words w:
+// the pair's 2*BITS bits land in bits 8.. of `slot` (table base + column).
+template <int BITS>
+__device__ __forceinline__ uint32_t pair_addr(const uint32_t* w, int q, uint32_t slot) {
+    if constexpr (BITS == 4) {
+        return __byte_perm(w[q >> 2], slot, 0x7604u | ((uint32_t)(q & 3) << 4));
+    } else {
+        constexpr int PB = 2 * BITS;
+        const int o = q * PB, i = o >> 5, r = o & 31;
+        uint32_t x;
+        if (r + PB <= 32) x = r >= 8 ? (w[i] >> (r - 8)) : (w[i] << (8 - r));
+        else x = __funnelshift_r(w[i], w[i + 1], r - 8);
+        return (x & (((1u << PB) - 1u) << 8)) | slot;
+    }
 }
 
-// q rotation: q16[b][h][j] = fp16( (H (s . q) / sqrt(d))_j * scale * log2(e) )
-static __global__ void __launch_bounds__(128) k_attn_qrot(const __nv_bfloat16* __restrict__ q,
-                                                   __half* __restrict__ q16,
-                                                   const __grid_constant__ AttnParams P) {
+// The 32 dims 32t..32t+31 of a K row (KB words).
+template <int KB>
+__device__ __forceinline__ void load_kfield(uint32_t addr, uint32_t (&w)[KB]) {
+    if constexpr (KB == 4) {
+        const uint4 u = lds_v4(addr);
+        w[0] = u.x;
+        w[1] = u.y;
+        w[2] = u.z;
+        w[3] = u.w;
+    } else if constexpr (KB == 3) {
+        w[0] = lds_u32(addr);
+        w[1] = lds_u32(addr + 4);
+        w[2] = lds_u32(addr + 8);
+    } else {
+        const uint2 u = lds_v2(addr);
+        w[0] = u.x;
+        w[1] = u.y;
+    }
+}
+
+// The 16 dims 16g..16g+15 of a V row starting at `row`, as bits 0.. of f.
+template <int VB>
+__device__ __forceinline__ void load_vfield(uint32_t row, int g, uint32_t (&f)[2]) {
+    if constexpr (VB == 4) {
+        const uint2 u = lds_v2(row + 8 * g);
+        f[0] = u.x;
+        f[1] = u.y;
+    } else if constexpr (VB == 3) {
+        // 6 bytes at byte 6g: read the aligned 8 bytes holding them
+        const uint32_t a = row + ((6u * g) & ~3u);
+        const uint32_t w0 = lds_u32(a), w1 = lds_u32(a + 4);
+        const uint32_t sh = (g & 1) << 4;
+        f[0] = __funnelshift_r(w0, w1, sh);
+        f[1] = w1 >> sh;
+    } else {
+        f[0] = lds_u32(row + 4 * g);
+        f[1] = 0u;
+    }
+}
+
+// Rotated queries: y = H (s . q) * q_mul (q_mul = scale * log2(e) /
+// (sqrt(d) * s_k)), stored per (batch, head) as qexp = 2^e and fp16 high and
+// low parts of y / 2^e, with e chosen so that max |y| / 2^e is in
+// [2^13, 2^14).  q16 layout: [B * Hq][2 (high, low)][128].
+static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __restrict__ q,
+                                                        __half* __restrict__ q16,
+                                                        float* __restrict__ qexp,
+                                                        const __grid_constant__ AttnParams P) {
     __shared__ float v[128];
+    __shared__ float wmax[4];
     const int bh = blockIdx.x, j = threadIdx.x;
     const float x = __bfloat162float(q[(int64_t)bh * 128 + j]);
     v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
     fwht_smem<128>(v, 1);
-    q16[(int64_t)bh * 128 + j] = __float2half_rn(v[j] * (P.inv_sqrt_d * P.scale * kLog2e));
+    const float y = v[j] * P.q_mul;
+    float a = fabsf(y);
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    if ((j & 31) == 0) wmax[j >> 5] = a;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    int e = 0;
+    if (M > 0.f && M <= FLT_MAX) {
+        int ex = 0;
+        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
+        e = min(100, max(-100, ex - 14));
+    }
+    const float ys = ldexpf(y, -e);
+    const __half hi = __float2half_rn(ys);
+    const __half lo = __float2half_rn(ys - __half2float(hi));
+    q16[(int64_t)bh * 256 + j] = hi;
+    q16[(int64_t)bh * 256 + 128 + j] = lo;
+    if (j == 0) qexp[bh] = ldexpf(1.f, e);
 }
 
-template <int KB, int VB>
-struct A2Smem {
-    static constexpr int kKTable = PairTable<KB>::kEntries * 32 * 4;
-    static constexpr int kVTable = PairTable<VB>::kEntries * 32 * 4;
-    static constexpr int kVTile = 16 * 128 * 2;  // per warp
-    static constexpr int kBytes = kKTable + kVTable + kA2Warps * kVTile;
-};
+template <int KB, int VB, int NG>
+__global__ void __launch_bounds__(A3Shape<NG>::kThreads, 1)
+k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv,
+              tq_cache_view cache, int64_t ctx_len, int warp_len, int n_splits, int64_t n_items,
+              float* __restrict__ part, int* status, const __grid_constant__ AttnParams P) {
+    using L = A3Layout<KB, VB, NG>;
+    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<NG>::kThreads;
+    extern __shared__ __align__(16) unsigned char a3_smem[];
+    const uint32_t base = smem_addr(a3_smem);
+    if (base > kA3RingAt) {  // the layout below assumes dynamic memory starts lower
+        if (threadIdx.x == 0) report_timeout(status, kA3StatusLayout);
+        return;
+    }
+    auto gptr = [&](uint32_t abs) { return a3_smem + (abs - base); };
 
-template <int KB, int VB>
-__global__ void __launch_bounds__(kA2Threads)
-k_attn2_split(const __half* __restrict__ q16, int Hq, int Hkv, tq_cache_view cache,
-              int64_t ctx_len, int n_splits, int64_t n_items, float* __restrict__ part,
-              const __grid_constant__ AttnParams P) {
-    constexpr int D = 128;
-    constexpr int KRB = D * KB / 8, VRB = D * VB / 8;
-    constexpr int KCH = 4 * KB;  // bytes of a K row per lane (32 dims)
-    constexpr int VCH = 8 * VB;  // bytes of a V row per lane (64 dims)
-    extern __shared__ __align__(128) unsigned char a2_smem[];
-    uint32_t* ktab = reinterpret_cast<uint32_t*>(a2_smem);
-    uint32_t* vtab = reinterpret_cast<uint32_t*>(a2_smem + A2Smem<KB, VB>::kKTable);
-    unsigned char* vtiles = a2_smem + A2Smem<KB, VB>::kKTable + A2Smem<KB, VB>::kVTable;
-    fill_pair_table<KB>(ktab, P.kcen);
-    fill_pair_table<VB>(vtab, P.vcen);
+    // ---- pair tables (K columns, V columns) and the per-warp barriers
+    {
+        constexpr int NK = 1 << (2 * KB), NV = 1 << (2 * VB), MK = (1 << KB) - 1, MV = (1 << VB) - 1;
+        for (int i = threadIdx.x; i < L::kEntries * 64; i += T) {
+            const int e = i >> 6, s = i & 63;
+            uint32_t v = 0u;
+            if (s < 32) {
+                if (e < NK) v = h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK]);
+            } else if (e < NV) {
+                v = h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
+            }
+            *reinterpret_cast<uint32_t*>(gptr(kA3TableAt + 256u * e + 4u * s)) = v;
+        }
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gptr(L::kBarAt)) + warp * S;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + s, 32);
+        mbar_fence_init();
+    }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int G = Hq / Hkv;
-    const int n_parts = n_splits * kA2Warps;
-    const uint32_t* kt = ktab + lane;
-    const uint32_t* vt = vtab + lane;
-    unsigned char* vtile = vtiles + warp * A2Smem<KB, VB>::kVTile;
-    const uint32_t vtile_s = static_cast<uint32_t>(__cvta_generic_to_shared(vtile));
-    const float thr = P.sparse_thr;
-    const bool head_ok = g < G;
+    const uint32_t kslot = kA3TableAt + 4u * lane, vslot = kslot + 128u;
+    const uint32_t ring = kA3RingAt + (uint32_t)(warp * S * L::kStage);
+    float* merge = reinterpret_cast<float*>(gptr(L::kMergeAt));
+    const int64_t i_begin = n_items * blockIdx.x / gridDim.x;
+    const int64_t i_end = n_items * (blockIdx.x + 1) / gridDim.x;
+    const int nC = warp_len / kA3Chunk;
+    const int64_t seg = (int64_t)W * warp_len;
+    const int64_t wofs = (int64_t)warp * warp_len;
+    bool bad = false;  // warp-uniform: a wait gave up; compute is skipped from then on
 
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int split = (int)(item % n_splits);
-        const int64_t bh = item / n_splits;
-        const int gh = (int)(bh % Hkv);
-        const int64_t b = bh / Hkv;
-        const int64_t start = (int64_t)split * kA2Split + warp * kA2WarpPos;
-        const int64_t end = min(start + kA2WarpPos, ctx_len);
-        const int head = gh * G + g;  // query head of this lane's row (if g < G)
-        float* out = part + (((b * Hq + head) * n_parts) + (int64_t)split * kA2Warps + warp) * (D + 2);
-
-        float O[16][4];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) O[j][0] = O[j][1] = O[j][2] = O[j][3] = 0.f;
-        float m_run = -INFINITY, l_run = 0.f;
-
-        if (start < end) {
-            // q fragments (permuted dims): qa[kk] = q[32t+4kk .. +1], qb[kk] = q[32t+4kk+2 .. +3]
-            uint32_t qa[8], qb[8];
-            if (head_ok) {
-                const uint2* qp = reinterpret_cast<const uint2*>(q16 + (b * Hq + head) * D + 32 * t);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint2 u = __ldg(qp + kk);
-                    qa[kk] = u.x;
-                    qb[kk] = u.y;
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) qa[kk] = qb[kk] = 0u;
+    // Valid positions of chunk c of split `split` for this warp.
+    auto chunk_len = [&](int split, int c) {
+        const int64_t rem = ctx_len - ((int64_t)split * seg + wofs + (int64_t)c * kA3Chunk);
+        return rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
+    };
+    // Producer cursor: the next chunk to copy (item, chunk, split, (b, KV head),
+    // stage), kept S chunks ahead of the consumer.
+    int64_t p_item = i_begin, p_bh = i_begin / n_splits;
+    int p_c = 0, p_split = (int)(i_begin % n_splits), p_st = 0;
+    auto issue_next = [&]() {
+        if (p_item >= i_end || bad) return;
+        const int n = chunk_len(p_split, p_c);
+        uint64_t* bar = bars + p_st;
+        const uint32_t sb = ring + (uint32_t)(p_st * L::kStage);
+        if (n > 0) {
+            const int64_t row = p_bh * cache.cap + (int64_t)p_split * seg + wofs + (int64_t)p_c * kA3Chunk;
+            if (lane == 0) {
+                fence_async_smem();  // earlier generic reads of this stage come first
+                mbar_expect_tx(bar, (uint32_t)(n * (L::kKRow + L::kVRow)));
+                bulk_load(sb, cache.k_packed + row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
+                bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
             }
-            const int64_t row0 = (b * Hkv + gh) * cache.cap;
-            const uint8_t* kbase = cache.k_packed + row0 * KRB + KCH * t;
-            const float* knorm = cache.k_norm + row0;
-            const float* vnorm = cache.v_norm + row0;
-
-            for (int64_t t0 = start; t0 < end; t0 += 16) {
-                // ---- scores for 16 positions (two n-tiles of 8)
-                float sc[2][2];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int64_t pk = min(t0 + 8 * nt + g, end - 1);
-                    uint32_t kw[KB];
-                    load_words<KCH>(kbase + pk * KRB, kw);
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t b0 = kt[pair_at<KB>(kw, 2 * kk) * 32];
-                        const uint32_t b1 = kt[pair_at<KB>(kw, 2 * kk + 1) * 32];
-                        mma16816(acc, qa[kk], 0u, qb[kk], 0u, b0, b1);
-                    }
-                    sc[nt][0] = acc[0];
-                    sc[nt][1] = acc[1];
-                }
-                // positions of this lane's scores: t0 + 8nt + 2t + e
-                float nk[2][2], nv[2][2];
-                bool ok[2][2];
-                float tmax = -INFINITY, nvmax = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int64_t ps = t0 + 8 * nt + 2 * t + e;
-                        ok[nt][e] = ps < end;
-                        const int64_t pc = ok[nt][e] ? ps : end - 1;
-                        nk[nt][e] = __ldg(knorm + pc);
-                        nv[nt][e] = __ldg(vnorm + pc);
-                        sc[nt][e] = ok[nt][e] ? sc[nt][e] * nk[nt][e] : -INFINITY;
-                        tmax = fmaxf(tmax, sc[nt][e]);
-                        nvmax = fmaxf(nvmax, nv[nt][e]);
-                    }
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 2));
-                // Rescale when this tile's max runs ahead of the running max by
-                // more than kLazy, or at all when large V norms could push
-                // p * n_v past the fp16 range.
-                const float lazy = nvmax > 200.f ? 0.f : kLazy;
-                const bool need = head_ok && tmax > m_run + lazy;
-                if (__any_sync(0xFFFFFFFFu, need)) {
-                    const float m_new = fmaxf(m_run, tmax);
-                    const float alpha = fast_exp2(m_run - m_new);  // m_run = -inf -> 0
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        O[j][0] *= alpha;
-                        O[j][1] *= alpha;
-                    }
-                    l_run *= alpha;
-                    m_run = m_new;
-                }
-                float p[2][2];
-                float pmax = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        p[nt][e] = (head_ok && ok[nt][e]) ? fast_exp2(sc[nt][e] - m_run) : 0.f;
-                        l_run += p[nt][e];
-                        pmax = fmaxf(pmax, p[nt][e]);
-                    }
-                // sparse-V: skip the tile's V rows when no head of the group
-                // reaches the threshold anywhere in the tile
-                if (!__any_sync(0xFFFFFFFFu, pmax >= thr)) continue;
-                const uint32_t pa0 = h2u(p[0][0] * nv[0][0], p[0][1] * nv[0][1]);
-                const uint32_t pa2 = h2u(p[1][0] * nv[1][0], p[1][1] * nv[1][1]);
-
-                // ---- V tile: lane -> position (lane & 15), dims 64*(lane >> 4) .. +63
-                {
-                    const int vp = lane & 15, hh = lane >> 4;
-                    const int64_t pv = min(t0 + vp, end - 1);
-                    uint32_t vw[VCH / 4 + 1];
-                    load_words<VCH>(cache.v_packed + (row0 + pv) * VRB + VCH * hh, vw);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 dims
-                        uint4 q4;
-                        q4.x = vt[pair_at<VB>(vw, 4 * c + 0) * 32];
-                        q4.y = vt[pair_at<VB>(vw, 4 * c + 1) * 32];
-                        q4.z = vt[pair_at<VB>(vw, 4 * c + 2) * 32];
-                        q4.w = vt[pair_at<VB>(vw, 4 * c + 3) * 32];
-                        const int chunk = 8 * hh + c;
-                        *reinterpret_cast<uint4*>(vtile + vp * 256 + ((chunk ^ (vp & 7)) << 4)) = q4;
-                    }
-                }
-                __syncwarp();
-                // ---- O += P V over 16 n-tiles of 8 dims
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int i = lane;
-                    const int pos = ((i >> 3) & 1) * 8 + (i & 7);
-                    const int chunk = 2 * j + (i >> 4);
-                    uint32_t r[4];
-                    ldsm_x4_trans(r, vtile_s + pos * 256 + ((chunk ^ (pos & 7)) << 4));
-                    mma16816(O[2 * j], pa0, 0u, pa2, 0u, r[0], r[1]);
-                    mma16816(O[2 * j + 1], pa0, 0u, pa2, 0u, r[2], r[3]);
-                }
-                __syncwarp();
+            if (lane < n) {
+                cp_async4(sb + L::kKnOff + 4u * lane, cache.k_norm + row + lane);
+                cp_async4(sb + L::kVnOff + 4u * lane, cache.v_norm + row + lane);
+            }
+            cp_async_arrive(bar);
+        } else {
+            mbar_arrive(bar);
+        }
+        if (++p_c == nC) {
+            p_c = 0;
+            ++p_item;
+            if (++p_split == n_splits) {
+                p_split = 0;
+                ++p_bh;
             }
         }
-        l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
-        l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
-        if (head_ok) {
+        if (++p_st == S) p_st = 0;
+    };
+    for (int i = 0; i < S; ++i) issue_next();
+
+    float O[NG][8][4];
+    float m_run[NG], l_run[NG], qx[NG];
+    uint32_t qb[NG][8][2];
+    bool hok[NG];
+    int vexp = 0;  // the V accumulators are in units of 2^vexp
+    float vlim = 128.f, vsc = 1.f;
+    int64_t cur_bh = -1;
+    const float thr = P.sparse_thr;
+    const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
+    const bool odd = (g & 1) != 0;
+
+    int split = (int)(i_begin % n_splits), cst = 0;
+    uint32_t cph = 0;
+    int64_t bh = i_begin / n_splits;
+    for (int64_t item = i_begin; item < i_end; ++item) {
+        {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<float2*>(out + 8 * j + 2 * t) = make_float2(O[j][0], O[j][1]);
-            if (t == 0) {
-                out[D] = m_run;
-                out[D + 1] = l_run;
+            for (int hg = 0; hg < NG; ++hg) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) O[hg][mt][0] = O[hg][mt][1] = O[hg][mt][2] = O[hg][mt][3] = 0.f;
+                m_run[hg] = -INFINITY;
+                l_run[hg] = 0.f;
             }
+            vexp = 0;
+            vlim = 128.f;
+            vsc = 1.f;
+            if (bh != cur_bh) {
+                cur_bh = bh;
+                const int64_t b = bh / Hkv;
+                const int gh = (int)(bh % Hkv);
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg) {
+                    const int hc = 4 * hg + (g >> 1);  // head of this lane's B column
+                    if (hc < G) {
+                        const uint4* qp = reinterpret_cast<const uint4*>(
+                            q16 + ((b * Hq + gh * G + hc) * 2 + (g & 1)) * 128 + 32 * t);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 u = __ldg(qp + i);
+                            qb[hg][2 * i][0] = u.x;
+                            qb[hg][2 * i][1] = u.y;
+                            qb[hg][2 * i + 1][0] = u.z;
+                            qb[hg][2 * i + 1][1] = u.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) qb[hg][kk][0] = qb[hg][kk][1] = 0u;
+                    }
+                    hok[hg] = 4 * hg + t < G;
+                    qx[hg] = hok[hg] ? __ldg(qexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
+                }
+            }
+        }
+
+        for (int c = 0; c < nC; ++c) {
+            if (!bad) {
+                const bool ok = mbar_wait(bars + cst, cph);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    if (lane == 0) report_timeout(status, kA3StatusWait);
+                    bad = true;
+                }
+            }
+            const int n = chunk_len(split, c);
+            if (n > 0 && !bad) {
+                const uint32_t sb = ring + (uint32_t)(cst * L::kStage);
+                const uint32_t sK = sb, sV = sb + L::kVOff;
+                // ---- scores of the chunk's 32 positions
+                float sacc[2][NG][4];
+                uint32_t kw[2][2][KB];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg) sacc[u][hg][0] = sacc[u][hg][1] = sacc[u][hg][2] = sacc[u][hg][3] = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[u][h]);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t a0 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk, kslot));
+                        const uint32_t a2 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk + 1, kslot));
+                        const uint32_t a1 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk, kslot));
+                        const uint32_t a3 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk + 1, kslot));
+#pragma unroll
+                        for (int hg = 0; hg < NG; ++hg)
+                            mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
+                    }
+                }
+                // lane (g, t): positions 16u + 8h + g of head 4hg + t
+                float sc[NG][2][2], vn[2][2];
+                bool ok[2][2];
+                float nvl = 0.f;
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = 16 * u + 8 * h + g;
+                        ok[u][h] = r < n;
+                        const float kn = lds_f32(sb + L::kKnOff + 4u * r);
+                        vn[u][h] = lds_f32(sb + L::kVnOff + 4u * r);
+                        if (ok[u][h]) nvl = fmaxf(nvl, vn[u][h]);
+#pragma unroll
+                        for (int hg = 0; hg < NG; ++hg)
+                            sc[hg][u][h] = ok[u][h] ? (sacc[u][hg][2 * h] + sacc[u][hg][2 * h + 1]) * kn * qx[hg]
+                                                    : -INFINITY;
+                    }
+                bool need = false;
+                float tmax[NG];
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg) {
+                    float mx = fmaxf(fmaxf(sc[hg][0][0], sc[hg][0][1]), fmaxf(sc[hg][1][0], sc[hg][1][1]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+                    tmax[hg] = mx;
+                    need = need || mx > m_run[hg] + kLazy;
+                }
+                if (__any_sync(0xFFFFFFFFu, need)) {
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg) {
+                        const float mn = fmaxf(m_run[hg], tmax[hg]);
+                        const float al = mn == -INFINITY ? 1.f : fast_exp2(m_run[hg] - mn);
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            O[hg][mt][0] *= al;
+                            O[hg][mt][1] *= al;
+                            O[hg][mt][2] *= al;
+                            O[hg][mt][3] *= al;
+                        }
+                        l_run[hg] *= al;
+                        m_run[hg] = mn;
+                    }
+                }
+                // V norms beyond 2^(vexp+7) would take p * n_v out of the fp16 range
+                if (__any_sync(0xFFFFFFFFu, nvl > vlim)) {
+                    float w = nvl;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+                    const int e2 = (int)((__float_as_uint(w) >> 23) & 0xFFu) - 126;  // w < 2^e2
+                    const int en = max(vexp, e2 - 7);
+                    const float f = ldexpf(1.f, vexp - en);
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            O[hg][mt][0] *= f;
+                            O[hg][mt][1] *= f;
+                            O[hg][mt][2] *= f;
+                            O[hg][mt][3] *= f;
+                        }
+                    vexp = en;
+                    vlim = ldexpf(1.f, en + 7);
+                    vsc = ldexpf(1.f, -en);
+                }
+                float p[NG][2][2];
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            p[hg][u][h] = fast_exp2(sc[hg][u][h] - m_run[hg]);
+                            l_run[hg] += p[hg][u][h];
+                        }
+
+                // ---- O^T += V^T P, per sub-tile
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    bool keep = false;
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg)
+                        keep = keep || (hok[hg] && fmaxf(p[hg][u][0], p[hg][u][1]) >= thr);
+                    if (!__any_sync(0xFFFFFFFFu, keep)) continue;  // sparse V: every head below thr
+                    uint32_t pb0[NG], pb1[NG];
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg) {
+                        const float x0 = ok[u][0] ? p[hg][u][0] * (vn[u][0] * vsc) : 0.f;
+                        const float x1 = ok[u][1] ? p[hg][u][1] * (vn[u][1] * vsc) : 0.f;
+                        const __half2 hh = __floats2half2_rn(x0, x1);
+                        const float2 hf = __half22float2(hh);
+                        const __half2 hl = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                        const uint32_t uH = *reinterpret_cast<const uint32_t*>(&hh);
+                        const uint32_t uL = *reinterpret_cast<const uint32_t*>(&hl);
+                        const uint32_t hA = __shfl_sync(0xFFFFFFFFu, uH, srcA);
+                        const uint32_t hB = __shfl_sync(0xFFFFFFFFu, uH, srcB);
+                        const uint32_t lA = __shfl_sync(0xFFFFFFFFu, uL, srcA);
+                        const uint32_t lB = __shfl_sync(0xFFFFFFFFu, uL, srcB);
+                        const uint32_t sA = odd ? lA : hA, sB = odd ? lB : hB;
+                        pb0[hg] = __byte_perm(sA, sB, 0x5410);  // positions 2t, 2t + 1
+                        pb1[hg] = __byte_perm(sA, sB, 0x7632);  // positions 2t + 8, 2t + 9
+                    }
+                    uint32_t fA[2], fB[2], fC[2], fD[2];
+                    const uint32_t r0 = sV + (uint32_t)((16 * u + 2 * t) * L::kVRow);
+                    load_vfield<VB>(r0, g, fA);
+                    load_vfield<VB>(r0 + L::kVRow, g, fB);
+                    load_vfield<VB>(r0 + 8 * L::kVRow, g, fC);
+                    load_vfield<VB>(r0 + 9 * L::kVRow, g, fD);
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const uint32_t uA = lds_tab(pair_addr<VB>(fA, mt, vslot));
+                        const uint32_t uB = lds_tab(pair_addr<VB>(fB, mt, vslot));
+                        const uint32_t uC = lds_tab(pair_addr<VB>(fC, mt, vslot));
+                        const uint32_t uD = lds_tab(pair_addr<VB>(fD, mt, vslot));
+                        const uint32_t a0 = __byte_perm(uA, uB, 0x5410), a1 = __byte_perm(uA, uB, 0x7632);
+                        const uint32_t a2 = __byte_perm(uC, uD, 0x5410), a3 = __byte_perm(uC, uD, 0x7632);
+#pragma unroll
+                        for (int hg = 0; hg < NG; ++hg) mma16816(O[hg][mt], a0, a1, a2, a3, pb0[hg], pb1[hg]);
+                    }
+                }
+            }
+            __syncwarp();
+            issue_next();
+            if (++cst == S) {
+                cst = 0;
+                cph ^= 1u;
+            }
+        }  // chunks
+
+        // ---- end of an item: merge the warps' partials, one per query head
+        {
+            const float mul = ldexpf(P.out_mul, vexp);
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) {
+                float l = l_run[hg];
+                l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+                l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+                l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+                if (hok[hg]) {
+                    float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float4 v;
+                        v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
+                        v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
+                        v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
+                        v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
+                        *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
+                    }
+                    if (g == 0) {
+                        row[128] = m_run[hg];
+                        row[129] = l;
+                    }
+                }
+            }
+            __syncthreads();
+            const int64_t b = bh / Hkv;
+            const int gh = (int)(bh % Hkv);
+            for (int i = threadIdx.x; i < G * 128; i += T) {
+                const int h = i >> 7, dim = i & 127;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < W; ++w)
+                    M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
+                float Ls = 0.f, A = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    const float* row = merge + (w * L::kHeads + h) * kA3MergeStride;
+                    const float f = row[128] == -INFINITY ? 0.f : fast_exp2(row[128] - M);
+                    Ls = fmaf(f, row[129], Ls);
+                    A = fmaf(f, row[dim], A);
+                }
+                float* o = part + ((b * Hq + gh * G + h) * n_splits + split) * 130;
+                o[dim] = A;
+                if (dim == 0) {
+                    o[128] = M;
+                    o[129] = Ls;
+                }
+            }
+            __syncthreads();
+        }
+        if (++split == n_splits) {
+            split = 0;
+            ++bh;
         }
     }
 }
 
 // Merge the partials of one (batch, query head) (m in log2 units), normalise
-// and rotate back.
-static __global__ void __launch_bounds__(128) k_attn2_combine(const float* __restrict__ part, int n_parts,
-                                                       float* __restrict__ out,
-                                                       const __grid_constant__ AttnParams P) {
+// and rotate back: out = s . (H o) / sqrt(d).
+static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_parts,
+                                                              float* __restrict__ out,
+                                                              const __grid_constant__ AttnParams P) {
     __shared__ float o[128];
     const int bh = blockIdx.x, j = threadIdx.x;
     const float* base = part + (int64_t)bh * n_parts * 130;
@@ -530,34 +830,47 @@ static __global__ void __launch_bounds__(128) k_attn2_combine(const float* __res
     out[(int64_t)bh * 128 + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }
 
+template <int KB, int VB, int NG>
+cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
+                               const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
+                               int64_t items, float* part, const AttnParams& P, cudaStream_t s) {
+    using L = A3Layout<KB, VB, NG>;
+    auto fn = k_attn3_split<KB, VB, NG>;
+    // The kernel addresses shared memory from window address 0, so it asks
+    // for kEnd bytes (the dynamic block starts at or below kA3RingAt).
+    static int attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kEnd);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
+    }
+    int64_t grid = num_sms();
+    if (grid > items) grid = items;
+    fn<<<(unsigned)grid, A3Shape<NG>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len, geo.warp_len,
+                                                  geo.n_splits, items, part, status_word(), P);
+    return cudaGetLastError();
+}
+
 template <int KB, int VB>
-cudaError_t attn2_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
+cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
                          int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
                          const AttnParams& P, cudaStream_t s) {
     __half* q16 = static_cast<__half*>(ws);
-    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + attn2_q16_bytes(B, Hq));
-    k_attn_qrot<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, P);
+    float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * Hq * 512);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + attn3_prefix_bytes(B, Hq));
+    k_attn3_q<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto fn = k_attn2_split<KB, VB>;
-    constexpr int smem = A2Smem<KB, VB>::kBytes;
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-    }
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)fn, kA2Threads, smem) != cudaSuccess ||
-        per_sm < 1) {
-        cudaGetLastError();
-        per_sm = 1;
-    }
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
-    int64_t grid = (int64_t)num_sms() * per_sm;
-    if (grid > items) grid = items;
-    fn<<<(unsigned)grid, kA2Threads, smem, s>>>(q16, Hq, Hkv, cache, ctx_len, geo.n_splits, items, part, P);
-    e = cudaGetLastError();
+    if (Hq / Hkv <= 4)
+        e = attn3_split_launch<KB, VB, 1>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, part, P, s);
+    else
+        e = attn3_split_launch<KB, VB, 2>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, part, P, s);
     if (e != cudaSuccess) return e;
-    k_attn2_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits * kA2Warps, out, P);
+    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, out, P);
     return cudaGetLastError();
 }
 
@@ -583,9 +896,9 @@ cudaError_t attn_vb(int vb, const void* q, int B, int Hq, int Hkv, const tq_cach
                     cudaStream_t s) {
     if constexpr (D == 128) {
         switch (vb) {
-            case 2: return attn2_launch<KB, 2>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-            case 3: return attn2_launch<KB, 3>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-            default: return attn2_launch<KB, 4>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
+            case 2: return attn3_launch<KB, 2>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
+            case 3: return attn3_launch<KB, 3>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
+            default: return attn3_launch<KB, 4>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
         }
     }
     switch (vb) {

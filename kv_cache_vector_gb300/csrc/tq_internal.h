@@ -31,6 +31,13 @@ struct AttnParams {
     float inv_sqrt_d;
     float scale;       // softmax scale applied to q . k
     float sparse_thr;  // 0 = dense
+    // d = 128 tensor-core kernels: fp16 values of c * s_k and c * s_v (exact
+    // in fp16), the query multiplier scale * log2(e) / (sqrt(d) * s_k) and the
+    // output multiplier 1 / s_v.
+    float kcen_h[16];
+    float vcen_h[16];
+    float q_mul;
+    float out_mul;
 };
 
 // Host plan (the public tq_plan).
@@ -40,7 +47,14 @@ struct Plan {
     int8_t signs[kMaxD];
     double c64[5][16], b64[5][16];  // index by bits (1..4)
     float c32[5][16], b32[5][16];
+    // Per width: a scale s in [1, 2) that puts every c32 * s close to an fp16
+    // value, and those fp16 values (the fp16 tensor-core attention).
+    float hscale[5];
+    float hcen[5][16];
 };
+
+void fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, float sparse_thr,
+                      AttnParams& A);
 
 // Bucketing lookup table geometry (encode): cell g covers the normalised
 // coordinate w with rint(w * kLutScale) = g - kLutCenter, i.e. the closed
@@ -64,16 +78,24 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
                             const tq_cache_view& cache, int64_t pos, const RowParams& PK,
                             const RowParams& PV, cudaStream_t s);
 
+// Warps per CTA of the d = 128 attention kernel, by GQA group size G.
+constexpr int kAttn3WarpsG4 = 12;  // G <= 4
+constexpr int kAttn3WarpsG8 = 8;   // 4 < G <= 8
+inline int attn3_warps(int G) { return G <= 4 ? kAttn3WarpsG4 : kAttn3WarpsG8; }
+
 struct AttnGeometry {
     int n_splits;
     int split_len;    // positions per split
-    int parts;        // partials written per split (one per warp in the d = 128 kernel)
+    int parts;        // partials written per split
+    int warp_len;     // d = 128: positions per warp and split
     bool q16;         // the workspace starts with the rotated fp16 queries
 };
-AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int num_sms, int d);
+AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
-inline size_t attn2_q16_bytes(int B, int Hq) {  // rotated queries, rounded to 256 B
-    return ((size_t)B * Hq * 128 * 2 + 255) / 256 * 256;
+// d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
+// their power-of-two scales (4 bytes per head), rounded up to 256 bytes.
+inline size_t attn3_prefix_bytes(int B, int Hq) {
+    return ((size_t)B * Hq * (512 + 4) + 255) / 256 * 256;
 }
 template <int D, int KB>
 cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,

@@ -54,31 +54,54 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
     return (unsigned)(want < 1 ? 1 : want);
 }
 
-// Split-K geometry of the decode attention.  d = 128 (tensor-core kernel):
-// splits of 512 positions, four partials each (one per warp).  Otherwise the
-// longest split (<= 512 positions) that still gives two CTAs per SM.
-AttnGeometry attn_geometry(int B, int Hkv, int64_t ctx_len, int sms, int d) {
+// Split-K geometry of the decode attention.  d = 128 (tensor-core kernel,
+// one CTA of attn3_warps(G) warps per SM): the longest per-warp range (256 down
+// to 32 positions) whose work items fill the last wave of CTAs to at least
+// 90%, else the one that fills it best.  Otherwise the longest split
+// (<= 512 positions) that still gives two CTAs per SM.
+AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d) {
     AttnGeometry g;
+    const int64_t pairs = (int64_t)B * Hkv;
     if (d == 128) {
-        g.split_len = 512;
-        g.n_splits = (int)((ctx_len + 511) / 512);
-        g.parts = 4;
+        const int64_t cap = sms > 0 ? sms : 1;
+        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1);
+        int best = 256;
+        double best_eff = -1.0;
+        for (int wl = 256; wl >= 32; wl /= 2) {
+            const int64_t seg = (int64_t)W * wl;
+            const int64_t items = pairs * ((ctx_len + seg - 1) / seg);
+            const int64_t grid = items < cap ? (items > 0 ? items : 1) : cap;
+            const int64_t rounds = (items + grid - 1) / grid;
+            const double eff = rounds > 0 ? (double)items / (double)(rounds * grid) : 1.0;
+            if (eff >= 0.9) {
+                best = wl;
+                break;
+            }
+            if (eff > best_eff + 1e-9) {
+                best_eff = eff;
+                best = wl;
+            }
+        }
+        g.warp_len = best;
+        g.split_len = W * best;
+        g.n_splits = (int)((ctx_len + g.split_len - 1) / g.split_len);
+        g.parts = 1;
         g.q16 = true;
         return g;
     }
     int split = 512;
-    const int64_t pairs = (int64_t)B * Hkv;
     const int64_t want = 2LL * (sms > 0 ? sms : 1);
     while (split > 64 && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
     g.split_len = split;
     g.n_splits = (int)((ctx_len + split - 1) / split);
     g.parts = 1;
+    g.warp_len = 0;
     g.q16 = false;
     return g;
 }
 
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g) {
-    return (g.q16 ? attn2_q16_bytes(B, Hq) : 0) +
+    return (g.q16 ? attn3_prefix_bytes(B, Hq) : 0) +
            sizeof(float) * (size_t)B * Hq * g.n_splits * g.parts * (d + 2);
 }
 

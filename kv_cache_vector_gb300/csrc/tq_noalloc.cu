@@ -82,7 +82,7 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, 
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    const tq::AttnGeometry g = tq::attn_geometry(B, Hkv, ctx_len, tq::num_sms(), P->d);
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d);
     if (tq::attn_workspace_bytes(B, Hq, P->d, g) > kScratchBytes) return TQ_ERR_WORKSPACE;
     void* ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
@@ -91,14 +91,7 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, 
         return TQ_ERR_CUDA;
     }
     tq::AttnParams A;
-    for (int i = 0; i < tq::kMaxD; ++i) A.sgn[i] = (i < P->d && P->signs[i] < 0) ? 0x80000000u : 0u;
-    for (int i = 0; i < 16; ++i) {
-        A.kcen[i] = P->c32[k_bits][i];
-        A.vcen[i] = P->c32[v_bits][i];
-    }
-    A.inv_sqrt_d = (float)(1.0 / std::sqrt((double)P->d));
-    A.scale = scale;
-    A.sparse_thr = sparse_v_threshold;
+    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (P->d) {
         case 32: e = launch_d<32>(k_bits, v_bits, q, B, Hq, Hkv, cache, ctx_len, out, ws, g, A, st); break;
