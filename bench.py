@@ -316,32 +316,65 @@ def parity_sample(W, S):
     return res
 
 
-def e2e_run(W, S, steps):
-    """The same step with host buffers: inputs copied from pinned host memory
-    and every result copied back, inside the timed region."""
+def e2e_run(W, S, steps, n_chunks=32):
+    """The same step with host buffers: every input copied from pinned host
+    memory and every result copied back, inside the timed region.  The codec
+    rows go through in n_chunks chunks on three streams, so that the
+    host->device copy of chunk i+1 and the device->host copy of chunk i-1
+    overlap the kernels of chunk i; the streams join at the end of every
+    step."""
     import torch
+    from kv_cache_vector_gb300 import abi
+
     def pinned_copy(t):
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         h.copy_(t)
         return h
 
     hK, hV, hq, hkn, hvn = (pinned_copy(t) for t in (S.K, S.V, S.q, S.k_new, S.v_new))
-    outs = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            for n, t in (("pk", S.pk), ("pv", S.pv), ("nk", S.nk), ("nv", S.nv), ("dk", S.dk),
-                         ("dv", S.dv), ("out", S.out))}
+    rows_out = (("pk", S.pk), ("pv", S.pv), ("nk", S.nk), ("nv", S.nv), ("dk", S.dk), ("dv", S.dv))
+    outs = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in rows_out}
+    outs["out"] = torch.empty(S.out.shape, dtype=S.out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in (hK, hV, hq, hkn, hvn))
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    cs = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    bounds = [(W.rows * i // n_chunks, W.rows * (i + 1) // n_chunks) for i in range(n_chunks)]
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks + 1)]
+    ev_done = [torch.cuda.Event() for _ in range(n_chunks + 1)]
 
     def one():
-        S.K.copy_(hK, non_blocking=True)
-        S.V.copy_(hV, non_blocking=True)
-        S.q.copy_(hq, non_blocking=True)
-        S.k_new.copy_(hkn, non_blocking=True)
-        S.v_new.copy_(hvn, non_blocking=True)
-        run_step(W, S)
-        for n, src in (("pk", S.pk), ("pv", S.pv), ("nk", S.nk), ("nv", S.nv), ("dk", S.dk),
-                       ("dv", S.dv), ("out", S.out)):
-            outs[n].copy_(src, non_blocking=True)
+        up.wait_stream(cs)
+        with torch.cuda.stream(up):
+            S.q.copy_(hq, non_blocking=True)
+            S.k_new.copy_(hkn, non_blocking=True)
+            S.v_new.copy_(hvn, non_blocking=True)
+            ev_in[n_chunks].record(up)
+        for i, (a, b) in enumerate(bounds):
+            with torch.cuda.stream(up):
+                S.K[a:b].copy_(hK[a:b], non_blocking=True)
+                S.V[a:b].copy_(hV[a:b], non_blocking=True)
+                ev_in[i].record(up)
+            cs.wait_event(ev_in[i])
+            abi.tq_encode(S.plan, W.kb, S.K[a:b], S.pk[a:b], S.nk[a:b])
+            abi.tq_encode(S.plan, W.vb, S.V[a:b], S.pv[a:b], S.nv[a:b])
+            abi.tq_decode(S.plan, W.kb, S.pk[a:b], S.nk[a:b], out=S.dk[a:b])
+            abi.tq_decode(S.plan, W.vb, S.pv[a:b], S.nv[a:b], out=S.dv[a:b])
+            ev_done[i].record(cs)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[i])
+                for n, t in rows_out:
+                    outs[n][a:b].copy_(t[a:b], non_blocking=True)
+        cs.wait_event(ev_in[n_chunks])
+        abi.tq_append(S.plan, S.cache, S.k_new, S.v_new, W.ctx - 1)
+        abi.tq_attn_decode(S.plan, S.q, S.cache, W.ctx, 1.0 / math.sqrt(D), 0.0, out=S.out,
+                           workspace=S.ws)
+        ev_done[n_chunks].record(cs)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[n_chunks])
+            outs["out"].copy_(S.out, non_blocking=True)
+        cs.wait_stream(up)
+        cs.wait_stream(down)
 
     one()
     torch.cuda.synchronize()

@@ -83,9 +83,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// 4-byte asynchronous copy from global memory to shared address `dst`.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+// 4-byte asynchronous copy from global memory to shared address `dst`; the
+// first `src_bytes` (0 or 4) bytes come from `src`, the rest are zero-filled.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
 }
 
 // Arrive on `bar` once this thread's earlier cp.async copies have landed;

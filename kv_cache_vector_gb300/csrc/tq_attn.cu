@@ -10,6 +10,7 @@
 // un-rotates.  "CITATIONS", Sparse V dequant: a V row is skipped when every
 // head's exp(sigma - m) is below the threshold; it still counts in l.
 #include <cfloat>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 
@@ -445,6 +446,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
               float* __restrict__ part, int* status, const __grid_constant__ AttnParams P) {
     using L = A3Layout<KB, VB, NG>;
     constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<NG>::kThreads;
+    constexpr uint32_t kAll = 0xFFFFFFFFu;
     extern __shared__ __align__(16) unsigned char a3_smem[];
     const uint32_t base = smem_addr(a3_smem);
     if (base > kA3RingAt) {  // the layout below assumes dynamic memory starts lower
@@ -487,32 +489,30 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     const int64_t wofs = (int64_t)warp * warp_len;
     bool bad = false;  // warp-uniform: a wait gave up; compute is skipped from then on
 
-    // Valid positions of chunk c of split `split` for this warp.
-    auto chunk_len = [&](int split, int c) {
-        const int64_t rem = ctx_len - ((int64_t)split * seg + wofs + (int64_t)c * kA3Chunk);
-        return rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
-    };
-    // Producer cursor: the next chunk to copy (item, chunk, split, (b, KV head),
-    // stage), kept S chunks ahead of the consumer.
+    // Producer cursor: the next chunk to copy, kept S chunks ahead of the
+    // consumer; position and cache row advance by additions.
     int64_t p_item = i_begin, p_bh = i_begin / n_splits;
     int p_c = 0, p_split = (int)(i_begin % n_splits), p_st = 0;
+    int64_t p_pos = (int64_t)p_split * seg + wofs;
+    int64_t p_row = p_bh * cache.cap + p_pos;
     auto issue_next = [&]() {
         if (p_item >= i_end || bad) return;
-        const int n = chunk_len(p_split, p_c);
+        const int64_t rem = ctx_len - p_pos;
+        const int n = rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
         uint64_t* bar = bars + p_st;
         const uint32_t sb = ring + (uint32_t)(p_st * L::kStage);
         if (n > 0) {
-            const int64_t row = p_bh * cache.cap + (int64_t)p_split * seg + wofs + (int64_t)p_c * kA3Chunk;
             if (lane == 0) {
                 fence_async_smem();  // earlier generic reads of this stage come first
                 mbar_expect_tx(bar, (uint32_t)(n * (L::kKRow + L::kVRow)));
-                bulk_load(sb, cache.k_packed + row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
-                bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
+                bulk_load(sb, cache.k_packed + p_row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
+                bulk_load(sb + L::kVOff, cache.v_packed + p_row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
             }
-            if (lane < n) {
-                cp_async4(sb + L::kKnOff + 4u * lane, cache.k_norm + row + lane);
-                cp_async4(sb + L::kVnOff + 4u * lane, cache.v_norm + row + lane);
-            }
+            // lanes past the end copy nothing (source size 0) from a valid row
+            const int64_t r = p_row + (lane < n ? lane : n - 1);
+            const uint32_t sz = lane < n ? 4u : 0u;
+            cp_async4(sb + L::kKnOff + 4u * lane, cache.k_norm + r, sz);
+            cp_async4(sb + L::kVnOff + 4u * lane, cache.v_norm + r, sz);
             cp_async_arrive(bar);
         } else {
             mbar_arrive(bar);
@@ -524,6 +524,11 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 p_split = 0;
                 ++p_bh;
             }
+            p_pos = (int64_t)p_split * seg + wofs;
+            p_row = p_bh * cache.cap + p_pos;
+        } else {
+            p_pos += kA3Chunk;
+            p_row += kA3Chunk;
         }
         if (++p_st == S) p_st = 0;
     };
@@ -537,209 +542,223 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     float vlim = 128.f, vsc = 1.f;
     int64_t cur_bh = -1;
     const float thr = P.sparse_thr;
+    const bool sparse = thr > 0.f;
     const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
     const bool odd = (g & 1) != 0;
+
+    // One chunk of 32 positions at shared address sb; FULL: all 32 valid.
+    auto chunk = [&](uint32_t sb, int n, auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const uint32_t sK = sb, sV = sb + L::kVOff;
+        // ---- scores
+        float sacc[2][NG][4];
+        uint32_t kw[2][2][KB];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) sacc[u][hg][0] = sacc[u][hg][1] = sacc[u][hg][2] = sacc[u][hg][3] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[u][h]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t a0 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk, kslot));
+                const uint32_t a2 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk + 1, kslot));
+                const uint32_t a1 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk, kslot));
+                const uint32_t a3 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk + 1, kslot));
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg)
+                    mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
+            }
+        }
+        // lane (g, t): positions 16u + 8h + g of head 4hg + t
+        float sc[NG][2][2], vn[2][2];
+        bool ok[2][2];
+        float nvl = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = 16 * u + 8 * h + g;
+                ok[u][h] = FULL || r < n;
+                const float kn = lds_f32(sb + L::kKnOff + 4u * r);
+                vn[u][h] = lds_f32(sb + L::kVnOff + 4u * r);
+                if (FULL) nvl = fmaxf(nvl, vn[u][h]);
+                else if (ok[u][h]) nvl = fmaxf(nvl, vn[u][h]);
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg) {
+                    const float v = (sacc[u][hg][2 * h] + sacc[u][hg][2 * h + 1]) * (kn * qx[hg]);
+                    sc[hg][u][h] = ok[u][h] ? v : -INFINITY;
+                }
+            }
+        bool need = false;
+        float tmax[NG];
+#pragma unroll
+        for (int hg = 0; hg < NG; ++hg) {
+            float mx = fmaxf(fmaxf(sc[hg][0][0], sc[hg][0][1]), fmaxf(sc[hg][1][0], sc[hg][1][1]));
+            mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 16));
+            tmax[hg] = mx;
+            need = need || mx > m_run[hg] + kLazy;
+        }
+        // rare: the running maximum moves, or a V norm would take p * n_v
+        // (p <= 2^kLazy) past the fp16 range in units of 2^vexp
+        if (__any_sync(kAll, need || nvl > vlim)) {
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) {
+                const float mn = fmaxf(m_run[hg], tmax[hg]);
+                const float al = mn == -INFINITY ? 1.f : fast_exp2(m_run[hg] - mn);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    O[hg][mt][0] *= al;
+                    O[hg][mt][1] *= al;
+                    O[hg][mt][2] *= al;
+                    O[hg][mt][3] *= al;
+                }
+                l_run[hg] *= al;
+                m_run[hg] = mn;
+            }
+            float w = nvl;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(kAll, w, o));
+            if (w > vlim) {
+                const int e2 = (int)((__float_as_uint(w) >> 23) & 0xFFu) - 126;  // w < 2^e2
+                const int en = max(vexp, e2 - 7);
+                const float f = ldexpf(1.f, vexp - en);
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        O[hg][mt][0] *= f;
+                        O[hg][mt][1] *= f;
+                        O[hg][mt][2] *= f;
+                        O[hg][mt][3] *= f;
+                    }
+                vexp = en;
+                vlim = ldexpf(1.f, en + 7);
+                vsc = ldexpf(1.f, -en);
+            }
+        }
+        float p[NG][2][2];
+#pragma unroll
+        for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    p[hg][u][h] = fast_exp2(sc[hg][u][h] - m_run[hg]);
+                    l_run[hg] += p[hg][u][h];
+                }
+
+        // ---- O^T += V^T P, per sub-tile
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (sparse) {  // skip when every head is below the threshold
+                bool keep = false;
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg)
+                    keep = keep || (hok[hg] && fmaxf(p[hg][u][0], p[hg][u][1]) >= thr);
+                if (!__any_sync(kAll, keep)) continue;
+            }
+            uint32_t pb0[NG], pb1[NG];
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) {
+                const float x0 = p[hg][u][0] * (vn[u][0] * vsc);
+                const float x1 = p[hg][u][1] * (vn[u][1] * vsc);
+                const float y0 = ok[u][0] ? x0 : 0.f, y1 = ok[u][1] ? x1 : 0.f;
+                const __half2 hh = __floats2half2_rn(y0, y1);
+                const float2 hf = __half22float2(hh);
+                const __half2 hl = __floats2half2_rn(y0 - hf.x, y1 - hf.y);
+                const uint32_t uH = *reinterpret_cast<const uint32_t*>(&hh);
+                const uint32_t uL = *reinterpret_cast<const uint32_t*>(&hl);
+                const uint32_t hA = __shfl_sync(kAll, uH, srcA);
+                const uint32_t hB = __shfl_sync(kAll, uH, srcB);
+                const uint32_t lA = __shfl_sync(kAll, uL, srcA);
+                const uint32_t lB = __shfl_sync(kAll, uL, srcB);
+                const uint32_t sA = odd ? lA : hA, sB = odd ? lB : hB;
+                pb0[hg] = __byte_perm(sA, sB, 0x5410);  // positions 2t, 2t + 1
+                pb1[hg] = __byte_perm(sA, sB, 0x7632);  // positions 2t + 8, 2t + 9
+            }
+            uint32_t fA[2], fB[2], fC[2], fD[2];
+            const uint32_t r0 = sV + (uint32_t)((16 * u + 2 * t) * L::kVRow);
+            load_vfield<VB>(r0, g, fA);
+            load_vfield<VB>(r0 + L::kVRow, g, fB);
+            load_vfield<VB>(r0 + 8 * L::kVRow, g, fC);
+            load_vfield<VB>(r0 + 9 * L::kVRow, g, fD);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const uint32_t uA = lds_tab(pair_addr<VB>(fA, mt, vslot));
+                const uint32_t uB = lds_tab(pair_addr<VB>(fB, mt, vslot));
+                const uint32_t uC = lds_tab(pair_addr<VB>(fC, mt, vslot));
+                const uint32_t uD = lds_tab(pair_addr<VB>(fD, mt, vslot));
+                const uint32_t a0 = __byte_perm(uA, uB, 0x5410), a1 = __byte_perm(uA, uB, 0x7632);
+                const uint32_t a2 = __byte_perm(uC, uD, 0x5410), a3 = __byte_perm(uC, uD, 0x7632);
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg) mma16816(O[hg][mt], a0, a1, a2, a3, pb0[hg], pb1[hg]);
+            }
+        }
+    };
 
     int split = (int)(i_begin % n_splits), cst = 0;
     uint32_t cph = 0;
     int64_t bh = i_begin / n_splits;
     for (int64_t item = i_begin; item < i_end; ++item) {
-        {
+#pragma unroll
+        for (int hg = 0; hg < NG; ++hg) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) O[hg][mt][0] = O[hg][mt][1] = O[hg][mt][2] = O[hg][mt][3] = 0.f;
+            m_run[hg] = -INFINITY;
+            l_run[hg] = 0.f;
+        }
+        vexp = 0;
+        vlim = 128.f;
+        vsc = 1.f;
+        if (bh != cur_bh) {
+            cur_bh = bh;
+            const int64_t b = bh / Hkv;
+            const int gh = (int)(bh % Hkv);
 #pragma unroll
             for (int hg = 0; hg < NG; ++hg) {
+                const int hc = 4 * hg + (g >> 1);  // head of this lane's B column
+                if (hc < G) {
+                    const uint4* qp = reinterpret_cast<const uint4*>(
+                        q16 + ((b * Hq + gh * G + hc) * 2 + (g & 1)) * 128 + 32 * t);
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) O[hg][mt][0] = O[hg][mt][1] = O[hg][mt][2] = O[hg][mt][3] = 0.f;
-                m_run[hg] = -INFINITY;
-                l_run[hg] = 0.f;
-            }
-            vexp = 0;
-            vlim = 128.f;
-            vsc = 1.f;
-            if (bh != cur_bh) {
-                cur_bh = bh;
-                const int64_t b = bh / Hkv;
-                const int gh = (int)(bh % Hkv);
-#pragma unroll
-                for (int hg = 0; hg < NG; ++hg) {
-                    const int hc = 4 * hg + (g >> 1);  // head of this lane's B column
-                    if (hc < G) {
-                        const uint4* qp = reinterpret_cast<const uint4*>(
-                            q16 + ((b * Hq + gh * G + hc) * 2 + (g & 1)) * 128 + 32 * t);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 u = __ldg(qp + i);
-                            qb[hg][2 * i][0] = u.x;
-                            qb[hg][2 * i][1] = u.y;
-                            qb[hg][2 * i + 1][0] = u.z;
-                            qb[hg][2 * i + 1][1] = u.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) qb[hg][kk][0] = qb[hg][kk][1] = 0u;
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 u = __ldg(qp + i);
+                        qb[hg][2 * i][0] = u.x;
+                        qb[hg][2 * i][1] = u.y;
+                        qb[hg][2 * i + 1][0] = u.z;
+                        qb[hg][2 * i + 1][1] = u.w;
                     }
-                    hok[hg] = 4 * hg + t < G;
-                    qx[hg] = hok[hg] ? __ldg(qexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) qb[hg][kk][0] = qb[hg][kk][1] = 0u;
                 }
+                hok[hg] = 4 * hg + t < G;
+                qx[hg] = hok[hg] ? __ldg(qexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
             }
         }
 
-        for (int c = 0; c < nC; ++c) {
+        int64_t pos = (int64_t)split * seg + wofs;
+        for (int c = 0; c < nC; ++c, pos += kA3Chunk) {
             if (!bad) {
                 const bool ok = mbar_wait(bars + cst, cph);
-                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                if (!__all_sync(kAll, ok)) {
                     if (lane == 0) report_timeout(status, kA3StatusWait);
                     bad = true;
                 }
             }
-            const int n = chunk_len(split, c);
+            const int64_t rem = ctx_len - pos;
+            const int n = rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
             if (n > 0 && !bad) {
                 const uint32_t sb = ring + (uint32_t)(cst * L::kStage);
-                const uint32_t sK = sb, sV = sb + L::kVOff;
-                // ---- scores of the chunk's 32 positions
-                float sacc[2][NG][4];
-                uint32_t kw[2][2][KB];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-#pragma unroll
-                    for (int hg = 0; hg < NG; ++hg) sacc[u][hg][0] = sacc[u][hg][1] = sacc[u][hg][2] = sacc[u][hg][3] = 0.f;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[u][h]);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t a0 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk, kslot));
-                        const uint32_t a2 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk + 1, kslot));
-                        const uint32_t a1 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk, kslot));
-                        const uint32_t a3 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk + 1, kslot));
-#pragma unroll
-                        for (int hg = 0; hg < NG; ++hg)
-                            mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
-                    }
-                }
-                // lane (g, t): positions 16u + 8h + g of head 4hg + t
-                float sc[NG][2][2], vn[2][2];
-                bool ok[2][2];
-                float nvl = 0.f;
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = 16 * u + 8 * h + g;
-                        ok[u][h] = r < n;
-                        const float kn = lds_f32(sb + L::kKnOff + 4u * r);
-                        vn[u][h] = lds_f32(sb + L::kVnOff + 4u * r);
-                        if (ok[u][h]) nvl = fmaxf(nvl, vn[u][h]);
-#pragma unroll
-                        for (int hg = 0; hg < NG; ++hg)
-                            sc[hg][u][h] = ok[u][h] ? (sacc[u][hg][2 * h] + sacc[u][hg][2 * h + 1]) * kn * qx[hg]
-                                                    : -INFINITY;
-                    }
-                bool need = false;
-                float tmax[NG];
-#pragma unroll
-                for (int hg = 0; hg < NG; ++hg) {
-                    float mx = fmaxf(fmaxf(sc[hg][0][0], sc[hg][0][1]), fmaxf(sc[hg][1][0], sc[hg][1][1]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-                    tmax[hg] = mx;
-                    need = need || mx > m_run[hg] + kLazy;
-                }
-                if (__any_sync(0xFFFFFFFFu, need)) {
-#pragma unroll
-                    for (int hg = 0; hg < NG; ++hg) {
-                        const float mn = fmaxf(m_run[hg], tmax[hg]);
-                        const float al = mn == -INFINITY ? 1.f : fast_exp2(m_run[hg] - mn);
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            O[hg][mt][0] *= al;
-                            O[hg][mt][1] *= al;
-                            O[hg][mt][2] *= al;
-                            O[hg][mt][3] *= al;
-                        }
-                        l_run[hg] *= al;
-                        m_run[hg] = mn;
-                    }
-                }
-                // V norms beyond 2^(vexp+7) would take p * n_v out of the fp16 range
-                if (__any_sync(0xFFFFFFFFu, nvl > vlim)) {
-                    float w = nvl;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-                    const int e2 = (int)((__float_as_uint(w) >> 23) & 0xFFu) - 126;  // w < 2^e2
-                    const int en = max(vexp, e2 - 7);
-                    const float f = ldexpf(1.f, vexp - en);
-#pragma unroll
-                    for (int hg = 0; hg < NG; ++hg)
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            O[hg][mt][0] *= f;
-                            O[hg][mt][1] *= f;
-                            O[hg][mt][2] *= f;
-                            O[hg][mt][3] *= f;
-                        }
-                    vexp = en;
-                    vlim = ldexpf(1.f, en + 7);
-                    vsc = ldexpf(1.f, -en);
-                }
-                float p[NG][2][2];
-#pragma unroll
-                for (int hg = 0; hg < NG; ++hg)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            p[hg][u][h] = fast_exp2(sc[hg][u][h] - m_run[hg]);
-                            l_run[hg] += p[hg][u][h];
-                        }
-
-                // ---- O^T += V^T P, per sub-tile
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    bool keep = false;
-#pragma unroll
-                    for (int hg = 0; hg < NG; ++hg)
-                        keep = keep || (hok[hg] && fmaxf(p[hg][u][0], p[hg][u][1]) >= thr);
-                    if (!__any_sync(0xFFFFFFFFu, keep)) continue;  // sparse V: every head below thr
-                    uint32_t pb0[NG], pb1[NG];
-#pragma unroll
-                    for (int hg = 0; hg < NG; ++hg) {
-                        const float x0 = ok[u][0] ? p[hg][u][0] * (vn[u][0] * vsc) : 0.f;
-                        const float x1 = ok[u][1] ? p[hg][u][1] * (vn[u][1] * vsc) : 0.f;
-                        const __half2 hh = __floats2half2_rn(x0, x1);
-                        const float2 hf = __half22float2(hh);
-                        const __half2 hl = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-                        const uint32_t uH = *reinterpret_cast<const uint32_t*>(&hh);
-                        const uint32_t uL = *reinterpret_cast<const uint32_t*>(&hl);
-                        const uint32_t hA = __shfl_sync(0xFFFFFFFFu, uH, srcA);
-                        const uint32_t hB = __shfl_sync(0xFFFFFFFFu, uH, srcB);
-                        const uint32_t lA = __shfl_sync(0xFFFFFFFFu, uL, srcA);
-                        const uint32_t lB = __shfl_sync(0xFFFFFFFFu, uL, srcB);
-                        const uint32_t sA = odd ? lA : hA, sB = odd ? lB : hB;
-                        pb0[hg] = __byte_perm(sA, sB, 0x5410);  // positions 2t, 2t + 1
-                        pb1[hg] = __byte_perm(sA, sB, 0x7632);  // positions 2t + 8, 2t + 9
-                    }
-                    uint32_t fA[2], fB[2], fC[2], fD[2];
-                    const uint32_t r0 = sV + (uint32_t)((16 * u + 2 * t) * L::kVRow);
-                    load_vfield<VB>(r0, g, fA);
-                    load_vfield<VB>(r0 + L::kVRow, g, fB);
-                    load_vfield<VB>(r0 + 8 * L::kVRow, g, fC);
-                    load_vfield<VB>(r0 + 9 * L::kVRow, g, fD);
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        const uint32_t uA = lds_tab(pair_addr<VB>(fA, mt, vslot));
-                        const uint32_t uB = lds_tab(pair_addr<VB>(fB, mt, vslot));
-                        const uint32_t uC = lds_tab(pair_addr<VB>(fC, mt, vslot));
-                        const uint32_t uD = lds_tab(pair_addr<VB>(fD, mt, vslot));
-                        const uint32_t a0 = __byte_perm(uA, uB, 0x5410), a1 = __byte_perm(uA, uB, 0x7632);
-                        const uint32_t a2 = __byte_perm(uC, uD, 0x5410), a3 = __byte_perm(uC, uD, 0x7632);
-#pragma unroll
-                        for (int hg = 0; hg < NG; ++hg) mma16816(O[hg][mt], a0, a1, a2, a3, pb0[hg], pb1[hg]);
-                    }
-                }
+                if (n == kA3Chunk) chunk(sb, n, std::true_type{});
+                else chunk(sb, n, std::false_type{});
             }
             __syncwarp();
             issue_next();
@@ -747,43 +766,42 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 cst = 0;
                 cph ^= 1u;
             }
-        }  // chunks
+        }
 
         // ---- end of an item: merge the warps' partials, one per query head
-        {
-            const float mul = ldexpf(P.out_mul, vexp);
+        const float mul = ldexpf(P.out_mul, vexp);
 #pragma unroll
-            for (int hg = 0; hg < NG; ++hg) {
-                float l = l_run[hg];
-                l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
-                l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
-                l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-                if (hok[hg]) {
-                    float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
+        for (int hg = 0; hg < NG; ++hg) {
+            float l = l_run[hg];
+            l += __shfl_xor_sync(kAll, l, 4);
+            l += __shfl_xor_sync(kAll, l, 8);
+            l += __shfl_xor_sync(kAll, l, 16);
+            if (hok[hg]) {
+                float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float4 v;
-                        v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
-                        v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
-                        v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
-                        v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
-                        *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
-                    }
-                    if (g == 0) {
-                        row[128] = m_run[hg];
-                        row[129] = l;
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    float4 v;
+                    v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
+                    v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
+                    v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
+                    v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
+                    *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
+                }
+                if (g == 0) {
+                    row[128] = m_run[hg];
+                    row[129] = l;
                 }
             }
-            __syncthreads();
+        }
+        __syncthreads();
+        {
             const int64_t b = bh / Hkv;
             const int gh = (int)(bh % Hkv);
             for (int i = threadIdx.x; i < G * 128; i += T) {
                 const int h = i >> 7, dim = i & 127;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < W; ++w)
-                    M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
+                for (int w = 0; w < W; ++w) M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
                 float Ls = 0.f, A = 0.f;
 #pragma unroll
                 for (int w = 0; w < W; ++w) {
@@ -799,8 +817,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                     o[129] = Ls;
                 }
             }
-            __syncthreads();
         }
+        __syncthreads();
         if (++split == n_splits) {
             split = 0;
             ++bh;

@@ -16,7 +16,7 @@
 // The d = 128 bf16 encode runs its Walsh-Hadamard transform on the tensor
 // cores (tcgen05) when this is 1, on CUDA cores (TMA-fed kernel) when 0.
 #ifndef TQ_ENCODE_TCGEN05
-#define TQ_ENCODE_TCGEN05 0
+#define TQ_ENCODE_TCGEN05 1
 #endif
 // Likewise for the d = 128 bf16-output decode.
 #ifndef TQ_DECODE_TCGEN05
@@ -153,6 +153,129 @@ __global__ void __launch_bounds__(kBlock) k_append(const T* __restrict__ k_new,
         case 2: append_rows<D, 2, T>(src, pk, nrm, n_items, n_new, cache.cap, pos, P, bnd_s); break;
         case 3: append_rows<D, 3, T>(src, pk, nrm, n_items, n_new, cache.cap, pos, P, bnd_s); break;
         default: append_rows<D, 4, T>(src, pk, nrm, n_items, n_new, cache.cap, pos, P, bnd_s); break;
+    }
+}
+
+// Append for d >= 32, built for latency (a decode step appends a few rows):
+// one warp per row, E = d / 32 consecutive elements per lane.  The transform
+// runs over the element bits in registers and over the lane bits with
+// shuffles, in the same bit order and with the same adds as the in-register
+// transform; each index is the count of boundaries below the coordinate
+// (same comparison as the other encoders), and the packed row is assembled
+// through a per-warp byte buffer, one 32-bit word per lane.
+constexpr int kAppWarps = 4;
+
+template <int E, typename T>
+__device__ __forceinline__ void load_lane(const T* __restrict__ row, int lane, const uint32_t* sg,
+                                          float (&v)[E]) {
+    if constexpr (sizeof(T) == 2) {
+        const uint16_t* p = reinterpret_cast<const uint16_t*>(row) + lane * E;
+        uint32_t h[E];
+        if constexpr (E == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                h[2 * k] = w[k] & 0xFFFFu;
+                h[2 * k + 1] = w[k] >> 16;
+            }
+        } else if constexpr (E == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            h[0] = u.x & 0xFFFFu;
+            h[1] = u.x >> 16;
+            h[2] = u.y & 0xFFFFu;
+            h[3] = u.y >> 16;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) h[e] = p[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __uint_as_float((h[e] << 16) ^ sg[lane * E + e]);
+    } else {
+        const float* p = reinterpret_cast<const float*>(row) + lane * E;
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < E / 4; ++k) {
+                const float4 u = reinterpret_cast<const float4*>(p)[k];
+                v[4 * k] = u.x;
+                v[4 * k + 1] = u.y;
+                v[4 * k + 2] = u.z;
+                v[4 * k + 3] = u.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[e] = p[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg[lane * E + e]);
+    }
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restrict__ k_new,
+                                                                const T* __restrict__ v_new, int64_t n_rows,
+                                                                int64_t n_new, tq_cache_view cache,
+                                                                int64_t pos, int k_bits, int v_bits,
+                                                                const __grid_constant__ RowParams PK,
+                                                                const __grid_constant__ RowParams PV) {
+    static_assert(D >= 32 && D <= kMaxD, "one warp per row");
+    constexpr int E = D / 32;
+    __shared__ uint32_t sg[D];
+    __shared__ uint8_t idxbuf[kAppWarps][D];
+    const bool is_v = blockIdx.y == 1;
+    const RowParams& P = is_v ? PV : PK;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) sg[i] = P.sgn[i];
+    __syncthreads();
+    const int bits = is_v ? v_bits : k_bits;
+    const int nb = (1 << bits) - 1;
+    const T* src = is_v ? v_new : k_new;
+    uint8_t* pk = is_v ? cache.v_packed : cache.k_packed;
+    float* nrm = is_v ? cache.v_norm : cache.k_norm;
+    const int rb = D * bits / 8;  // bytes per packed row (a multiple of 4)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ib = idxbuf[warp];
+    for (int64_t srow = (int64_t)blockIdx.x * kAppWarps + warp; srow < n_rows;
+         srow += (int64_t)gridDim.x * kAppWarps) {
+        float v[E];
+        load_lane<E, T>(src + srow * D, lane, sg, v);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        fwht_reg<E>(v);
+#pragma unroll
+        for (int b = 1; b < 32; b <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
+                v[e] = (lane & b) ? o - v[e] : v[e] + o;  // (lo + hi, lo - hi)
+            }
+        }
+        const float n = __fsqrt_rn(ss);
+        const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            int id = 0;
+            for (int j = 0; j < nb; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
+            ib[lane * E + e] = (uint8_t)id;
+        }
+        __syncwarp();
+        const int64_t i_in = srow % n_new;
+        const int64_t drow = (srow / n_new) * cache.cap + pos + i_in;
+        if (4 * lane < rb) {  // word `lane` of the packed row: stream bits [32 lane, 32 lane + 32)
+            const int b0 = 32 * lane;
+            const int i0 = b0 / bits, i1 = min(D - 1, (b0 + 31) / bits);
+            uint32_t word = 0u;
+            for (int i = i0; i <= i1; ++i) {
+                const int sh = i * bits - b0;
+                const uint32_t x = ib[i];
+                word |= sh >= 0 ? x << sh : x >> -sh;
+            }
+            reinterpret_cast<uint32_t*>(pk + drow * rb)[lane] = word;
+        }
+        if (lane == 0) nrm[drow] = n;
+        __syncwarp();
     }
 }
 
@@ -399,12 +522,45 @@ k_encode_tma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* 
 // (32x32b loads), forms the norm, buckets through the exact table and packs.
 
 constexpr int kUmRows = 128;
-constexpr int kUmStages = 4;
+constexpr int kUmStages = 3;
 constexpr int kUmAcc = 4;             // tensor-memory accumulators of 128 columns
 constexpr int kUmThreads = 10 * 32;
 constexpr int kUmStageBytes = kUmRows * 128 * 2;
-constexpr int kUmSmemBytes = 1024 + kUmStages * kUmStageBytes + 128 * 128 * 2 + kLutCells * 8 +
-                             (2 * kUmStages + 2 * kUmAcc) * 8 + 16;
+// Shared memory by absolute shared-window address.  The lane-replicated
+// bucketing table sits at 64 KiB: entry (cell c, lane l) is at
+// kUmRepAt + 256 c + 8 l, so its address is one byte permute of the cell's
+// low byte.
+constexpr uint32_t kUmHbAt = 2048;                              // D H (32 KB)
+constexpr uint32_t kUmBarAt = kUmHbAt + 128 * 128 * 2;          // barriers, TMEM slot
+constexpr uint32_t kUmRepAt = 65536;                            // replicated window (64 KB)
+constexpr uint32_t kUmXsAt = 131072;                            // X stages
+constexpr uint32_t kUmEnd = kUmXsAt + kUmStages * kUmStageBytes;
+static_assert(kUmBarAt + (2 * kUmStages + 2 * kUmAcc) * 8 + 16 <= kUmRepAt, "layout");
+static_assert(kUmEnd <= 232448, "shared memory");
+// The window: cells k = rint(w * kLutScale) in [-128, 128), i.e. |w| < 0.5.
+constexpr int kRepCells = 256;
+constexpr uint32_t kRepMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
+
+__device__ __forceinline__ LutEntry lds_entry(uint32_t addr) {
+    LutEntry e;
+    asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(e.lo), "=f"(e.thr) : "r"(addr));
+    return e;
+}
+
+// Table entry of the cell k = rint(w * kLutScale) (same rule as build_lut).
+__device__ __forceinline__ LutEntry lut_cell(const float* bnd, int nb, int k) {
+    const float lo = (float)(k - 0.5) / (float)kLutScale;
+    const float hi = (float)(k + 0.5) / (float)kLutScale;
+    LutEntry e;
+    e.lo = 0;
+    e.thr = __int_as_float(0x7F800000);
+    for (int j = 0; j < nb; ++j) {
+        const float b = bnd[j];
+        if (b < lo) e.lo += 1;
+        else if (b <= hi) e.thr = b;
+    }
+    return e;
+}
 
 template <int BITS>
 __global__ void __launch_bounds__(kUmThreads, 1)
@@ -412,11 +568,15 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
               float* __restrict__ norms, int* status, const __grid_constant__ RowParams P) {
     constexpr int RB = 128 * BITS / 8;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    unsigned char* xs = base;                                   // stages of X
-    unsigned char* hb = xs + kUmStages * kUmStageBytes;         // D H, K-major
-    LutEntry* lut = reinterpret_cast<LutEntry*>(hb + 128 * 128 * 2);
-    uint64_t* full = reinterpret_cast<uint64_t*>(lut + kLutCells);
+    const uint32_t sbase = smem_addr(smem_raw);
+    if (sbase > kUmHbAt) {  // the layout assumes dynamic memory starts lower
+        if (threadIdx.x == 0) report_timeout(status, 17);
+        return;
+    }
+    auto at = [&](uint32_t a) { return smem_raw + (a - sbase); };
+    unsigned char* xs = at(kUmXsAt);                            // stages of X
+    unsigned char* hb = at(kUmHbAt);                            // D H, K-major
+    uint64_t* full = reinterpret_cast<uint64_t*>(at(kUmBarAt));
     uint64_t* empty = full + kUmStages;
     uint64_t* accf = empty + kUmStages;
     uint64_t* acce = accf + kUmAcc;
@@ -431,7 +591,12 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
         const int off = (k >> 6) * 16384 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
         *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBF80u : 0x3F80u;
     }
-    build_lut(lut, P.bnd, (1 << BITS) - 1);
+    for (int c = threadIdx.x; c < kRepCells; c += blockDim.x) {
+        const LutEntry e = lut_cell(P.bnd, (1 << BITS) - 1, c - kRepCells / 2);
+        LutEntry* row = reinterpret_cast<LutEntry*>(at(kUmRepAt + 256u * c));
+#pragma unroll 4
+        for (int l = 0; l < 32; ++l) row[l] = e;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kUmStages; ++i) {
             mbar_init(&full[i], 1);
@@ -507,8 +672,9 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
         const int wg = (warp - 2) >> 2, q = warp & 3;
         const int r = 32 * q + lane;
         constexpr int NW = 128 * BITS / 32;
-        constexpr float kMagic = 12582912.0f + (float)kLutCenter;
+        constexpr float kMagic = 12582912.0f + (float)(kRepCells / 2);
         const F2 M2 = f2(kMagic, kMagic);
+        const uint32_t rep_slot = kUmRepAt + 8u * lane;
         int it = wg;
         for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < n_tiles;
              tile += 2 * (int64_t)gridDim.x, it += 2) {
@@ -544,6 +710,11 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
             uint32_t w[NW];
 #pragma unroll
             for (int k = 0; k < NW; ++k) w[k] = 0;
+            // Cells come from the replicated window (conflict-free: lane l
+            // reads only its own column); `out` collects every bit outside
+            // the window's low byte, non-zero iff some |w| >= 0.5 (or the row
+            // is not finite).
+            uint32_t out = 0u;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t y[32];
@@ -554,8 +725,10 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
                     const float y0 = __uint_as_float(y[i]), y1 = __uint_as_float(y[i + 1]);
                     float fx, fy;
                     f2_split(f2_fma(f2(y0, y1), K2, M2), fx, fy);
-                    const LutEntry e0 = lut[__float_as_uint(fx) & (kLutCells - 1)];
-                    const LutEntry e1 = lut[__float_as_uint(fy) & (kLutCells - 1)];
+                    const uint32_t bx = __float_as_uint(fx), by = __float_as_uint(fy);
+                    out |= (bx ^ kRepMagicBits) | (by ^ kRepMagicBits);
+                    const LutEntry e0 = lds_entry(__byte_perm(bx, rep_slot, 0x7604));
+                    const LutEntry e1 = lds_entry(__byte_perm(by, rep_slot, 0x7604));
                     const int id0 = e0.lo + (fmaf(y0, inv, -e0.thr) >= 0.0f ? 1 : 0);
                     const int id1 = e1.lo + (fmaf(y1, inv, -e1.thr) >= 0.0f ? 1 : 0);
 #pragma unroll
@@ -564,6 +737,30 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
                         const int pos = (32 * c + i + h) * BITS, wi = pos / 32, sh = pos % 32;
                         w[wi] += (uint32_t)id << sh;
                         if (sh + BITS > 32) w[wi + 1] += (uint32_t)id >> (32 - sh);
+                    }
+                }
+            }
+            // Rows with a coordinate outside the window: exact binary search
+            // over the boundaries (the tensor-memory loads are warp-wide).
+            const bool slow = (out & ~0xFFu) != 0u;
+            if (__any_sync(0xFFFFFFFFu, slow)) {
+                if (slow) {
+#pragma unroll
+                    for (int k = 0; k < NW; ++k) w[k] = 0;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(ta + 32 * c, y);
+                    tmem_wait_ld();
+                    if (slow) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int id = bucket_search<BITS>(P.bnd, __uint_as_float(y[i]), inv);
+                            const int pos = (32 * c + i) * BITS, wi = pos / 32, sh = pos % 32;
+                            w[wi] += (uint32_t)id << sh;
+                            if (sh + BITS > 32) w[wi + 1] += (uint32_t)id >> (32 - sh);
+                        }
                     }
                 }
             }
@@ -1039,12 +1236,13 @@ cudaError_t enc_umma(const void* x, int64_t n, uint8_t* pk, float* nm, const Row
     cudaError_t e = make_rows_map(&map, x, 2, 128, (uint64_t)n, dev::kUmRows);
     if (e != cudaSuccess) return e;
     auto fn = dev::k_encode_umma<BITS>;
-    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kUmSmemBytes);
+    // absolute layout: ask for kUmEnd bytes (the dynamic block starts below kUmHbAt)
+    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev::kUmEnd);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (n + dev::kUmRows - 1) / dev::kUmRows;
     int64_t grid = num_sms();
     if (grid > tiles) grid = tiles;
-    fn<<<(unsigned)grid, dev::kUmThreads, dev::kUmSmemBytes, s>>>(map, n, pk, nm, status_word(), P);
+    fn<<<(unsigned)grid, dev::kUmThreads, dev::kUmEnd, s>>>(map, n, pk, nm, status_word(), P);
     return cudaGetLastError();
 }
 
@@ -1118,11 +1316,21 @@ cudaError_t dec(const uint8_t* pk, const float* nm, int64_t n, void* y, const Ro
 template <int D, typename T>
 cudaError_t app(const void* kn, const void* vn, int B, int Hkv, int64_t n_new, const tq_cache_view& c,
                 int64_t pos, int kb, int vb, const RowParams& PK, const RowParams& PV, cudaStream_t s) {
-    auto fn = dev::k_append<D, T>;
     const int64_t rows = (int64_t)B * Hkv * n_new;
-    unsigned g = grid_for((const void*)fn, dev::kBlock, rows * dev::RowShape<D>::R);
-    fn<<<dim3(g, 2), dev::kBlock, 0, s>>>(static_cast<const T*>(kn), static_cast<const T*>(vn), rows,
-                                          n_new, c, pos, kb, vb, PK, PV);
+    if constexpr (D >= 32) {
+        auto fn = dev::k_append_warp<D, T>;
+        int64_t g = (rows + dev::kAppWarps - 1) / dev::kAppWarps;
+        const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kAppWarps, 0);
+        if (g > cap) g = cap;
+        fn<<<dim3((unsigned)g, 2), 32 * dev::kAppWarps, 0, s>>>(static_cast<const T*>(kn),
+                                                                static_cast<const T*>(vn), rows, n_new, c,
+                                                                pos, kb, vb, PK, PV);
+    } else {
+        auto fn = dev::k_append<D, T>;
+        unsigned g = grid_for((const void*)fn, dev::kBlock, rows * dev::RowShape<D>::R);
+        fn<<<dim3(g, 2), dev::kBlock, 0, s>>>(static_cast<const T*>(kn), static_cast<const T*>(vn), rows,
+                                              n_new, c, pos, kb, vb, PK, PV);
+    }
     return cudaGetLastError();
 }
 

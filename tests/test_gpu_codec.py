@@ -79,6 +79,33 @@ def test_encode_edge_rows(d):
         assert np.array_equal(idx[k], idx[8])
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("d", [64, 128])
+def test_encode_spiky_rotated_rows_bf16(d, bits):
+    """bf16 rows whose rotated, normalised coordinates reach |u| = 1 or sit
+    near |u| = 0.5: a sign-flipped column of the Hadamard matrix, scaled, plus
+    seeded noise.  The d = 128 encoder buckets |u| < 0.5 through a windowed
+    table and redoes any other row by binary search; both must agree with the
+    oracle."""
+    s = O.signs(42, d)
+    noise = synth.normal_rows(4242 + d, 64, d).double().numpy()
+    j = np.arange(d)
+    rows = []
+    for r in range(64):
+        k = (r * 37) % d
+        col = s * np.where([bin(int(i) & k).count("1") % 2 for i in j], -1.0, 1.0)
+        a = (1.0, -1.0, 0.9, 0.6, 0.52, 0.5, 0.48, 0.3)[r % 8]
+        b = 0.0 if r % 16 < 2 else 0.03 * (1 + r % 5)
+        rows.append(a * col / math.sqrt(d) + b * noise[r])
+    x = torch.tensor(np.stack(rows), dtype=torch.float32).to(torch.bfloat16)
+    plan = abi.Plan(d, 42)
+    pk, nm = _encode(plan, bits, x)
+    compare_encode(s, bits, x.double().numpy(), pk, nm)
+    u = O.encode(s, bits, x.double().numpy(), want_u=True)[2]
+    m = np.abs(u).max(axis=1)
+    assert m.max() > 0.99 and (m >= 0.5).sum() >= 16 and ((m > 0.4) & (m < 0.6)).sum() >= 8
+
+
 def test_encode_single_row_and_empty():
     plan = abi.Plan(128, 3)
     x = synth.normal_rows(5, 1, 128)

@@ -137,11 +137,17 @@ def test_gemma_window_encode_and_append_loop():
     new_v = synth.device_normal(4003, (steps, L, 1, Hkv, 1, d))
     for l in range(L):
         abi.tq_append(plan, caches[l], win_k[l], win_v[l], 0)
-    # flat encode of the same window agrees with the cache rows
+    # flat encode of the same window agrees with the cache rows: the two
+    # kernels sum the norm in different orders, so an index may differ only
+    # where a coordinate sits on a boundary (both are checked against the
+    # oracle below)
     pk, nm = abi.tq_encode(plan, 4, win_k.reshape(-1, d))
     torch.cuda.synchronize()
-    assert torch.equal(pk.view(L, Hkv, T, -1).cpu(),
-                       torch.stack([c.k_packed[0, :, :T].cpu() for c in caches]))
+    flat = O.unpack(pk.cpu().numpy(), d, 4)
+    app = O.unpack(torch.stack([c.k_packed[0, :, :T] for c in caches]).reshape(-1, d // 2).cpu().numpy(), d, 4)
+    assert np.mean(flat != app) <= 1e-5
+    napp = torch.stack([c.k_norm[0, :, :T] for c in caches]).reshape(-1)
+    assert torch.allclose(nm, napp, rtol=1e-6, atol=0)
     # one decode step (34 appends) captured once per position
     stream = torch.cuda.Stream()
     for step in range(steps):
