@@ -25,20 +25,36 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 // A pointer the GPU cannot dereference (pageable host memory on a system
 // without pageable-memory access) is turned into an error instead of a fault.
 // Unknown answers are let through.
+// A pointer the GPU cannot dereference (pageable host memory on a system
+// without pageable-memory access) is turned into an error instead of a fault.
+// Unknown answers are let through.  Where the device reads pageable memory
+// every pointer qualifies, so no per-pointer query is made (the answer is
+// cached per device).
+bool pageable_access() {
+    static int cached[64] = {};  // 0 unknown, 1 no, 2 yes
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 2;
+    int pageable = 0;
+    if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (dev >= 0 && dev < 64) cached[dev] = pageable ? 2 : 1;
+    return pageable != 0;
+}
+
 bool device_accessible(const void* p) {
+    if (pageable_access()) return true;
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
         cudaGetLastError();
         return true;
     }
-    if (a.type != cudaMemoryTypeUnregistered) return true;
-    int dev = 0, pageable = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return true;
-    }
-    return pageable != 0;
+    return a.type != cudaMemoryTypeUnregistered;
 }
 
 // ------------------------------------------------------------ signs
@@ -380,8 +396,7 @@ size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !is_pow2(d) ||
         d > tq::kMaxD)
         return 0;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), d);
-    return tq::attn_workspace_bytes(B, Hq, d, g);
+    return tq::attn_workspace_bound(B, Hq, Hkv, ctx_len, tq::num_sms(), d);
 }
 
 tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
@@ -403,7 +418,7 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d);
+    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
     size_t need = tq::attn_workspace_bytes(B, Hq, P->d, g);
     if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;

@@ -271,29 +271,30 @@ constexpr float kLazy = 8.0f;        // log2 units
 // table starts at 128 KiB: entry e of lane l's column is at
 // kA3TableAt + e * 256 + 4 * l (K) or + 128 + 4 * l (V), so a lookup address
 // is (e << 8) | slot, one byte permute for a 4-bit pair.
-constexpr uint32_t kA3RingAt = 2048;
-constexpr uint32_t kA3TableAt = 131072;
+constexpr uint32_t kA3RingAt = kAttn3RingAt;
+constexpr uint32_t kA3TableAt = kAttn3TableAt;
 // Device status codes.
 constexpr int kA3StatusWait = 31;    // a ring stage did not complete within the bound
 constexpr int kA3StatusLayout = 32;  // dynamic shared memory starts above kA3RingAt
 
-// Warps and ring stages per CTA: 12 x 2 for up to four query heads per KV
-// head (about 160 registers a thread), 8 x 3 for up to eight (about 220).
-template <int NG>
+// Warps and ring stages per CTA (attn3_warps, attn3_stages): up to 16 x 2
+// for up to four query heads per KV head, 8 x 3 for up to eight.
+template <int KB, int VB, int NG>
 struct A3Shape {
-    static constexpr int kWarps = NG == 1 ? kAttn3WarpsG4 : kAttn3WarpsG8;
-    static constexpr int kStages = NG == 1 ? 2 : 3;
+    static constexpr int kWarps = attn3_warps(4 * NG, KB, VB);
+    static constexpr int kStages = attn3_stages(4 * NG);
     static constexpr int kThreads = 32 * kWarps;
 };
 
 template <int KB, int VB, int NG>
 struct A3Layout {
-    static constexpr int kWarps = A3Shape<NG>::kWarps, kStages = A3Shape<NG>::kStages;
+    static constexpr int kWarps = A3Shape<KB, VB, NG>::kWarps, kStages = A3Shape<KB, VB, NG>::kStages;
     static constexpr int kKRow = 16 * KB, kVRow = 16 * VB;  // bytes of a d = 128 row
     static constexpr int kVOff = kA3Chunk * kKRow;
     static constexpr int kKnOff = kA3Chunk * (kKRow + kVRow);
     static constexpr int kVnOff = kKnOff + 4 * kA3Chunk;
     static constexpr int kStage = kVnOff + 4 * kA3Chunk;
+    static_assert(kStage == attn3_stage_bytes(KB, VB), "stage size");
     static constexpr int kEntries = 1 << (2 * (KB > VB ? KB : VB));
     static constexpr int kHeads = 4 * NG;
     static constexpr uint32_t kMergeAt = kA3TableAt + 256u * kEntries;
@@ -321,6 +322,13 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Work items are split over the CTAs of the grid as contiguous ranges:
+// CTA c takes items [n_items c / grid, n_items (c + 1) / grid).  The CTA that
+// takes item i:
+__host__ __device__ __forceinline__ int attn3_cta_of(int64_t i, int grid, int64_t n_items) {
+    return (int)(((i + 1) * grid - 1) / n_items);
 }
 
 // Table lookup (the table is written once, before the first barrier).
@@ -440,12 +448,12 @@ static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __r
 }
 
 template <int KB, int VB, int NG>
-__global__ void __launch_bounds__(A3Shape<NG>::kThreads, 1)
+__global__ void __launch_bounds__(A3Shape<KB, VB, NG>::kThreads, 1)
 k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv,
               tq_cache_view cache, int64_t ctx_len, int warp_len, int n_splits, int64_t n_items,
               float* __restrict__ part, int* status, const __grid_constant__ AttnParams P) {
     using L = A3Layout<KB, VB, NG>;
-    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<NG>::kThreads;
+    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG>::kThreads;
     constexpr uint32_t kAll = 0xFFFFFFFFu;
     extern __shared__ __align__(16) unsigned char a3_smem[];
     const uint32_t base = smem_addr(a3_smem);
@@ -703,22 +711,81 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         }
     };
 
+    // Merge the warps' running partials of the (batch, KV head) run_bh into
+    // one partial per query head; its slot is this CTA's offset from the
+    // first CTA whose items reach run_bh.
+    auto publish = [&](int64_t run_bh) {
+        const float mul = ldexpf(P.out_mul, vexp);
+#pragma unroll
+        for (int hg = 0; hg < NG; ++hg) {
+            float l = l_run[hg];
+            l += __shfl_xor_sync(kAll, l, 4);
+            l += __shfl_xor_sync(kAll, l, 8);
+            l += __shfl_xor_sync(kAll, l, 16);
+            if (hok[hg]) {
+                float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float4 v;
+                    v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
+                    v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
+                    v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
+                    v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
+                    *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
+                }
+                if (g == 0) {
+                    row[128] = m_run[hg];
+                    row[129] = l;
+                }
+            }
+        }
+        __syncthreads();
+        const int64_t b = run_bh / Hkv;
+        const int gh = (int)(run_bh % Hkv);
+        const int slot = (int)blockIdx.x - attn3_cta_of(run_bh * n_splits, gridDim.x, n_items);
+        for (int i = threadIdx.x; i < G * 128; i += T) {
+            const int h = i >> 7, dim = i & 127;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; ++w) M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
+            float Ls = 0.f, A = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) {
+                const float* row = merge + (w * L::kHeads + h) * kA3MergeStride;
+                const float f = row[128] == -INFINITY ? 0.f : fast_exp2(row[128] - M);
+                Ls = fmaf(f, row[129], Ls);
+                A = fmaf(f, row[dim], A);
+            }
+            float* o = part + ((b * Hq + gh * G + h) * n_splits + slot) * 130;
+            o[dim] = A;
+            if (dim == 0) {
+                o[128] = M;
+                o[129] = Ls;
+            }
+        }
+        __syncthreads();
+    };
+
+    // Items of one (batch, KV head) are consecutive: the warps accumulate
+    // across them and publish when the pair changes and at the end.
     int split = (int)(i_begin % n_splits), cst = 0;
     uint32_t cph = 0;
     int64_t bh = i_begin / n_splits;
-    for (int64_t item = i_begin; item < i_end; ++item) {
-#pragma unroll
-        for (int hg = 0; hg < NG; ++hg) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) O[hg][mt][0] = O[hg][mt][1] = O[hg][mt][2] = O[hg][mt][3] = 0.f;
-            m_run[hg] = -INFINITY;
-            l_run[hg] = 0.f;
-        }
-        vexp = 0;
-        vlim = 128.f;
-        vsc = 1.f;
-        if (bh != cur_bh) {
+    for (int64_t item = i_begin; item <= i_end; ++item) {
+        if (item == i_end || bh != cur_bh) {
+            if (cur_bh >= 0) publish(cur_bh);
+            if (item == i_end) break;
             cur_bh = bh;
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) O[hg][mt][0] = O[hg][mt][1] = O[hg][mt][2] = O[hg][mt][3] = 0.f;
+                m_run[hg] = -INFINITY;
+                l_run[hg] = 0.f;
+            }
+            vexp = 0;
+            vlim = 128.f;
+            vsc = 1.f;
             const int64_t b = bh / Hkv;
             const int gh = (int)(bh % Hkv);
 #pragma unroll
@@ -767,58 +834,6 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 cph ^= 1u;
             }
         }
-
-        // ---- end of an item: merge the warps' partials, one per query head
-        const float mul = ldexpf(P.out_mul, vexp);
-#pragma unroll
-        for (int hg = 0; hg < NG; ++hg) {
-            float l = l_run[hg];
-            l += __shfl_xor_sync(kAll, l, 4);
-            l += __shfl_xor_sync(kAll, l, 8);
-            l += __shfl_xor_sync(kAll, l, 16);
-            if (hok[hg]) {
-                float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float4 v;
-                    v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
-                    v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
-                    v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
-                    v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
-                    *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
-                }
-                if (g == 0) {
-                    row[128] = m_run[hg];
-                    row[129] = l;
-                }
-            }
-        }
-        __syncthreads();
-        {
-            const int64_t b = bh / Hkv;
-            const int gh = (int)(bh % Hkv);
-            for (int i = threadIdx.x; i < G * 128; i += T) {
-                const int h = i >> 7, dim = i & 127;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < W; ++w) M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
-                float Ls = 0.f, A = 0.f;
-#pragma unroll
-                for (int w = 0; w < W; ++w) {
-                    const float* row = merge + (w * L::kHeads + h) * kA3MergeStride;
-                    const float f = row[128] == -INFINITY ? 0.f : fast_exp2(row[128] - M);
-                    Ls = fmaf(f, row[129], Ls);
-                    A = fmaf(f, row[dim], A);
-                }
-                float* o = part + ((b * Hq + gh * G + h) * n_splits + split) * 130;
-                o[dim] = A;
-                if (dim == 0) {
-                    o[128] = M;
-                    o[129] = Ls;
-                }
-            }
-        }
-        __syncthreads();
         if (++split == n_splits) {
             split = 0;
             ++bh;
@@ -827,22 +842,59 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 }
 
 // Merge the partials of one (batch, query head) (m in log2 units), normalise
-// and rotate back: out = s . (H o) / sqrt(d).
-static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_parts,
+// and rotate back: out = s . (H o) / sqrt(d).  Thread j owns dim j.  The
+// partials' maxima and weights are computed 128 at a time in parallel and
+// kept in shared memory, so the accumulation issues independent, coalesced
+// loads instead of a dependent chain per partial.
+__device__ __forceinline__ float block128_max(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+}
+__device__ __forceinline__ float block128_sum(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_splits,
+                                                              int grid, int64_t n_items, int Hq, int Hkv,
                                                               float* __restrict__ out,
                                                               const __grid_constant__ AttnParams P) {
     __shared__ float o[128];
+    __shared__ float f[128];
+    __shared__ float red[4];
     const int bh = blockIdx.x, j = threadIdx.x;
-    const float* base = part + (int64_t)bh * n_parts * 130;
+    // partials of this (batch, query head): one per CTA whose items reach its KV head
+    const int64_t bhk = (int64_t)(bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
+    const int n_parts = attn3_cta_of((bhk + 1) * n_splits - 1, grid, n_items) -
+                        attn3_cta_of(bhk * n_splits, grid, n_items) + 1;
+    const float* base = part + (int64_t)bh * n_splits * 130;
     float M = -INFINITY;
-    for (int s = 0; s < n_parts; ++s) M = fmaxf(M, base[s * 130 + 128]);
-    float L = 0.f, a = 0.f;
-    for (int s = 0; s < n_parts; ++s) {
-        const float ms = base[s * 130 + 128];
-        const float f = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-        L = fmaf(f, base[s * 130 + 129], L);
-        a = fmaf(f, base[s * 130 + j], a);
+    for (int s = j; s < n_parts; s += 128) M = fmaxf(M, base[s * 130 + 128]);
+    M = block128_max(M, red);
+    float a = 0.f, lsum = 0.f;
+    for (int s0 = 0; s0 < n_parts; s0 += 128) {
+        const int s = s0 + j;
+        float w = 0.f;
+        if (s < n_parts) {
+            const float ms = base[s * 130 + 128];
+            w = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
+            lsum = fmaf(w, base[s * 130 + 129], lsum);
+        }
+        f[j] = w;
+        __syncthreads();
+        const int cnt = min(128, n_parts - s0);
+        const float* col = base + (int64_t)s0 * 130 + j;
+#pragma unroll 8
+        for (int k = 0; k < cnt; ++k) a = fmaf(f[k], col[k * 130], a);
+        __syncthreads();
     }
+    const float L = block128_sum(lsum, red);
     o[j] = a / L;
     fwht_smem<128>(o, 1);
     out[(int64_t)bh * 128 + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
@@ -851,7 +903,7 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
 template <int KB, int VB, int NG>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
-                               int64_t items, float* part, const AttnParams& P, cudaStream_t s) {
+                               int64_t items, int grid, float* part, const AttnParams& P, cudaStream_t s) {
     using L = A3Layout<KB, VB, NG>;
     auto fn = k_attn3_split<KB, VB, NG>;
     // The kernel addresses shared memory from window address 0, so it asks
@@ -865,10 +917,9 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    int64_t grid = num_sms();
-    if (grid > items) grid = items;
-    fn<<<(unsigned)grid, A3Shape<NG>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len, geo.warp_len,
-                                                  geo.n_splits, items, part, status_word(), P);
+    fn<<<(unsigned)grid, A3Shape<KB, VB, NG>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len,
+                                                                      geo.warp_len, geo.n_splits, items,
+                                                                      part, status_word(), P);
     return cudaGetLastError();
 }
 
@@ -883,12 +934,13 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
+    const int grid = (int)(items < num_sms() ? items : num_sms());  // one CTA per SM
     if (Hq / Hkv <= 4)
-        e = attn3_split_launch<KB, VB, 1>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, part, P, s);
+        e = attn3_split_launch<KB, VB, 1>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P, s);
     else
-        e = attn3_split_launch<KB, VB, 2>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, part, P, s);
+        e = attn3_split_launch<KB, VB, 2>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P, s);
     if (e != cudaSuccess) return e;
-    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, out, P);
+    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv, out, P);
     return cudaGetLastError();
 }
 

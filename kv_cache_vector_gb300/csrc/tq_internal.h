@@ -78,10 +78,21 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
                             const tq_cache_view& cache, int64_t pos, const RowParams& PK,
                             const RowParams& PV, cudaStream_t s);
 
-// Warps per CTA of the d = 128 attention kernel, by GQA group size G.
-constexpr int kAttn3WarpsG4 = 12;  // G <= 4
-constexpr int kAttn3WarpsG8 = 8;   // 4 < G <= 8
-inline int attn3_warps(int G) { return G <= 4 ? kAttn3WarpsG4 : kAttn3WarpsG8; }
+// Shape of the d = 128 attention kernel.  Each warp streams 32-position
+// chunks (packed K and V rows plus two fp32 norms each) through its own ring
+// of stages in shared memory below kAttn3TableAt.  Up to four query heads
+// per KV head: 2 stages and as many warps (at most 16) as the ring holds; up
+// to eight: 8 warps and 3 stages.
+constexpr int kAttn3RingAt = 2048;
+constexpr int kAttn3TableAt = 131072;
+constexpr int attn3_stage_bytes(int kb, int vb) { return 32 * (16 * kb + 16 * vb + 8); }
+constexpr int attn3_stages(int G) { return G <= 4 ? 2 : 3; }
+constexpr int attn3_warps(int G, int kb, int vb) {
+    return G > 4 ? 8
+                 : ((kAttn3TableAt - kAttn3RingAt) / (2 * attn3_stage_bytes(kb, vb)) < 16
+                        ? (kAttn3TableAt - kAttn3RingAt) / (2 * attn3_stage_bytes(kb, vb))
+                        : 16);
+}
 
 struct AttnGeometry {
     int n_splits;
@@ -90,7 +101,10 @@ struct AttnGeometry {
     int warp_len;     // d = 128: positions per warp and split
     bool q16;         // the workspace starts with the rotated fp16 queries
 };
-AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
+AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d, int kb,
+                           int vb);
+// Workspace that covers every K/V width pair (the public size query takes none).
+size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
 // their power-of-two scales (4 bytes per head), rounded up to 256 bytes.

@@ -14,13 +14,21 @@ __device__ int g_status = 0;
 }
 
 int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return 1;
     }
-    return n > 0 ? n : 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
 }
 
 // Resident blocks per SM of a kernel at a block size, asked once per kernel.
@@ -55,16 +63,16 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
 }
 
 // Split-K geometry of the decode attention.  d = 128 (tensor-core kernel,
-// one CTA of attn3_warps(G) warps per SM): the longest per-warp range (256 down
-// to 32 positions) whose work items fill the last wave of CTAs to at least
-// 90%, else the one that fills it best.  Otherwise the longest split
+// one CTA of attn3_warps(G, kb, vb) warps per SM): the longest per-warp range
+// (256 down to 32 positions) whose work items fill the last wave of CTAs to
+// at least 90%, else the one that fills it best.  Otherwise the longest split
 // (<= 512 positions) that still gives two CTAs per SM.
-AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d) {
+AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d, int kb, int vb) {
     AttnGeometry g;
     const int64_t pairs = (int64_t)B * Hkv;
     if (d == 128) {
         const int64_t cap = sms > 0 ? sms : 1;
-        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1);
+        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb);
         int best = 256;
         double best_eff = -1.0;
         for (int wl = 256; wl >= 32; wl /= 2) {
@@ -98,6 +106,16 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
     g.warp_len = 0;
     g.q16 = false;
     return g;
+}
+
+size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d) {
+    size_t most = 0;
+    for (int kb = 2; kb <= 4; ++kb)
+        for (int vb = 2; vb <= 4; ++vb) {
+            const size_t w = attn_workspace_bytes(B, Hq, d, attn_geometry(B, Hq, Hkv, ctx_len, sms, d, kb, vb));
+            if (w > most) most = w;
+        }
+    return most;
 }
 
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g) {

@@ -82,7 +82,7 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, 
     if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d);
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
     if (tq::attn_workspace_bytes(B, Hq, P->d, g) > kScratchBytes) return TQ_ERR_WORKSPACE;
     void* ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
