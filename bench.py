@@ -149,17 +149,33 @@ def measured_peak():
     return 6800.0, "fallback"
 
 
-def traffic_for(kernel_key: str):
-    """Per-launch DRAM bytes of an ncu capture, if taken on the current source."""
-    p = os.path.join(ROOT, "profiles", "traffic.txt")
-    if not os.path.exists(p):
-        return None
+# Source files that define each timed kernel (a traffic figure is void once
+# any of them changes).
+KERNEL_SOURCES = {
+    "encode_k": ("tq_codec.cu", "tq_device.cuh", "tq_async.cuh", "tq_umma.cuh"),
+    "encode_v": ("tq_codec.cu", "tq_device.cuh", "tq_async.cuh", "tq_umma.cuh"),
+    "decode_k": ("tq_codec.cu", "tq_device.cuh", "tq_async.cuh", "tq_umma.cuh"),
+    "decode_v": ("tq_codec.cu", "tq_device.cuh", "tq_async.cuh", "tq_umma.cuh"),
+    "append": ("tq_codec.cu", "tq_device.cuh"),
+    "attn": ("tq_attn.cu", "tq_device.cuh", "tq_async.cuh"),
+}
+
+
+def kernel_source_hash(kernel_key: str) -> str:
     src = os.path.join(ROOT, "kv_cache_vector_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
+    for f in KERNEL_SOURCES[kernel_key]:
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
-    cur = h.hexdigest()[:16]
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str):
+    """Per-launch DRAM bytes of an ncu capture, if taken on the kernel's current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p) or kernel_key not in KERNEL_SOURCES:
+        return None
+    cur = kernel_source_hash(kernel_key)
     with open(p) as f:
         for line in f:
             parts = line.split()
