@@ -295,7 +295,7 @@ struct A3Layout {
     static constexpr int kVnOff = kKnOff + 4 * kA3Chunk;
     static constexpr int kStage = kVnOff + 4 * kA3Chunk;
     static_assert(kStage == attn3_stage_bytes(KB, VB), "stage size");
-    static constexpr int kEntries = 1 << (2 * (KB > VB ? KB : VB));
+    static constexpr int kEntries = 256;  // rows of the pair table (one byte of index)
     static constexpr int kHeads = 4 * NG;
     static constexpr uint32_t kMergeAt = kA3TableAt + 256u * kEntries;
     static constexpr uint32_t kBarAt = kMergeAt + 4u * kWarps * kHeads * kA3MergeStride;
@@ -357,20 +357,21 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     return v;
 }
 
-// Lookup address of pair q (stream order) of a packed field held in words w:
-// the pair's 2*BITS bits land in bits 8.. of `slot` (table base + column).
-template <int BITS>
-__device__ __forceinline__ uint32_t pair_addr(const uint32_t* w, int q, uint32_t slot) {
-    if constexpr (BITS == 4) {
-        return __byte_perm(w[q >> 2], slot, 0x7604u | ((uint32_t)(q & 3) << 4));
-    } else {
-        constexpr int PB = 2 * BITS;
-        const int o = q * PB, i = o >> 5, r = o & 31;
-        uint32_t x;
-        if (r + PB <= 32) x = r >= 8 ? (w[i] >> (r - 8)) : (w[i] << (8 - r));
-        else x = __funnelshift_r(w[i], w[i + 1], r - 8);
-        return (x & (((1u << PB) - 1u) << 8)) | slot;
-    }
+// Lookup address of pair q (stream order) of a packed field held in the NW
+// words w: the byte holding the pair's first bit -- of w itself, or of w
+// shifted right by the pair's bit offset within a byte -- lands in bits
+// 8..15 of `slot` (table base + column) by one byte permute.  The table has
+// 256 rows and row e holds the pair e mod 2^(2 BITS), so the bits of the next
+// pair that share the byte do not matter.  Shifted words with the same
+// (offset, word) are common subexpressions across q.
+template <int BITS, int NW>
+__device__ __forceinline__ uint32_t pair_addr(const uint32_t (&w)[NW], int q, uint32_t slot) {
+    const int o = q * 2 * BITS, sh = o & 7, byte = o >> 3, wi = byte >> 2, bi = byte & 3;
+    uint32_t x;
+    if (sh == 0) x = w[wi];
+    else if (wi + 1 < NW) x = __funnelshift_r(w[wi], w[wi + 1], sh);
+    else x = w[wi] >> sh;
+    return __byte_perm(x, slot, 0x7604u | ((uint32_t)bi << 4));
 }
 
 // The 32 dims 32t..32t+31 of a K row (KB words).
@@ -465,15 +466,11 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 
     // ---- pair tables (K columns, V columns) and the per-warp barriers
     {
-        constexpr int NK = 1 << (2 * KB), NV = 1 << (2 * VB), MK = (1 << KB) - 1, MV = (1 << VB) - 1;
+        constexpr int MK = (1 << KB) - 1, MV = (1 << VB) - 1;
         for (int i = threadIdx.x; i < L::kEntries * 64; i += T) {
-            const int e = i >> 6, s = i & 63;
-            uint32_t v = 0u;
-            if (s < 32) {
-                if (e < NK) v = h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK]);
-            } else if (e < NV) {
-                v = h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
-            }
+            const int e = i >> 6, s = i & 63;  // row e holds the pair e mod 2^(2 bits)
+            const uint32_t v = s < 32 ? h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK])
+                                      : h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
             *reinterpret_cast<uint32_t*>(gptr(kA3TableAt + 256u * e + 4u * s)) = v;
         }
     }
