@@ -460,6 +460,56 @@ def extra_long_context(peak):
     return res
 
 
+def extra_paged(peak):
+    """Paged cache with a length per sequence (serving-style decode): batch 32,
+    32 query / 8 KV heads, d 128, K4/V3, pages of 256 positions in a shuffled
+    order, lengths drawn uniformly from [1, 32768] (seeded); the rows are
+    low-rank + diag like the prefill, encoded into the pages by tq_encode.
+    Reported against the bytes of the positions actually attended."""
+    import torch
+    from kv_cache_vector_gb300 import abi, synth
+    B, Hq, Hkv, page, kb, vb, max_ctx = 32, 32, 8, 256, 4, 3, 32768
+    g = torch.Generator().manual_seed(77)
+    lens = torch.randint(1, max_ctx + 1, (B,), generator=g, dtype=torch.int32)
+    need = [-(-int(l) // page) for l in lens]
+    max_pages = max_ctx // page
+    n_pages = sum(need)
+    perm = torch.randperm(n_pages, generator=g)
+    bt = torch.full((B, max_pages), -1, dtype=torch.int32)
+    k = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[k:k + need[b]].to(torch.int32)
+        k += need[b]
+    plan = abi.Plan(D, 42)
+    cache = abi.PagedCache.empty(n_pages, Hkv, page, D, kb, vb)
+    rows = n_pages * Hkv * page
+    for side, bits, pk, nm, stream in (("k", kb, cache.k_packed, cache.k_norm, 30000),
+                                       ("v", vb, cache.v_packed, cache.v_norm, 31000)):
+        for i0 in range(0, rows, 1 << 22):
+            i1 = min(rows, i0 + (1 << 22))
+            x = synth.lowrank_rows(91, i1 - i0, D, stream=stream + i0 // (1 << 22), device="cuda")
+            abi.tq_encode(plan, bits, x, pk.view(-1, D * bits // 8)[i0:i1], nm.view(-1)[i0:i1])
+    q = synth.device_normal(92, (B, Hq, D))
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(abi.tq_attn_paged_workspace_bytes(B, Hq, Hkv, D, max_ctx), dtype=torch.uint8, device="cuda")
+    bt_d, lens_d = bt.cuda(), lens.cuda()
+
+    def call():
+        abi.tq_attn_decode_paged(plan, q, cache, bt_d, lens_d, max_ctx, 1.0 / math.sqrt(D), 0.0,
+                                 out=out, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    us = time_events(call, 20) * 1e3
+    nbytes = int(lens.sum()) * Hkv * (D * (kb + vb) // 8 + 8)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "positions": int(lens.sum()),
+            "config": f"B{B} Hq{Hq}/Hkv{Hkv} d128 K{kb}/V{vb}, pages of {page}, lengths uniform in [1, {max_ctx}] "
+                      f"(seeded; mean {float(lens.float().mean()):.0f}), low-rank+diag rows"}
+
+
 def extra_gemma(peak):
     """34 layers x 4 KV heads x d 256 x 512 tokens bf16 N(0,1), K4/V4: window
     encode GB/s (L2 flushed), then the append-only decode step: one tq_append
@@ -655,6 +705,7 @@ def main():
         torch.cuda.empty_cache()
         out["long_context"] = extra_long_context(peak)
         out["gemma_cache"] = extra_gemma(peak)
+        out["paged_varlen"] = extra_paged(peak)
     print(json.dumps(out))
     barrier(world)
 

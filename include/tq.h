@@ -135,6 +135,11 @@ tq_status tq_append(const tq_plan *plan, int k_bits, int v_bits, const void *k_n
  * (split-K partials).  0 for invalid sizes. */
 size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len);
 
+/* Workspace bytes tq_attn_decode_paged needs for these sizes on the current
+ * device (split-K partials and the work partition).  0 for invalid sizes or
+ * d != 128. */
+size_t tq_attn_paged_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t max_ctx);
+
 /* Decode attention over the packed cache, one query token per sequence
  * ("TurboQuant KV Cache Compression -- Spec", fa_tq_attention_cached and
  * Optimization: Fused dequant-dot; "CITATIONS", Sparse V dequant and
@@ -188,6 +193,61 @@ tq_status tq_attn_decode_noalloc(const tq_plan *plan, const void *q, int B, int 
                                  tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
                                  float scale, float sparse_v_threshold, float *out,
                                  tq_stream_t stream);
+
+/* One layer of a paged KV cache ("CITATIONS" (Atlas), N(0, 1/d) codebook
+ * replacement and Sparse V dequant: the paged write path and the
+ * paged_decode_attn kernels; "TurboQuant KV Cache Compression -- Spec", API:
+ * fa_tq_attention_cached).  Fixed-size pages of page_size positions, each page
+ * holding every KV head, caller-owned device memory:
+ *   k_packed [n_pages][Hkv][page_size][d*k_bits/8]   k_norm [n_pages][Hkv][page_size]
+ *   v_packed [n_pages][Hkv][page_size][d*v_bits/8]   v_norm [n_pages][Hkv][page_size]
+ * Sequence b keeps position p at offset p % page_size of page
+ * block_table[b * max_pages + p / page_size] (int32 on the device).  page_size
+ * is a power of two, at least 32. */
+typedef struct {
+    uint8_t *k_packed;
+    float *k_norm;
+    uint8_t *v_packed;
+    float *v_norm;
+    int64_t n_pages;
+    int32_t page_size;
+} tq_paged_cache;
+
+/* Append one new token per sequence to a paged cache: the pages' write path
+ * (quantize into the cache) with the row codec of tq_encode.
+ *   k_new, v_new: [B][Hkv][d] (dtype), device
+ *   block_table:  [B][max_pages] int32 page ids, device
+ *   positions:    [B] int32, device: the position written for sequence b
+ * The rows land at positions[b] of every KV head of sequence b.  Positions and
+ * page ids are read on the device: a position outside [0, max_pages *
+ * page_size) or a page id outside [0, n_pages) writes nothing for that
+ * sequence and sets the device status word (tq_device_status) to 42.
+ * d >= 32.  Errors: TQ_ERR_UNSUPPORTED (d < 32, page_size not a power of two
+ * >= 32, bits, dtype), TQ_ERR_INVALID_ARG, TQ_ERR_ALIGNMENT. */
+tq_status tq_append_paged(const tq_plan *plan, int k_bits, int v_bits, const void *k_new,
+                          const void *v_new, tq_dtype dtype, int B, int Hkv, tq_paged_cache cache,
+                          const int32_t *block_table, int max_pages, const int32_t *positions,
+                          tq_stream_t stream);
+
+/* Decode attention over a paged cache with a context length per sequence:
+ * for sequence b and query head h, the tq_attn_decode result over positions
+ * [0, min(ctx_lens[b], max_ctx)) of sequence b (an empty context gives a zero
+ * output row).  d = 128 only.
+ *   q:   [B][Hq][d] bf16, device;  out: [B][Hq][d] fp32, device
+ *   block_table: [B][max_pages] int32, device;  ctx_lens: [B] int32, device
+ *   max_ctx: an upper bound of the lengths, <= max_pages * page_size; it sizes
+ *     the split-K geometry: the workspace is
+ *     tq_attn_paged_workspace_bytes(B, Hq, Hkv, 128, max_ctx) bytes.
+ * A page id outside [0, n_pages) is not read; the device status word is set
+ * to 33 and that chunk's result is undefined.
+ * Errors: as tq_attn_decode; TQ_ERR_UNSUPPORTED also for d != 128 or a
+ * page_size that is not a power of two >= 32; TQ_ERR_RANGE if max_ctx < 1 or
+ * max_ctx > max_pages * page_size. */
+tq_status tq_attn_decode_paged(const tq_plan *plan, const void *q, int B, int Hq, int Hkv,
+                               tq_paged_cache cache, const int32_t *block_table, int max_pages,
+                               const int32_t *ctx_lens, int64_t max_ctx, int k_bits, int v_bits,
+                               float scale, float sparse_v_threshold, float *out, void *workspace,
+                               size_t workspace_bytes, tq_stream_t stream);
 
 /* Text for a status code (static storage). */
 const char *tq_status_string(tq_status status);

@@ -24,9 +24,9 @@ STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_E
 
 # every symbol include/tq.h declares
 EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_signs",
-           "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes",
+           "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes", "tq_attn_paged_workspace_bytes",
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
-           "tq_attn_decode_noalloc")
+           "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged")
 
 
 class TQError(RuntimeError):
@@ -43,6 +43,12 @@ class CacheView(ctypes.Structure):
     _fields_ = [("k_packed", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
                 ("v_packed", ctypes.c_void_p), ("v_norm", ctypes.c_void_p),
                 ("cap", ctypes.c_int64)]
+
+
+class PagedCacheView(ctypes.Structure):
+    _fields_ = [("k_packed", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+                ("v_packed", ctypes.c_void_p), ("v_norm", ctypes.c_void_p),
+                ("n_pages", ctypes.c_int64), ("page_size", ctypes.c_int32)]
 
 
 @lru_cache(maxsize=1)
@@ -63,10 +69,14 @@ def lib() -> ctypes.CDLL:
         ("tq_decode", i32, [vp, i32, vp, vp, i64, vp, i32, vp]),
         ("tq_append", i32, [vp, i32, i32, vp, vp, i32, i32, i32, i64, CacheView, i64, vp]),
         ("tq_attn_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32, i64]),
+        ("tq_attn_paged_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32, i64]),
         ("tq_attn_decode", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32, vp, vp,
                                  ctypes.c_size_t, vp]),
         ("tq_attn_decode_noalloc", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32,
                                          vp, vp]),
+        ("tq_append_paged", i32, [vp, i32, i32, vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, vp]),
+        ("tq_attn_decode_paged", i32, [vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, i64, i32, i32,
+                                       f32, f32, vp, vp, ctypes.c_size_t, vp]),
         ("tq_status_string", ctypes.c_char_p, [i32]),
         ("tq_last_cuda_error", i32, []),
         ("tq_device_status", i32, [i32, ctypes.POINTER(i32)]),
@@ -211,6 +221,10 @@ def tq_attn_workspace_bytes(B: int, Hq: int, Hkv: int, d: int, ctx_len: int) -> 
     return int(lib().tq_attn_workspace_bytes(B, Hq, Hkv, d, ctx_len))
 
 
+def tq_attn_paged_workspace_bytes(B: int, Hq: int, Hkv: int, d: int, max_ctx: int) -> int:
+    return int(lib().tq_attn_paged_workspace_bytes(B, Hq, Hkv, d, max_ctx))
+
+
 def tq_attn_decode(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scale: float,
                    sparse_v_threshold: float = 0.0, out: torch.Tensor | None = None,
                    workspace: torch.Tensor | None = None) -> torch.Tensor:
@@ -250,6 +264,90 @@ def tq_attn_decode_noalloc(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: i
     _check("tq_attn_decode_noalloc", lib().tq_attn_decode_noalloc(
         plan.handle, q.data_ptr(), B, Hq, Hkv, cache.view(), ctx_len, cache.k_bits, cache.v_bits,
         ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(), _stream(q)))
+    return out
+
+
+@dataclass
+class PagedCache:
+    """One layer of a paged KV cache (caller-owned device tensors): pages of
+    page_size positions, each holding every KV head."""
+    k_packed: torch.Tensor  # [n_pages, Hkv, page_size, d*kb/8] uint8
+    k_norm: torch.Tensor    # [n_pages, Hkv, page_size] fp32
+    v_packed: torch.Tensor  # [n_pages, Hkv, page_size, d*vb/8] uint8
+    v_norm: torch.Tensor    # [n_pages, Hkv, page_size] fp32
+    k_bits: int
+    v_bits: int
+
+    @staticmethod
+    def empty(n_pages, Hkv, page_size, d, k_bits, v_bits, device="cuda"):
+        return PagedCache(
+            torch.zeros(n_pages, Hkv, page_size, d * k_bits // 8, dtype=torch.uint8, device=device),
+            torch.zeros(n_pages, Hkv, page_size, dtype=torch.float32, device=device),
+            torch.zeros(n_pages, Hkv, page_size, d * v_bits // 8, dtype=torch.uint8, device=device),
+            torch.zeros(n_pages, Hkv, page_size, dtype=torch.float32, device=device), k_bits, v_bits)
+
+    @property
+    def n_pages(self) -> int:
+        return self.k_norm.shape[0]
+
+    @property
+    def Hkv(self) -> int:
+        return self.k_norm.shape[1]
+
+    @property
+    def page_size(self) -> int:
+        return self.k_norm.shape[2]
+
+    def view(self) -> PagedCacheView:
+        _cuda(self.k_packed, self.k_norm, self.v_packed, self.v_norm)
+        return PagedCacheView(self.k_packed.data_ptr(), self.k_norm.data_ptr(), self.v_packed.data_ptr(),
+                              self.v_norm.data_ptr(), self.n_pages, self.page_size)
+
+
+def _i32(t: torch.Tensor, name: str):
+    _cuda(t)
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+
+
+def tq_append_paged(plan: Plan, cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                    block_table: torch.Tensor, positions: torch.Tensor):
+    """k_new, v_new: [B, Hkv, d] fp32/bf16; block_table [B, max_pages] int32;
+    positions [B] int32: row (b, h) goes to position positions[b] of sequence b."""
+    B, Hkv, d = k_new.shape
+    if v_new.shape != k_new.shape or v_new.dtype != k_new.dtype or d != plan.d or Hkv != cache.Hkv:
+        raise ValueError("k_new / v_new must both be [B, Hkv, d] of one dtype")
+    _cuda(k_new, v_new)
+    _i32(block_table, "block_table")
+    _i32(positions, "positions")
+    _check("tq_append_paged", lib().tq_append_paged(
+        plan.handle, cache.k_bits, cache.v_bits, k_new.data_ptr(), v_new.data_ptr(), _dt(k_new), B, Hkv,
+        cache.view(), block_table.data_ptr(), block_table.shape[1], positions.data_ptr(), _stream(k_new)))
+
+
+def tq_attn_decode_paged(plan: Plan, q: torch.Tensor, cache: PagedCache, block_table: torch.Tensor,
+                         ctx_lens: torch.Tensor, max_ctx: int, scale: float,
+                         sparse_v_threshold: float = 0.0, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """q: [B, Hq, d] bf16; block_table [B, max_pages] int32; ctx_lens [B] int32
+    (each at most max_ctx) -> out [B, Hq, d] fp32."""
+    B, Hq, d = q.shape
+    Hkv = cache.Hkv
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    need = tq_attn_paged_workspace_bytes(B, Hq, Hkv, d, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(q, out, workspace)
+    _i32(block_table, "block_table")
+    _i32(ctx_lens, "ctx_lens")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    _check("tq_attn_decode_paged", lib().tq_attn_decode_paged(
+        plan.handle, q.data_ptr(), B, Hq, Hkv, cache.view(), block_table.data_ptr(), block_table.shape[1],
+        ctx_lens.data_ptr(), max_ctx, cache.k_bits, cache.v_bits, ctypes.c_float(scale),
+        ctypes.c_float(sparse_v_threshold), out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+        _stream(q)))
     return out
 
 

@@ -1,6 +1,7 @@
 // tq_api.cpp -- the C ABI: plan construction (codebooks, signs), argument
 // validation, and dispatch to the sm_103a kernels.  See include/tq.h.
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <limits>
@@ -399,6 +400,11 @@ size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
     return tq::attn_workspace_bound(B, Hq, Hkv, ctx_len, tq::num_sms(), d);
 }
 
+size_t tq_attn_paged_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t max_ctx) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_ctx < 1 || d != 128) return 0;
+    return tq::attn_paged_workspace_bound(B, Hq, Hkv, max_ctx, tq::num_sms());
+}
+
 tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
                          tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
                          float scale, float sparse_v_threshold, float* out, void* workspace,
@@ -437,6 +443,107 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
             default: return tq::launch_attn_dk<d, 4>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
         }
     });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------ paged cache
+
+namespace {
+// page_size a power of two >= 32: its log2, else -1.
+int page_shift_of(int32_t page_size) {
+    if (page_size < 32 || (page_size & (page_size - 1)) != 0) return -1;
+    int sh = 0;
+    while ((1 << sh) < page_size) ++sh;
+    return sh;
+}
+bool paged_pointers_ok(const tq_paged_cache& c) {
+    return c.k_packed && c.k_norm && c.v_packed && c.v_norm;
+}
+bool paged_aligned(const tq_paged_cache& c) {
+    return aligned16(c.k_packed) && aligned16(c.v_packed) && aligned4(c.k_norm) && aligned4(c.v_norm);
+}
+bool paged_accessible(const tq_paged_cache& c) {
+    return device_accessible(c.k_packed) && device_accessible(c.v_packed) &&
+           device_accessible(c.k_norm) && device_accessible(c.v_norm);
+}
+tq_cache_view paged_as_view(const tq_paged_cache& c) {
+    tq_cache_view v;
+    v.k_packed = c.k_packed;
+    v.k_norm = c.k_norm;
+    v.v_packed = c.v_packed;
+    v.v_norm = c.v_norm;
+    v.cap = 0;  // unused on the paged paths
+    return v;
+}
+}  // namespace
+
+tq_status tq_append_paged(const tq_plan* plan, int k_bits, int v_bits, const void* k_new,
+                          const void* v_new, tq_dtype dtype, int B, int Hkv, tq_paged_cache cache,
+                          const int32_t* block_table, int max_pages, const int32_t* positions,
+                          tq_stream_t stream) {
+    if (!plan || B < 0 || Hkv <= 0 || max_pages < 1 || cache.n_pages < 1) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits) || !valid_dtype(dtype)) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    const int shift = page_shift_of(cache.page_size);
+    if (P->d < 32 || shift < 0) return TQ_ERR_UNSUPPORTED;
+    if (B == 0) return TQ_OK;
+    if (!k_new || !v_new || !block_table || !positions || !paged_pointers_ok(cache)) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned4(block_table) || !aligned4(positions) ||
+        !paged_aligned(cache))
+        return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(k_new) || !device_accessible(v_new) || !device_accessible(block_table) ||
+        !device_accessible(positions) || !paged_accessible(cache))
+        return TQ_ERR_INVALID_ARG;
+    tq::RowParams PK, PV;
+    fill_row_params(*P, k_bits, PK);
+    fill_row_params(*P, v_bits, PV);
+    const tq::PagedArgs pa{block_table, positions, cache.n_pages, max_pages, shift};
+    const tq_cache_view view = paged_as_view(cache);
+    cudaError_t e = dispatch_d(P->d, [&](auto D) {
+        return tq::launch_append_paged_d<decltype(D)::value>(k_bits, v_bits, dtype, k_new, v_new, B, Hkv,
+                                                             view, pa, PK, PV,
+                                                             reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_attn_decode_paged(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                               tq_paged_cache cache, const int32_t* block_table, int max_pages,
+                               const int32_t* ctx_lens, int64_t max_ctx, int k_bits, int v_bits,
+                               float scale, float sparse_v_threshold, float* out, void* workspace,
+                               size_t workspace_bytes, tq_stream_t stream) {
+    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages < 1 || cache.n_pages < 1)
+        return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits) || Hq / Hkv > 8) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    const int shift = page_shift_of(cache.page_size);
+    if (P->d != 128 || shift < 0) return TQ_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
+        return TQ_ERR_INVALID_ARG;
+    if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
+    if (B == 0) return TQ_OK;
+    if (!q || !out || !block_table || !ctx_lens || !paged_pointers_ok(cache)) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned4(block_table) || !aligned4(ctx_lens) ||
+        !paged_aligned(cache))
+        return TQ_ERR_ALIGNMENT;
+    tq::AttnGeometry g = tq::attn_geometry_paged(B, Hq, Hkv, max_ctx, tq::num_sms(), k_bits, v_bits);
+    if ((int64_t)B * Hkv * g.n_splits > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // work items are int32
+    if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(workspace) ||
+        !device_accessible(block_table) || !device_accessible(ctx_lens) || !paged_accessible(cache))
+        return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
+    const tq::PagedArgs pa{block_table, ctx_lens, cache.n_pages, max_pages, shift};
+    const tq_cache_view view = paged_as_view(cache);
+    auto st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (k_bits) {
+        case 2: e = tq::launch_attn128_paged<2>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st); break;
+        case 3: e = tq::launch_attn128_paged<3>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st); break;
+        default: e = tq::launch_attn128_paged<4>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st); break;
+    }
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

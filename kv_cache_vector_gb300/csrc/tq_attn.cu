@@ -253,16 +253,18 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
 // the query and 1/s_v into the output.  Query heads go in groups of four:
 // NG = 1 for G <= 4, NG = 2 for G <= 8.
 //
-// Data movement: CTAs of kAttn3Warps warps take contiguous ranges of work
-// items (batch, KV head, segment of kAttn3Warps * warp_len positions); warp w
-// takes positions [w * warp_len, (w + 1) * warp_len) of each segment, in
-// chunks of 32.  A warp streams its own chunks through a 3-stage ring in
+// Data movement: CTAs of W warps take contiguous ranges of work items
+// (batch, KV head, segment of W * warp_len positions); the segment is cut
+// into chunks of 32 positions and warp w takes chunks w, w + W, w + 2W, ...,
+// so the rows of a segment that a sequence fills spread evenly over the
+// warps.  A warp streams its own chunks through a ring of 2 or 3 stages in
 // shared memory: one lane issues 1-D bulk copies (cp.async.bulk) of the
 // chunk's packed K and V rows, each lane copies the two norms of one
 // position (cp.async, 4 bytes), and one mbarrier per stage completes when
-// all of it has landed.  At the end of an item the warps merge their
-// partials through shared memory and write one partial (acc[128], m, l) per
-// query head; k_attn3_combine merges the items of a (batch, head).
+// all of it has landed.  When the (batch, KV head) of the items changes and
+// at the end of the range, the warps merge their partials through shared
+// memory and write one partial (acc[128], m, l) per query head;
+// k_attn3_combine merges a (batch, head)'s partials.
 
 constexpr int kA3Chunk = 32;
 constexpr int kA3MergeStride = 132;  // floats per (warp, head) row of the merge buffer
@@ -276,6 +278,7 @@ constexpr uint32_t kA3TableAt = kAttn3TableAt;
 // Device status codes.
 constexpr int kA3StatusWait = 31;    // a ring stage did not complete within the bound
 constexpr int kA3StatusLayout = 32;  // dynamic shared memory starts above kA3RingAt
+constexpr int kA3StatusPage = 33;    // a paged cache's block table names a page out of range
 
 // Warps and ring stages per CTA (attn3_warps, attn3_stages): up to 16 x 2
 // for up to four query heads per KV head, 8 x 3 for up to eight.
@@ -448,11 +451,176 @@ static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __r
     if (j == 0) qexp[bh] = ldexpf(1.f, e);
 }
 
-template <int KB, int VB, int NG>
+// Work partition of the paged kernel (written by k_attn3_plan): CTA c takes
+// items [cta_begin[c], cta_begin[c + 1]); slot_base[c] counts the CTAs before
+// c that take any item; c0 / clast hold the first and last CTA taking items
+// of each (batch, KV head).
+struct A3Meta {
+    int32_t* cta_begin;
+    int32_t* slot_base;
+    int32_t* c0;
+    int32_t* clast;
+};
+// Weights of the work partition, in rows of the busiest warp: an item that
+// holds rows costs its busiest warp's rows plus kA3ItemCost, an empty item
+// kA3EmptyCost (the consumer steps over it), and the first item of a
+// (batch, KV head) also kA3RunCost (merging the warps' partials and loading
+// the query).
+constexpr int kA3ItemCost = 4;
+constexpr int kA3EmptyCost = 1;
+constexpr int kA3RunCost = 32;
+constexpr int kA3PlanSmemPairs = 8192;  // pair prefixes kept in shared memory up to this count
+
+// Block-wide inclusive scan over 1024 threads; `total` gets the sum.
+__device__ __forceinline__ int64_t block1024_scan(int64_t v, int64_t* wsum, int64_t& total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) wsum[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        int64_t x = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += t;
+        }
+        wsum[lane] = x;
+    }
+    __syncthreads();
+    const int64_t r = v + (wid > 0 ? wsum[wid - 1] : 0);
+    total = wsum[31];
+    __syncthreads();
+    return r;
+}
+
+// The items of one (batch, KV head) with L rows, in split order: nf full
+// segments, then a partial one of r rows if r > 0, then empty ones.
+struct A3PairCost {
+    int64_t nf, wf, wp;
+    int has_p;
+    __device__ A3PairCost(int64_t L, int64_t seg, int W, int nC) {
+        nf = L / seg;
+        const int64_t r = L - nf * seg;
+        has_p = r > 0;
+        wf = (int64_t)nC * kA3Chunk + kA3ItemCost;
+        const int64_t f = (r + kA3Chunk - 1) / kA3Chunk;
+        wp = (f + W - 1) / W * kA3Chunk + kA3ItemCost;
+    }
+    // weight of items [0, j)
+    __device__ int64_t before(int64_t j) const {
+        if (j <= 0) return 0;
+        int64_t e = kA3RunCost + (j < nf ? j : nf) * wf;
+        if (j > nf && has_p) e += wp;
+        const int64_t ne = j - nf - has_p;
+        if (ne > 0) e += ne * kA3EmptyCost;
+        return e;
+    }
+};
+
+// One block of 1024 threads.  The W warps of a CTA share each item's chunks
+// round robin, so the warp with the most chunks (warp 0) sets the CTA's time
+// and the items are weighed in its rows (A3PairCost).  Items are cut into
+// `grid` contiguous ranges of about equal weight: item i goes to CTA
+// floor(P_i grid / total), P_i the weight of the items before it, so CTA c
+// starts at the first item with P_i >= ceil(c total / grid), found by a
+// binary search over the pairs' prefix weights and one within the pair.  A
+// CTA's range thus runs through consecutive splits of one (batch, KV head)
+// at a time.
+static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __restrict__ lens, int Hkv,
+                                                            int n_splits, int64_t seg, int warp_len,
+                                                            int64_t max_ctx, int n_pairs, int grid, A3Meta m) {
+    extern __shared__ __align__(16) unsigned char plan_smem[];
+    __shared__ int64_t wsum[32];
+    __shared__ int32_t cb[1025];
+    const int tid = threadIdx.x;
+    const int W = (int)(seg / warp_len), nC = warp_len / kA3Chunk;
+    // exclusive prefix weight of each pair: shared memory, or the c0/clast
+    // area of the workspace (8 bytes per pair fit in its 8 bytes per query head)
+    int64_t* pre = n_pairs <= kA3PlanSmemPairs ? reinterpret_cast<int64_t*>(plan_smem)
+                                               : reinterpret_cast<int64_t*>(m.c0);
+    auto pair_len = [&](int bh) {
+        int64_t L = __ldg(lens + bh / Hkv);
+        return L < 0 ? 0 : (L > max_ctx ? max_ctx : L);
+    };
+    int64_t carry = 0;
+    for (int base = 0; base < n_pairs; base += 1024) {
+        const int bh = base + tid;
+        const int64_t w = bh < n_pairs ? A3PairCost(pair_len(bh), seg, W, nC).before(n_splits) : 0;
+        int64_t chunk_total;
+        const int64_t incl = block1024_scan(w, wsum, chunk_total);
+        if (bh < n_pairs) pre[bh] = carry + incl - w;
+        carry += chunk_total;
+    }
+    const int64_t total = carry;
+    __syncthreads();
+    // CTA c's first item
+    const int64_t n_items = (int64_t)n_pairs * n_splits;
+    if (tid <= grid) {
+        int64_t first;
+        if (tid == 0) {
+            first = 0;
+        } else if (tid == grid) {
+            first = n_items;
+        } else {
+            const int64_t t = ((int64_t)tid * total + grid - 1) / grid;  // ceil(c total / grid) > 0
+            // the last pair whose prefix is below t (pair 0's is 0 < t)
+            int lo = 0, hi = n_pairs;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (pre[mid] < t) lo = mid;
+                else hi = mid;
+            }
+            const A3PairCost pc(pair_len(lo), seg, W, nC);
+            const int64_t need = t - pre[lo];
+            // the first split j in [1, n_splits] with before(j) >= need; n_splits: the next pair's item 0
+            int64_t jl = 0, jh = n_splits;  // before(jl) < need <= before(jh) or jh = n_splits
+            while (jh - jl > 1) {
+                const int64_t mid = (jl + jh) >> 1;
+                if (pc.before(mid) < need) jl = mid;
+                else jh = mid;
+            }
+            first = (int64_t)lo * n_splits + jh;
+        }
+        cb[tid] = (int32_t)first;
+        m.cta_begin[tid] = (int32_t)first;
+    }
+    __syncthreads();
+    // slot bases: a dense numbering of the CTAs that take items
+    {
+        const int64_t ne = tid < grid ? (cb[tid + 1] > cb[tid] ? 1 : 0) : 0;
+        int64_t tot;
+        const int64_t incl = block1024_scan(ne, wsum, tot);
+        if (tid <= grid) m.slot_base[tid] = (int32_t)(incl - ne);
+    }
+    // first and last CTA of each pair: the last CTA whose range starts at or before the item
+    auto cta_of = [&](int64_t item) {
+        int lo = 0, hi = grid;  // cb[lo] <= item < cb[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cb[mid] <= item) lo = mid;
+            else hi = mid;
+        }
+        return lo;
+    };
+    for (int bh = tid; bh < n_pairs; bh += 1024) {
+        const int a = cta_of((int64_t)bh * n_splits), z = cta_of((int64_t)bh * n_splits + n_splits - 1);
+        m.c0[bh] = a;
+        m.clast[bh] = z;
+    }
+}
+
+// PAGED: the cache is paged (PagedArgs), each sequence attends over its own
+// length (at most ctx_len) and CTA ranges come from k_attn3_plan; otherwise
+// rows are [B][Hkv][cap], every sequence attends over ctx_len and CTA c takes
+// items [n_items c / grid, n_items (c + 1) / grid).
+template <int KB, int VB, int NG, bool PAGED>
 __global__ void __launch_bounds__(A3Shape<KB, VB, NG>::kThreads, 1)
 k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv,
               tq_cache_view cache, int64_t ctx_len, int warp_len, int n_splits, int64_t n_items,
-              float* __restrict__ part, int* status, const __grid_constant__ AttnParams P) {
+              float* __restrict__ part, int* status, const __grid_constant__ AttnParams P,
+              const PagedArgs pa, const A3Meta meta) {
     using L = A3Layout<KB, VB, NG>;
     constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG>::kThreads;
     constexpr uint32_t kAll = 0xFFFFFFFFu;
@@ -487,57 +655,110 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     const uint32_t kslot = kA3TableAt + 4u * lane, vslot = kslot + 128u;
     const uint32_t ring = kA3RingAt + (uint32_t)(warp * S * L::kStage);
     float* merge = reinterpret_cast<float*>(gptr(L::kMergeAt));
-    const int64_t i_begin = n_items * blockIdx.x / gridDim.x;
-    const int64_t i_end = n_items * (blockIdx.x + 1) / gridDim.x;
+    const int64_t i_begin = PAGED ? (int64_t)meta.cta_begin[blockIdx.x] : n_items * blockIdx.x / gridDim.x;
+    const int64_t i_end = PAGED ? (int64_t)meta.cta_begin[blockIdx.x + 1] : n_items * (blockIdx.x + 1) / gridDim.x;
     const int nC = warp_len / kA3Chunk;
     const int64_t seg = (int64_t)W * warp_len;
-    const int64_t wofs = (int64_t)warp * warp_len;
+    const int64_t wofs = (int64_t)warp * kA3Chunk;  // first chunk of the warp in a segment
+    constexpr int kStride = W * kA3Chunk;             // from one of its chunks to the next
     bool bad = false;  // warp-uniform: a wait gave up; compute is skipped from then on
+    int inflight = 0;  // stages issued and not yet waited for
 
-    // Producer cursor: the next chunk to copy, kept S chunks ahead of the
-    // consumer; position and cache row advance by additions.
+    // Producer cursor: the next chunk slot to look at.  Only slots that hold
+    // rows of the sequence go through the ring: the consumer computes the
+    // same row counts, so both sides skip the empty slots and take stages and
+    // phases in the same order, and the producer stays S non-empty slots
+    // ahead.  Position and cache row advance by additions.
     int64_t p_item = i_begin, p_bh = i_begin / n_splits;
     int p_c = 0, p_split = (int)(i_begin % n_splits), p_st = 0;
     int64_t p_pos = (int64_t)p_split * seg + wofs;
     int64_t p_row = p_bh * cache.cap + p_pos;
-    auto issue_next = [&]() {
-        if (p_item >= i_end || bad) return;
-        const int64_t rem = ctx_len - p_pos;
-        const int n = rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
+    // paged: the sequence, head and context length of p_bh, cached per pair
+    int64_t p_ctx = ctx_len, p_cbh = -1, p_b = 0;
+    int p_h = 0;
+    auto next_item = [&]() {
+        p_c = 0;
+        ++p_item;
+        if (++p_split == n_splits) {
+            p_split = 0;
+            ++p_bh;
+        }
+        p_pos = (int64_t)p_split * seg + wofs;
+        p_row = p_bh * cache.cap + p_pos;
+    };
+    // seek() moves the cursor to the next slot that holds rows (or to the end
+    // of the range), finds its row count and, paged, loads its page id.  It
+    // runs before the consumer works on its current chunk and the page id is
+    // first used in issue(), after that work, so the load's latency is hidden.
+    int q_n = 0;  // rows of the slot found
+    int q_page = 0;
+    auto seek = [&]() {
+        q_n = 0;
+        while (p_item < i_end && !bad) {
+            if constexpr (PAGED) {
+                if (p_bh != p_cbh) {
+                    p_cbh = p_bh;
+                    p_b = p_bh / Hkv;
+                    p_h = (int)(p_bh - p_b * Hkv);
+                    const int64_t len = __ldg(pa.lens + p_b);
+                    p_ctx = len < 0 ? 0 : (len < ctx_len ? len : ctx_len);
+                }
+            }
+            const int64_t rem = p_ctx - p_pos;
+            if (rem <= 0) {  // the item's later slots of this warp lie further out
+                next_item();
+                continue;
+            }
+            q_n = rem >= kA3Chunk ? kA3Chunk : (int)rem;
+            if constexpr (PAGED) q_page = __ldg(pa.bt + p_b * pa.max_pages + (p_pos >> pa.page_shift));
+            return;
+        }
+    };
+    auto issue = [&]() {
+        if (q_n == 0 || bad) return;
+        const int n = q_n;
+        int64_t row = p_row;
+        bool ok = true;
+        if constexpr (PAGED) {
+            if (q_page < 0 || q_page >= pa.n_pages) {
+                if (lane == 0) report_timeout(status, kA3StatusPage);
+                ok = false;
+            } else {
+                row = (((int64_t)q_page * Hkv + p_h) << pa.page_shift) + (p_pos & ((int64_t(1) << pa.page_shift) - 1));
+            }
+        }
         uint64_t* bar = bars + p_st;
         const uint32_t sb = ring + (uint32_t)(p_st * L::kStage);
-        if (n > 0) {
+        if (ok) {
             if (lane == 0) {
                 fence_async_smem();  // earlier generic reads of this stage come first
                 mbar_expect_tx(bar, (uint32_t)(n * (L::kKRow + L::kVRow)));
-                bulk_load(sb, cache.k_packed + p_row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
-                bulk_load(sb + L::kVOff, cache.v_packed + p_row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
+                bulk_load(sb, cache.k_packed + row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
+                bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
             }
             // lanes past the end copy nothing (source size 0) from a valid row
-            const int64_t r = p_row + (lane < n ? lane : n - 1);
+            const int64_t r = row + (lane < n ? lane : n - 1);
             const uint32_t sz = lane < n ? 4u : 0u;
             cp_async4(sb + L::kKnOff + 4u * lane, cache.k_norm + r, sz);
             cp_async4(sb + L::kVnOff + 4u * lane, cache.v_norm + r, sz);
             cp_async_arrive(bar);
         } else {
-            mbar_arrive(bar);
+            mbar_arrive(bar);  // a bad page: nothing is copied, the chunk's result is undefined
         }
         if (++p_c == nC) {
-            p_c = 0;
-            ++p_item;
-            if (++p_split == n_splits) {
-                p_split = 0;
-                ++p_bh;
-            }
-            p_pos = (int64_t)p_split * seg + wofs;
-            p_row = p_bh * cache.cap + p_pos;
+            next_item();
         } else {
-            p_pos += kA3Chunk;
-            p_row += kA3Chunk;
+            p_pos += kStride;
+            p_row += kStride;
         }
         if (++p_st == S) p_st = 0;
+        ++inflight;
+        q_n = 0;
     };
-    for (int i = 0; i < S; ++i) issue_next();
+    for (int i = 0; i < S; ++i) {
+        seek();
+        issue();
+    }
 
     float O[NG][8][4];
     float m_run[NG], l_run[NG], qx[NG];
@@ -546,6 +767,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     int vexp = 0;  // the V accumulators are in units of 2^vexp
     float vlim = 128.f, vsc = 1.f;
     int64_t cur_bh = -1;
+    int64_t ctx_run = ctx_len;  // context length of the current (batch, KV head) run
     const float thr = P.sparse_thr;
     const bool sparse = thr > 0.f;
     const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
@@ -739,7 +961,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         __syncthreads();
         const int64_t b = run_bh / Hkv;
         const int gh = (int)(run_bh % Hkv);
-        const int slot = (int)blockIdx.x - attn3_cta_of(run_bh * n_splits, gridDim.x, n_items);
+        const int slot = PAGED ? meta.slot_base[blockIdx.x] - meta.slot_base[meta.c0[run_bh]]
+                               : (int)blockIdx.x - attn3_cta_of(run_bh * n_splits, gridDim.x, n_items);
         for (int i = threadIdx.x; i < G * 128; i += T) {
             const int h = i >> 7, dim = i & 127;
             float M = -INFINITY;
@@ -785,6 +1008,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             vsc = 1.f;
             const int64_t b = bh / Hkv;
             const int gh = (int)(bh % Hkv);
+            if constexpr (PAGED) {
+                const int64_t len = __ldg(pa.lens + b);
+                ctx_run = len < 0 ? 0 : (len < ctx_len ? len : ctx_len);
+            }
 #pragma unroll
             for (int hg = 0; hg < NG; ++hg) {
                 const int hc = 4 * hg + (g >> 1);  // head of this lane's B column
@@ -809,24 +1036,28 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         }
 
         int64_t pos = (int64_t)split * seg + wofs;
-        for (int c = 0; c < nC; ++c, pos += kA3Chunk) {
+        for (int c = 0; c < nC; ++c, pos += kStride) {
+            const int64_t rem = ctx_run - pos;
+            if (rem <= 0) break;  // this slot and the item's later ones hold no rows
+            const int n = rem >= kA3Chunk ? kA3Chunk : (int)rem;
+            seek();
             if (!bad) {
                 const bool ok = mbar_wait(bars + cst, cph);
                 if (!__all_sync(kAll, ok)) {
                     if (lane == 0) report_timeout(status, kA3StatusWait);
-                    bad = true;
+                    bad = true;  // cst and cph stay at the stage that gave up
+                } else {
+                    --inflight;
                 }
             }
-            const int64_t rem = ctx_len - pos;
-            const int n = rem <= 0 ? 0 : (rem >= kA3Chunk ? kA3Chunk : (int)rem);
-            if (n > 0 && !bad) {
+            if (!bad) {
                 const uint32_t sb = ring + (uint32_t)(cst * L::kStage);
                 if (n == kA3Chunk) chunk(sb, n, std::true_type{});
                 else chunk(sb, n, std::false_type{});
             }
             __syncwarp();
-            issue_next();
-            if (++cst == S) {
+            issue();
+            if (!bad && ++cst == S) {
                 cst = 0;
                 cph ^= 1u;
             }
@@ -834,6 +1065,17 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         if (++split == n_splits) {
             split = 0;
             ++bh;
+        }
+    }
+    // A wait gave up: wait, again for a bounded time each, for the copies
+    // this warp still has in flight before its shared memory is released.
+    if (bad) {
+        for (int k = 0; k < inflight; ++k) {
+            mbar_wait(bars + cst, cph);
+            if (++cst == S) {
+                cst = 0;
+                cph ^= 1u;
+            }
         }
     }
 }
@@ -861,15 +1103,17 @@ __device__ __forceinline__ float block128_sum(float v, float* red) {
 static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_splits,
                                                               int grid, int64_t n_items, int Hq, int Hkv,
                                                               float* __restrict__ out,
-                                                              const __grid_constant__ AttnParams P) {
+                                                              const __grid_constant__ AttnParams P,
+                                                              bool paged, const A3Meta meta) {
     __shared__ float o[128];
     __shared__ float f[128];
     __shared__ float red[4];
     const int bh = blockIdx.x, j = threadIdx.x;
     // partials of this (batch, query head): one per CTA whose items reach its KV head
     const int64_t bhk = (int64_t)(bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
-    const int n_parts = attn3_cta_of((bhk + 1) * n_splits - 1, grid, n_items) -
-                        attn3_cta_of(bhk * n_splits, grid, n_items) + 1;
+    const int n_parts = paged ? meta.slot_base[meta.clast[bhk]] - meta.slot_base[meta.c0[bhk]] + 1
+                              : attn3_cta_of((bhk + 1) * n_splits - 1, grid, n_items) -
+                                    attn3_cta_of(bhk * n_splits, grid, n_items) + 1;
     const float* base = part + (int64_t)bh * n_splits * 130;
     float M = -INFINITY;
     for (int s = j; s < n_parts; s += 128) M = fmaxf(M, base[s * 130 + 128]);
@@ -892,17 +1136,18 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
         __syncthreads();
     }
     const float L = block128_sum(lsum, red);
-    o[j] = a / L;
+    o[j] = L > 0.f ? a / L : 0.f;  // an empty context (paged, length 0) gives zeros
     fwht_smem<128>(o, 1);
     out[(int64_t)bh * 128 + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }
 
-template <int KB, int VB, int NG>
+template <int KB, int VB, int NG, bool PAGED>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
-                               int64_t items, int grid, float* part, const AttnParams& P, cudaStream_t s) {
+                               int64_t items, int grid, float* part, const AttnParams& P,
+                               const PagedArgs& pa, const A3Meta& meta, cudaStream_t s) {
     using L = A3Layout<KB, VB, NG>;
-    auto fn = k_attn3_split<KB, VB, NG>;
+    auto fn = k_attn3_split<KB, VB, NG, PAGED>;
     // The kernel addresses shared memory from window address 0, so it asks
     // for kEnd bytes (the dynamic block starts at or below kA3RingAt).
     static int attr_done[64] = {};
@@ -916,28 +1161,55 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
     }
     fn<<<(unsigned)grid, A3Shape<KB, VB, NG>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len,
                                                                       geo.warp_len, geo.n_splits, items,
-                                                                      part, status_word(), P);
+                                                                      part, status_word(), P, pa, meta);
     return cudaGetLastError();
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool PAGED = false>
 cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
                          int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
-                         const AttnParams& P, cudaStream_t s) {
+                         const AttnParams& P, cudaStream_t s, const PagedArgs& pa = PagedArgs{}) {
     __half* q16 = static_cast<__half*>(ws);
     float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * Hq * 512);
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + attn3_prefix_bytes(B, Hq));
+    const int sms = num_sms();
+    A3Meta meta;
+    meta.cta_begin = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(part) + attn3_partial_bytes(B, Hq, geo.n_splits));
+    meta.slot_base = meta.cta_begin + (sms + 1);
+    meta.c0 = meta.slot_base + (sms + 1);
+    meta.clast = meta.c0 + (size_t)B * Hq;
     k_attn3_q<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
-    const int grid = (int)(items < num_sms() ? items : num_sms());  // one CTA per SM
+    int grid = (int)(items < sms ? items : sms);  // one CTA per SM
+    if (PAGED) {
+        if (grid > 1024) grid = 1024;  // the planning block gives one thread to each CTA
+        const int n_pairs = B * Hkv;
+        const size_t plan_smem = n_pairs <= kA3PlanSmemPairs ? sizeof(int64_t) * (size_t)n_pairs : 0;
+        static int plan_attr[64] = {};
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64 || !plan_attr[dev]) {
+            e = cudaFuncSetAttribute((const void*)k_attn3_plan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(sizeof(int64_t) * kA3PlanSmemPairs));
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < 64) plan_attr[dev] = 1;
+        }
+        k_attn3_plan<<<1, 1024, plan_smem, s>>>(pa.lens, Hkv, geo.n_splits, (int64_t)geo.split_len, geo.warp_len,
+                                                ctx_len, n_pairs, grid, meta);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (Hq / Hkv <= 4)
-        e = attn3_split_launch<KB, VB, 1>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P, s);
+        e = attn3_split_launch<KB, VB, 1, PAGED>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P,
+                                                 pa, meta, s);
     else
-        e = attn3_split_launch<KB, VB, 2>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P, s);
+        e = attn3_split_launch<KB, VB, 2, PAGED>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P,
+                                                 pa, meta, s);
     if (e != cudaSuccess) return e;
-    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv, out, P);
+    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv, out, P, PAGED, meta);
     return cudaGetLastError();
 }
 
@@ -983,6 +1255,23 @@ cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
                            const AttnGeometry& g, const AttnParams& P, cudaStream_t s) {
     return dev::attn_vb<D, KB>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, P, s);
 }
+
+#if TQ_UNIT_D == 128
+template <int KB>
+cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
+                                 const tq_cache_view& pages, int64_t max_ctx, float* out,
+                                 void* workspace, const AttnGeometry& g, const AttnParams& P,
+                                 const PagedArgs& pa, cudaStream_t s) {
+    switch (v_bits) {
+        case 2: return dev::attn3_launch<KB, 2, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
+        case 3: return dev::attn3_launch<KB, 3, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
+        default: return dev::attn3_launch<KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
+    }
+}
+template cudaError_t launch_attn128_paged<TQ_UNIT_KB>(int, const void*, int, int, int, const tq_cache_view&,
+                                                      int64_t, float*, void*, const AttnGeometry&,
+                                                      const AttnParams&, const PagedArgs&, cudaStream_t);
+#endif
 
 #if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB)
 #error "compile once per head dimension and K width with -DTQ_UNIT_D=<d> -DTQ_UNIT_KB=<bits>"

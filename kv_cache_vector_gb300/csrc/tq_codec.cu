@@ -211,13 +211,19 @@ __device__ __forceinline__ void load_lane(const T* __restrict__ row, int lane, c
     }
 }
 
-template <int D, typename T>
+// PAGED: one new row per (sequence, KV head) (n_new = 1), written at position
+// pa.lens[b] of a paged cache; a position or page id out of range writes
+// nothing and sets the status word to kAppStatusRange.
+constexpr int kAppStatusRange = 42;
+
+template <int D, typename T, bool PAGED>
 __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restrict__ k_new,
                                                                 const T* __restrict__ v_new, int64_t n_rows,
                                                                 int64_t n_new, tq_cache_view cache,
                                                                 int64_t pos, int k_bits, int v_bits,
                                                                 const __grid_constant__ RowParams PK,
-                                                                const __grid_constant__ RowParams PV) {
+                                                                const __grid_constant__ RowParams PV,
+                                                                const PagedArgs pa, int Hkv, int* status) {
     static_assert(D >= 32 && D <= kMaxD, "one warp per row");
     constexpr int E = D / 32;
     __shared__ uint32_t sg[D];
@@ -261,8 +267,22 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
             ib[lane * E + e] = (uint8_t)id;
         }
         __syncwarp();
-        const int64_t i_in = srow % n_new;
-        const int64_t drow = (srow / n_new) * cache.cap + pos + i_in;
+        int64_t drow;
+        if constexpr (PAGED) {
+            const int64_t b = srow / Hkv;
+            const int h = (int)(srow - b * Hkv);
+            const int64_t p = __ldg(pa.lens + b);
+            const int64_t cap = (int64_t)pa.max_pages << pa.page_shift;
+            const int page = (p >= 0 && p < cap) ? __ldg(pa.bt + b * pa.max_pages + (p >> pa.page_shift)) : -1;
+            if (page < 0 || page >= pa.n_pages) {  // warp-uniform: nothing is written for this row
+                if (lane == 0 && status) atomicCAS(status, 0, kAppStatusRange);
+                __syncwarp();
+                continue;
+            }
+            drow = (((int64_t)page * Hkv + h) << pa.page_shift) + (p & ((int64_t(1) << pa.page_shift) - 1));
+        } else {
+            drow = (srow / n_new) * cache.cap + pos + srow % n_new;
+        }
         if (4 * lane < rb) {  // word `lane` of the packed row: stream bits [32 lane, 32 lane + 32)
             const int b0 = 32 * lane;
             const int i0 = b0 / bits, i1 = min(D - 1, (b0 + 31) / bits);
@@ -1318,13 +1338,13 @@ cudaError_t app(const void* kn, const void* vn, int B, int Hkv, int64_t n_new, c
                 int64_t pos, int kb, int vb, const RowParams& PK, const RowParams& PV, cudaStream_t s) {
     const int64_t rows = (int64_t)B * Hkv * n_new;
     if constexpr (D >= 32) {
-        auto fn = dev::k_append_warp<D, T>;
+        auto fn = dev::k_append_warp<D, T, false>;
         int64_t g = (rows + dev::kAppWarps - 1) / dev::kAppWarps;
         const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kAppWarps, 0);
         if (g > cap) g = cap;
         fn<<<dim3((unsigned)g, 2), 32 * dev::kAppWarps, 0, s>>>(static_cast<const T*>(kn),
                                                                 static_cast<const T*>(vn), rows, n_new, c,
-                                                                pos, kb, vb, PK, PV);
+                                                                pos, kb, vb, PK, PV, PagedArgs{}, Hkv, nullptr);
     } else {
         auto fn = dev::k_append<D, T>;
         unsigned g = grid_for((const void*)fn, dev::kBlock, rows * dev::RowShape<D>::R);
@@ -1380,6 +1400,31 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
                : app<D, float>(k_new, v_new, B, Hkv, n_new, cache, pos, k_bits, v_bits, PK, PV, s);
 }
 
+template <int D>
+cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,
+                                  const void* v_new, int B, int Hkv, const tq_cache_view& pages,
+                                  const PagedArgs& pa, const RowParams& PK, const RowParams& PV,
+                                  cudaStream_t s) {
+    if constexpr (D >= 32) {
+        const int64_t rows = (int64_t)B * Hkv;
+        auto launch = [&](auto tag) {
+            using T = decltype(tag);
+            auto fn = dev::k_append_warp<D, T, true>;
+            int64_t g = (rows + dev::kAppWarps - 1) / dev::kAppWarps;
+            const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kAppWarps, 0);
+            if (g > cap) g = cap;
+            fn<<<dim3((unsigned)g, 2), 32 * dev::kAppWarps, 0, s>>>(static_cast<const T*>(k_new),
+                                                                    static_cast<const T*>(v_new), rows, 1,
+                                                                    pages, 0, k_bits, v_bits, PK, PV, pa, Hkv,
+                                                                    status_word());
+            return cudaGetLastError();
+        };
+        return dt == TQ_BF16 ? launch(__nv_bfloat16{}) : launch(float{});
+    } else {
+        return cudaErrorInvalidValue;
+    }
+}
+
 #ifndef TQ_UNIT_D
 #error "compile once per head dimension with -DTQ_UNIT_D=<d>"
 #endif
@@ -1387,6 +1432,9 @@ template cudaError_t launch_encode_d<TQ_UNIT_D>(int, tq_dtype, const void*, int6
                                                 const RowParams&, cudaStream_t);
 template cudaError_t launch_decode_d<TQ_UNIT_D>(int, tq_dtype, const uint8_t*, const float*, int64_t,
                                                 void*, const RowParams&, cudaStream_t);
+template cudaError_t launch_append_paged_d<TQ_UNIT_D>(int, int, tq_dtype, const void*, const void*, int, int,
+                                                      const tq_cache_view&, const PagedArgs&,
+                                                      const RowParams&, const RowParams&, cudaStream_t);
 template cudaError_t launch_append_d<TQ_UNIT_D>(int, int, tq_dtype, const void*, const void*, int, int,
                                                 int64_t, const tq_cache_view&, int64_t,
                                                 const RowParams&, const RowParams&, cudaStream_t);

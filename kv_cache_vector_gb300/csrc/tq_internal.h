@@ -103,11 +103,25 @@ struct AttnGeometry {
 };
 AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d, int kb,
                            int vb);
+// d = 128, paged cache with a length per sequence: shorter warp slices, so a
+// sequence's last, partly filled split wastes little of a CTA's time.
+AttnGeometry attn_geometry_paged(int B, int Hq, int Hkv, int64_t max_ctx, int num_sms, int kb, int vb);
+size_t attn_paged_workspace_bound(int B, int Hq, int Hkv, int64_t max_ctx, int num_sms);
 // Workspace that covers every K/V width pair (the public size query takes none).
 size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
 // their power-of-two scales (4 bytes per head), rounded up to 256 bytes.
+// d = 128, paged attention: the work partition written by the planning
+// kernel after the partials: int32 CTA range starts [sms + 1], slot bases
+// [sms + 1], first and last CTA per (batch, KV head) [B * Hq] each (Hq bounds
+// Hkv), rounded up to 256 bytes.
+inline size_t attn3_meta_bytes(int B, int Hq, int sms) {
+    return ((size_t)4 * (2 * ((size_t)sms + 1) + 2 * (size_t)B * Hq) + 255) / 256 * 256;
+}
+inline size_t attn3_partial_bytes(int B, int Hq, int n_splits) {
+    return ((size_t)4 * B * Hq * n_splits * 130 + 255) / 256 * 256;
+}
 inline size_t attn3_prefix_bytes(int B, int Hq) {
     return ((size_t)B * Hq * (512 + 4) + 255) / 256 * 256;
 }
@@ -115,6 +129,31 @@ template <int D, int KB>
 cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
                            const tq_cache_view& cache, int64_t ctx_len, float* out, void* workspace,
                            const AttnGeometry& g, const AttnParams& P, cudaStream_t s);
+
+// Paged-cache addressing: sequence b keeps position p at offset
+// p & (2^page_shift - 1) of page bt[b * max_pages + (p >> page_shift)]; a page
+// holds every KV head, [page][Hkv][page_size] rows.  `lens` holds the context
+// length (attention) or the position written (append) of each sequence.
+struct PagedArgs {
+    const int32_t* bt;
+    const int32_t* lens;
+    int64_t n_pages;
+    int max_pages;
+    int page_shift;
+};
+// d = 128 paged attention (tq_attn.cu, compiled in the d = 128 units); the
+// tq_cache_view carries the page arrays (its cap is unused).
+template <int KB>
+cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
+                                 const tq_cache_view& pages, int64_t max_ctx, float* out,
+                                 void* workspace, const AttnGeometry& g, const AttnParams& P,
+                                 const PagedArgs& pa, cudaStream_t s);
+// Paged append of one token per sequence, d >= 32 (tq_codec.cu).
+template <int D>
+cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,
+                                  const void* v_new, int B, int Hkv, const tq_cache_view& pages,
+                                  const PagedArgs& pa, const RowParams& PK, const RowParams& PV,
+                                  cudaStream_t s);
 
 // Shared launch helpers (tq_launch.cpp).
 int num_sms();

@@ -108,6 +108,35 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
     return g;
 }
 
+AttnGeometry attn_geometry_paged(int B, int Hq, int Hkv, int64_t max_ctx, int sms, int kb, int vb) {
+    // The CTAs' shares are balanced on the device from the actual lengths;
+    // here only the slice length is chosen: the longest one that stays under
+    // 1/8 of a warp's share if every sequence were max_ctx long.  Longer
+    // slices measured faster with varied lengths (fewer items and pair
+    // switches per CTA) although they balance more coarsely.
+    AttnGeometry g;
+    const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb);
+    const int64_t per_warp = (int64_t)B * Hkv * max_ctx / ((int64_t)W * (sms > 0 ? sms : 1));
+    int wl = 256;
+    while (wl > 32 && (int64_t)wl * 8 > per_warp) wl /= 2;
+    g.warp_len = wl;
+    g.split_len = W * wl;
+    g.n_splits = (int)((max_ctx + g.split_len - 1) / g.split_len);
+    g.parts = 1;
+    g.q16 = true;
+    return g;
+}
+
+size_t attn_paged_workspace_bound(int B, int Hq, int Hkv, int64_t max_ctx, int sms) {
+    size_t most = 0;
+    for (int kb = 2; kb <= 4; ++kb)
+        for (int vb = 2; vb <= 4; ++vb) {
+            const size_t w = attn_workspace_bytes(B, Hq, 128, attn_geometry_paged(B, Hq, Hkv, max_ctx, sms, kb, vb));
+            if (w > most) most = w;
+        }
+    return most;
+}
+
 size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d) {
     size_t most = 0;
     for (int kb = 2; kb <= 4; ++kb)
@@ -119,8 +148,10 @@ size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int sms, in
 }
 
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g) {
-    return (g.q16 ? attn3_prefix_bytes(B, Hq) : 0) +
-           sizeof(float) * (size_t)B * Hq * g.n_splits * g.parts * (d + 2);
+    if (g.q16)
+        return attn3_prefix_bytes(B, Hq) + attn3_partial_bytes(B, Hq, g.n_splits) +
+               attn3_meta_bytes(B, Hq, num_sms());
+    return sizeof(float) * (size_t)B * Hq * g.n_splits * g.parts * (d + 2);
 }
 
 int* status_word() {

@@ -98,6 +98,8 @@ def test_hot_call_validation_before_launch(L):
     assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 17, 4, 2, f(1.0), f(0.0), A, A, 1 << 20, s) == 4
     assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 8, 4, 2, f(1.0), f(-1.0), A, A, 1 << 20, s) == 1
     assert L.tq_attn_workspace_bytes(1, 6, 4, 128, 8) == 0
+    assert L.tq_attn_paged_workspace_bytes(1, 6, 4, 128, 8) == 0
+    assert L.tq_attn_paged_workspace_bytes(1, 8, 2, 64, 8) == 0
     p.close()
 
 
@@ -139,3 +141,46 @@ def test_bucketing_table_is_exact(L, d, bits):
     want = np.searchsorted(bnd, w, side="right")
     assert np.array_equal(_emulate_table_bucket(bnd, w), want)
     p.close()
+
+
+def test_paged_call_validation_before_launch(L):
+    """The paged entry points check their arguments on the host and return
+    status codes before any launch."""
+    p128, p64, p16 = abi.Plan(128, 42), abi.Plan(64, 42), abi.Plan(16, 42)
+    A = 1 << 20
+    s = None
+    f = ctypes.c_float
+
+    def pc(n_pages=4, page_size=64):
+        return abi.PagedCacheView(A, A, A, A, n_pages, page_size)
+
+    h = p128.handle
+    # tq_append_paged(plan, kb, vb, k_new, v_new, dtype, B, Hkv, cache, bt, max_pages, positions, s)
+    assert L.tq_append_paged(None, 4, 2, A, A, 1, 2, 2, pc(), A, 4, A, s) == 1
+    assert L.tq_append_paged(h, 5, 2, A, A, 1, 2, 2, pc(), A, 4, A, s) == 2
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(page_size=48), A, 4, A, s) == 2
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(page_size=16), A, 4, A, s) == 2
+    assert L.tq_append_paged(p16.handle, 4, 2, A, A, 1, 2, 2, pc(), A, 4, A, s) == 2
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(), A, 0, A, s) == 1
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(n_pages=0), A, 4, A, s) == 1
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 0, 2, pc(), None, 4, None, s) == 0  # B = 0: no-op
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(), None, 4, A, s) == 1
+    assert L.tq_append_paged(h, 4, 2, A + 8, A, 1, 2, 2, pc(), A, 4, A, s) == 3
+    assert L.tq_append_paged(h, 4, 2, A, A, 1, 2, 2, pc(), A, 4, A + 2, s) == 3
+    # tq_attn_decode_paged(plan, q, B, Hq, Hkv, cache, bt, max_pages, lens, max_ctx, kb, vb,
+    #                      scale, thr, out, ws, ws_bytes, s)
+    W = 1 << 24
+    assert L.tq_attn_decode_paged(h, A, 1, 6, 4, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
+    assert L.tq_attn_decode_paged(h, A, 1, 32, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2
+    assert L.tq_attn_decode_paged(p64.handle, A, 1, 8, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W,
+                                  s) == 2
+    assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(page_size=100), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A,
+                                  A, W, s) == 2
+    assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(), A, 4, A, 0, 4, 3, f(1.0), f(0.0), A, A, W, s) == 4
+    assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(), A, 4, A, 257, 4, 3, f(1.0), f(0.0), A, A, W, s) == 4
+    assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(-1.0), A, A, W, s) == 1
+    assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, 16, s) == 5
+    assert L.tq_attn_decode_paged(h, A + 4, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W,
+                                  s) == 3
+    assert L.tq_attn_decode_paged(h, A, 0, 8, 2, pc(), None, 4, None, 256, 4, 3, f(1.0), f(0.0), None,
+                                  None, 0, s) == 0  # B = 0: no-op
