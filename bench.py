@@ -47,6 +47,8 @@ def args_():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["encode", "decode", "attn", "append"], default=None,
                     help="run just one kernel per step (profiling of one kernel)")
+    ap.add_argument("--extra", choices=["long_context", "gemma_cache", "paged_varlen"], default=None,
+                    help="run just one of the extra measurements and print its result (profiling)")
     return ap.parse_args()
 
 
@@ -629,6 +631,12 @@ def main():
     if rank == 0:
         build.build()
     barrier(world)
+    if a.extra:
+        if rank == 0:
+            fn = {"long_context": extra_long_context, "gemma_cache": extra_gemma, "paged_varlen": extra_paged}
+            print(json.dumps({"extra": a.extra, **fn[a.extra](measured_peak()[0])}))
+        barrier(world)
+        return
     S = make_state(W, rank)
     active = [k for k in KERNELS if not a.only or k.startswith(a.only)]
     for _ in range(max(3, a.warmup)):
