@@ -506,7 +506,28 @@ def extra_paged(peak):
     us = time_events(call, 20) * 1e3
     nbytes = int(lens.sum()) * Hkv * (D * (kb + vb) // 8 + 8)
     gbs = nbytes / (us * 1e-6) / 1e9
+    # One decode step: the newest token's K/V rows are written at position len - 1 and the
+    # sequence attends over its len rows, fused (one call) or as append + attend.
+    k_new = synth.device_normal(93, (B, Hkv, D))
+    v_new = synth.device_normal(94, (B, Hkv, D))
+    last = (lens_d - 1).contiguous()
+
+    def fused():
+        abi.tq_attn_decode_append_paged(plan, q, k_new, v_new, cache, bt_d, last, max_ctx, 1.0 / math.sqrt(D),
+                                        0.0, out=out, workspace=ws)
+
+    def separate():
+        abi.tq_append_paged(plan, cache, k_new, v_new, bt_d, last)
+        call()
+
+    steps = {}
+    for name, f in (("fused", fused), ("separate", separate)):
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        steps[name] = round(time_events(f, 20) * 1e3, 2)
     return {"us": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "append_attend_step_us": steps,
             "positions": int(lens.sum()),
             "config": f"B{B} Hq{Hq}/Hkv{Hkv} d128 K{kb}/V{vb}, pages of {page}, lengths uniform in [1, {max_ctx}] "
                       f"(seeded; mean {float(lens.float().mean()):.0f}), low-rank+diag rows"}

@@ -249,6 +249,31 @@ tq_status tq_attn_decode_paged(const tq_plan *plan, const void *q, int B, int Hq
                                float scale, float sparse_v_threshold, float *out, void *workspace,
                                size_t workspace_bytes, tq_stream_t stream);
 
+/* One decode step on a paged cache: append each sequence's new token, then
+ * attend over the sequence including it ("TurboQuant KV Cache Compression --
+ * Spec", fa_tq_attention_cached: the new K and V are quantised into the cache
+ * and the cached K and V are read for attention).  For sequence b the new
+ * rows are written at position positions[b], exactly as tq_append_paged
+ * writes them, and the output is the tq_attn_decode_paged result over
+ * positions [0, min(positions[b] + 1, max_ctx)).  The append rides on the
+ * attention's first launch; no launch is added.  d = 128 only.
+ *   q:      [B][Hq][d] bf16, device;  out: [B][Hq][d] fp32, device
+ *   k_new, v_new: [B][Hkv][d] (kv_dtype), device
+ *   block_table: [B][max_pages] int32, device;  positions: [B] int32, device
+ *   max_ctx: an upper bound of positions[b] + 1, <= max_pages * page_size; the
+ *     workspace is tq_attn_paged_workspace_bytes(B, Hq, Hkv, 128, max_ctx).
+ * A position outside [0, max_pages * page_size) or a page id outside
+ * [0, n_pages) writes nothing for that sequence and sets the device status
+ * word to 42; its attention still runs over min(positions[b] + 1, max_ctx)
+ * positions (none if positions[b] < 0).
+ * Errors: as tq_attn_decode_paged; TQ_ERR_UNSUPPORTED also for kv_dtype. */
+tq_status tq_attn_decode_append_paged(const tq_plan *plan, const void *q, const void *k_new,
+                                      const void *v_new, tq_dtype kv_dtype, int B, int Hq, int Hkv,
+                                      tq_paged_cache cache, const int32_t *block_table, int max_pages,
+                                      const int32_t *positions, int64_t max_ctx, int k_bits, int v_bits,
+                                      float scale, float sparse_v_threshold, float *out, void *workspace,
+                                      size_t workspace_bytes, tq_stream_t stream);
+
 /* Text for a status code (static storage). */
 const char *tq_status_string(tq_status status);
 

@@ -26,7 +26,8 @@ STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_E
 EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_signs",
            "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes", "tq_attn_paged_workspace_bytes",
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
-           "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged")
+           "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged",
+           "tq_attn_decode_append_paged")
 
 
 class TQError(RuntimeError):
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         ("tq_append_paged", i32, [vp, i32, i32, vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, vp]),
         ("tq_attn_decode_paged", i32, [vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, i64, i32, i32,
                                        f32, f32, vp, vp, ctypes.c_size_t, vp]),
+        ("tq_attn_decode_append_paged", i32, [vp, vp, vp, vp, i32, i32, i32, i32, PagedCacheView, vp, i32, vp,
+                                              i64, i32, i32, f32, f32, vp, vp, ctypes.c_size_t, vp]),
         ("tq_status_string", ctypes.c_char_p, [i32]),
         ("tq_last_cuda_error", i32, []),
         ("tq_device_status", i32, [i32, ctypes.POINTER(i32)]),
@@ -348,6 +351,39 @@ def tq_attn_decode_paged(plan: Plan, q: torch.Tensor, cache: PagedCache, block_t
         ctx_lens.data_ptr(), max_ctx, cache.k_bits, cache.v_bits, ctypes.c_float(scale),
         ctypes.c_float(sparse_v_threshold), out.data_ptr(), workspace.data_ptr(), workspace.numel(),
         _stream(q)))
+    return out
+
+
+def tq_attn_decode_append_paged(plan: Plan, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                cache: PagedCache, block_table: torch.Tensor, positions: torch.Tensor,
+                                max_ctx: int, scale: float, sparse_v_threshold: float = 0.0,
+                                out: torch.Tensor | None = None,
+                                workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode step: append k_new/v_new [B, Hkv, d] (fp32 or bf16) at
+    positions [B] int32, then attend q [B, Hq, d] bf16 over positions + 1
+    (at most max_ctx) -> out [B, Hq, d] fp32."""
+    B, Hq, d = q.shape
+    Hkv = cache.Hkv
+    if tuple(k_new.shape) != (B, Hkv, d) or tuple(v_new.shape) != (B, Hkv, d):
+        raise ValueError("k_new and v_new must be [B, Hkv, d]")
+    if k_new.dtype != v_new.dtype:
+        raise TypeError("k_new and v_new must share a dtype")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    need = tq_attn_paged_workspace_bytes(B, Hq, Hkv, d, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(q, k_new, v_new, out, workspace)
+    _i32(block_table, "block_table")
+    _i32(positions, "positions")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    _check("tq_attn_decode_append_paged", lib().tq_attn_decode_append_paged(
+        plan.handle, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), _dt(k_new), B, Hq, Hkv, cache.view(),
+        block_table.data_ptr(), block_table.shape[1], positions.data_ptr(), max_ctx, cache.k_bits,
+        cache.v_bits, ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel(), _stream(q)))
     return out
 
 

@@ -547,6 +547,54 @@ tq_status tq_attn_decode_paged(const tq_plan* plan, const void* q, int B, int Hq
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
+tq_status tq_attn_decode_append_paged(const tq_plan* plan, const void* q, const void* k_new,
+                                      const void* v_new, tq_dtype kv_dtype, int B, int Hq, int Hkv,
+                                      tq_paged_cache cache, const int32_t* block_table, int max_pages,
+                                      const int32_t* positions, int64_t max_ctx, int k_bits, int v_bits,
+                                      float scale, float sparse_v_threshold, float* out, void* workspace,
+                                      size_t workspace_bytes, tq_stream_t stream) {
+    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages < 1 || cache.n_pages < 1)
+        return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits) || Hq / Hkv > 8 || !valid_dtype(kv_dtype))
+        return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    const int shift = page_shift_of(cache.page_size);
+    if (P->d != 128 || shift < 0) return TQ_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
+        return TQ_ERR_INVALID_ARG;
+    if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
+    if (B == 0) return TQ_OK;
+    if (!q || !k_new || !v_new || !out || !block_table || !positions || !paged_pointers_ok(cache))
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || !aligned4(block_table) ||
+        !aligned4(positions) || !paged_aligned(cache))
+        return TQ_ERR_ALIGNMENT;
+    tq::AttnGeometry g = tq::attn_geometry_paged(B, Hq, Hkv, max_ctx, tq::num_sms(), k_bits, v_bits);
+    if ((int64_t)B * Hkv * g.n_splits > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // work items are int32
+    if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(k_new) || !device_accessible(v_new) ||
+        !device_accessible(out) || !device_accessible(workspace) || !device_accessible(block_table) ||
+        !device_accessible(positions) || !paged_accessible(cache))
+        return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
+    tq::RowParams PK, PV;
+    fill_row_params(*P, k_bits, PK);
+    fill_row_params(*P, v_bits, PV);
+    const tq::AttnAppend app{k_new, v_new, kv_dtype == TQ_BF16, &PK, &PV};
+    const tq::PagedArgs pa{block_table, positions, cache.n_pages, max_pages, shift};
+    const tq_cache_view view = paged_as_view(cache);
+    auto st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (k_bits) {
+        case 2: e = tq::launch_attn128_paged<2>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st, &app); break;
+        case 3: e = tq::launch_attn128_paged<3>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st, &app); break;
+        default: e = tq::launch_attn128_paged<4>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, st, &app); break;
+    }
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 const char* tq_status_string(tq_status s) {
     switch (s) {
         case TQ_OK: return "ok";

@@ -279,6 +279,7 @@ constexpr uint32_t kA3TableAt = kAttn3TableAt;
 constexpr int kA3StatusWait = 31;    // a ring stage did not complete within the bound
 constexpr int kA3StatusLayout = 32;  // dynamic shared memory starts above kA3RingAt
 constexpr int kA3StatusPage = 33;    // a paged cache's block table names a page out of range
+constexpr int kA3StatusAppend = 42;  // an appended row's position or page is out of range (as the append)
 
 // Warps and ring stages per CTA (attn3_warps, attn3_stages): up to 16 x 2
 // for up to four query heads per KV head, 8 x 3 for up to eight.
@@ -421,10 +422,8 @@ __device__ __forceinline__ void load_vfield(uint32_t row, int g, uint32_t (&f)[2
 // (sqrt(d) * s_k)), stored per (batch, head) as qexp = 2^e and fp16 high and
 // low parts of y / 2^e, with e chosen so that max |y| / 2^e is in
 // [2^13, 2^14).  q16 layout: [B * Hq][2 (high, low)][128].
-static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __restrict__ q,
-                                                        __half* __restrict__ q16,
-                                                        float* __restrict__ qexp,
-                                                        const __grid_constant__ AttnParams P) {
+__device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__ q, __half* __restrict__ q16,
+                                               float* __restrict__ qexp, const AttnParams& P) {
     __shared__ float v[128];
     __shared__ float wmax[4];
     const int bh = blockIdx.x, j = threadIdx.x;
@@ -449,6 +448,57 @@ static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __r
     q16[(int64_t)bh * 256 + j] = hi;
     q16[(int64_t)bh * 256 + 128 + j] = lo;
     if (j == 0) qexp[bh] = ldexpf(1.f, e);
+}
+
+static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __restrict__ q,
+                                                        __half* __restrict__ q16,
+                                                        float* __restrict__ qexp,
+                                                        const __grid_constant__ AttnParams P) {
+    attn3_rotate_q(q, q16, qexp, P);
+}
+
+// The query rotation of the paged attention with the decode step's append
+// folded in ("TurboQuant KV Cache Compression -- Spec", fa_tq_attention_cached:
+// quantise the new K and V into the cache, then attend).  Block (b, h) rotates
+// query head h of sequence b as k_attn3_q does.  The first block of each KV
+// head's query group also encodes that head's new K row (warp 0) and V row
+// (warp 1) with the row codec of the append and writes them at position
+// pa.lens[b]; a position or page id out of range writes nothing and sets the
+// status word to 42.  Block (b, 0) writes the attended length pa.lens[b] + 1
+// to len1[b] for the planning and split kernels, which run after this launch.
+template <typename T>
+static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat16* __restrict__ q,
+                                                               __half* __restrict__ q16, float* __restrict__ qexp,
+                                                               const __grid_constant__ AttnParams P, int Hq, int Hkv,
+                                                               const T* __restrict__ k_new, const T* __restrict__ v_new,
+                                                               tq_cache_view cache, const PagedArgs pa,
+                                                               const __grid_constant__ RowParams PK,
+                                                               const __grid_constant__ RowParams PV, int k_bits,
+                                                               int v_bits, int32_t* __restrict__ len1, int* status) {
+    __shared__ uint32_t sg[128];
+    __shared__ uint8_t ib[2][128];
+    const int j = threadIdx.x;
+    sg[j] = P.sgn[j];
+    const int b = blockIdx.x / Hq, h = blockIdx.x - b * Hq, G = Hq / Hkv;
+    const int64_t p = __ldg(pa.lens + b);
+    if (h == 0 && j == 0) len1[b] = p < 0 ? 0 : (p >= INT32_MAX ? INT32_MAX : (int32_t)(p + 1));
+    attn3_rotate_q(q, q16, qexp, P);  // synchronises the block, so sg is complete
+    if (h % G != 0 || j >= 64) return;
+    const int warp = j >> 5, lane = j & 31, kvh = h / G;
+    const bool is_v = warp == 1;
+    const RowParams& R = is_v ? PV : PK;
+    const int bits = is_v ? v_bits : k_bits;
+    const int64_t cap = (int64_t)pa.max_pages << pa.page_shift;
+    const int page = (p >= 0 && p < cap) ? __ldg(pa.bt + (int64_t)b * pa.max_pages + (p >> pa.page_shift)) : -1;
+    if (page < 0 || page >= pa.n_pages) {  // warp-uniform: nothing is written for this row
+        if (lane == 0) atomicCAS(status, 0, kA3StatusAppend);
+        return;
+    }
+    const int64_t drow = (((int64_t)page * Hkv + kvh) << pa.page_shift) + (p & ((int64_t(1) << pa.page_shift) - 1));
+    const T* src = (is_v ? v_new : k_new) + ((int64_t)b * Hkv + kvh) * 128;
+    const float n = warp_encode_indices<128, T>(src, lane, sg, R, (1 << bits) - 1, ib[warp]);
+    warp_pack_row<128>(ib[warp], lane, bits, (is_v ? cache.v_packed : cache.k_packed) + drow * (16 * bits));
+    if (lane == 0) (is_v ? cache.v_norm : cache.k_norm)[drow] = n;
 }
 
 // Work partition of the paged kernel (written by k_attn3_plan): CTA c takes
@@ -1168,7 +1218,8 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
 template <int KB, int VB, bool PAGED = false>
 cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
                          int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
-                         const AttnParams& P, cudaStream_t s, const PagedArgs& pa = PagedArgs{}) {
+                         const AttnParams& P, cudaStream_t s, const PagedArgs& pa_in = PagedArgs{},
+                         const AttnAppend* app = nullptr) {
     __half* q16 = static_cast<__half*>(ws);
     float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * Hq * 512);
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + attn3_prefix_bytes(B, Hq));
@@ -1178,8 +1229,26 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     meta.slot_base = meta.cta_begin + (sms + 1);
     meta.c0 = meta.slot_base + (sms + 1);
     meta.clast = meta.c0 + (size_t)B * Hq;
-    k_attn3_q<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, P);
-    cudaError_t e = cudaGetLastError();
+    PagedArgs pa = pa_in;
+    cudaError_t e;
+    if (PAGED && app) {
+        int32_t* len1 = meta.clast + (size_t)B * Hq;  // attended lengths, written by the append launch
+        auto qb = static_cast<const __nv_bfloat16*>(q);
+        if (app->bf16)
+            k_attn3_q_append<__nv_bfloat16><<<B * Hq, 128, 0, s>>>(
+                qb, q16, qexp, P, Hq, Hkv, static_cast<const __nv_bfloat16*>(app->k_new),
+                static_cast<const __nv_bfloat16*>(app->v_new), cache, pa, *app->PK, *app->PV, KB, VB, len1,
+                status_word());
+        else
+            k_attn3_q_append<float><<<B * Hq, 128, 0, s>>>(qb, q16, qexp, P, Hq, Hkv,
+                                                          static_cast<const float*>(app->k_new),
+                                                          static_cast<const float*>(app->v_new), cache, pa,
+                                                          *app->PK, *app->PV, KB, VB, len1, status_word());
+        pa.lens = len1;
+    } else {
+        k_attn3_q<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, P);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
     int grid = (int)(items < sms ? items : sms);  // one CTA per SM
@@ -1261,16 +1330,17 @@ template <int KB>
 cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
                                  const tq_cache_view& pages, int64_t max_ctx, float* out,
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
-                                 const PagedArgs& pa, cudaStream_t s) {
+                                 const PagedArgs& pa, cudaStream_t s, const AttnAppend* app) {
     switch (v_bits) {
-        case 2: return dev::attn3_launch<KB, 2, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
-        case 3: return dev::attn3_launch<KB, 3, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
-        default: return dev::attn3_launch<KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa);
+        case 2: return dev::attn3_launch<KB, 2, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, app);
+        case 3: return dev::attn3_launch<KB, 3, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, app);
+        default: return dev::attn3_launch<KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, app);
     }
 }
 template cudaError_t launch_attn128_paged<TQ_UNIT_KB>(int, const void*, int, int, int, const tq_cache_view&,
                                                       int64_t, float*, void*, const AttnGeometry&,
-                                                      const AttnParams&, const PagedArgs&, cudaStream_t);
+                                                      const AttnParams&, const PagedArgs&, cudaStream_t,
+                                                      const AttnAppend*);
 #endif
 
 #if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB)

@@ -157,59 +157,9 @@ __global__ void __launch_bounds__(kBlock) k_append(const T* __restrict__ k_new,
 }
 
 // Append for d >= 32, built for latency (a decode step appends a few rows):
-// one warp per row, E = d / 32 consecutive elements per lane.  The transform
-// runs over the element bits in registers and over the lane bits with
-// shuffles, in the same bit order and with the same adds as the in-register
-// transform; each index is the count of boundaries below the coordinate
-// (same comparison as the other encoders), and the packed row is assembled
-// through a per-warp byte buffer, one 32-bit word per lane.
+// one warp per row (warp_encode_indices, warp_pack_row), kAppWarps rows per
+// block.
 constexpr int kAppWarps = 4;
-
-template <int E, typename T>
-__device__ __forceinline__ void load_lane(const T* __restrict__ row, int lane, const uint32_t* sg,
-                                          float (&v)[E]) {
-    if constexpr (sizeof(T) == 2) {
-        const uint16_t* p = reinterpret_cast<const uint16_t*>(row) + lane * E;
-        uint32_t h[E];
-        if constexpr (E == 8) {
-            const uint4 u = *reinterpret_cast<const uint4*>(p);
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                h[2 * k] = w[k] & 0xFFFFu;
-                h[2 * k + 1] = w[k] >> 16;
-            }
-        } else if constexpr (E == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(p);
-            h[0] = u.x & 0xFFFFu;
-            h[1] = u.x >> 16;
-            h[2] = u.y & 0xFFFFu;
-            h[3] = u.y >> 16;
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) h[e] = p[e];
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = __uint_as_float((h[e] << 16) ^ sg[lane * E + e]);
-    } else {
-        const float* p = reinterpret_cast<const float*>(row) + lane * E;
-        if constexpr (E % 4 == 0) {
-#pragma unroll
-            for (int k = 0; k < E / 4; ++k) {
-                const float4 u = reinterpret_cast<const float4*>(p)[k];
-                v[4 * k] = u.x;
-                v[4 * k + 1] = u.y;
-                v[4 * k + 2] = u.z;
-                v[4 * k + 3] = u.w;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) v[e] = p[e];
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg[lane * E + e]);
-    }
-}
 
 // PAGED: one new row per (sequence, KV head) (n_new = 1), written at position
 // pa.lens[b] of a paged cache; a position or page id out of range writes
@@ -225,7 +175,6 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
                                                                 const __grid_constant__ RowParams PV,
                                                                 const PagedArgs pa, int Hkv, int* status) {
     static_assert(D >= 32 && D <= kMaxD, "one warp per row");
-    constexpr int E = D / 32;
     __shared__ uint32_t sg[D];
     __shared__ uint8_t idxbuf[kAppWarps][D];
     const bool is_v = blockIdx.y == 1;
@@ -242,31 +191,7 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
     uint8_t* ib = idxbuf[warp];
     for (int64_t srow = (int64_t)blockIdx.x * kAppWarps + warp; srow < n_rows;
          srow += (int64_t)gridDim.x * kAppWarps) {
-        float v[E];
-        load_lane<E, T>(src + srow * D, lane, sg, v);
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-        fwht_reg<E>(v);
-#pragma unroll
-        for (int b = 1; b < 32; b <<= 1) {
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
-                v[e] = (lane & b) ? o - v[e] : v[e] + o;  // (lo + hi, lo - hi)
-            }
-        }
-        const float n = __fsqrt_rn(ss);
-        const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            int id = 0;
-            for (int j = 0; j < nb; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
-            ib[lane * E + e] = (uint8_t)id;
-        }
-        __syncwarp();
+        const float n = warp_encode_indices<D, T>(src + srow * D, lane, sg, P, nb, ib);
         int64_t drow;
         if constexpr (PAGED) {
             const int64_t b = srow / Hkv;
@@ -283,17 +208,7 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
         } else {
             drow = (srow / n_new) * cache.cap + pos + srow % n_new;
         }
-        if (4 * lane < rb) {  // word `lane` of the packed row: stream bits [32 lane, 32 lane + 32)
-            const int b0 = 32 * lane;
-            const int i0 = b0 / bits, i1 = min(D - 1, (b0 + 31) / bits);
-            uint32_t word = 0u;
-            for (int i = i0; i <= i1; ++i) {
-                const int sh = i * bits - b0;
-                const uint32_t x = ib[i];
-                word |= sh >= 0 ? x << sh : x >> -sh;
-            }
-            reinterpret_cast<uint32_t*>(pk + drow * rb)[lane] = word;
-        }
+        warp_pack_row<D>(ib, lane, bits, pk + drow * rb);
         if (lane == 0) nrm[drow] = n;
         __syncwarp();
     }

@@ -312,5 +312,112 @@ __device__ __forceinline__ void load_bytes(const uint8_t* src, uint32_t* w) {
     }
 }
 
+// ---------------------------------------------------------- one row per warp
+// The row codec with one warp per row, E = d / 32 consecutive elements per
+// lane, for the decode-time append of a few rows.  The transform runs over
+// the element bits in registers and over the lane bits with shuffles, in the
+// same bit order and with the same adds as the in-register transform; each
+// index is the count of boundaries below the coordinate (the same comparison
+// as the other encoders).
+
+template <int E, typename T>
+__device__ __forceinline__ void load_lane(const T* __restrict__ row, int lane, const uint32_t* sg,
+                                          float (&v)[E]) {
+    if constexpr (sizeof(T) == 2) {
+        const uint16_t* p = reinterpret_cast<const uint16_t*>(row) + lane * E;
+        uint32_t h[E];
+        if constexpr (E == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                h[2 * k] = w[k] & 0xFFFFu;
+                h[2 * k + 1] = w[k] >> 16;
+            }
+        } else if constexpr (E == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            h[0] = u.x & 0xFFFFu;
+            h[1] = u.x >> 16;
+            h[2] = u.y & 0xFFFFu;
+            h[3] = u.y >> 16;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) h[e] = p[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __uint_as_float((h[e] << 16) ^ sg[lane * E + e]);
+    } else {
+        const float* p = reinterpret_cast<const float*>(row) + lane * E;
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < E / 4; ++k) {
+                const float4 u = reinterpret_cast<const float4*>(p)[k];
+                v[4 * k] = u.x;
+                v[4 * k + 1] = u.y;
+                v[4 * k + 2] = u.z;
+                v[4 * k + 3] = u.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[e] = p[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg[lane * E + e]);
+    }
+}
+
+// Sign-flip, transform and bucket one row; the indices go to ib[0, D) (a
+// per-warp byte buffer) and the row's L2 norm is returned.  sg: the sign masks
+// in shared memory; nb = 2^bits - 1 boundaries of P are used.
+template <int D, typename T>
+__device__ __forceinline__ float warp_encode_indices(const T* __restrict__ row, int lane, const uint32_t* sg,
+                                                     const RowParams& P, int nb, uint8_t* ib) {
+    constexpr int E = D / 32;
+    float v[E];
+    load_lane<E, T>(row, lane, sg, v);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    fwht_reg<E>(v);
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
+            v[e] = (lane & b) ? o - v[e] : v[e] + o;  // (lo + hi, lo - hi)
+        }
+    }
+    const float n = __fsqrt_rn(ss);
+    const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        int id = 0;
+        for (int j = 0; j < nb; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
+        ib[lane * E + e] = (uint8_t)id;
+    }
+    __syncwarp();
+    return n;
+}
+
+// Pack the D indices of ib into the dense LSB-first stream at dst (d * bits / 8
+// bytes, 4-byte aligned): lane l writes word l, stream bits [32 l, 32 l + 32).
+template <int D>
+__device__ __forceinline__ void warp_pack_row(const uint8_t* ib, int lane, int bits, uint8_t* dst) {
+    const int rb = D * bits / 8;
+    if (4 * lane < rb) {
+        const int b0 = 32 * lane;
+        const int i0 = b0 / bits, i1 = min(D - 1, (b0 + 31) / bits);
+        uint32_t word = 0u;
+        for (int i = i0; i <= i1; ++i) {
+            const int sh = i * bits - b0;
+            const uint32_t x = ib[i];
+            word |= sh >= 0 ? x << sh : x >> -sh;
+        }
+        reinterpret_cast<uint32_t*>(dst)[lane] = word;
+    }
+}
+
 }  // namespace dev
 }  // namespace tq

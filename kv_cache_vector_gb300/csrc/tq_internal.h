@@ -117,7 +117,7 @@ size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // [sms + 1], first and last CTA per (batch, KV head) [B * Hq] each (Hq bounds
 // Hkv), rounded up to 256 bytes.
 inline size_t attn3_meta_bytes(int B, int Hq, int sms) {
-    return ((size_t)4 * (2 * ((size_t)sms + 1) + 2 * (size_t)B * Hq) + 255) / 256 * 256;
+    return ((size_t)4 * (2 * ((size_t)sms + 1) + 2 * (size_t)B * Hq + (size_t)B) + 255) / 256 * 256;
 }
 inline size_t attn3_partial_bytes(int B, int Hq, int n_splits) {
     return ((size_t)4 * B * Hq * n_splits * 130 + 255) / 256 * 256;
@@ -141,13 +141,25 @@ struct PagedArgs {
     int max_pages;
     int page_shift;
 };
+// The decode step's append folded into the paged attention: one new K and V
+// row per (sequence, KV head), [B][Hkv][128] fp32 or bf16, written at the
+// position pa.lens[b] before the attention reads lengths pa.lens[b] + 1.
+struct AttnAppend {
+    const void* k_new;
+    const void* v_new;
+    bool bf16;
+    const RowParams* PK;
+    const RowParams* PV;
+};
 // d = 128 paged attention (tq_attn.cu, compiled in the d = 128 units); the
-// tq_cache_view carries the page arrays (its cap is unused).
+// tq_cache_view carries the page arrays (its cap is unused).  With `app`, the
+// rows of app are appended first (same launches, the append rides on the
+// query rotation).
 template <int KB>
 cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
                                  const tq_cache_view& pages, int64_t max_ctx, float* out,
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
-                                 const PagedArgs& pa, cudaStream_t s);
+                                 const PagedArgs& pa, cudaStream_t s, const AttnAppend* app = nullptr);
 // Paged append of one token per sequence, d >= 32 (tq_codec.cu).
 template <int D>
 cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,

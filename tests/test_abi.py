@@ -184,3 +184,16 @@ def test_paged_call_validation_before_launch(L):
                                   s) == 3
     assert L.tq_attn_decode_paged(h, A, 0, 8, 2, pc(), None, 4, None, 256, 4, 3, f(1.0), f(0.0), None,
                                   None, 0, s) == 0  # B = 0: no-op
+    # tq_attn_decode_append_paged(plan, q, k_new, v_new, kv_dtype, B, Hq, Hkv, cache, bt, max_pages,
+    #                             positions, max_ctx, kb, vb, scale, thr, out, ws, ws_bytes, s)
+    fa = L.tq_attn_decode_append_paged
+    assert fa(None, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
+    assert fa(h, A, A, A, 7, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2  # dtype
+    assert fa(h, A, A, A, 1, 1, 32, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2  # GQA 16
+    assert fa(p64.handle, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2
+    assert fa(h, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 257, 4, 3, f(1.0), f(0.0), A, A, W, s) == 4
+    assert fa(h, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, 16, s) == 5
+    assert fa(h, A, A + 8, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 3
+    assert fa(h, A, A, None, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
+    assert fa(h, A, None, None, 1, 0, 8, 2, pc(), None, 4, None, 256, 4, 3, f(1.0), f(0.0), None, None, 0,
+              s) == 0  # B = 0: no-op

@@ -207,3 +207,80 @@ def test_paged_append_then_attend():
         seq = (np.concatenate([kpb, kpn[:, None]], 1), np.concatenate([knb, knn[:, None]], 1),
                np.concatenate([vpb, vpn[:, None]], 1), np.concatenate([vnb, vnn[:, None]], 1))
         compare_attention(got[b][None], oracle_seq(s, q[b], seq, kb, vb, L + 1, scale)[None])
+
+
+@pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float32])
+def test_fused_append_attend_matches_two_calls(kv_dtype):
+    """tq_attn_decode_append_paged writes the same cache bytes as
+    tq_append_paged and returns what tq_attn_decode_paged returns over the
+    lengths + 1; both agree with the oracle over the grown sequences."""
+    lens, Hq, Hkv, page, kb, vb = [63, 64, 10, 1, 300], 8, 2, 64, 4, 3
+    d = 128
+    plan = abi.Plan(d, 42)
+    s, q, seqs, cache, bt, max_pages = make_paged(15, lens, Hq, Hkv, d, page, kb, vb, extra_slot=True)
+    B = len(lens)
+    k_new = synth.normal_rows(41, B * Hkv, d, kv_dtype, stream=1).reshape(B, Hkv, d)
+    v_new = synth.normal_rows(41, B * Hkv, d, kv_dtype, stream=2).reshape(B, Hkv, d)
+    pos = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    max_ctx = max(lens) + 1
+    twin = abi.PagedCache(*(t.clone() for t in (cache.k_packed, cache.k_norm, cache.v_packed, cache.v_norm)),
+                          kb, vb)
+    abi.tq_append_paged(plan, twin, k_new.cuda(), v_new.cuda(), bt, pos)
+    want = abi.tq_attn_decode_paged(plan, q.cuda(), twin, bt, pos + 1, max_ctx, scale)
+    got = abi.tq_attn_decode_append_paged(plan, q.cuda(), k_new.cuda(), v_new.cuda(), cache, bt, pos, max_ctx,
+                                          scale)
+    torch.cuda.synchronize()
+    assert abi.tq_device_status(reset=True) == 0
+    for a, b in zip((cache.k_packed, cache.k_norm, cache.v_packed, cache.v_norm),
+                    (twin.k_packed, twin.k_norm, twin.v_packed, twin.v_norm)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert torch.equal(got, want)
+    out = got.cpu().numpy()
+    for b, L in enumerate(lens):
+        kpn, knn = O.encode(s, kb, k_new[b].double().numpy())
+        vpn, vnn = O.encode(s, vb, v_new[b].double().numpy())
+        kpb, knb, vpb, vnb = seqs[b]
+        seq = (np.concatenate([kpb, kpn[:, None]], 1), np.concatenate([knb, knn[:, None]], 1),
+               np.concatenate([vpb, vpn[:, None]], 1), np.concatenate([vnb, vnn[:, None]], 1))
+        compare_attention(out[b][None], oracle_seq(s, q[b], seq, kb, vb, L + 1, scale)[None])
+
+
+def test_fused_append_attend_range_checks():
+    """A position out of range (negative, or on a -1 page) writes nothing,
+    sets status 42, and that sequence attends over min(position + 1, max_ctx)
+    rows (none for a negative position); the other sequences are unaffected."""
+    lens, Hq, Hkv, page, kb, vb = [40, 64, 5], 8, 2, 64, 3, 2
+    d = 128
+    plan = abi.Plan(d, 42)
+    s, q, seqs, cache, bt, max_pages = make_paged(16, lens, Hq, Hkv, d, page, kb, vb)
+    B = len(lens)
+    k_new = synth.normal_rows(42, B * Hkv, d, torch.bfloat16, stream=1).reshape(B, Hkv, d)
+    v_new = synth.normal_rows(42, B * Hkv, d, torch.bfloat16, stream=2).reshape(B, Hkv, d)
+    # sequence 0: a negative position; sequence 1: position 64, past max_pages * page_size (one
+    # page each here); sequence 2: a valid append at its length
+    pos = torch.tensor([-1, 64, 5], dtype=torch.int32, device="cuda")
+    before = [t.clone() for t in (cache.k_packed, cache.k_norm, cache.v_packed, cache.v_norm)]
+    scale = 1.0 / math.sqrt(d)
+    got = abi.tq_attn_decode_append_paged(plan, q.cuda(), k_new.cuda(), v_new.cuda(), cache, bt, pos, 64, scale)
+    torch.cuda.synchronize()
+    assert abi.tq_device_status(reset=True) == 42
+    btn = bt.cpu().numpy()
+    # bytes, not values: unused slots hold NaN norms
+    changed = [(t0.view(torch.uint8) != t1.view(torch.uint8)).reshape(t0.shape[0], Hkv, page, -1)
+               for t0, t1 in zip(before, (cache.k_packed, cache.k_norm, cache.v_packed, cache.v_norm))]
+    # only sequence 2's slot at position 5 changed
+    pg, off = btn[2, 0], 5
+    for c in changed:
+        c = c.cpu().numpy().copy()
+        c[pg, :, off] = False
+        assert not c.any()
+    out = got.cpu().numpy()
+    assert np.all(out[0] == 0)
+    compare_attention(out[1][None], oracle_seq(s, q[1], seqs[1], kb, vb, 64, scale)[None])
+    kpn, knn = O.encode(s, kb, k_new[2].double().numpy())
+    vpn, vnn = O.encode(s, vb, v_new[2].double().numpy())
+    kpb, knb, vpb, vnb = seqs[2]
+    seq = (np.concatenate([kpb, kpn[:, None]], 1), np.concatenate([knb, knn[:, None]], 1),
+           np.concatenate([vpb, vpn[:, None]], 1), np.concatenate([vnb, vnn[:, None]], 1))
+    compare_attention(out[2][None], oracle_seq(s, q[2], seq, kb, vb, 6, scale)[None])
