@@ -94,11 +94,33 @@ typedef struct {
  * Errors: TQ_ERR_INVALID_ARG (null), TQ_ERR_UNSUPPORTED (d or bits). */
 tq_status tq_codebook_init(int d, int bits, double *centroids, double *boundaries);
 
+/* The Lloyd-Max codebook of N(0, 1/d) (TQ_PLAN_GAUSSIAN_CODEBOOK), same
+ * layout; d >= 1. */
+tq_status tq_codebook_init_gaussian(int d, int bits, double *centroids, double *boundaries);
+
 /* Build a plan for head dimension d (power of two, 8..256) and sign seed
  * (the pages' fa_tq_init(head_dim, config, seed)).  Computes the codebooks
  * for bits 2, 3, 4 and the sign diagonal.  *out receives a host object that
  * the caller releases with tq_plan_destroy. */
 tq_status tq_plan_create(int d, uint64_t seed, tq_plan **out);
+
+/* Format variants of the plan, for interoperability with caches written by
+ * the turbo3/turbo4-style kernels ("CITATIONS", N(0, 1/d) codebook
+ * replacement; Two-sided Rademacher signs in WHT):
+ *   TQ_PLAN_GAUSSIAN_CODEBOOK: the Lloyd-Max codebook of N(0, 1/d), the
+ *     large-d limit of the coordinate density, instead of the exact one.
+ *   TQ_PLAN_TWO_SIDED_SIGNS: the rotation is S2 H S1 / sqrt(d), with s1 the
+ *     first d outputs of the seed's sign stream and s2 the next d; decode and
+ *     the attention's output rotation use S1 H S2 / sqrt(d).  Dot products are
+ *     preserved, so attention over such a cache is unchanged in form.
+ * tq_plan_create(d, seed, out) is tq_plan_create_ex(d, seed, 0, out).
+ * Errors: TQ_ERR_UNSUPPORTED for unknown flag bits, as tq_plan_create else. */
+enum { TQ_PLAN_GAUSSIAN_CODEBOOK = 1, TQ_PLAN_TWO_SIDED_SIGNS = 2 };
+tq_status tq_plan_create_ex(int d, uint64_t seed, uint32_t flags, tq_plan **out);
+
+/* The second sign vector s2 (d entries of -1/+1; all +1 without
+ * TQ_PLAN_TWO_SIDED_SIGNS). */
+tq_status tq_plan_signs2(const tq_plan *plan, int8_t *signs);
 tq_status tq_plan_destroy(tq_plan *plan);
 
 /* Inspection helpers (host memory): the d signs (+1/-1) of the plan, and the

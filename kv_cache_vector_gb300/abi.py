@@ -27,7 +27,7 @@ EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_sig
            "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes", "tq_attn_paged_workspace_bytes",
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
            "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged",
-           "tq_attn_decode_append_paged")
+           "tq_attn_decode_append_paged", "tq_plan_create_ex", "tq_plan_signs2", "tq_codebook_init_gaussian")
 
 
 class TQError(RuntimeError):
@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
     for name, res, args in [
         ("tq_codebook_init", i32, [i32, i32, vp, vp]),
         ("tq_plan_create", i32, [i32, u64, ctypes.POINTER(vp)]),
+        ("tq_plan_create_ex", i32, [i32, u64, ctypes.c_uint32, ctypes.POINTER(vp)]),
+        ("tq_plan_signs2", i32, [vp, vp]),
+        ("tq_codebook_init_gaussian", i32, [i32, i32, vp, vp]),
         ("tq_plan_destroy", i32, [vp]),
         ("tq_plan_signs", i32, [vp, vp]),
         ("tq_plan_codebook", i32, [vp, i32, vp, vp]),
@@ -121,17 +124,26 @@ def tq_codebook_init(d: int, bits: int):
     return c, b
 
 
-class Plan:
-    """Owns a tq_plan (host object: d, seed, signs, fp32 codebooks)."""
+PLAN_GAUSSIAN_CODEBOOK = 1  # TQ_PLAN_GAUSSIAN_CODEBOOK
+PLAN_TWO_SIDED_SIGNS = 2    # TQ_PLAN_TWO_SIDED_SIGNS
 
-    def __init__(self, d: int, seed: int):
+
+class Plan:
+    """Owns a tq_plan (host object: d, seed, format flags, signs, fp32 codebooks)."""
+
+    def __init__(self, d: int, seed: int, flags: int = 0):
         h = ctypes.c_void_p()
-        _check("tq_plan_create", lib().tq_plan_create(d, ctypes.c_uint64(seed), ctypes.byref(h)))
-        self.handle, self.d, self.seed = h, d, seed
+        _check("tq_plan_create_ex", lib().tq_plan_create_ex(d, ctypes.c_uint64(seed), flags, ctypes.byref(h)))
+        self.handle, self.d, self.seed, self.flags = h, d, seed, flags
 
     def signs(self) -> np.ndarray:
         s = np.empty(self.d, np.int8)
         _check("tq_plan_signs", lib().tq_plan_signs(self.handle, s.ctypes.data))
+        return s
+
+    def signs2(self) -> np.ndarray:
+        s = np.empty(self.d, np.int8)
+        _check("tq_plan_signs2", lib().tq_plan_signs2(self.handle, s.ctypes.data))
         return s
 
     def codebook(self, bits: int):
@@ -152,8 +164,16 @@ class Plan:
             pass
 
 
-def tq_plan_create(d: int, seed: int) -> Plan:
-    return Plan(d, seed)
+def tq_plan_create(d: int, seed: int, flags: int = 0) -> Plan:
+    return Plan(d, seed, flags)
+
+
+def tq_codebook_init_gaussian(d: int, bits: int):
+    """(centroids[2^b], boundaries[2^b - 1]) of N(0, 1/d), float64, on the host."""
+    c = np.empty(1 << bits, np.float64)
+    b = np.empty((1 << bits) - 1, np.float64)
+    _check("tq_codebook_init_gaussian", lib().tq_codebook_init_gaussian(d, bits, c.ctypes.data, b.ctypes.data))
+    return c, b
 
 
 def tq_encode(plan: Plan, bits: int, x: torch.Tensor, packed: torch.Tensor | None = None,

@@ -94,7 +94,7 @@ double cos_power_integral(int n, double T) {
     return w;
 }
 
-struct HalfDensity {
+struct SphereHalf {
     int d;
     double mass(double a, double b) const {  // 0 <= a <= b <= 1
         return cos_power_integral(d - 2, std::asin(b)) - cos_power_integral(d - 2, std::asin(a));
@@ -105,18 +105,37 @@ struct HalfDensity {
     }
 };
 
-// Lloyd iteration on the positive half-line (the density is symmetric and
-// log-concave, so the optimum is symmetric and unique): centroids are
+// N(0, 1/d), the large-d limit of the coordinate density ("CITATIONS", N(0,
+// 1/d) codebook replacement: after the transform the per-coordinate variance
+// is 1/d).  With sigma = 1/sqrt(d), the mass of [a, b] is
+// (erfc(a / (sigma sqrt 2)) - erfc(b / (sigma sqrt 2))) / 2 and the first
+// moment sigma^2 (phi(a) - phi(b)), phi the N(0, sigma^2) density; b may be
+// +infinity.
+struct GaussHalf {
+    double sigma;
+    double mass(double a, double b) const {
+        const double k = 1.0 / (sigma * std::sqrt(2.0));
+        return 0.5 * (std::erfc(a * k) - std::erfc(b * k));
+    }
+    double moment(double a, double b) const {
+        auto g = [&](double x) { return std::isinf(x) ? 0.0 : std::exp(-0.5 * (x / sigma) * (x / sigma)); };
+        return sigma / std::sqrt(2.0 * 3.14159265358979323846) * (g(a) - g(b));
+    }
+};
+
+// Lloyd iteration on the positive half-line (both densities are symmetric
+// and log-concave, so the optimum is symmetric and unique): centroids are
 // conditional means of their cells, interior boundaries midpoints of
 // neighbouring centroids.  Starts from cells evenly spread over
 // [0, 2.5/sqrt(d)] and runs until the centroids settle at rounding level.
-bool lloyd_half(int d, int bits, double* c, double* beta) {
+// `top` is the end of the support (1 for the sphere, +infinity for N(0, 1/d)).
+template <class Density>
+bool lloyd_half(const Density& f, int d, double top, int bits, double* c, double* beta) {
     const int H = (1 << bits) / 2;
-    HalfDensity f{d};
     double w = 2.5 / std::sqrt((double)d);
     if (w > 1.0) w = 1.0;
     beta[0] = 0.0;
-    beta[H] = 1.0;
+    beta[H] = top;
     for (int k = 1; k < H; ++k) beta[k] = w * k / H;
     double best = std::numeric_limits<double>::infinity();
     int stall = 0;
@@ -142,10 +161,13 @@ bool lloyd_half(int d, int bits, double* c, double* beta) {
     return false;
 }
 
-bool codebook(int d, int bits, double* cen, double* bnd) {
+bool codebook(int d, int bits, double* cen, double* bnd, bool gaussian = false) {
     const int L = 1 << bits, H = L / 2;
     double c[8], beta[9];
-    if (!lloyd_half(d, bits, c, beta)) return false;
+    const bool ok = gaussian ? lloyd_half(GaussHalf{1.0 / std::sqrt((double)d)}, d,
+                                          std::numeric_limits<double>::infinity(), bits, c, beta)
+                             : lloyd_half(SphereHalf{d}, d, 1.0, bits, c, beta);
+    if (!ok) return false;
     for (int k = 0; k < H; ++k) {
         cen[H + k] = c[k];
         cen[H - 1 - k] = -c[k];
@@ -169,8 +191,11 @@ bool lut_exact(const float* b32, int nb) {
 }
 
 void fill_row_params(const tq::Plan& P, int bits, tq::RowParams& R) {
-    for (int i = 0; i < tq::kMaxD; ++i)
+    for (int i = 0; i < tq::kMaxD; ++i) {
         R.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
+        R.sgn2[i] = (i < P.d && P.signs2[i] < 0) ? 0x80000000u : 0u;
+    }
+    R.two_sided = (P.flags & TQ_PLAN_TWO_SIDED_SIGNS) ? 1 : 0;
     for (int i = 0; i < 16; ++i) {
         R.cen[i] = P.c32[bits][i];
         R.bnd[i] = P.b32[bits][i];
@@ -247,7 +272,11 @@ void tq::set_last_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
 void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, float sparse_thr,
                           AttnParams& A) {
-    for (int i = 0; i < kMaxD; ++i) A.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
+    for (int i = 0; i < kMaxD; ++i) {
+        A.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
+        A.sgn2[i] = (i < P.d && P.signs2[i] < 0) ? 0x80000000u : 0u;
+    }
+    A.two_sided = (P.flags & TQ_PLAN_TWO_SIDED_SIGNS) ? 1 : 0;
     for (int i = 0; i < 16; ++i) {
         A.kcen[i] = P.c32[k_bits][i];
         A.vcen[i] = P.c32[v_bits][i];
@@ -272,20 +301,34 @@ tq_status tq_codebook_init(int d, int bits, double* centroids, double* boundarie
     return codebook(d, bits, centroids, boundaries) ? TQ_OK : TQ_ERR_UNSUPPORTED;
 }
 
-tq_status tq_plan_create(int d, uint64_t seed, tq_plan** out) {
+tq_status tq_codebook_init_gaussian(int d, int bits, double* centroids, double* boundaries) {
+    if (!centroids || !boundaries) return TQ_ERR_INVALID_ARG;
+    if (d < 1 || d > 65536 || bits < 1 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    return codebook(d, bits, centroids, boundaries, true) ? TQ_OK : TQ_ERR_UNSUPPORTED;
+}
+
+tq_status tq_plan_create(int d, uint64_t seed, tq_plan** out) { return tq_plan_create_ex(d, seed, 0u, out); }
+
+tq_status tq_plan_create_ex(int d, uint64_t seed, uint32_t flags, tq_plan** out) {
     if (!out) return TQ_ERR_INVALID_ARG;
     *out = nullptr;
+    if (flags & ~(uint32_t)(TQ_PLAN_GAUSSIAN_CODEBOOK | TQ_PLAN_TWO_SIDED_SIGNS)) return TQ_ERR_UNSUPPORTED;
     if (!is_pow2(d) || d < 8 || d > tq::kMaxD) return TQ_ERR_UNSUPPORTED;
     tq::Plan* P = new (std::nothrow) tq::Plan;
     if (!P) return TQ_ERR_NOMEM;
     std::memset(P, 0, sizeof(*P));
     P->d = d;
     P->seed = seed;
+    P->flags = flags;
+    // s1 = the stream's first d outputs; two-sided: s2 = the next d
     uint64_t st = seed;
     for (int i = 0; i < d; ++i) P->signs[i] = (splitmix64(st) >> 63) ? -1 : 1;
+    for (int i = 0; i < d; ++i)
+        P->signs2[i] = (flags & TQ_PLAN_TWO_SIDED_SIGNS) ? ((splitmix64(st) >> 63) ? -1 : 1) : 1;
+    const bool gauss = (flags & TQ_PLAN_GAUSSIAN_CODEBOOK) != 0;
     for (int bits = 1; bits <= 4; ++bits) {
         const int L = 1 << bits;
-        if (!codebook(d, bits, P->c64[bits], P->b64[bits])) {
+        if (!codebook(d, bits, P->c64[bits], P->b64[bits], gauss)) {
             delete P;
             return TQ_ERR_UNSUPPORTED;
         }
@@ -313,6 +356,13 @@ tq_status tq_plan_signs(const tq_plan* plan, int8_t* signs) {
     if (!plan || !signs) return TQ_ERR_INVALID_ARG;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
     std::memcpy(signs, P->signs, (size_t)P->d);
+    return TQ_OK;
+}
+
+tq_status tq_plan_signs2(const tq_plan* plan, int8_t* signs) {
+    if (!plan || !signs) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    std::memcpy(signs, P->signs2, (size_t)P->d);
     return TQ_OK;
 }
 

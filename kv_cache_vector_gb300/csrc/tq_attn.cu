@@ -79,7 +79,10 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         qrot[i] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
     }
     fwht_smem<D>(qrot, G);
-    for (int i = tid; i < G * D; i += blockDim.x) qrot[i] *= P.inv_sqrt_d * P.scale;
+    for (int i = tid; i < G * D; i += blockDim.x) {
+        const uint32_t m = P.two_sided ? P.sgn2[i % D] : 0u;
+        qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
+    }
     __syncthreads();
 
     const int64_t row0 = ((int64_t)b * Hkv + g) * cache.cap + t0;
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
         L = fmaf(f, base[s * (D + 2) + D + 1], L);
         a = fmaf(f, base[s * (D + 2) + j], a);
     }
-    o[j] = a / L;
+    o[j] = __uint_as_float(__float_as_uint(a / L) ^ (P.two_sided ? P.sgn2[j] : 0u));
     fwht_smem<D>(o, 1);
     out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }
@@ -430,7 +433,7 @@ __device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__
     const float x = __bfloat162float(q[(int64_t)bh * 128 + j]);
     v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
     fwht_smem<128>(v, 1);
-    const float y = v[j] * P.q_mul;
+    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u)) * P.q_mul;
     float a = fabsf(y);
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
     if ((j & 31) == 0) wmax[j >> 5] = a;
@@ -475,10 +478,11 @@ static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat
                                                                const __grid_constant__ RowParams PK,
                                                                const __grid_constant__ RowParams PV, int k_bits,
                                                                int v_bits, int32_t* __restrict__ len1, int* status) {
-    __shared__ uint32_t sg[128];
+    __shared__ uint32_t sg[128], sg2[128];
     __shared__ uint8_t ib[2][128];
     const int j = threadIdx.x;
     sg[j] = P.sgn[j];
+    sg2[j] = P.sgn2[j];
     const int b = blockIdx.x / Hq, h = blockIdx.x - b * Hq, G = Hq / Hkv;
     const int64_t p = __ldg(pa.lens + b);
     if (h == 0 && j == 0) len1[b] = p < 0 ? 0 : (p >= INT32_MAX ? INT32_MAX : (int32_t)(p + 1));
@@ -496,7 +500,8 @@ static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat
     }
     const int64_t drow = (((int64_t)page * Hkv + kvh) << pa.page_shift) + (p & ((int64_t(1) << pa.page_shift) - 1));
     const T* src = (is_v ? v_new : k_new) + ((int64_t)b * Hkv + kvh) * 128;
-    const float n = warp_encode_indices<128, T>(src, lane, sg, R, (1 << bits) - 1, ib[warp]);
+    const float n = warp_encode_indices<128, T>(src, lane, sg, P.two_sided ? sg2 : nullptr, R, (1 << bits) - 1,
+                                                ib[warp]);
     warp_pack_row<128>(ib[warp], lane, bits, (is_v ? cache.v_packed : cache.k_packed) + drow * (16 * bits));
     if (lane == 0) (is_v ? cache.v_norm : cache.k_norm)[drow] = n;
 }
@@ -1187,6 +1192,7 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
     }
     const float L = block128_sum(lsum, red);
     o[j] = L > 0.f ? a / L : 0.f;  // an empty context (paged, length 0) gives zeros
+    if (P.two_sided) o[j] = __uint_as_float(__float_as_uint(o[j]) ^ P.sgn2[j]);
     fwht_smem<128>(o, 1);
     out[(int64_t)bh * 128 + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }

@@ -53,6 +53,7 @@ __device__ __forceinline__ void encode_part(const T* __restrict__ row, uint8_t* 
     if constexpr (R == 2) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
     fwht_reg<E>(v);
     if constexpr (R == 2) fwht_cross<E>(v, p);
+    if (P.two_sided) flip_rotated<D>(v, p, P.sgn2);
     const float n = __fsqrt_rn(ss);
     // w = y * inv is the normalised coordinate u = (H s x / sqrt(d)) / n
     const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
@@ -175,11 +176,14 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
                                                                 const __grid_constant__ RowParams PV,
                                                                 const PagedArgs pa, int Hkv, int* status) {
     static_assert(D >= 32 && D <= kMaxD, "one warp per row");
-    __shared__ uint32_t sg[D];
+    __shared__ uint32_t sg[D], sg2[D];
     __shared__ uint8_t idxbuf[kAppWarps][D];
     const bool is_v = blockIdx.y == 1;
     const RowParams& P = is_v ? PV : PK;
-    for (int i = threadIdx.x; i < D; i += blockDim.x) sg[i] = P.sgn[i];
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        sg[i] = P.sgn[i];
+        sg2[i] = P.sgn2[i];
+    }
     __syncthreads();
     const int bits = is_v ? v_bits : k_bits;
     const int nb = (1 << bits) - 1;
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
     uint8_t* ib = idxbuf[warp];
     for (int64_t srow = (int64_t)blockIdx.x * kAppWarps + warp; srow < n_rows;
          srow += (int64_t)gridDim.x * kAppWarps) {
-        const float n = warp_encode_indices<D, T>(src + srow * D, lane, sg, P, nb, ib);
+        const float n = warp_encode_indices<D, T>(src + srow * D, lane, sg, P.two_sided ? sg2 : nullptr, P, nb, ib);
         int64_t drow;
         if constexpr (PAGED) {
             const int64_t b = srow / Hkv;
@@ -233,6 +237,7 @@ __device__ __forceinline__ void decode_part(const uint8_t* __restrict__ src, flo
     float v[E];
 #pragma unroll
     for (int i = 0; i < E; ++i) v[i] = cen_s[unpack_one<BITS>(w, i)];
+    if (P.two_sided) flip_rotated<D>(v, p, P.sgn2);
     fwht_reg<E>(v);
     if constexpr (R == 2) fwht_cross<E>(v, p);  // split -> contiguous
     const float sc = norm * P.inv_sqrt_d;
@@ -412,6 +417,7 @@ k_encode_tma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* 
         f2_split(sb, s2, s3);
         const float ss = (s0 + s1) + (s2 + s3);
         fwht_reg2<D>(v);
+        if (P.two_sided) flip_rotated<D>(v, 0, P.sgn2);
         const float n = __fsqrt_rn(ss);
         const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
         const float ks = inv * (float)kLutScale;
@@ -518,11 +524,12 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
     uint32_t* slot = reinterpret_cast<uint32_t*>(acce + kUmAcc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // B operand: element (n, k) = s_k * (-1)^popcount(n & k), stored like a
-    // TMA 128-byte-swizzled K-major tile (two 64-column halves of 16 KB).
+    // B operand: element (n, k) = s2_n * (-1)^popcount(n & k) * s_k (s2 all
+    // +1 unless the signs are two-sided), stored like a TMA 128-byte-swizzled
+    // K-major tile (two 64-column halves of 16 KB).
     for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
         const int n = i >> 7, k = i & 127;
-        const bool neg = ((__popc(n & k) & 1) != 0) != (P.sgn[k] != 0u);
+        const bool neg = (((__popc(n & k) & 1) != 0) != (P.sgn[k] != 0u)) != (P.sgn2[n] != 0u);
         const int off = (k >> 6) * 16384 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
         *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBF80u : 0x3F80u;
     }
@@ -799,6 +806,7 @@ __global__ void __launch_bounds__(128, 3) k_decode2(const uint8_t* __restrict__ 
         }
         float v[D];
         centroids_of<BITS, D>(w, cen_s, v);
+        if (P.two_sided) flip_rotated<D>(v, 0, P.sgn2);
         fwht_reg2<D>(v);
         const float scs = norm * P.inv_sqrt_d;
         const F2 sc = f2(scs, scs);
@@ -882,6 +890,7 @@ k_decode3(const uint8_t* __restrict__ packed, const float* __restrict__ norms, i
         fetch(tile + wstride);
         float v[D];
         centroids_of<BITS, D>(w, cen_s, v);
+        if (P.two_sided) flip_rotated<D>(v, 0, P.sgn2);
         fwht_reg2<D>(v);
         const float scs = norm * P.inv_sqrt_d;
         const F2 sc = f2(scs, scs);
@@ -1054,6 +1063,7 @@ k_decode_umma(const uint8_t* __restrict__ packed, const float* __restrict__ norm
                     if (sh + BITS <= 32) x = w[wi] >> sh;
                     else x = __funnelshift_r(w[wi], w[wi + 1], sh);
                     e[m] = *reinterpret_cast<const uint32_t*>(cb + ((x << 2) & (((1u << BITS) - 1) << 2)));
+                    if (P.two_sided && P.sgn2[i]) e[m] ^= 0x80008000u;  // both fp16 halves
                 }
                 uint4 h, l;
                 h.x = __byte_perm(e[0], e[1], 0x5410); l.x = __byte_perm(e[0], e[1], 0x7632);

@@ -31,6 +31,23 @@ struct RowShape {
     static constexpr int E = D / R;              // elements per thread
 };
 
+// Coordinate of element i of part p in the rotated domain.  With two threads
+// per row the rotated coordinates are split: part p holds [p E/2, (p+1) E/2)
+// and [E + p E/2, E + (p+1) E/2), the order of the packed row.
+template <int D>
+__device__ __forceinline__ int rotated_coord(int p, int i) {
+    constexpr int R = RowShape<D>::R, E = RowShape<D>::E;
+    if constexpr (R == 1) return i;
+    else return i < E / 2 ? p * (E / 2) + i : E + p * (E / 2) + (i - E / 2);
+}
+
+// Two-sided signs: flip the rotated-domain values of part p by s2.
+template <int D, int E>
+__device__ __forceinline__ void flip_rotated(float (&v)[E], int p, const uint32_t* sgn2) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ sgn2[rotated_coord<D>(p, i)]);
+}
+
 // ------------------------------------------------------------- load + sign
 
 // v[s] = s_i * x_i for the thread's E elements starting at element `first`
@@ -368,10 +385,12 @@ __device__ __forceinline__ void load_lane(const T* __restrict__ row, int lane, c
 
 // Sign-flip, transform and bucket one row; the indices go to ib[0, D) (a
 // per-warp byte buffer) and the row's L2 norm is returned.  sg: the sign masks
-// in shared memory; nb = 2^bits - 1 boundaries of P are used.
+// in shared memory; sg2: the second sign masks in shared memory (two-sided
+// signs) or null; nb = 2^bits - 1 boundaries of P are used.
 template <int D, typename T>
 __device__ __forceinline__ float warp_encode_indices(const T* __restrict__ row, int lane, const uint32_t* sg,
-                                                     const RowParams& P, int nb, uint8_t* ib) {
+                                                     const uint32_t* sg2, const RowParams& P, int nb,
+                                                     uint8_t* ib) {
     constexpr int E = D / 32;
     float v[E];
     load_lane<E, T>(row, lane, sg, v);
@@ -388,6 +407,10 @@ __device__ __forceinline__ float warp_encode_indices(const T* __restrict__ row, 
             const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
             v[e] = (lane & b) ? o - v[e] : v[e] + o;  // (lo + hi, lo - hi)
         }
+    }
+    if (sg2) {  // element e of lane l is rotated coordinate l E + e
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
     }
     const float n = __fsqrt_rn(ss);
     const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;

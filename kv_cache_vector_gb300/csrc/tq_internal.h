@@ -21,6 +21,10 @@ struct RowParams {
     float cen[16];        // fp32 centroids, ascending (2^bits used)
     float bnd[16];        // fp32 boundaries, ascending (2^bits - 1 used), rest +inf
     float inv_sqrt_d;
+    // Two-sided signs (R = S2 H S1 / sqrt(d)): masks of the second diagonal,
+    // applied after the forward transform and before the inverse one.
+    int two_sided;
+    uint32_t sgn2[kMaxD];
 };
 
 // Constants of the attention kernels.
@@ -38,13 +42,17 @@ struct AttnParams {
     float vcen_h[16];
     float q_mul;
     float out_mul;
+    int two_sided;  // as RowParams
+    uint32_t sgn2[kMaxD];
 };
 
 // Host plan (the public tq_plan).
 struct Plan {
     int d;
     uint64_t seed;
+    uint32_t flags;  // TQ_PLAN_* of tq_plan_create_ex
     int8_t signs[kMaxD];
+    int8_t signs2[kMaxD];  // all +1 unless TQ_PLAN_TWO_SIDED_SIGNS
     double c64[5][16], b64[5][16];  // index by bits (1..4)
     float c32[5][16], b32[5][16];
     // Per width: a scale s in [1, 2) that puts every c32 * s close to an fp16

@@ -46,24 +46,28 @@ def _lib():
     L.orc_splitmix64_next.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     L.orc_signs.argtypes = [ctypes.c_uint64, ctypes.c_int, _i8p]
     L.orc_fwht.argtypes = [_f64p, ctypes.c_int]
-    L.orc_rotate.argtypes = [_i8p, ctypes.c_int, _f64p, _f64p]
-    L.orc_unrotate.argtypes = [_i8p, ctypes.c_int, _f64p, _f64p]
+    L.orc_rotate.argtypes = [_i8p, _i8p, ctypes.c_int, _f64p, _f64p]
+    L.orc_unrotate.argtypes = [_i8p, _i8p, ctypes.c_int, _f64p, _f64p]
     L.orc_codebook.restype = ctypes.c_int
     L.orc_codebook.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p]
     L.orc_codebook_mse.restype = ctypes.c_double
     L.orc_codebook_mse.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p]
+    L.orc_codebook_gauss.restype = ctypes.c_int
+    L.orc_codebook_gauss.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p]
+    L.orc_codebook_gauss_mse.restype = ctypes.c_double
+    L.orc_codebook_gauss_mse.argtypes = [ctypes.c_int, ctypes.c_int, _f64p, _f64p]
     L.orc_density_mass.restype = ctypes.c_double
     L.orc_density_mass.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double]
     L.orc_bucket.restype = ctypes.c_int
     L.orc_bucket.argtypes = [ctypes.c_float, ctypes.c_int, _f32p]
     L.orc_pack.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, _u8p]
     L.orc_unpack.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, _u8p]
-    L.orc_encode.argtypes = [_i8p, ctypes.c_int, ctypes.c_int, _f32p, _f64p,
+    L.orc_encode.argtypes = [_i8p, _i8p, ctypes.c_int, ctypes.c_int, _f32p, _f64p,
                              ctypes.c_int64, _u8p, _f32p, _f64p]
-    L.orc_decode.argtypes = [_i8p, ctypes.c_int, ctypes.c_int, _f32p, _u8p, _f32p,
+    L.orc_decode.argtypes = [_i8p, _i8p, ctypes.c_int, ctypes.c_int, _f32p, _u8p, _f32p,
                              ctypes.c_int64, _f64p]
     L.orc_attention.argtypes = [
-        _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+        _i8p, _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_int, _f32p, _u8p, _f32p, ctypes.c_int, _f32p, _u8p,
         _f32p, _f64p, ctypes.c_double, ctypes.c_double, _f64p, _i64p]
     return L
@@ -86,6 +90,19 @@ def signs(seed: int, d: int) -> np.ndarray:
     return s
 
 
+def signs2(seed: int, d: int) -> np.ndarray:
+    """Second sign vector of the two-sided rotation ("CITATIONS", Two-sided
+    Rademacher signs in WHT): outputs d .. 2d - 1 of the same splitmix64
+    stream, s2_i = -1 iff the top bit is set."""
+    s = np.empty(2 * d, np.int8)
+    _lib().orc_signs(ctypes.c_uint64(seed), 2 * d, _p(s, _i8p))
+    return np.ascontiguousarray(s[d:])
+
+
+def _s2p(s2):
+    return None if s2 is None else _p(np.ascontiguousarray(s2, np.int8), _i8p)
+
+
 def fwht(v: np.ndarray) -> np.ndarray:
     out = np.ascontiguousarray(v, dtype=np.float64).copy()
     for row in out.reshape(-1, out.shape[-1]):
@@ -93,31 +110,33 @@ def fwht(v: np.ndarray) -> np.ndarray:
     return out
 
 
-def rotate(s: np.ndarray, x: np.ndarray) -> np.ndarray:
+def rotate(s: np.ndarray, x: np.ndarray, s2: np.ndarray | None = None) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.empty_like(x)
     d = x.shape[-1]
     for xr, yr in zip(x.reshape(-1, d), y.reshape(-1, d)):
-        _lib().orc_rotate(_p(s, _i8p), d, _p(xr, _f64p), _p(yr, _f64p))
+        _lib().orc_rotate(_p(s, _i8p), _s2p(s2), d, _p(xr, _f64p), _p(yr, _f64p))
     return y
 
 
-def unrotate(s: np.ndarray, y: np.ndarray) -> np.ndarray:
+def unrotate(s: np.ndarray, y: np.ndarray, s2: np.ndarray | None = None) -> np.ndarray:
     y = np.ascontiguousarray(y, dtype=np.float64)
     x = np.empty_like(y)
     d = y.shape[-1]
     for yr, xr in zip(y.reshape(-1, d), x.reshape(-1, d)):
-        _lib().orc_unrotate(_p(s, _i8p), d, _p(yr, _f64p), _p(xr, _f64p))
+        _lib().orc_unrotate(_p(s, _i8p), _s2p(s2), d, _p(yr, _f64p), _p(xr, _f64p))
     return x
 
 
 @lru_cache(maxsize=None)
-def codebook(d: int, bits: int):
-    """(centroids[2^b], boundaries[2^b - 1], iterations), double precision."""
+def codebook(d: int, bits: int, kind: str = "sphere"):
+    """(centroids[2^b], boundaries[2^b - 1], iterations), double precision.
+    kind "sphere": the exact coordinate density; "gauss": N(0, 1/d)."""
     L = 1 << bits
     c = np.empty(L, np.float64)
     b = np.empty(L - 1, np.float64)
-    it = _lib().orc_codebook(d, bits, _p(c, _f64p), _p(b, _f64p))
+    fn = {"sphere": _lib().orc_codebook, "gauss": _lib().orc_codebook_gauss}[kind]
+    it = fn(d, bits, _p(c, _f64p), _p(b, _f64p))
     if it < 0:
         raise RuntimeError(f"oracle codebook failed for d={d} bits={bits}")
     c.setflags(write=False)
@@ -125,16 +144,17 @@ def codebook(d: int, bits: int):
     return c, b, it
 
 
-def codebook_f32(d: int, bits: int):
+def codebook_f32(d: int, bits: int, kind: str = "sphere"):
     """The stored (fp32) form of the codebook."""
-    c, b, _ = codebook(d, bits)
+    c, b, _ = codebook(d, bits, kind)
     return c.astype(np.float32), b.astype(np.float32)
 
 
-def codebook_mse(d: int, bits: int, c: np.ndarray, b: np.ndarray) -> float:
+def codebook_mse(d: int, bits: int, c: np.ndarray, b: np.ndarray, kind: str = "sphere") -> float:
     c = np.ascontiguousarray(c, np.float64)
     b = np.ascontiguousarray(b, np.float64)
-    return _lib().orc_codebook_mse(d, bits, _p(c, _f64p), _p(b, _f64p))
+    fn = {"sphere": _lib().orc_codebook_mse, "gauss": _lib().orc_codebook_gauss_mse}[kind]
+    return fn(d, bits, _p(c, _f64p), _p(b, _f64p))
 
 
 def density_mass(d: int, a: float, b: float) -> float:
@@ -164,48 +184,51 @@ def unpack(packed: np.ndarray, d: int, bits: int) -> np.ndarray:
     return out
 
 
-def encode(s: np.ndarray, bits: int, x: np.ndarray, want_u: bool = False):
+def encode(s: np.ndarray, bits: int, x: np.ndarray, want_u: bool = False, s2: np.ndarray | None = None,
+           kind: str = "sphere"):
     """x: [n, d] (any real dtype; converted exactly to double).
-    Returns packed [n, d*bits/8] uint8, norms [n] float32 (and u [n, d])."""
+    Returns packed [n, d*bits/8] uint8, norms [n] float32 (and u [n, d]).
+    s2: the second signs of a two-sided rotation; kind: the codebook."""
     x = np.ascontiguousarray(x, np.float64)
     n, d = x.shape
-    _, bnd = codebook_f32(d, bits)
+    _, bnd = codebook_f32(d, bits, kind)
     packed = np.empty((n, d * bits // 8), np.uint8)
     norms = np.empty(n, np.float32)
     u = np.empty((n, d), np.float64) if want_u else None
-    _lib().orc_encode(_p(s, _i8p), d, bits, _p(bnd, _f32p), _p(x, _f64p), n,
+    _lib().orc_encode(_p(s, _i8p), _s2p(s2), d, bits, _p(bnd, _f32p), _p(x, _f64p), n,
                       _p(packed, _u8p), _p(norms, _f32p),
                       _p(u, _f64p) if want_u else None)
     return (packed, norms, u) if want_u else (packed, norms)
 
 
-def decode(s: np.ndarray, bits: int, packed: np.ndarray, norms: np.ndarray) -> np.ndarray:
+def decode(s: np.ndarray, bits: int, packed: np.ndarray, norms: np.ndarray, s2: np.ndarray | None = None,
+           kind: str = "sphere") -> np.ndarray:
     packed = np.ascontiguousarray(packed, np.uint8)
     norms = np.ascontiguousarray(norms, np.float32)
     n = norms.shape[0]
     d = packed.shape[-1] * 8 // bits
-    cen, _ = codebook_f32(d, bits)
+    cen, _ = codebook_f32(d, bits, kind)
     out = np.empty((n, d), np.float64)
-    _lib().orc_decode(_p(s, _i8p), d, bits, _p(cen, _f32p), _p(packed, _u8p),
+    _lib().orc_decode(_p(s, _i8p), _s2p(s2), d, bits, _p(cen, _f32p), _p(packed, _u8p),
                       _p(norms, _f32p), n, _p(out, _f64p))
     return out
 
 
 def attention(s, q, k_packed, k_norm, v_packed, v_norm, k_bits, v_bits, ctx_len,
-              scale, sparse_thr=0.0, want_kept=False):
+              scale, sparse_thr=0.0, want_kept=False, s2=None, kind="sphere"):
     """q: [B, Hq, d]; k_packed: [B, Hkv, cap, d*kb/8]; k_norm: [B, Hkv, cap]."""
     q = np.ascontiguousarray(q, np.float64)
     B, Hq, d = q.shape
     Hkv, cap = k_norm.shape[1], k_norm.shape[2]
-    kc, _ = codebook_f32(d, k_bits)
-    vc, _ = codebook_f32(d, v_bits)
+    kc, _ = codebook_f32(d, k_bits, kind)
+    vc, _ = codebook_f32(d, v_bits, kind)
     k_packed = np.ascontiguousarray(k_packed, np.uint8)
     v_packed = np.ascontiguousarray(v_packed, np.uint8)
     k_norm = np.ascontiguousarray(k_norm, np.float32)
     v_norm = np.ascontiguousarray(v_norm, np.float32)
     out = np.empty((B, Hq, d), np.float64)
     kept = np.empty((B, Hq), np.int64)
-    _lib().orc_attention(_p(s, _i8p), d, B, Hq, Hkv, cap, ctx_len, k_bits,
+    _lib().orc_attention(_p(s, _i8p), _s2p(s2), d, B, Hq, Hkv, cap, ctx_len, k_bits,
                          _p(kc, _f32p), _p(k_packed, _u8p), _p(k_norm, _f32p),
                          v_bits, _p(vc, _f32p), _p(v_packed, _u8p), _p(v_norm, _f32p),
                          _p(q, _f64p), float(scale), float(sparse_thr), _p(out, _f64p),

@@ -58,18 +58,21 @@ void orc_fwht(double *v, int d) {
 
 /* [FS] As-Built Note 1: the sign diagonal is applied before the FWHT,
  * rotate(x) = H (D x) / sqrt(d). */
-void orc_rotate(const int8_t *s, int d, const double *x, double *y) {
+void orc_rotate(const int8_t *s, const int8_t *s2, int d, const double *x, double *y) {
     for (int i = 0; i < d; ++i) y[i] = (double)s[i] * x[i];
     orc_fwht(y, d);
     double inv = 1.0 / sqrt((double)d);
     for (int i = 0; i < d; ++i) y[i] *= inv;
+    /* "CITATIONS", Two-sided Rademacher signs in WHT: signs2 after the butterfly */
+    if (s2)
+        for (int i = 0; i < d; ++i) y[i] *= (double)s2[i];
 }
 
 /* [FS] Hadamard Transform Detail: "Inverse: same operation (FWHT is its own
  * inverse up to scaling, and D is its own inverse)", applied in reverse
  * order: x = D H y / sqrt(d). */
-void orc_unrotate(const int8_t *s, int d, const double *y, double *x) {
-    for (int i = 0; i < d; ++i) x[i] = y[i];
+void orc_unrotate(const int8_t *s, const int8_t *s2, int d, const double *y, double *x) {
+    for (int i = 0; i < d; ++i) x[i] = s2 ? (double)s2[i] * y[i] : y[i];
     orc_fwht(x, d);
     double inv = 1.0 / sqrt((double)d);
     for (int i = 0; i < d; ++i) x[i] = (double)s[i] * x[i] * inv;
@@ -221,6 +224,88 @@ int orc_codebook(int d, int bits, double *centroids, double *boundaries) {
     return converged ? it : -1;
 }
 
+/* ---------------------------------------------- Gaussian codebook
+ * "CITATIONS", N(0, 1/d) codebook replacement: the Lloyd-Max codebook of a
+ * Gaussian with variance 1/d (the per-coordinate variance after the
+ * transform).  For X ~ N(0, sigma^2) and a cell (a, b) (a = -inf or b = +inf
+ * allowed): P = (erfc(a/(sigma sqrt 2)) - erfc(b/(sigma sqrt 2))) / 2 and
+ * E[X 1{a<X<b}] = sigma^2 (phi(a) - phi(b)), phi the N(0, sigma^2) density.
+ * All 2^b cells are iterated (no use of symmetry), from levels evenly spread
+ * over [-3 sigma, 3 sigma].  The iteration converges linearly and slowly, so
+ * it runs until the step reaches rounding level: no centroid moves by more
+ * than 1e-15 sigma, or the step has stayed below 1e-13 sigma without a new
+ * minimum for 2000 iterations (the floor set by the libm's erfc and exp). */
+static double gauss_pdf(double x, double sigma) {
+    if (isinf(x)) return 0.0;
+    double z = x / sigma;
+    return exp(-0.5 * z * z) / (sigma * sqrt(2.0 * M_PI));
+}
+static double gauss_mass(double a, double b, double sigma) {
+    double k = 1.0 / (sigma * sqrt(2.0));
+    return 0.5 * (erfc(a * k) - erfc(b * k));
+}
+
+int orc_codebook_gauss(int d, int bits, double *centroids, double *boundaries) {
+    int L = 1 << bits;
+    double sigma = 1.0 / sqrt((double)d);
+    double c[16];
+    for (int i = 0; i < L; ++i) c[i] = sigma * (-3.0 + 6.0 * (i + 0.5) / L);
+    double best = INFINITY;
+    int stall = 0;
+    for (int it = 1; it <= 2000000; ++it) {
+        double moved = 0.0;
+        double edge[17];
+        edge[0] = -INFINITY;
+        edge[L] = INFINITY;
+        for (int i = 1; i < L; ++i) edge[i] = 0.5 * (c[i - 1] + c[i]);
+        for (int i = 0; i < L; ++i) {
+            double p = gauss_mass(edge[i], edge[i + 1], sigma);
+            double m1 = sigma * sigma * (gauss_pdf(edge[i], sigma) - gauss_pdf(edge[i + 1], sigma));
+            double ci = m1 / p;
+            if (!isfinite(ci)) return -1;
+            if (fabs(ci - c[i]) > moved) moved = fabs(ci - c[i]);
+            c[i] = ci;
+        }
+        if (moved < best) {
+            best = moved;
+            stall = 0;
+        } else {
+            ++stall;
+        }
+        if (moved < 1e-15 * sigma || (best < 1e-13 * sigma && stall > 2000)) {
+            /* The density is symmetric, so the exact quantiser is: remove the
+             * rounding-level asymmetry, which puts the middle boundary at 0. */
+            for (int i = 0; i < L / 2; ++i) {
+                double a = 0.5 * (c[L - 1 - i] - c[i]);
+                c[i] = -a;
+                c[L - 1 - i] = a;
+            }
+            for (int i = 0; i < L; ++i) centroids[i] = c[i];
+            for (int i = 1; i < L; ++i) boundaries[i - 1] = 0.5 * (c[i - 1] + c[i]);
+            return it;
+        }
+    }
+    return -1;
+}
+
+/* E[(X - Q(X))^2] for X ~ N(0, 1/d): per cell, the second moment about the
+ * centroid, sigma^2 P + sigma^2 (a phi(a) - b phi(b)) - 2 c sigma^2 (phi(a) -
+ * phi(b)) + c^2 P, with x phi(x) = 0 at infinity. */
+double orc_codebook_gauss_mse(int d, int bits, const double *centroids, const double *boundaries) {
+    int L = 1 << bits;
+    double sigma = 1.0 / sqrt((double)d), s2 = sigma * sigma, mse = 0.0;
+    for (int i = 0; i < L; ++i) {
+        double a = (i == 0) ? -INFINITY : boundaries[i - 1];
+        double b = (i == L - 1) ? INFINITY : boundaries[i];
+        double p = gauss_mass(a, b, sigma);
+        double pa = gauss_pdf(a, sigma), pb = gauss_pdf(b, sigma);
+        double apa = isinf(a) ? 0.0 : a * pa, bpb = isinf(b) ? 0.0 : b * pb;
+        double m1 = s2 * (pa - pb), m2 = s2 * p + s2 * (apa - bpb);
+        mse += m2 - 2.0 * centroids[i] * m1 + centroids[i] * centroids[i] * p;
+    }
+    return mse;
+}
+
 double orc_codebook_mse(int d, int bits, const double *centroids,
                         const double *boundaries) {
     gl_init();
@@ -280,7 +365,7 @@ void orc_unpack(const uint8_t *in, int d, int bits, uint8_t *idx) {
 
 /* --------------------------------------------------------- encode/decode */
 
-void orc_encode(const int8_t *s, int d, int bits, const float *boundaries,
+void orc_encode(const int8_t *s, const int8_t *s2, int d, int bits, const float *boundaries,
                 const double *x, int64_t n_rows, uint8_t *packed, float *norms,
                 double *u_out) {
     int rb = d * bits / 8;
@@ -291,7 +376,7 @@ void orc_encode(const int8_t *s, int d, int bits, const float *boundaries,
         double ss = 0.0;
         for (int i = 0; i < d; ++i) ss += xr[i] * xr[i];
         double n = sqrt(ss);                     /* [FS] As-Built Note 2 */
-        orc_rotate(s, d, xr, y);
+        orc_rotate(s, s2, d, xr, y);
         norms[r] = (float)n;                     /* stored fp32 ([LS] 2.2) */
         for (int i = 0; i < d; ++i) {
             double u = (n > 0.0) ? y[i] / n : 0.0;
@@ -304,7 +389,7 @@ void orc_encode(const int8_t *s, int d, int bits, const float *boundaries,
     free(idx);
 }
 
-void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
+void orc_decode(const int8_t *s, const int8_t *s2, int d, int bits, const float *centroids,
                 const uint8_t *packed, const float *norms, int64_t n_rows,
                 double *out) {
     int rb = d * bits / 8;
@@ -314,7 +399,7 @@ void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
         orc_unpack(packed + r * rb, d, bits, idx);
         for (int i = 0; i < d; ++i) c[i] = (double)centroids[idx[i]];
         double *o = out + r * d;
-        orc_unrotate(s, d, c, o);
+        orc_unrotate(s, s2, d, c, o);
         for (int i = 0; i < d; ++i) o[i] *= (double)norms[r];
     }
     free(c);
@@ -323,7 +408,7 @@ void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
 
 /* ------------------------------------------------------------ attention */
 
-void orc_attention(const int8_t *s, int d, int B, int Hq, int Hkv, int64_t cap,
+void orc_attention(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int Hkv, int64_t cap,
                    int64_t ctx_len, int k_bits, const float *k_centroids,
                    const uint8_t *k_packed, const float *k_norm, int v_bits,
                    const float *v_centroids, const uint8_t *v_packed,
@@ -337,9 +422,9 @@ void orc_attention(const int8_t *s, int d, int B, int Hq, int Hkv, int64_t cap,
     for (int b = 0; b < B; ++b) {
         for (int g = 0; g < Hkv; ++g) {
             int64_t row0 = ((int64_t)b * Hkv + g) * cap;
-            orc_decode(s, d, k_bits, k_centroids, k_packed + row0 * rbk,
+            orc_decode(s, s2, d, k_bits, k_centroids, k_packed + row0 * rbk,
                        k_norm + row0, ctx_len, kh);
-            orc_decode(s, d, v_bits, v_centroids, v_packed + row0 * rbv,
+            orc_decode(s, s2, d, v_bits, v_centroids, v_packed + row0 * rbv,
                        v_norm + row0, ctx_len, vh);
             for (int hh = 0; hh < G; ++hh) {
                 int h = g * G + hh;

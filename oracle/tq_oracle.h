@@ -61,10 +61,19 @@ void orc_signs(uint64_t seed, int d, int8_t *s);
  * [FS] Hadamard Transform Detail. */
 void orc_fwht(double *v, int d);
 
-/* y = H (s . x) / sqrt(d)   ([FS] As-Built Note 1, Hadamard Transform Detail) */
-void orc_rotate(const int8_t *s, int d, const double *x, double *y);
-/* x = s . (H y) / sqrt(d)   (the inverse: H/sqrt(d) and D are self-inverse) */
-void orc_unrotate(const int8_t *s, int d, const double *y, double *x);
+/* y = H (s . x) / sqrt(d)   ([FS] As-Built Note 1, Hadamard Transform Detail);
+ * with s2 (not NULL) y = s2 . H (s . x) / sqrt(d) ([AC] Two-sided Rademacher
+ * signs in WHT: signs1 before, signs2 after the butterfly). */
+void orc_rotate(const int8_t *s, const int8_t *s2, int d, const double *x, double *y);
+/* x = s . (H y) / sqrt(d)   (the inverse: H/sqrt(d) and D are self-inverse);
+ * with s2: x = s . H (s2 . y) / sqrt(d). */
+void orc_unrotate(const int8_t *s, const int8_t *s2, int d, const double *y, double *x);
+
+/* Lloyd-Max codebook of N(0, 1/d) ([AC] N(0,1/d) codebook replacement): same
+ * layout as orc_codebook; returns the iteration count, or -1. */
+int orc_codebook_gauss(int d, int bits, double *centroids, double *boundaries);
+/* E[(X - Q(X))^2] of a codebook for X ~ N(0, 1/d). */
+double orc_codebook_gauss_mse(int d, int bits, const double *centroids, const double *boundaries);
 
 /* Lloyd-Max codebook for one coordinate of a uniform unit vector in R^d,
  * 2^bits levels, bits in [1, 8], d >= 3.  Writes 2^bits centroids and
@@ -92,12 +101,13 @@ void orc_unpack(const uint8_t *in, int d, int bits, uint8_t *idx);
  *  packed: [n_rows][d*bits/8], norms: [n_rows] fp32 (round to nearest of the
  *  exact-in-double L2 norm).  u_out (optional, may be NULL): [n_rows][d], the
  *  normalised rotated coordinate in double before the fp32 decision. */
-void orc_encode(const int8_t *s, int d, int bits, const float *boundaries,
+void orc_encode(const int8_t *s, const int8_t *s2, int d, int bits, const float *boundaries,
                 const double *x, int64_t n_rows, uint8_t *packed, float *norms,
                 double *u_out);
 
-/* Decode: x_hat = norm * s . (H c_idx) / sqrt(d), in double. */
-void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
+/* Decode: x_hat = norm * s . (H c_idx) / sqrt(d), in double (with s2:
+ * norm * s . H (s2 . c_idx) / sqrt(d)).  s2 may be NULL in every call. */
+void orc_decode(const int8_t *s, const int8_t *s2, int d, int bits, const float *centroids,
                 const uint8_t *packed, const float *norms, int64_t n_rows,
                 double *out);
 
@@ -109,7 +119,7 @@ void orc_decode(const int8_t *s, int d, int bits, const float *centroids,
  *  o = sum_t p_t v_hat_t, where rows with exp(sigma_t - max) < sparse_thr
  *  contribute zero (sparse_thr = 0: dense).
  *  out: [B][Hq][d] double; kept (optional): [B][Hq] number of V rows used. */
-void orc_attention(const int8_t *s, int d, int B, int Hq, int Hkv, int64_t cap,
+void orc_attention(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int Hkv, int64_t cap,
                    int64_t ctx_len, int k_bits, const float *k_centroids,
                    const uint8_t *k_packed, const float *k_norm, int v_bits,
                    const float *v_centroids, const uint8_t *v_packed,

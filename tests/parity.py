@@ -24,15 +24,16 @@ DECODE_REL = 1e-5
 ATTN_ATOL = 2e-3
 
 
-def compare_encode(s, bits, x64, gpu_packed, gpu_norms):
-    """Returns a dict of statistics; raises AssertionError on a violation."""
+def compare_encode(s, bits, x64, gpu_packed, gpu_norms, s2=None, kind="sphere"):
+    """Returns a dict of statistics; raises AssertionError on a violation.
+    s2 / kind: the plan's format variant (second signs, codebook kind)."""
     n, d = x64.shape
-    opk, onm, u = O.encode(s, bits, x64, want_u=True)
+    opk, onm, u = O.encode(s, bits, x64, want_u=True, s2=s2, kind=kind)
     gi = O.unpack(gpu_packed, d, bits)
     oi = O.unpack(opk, d, bits)
     diff = gi != oi
     ndiff = int(diff.sum())
-    _, bnd = O.codebook_f32(d, bits)
+    _, bnd = O.codebook_f32(d, bits, kind)
     dist = np.min(np.abs(u[..., None] - bnd.astype(np.float64)), axis=-1)
     near_pop = float((dist <= NEAR_BOUNDARY).mean())
     if ndiff:
@@ -53,9 +54,9 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.where(ax > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def compare_decode(s, bits, packed, norms, gpu_out, bf16: bool):
+def compare_decode(s, bits, packed, norms, gpu_out, bf16: bool, s2=None, kind="sphere"):
     n = norms.shape[0]
-    want = O.decode(s, bits, packed, norms)
+    want = O.decode(s, bits, packed, norms, s2=s2, kind=kind)
     d = want.shape[1]
     got = gpu_out.astype(np.float64)
     tol = DECODE_REL * np.linalg.norm(want, axis=1, keepdims=True) / math.sqrt(d)

@@ -57,6 +57,37 @@ def test_plan_signs_and_codebooks(L, seed, d):
     p.close()
 
 
+@pytest.mark.parametrize("d", [1, 8, 64, 128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_gaussian_codebook_matches_oracle(L, d, bits):
+    """N(0, 1/d) codebooks: the library's (positive half, mirrored) and the
+    oracle's (all cells) agree to rounding, and identically after fp32."""
+    c, b = abi.tq_codebook_init_gaussian(d, bits)
+    oc, ob, _ = O.codebook(d, bits, "gauss")
+    scale = 1.0 / math.sqrt(d)
+    assert np.max(np.abs(c - oc)) < 1e-12 * scale
+    assert np.max(np.abs(b - ob)) < 1e-12 * scale
+    assert np.array_equal(c.astype(np.float32), oc.astype(np.float32))
+    assert np.array_equal(b.astype(np.float32), ob.astype(np.float32))
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3])
+@pytest.mark.parametrize("d", [8, 128, 256])
+def test_plan_format_variants(L, flags, d):
+    """Plan flags: the codebook kind and the second sign vector follow the
+    oracle's definitions; s1 does not change."""
+    p = abi.Plan(d, 42, flags)
+    kind = "gauss" if flags & abi.PLAN_GAUSSIAN_CODEBOOK else "sphere"
+    assert np.array_equal(p.signs(), O.signs(42, d))
+    want2 = O.signs2(42, d) if flags & abi.PLAN_TWO_SIDED_SIGNS else np.ones(d, np.int8)
+    assert np.array_equal(p.signs2(), want2)
+    for bits in (2, 3, 4):
+        c, b = p.codebook(bits)
+        oc, ob = O.codebook_f32(d, bits, kind)
+        assert np.array_equal(c, oc) and np.array_equal(b, ob)
+    p.close()
+
+
 def test_codebook_and_plan_argument_errors(L):
     c = np.empty(16)
     b = np.empty(15)
@@ -67,6 +98,11 @@ def test_codebook_and_plan_argument_errors(L):
     for d in (0, 4, 96, 512):
         assert L.tq_plan_create(d, 1, ctypes.byref(h)) == 2
     assert L.tq_plan_create(128, 1, None) == 1
+    assert L.tq_plan_create_ex(128, 1, 4, ctypes.byref(h)) == 2  # unknown flag bit
+    assert L.tq_plan_create_ex(96, 1, 1, ctypes.byref(h)) == 2
+    assert L.tq_codebook_init_gaussian(0, 2, c.ctypes.data, b.ctypes.data) == 2
+    assert L.tq_codebook_init_gaussian(128, 5, c.ctypes.data, b.ctypes.data) == 2
+    assert L.tq_plan_signs2(None, c.ctypes.data) == 1
     assert L.tq_status_string(0) == b"ok"
 
 
