@@ -70,6 +70,10 @@ def _lib():
         _i8p, _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_int, _f32p, _u8p, _f32p, ctypes.c_int, _f32p, _u8p,
         _f32p, _f64p, ctypes.c_double, ctypes.c_double, _f64p, _i64p]
+    L.orc_attention_prefill.argtypes = [
+        _i8p, _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+        ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _f32p, _u8p, _f32p, ctypes.c_int, _f32p, _u8p, _f32p,
+        _f64p, ctypes.c_double, _f64p]
     return L
 
 
@@ -234,3 +238,28 @@ def attention(s, q, k_packed, k_norm, v_packed, v_norm, k_bits, v_bits, ctx_len,
                          _p(q, _f64p), float(scale), float(sparse_thr), _p(out, _f64p),
                          _p(kept, _i64p))
     return (out, kept) if want_kept else out
+
+
+def attention_prefill(s, q, k_packed, k_norm, v_packed, v_norm, k_bits, v_bits, q_start, scale, s2=None,
+                      kind="sphere"):
+    """Prefill attention, plain definition. q: [B, T, Hq, d]; k_packed:
+    [B, Hkv, cap, d*kb/8]; q_start: [B] (token t of sequence b sits at
+    q_start[b] + t and attends causally). Returns [B, T, Hq, d]."""
+    q = np.ascontiguousarray(q, np.float64)
+    B, T, Hq, d = q.shape
+    Hkv, cap = k_norm.shape[1], k_norm.shape[2]
+    kc, _ = codebook_f32(d, k_bits, kind)
+    vc, _ = codebook_f32(d, v_bits, kind)
+    qs = np.ascontiguousarray(q_start, np.int32)
+    assert np.all(qs >= 0) and np.all(qs + T <= cap)
+    k_packed = np.ascontiguousarray(k_packed, np.uint8)
+    v_packed = np.ascontiguousarray(v_packed, np.uint8)
+    k_norm = np.ascontiguousarray(k_norm, np.float32)
+    v_norm = np.ascontiguousarray(v_norm, np.float32)
+    out = np.empty((B, T, Hq, d), np.float64)
+    _lib().orc_attention_prefill(_p(s, _i8p), _s2p(s2), d, B, T, Hq, Hkv, cap,
+                                 qs.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), k_bits,
+                                 _p(kc, _f32p), _p(k_packed, _u8p), _p(k_norm, _f32p),
+                                 v_bits, _p(vc, _f32p), _p(v_packed, _u8p), _p(v_norm, _f32p),
+                                 _p(q, _f64p), float(scale), _p(out, _f64p))
+    return out

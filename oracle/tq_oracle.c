@@ -455,3 +455,52 @@ void orc_attention(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int 
     free(vh);
     free(sig);
 }
+
+/* Prefill (multi-query) attention over the packed cache, plain definition:
+ * token t of sequence b (absolute position q_start[b] + t) attends, for query
+ * head h, over positions [0, q_start[b] + t] of KV head h / (Hq/Hkv) -- the
+ * decode attention above with one query per token and a causal length.
+ *  q:   [B][T][Hq][d] double;  out: [B][T][Hq][d] double. */
+void orc_attention_prefill(const int8_t *s, const int8_t *s2, int d, int B, int T, int Hq, int Hkv,
+                           int64_t cap, const int32_t *q_start, int k_bits,
+                           const float *k_centroids, const uint8_t *k_packed, const float *k_norm,
+                           int v_bits, const float *v_centroids, const uint8_t *v_packed,
+                           const float *v_norm, const double *q, double scale, double *out) {
+    int G = Hq / Hkv;
+    int rbk = d * k_bits / 8, rbv = d * v_bits / 8;
+    for (int b = 0; b < B; ++b) {
+        int64_t n = (int64_t)q_start[b] + T; /* rows the chunk can reach */
+        double *kh = (double *)malloc(sizeof(double) * (size_t)(n * d + 1));
+        double *vh = (double *)malloc(sizeof(double) * (size_t)(n * d + 1));
+        double *sig = (double *)malloc(sizeof(double) * (size_t)(n + 1));
+        for (int g = 0; g < Hkv; ++g) {
+            int64_t row0 = ((int64_t)b * Hkv + g) * cap;
+            orc_decode(s, s2, d, k_bits, k_centroids, k_packed + row0 * rbk, k_norm + row0, n, kh);
+            orc_decode(s, s2, d, v_bits, v_centroids, v_packed + row0 * rbv, v_norm + row0, n, vh);
+            for (int t = 0; t < T; ++t) {
+                int64_t ctx = (int64_t)q_start[b] + t + 1;
+                for (int hh = 0; hh < G; ++hh) {
+                    int h = g * G + hh;
+                    const double *qh = q + (((int64_t)b * T + t) * Hq + h) * d;
+                    double *o = out + (((int64_t)b * T + t) * Hq + h) * d;
+                    double m = -INFINITY, l = 0.0;
+                    for (int64_t u = 0; u < ctx; ++u) {
+                        double dot = 0.0;
+                        for (int j = 0; j < d; ++j) dot += qh[j] * kh[u * d + j];
+                        sig[u] = scale * dot;
+                        if (sig[u] > m) m = sig[u];
+                    }
+                    for (int64_t u = 0; u < ctx; ++u) l += exp(sig[u] - m);
+                    for (int j = 0; j < d; ++j) o[j] = 0.0;
+                    for (int64_t u = 0; u < ctx; ++u) {
+                        double p = exp(sig[u] - m) / l;
+                        for (int j = 0; j < d; ++j) o[j] += p * vh[u * d + j];
+                    }
+                }
+            }
+        }
+        free(kh);
+        free(vh);
+        free(sig);
+    }
+}

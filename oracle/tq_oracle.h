@@ -126,6 +126,16 @@ void orc_attention(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int 
                    const float *v_norm, const double *q, double scale,
                    double sparse_thr, double *out, int64_t *kept);
 
+/* Prefill (multi-query) attention: token t of sequence b attends over
+ * positions [0, q_start[b] + t] (causal), otherwise as orc_attention.
+ *  q: [B][T][Hq][d] double; out: [B][T][Hq][d] double; the cache must hold
+ *  q_start[b] + T rows of every sequence. */
+void orc_attention_prefill(const int8_t *s, const int8_t *s2, int d, int B, int T, int Hq, int Hkv,
+                           int64_t cap, const int32_t *q_start, int k_bits,
+                           const float *k_centroids, const uint8_t *k_packed, const float *k_norm,
+                           int v_bits, const float *v_centroids, const uint8_t *v_packed,
+                           const float *v_norm, const double *q, double scale, double *out);
+
 #ifdef __cplusplus
 }
 #endif
