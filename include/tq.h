@@ -296,6 +296,31 @@ tq_status tq_attn_decode_append_paged(const tq_plan *plan, const void *q, const 
                                       float scale, float sparse_v_threshold, float *out, void *workspace,
                                       size_t workspace_bytes, tq_stream_t stream);
 
+/* Workspace bytes tq_attn_prefill needs (the rotated queries); 0 for invalid
+ * sizes or d != 128. */
+size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int d);
+
+/* Prefill (chunked, multi-query) attention over the packed cache: a chunk of
+ * T query tokens per sequence, token t of sequence b at absolute position
+ * q_start[b] + t, attending causally over positions [0, q_start[b] + t] of
+ * the contiguous cache (the chunk's own K/V rows already appended).  This is
+ * the decode attention ("TurboQuant KV Cache Compression -- Spec",
+ * fa_tq_attention_cached; Optimization: Fused dequant-dot -- scores against
+ * the centroids in the rotated domain, V accumulated rotated, one inverse
+ * rotation per output) with one query per token; both contractions run on
+ * the tensor cores.  d = 128, Hq / Hkv in {1, 2, 4, 8}; dense (no sparse-V).
+ *   q:   [B][T][Hq][d] bf16, device;  out: [B][T][Hq][d] fp32, device
+ *   q_start: [B] int32, device; every q_start[b] + T must be <= cache.cap
+ *     (checked on the device: a sequence that breaks it gets zero rows and
+ *     the device status word 52).
+ *   workspace: tq_attn_prefill_workspace_bytes(B, T, Hq, 128) bytes.
+ * Errors: TQ_ERR_UNSUPPORTED (d, group size, bits), TQ_ERR_RANGE (cap < T),
+ * TQ_ERR_INVALID_ARG, TQ_ERR_ALIGNMENT, TQ_ERR_WORKSPACE. */
+tq_status tq_attn_prefill(const tq_plan *plan, const void *q, int B, int T, int Hq, int Hkv,
+                          tq_cache_view cache, const int32_t *q_start, int k_bits, int v_bits,
+                          float scale, float *out, void *workspace, size_t workspace_bytes,
+                          tq_stream_t stream);
+
 /* Text for a status code (static storage). */
 const char *tq_status_string(tq_status status);
 

@@ -27,7 +27,8 @@ EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_sig
            "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes", "tq_attn_paged_workspace_bytes",
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
            "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged",
-           "tq_attn_decode_append_paged", "tq_plan_create_ex", "tq_plan_signs2", "tq_codebook_init_gaussian")
+           "tq_attn_decode_append_paged", "tq_plan_create_ex", "tq_plan_signs2", "tq_codebook_init_gaussian",
+           "tq_attn_prefill_workspace_bytes", "tq_attn_prefill")
 
 
 class TQError(RuntimeError):
@@ -83,6 +84,9 @@ def lib() -> ctypes.CDLL:
                                        f32, f32, vp, vp, ctypes.c_size_t, vp]),
         ("tq_attn_decode_append_paged", i32, [vp, vp, vp, vp, i32, i32, i32, i32, PagedCacheView, vp, i32, vp,
                                               i64, i32, i32, f32, f32, vp, vp, ctypes.c_size_t, vp]),
+        ("tq_attn_prefill_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32]),
+        ("tq_attn_prefill", i32, [vp, vp, i32, i32, i32, i32, CacheView, vp, i32, i32, f32, vp, vp,
+                                  ctypes.c_size_t, vp]),
         ("tq_status_string", ctypes.c_char_p, [i32]),
         ("tq_last_cuda_error", i32, []),
         ("tq_device_status", i32, [i32, ctypes.POINTER(i32)]),
@@ -404,6 +408,28 @@ def tq_attn_decode_append_paged(plan: Plan, q: torch.Tensor, k_new: torch.Tensor
         block_table.data_ptr(), block_table.shape[1], positions.data_ptr(), max_ctx, cache.k_bits,
         cache.v_bits, ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(),
         workspace.data_ptr(), workspace.numel(), _stream(q)))
+    return out
+
+
+def tq_attn_prefill(plan: Plan, q: torch.Tensor, cache: Cache, q_start: torch.Tensor, scale: float,
+                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """q: [B, T, Hq, d] bf16; q_start [B] int32 (token t of sequence b sits at
+    q_start[b] + t and attends causally) -> out [B, T, Hq, d] fp32."""
+    B, T, Hq, d = q.shape
+    Hkv = cache.k_norm.shape[1]
+    if out is None:
+        out = torch.empty(B, T, Hq, d, dtype=torch.float32, device=q.device)
+    need = int(lib().tq_attn_prefill_workspace_bytes(B, T, Hq, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(q, out, workspace)
+    _i32(q_start, "q_start")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    _check("tq_attn_prefill", lib().tq_attn_prefill(
+        plan.handle, q.contiguous().data_ptr(), B, T, Hq, Hkv, cache.view(), q_start.data_ptr(), cache.k_bits,
+        cache.v_bits, ctypes.c_float(scale), out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+        _stream(q)))
     return out
 
 

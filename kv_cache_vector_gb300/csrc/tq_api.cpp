@@ -645,6 +645,46 @@ tq_status tq_attn_decode_append_paged(const tq_plan* plan, const void* q, const 
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
+size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int d) {
+    if (B < 0 || T < 1 || Hq <= 0 || d != 128) return 0;
+    return tq::attn_prefill_ws_bytes(B, T, Hq);
+}
+
+tq_status tq_attn_prefill(const tq_plan* plan, const void* q, int B, int T, int Hq, int Hkv, tq_cache_view cache,
+                          const int32_t* q_start, int k_bits, int v_bits, float scale, float* out,
+                          void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    if (!plan || B < 0 || T < 1 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits)) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    const int G = Hq / Hkv;
+    if (P->d != 128 || (G != 1 && G != 2 && G != 4 && G != 8)) return TQ_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+    if (cache.cap < T) return TQ_ERR_RANGE;
+    if (B == 0) return TQ_OK;
+    if ((int64_t)B * Hkv > 65535 || (int64_t)B * T * Hq > INT32_MAX) return TQ_ERR_UNSUPPORTED;
+    if (!q || !out || !q_start || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned16(cache.k_packed) ||
+        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
+        return TQ_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < tq::attn_prefill_ws_bytes(B, T, Hq)) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(q_start) ||
+        !device_accessible(workspace) || !device_accessible(cache.k_packed) || !device_accessible(cache.v_packed) ||
+        !device_accessible(cache.k_norm) || !device_accessible(cache.v_norm))
+        return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    tq::fill_attn_params(*P, k_bits, v_bits, scale, 0.0f, A);
+    auto st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (k_bits) {
+        case 2: e = tq::launch_attn_prefill<2>(v_bits, q, B, T, Hq, Hkv, q_start, cache, out, workspace, A, st); break;
+        case 3: e = tq::launch_attn_prefill<3>(v_bits, q, B, T, Hq, Hkv, q_start, cache, out, workspace, A, st); break;
+        default: e = tq::launch_attn_prefill<4>(v_bits, q, B, T, Hq, Hkv, q_start, cache, out, workspace, A, st); break;
+    }
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
 const char* tq_status_string(tq_status s) {
     switch (s) {
         case TQ_OK: return "ok";

@@ -24,24 +24,6 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxGroup = 8;
 
-// Unnormalised Walsh-Hadamard transform of `nvec` vectors of length D held in
-// shared memory (every thread of the block takes part).
-template <int D>
-__device__ void fwht_smem(float* v, int nvec) {
-    for (int len = 1; len < D; len <<= 1) {
-        __syncthreads();
-        for (int t = threadIdx.x; t < nvec * D / 2; t += blockDim.x) {
-            const int vec = t / (D / 2), k = t % (D / 2);
-            const int i = (k / len) * 2 * len + (k % len);
-            float* x = v + vec * D;
-            const float a = x[i], b = x[i + len];
-            x[i] = a + b;
-            x[i + len] = a - b;
-        }
-    }
-    __syncthreads();
-}
-
 template <int BITS, int D>
 __device__ __forceinline__ void load_packed_row(const uint8_t* p, uint32_t (&w)[(D * BITS + 31) / 32]) {
     load_bytes<D * BITS / 8>(p, w);
@@ -427,30 +409,8 @@ __device__ __forceinline__ void load_vfield(uint32_t row, int g, uint32_t (&f)[2
 // [2^13, 2^14).  q16 layout: [B * Hq][2 (high, low)][128].
 __device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__ q, __half* __restrict__ q16,
                                                float* __restrict__ qexp, const AttnParams& P) {
-    __shared__ float v[128];
-    __shared__ float wmax[4];
-    const int bh = blockIdx.x, j = threadIdx.x;
-    const float x = __bfloat162float(q[(int64_t)bh * 128 + j]);
-    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
-    fwht_smem<128>(v, 1);
-    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u)) * P.q_mul;
-    float a = fabsf(y);
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-    if ((j & 31) == 0) wmax[j >> 5] = a;
-    __syncthreads();
-    const float M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-    int e = 0;
-    if (M > 0.f && M <= FLT_MAX) {
-        int ex = 0;
-        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
-        e = min(100, max(-100, ex - 14));
-    }
-    const float ys = ldexpf(y, -e);
-    const __half hi = __float2half_rn(ys);
-    const __half lo = __float2half_rn(ys - __half2float(hi));
-    q16[(int64_t)bh * 256 + j] = hi;
-    q16[(int64_t)bh * 256 + 128 + j] = lo;
-    if (j == 0) qexp[bh] = ldexpf(1.f, e);
+    const int64_t bh = blockIdx.x;
+    rotate_q_row(q + bh * 128, q16 + bh * 256, qexp + bh, P);
 }
 
 static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __restrict__ q,

@@ -18,7 +18,10 @@
 
 #include <cstdint>
 
+#include <cfloat>
+
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "tq_internal.h"
 
@@ -440,6 +443,58 @@ __device__ __forceinline__ void warp_pack_row(const uint8_t* ib, int lane, int b
         }
         reinterpret_cast<uint32_t*>(dst)[lane] = word;
     }
+}
+
+// Unnormalised Walsh-Hadamard transform of `nvec` vectors of length D held in
+// shared memory (every thread of the block takes part).
+template <int D>
+__device__ void fwht_smem(float* v, int nvec) {
+    for (int len = 1; len < D; len <<= 1) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < nvec * D / 2; t += blockDim.x) {
+            const int vec = t / (D / 2), k = t % (D / 2);
+            const int i = (k / len) * 2 * len + (k % len);
+            float* x = v + vec * D;
+            const float a = x[i], b = x[i + len];
+            x[i] = a + b;
+            x[i + len] = a - b;
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------- query rotation (d = 128)
+// One block of 128 threads rotates one query row for the tensor-core
+// attention: q~ = s2 . H (s . q) / sqrt(d) (s2 only with two-sided signs),
+// times the plan's query multiplier scale * log2(e) / (sqrt(d) * s_k),
+// written as fp16 high and low parts (q16_row[0, 128) and [128, 256)) of the
+// row divided by a power of two (*qexp_out) that keeps them below 2^14.
+__device__ __forceinline__ void rotate_q_row(const __nv_bfloat16* __restrict__ q_row, __half* __restrict__ q16_row,
+                                             float* __restrict__ qexp_out, const AttnParams& P) {
+    __shared__ float v[128];
+    __shared__ float wmax[4];
+    const int j = threadIdx.x;
+    const float x = __bfloat162float(q_row[j]);
+    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
+    fwht_smem<128>(v, 1);
+    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u)) * P.q_mul;
+    float a = fabsf(y);
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    if ((j & 31) == 0) wmax[j >> 5] = a;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    int e = 0;
+    if (M > 0.f && M <= FLT_MAX) {
+        int ex = 0;
+        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
+        e = min(100, max(-100, ex - 14));
+    }
+    const float ys = ldexpf(y, -e);
+    const __half hi = __float2half_rn(ys);
+    const __half lo = __float2half_rn(ys - __half2float(hi));
+    q16_row[j] = hi;
+    q16_row[128 + j] = lo;
+    if (j == 0) *qexp_out = ldexpf(1.f, e);
 }
 
 }  // namespace dev

@@ -168,6 +168,15 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
                                  const tq_cache_view& pages, int64_t max_ctx, float* out,
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
                                  const PagedArgs& pa, cudaStream_t s, const AttnAppend* app = nullptr);
+// Prefill (multi-query, causal) attention, d = 128 (tq_prefill.cu, one unit
+// per K width).  workspace: the rotated queries, attn_prefill_ws_bytes.
+inline size_t attn_prefill_ws_bytes(int B, int T, int Hq) {
+    return ((size_t)B * T * Hq * (512 + 4) + 255) / 256 * 256;
+}
+template <int KB>
+cudaError_t launch_attn_prefill(int v_bits, const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
+                                const tq_cache_view& cache, float* out, void* workspace, const AttnParams& P,
+                                cudaStream_t s);
 // Paged append of one token per sequence, d >= 32 (tq_codec.cu).
 template <int D>
 cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,

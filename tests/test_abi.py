@@ -233,3 +233,26 @@ def test_paged_call_validation_before_launch(L):
     assert fa(h, A, A, None, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
     assert fa(h, A, None, None, 1, 0, 8, 2, pc(), None, 4, None, 256, 4, 3, f(1.0), f(0.0), None, None, 0,
               s) == 0  # B = 0: no-op
+
+
+def test_prefill_call_validation_before_launch(L):
+    """tq_attn_prefill checks its arguments on the host before any launch."""
+    p128, p64 = abi.Plan(128, 42), abi.Plan(64, 42)
+    h = p128.handle
+    A = 1 << 20
+    f = ctypes.c_float
+    cv = abi.CacheView(A, A, A, A, 256)
+    W = 1 << 24
+    # tq_attn_prefill(plan, q, B, T, Hq, Hkv, cache, q_start, kb, vb, scale, out, ws, ws_bytes, s)
+    assert L.tq_attn_prefill(None, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 1
+    assert L.tq_attn_prefill(h, A, 1, 0, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 1      # T = 0
+    assert L.tq_attn_prefill(h, A, 1, 8, 12, 4, cv, A, 4, 3, f(1.0), A, A, W, None) == 2     # group of 3
+    assert L.tq_attn_prefill(p64.handle, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 2
+    assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 5, 3, f(1.0), A, A, W, None) == 2
+    assert L.tq_attn_prefill(h, A, 1, 300, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 4    # cap < T
+    assert L.tq_attn_prefill(h, A + 8, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 3
+    assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, 16, None) == 5
+    assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(float("nan")), A, A, W, None) == 1
+    assert L.tq_attn_prefill(h, None, 0, 8, 8, 2, cv, None, 4, 3, f(1.0), None, None, 0, None) == 0
+    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 128) == (2 * 10 * 8 * 516 + 255) // 256 * 256
+    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 64) == 0
