@@ -47,7 +47,7 @@ def args_():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["encode", "decode", "attn", "append"], default=None,
                     help="run just one kernel per step (profiling of one kernel)")
-    ap.add_argument("--extra", choices=["long_context", "gemma_cache", "paged_varlen"], default=None,
+    ap.add_argument("--extra", choices=["long_context", "gemma_cache", "paged_varlen", "prefill"], default=None,
                     help="run just one of the extra measurements and print its result (profiling)")
     return ap.parse_args()
 
@@ -533,6 +533,57 @@ def extra_paged(peak):
                       f"(seeded; mean {float(lens.float().mean()):.0f}), low-rank+diag rows"}
 
 
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            v = json.load(f).get("bf16_tflops")
+        if v:
+            return float(v), "measured"
+    return 1900.0, "fallback"
+
+
+def extra_prefill(peak_hbm):
+    """Prefill (multi-query, causal) attention over a packed K4/V3 cache,
+    Llama-8B-shaped heads (32 query / 8 KV, d 128): a fresh 2048-token
+    prompt (batch 1, q_start 0) and a chunk of 512 tokens after 4096 cached
+    ones (batch 4).  FLOPs counted are the useful ones, 4 d Hq sum_t ctx_t (QK
+    and PV, causal); the kernel runs the fp16 high and low parts of Q and P,
+    twice that on the tensor cores.  Against the measured bf16 tensor peak
+    (fp16 has the same rate)."""
+    import torch
+    from kv_cache_vector_gb300 import abi, synth
+    peak, kind = measured_tensor_peak()
+    Hq, Hkv, kb, vb = 32, 8, 4, 3
+    plan = abi.Plan(D, 42)
+    res = {}
+    for name, B, T, start in (("fresh_2048", 1, 2048, 0), ("chunk_512_after_4096", 4, 512, 4096)):
+        cap = start + T
+        cache = abi.Cache.empty(B, Hkv, cap, D, kb, vb)
+        rows = B * Hkv * cap
+        for bits, pk, nm, stream in ((kb, cache.k_packed, cache.k_norm, 40000), (vb, cache.v_packed, cache.v_norm, 41000)):
+            x = synth.lowrank_rows(95, rows, D, stream=stream, device="cuda")
+            abi.tq_encode(plan, bits, x, pk.view(-1, D * bits // 8), nm.view(-1))
+        q = synth.device_normal(96, (B, T, Hq, D))
+        qs = torch.full((B,), start, dtype=torch.int32, device="cuda")
+        out = torch.empty(B, T, Hq, D, dtype=torch.float32, device="cuda")
+        ws = torch.empty(abi.lib().tq_attn_prefill_workspace_bytes(B, T, Hq, D), dtype=torch.uint8, device="cuda")
+        f = lambda: abi.tq_attn_prefill(plan, q, cache, qs, 1.0 / math.sqrt(D), out=out, workspace=ws)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        us = time_events(f, 10) * 1e3
+        ctx_sum = B * (T * start + T * (T + 1) // 2)
+        flops = 4.0 * D * Hq * ctx_sum
+        tf = flops / (us * 1e-6) / 1e12
+        res[name] = {"us": round(us, 2), "TFLOPs": round(tf, 1), "frac": round(tf / peak, 4),
+                     "config": f"B{B} T{T} q_start {start}, Hq{Hq}/Hkv{Hkv} d128 K{kb}/V{vb}"}
+        del cache, q, out, ws
+        torch.cuda.empty_cache()
+    res["peak"] = {"TFLOPs": peak, "source": kind, "bound": "tensor"}
+    return res
+
+
 def extra_gemma(peak):
     """34 layers x 4 KV heads x d 256 x 512 tokens bf16 N(0,1), K4/V4: window
     encode GB/s (L2 flushed), then the append-only decode step: one tq_append
@@ -654,7 +705,8 @@ def main():
     barrier(world)
     if a.extra:
         if rank == 0:
-            fn = {"long_context": extra_long_context, "gemma_cache": extra_gemma, "paged_varlen": extra_paged}
+            fn = {"long_context": extra_long_context, "gemma_cache": extra_gemma, "paged_varlen": extra_paged,
+                  "prefill": extra_prefill}
             print(json.dumps({"extra": a.extra, **fn[a.extra](measured_peak()[0])}))
         barrier(world)
         return
@@ -735,6 +787,7 @@ def main():
         out["long_context"] = extra_long_context(peak)
         out["gemma_cache"] = extra_gemma(peak)
         out["paged_varlen"] = extra_paged(peak)
+        out["prefill"] = extra_prefill(peak)
     print(json.dumps(out))
     barrier(world)
 

@@ -90,6 +90,16 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), zero-filled past
+// src_bytes (0 or 16); group it with cp_async_commit, wait with
+// cp_async_wait_all (this thread's own copies).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Arrive on `bar` once this thread's earlier cp.async copies have landed;
 // the arrival is one of the phase's expected arrivals.
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {

@@ -9,7 +9,7 @@
 // output) with many queries per KV head, which turns both contractions into
 // dense matrix products.
 //
-// One CTA of four warps takes 128 query rows of one (sequence, KV head):
+// One CTA of sixteen warps takes 128 query rows of one (sequence, KV head):
 // 128 / G consecutive tokens times the G query heads of the group (row r =
 // token (r / G), head (r % G)).  Per block of 128 KV positions:
 //   1. the packed K and V rows and their norms are staged in shared memory;
@@ -22,16 +22,17 @@
 //   4. meanwhile the threads turn V into fp16 centroids c * s_v, transposed
 //      (positions contiguous per dim; lookups in a table of centroid pairs of
 //      two consecutive positions);
-//   5. each thread reads its row of S from tensor memory, applies the query's
-//      power-of-two scale, the K norms and the causal mask, and updates its
-//      running max and denominator (log2 units); P = exp2(s - m) times the V
-//      norm over 2^E (E fixed per CTA from the largest V norm it reads, so P
-//      <= 1) goes to shared memory as fp16 high and low parts;
+//   5. four threads share a row of S (a quarter of the columns each): they
+//      read it from tensor memory, apply the query's power-of-two scale, the
+//      K norms and the causal mask, merge their maxima through shared memory
+//      and update the running max and denominator (log2 units); P = exp2(s -
+//      m) times the V norm over 2^E (E fixed per CTA from the largest V norm
+//      it reads, so P <= 1) goes to shared memory as fp16 high and low parts;
 //   6. one thread issues O_blk = P_hi V + P_lo V into tensor memory; each
-//      thread folds its row into the running output held in registers,
-//      O = O * exp2(m_old - m_new) + O_blk.
-// At the end the row is divided by the denominator, scaled by 2^E / s_v and
-// rotated back (s . H (s2 . o) / sqrt(d)) in registers.
+//      thread folds its quarter of the row into the running output held in
+//      registers, O = O * exp2(m_old - m_new) + O_blk.
+// At the end the rows are divided by the denominator, scaled by 2^E / s_v,
+// staged in shared memory and rotated back (s . H (s2 . o) / sqrt(d)).
 //
 // Every wait on an mbarrier is bounded (2 s); a wait that gives up sets the
 // device status word, the CTA stops, waits (bounded) for its MMAs in flight,
@@ -48,24 +49,30 @@
 namespace tq {
 namespace dev {
 
-constexpr int kPfRows = 128;   // query rows per CTA
-constexpr int kPfBlock = 128;  // KV positions per block
+constexpr int kPfRows = 128;     // query rows per CTA
+constexpr int kPfBlock = 128;    // KV positions per block
+constexpr int kPfThreads = 512;  // 16 warps; warp w reads tensor-memory lanes 32 (w % 4) .. + 31,
+                                 // columns 32 (w / 4) .. + 31 of its rows
 // shared memory, offsets from a 1024-aligned base
-constexpr uint32_t kPfQH = 0;          // Q high parts, 128 x 128 fp16
+constexpr uint32_t kPfQH = 0;          // Q high parts, 128 x 128 fp16 (the output rows at the end)
 constexpr uint32_t kPfQL = 32768;      // Q low parts
 constexpr uint32_t kPfKT = 65536;      // K centroids of the block, [position][dim]
 constexpr uint32_t kPfVT = 98304;      // V centroids of the block, [dim][position]
 constexpr uint32_t kPfPH = 131072;     // P high parts, [row][position]
 constexpr uint32_t kPfPL = 163840;     // P low parts
-constexpr uint32_t kPfKS = 196608;     // packed K rows of the block, 64-byte stride
-constexpr uint32_t kPfVS = 204800;     // packed V rows
-constexpr uint32_t kPfKN = 212992;     // K norms of the block (128 floats)
-constexpr uint32_t kPfVN = 213504;     // V norms
-constexpr uint32_t kPfTK = 214016;     // K pair table (up to 256 words)
-constexpr uint32_t kPfTV = 215040;     // V pair table
-constexpr uint32_t kPfBar = 216064;    // two mbarriers
-constexpr uint32_t kPfMisc = 216080;   // tensor-memory base, reduction scratch
-constexpr uint32_t kPfEnd = 216128;
+constexpr uint32_t kPfTK = 196608;     // K pair table, 4 copies (up to 256 x 4 words)
+constexpr uint32_t kPfTV = 200704;     // V pair table, 4 copies
+constexpr uint32_t kPfSK = 204800;     // staged packed K rows of the next block, 64-byte stride
+constexpr uint32_t kPfSV = 212992;     // staged packed V rows
+constexpr uint32_t kPfSKN = 221184;    // staged K norms (128 floats)
+constexpr uint32_t kPfSVN = 221696;    // staged V norms
+constexpr uint32_t kPfKN = 222208;     // K norms of the block (128 floats)
+constexpr uint32_t kPfVN = 222720;     // V norms of the block over 2^E
+constexpr uint32_t kPfRed = 223232;    // [4][128] floats: per-quarter row maxima / sums
+constexpr uint32_t kPfBar = 225280;    // two mbarriers
+constexpr uint32_t kPfMisc = 225296;   // tensor-memory base, reduction scratch (16 floats)
+constexpr uint32_t kPfEnd = 225424;
+constexpr int kPfCopies = 4;           // table copies: lane l reads copy l % 4 (fewer bank conflicts)
 constexpr uint32_t kPfSmem = kPfEnd + 1024;  // plus alignment slack
 constexpr int kPfStatusWait = 51;      // an MMA completion wait gave up
 constexpr int kPfStatusRange = 52;     // q_start[b] + T exceeds the cache capacity, or q_start < 0
@@ -77,13 +84,42 @@ __device__ __forceinline__ uint32_t pf_chunk(int row, int k8) {
     return (uint32_t)((k8 >> 3) * 16384 + row * 128 + (((k8 & 7) ^ (row & 7)) << 4));
 }
 
-// The 32 bits of a packed row from bit `pos` on (the row is read as 32-bit
-// words; when `pos` is not word aligned the next word is read too, which for
-// the last fields of a row lies in the row's 64-byte staging slot and only
-// feeds bits above the ones used).
+// N bits (N <= 32) of a staged packed row from bit `pos` on, in the low
+// bits; the row is read as 32-bit words, the next word only when the field
+// crosses into it.
+template <int N>
 __device__ __forceinline__ uint32_t pf_bits(const uint32_t* w, int pos) {
     const int i = pos >> 5, sh = pos & 31;
-    return sh == 0 ? w[i] : __funnelshift_r(w[i], w[i + 1], sh);
+    const uint32_t lo = w[i];
+    if (sh == 0) return lo;
+    return sh + N > 32 ? __funnelshift_r(lo, w[i + 1], sh) : lo >> sh;
+}
+
+// Stage the packed K and V rows and the norms of positions t0 .. t0 + 127 of
+// cache rows crow0 + .. with cp.async (zero fill past n valid rows; the
+// source of a zero-filled copy is row crow0, which exists).
+template <int KB, int VB>
+__device__ __forceinline__ void pf_stage(uint32_t sa, const tq_cache_view& cache, int64_t crow0, int64_t t0,
+                                         int n, int tid) {
+    constexpr int KP = KB, VP = VB;  // 16-byte parts per packed row (16 * bits bytes)
+    if (tid < 128 * KP) {
+        const int row = tid / KP, part = tid - row * KP;
+        const bool in = row < n;
+        const uint8_t* src = cache.k_packed + (crow0 + (in ? t0 + row : 0)) * (16 * KB) + part * 16;
+        cp_async16(sa + kPfSK + row * 64 + part * 16, src, in ? 16u : 0u);
+    }
+    if (tid < 128 * VP) {
+        const int row = tid / VP, part = tid - row * VP;
+        const bool in = row < n;
+        const uint8_t* src = cache.v_packed + (crow0 + (in ? t0 + row : 0)) * (16 * VB) + part * 16;
+        cp_async16(sa + kPfSV + row * 64 + part * 16, src, in ? 16u : 0u);
+    }
+    if (tid < 256) {  // norms, one per copy (a norm row is only 4-byte aligned); zeros past n
+        const int k = tid & 127, side = tid >> 7;
+        const float* nrm = side ? cache.v_norm : cache.k_norm;
+        cp_async4(sa + (side ? kPfSVN : kPfSKN) + 4 * k, nrm + crow0 + (k < n ? t0 + k : 0), k < n ? 4u : 0u);
+    }
+    cp_async_commit();
 }
 
 __device__ __forceinline__ uint32_t pf_pack_half2(float a, float b) {
@@ -96,10 +132,10 @@ __device__ __forceinline__ float pf_exp2(float x) {
     return y;
 }
 
-// A row of the prefill output attends over [0, pos]; rows past the chunk
-// (the last tile of a (sequence, KV head)) attend nowhere and write nothing.
+// Tiles of a (sequence, KV head) are taken last first: with a causal mask the
+// last tiles read the most KV blocks, so the longest CTAs start first.
 template <int KB, int VB>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kPfThreads, 1)
 k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv, int T,
                const int32_t* __restrict__ q_start, tq_cache_view cache, float* __restrict__ out,
                int* status, const __grid_constant__ AttnParams P) {
@@ -107,14 +143,17 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     unsigned char* sm = pf_raw + ((1024u - (smem_addr(pf_raw) & 1023u)) & 1023u);
     const uint32_t sa = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane;  // this thread's query row in the tile
+    const int cq = warp >> 2;              // and its quarter of the columns
     const int G = Hq / Hkv, tpr = kPfRows / G;
     const int bg = blockIdx.y, b = bg / Hkv, g = bg - b * Hkv;
+    const int mt = (int)(gridDim.x - 1 - blockIdx.x);
     const int rows_total = T * G;
-    const int grow = blockIdx.x * kPfRows + tid;  // this thread's row within (b, g)
+    const int grow = mt * kPfRows + r;  // this thread's row within (b, g)
     const bool rvalid = grow < rows_total;
     const int tok = rvalid ? grow / G : 0, hh = grow - (grow / G) * G;
     int64_t qs = __ldg(q_start + b);
-    const int last_tok = min(T, (int)(blockIdx.x + 1) * tpr) - 1;
+    const int last_tok = min(T, (mt + 1) * tpr) - 1;
     if (qs < 0 || qs + T > cache.cap) {  // nothing sensible to read: report and write zeros
         if (tid == 0) report_timeout(status, kPfStatusRange);
         qs = -1;
@@ -124,17 +163,25 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kPfBar);
     uint64_t* bar_pv = bar_s + 1;
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
-    float* red = reinterpret_cast<float*>(sm + kPfMisc + 16);
+    float* wred = reinterpret_cast<float*>(sm + kPfMisc + 16);
     uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPfTK);
     uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPfTV);
     float* kn_s = reinterpret_cast<float*>(sm + kPfKN);
     float* vn_s = reinterpret_cast<float*>(sm + kPfVN);
+    float* red = reinterpret_cast<float*>(sm + kPfRed);
 
-    // pair tables: entry e = (c[e % 2^b], c[e / 2^b]) as two fp16 halves
-    for (int e = tid; e < (1 << (2 * KB)); e += 128)
-        tk[e] = pf_pack_half2(P.kcen_h[e & ((1 << KB) - 1)], P.kcen_h[e >> KB]);
-    for (int e = tid; e < (1 << (2 * VB)); e += 128)
-        tv[e] = pf_pack_half2(P.vcen_h[e & ((1 << VB) - 1)], P.vcen_h[e >> VB]);
+    // pair tables: entry e = (c[e % 2^b], c[e / 2^b]) as two fp16 halves, copy
+    // c of entry e at word 8 e + c
+    for (int i = tid; i < (kPfCopies << (2 * KB)); i += kPfThreads) {
+        const int e = i / kPfCopies;
+        tk[i] = pf_pack_half2(P.kcen_h[e & ((1 << KB) - 1)], P.kcen_h[e >> KB]);
+    }
+    for (int i = tid; i < (kPfCopies << (2 * VB)); i += kPfThreads) {
+        const int e = i / kPfCopies;
+        tv[i] = pf_pack_half2(P.vcen_h[e & ((1 << VB) - 1)], P.vcen_h[e >> VB]);
+    }
+    const uint32_t* tkl = tk + (lane & (kPfCopies - 1));  // this lane's copy
+    const uint32_t* tvl = tv + (lane & (kPfCopies - 1));
     if (tid == 0) {
         mbar_init(bar_s, 1);
         mbar_init(bar_pv, 1);
@@ -145,19 +192,20 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     // E: the largest V norm this CTA reads is below 2^E
     const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
     float vmax = 0.f;
-    for (int64_t t = tid; t < kv_end; t += 128) vmax = fmaxf(vmax, fabsf(__ldg(cache.v_norm + crow0 + t)));
+    for (int64_t t = tid; t < kv_end; t += kPfThreads) vmax = fmaxf(vmax, fabsf(__ldg(cache.v_norm + crow0 + t)));
     for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
-    if (lane == 0) red[warp] = vmax;
+    if (lane == 0) wred[warp] = vmax;
 
-    // Q tile: row tid, high and low parts
+    // Q tile: row r, chunks 4 cq .. 4 cq + 3 of the high and low parts
     {
         const uint4* src = reinterpret_cast<const uint4*>(q16 + ((int64_t)bg * rows_total + grow) * 256);
-#pragma unroll 4
-        for (int k8 = 0; k8 < 16; ++k8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k8 = 4 * cq + i;
             const uint4 h = rvalid ? __ldg(src + k8) : make_uint4(0, 0, 0, 0);
             const uint4 l = rvalid ? __ldg(src + 16 + k8) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kPfQH + pf_chunk(tid, k8)) = h;
-            *reinterpret_cast<uint4*>(sm + kPfQL + pf_chunk(tid, k8)) = l;
+            *reinterpret_cast<uint4*>(sm + kPfQH + pf_chunk(r, k8)) = h;
+            *reinterpret_cast<uint4*>(sm + kPfQL + pf_chunk(r, k8)) = l;
         }
     }
     const float qx = rvalid ? __ldg(qexp + (int64_t)bg * rows_total + grow) : 0.f;
@@ -168,54 +216,51 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     const uint32_t tmem = *slot;
     int E = 0;
     {
-        const float vm = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        float vm = 0.f;
+#pragma unroll
+        for (int w = 0; w < kPfThreads / 32; ++w) vm = fmaxf(vm, wred[w]);
         if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
     }
     const float inv2E = ldexpf(1.f, -E);
-    const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's lanes
+    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cq;  // this thread's S columns
     constexpr uint32_t idesc = umma_idesc_f16(128, 128, false);
 
-    float O[128];
+    float O[32];  // columns 32 cq .. 32 cq + 31 of the output row (rotated, units of 2^E s_v)
 #pragma unroll
-    for (int j = 0; j < 128; ++j) O[j] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < 32; ++j) O[j] = 0.f;
+    float m = -INFINITY, lp = 0.f;  // running max of the row (s' units) and this quarter's sum
     bool bad = false;
-    int pend = 0;  // 1: the S MMAs of block `blk` may be in flight; 2: the PV MMAs
+    int pend = 0;  // 1: the S MMAs of the current block may be in flight; 2: the PV MMAs
     int pend_par = 0;
     const int nblk = (int)((kv_end + kPfBlock - 1) / kPfBlock);
-    constexpr int RBK = 16 * KB, RBV = 16 * VB;  // packed bytes per row
+    if (nblk > 0) pf_stage<KB, VB>(sa, cache, crow0, 0, kv_end < kPfBlock ? (int)kv_end : kPfBlock, tid);
 
     for (int blk = 0; blk < nblk; ++blk) {
         const int64_t t0 = (int64_t)blk * kPfBlock;
         const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
-        // 1. stage the packed rows and norms of positions t0 .. t0 + 127 (zeros past kv_end)
-        {
-            const int64_t crow = crow0 + t0 + tid;
-            uint4* ks = reinterpret_cast<uint4*>(sm + kPfKS + tid * 64);
-            uint4* vs = reinterpret_cast<uint4*>(sm + kPfVS + tid * 64);
-            const bool in = tid < nv;
-#pragma unroll
-            for (int i = 0; i < RBK / 16; ++i)
-                ks[i] = in ? __ldg(reinterpret_cast<const uint4*>(cache.k_packed + crow * RBK) + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < RBV / 16; ++i)
-                vs[i] = in ? __ldg(reinterpret_cast<const uint4*>(cache.v_packed + crow * RBV) + i) : make_uint4(0, 0, 0, 0);
-            kn_s[tid] = in ? __ldg(cache.k_norm + crow) : 0.f;
-            vn_s[tid] = in ? __ldg(cache.v_norm + crow) : 0.f;
-        }
+        // 1. the staged rows of this block have landed; the norms move to their
+        //    own arrays (the staging area takes the next block during this one)
+        cp_async_wait_all();
         __syncthreads();
-        // 2. K tile: thread tid = position tid, 16 chunks of 8 dims (4 pair lookups each)
+        if (tid < 128) kn_s[tid] = reinterpret_cast<const float*>(sm + kPfSKN)[tid];
+        else if (tid < 256) vn_s[tid - 128] = reinterpret_cast<const float*>(sm + kPfSVN)[tid - 128] * inv2E;
+        // 2. K tile: lanes take the 16 chunks of 8 dims of a row (consecutive
+        //    words of the staged row, conflict-free tile stores); row
+        //    (tid / 16) + 32 i; 4 pair lookups per chunk
         {
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(sm + kPfKS + tid * 64);
-#pragma unroll 4
-            for (int k8 = 0; k8 < 16; ++k8) {
-                const uint32_t f = pf_bits(w, k8 * 8 * KB);
+            const int k8 = tid & 15;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = (tid >> 4) + 32 * i;
+                const uint32_t f =
+                    pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sm + kPfSK + t * 64), k8 * 8 * KB);
+                constexpr uint32_t M = (1u << (2 * KB)) - 1;
                 uint4 c;
-                c.x = tk[f & ((1u << (2 * KB)) - 1)];
-                c.y = tk[(f >> (2 * KB)) & ((1u << (2 * KB)) - 1)];
-                c.z = tk[(f >> (4 * KB)) & ((1u << (2 * KB)) - 1)];
-                c.w = tk[(f >> (6 * KB)) & ((1u << (2 * KB)) - 1)];
-                *reinterpret_cast<uint4*>(sm + kPfKT + pf_chunk(tid, k8)) = c;
+                c.x = tkl[kPfCopies * (f & M)];
+                c.y = tkl[kPfCopies * ((f >> (2 * KB)) & M)];
+                c.z = tkl[kPfCopies * ((f >> (4 * KB)) & M)];
+                c.w = tkl[kPfCopies * ((f >> (6 * KB)) & M)];
+                *reinterpret_cast<uint4*>(sm + kPfKT + pf_chunk(t, k8)) = c;
             }
         }
         fence_proxy_async_smem();
@@ -239,32 +284,36 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         }
         pend = 1;
         pend_par = blk & 1;
-        // 4. V tile: thread = (8 positions, 16 dims); entry (c[idx(t, j)], c[idx(t + 1, j)])
+        // 4. V tile: lanes take consecutive dim pairs (2 jp, 2 jp + 1) of the
+        //    same rows; thread = (dim pair tid % 64, position groups (tid / 64)
+        //    + 8 i of 8 positions); entry (c[idx(t, j)], c[idx(t + 1, j)])
         {
-            const int t8 = tid & 15, dg = tid >> 4;
-            uint64_t f[8];
+            const int jp = tid & 63;
+            constexpr uint32_t M = (1u << VB) - 1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(sm + kPfVS + (8 * t8 + i) * 64);
-                const int bp = dg * 16 * VB;  // bit offset of dim 16 dg
-                const int wi = bp >> 5, sh = bp & 31;
-                const uint64_t x = (uint64_t)w[wi] | ((uint64_t)w[wi + 1] << 32);
-                f[i] = x >> sh;  // 16 fields of VB bits in the low 16 VB bits
-            }
+            for (int i = 0; i < 2; ++i) {
+                const int t8 = (tid >> 6) + 8 * i;
+                uint32_t f[8];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                uint32_t c[4];
+                for (int u = 0; u < 8; ++u)
+                    f[u] = pf_bits<2 * VB>(reinterpret_cast<const uint32_t*>(sm + kPfSV + (8 * t8 + u) * 64),
+                                           2 * jp * VB);
 #pragma unroll
-                for (int pp = 0; pp < 4; ++pp) {
-                    const uint32_t a = (uint32_t)(f[2 * pp] >> (jj * VB)) & ((1u << VB) - 1);
-                    const uint32_t bb = (uint32_t)(f[2 * pp + 1] >> (jj * VB)) & ((1u << VB) - 1);
-                    c[pp] = tv[a | (bb << VB)];
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t c[4];
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const uint32_t a = (f[2 * pp] >> (jj * VB)) & M;
+                        const uint32_t bb = (f[2 * pp + 1] >> (jj * VB)) & M;
+                        c[pp] = tvl[kPfCopies * (a | (bb << VB))];
+                    }
+                    *reinterpret_cast<uint4*>(sm + kPfVT + pf_chunk(2 * jp + jj, t8)) =
+                        make_uint4(c[0], c[1], c[2], c[3]);
                 }
-                *reinterpret_cast<uint4*>(sm + kPfVT + pf_chunk(16 * dg + jj, t8)) = make_uint4(c[0], c[1], c[2], c[3]);
             }
         }
         fence_proxy_async_smem();
-        // 5. softmax of this thread's row
+        // 5. softmax: this thread's 32 columns of its row
         const bool ok_s = mbar_wait(bar_s, blk & 1);
         if (__syncthreads_or(!ok_s)) {
             if (tid == 0) report_timeout(status, kPfStatusWait);
@@ -272,53 +321,82 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
             break;
         }
         pend = 0;
+        if (blk + 1 < nblk) {  // the staging area is free: fetch the next block during this one
+            const int64_t t1 = t0 + kPfBlock;
+            pf_stage<KB, VB>(sa, cache, crow0, t1, kv_end - t1 < kPfBlock ? (int)(kv_end - t1) : kPfBlock, tid);
+        }
         tc_fence_after();
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t s[32];
-            tmem_ld32(t_row + 32 * c, s);
+        // s' = S * |k| per column; the row's scores in log2 units are s' * qx
+        // (qx > 0), so the running max is kept in s' units and
+        // p = exp2(s' qx - m qx).  Columns inside the row's range for the whole
+        // quarter skip the per-column mask.
+        float sv[32];
+        {
+            uint32_t sr[32];
+            tmem_ld32(t_row, sr);
             tmem_wait_ld();
+            const float4* kn4 = reinterpret_cast<const float4*>(kn_s + 32 * cq);
+            const bool full = rvalid && 32 * cq + 31 < nv && t0 + 32 * cq + 31 <= pos;
+            float mx = -INFINITY;
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int k = 32 * c + i;
-                const bool valid = rvalid && k < nv && t0 + k <= pos;
-                const float v = __uint_as_float(s[i]) * qx * kn_s[k];
-                mx = valid ? fmaxf(mx, v) : mx;
-            }
-        }
-        const float m_new = fmaxf(m, mx);
-        const float alpha = (m_new == -INFINITY || m == -INFINITY) ? 0.f : pf_exp2(m - m_new);
-        float lb = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t s[32];
-            tmem_ld32(t_row + 32 * c, s);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k8 = 0; k8 < 4; ++k8) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    float w2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 8 * k8 + 2 * pr + u, k = 32 * c + i;
-                        const bool valid = rvalid && k < nv && t0 + k <= pos;
-                        const float p = valid ? pf_exp2(__uint_as_float(s[i]) * qx * kn_s[k] - m_new) : 0.f;
-                        lb += p;
-                        w2[u] = p * vn_s[k] * inv2E;
-                    }
-                    const __half h0 = __float2half_rn(w2[0]), h1 = __float2half_rn(w2[1]);
-                    hi[pr] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-                    lo[pr] = pf_pack_half2(w2[0] - __half2float(h0), w2[1] - __half2float(h1));
+                for (int j = 0; j < 8; ++j) {
+                    const float4 kk = kn4[j];
+                    f2_split(f2_mul(f2(__uint_as_float(sr[4 * j]), __uint_as_float(sr[4 * j + 1])), f2(kk.x, kk.y)),
+                             sv[4 * j], sv[4 * j + 1]);
+                    f2_split(f2_mul(f2(__uint_as_float(sr[4 * j + 2]), __uint_as_float(sr[4 * j + 3])), f2(kk.z, kk.w)),
+                             sv[4 * j + 2], sv[4 * j + 3]);
+                    mx = fmaxf(mx, fmaxf(fmaxf(sv[4 * j], sv[4 * j + 1]), fmaxf(sv[4 * j + 2], sv[4 * j + 3])));
                 }
-                const int kc = 4 * c + k8;  // chunk of 8 positions
-                *reinterpret_cast<uint4*>(sm + kPfPH + pf_chunk(tid, kc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sm + kPfPL + pf_chunk(tid, kc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int k = 32 * cq + i;
+                    const bool valid = rvalid && k < nv && t0 + k <= pos;
+                    sv[i] = valid ? __uint_as_float(sr[i]) * kn_s[k] : -INFINITY;
+                    mx = fmaxf(mx, sv[i]);
+                }
             }
+            red[cq * 128 + r] = mx;
         }
-        l = l * alpha + lb;
+        __syncthreads();
+        const float m_new = fmaxf(m, fmaxf(fmaxf(red[r], red[128 + r]), fmaxf(red[256 + r], red[384 + r])));
+        const float qxs = rvalid ? qx : 1.f;
+        const float alpha = (m_new == -INFINITY || m == -INFINITY) ? 0.f : pf_exp2((m - m_new) * qxs);
+        const float nmq = m_new == -INFINITY ? 0.f : -m_new * qxs;  // masked columns: exp2(-inf) = 0
+        const F2 QX = f2(qxs, qxs), NMQ = f2(nmq, nmq);
+        F2 LB = f2(0.f, 0.f);
+        const float4* vn4 = reinterpret_cast<const float4*>(vn_s + 32 * cq);  // |v| / 2^E
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const float4 vv = vn4[2 * k8 + h2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = 8 * k8 + 4 * h2 + 2 * u;
+                    float a0, a1;
+                    f2_split(f2_fma(f2(sv[i], sv[i + 1]), QX, NMQ), a0, a1);
+                    const F2 pp = f2(pf_exp2(a0), pf_exp2(a1));
+                    LB = f2_add(LB, pp);
+                    float w0, w1;
+                    f2_split(f2_mul(pp, u == 0 ? f2(vv.x, vv.y) : f2(vv.z, vv.w)), w0, w1);
+                    const __half2 hh2 = __floats2half2_rn(w0, w1);
+                    const float2 hf = __half22float2(hh2);
+                    const __half2 ll2 = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
+                    hi[2 * h2 + u] = *reinterpret_cast<const uint32_t*>(&hh2);
+                    lo[2 * h2 + u] = *reinterpret_cast<const uint32_t*>(&ll2);
+                }
+            }
+            const int kc = 4 * cq + k8;  // chunk of 8 positions
+            *reinterpret_cast<uint4*>(sm + kPfPH + pf_chunk(r, kc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + kPfPL + pf_chunk(r, kc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        float lb0, lb1;
+        f2_split(LB, lb0, lb1);
+        const float lb = lb0 + lb1;
+        lp = lp * alpha + lb;
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -349,37 +427,47 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         }
         pend = 0;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        {
             uint32_t o[32];
-            tmem_ld32(t_row + 128 + 32 * c, o);
+            tmem_ld32(t_row + 128, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) O[32 * c + i] = fmaf(O[32 * c + i], alpha, __uint_as_float(o[i]));
+            for (int i = 0; i < 32; ++i) O[i] = fmaf(O[i], alpha, __uint_as_float(o[i]));
         }
         m = m_new;
         tc_fence_before();
-        __syncthreads();  // S, O_blk and the staging buffers are free for the next block
+        __syncthreads();  // S, O_blk, the staging buffers and red are free for the next block
     }
 
+    cp_async_wait_all();  // no copy of this thread is left in flight
     if (bad && pend) mbar_wait(pend == 1 ? bar_s : bar_pv, pend_par);  // bounded: let MMAs in flight finish
-    // normalise, rotate back (s . H (s2 . o) / sqrt(d)) and store the row
-    if (rvalid && !bad) {
+    // normalise (the row's sum over its four quarters), stage the rows in the
+    // Q region (fp32 [128][128]), rotate back (s . H (s2 . o) / sqrt(d)) and store
+    red[cq * 128 + r] = lp;
+    __syncthreads();
+    {
+        const float l = red[r] + red[128 + r] + red[256 + r] + red[384 + r];
         const float sc = l > 0.f ? ldexpf(P.out_mul, E) / l : 0.f;
-        if (P.two_sided) {
+        float* orow = reinterpret_cast<float*>(sm + kPfQH) + r * 128 + 32 * cq;
 #pragma unroll
-            for (int j = 0; j < 128; ++j) O[j] = __uint_as_float(__float_as_uint(O[j]) ^ P.sgn2[j]);
+        for (int i = 0; i < 32; ++i) {
+            const float v = O[i] * sc;
+            orow[i] = P.two_sided ? __uint_as_float(__float_as_uint(v) ^ P.sgn2[32 * cq + i]) : v;
         }
-        fwht_reg<128>(O);
-        float* dst = out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128;
+    }
+    fwht_smem<128>(reinterpret_cast<float*>(sm + kPfQH), kPfRows);  // synchronises the block
+    if (rvalid && !bad) {
+        const float* orow = reinterpret_cast<const float*>(sm + kPfQH) + r * 128 + 32 * cq;
+        float4* dst = reinterpret_cast<float4*>(out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128 + 32 * cq);
 #pragma unroll
-        for (int j = 0; j < 128; j += 4) {
+        for (int i = 0; i < 32; i += 4) {
+            const int j = 32 * cq + i;
             float4 v;
-            v.x = __uint_as_float(__float_as_uint(O[j] * sc * P.inv_sqrt_d) ^ P.sgn[j]);
-            v.y = __uint_as_float(__float_as_uint(O[j + 1] * sc * P.inv_sqrt_d) ^ P.sgn[j + 1]);
-            v.z = __uint_as_float(__float_as_uint(O[j + 2] * sc * P.inv_sqrt_d) ^ P.sgn[j + 2]);
-            v.w = __uint_as_float(__float_as_uint(O[j + 3] * sc * P.inv_sqrt_d) ^ P.sgn[j + 3]);
-            reinterpret_cast<float4*>(dst)[j / 4] = v;
+            v.x = __uint_as_float(__float_as_uint(orow[i] * P.inv_sqrt_d) ^ P.sgn[j]);
+            v.y = __uint_as_float(__float_as_uint(orow[i + 1] * P.inv_sqrt_d) ^ P.sgn[j + 1]);
+            v.z = __uint_as_float(__float_as_uint(orow[i + 2] * P.inv_sqrt_d) ^ P.sgn[j + 2]);
+            v.w = __uint_as_float(__float_as_uint(orow[i + 3] * P.inv_sqrt_d) ^ P.sgn[j + 3]);
+            dst[i / 4] = v;
         }
     }
     tc_fence_before();
@@ -427,7 +515,7 @@ cudaError_t prefill_launch(const void* q, int B, int T, int Hq, int Hkv, const i
     }
     const int G = Hq / Hkv;
     const dim3 grid((unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows), (unsigned)(B * Hkv));
-    fn<<<grid, 128, kPfSmem, s>>>(q16, qexp, Hq, Hkv, T, q_start, cache, out, status_word(), P);
+    fn<<<grid, kPfThreads, kPfSmem, s>>>(q16, qexp, Hq, Hkv, T, q_start, cache, out, status_word(), P);
     return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ CASES = [
     (1, 50, 4, 4, [130], 256, 2, 2),
     (2, 33, 16, 2, [5, 200], 300, 4, 2),
     (1, 200, 8, 8, [0], 256, 2, 4),
+    (2, 45, 8, 2, [3, 211], 257, 3, 3),  # a capacity that leaves norm rows 4-byte aligned only
 ]
 
 
