@@ -483,7 +483,7 @@ struct A3Meta {
 // the query).
 constexpr int kA3ItemCost = 4;
 constexpr int kA3EmptyCost = 1;
-constexpr int kA3RunCost = 32;
+constexpr int kA3RunCost = 128;
 constexpr int kA3PlanSmemPairs = 8192;  // pair prefixes kept in shared memory up to this count
 
 // Block-wide inclusive scan over 1024 threads; `total` gets the sum.

@@ -234,19 +234,19 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     int pend_par = 0;
     const int nblk = (int)((kv_end + kPfBlock - 1) / kPfBlock);
     if (nblk > 0) pf_stage<KB, VB>(sa, cache, crow0, 0, kv_end < kPfBlock ? (int)kv_end : kPfBlock, tid);
-
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int64_t t0 = (int64_t)blk * kPfBlock;
-        const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
-        // 1. the staged rows of this block have landed; the norms move to their
-        //    own arrays (the staging area takes the next block during this one)
+    // The K tile of block j + 1 is built while the PV product of block j runs
+    // (the K tile is free once S_j is done), and S_{j+1} is issued before the
+    // V tile of block j + 1 is built.
+    auto stage_k = [&]() {
+        // the staged rows of the block have landed; the norms move to their own
+        // arrays (the staging area takes the next block during this one)
         cp_async_wait_all();
         __syncthreads();
         if (tid < 128) kn_s[tid] = reinterpret_cast<const float*>(sm + kPfSKN)[tid];
         else if (tid < 256) vn_s[tid - 128] = reinterpret_cast<const float*>(sm + kPfSVN)[tid - 128] * inv2E;
-        // 2. K tile: lanes take the 16 chunks of 8 dims of a row (consecutive
-        //    words of the staged row, conflict-free tile stores); row
-        //    (tid / 16) + 32 i; 4 pair lookups per chunk
+        // K tile: lanes take the 16 chunks of 8 dims of a row (consecutive words
+        // of the staged row, conflict-free tile stores); row (tid / 16) + 32 i;
+        // 4 pair lookups per chunk
         {
             const int k8 = tid & 15;
 #pragma unroll
@@ -263,10 +263,12 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
                 *reinterpret_cast<uint4*>(sm + kPfKT + pf_chunk(t, k8)) = c;
             }
         }
+    };
+    auto issue_s = [&]() {
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // 3. S = Q K^T (high and low parts of Q)
+        // S = Q K^T (high and low parts of Q)
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -282,11 +284,20 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
             }
             umma_commit(bar_s);
         }
+    };
+    if (nblk > 0) {
+        stage_k();
+        issue_s();
         pend = 1;
-        pend_par = blk & 1;
-        // 4. V tile: lanes take consecutive dim pairs (2 jp, 2 jp + 1) of the
-        //    same rows; thread = (dim pair tid % 64, position groups (tid / 64)
-        //    + 8 i of 8 positions); entry (c[idx(t, j)], c[idx(t + 1, j)])
+        pend_par = 0;
+    }
+
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int64_t t0 = (int64_t)blk * kPfBlock;
+        const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
+        // V tile: lanes take consecutive dim pairs (2 jp, 2 jp + 1) of the same
+        // rows; thread = (dim pair tid % 64, position groups (tid / 64) + 8 i of
+        // 8 positions); entry (c[idx(t, j)], c[idx(t + 1, j)])
         {
             const int jp = tid & 63;
             constexpr uint32_t M = (1u << VB) - 1;
@@ -313,7 +324,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
             }
         }
         fence_proxy_async_smem();
-        // 5. softmax: this thread's 32 columns of its row
+        // softmax: this thread's 32 columns of its row
         const bool ok_s = mbar_wait(bar_s, blk & 1);
         if (__syncthreads_or(!ok_s)) {
             if (tid == 0) report_timeout(status, kPfStatusWait);
@@ -400,7 +411,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // 6. O_blk = P V (high and low parts of P), folded into the running output
+        // O_blk = P V (high and low parts of P), folded into the running output
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -419,6 +430,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         }
         pend = 2;
         pend_par = blk & 1;
+        if (blk + 1 < nblk) stage_k();  // K tile of the next block while PV runs
         const bool ok_pv = mbar_wait(bar_pv, blk & 1);
         if (__syncthreads_or(!ok_pv)) {
             if (tid == 0) report_timeout(status, kPfStatusWait);
@@ -435,8 +447,14 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
             for (int i = 0; i < 32; ++i) O[i] = fmaf(O[i], alpha, __uint_as_float(o[i]));
         }
         m = m_new;
-        tc_fence_before();
-        __syncthreads();  // S, O_blk, the staging buffers and red are free for the next block
+        if (blk + 1 < nblk) {  // its barrier also ends this block: S, O_blk and red are free
+            issue_s();
+            pend = 1;
+            pend_par = (blk + 1) & 1;
+        } else {
+            tc_fence_before();
+            __syncthreads();
+        }
     }
 
     cp_async_wait_all();  // no copy of this thread is left in flight
