@@ -163,6 +163,15 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kPfBar);
     uint64_t* bar_pv = bar_s + 1;
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
+    volatile int* wflag = reinterpret_cast<volatile int*>(sm + kPfMisc + 8);
+    // One thread waits (bounded) for an MMA to complete and the block's
+    // barrier releases the others: no warp spins on the mbarrier while others
+    // still have work.  Returns false for every thread if the wait gave up.
+    auto block_wait = [&](uint64_t* bar, int parity) {
+        if (tid == 0) *wflag = mbar_wait(bar, parity) ? 1 : 0;
+        __syncthreads();
+        return *wflag != 0;
+    };
     float* wred = reinterpret_cast<float*>(sm + kPfMisc + 16);
     uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPfTK);
     uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPfTV);
@@ -325,8 +334,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         }
         fence_proxy_async_smem();
         // softmax: this thread's 32 columns of its row
-        const bool ok_s = mbar_wait(bar_s, blk & 1);
-        if (__syncthreads_or(!ok_s)) {
+        if (!block_wait(bar_s, blk & 1)) {
             if (tid == 0) report_timeout(status, kPfStatusWait);
             bad = true;
             break;
@@ -431,8 +439,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         pend = 2;
         pend_par = blk & 1;
         if (blk + 1 < nblk) stage_k();  // K tile of the next block while PV runs
-        const bool ok_pv = mbar_wait(bar_pv, blk & 1);
-        if (__syncthreads_or(!ok_pv)) {
+        if (!block_wait(bar_pv, blk & 1)) {
             if (tid == 0) report_timeout(status, kPfStatusWait);
             bad = true;
             break;
