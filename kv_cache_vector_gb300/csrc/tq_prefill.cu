@@ -31,8 +31,9 @@
 //   6. one thread issues O_blk = P_hi V + P_lo V into tensor memory; each
 //      thread folds its quarter of the row into the running output held in
 //      registers, O = O * exp2(m_old - m_new) + O_blk.
-// At the end the rows are divided by the denominator, scaled by 2^E / s_v,
-// staged in shared memory and rotated back (s . H (s2 . o) / sqrt(d)).
+// At the end the rows are divided by the denominator, scaled by 2^E / s_v
+// and rotated back (s . H (s2 . o) / sqrt(d)): butterflies over a thread's
+// quarter in registers, the two across quarters through shared memory.
 //
 // Every wait on an mbarrier is bounded (2 s); a wait that gives up sets the
 // device status word, the CTA stops, waits (bounded) for its MMAs in flight,
@@ -466,32 +467,49 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
 
     cp_async_wait_all();  // no copy of this thread is left in flight
     if (bad && pend) mbar_wait(pend == 1 ? bar_s : bar_pv, pend_par);  // bounded: let MMAs in flight finish
-    // normalise (the row's sum over its four quarters), stage the rows in the
-    // Q region (fp32 [128][128]), rotate back (s . H (s2 . o) / sqrt(d)) and store
+    // normalise (the row's sum over its four quarters) and rotate back,
+    // s . H (s2 . o) / sqrt(d): H over the 7 index bits of a row is the
+    // butterflies over bits 0-4 (a thread's quarter, in registers) and over
+    // bits 5 and 6 (between the four threads of the row, through shared
+    // memory laid out [quarter][element][row] so that a warp's accesses hit
+    // 32 banks).  The Q region holds the exchange buffer (64 KB).
     red[cq * 128 + r] = lp;
     __syncthreads();
     {
         const float l = red[r] + red[128 + r] + red[256 + r] + red[384 + r];
         const float sc = l > 0.f ? ldexpf(P.out_mul, E) / l : 0.f;
-        float* orow = reinterpret_cast<float*>(sm + kPfQH) + r * 128 + 32 * cq;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float v = O[i] * sc;
-            orow[i] = P.two_sided ? __uint_as_float(__float_as_uint(v) ^ P.sgn2[32 * cq + i]) : v;
+            O[i] = P.two_sided ? __uint_as_float(__float_as_uint(v) ^ P.sgn2[32 * cq + i]) : v;
         }
     }
-    fwht_smem<128>(reinterpret_cast<float*>(sm + kPfQH), kPfRows);  // synchronises the block
+    fwht_reg<32>(O);
+    float* xs = reinterpret_cast<float*>(sm + kPfQH);
+#pragma unroll
+    for (int bit = 1; bit <= 2; bit <<= 1) {  // quarter index bits: index bits 5 and 6
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xs[(cq * 32 + i) * 128 + r] = O[i];
+        __syncthreads();
+        const int pq = cq ^ bit;
+        const bool upper = (cq & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float o = xs[(pq * 32 + i) * 128 + r];
+            O[i] = upper ? o - O[i] : O[i] + o;  // (lo + hi, lo - hi)
+        }
+        __syncthreads();
+    }
     if (rvalid && !bad) {
-        const float* orow = reinterpret_cast<const float*>(sm + kPfQH) + r * 128 + 32 * cq;
         float4* dst = reinterpret_cast<float4*>(out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128 + 32 * cq);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             const int j = 32 * cq + i;
             float4 v;
-            v.x = __uint_as_float(__float_as_uint(orow[i] * P.inv_sqrt_d) ^ P.sgn[j]);
-            v.y = __uint_as_float(__float_as_uint(orow[i + 1] * P.inv_sqrt_d) ^ P.sgn[j + 1]);
-            v.z = __uint_as_float(__float_as_uint(orow[i + 2] * P.inv_sqrt_d) ^ P.sgn[j + 2]);
-            v.w = __uint_as_float(__float_as_uint(orow[i + 3] * P.inv_sqrt_d) ^ P.sgn[j + 3]);
+            v.x = __uint_as_float(__float_as_uint(O[i] * P.inv_sqrt_d) ^ P.sgn[j]);
+            v.y = __uint_as_float(__float_as_uint(O[i + 1] * P.inv_sqrt_d) ^ P.sgn[j + 1]);
+            v.z = __uint_as_float(__float_as_uint(O[i + 2] * P.inv_sqrt_d) ^ P.sgn[j + 2]);
+            v.w = __uint_as_float(__float_as_uint(O[i + 3] * P.inv_sqrt_d) ^ P.sgn[j + 3]);
             dst[i / 4] = v;
         }
     }
