@@ -197,7 +197,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         mbar_init(bar_pv, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc<256>(slot);
+    if (warp == 0) tmem_alloc<512>(slot);  // S 0-127, O_blk 128-255, P high 256-319, P low 320-383
 
     // E: the largest V norm this CTA reads is below 2^E
     const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
@@ -387,9 +387,11 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
         const F2 QX = f2(qxs, qxs), NMQ = f2(nmq, nmq);
         F2 LB = f2(0.f, 0.f);
         const float4* vn4 = reinterpret_cast<const float4*>(vn_s + 32 * cq);  // |v| / 2^E
+        uint32_t hi16[16], lo16[16];  // this quarter's 32 positions of P as fp16 pairs
 #pragma unroll
         for (int k8 = 0; k8 < 4; ++k8) {
-            uint32_t hi[4], lo[4];
+            uint32_t* hi = hi16 + 4 * k8;
+            uint32_t* lo = lo16 + 4 * k8;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const float4 vv = vn4[2 * k8 + h2];
@@ -409,9 +411,13 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
                     lo[2 * h2 + u] = *reinterpret_cast<const uint32_t*>(&ll2);
                 }
             }
-            const int kc = 4 * cq + k8;  // chunk of 8 positions
-            *reinterpret_cast<uint4*>(sm + kPfPH + pf_chunk(r, kc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sm + kPfPL + pf_chunk(r, kc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        // P to tensor memory, row r, columns 16 cq .. 16 cq + 15 of each part
+        {
+            const uint32_t t_p = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 16 * cq;
+            tmem_st16(t_p, hi16);
+            tmem_st16(t_p + 64, lo16);
+            tmem_wait_st();
         }
         float lb0, lb1;
         f2_split(LB, lb0, lb1);
@@ -426,14 +432,13 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem + 128, umma_desc_sw128(sa + kPfPH + off), umma_desc_sw128(sa + kPfVT + off), idesc,
-                         kk > 0 ? 1u : 0u);
+                umma_f16_ts(tmem + 128, tmem + 256 + 8 * kk, umma_desc_sw128(sa + kPfVT + off), idesc,
+                            kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem + 128, umma_desc_sw128(sa + kPfPL + off), umma_desc_sw128(sa + kPfVT + off), idesc,
-                         1u);
+                umma_f16_ts(tmem + 128, tmem + 320 + 8 * kk, umma_desc_sw128(sa + kPfVT + off), idesc, 1u);
             }
             umma_commit(bar_pv);
         }
@@ -517,7 +522,7 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc<256>(tmem);
+        tmem_dealloc<512>(tmem);
     }
 }
 
