@@ -567,7 +567,7 @@ def extra_prefill(peak_hbm):
         q = synth.device_normal(96, (B, T, Hq, D))
         qs = torch.full((B,), start, dtype=torch.int32, device="cuda")
         out = torch.empty(B, T, Hq, D, dtype=torch.float32, device="cuda")
-        ws = torch.empty(abi.lib().tq_attn_prefill_workspace_bytes(B, T, Hq, D), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(abi.lib().tq_attn_prefill_workspace_bytes(B, T, Hq, Hkv, cap, D), dtype=torch.uint8, device="cuda")
         f = lambda: abi.tq_attn_prefill(plan, q, cache, qs, 1.0 / math.sqrt(D), out=out, workspace=ws)
         for _ in range(3):
             f()

@@ -296,9 +296,11 @@ tq_status tq_attn_decode_append_paged(const tq_plan *plan, const void *q, const 
                                       float scale, float sparse_v_threshold, float *out, void *workspace,
                                       size_t workspace_bytes, tq_stream_t stream);
 
-/* Workspace bytes tq_attn_prefill needs (the rotated queries); 0 for invalid
- * sizes or d != 128. */
-size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int d);
+/* Workspace bytes tq_attn_prefill needs for a cache of capacity `cap`: the
+ * expanded K/V tiles, 66564 bytes per 128 cache positions per sequence and
+ * KV head (about 4.3 times the packed K4/V3 cache they expand); 0 for
+ * invalid sizes, cap < T or d != 128.  B, T, Hq are checked only. */
+size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int Hkv, int64_t cap, int d);
 
 /* Prefill (chunked, multi-query) attention over the packed cache: a chunk of
  * T query tokens per sequence, token t of sequence b at absolute position
@@ -313,7 +315,9 @@ size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int d);
  *   q_start: [B] int32, device; every q_start[b] + T must be <= cache.cap
  *     (checked on the device: a sequence that breaks it gets zero rows and
  *     the device status word 52).
- *   workspace: tq_attn_prefill_workspace_bytes(B, T, Hq, 128) bytes.
+ *   workspace: tq_attn_prefill_workspace_bytes(B, T, Hq, Hkv, cache.cap, 128)
+ *     bytes; the prefix of every sequence is expanded there once into fp16
+ *     centroid tiles, then read by every query tile of its KV head.
  * Errors: TQ_ERR_UNSUPPORTED (d, group size, bits), TQ_ERR_RANGE (cap < T),
  * TQ_ERR_INVALID_ARG, TQ_ERR_ALIGNMENT, TQ_ERR_WORKSPACE. */
 tq_status tq_attn_prefill(const tq_plan *plan, const void *q, int B, int T, int Hq, int Hkv,

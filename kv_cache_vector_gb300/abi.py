@@ -84,7 +84,7 @@ def lib() -> ctypes.CDLL:
                                        f32, f32, vp, vp, ctypes.c_size_t, vp]),
         ("tq_attn_decode_append_paged", i32, [vp, vp, vp, vp, i32, i32, i32, i32, PagedCacheView, vp, i32, vp,
                                               i64, i32, i32, f32, f32, vp, vp, ctypes.c_size_t, vp]),
-        ("tq_attn_prefill_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32]),
+        ("tq_attn_prefill_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32, i64, i32]),
         ("tq_attn_prefill", i32, [vp, vp, i32, i32, i32, i32, CacheView, vp, i32, i32, f32, vp, vp,
                                   ctypes.c_size_t, vp]),
         ("tq_status_string", ctypes.c_char_p, [i32]),
@@ -419,7 +419,7 @@ def tq_attn_prefill(plan: Plan, q: torch.Tensor, cache: Cache, q_start: torch.Te
     Hkv = cache.k_norm.shape[1]
     if out is None:
         out = torch.empty(B, T, Hq, d, dtype=torch.float32, device=q.device)
-    need = int(lib().tq_attn_prefill_workspace_bytes(B, T, Hq, d))
+    need = int(lib().tq_attn_prefill_workspace_bytes(B, T, Hq, Hkv, cache.cap, d))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _cuda(q, out, workspace)

@@ -645,9 +645,9 @@ tq_status tq_attn_decode_append_paged(const tq_plan* plan, const void* q, const 
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
-size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int d) {
-    if (B < 0 || T < 1 || Hq <= 0 || d != 128) return 0;
-    return tq::attn_prefill_ws_bytes(B, T, Hq);
+size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int Hkv, int64_t cap, int d) {
+    if (B < 0 || T < 1 || Hq <= 0 || Hkv <= 0 || cap < T || d != 128) return 0;
+    return tq::attn_prefill_ws_bytes(B, Hkv, cap);
 }
 
 tq_status tq_attn_prefill(const tq_plan* plan, const void* q, int B, int T, int Hq, int Hkv, tq_cache_view cache,
@@ -667,7 +667,7 @@ tq_status tq_attn_prefill(const tq_plan* plan, const void* q, int B, int T, int 
     if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned16(cache.k_packed) ||
         !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
         return TQ_ERR_ALIGNMENT;
-    if (!workspace || workspace_bytes < tq::attn_prefill_ws_bytes(B, T, Hq)) return TQ_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < tq::attn_prefill_ws_bytes(B, Hkv, cache.cap)) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
     if (!device_accessible(q) || !device_accessible(out) || !device_accessible(q_start) ||
         !device_accessible(workspace) || !device_accessible(cache.k_packed) || !device_accessible(cache.v_packed) ||

@@ -169,14 +169,24 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
                                  const PagedArgs& pa, cudaStream_t s, const AttnAppend* app = nullptr);
 // Prefill (multi-query, causal) attention, d = 128 (tq_prefill.cu, one unit
-// per K width).  workspace: the rotated queries, attn_prefill_ws_bytes.
-inline size_t attn_prefill_ws_bytes(int B, int T, int Hq) {
-    return ((size_t)B * T * Hq * (512 + 4) + 255) / 256 * 256;
+// per K width).  workspace: one expanded tile image of kPfImgBytes per block
+// of 128 cache positions per (sequence, KV head), then each block's largest
+// V norm (a float).
+constexpr size_t kPfImgBytes = 66560;
+inline size_t attn_prefill_img_bytes(int B, int Hkv, int64_t cap) {
+    return (size_t)B * Hkv * (size_t)((cap + 127) / 128) * kPfImgBytes;
+}
+inline size_t attn_prefill_ws_bytes(int B, int Hkv, int64_t cap) {
+    return attn_prefill_img_bytes(B, Hkv, cap) + ((size_t)B * Hkv * (size_t)((cap + 127) / 128) * 4 + 15) / 16 * 16;
 }
 template <int KB>
 cudaError_t launch_attn_prefill(int v_bits, const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
                                 const tq_cache_view& cache, float* out, void* workspace, const AttnParams& P,
                                 cudaStream_t s);
+// The attention kernel of the prefill (after the tile images are written).
+cudaError_t launch_prefill_attention(const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
+                                     const tq_cache_view& cache, float* out, void* workspace,
+                                     const AttnParams& P, cudaStream_t s);
 // Paged append of one token per sequence, d >= 32 (tq_codec.cu).
 template <int D>
 cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const void* k_new,

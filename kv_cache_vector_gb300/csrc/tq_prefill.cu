@@ -9,35 +9,42 @@
 // output) with many queries per KV head, which turns both contractions into
 // dense matrix products.
 //
-// One CTA of sixteen warps takes 128 query rows of one (sequence, KV head):
-// 128 / G consecutive tokens times the G query heads of the group (row r =
-// token (r / G), head (r % G)).  Per block of 128 KV positions:
-//   1. the packed K and V rows and their norms are staged in shared memory;
-//   2. the threads turn K into fp16 centroids c * s_k (a 128 x 128 tile in
-//      the 128-byte-swizzled K-major layout; lookups in a table of centroid
-//      pairs of two consecutive dims);
-//   3. one thread issues S = Q_hi K^T + Q_lo K^T (tcgen05.mma kind::f16, fp32
-//      accumulator in tensor memory): the rotated query is split into fp16
-//      high and low parts, so it keeps about 22 significant bits;
-//   4. meanwhile the threads turn V into fp16 centroids c * s_v, transposed
-//      (positions contiguous per dim; lookups in a table of centroid pairs of
-//      two consecutive positions);
-//   5. four threads share a row of S (a quarter of the columns each): they
-//      read it from tensor memory, apply the query's power-of-two scale, the
-//      K norms and the causal mask, merge their maxima through shared memory
-//      and update the running max and denominator (log2 units); P = exp2(s -
-//      m) times the V norm over 2^E (E fixed per CTA from the largest V norm
-//      it reads, so P <= 1) goes to shared memory as fp16 high and low parts;
-//   6. one thread issues O_blk = P_hi V + P_lo V into tensor memory; each
-//      thread folds its quarter of the row into the running output held in
-//      registers, O = O * exp2(m_old - m_new) + O_blk.
-// At the end the rows are divided by the denominator, scaled by 2^E / s_v
-// and rotated back (s . H (s2 . o) / sqrt(d)): butterflies over a thread's
-// quarter in registers, the two across quarters through shared memory.
+// Two kernels.  Every (sequence, KV head) has many query tiles, and each of
+// them reads the whole prefix, so the packed rows are expanded once, not once
+// per tile:
+//   k_prefill_expand  turns each block of 128 cached positions into a tile
+//     image in the workspace: the K centroids [position][dim] and the V
+//     centroids [dim][position] as fp16, both in the 128-byte-swizzled
+//     K-major layout the tensor cores read, then the 128 K norms and the
+//     128 V norms (65 KB; norms past the sequence's last position are zero,
+//     centroids there c[0]).
+//   k_attn_prefill  takes 128 query rows of one (sequence, KV head): 128 / G
+//     consecutive tokens times the G query heads of the group (row r = token
+//     r / G, head r % G), with warp roles:
+//       warp 0    streams the tile images into two stages (bulk copies);
+//       warp 1    issues S = Q_hi K^T + Q_lo K^T into one of two tensor-memory
+//                 buffers (the rotated query split into fp16 high and low
+//                 parts keeps about 22 significant bits) and, once the
+//                 softmax has written P over it, O += P_hi V + P_lo V (A read
+//                 from tensor memory);
+//       warps 2-9 two threads per query row, 64 columns each: scores times
+//                 the K norms and the query's power-of-two scale, the causal
+//                 mask, the row max merged through shared memory; P = exp2(s
+//                 - m) times the V norm over 2^E (E fixed per CTA from the
+//                 largest V norm it reads) as fp16 high and low parts,
+//                 stored over the thread's own S columns.
+//     The output accumulates in tensor memory.  The reference max m of a row
+//     moves only when a block raises the row max by more than 8 (log2 units),
+//     so P stays below 2^8; when it moves, the softmax threads rescale their
+//     output columns in tensor memory after the previous PV product is done.
+//     At the end the rows are divided by the denominator, scaled by 2^E / s_v
+//     and rotated back (s . H (s2 . o) / sqrt(d)): butterflies over a
+//     thread's 64 columns in registers, the last one through shared memory.
 //
 // Every wait on an mbarrier is bounded (2 s); a wait that gives up sets the
-// device status word, the CTA stops, waits (bounded) for its MMAs in flight,
-// frees its tensor memory and returns.
+// device status word and a flag that ends every other wait of the CTA, the
+// MMA thread waits (bounded) for its products in flight, the copy thread for
+// its copies, and the CTA frees its tensor memory and returns.
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -47,36 +54,29 @@
 #include "tq_device.cuh"
 #include "tq_umma.cuh"
 
+#if !defined(TQ_UNIT_KB)
+#error "compile once per K width with -DTQ_UNIT_KB=<bits>"
+#endif
+
 namespace tq {
 namespace dev {
 
-constexpr int kPfRows = 128;     // query rows per CTA
 constexpr int kPfBlock = 128;    // KV positions per block
-constexpr int kPfThreads = 512;  // 16 warps; warp w reads tensor-memory lanes 32 (w % 4) .. + 31,
-                                 // columns 32 (w / 4) .. + 31 of its rows
-// shared memory, offsets from a 1024-aligned base
-constexpr uint32_t kPfQH = 0;          // Q high parts, 128 x 128 fp16 (the output rows at the end)
-constexpr uint32_t kPfQL = 32768;      // Q low parts
-constexpr uint32_t kPfKT = 65536;      // K centroids of the block, [position][dim]
-constexpr uint32_t kPfVT = 98304;      // V centroids of the block, [dim][position]
-constexpr uint32_t kPfPH = 131072;     // P high parts, [row][position]
-constexpr uint32_t kPfPL = 163840;     // P low parts
-constexpr uint32_t kPfTK = 196608;     // K pair table, 4 copies (up to 256 x 4 words)
-constexpr uint32_t kPfTV = 200704;     // V pair table, 4 copies
-constexpr uint32_t kPfSK = 204800;     // staged packed K rows of the next block, 64-byte stride
-constexpr uint32_t kPfSV = 212992;     // staged packed V rows
-constexpr uint32_t kPfSKN = 221184;    // staged K norms (128 floats)
-constexpr uint32_t kPfSVN = 221696;    // staged V norms
-constexpr uint32_t kPfKN = 222208;     // K norms of the block (128 floats)
-constexpr uint32_t kPfVN = 222720;     // V norms of the block over 2^E
-constexpr uint32_t kPfRed = 223232;    // [4][128] floats: per-quarter row maxima / sums
-constexpr uint32_t kPfBar = 225280;    // two mbarriers
-constexpr uint32_t kPfMisc = 225296;   // tensor-memory base, reduction scratch (16 floats)
-constexpr uint32_t kPfEnd = 225424;
-constexpr int kPfCopies = 4;           // table copies: lane l reads copy l % 4 (fewer bank conflicts)
-constexpr uint32_t kPfSmem = kPfEnd + 1024;  // plus alignment slack
-constexpr int kPfStatusWait = 51;      // an MMA completion wait gave up
-constexpr int kPfStatusRange = 52;     // q_start[b] + T exceeds the cache capacity, or q_start < 0
+// tile image of one block, offsets within it
+constexpr uint32_t kPfImgK = 0;        // K centroids, 128 x 128 fp16, [position][dim]
+constexpr uint32_t kPfImgV = 32768;    // V centroids, [dim][position]
+constexpr uint32_t kPfImgKN = 65536;   // K norms (128 floats)
+constexpr uint32_t kPfImgVN = 66048;   // V norms
+static_assert(kPfImgVN + 512 == kPfImgBytes, "tile image layout");
+
+// ---- expansion kernel
+constexpr int kPxThreads = 256;
+constexpr uint32_t kPxSK = kPfImgBytes;      // staged packed K rows, 64-byte stride
+constexpr uint32_t kPxSV = kPxSK + 8192;     // staged packed V rows
+constexpr uint32_t kPxTK = kPxSV + 8192;     // K pair table, 4 copies (up to 256 x 4 words)
+constexpr uint32_t kPxTV = kPxTK + 4096;     // V pair table, 4 copies
+constexpr uint32_t kPxSmem = kPxTV + 4096;
+constexpr int kPfCopies = 4;                 // table copies: lane l reads copy l % 4 (fewer bank conflicts)
 
 // Offset of the 16-byte chunk holding elements [8 k8, 8 k8 + 8) of `row` in a
 // 128 x 128 fp16 K-major tile with the 128-byte swizzle (two 64-column
@@ -96,228 +96,103 @@ __device__ __forceinline__ uint32_t pf_bits(const uint32_t* w, int pos) {
     return sh + N > 32 ? __funnelshift_r(lo, w[i + 1], sh) : lo >> sh;
 }
 
-// Stage the packed K and V rows and the norms of positions t0 .. t0 + 127 of
-// cache rows crow0 + .. with cp.async (zero fill past n valid rows; the
-// source of a zero-filled copy is row crow0, which exists).
-template <int KB, int VB>
-__device__ __forceinline__ void pf_stage(uint32_t sa, const tq_cache_view& cache, int64_t crow0, int64_t t0,
-                                         int n, int tid) {
-    constexpr int KP = KB, VP = VB;  // 16-byte parts per packed row (16 * bits bytes)
-    if (tid < 128 * KP) {
-        const int row = tid / KP, part = tid - row * KP;
-        const bool in = row < n;
-        const uint8_t* src = cache.k_packed + (crow0 + (in ? t0 + row : 0)) * (16 * KB) + part * 16;
-        cp_async16(sa + kPfSK + row * 64 + part * 16, src, in ? 16u : 0u);
-    }
-    if (tid < 128 * VP) {
-        const int row = tid / VP, part = tid - row * VP;
-        const bool in = row < n;
-        const uint8_t* src = cache.v_packed + (crow0 + (in ? t0 + row : 0)) * (16 * VB) + part * 16;
-        cp_async16(sa + kPfSV + row * 64 + part * 16, src, in ? 16u : 0u);
-    }
-    if (tid < 256) {  // norms, one per copy (a norm row is only 4-byte aligned); zeros past n
-        const int k = tid & 127, side = tid >> 7;
-        const float* nrm = side ? cache.v_norm : cache.k_norm;
-        cp_async4(sa + (side ? kPfSVN : kPfSKN) + 4 * k, nrm + crow0 + (k < n ? t0 + k : 0), k < n ? 4u : 0u);
-    }
-    cp_async_commit();
-}
-
 __device__ __forceinline__ uint32_t pf_pack_half2(float a, float b) {
     return (uint32_t)__half_as_ushort(__float2half_rn(a)) | ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
 }
 
-__device__ __forceinline__ float pf_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
+// ------------------------------------------------------------------ expansion
 
-// Tiles of a (sequence, KV head) are taken last first: with a causal mask the
-// last tiles read the most KV blocks, so the longest CTAs start first.
+// Block (x, bg) expands blocks x, x + gridDim.x, .. of (sequence, KV head) bg
+// into img + (bg nbmax + j) kPfImgBytes, and the block's largest |V norm|
+// into bmax[bg nbmax + j].  Blocks at or past the sequence's last position
+// q_start[b] + T are not read; a sequence whose range is invalid is skipped
+// (the attention kernel reports it).
 template <int KB, int VB>
-__global__ void __launch_bounds__(kPfThreads, 1)
-k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv, int T,
-               const int32_t* __restrict__ q_start, tq_cache_view cache, float* __restrict__ out,
-               int* status, const __grid_constant__ AttnParams P) {
-    extern __shared__ __align__(1024) unsigned char pf_raw[];
-    unsigned char* sm = pf_raw + ((1024u - (smem_addr(pf_raw) & 1023u)) & 1023u);
-    const uint32_t sa = smem_addr(sm);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = 32 * (warp & 3) + lane;  // this thread's query row in the tile
-    const int cq = warp >> 2;              // and its quarter of the columns
-    const int G = Hq / Hkv, tpr = kPfRows / G;
-    const int bg = blockIdx.y, b = bg / Hkv, g = bg - b * Hkv;
-    const int mt = (int)(gridDim.x - 1 - blockIdx.x);
-    const int rows_total = T * G;
-    const int grow = mt * kPfRows + r;  // this thread's row within (b, g)
-    const bool rvalid = grow < rows_total;
-    const int tok = rvalid ? grow / G : 0, hh = grow - (grow / G) * G;
-    int64_t qs = __ldg(q_start + b);
-    const int last_tok = min(T, (mt + 1) * tpr) - 1;
-    if (qs < 0 || qs + T > cache.cap) {  // nothing sensible to read: report and write zeros
-        if (tid == 0) report_timeout(status, kPfStatusRange);
-        qs = -1;
-    }
-    const int64_t pos = qs + tok;                            // this row attends [0, pos]
-    const int64_t kv_end = qs < 0 ? 0 : qs + last_tok + 1;   // rows this CTA reads
-    uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kPfBar);
-    uint64_t* bar_pv = bar_s + 1;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
-    volatile int* wflag = reinterpret_cast<volatile int*>(sm + kPfMisc + 8);
-    // One thread waits (bounded) for an MMA to complete and the block's
-    // barrier releases the others: no warp spins on the mbarrier while others
-    // still have work.  Returns false for every thread if the wait gave up.
-    auto block_wait = [&](uint64_t* bar, int parity) {
-        if (tid == 0) *wflag = mbar_wait(bar, parity) ? 1 : 0;
-        __syncthreads();
-        return *wflag != 0;
-    };
-    float* wred = reinterpret_cast<float*>(sm + kPfMisc + 16);
-    uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPfTK);
-    uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPfTV);
-    float* kn_s = reinterpret_cast<float*>(sm + kPfKN);
-    float* vn_s = reinterpret_cast<float*>(sm + kPfVN);
-    float* red = reinterpret_cast<float*>(sm + kPfRed);
-
+__global__ void __launch_bounds__(kPxThreads, 2)
+k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_view cache, int nbmax,
+                 unsigned char* __restrict__ img, float* __restrict__ bmax, const __grid_constant__ AttnParams P) {
+    extern __shared__ __align__(16) unsigned char px_raw[];
+    unsigned char* sm = px_raw;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int bg = blockIdx.y, b = bg / Hkv;
+    const int64_t qs = __ldg(q_start + b);
+    if (qs < 0 || qs + T > cache.cap) return;
+    const int64_t kv_end = qs + T;
+    const int nb = (int)((kv_end + kPfBlock - 1) / kPfBlock);
+    if ((int)blockIdx.x >= nb) return;
+    const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
+    uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPxTK);
+    uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPxTV);
     // pair tables: entry e = (c[e % 2^b], c[e / 2^b]) as two fp16 halves, copy
-    // c of entry e at word 8 e + c
-    for (int i = tid; i < (kPfCopies << (2 * KB)); i += kPfThreads) {
+    // c of entry e at word 4 e + c
+    for (int i = tid; i < (kPfCopies << (2 * KB)); i += kPxThreads) {
         const int e = i / kPfCopies;
         tk[i] = pf_pack_half2(P.kcen_h[e & ((1 << KB) - 1)], P.kcen_h[e >> KB]);
     }
-    for (int i = tid; i < (kPfCopies << (2 * VB)); i += kPfThreads) {
+    for (int i = tid; i < (kPfCopies << (2 * VB)); i += kPxThreads) {
         const int e = i / kPfCopies;
         tv[i] = pf_pack_half2(P.vcen_h[e & ((1 << VB) - 1)], P.vcen_h[e >> VB]);
     }
     const uint32_t* tkl = tk + (lane & (kPfCopies - 1));  // this lane's copy
     const uint32_t* tvl = tv + (lane & (kPfCopies - 1));
-    if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_pv, 1);
-        mbar_fence_init();
-    }
-    if (warp == 0) tmem_alloc<512>(slot);  // S 0-127, O_blk 128-255, P high 256-319, P low 320-383
 
-    // E: the largest V norm this CTA reads is below 2^E
-    const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
-    float vmax = 0.f;
-    for (int64_t t = tid; t < kv_end; t += kPfThreads) vmax = fmaxf(vmax, fabsf(__ldg(cache.v_norm + crow0 + t)));
-    for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
-    if (lane == 0) wred[warp] = vmax;
-
-    // Q tile: row r, chunks 4 cq .. 4 cq + 3 of the high and low parts
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(q16 + ((int64_t)bg * rows_total + grow) * 256);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k8 = 4 * cq + i;
-            const uint4 h = rvalid ? __ldg(src + k8) : make_uint4(0, 0, 0, 0);
-            const uint4 l = rvalid ? __ldg(src + 16 + k8) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kPfQH + pf_chunk(r, k8)) = h;
-            *reinterpret_cast<uint4*>(sm + kPfQL + pf_chunk(r, k8)) = l;
+    for (int j = blockIdx.x; j < nb; j += gridDim.x) {
+        const int64_t t0 = (int64_t)j * kPfBlock;
+        const int n = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
+        // packed rows (one contiguous run of the cache) and norms; zeros past n
+        for (int i = tid; i < kPfBlock * KB; i += kPxThreads) {
+            const int row = i / KB, part = i - row * KB;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < n)
+                v = __ldg(reinterpret_cast<const uint4*>(cache.k_packed + (crow0 + t0 + row) * (16 * KB)) + part);
+            *reinterpret_cast<uint4*>(sm + kPxSK + row * 64 + part * 16) = v;
         }
-    }
-    const float qx = rvalid ? __ldg(qexp + (int64_t)bg * rows_total + grow) : 0.f;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *slot;
-    int E = 0;
-    {
-        float vm = 0.f;
-#pragma unroll
-        for (int w = 0; w < kPfThreads / 32; ++w) vm = fmaxf(vm, wred[w]);
-        if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
-    }
-    const float inv2E = ldexpf(1.f, -E);
-    const uint32_t t_row = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cq;  // this thread's S columns
-    constexpr uint32_t idesc = umma_idesc_f16(128, 128, false);
-
-    float O[32];  // columns 32 cq .. 32 cq + 31 of the output row (rotated, units of 2^E s_v)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) O[j] = 0.f;
-    float m = -INFINITY, lp = 0.f;  // running max of the row (s' units) and this quarter's sum
-    bool bad = false;
-    int pend = 0;  // 1: the S MMAs of the current block may be in flight; 2: the PV MMAs
-    int pend_par = 0;
-    const int nblk = (int)((kv_end + kPfBlock - 1) / kPfBlock);
-    if (nblk > 0) pf_stage<KB, VB>(sa, cache, crow0, 0, kv_end < kPfBlock ? (int)kv_end : kPfBlock, tid);
-    // The K tile of block j + 1 is built while the PV product of block j runs
-    // (the K tile is free once S_j is done), and S_{j+1} is issued before the
-    // V tile of block j + 1 is built.
-    auto stage_k = [&]() {
-        // the staged rows of the block have landed; the norms move to their own
-        // arrays (the staging area takes the next block during this one)
-        cp_async_wait_all();
+        for (int i = tid; i < kPfBlock * VB; i += kPxThreads) {
+            const int row = i / VB, part = i - row * VB;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row < n)
+                v = __ldg(reinterpret_cast<const uint4*>(cache.v_packed + (crow0 + t0 + row) * (16 * VB)) + part);
+            *reinterpret_cast<uint4*>(sm + kPxSV + row * 64 + part * 16) = v;
+        }
+        {
+            const int k = tid & 127;
+            const float* nrm = tid < 128 ? cache.k_norm : cache.v_norm;
+            reinterpret_cast<float*>(sm + (tid < 128 ? kPfImgKN : kPfImgVN))[k] =
+                k < n ? __ldg(nrm + crow0 + t0 + k) : 0.f;
+        }
         __syncthreads();
-        if (tid < 128) kn_s[tid] = reinterpret_cast<const float*>(sm + kPfSKN)[tid];
-        else if (tid < 256) vn_s[tid - 128] = reinterpret_cast<const float*>(sm + kPfSVN)[tid - 128] * inv2E;
         // K tile: lanes take the 16 chunks of 8 dims of a row (consecutive words
-        // of the staged row, conflict-free tile stores); row (tid / 16) + 32 i;
+        // of the staged row, conflict-free tile stores); rows (tid / 16) + 16 i;
         // 4 pair lookups per chunk
         {
             const int k8 = tid & 15;
+            constexpr uint32_t M = (1u << (2 * KB)) - 1;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = (tid >> 4) + 32 * i;
+            for (int i = 0; i < 8; ++i) {
+                const int t = (tid >> 4) + 16 * i;
                 const uint32_t f =
-                    pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sm + kPfSK + t * 64), k8 * 8 * KB);
-                constexpr uint32_t M = (1u << (2 * KB)) - 1;
+                    pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sm + kPxSK + t * 64), k8 * 8 * KB);
                 uint4 c;
                 c.x = tkl[kPfCopies * (f & M)];
                 c.y = tkl[kPfCopies * ((f >> (2 * KB)) & M)];
                 c.z = tkl[kPfCopies * ((f >> (4 * KB)) & M)];
                 c.w = tkl[kPfCopies * ((f >> (6 * KB)) & M)];
-                *reinterpret_cast<uint4*>(sm + kPfKT + pf_chunk(t, k8)) = c;
+                *reinterpret_cast<uint4*>(sm + kPfImgK + pf_chunk(t, k8)) = c;
             }
         }
-    };
-    auto issue_s = [&]() {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // S = Q K^T (high and low parts of Q)
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem, umma_desc_sw128(sa + kPfQH + off), umma_desc_sw128(sa + kPfKT + off), idesc,
-                         kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem, umma_desc_sw128(sa + kPfQL + off), umma_desc_sw128(sa + kPfKT + off), idesc, 1u);
-            }
-            umma_commit(bar_s);
-        }
-    };
-    if (nblk > 0) {
-        stage_k();
-        issue_s();
-        pend = 1;
-        pend_par = 0;
-    }
-
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int64_t t0 = (int64_t)blk * kPfBlock;
-        const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
         // V tile: lanes take consecutive dim pairs (2 jp, 2 jp + 1) of the same
-        // rows; thread = (dim pair tid % 64, position groups (tid / 64) + 8 i of
-        // 8 positions); entry (c[idx(t, j)], c[idx(t + 1, j)])
+        // rows; thread = (dim pair tid % 64, groups (tid / 64) + 4 i of 8
+        // positions); entry (c[idx(t, j)], c[idx(t + 1, j)])
         {
             const int jp = tid & 63;
             constexpr uint32_t M = (1u << VB) - 1;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int t8 = (tid >> 6) + 8 * i;
+            for (int i = 0; i < 4; ++i) {
+                const int t8 = (tid >> 6) + 4 * i;
                 uint32_t f[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    f[u] = pf_bits<2 * VB>(reinterpret_cast<const uint32_t*>(sm + kPfSV + (8 * t8 + u) * 64),
+                    f[u] = pf_bits<2 * VB>(reinterpret_cast<const uint32_t*>(sm + kPxSV + (8 * t8 + u) * 64),
                                            2 * jp * VB);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
@@ -328,261 +203,584 @@ k_attn_prefill(const __half* __restrict__ q16, const float* __restrict__ qexp, i
                         const uint32_t bb = (f[2 * pp + 1] >> (jj * VB)) & M;
                         c[pp] = tvl[kPfCopies * (a | (bb << VB))];
                     }
-                    *reinterpret_cast<uint4*>(sm + kPfVT + pf_chunk(2 * jp + jj, t8)) =
+                    *reinterpret_cast<uint4*>(sm + kPfImgV + pf_chunk(2 * jp + jj, t8)) =
                         make_uint4(c[0], c[1], c[2], c[3]);
                 }
             }
         }
-        fence_proxy_async_smem();
-        // softmax: this thread's 32 columns of its row
-        if (!block_wait(bar_s, blk & 1)) {
-            if (tid == 0) report_timeout(status, kPfStatusWait);
-            bad = true;
-            break;
+        __syncthreads();
+        if (tid >= 128 && tid < 160) {  // the block's largest |V norm|
+            const float* vn = reinterpret_cast<const float*>(sm + kPfImgVN);
+            float v = fmaxf(fmaxf(fabsf(vn[lane]), fabsf(vn[lane + 32])), fmaxf(fabsf(vn[lane + 64]), fabsf(vn[lane + 96])));
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+            if (lane == 0) bmax[(int64_t)bg * nbmax + j] = v;
         }
-        pend = 0;
-        if (blk + 1 < nblk) {  // the staging area is free: fetch the next block during this one
-            const int64_t t1 = t0 + kPfBlock;
-            pf_stage<KB, VB>(sa, cache, crow0, t1, kv_end - t1 < kPfBlock ? (int)(kv_end - t1) : kPfBlock, tid);
-        }
-        tc_fence_after();
-        // s' = S * |k| per column; the row's scores in log2 units are s' * qx
-        // (qx > 0), so the running max is kept in s' units and
-        // p = exp2(s' qx - m qx).  Columns inside the row's range for the whole
-        // quarter skip the per-column mask.
-        float sv[32];
         {
-            uint32_t sr[32];
-            tmem_ld32(t_row, sr);
-            tmem_wait_ld();
-            const float4* kn4 = reinterpret_cast<const float4*>(kn_s + 32 * cq);
-            const bool full = rvalid && 32 * cq + 31 < nv && t0 + 32 * cq + 31 <= pos;
-            float mx = -INFINITY;
-            if (full) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 kk = kn4[j];
-                    f2_split(f2_mul(f2(__uint_as_float(sr[4 * j]), __uint_as_float(sr[4 * j + 1])), f2(kk.x, kk.y)),
-                             sv[4 * j], sv[4 * j + 1]);
-                    f2_split(f2_mul(f2(__uint_as_float(sr[4 * j + 2]), __uint_as_float(sr[4 * j + 3])), f2(kk.z, kk.w)),
-                             sv[4 * j + 2], sv[4 * j + 3]);
-                    mx = fmaxf(mx, fmaxf(fmaxf(sv[4 * j], sv[4 * j + 1]), fmaxf(sv[4 * j + 2], sv[4 * j + 3])));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int k = 32 * cq + i;
-                    const bool valid = rvalid && k < nv && t0 + k <= pos;
-                    sv[i] = valid ? __uint_as_float(sr[i]) * kn_s[k] : -INFINITY;
-                    mx = fmaxf(mx, sv[i]);
-                }
-            }
-            red[cq * 128 + r] = mx;
+            const uint4* src = reinterpret_cast<const uint4*>(sm);
+            uint4* dst = reinterpret_cast<uint4*>(img + ((int64_t)bg * nbmax + j) * kPfImgBytes);
+            for (int i = tid; i < (int)(kPfImgBytes / 16); i += kPxThreads) dst[i] = src[i];
         }
         __syncthreads();
-        const float m_new = fmaxf(m, fmaxf(fmaxf(red[r], red[128 + r]), fmaxf(red[256 + r], red[384 + r])));
-        const float qxs = rvalid ? qx : 1.f;
-        const float alpha = (m_new == -INFINITY || m == -INFINITY) ? 0.f : pf_exp2((m - m_new) * qxs);
-        const float nmq = m_new == -INFINITY ? 0.f : -m_new * qxs;  // masked columns: exp2(-inf) = 0
-        const F2 QX = f2(qxs, qxs), NMQ = f2(nmq, nmq);
-        F2 LB = f2(0.f, 0.f);
-        const float4* vn4 = reinterpret_cast<const float4*>(vn_s + 32 * cq);  // |v| / 2^E
-        uint32_t hi16[16], lo16[16];  // this quarter's 32 positions of P as fp16 pairs
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-            uint32_t* hi = hi16 + 4 * k8;
-            uint32_t* lo = lo16 + 4 * k8;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const float4 vv = vn4[2 * k8 + h2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int i = 8 * k8 + 4 * h2 + 2 * u;
-                    float a0, a1;
-                    f2_split(f2_fma(f2(sv[i], sv[i + 1]), QX, NMQ), a0, a1);
-                    const F2 pp = f2(pf_exp2(a0), pf_exp2(a1));
-                    LB = f2_add(LB, pp);
-                    float w0, w1;
-                    f2_split(f2_mul(pp, u == 0 ? f2(vv.x, vv.y) : f2(vv.z, vv.w)), w0, w1);
-                    const __half2 hh2 = __floats2half2_rn(w0, w1);
-                    const float2 hf = __half22float2(hh2);
-                    const __half2 ll2 = __floats2half2_rn(w0 - hf.x, w1 - hf.y);
-                    hi[2 * h2 + u] = *reinterpret_cast<const uint32_t*>(&hh2);
-                    lo[2 * h2 + u] = *reinterpret_cast<const uint32_t*>(&ll2);
-                }
-            }
-        }
-        // P to tensor memory, row r, columns 16 cq .. 16 cq + 15 of each part
-        {
-            const uint32_t t_p = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 16 * cq;
-            tmem_st16(t_p, hi16);
-            tmem_st16(t_p + 64, lo16);
-            tmem_wait_st();
-        }
-        float lb0, lb1;
-        f2_split(LB, lb0, lb1);
-        const float lb = lb0 + lb1;
-        lp = lp * alpha + lb;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // O_blk = P V (high and low parts of P), folded into the running output
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16_ts(tmem + 128, tmem + 256 + 8 * kk, umma_desc_sw128(sa + kPfVT + off), idesc,
-                            kk > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16_ts(tmem + 128, tmem + 320 + 8 * kk, umma_desc_sw128(sa + kPfVT + off), idesc, 1u);
-            }
-            umma_commit(bar_pv);
-        }
-        pend = 2;
-        pend_par = blk & 1;
-        if (blk + 1 < nblk) stage_k();  // K tile of the next block while PV runs
-        if (!block_wait(bar_pv, blk & 1)) {
-            if (tid == 0) report_timeout(status, kPfStatusWait);
-            bad = true;
-            break;
-        }
-        pend = 0;
-        tc_fence_after();
-        {
-            uint32_t o[32];
-            tmem_ld32(t_row + 128, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) O[i] = fmaf(O[i], alpha, __uint_as_float(o[i]));
-        }
-        m = m_new;
-        if (blk + 1 < nblk) {  // its barrier also ends this block: S, O_blk and red are free
-            issue_s();
-            pend = 1;
-            pend_par = (blk + 1) & 1;
-        } else {
-            tc_fence_before();
-            __syncthreads();
-        }
     }
+}
 
-    cp_async_wait_all();  // no copy of this thread is left in flight
-    if (bad && pend) mbar_wait(pend == 1 ? bar_s : bar_pv, pend_par);  // bounded: let MMAs in flight finish
-    // normalise (the row's sum over its four quarters) and rotate back,
-    // s . H (s2 . o) / sqrt(d): H over the 7 index bits of a row is the
-    // butterflies over bits 0-4 (a thread's quarter, in registers) and over
-    // bits 5 and 6 (between the four threads of the row, through shared
-    // memory laid out [quarter][element][row] so that a warp's accesses hit
-    // 32 banks).  The Q region holds the exchange buffer (64 KB).
-    red[cq * 128 + r] = lp;
-    __syncthreads();
+// ------------------------------------------------------------------ attention
+// The attention kernel does not depend on the bit widths: one copy, in the
+// unit of K width 4.
+#if TQ_UNIT_KB == 4
+
+// ---- attention kernel
+constexpr int kPfRows = 128;           // query rows per CTA
+constexpr int kPfThreads = 352;        // warp 0 K copies, warp 1 MMAs, warps 2-9 softmax, warp 10 V copies
+constexpr int kPfSoftmax = 256;
+constexpr uint32_t kPfQH = 0;          // Q high parts, 128 x 128 fp16 (the output exchange at the end)
+constexpr uint32_t kPfQL = 32768;      // Q low parts
+constexpr uint32_t kPfKS = 65536;      // two K stages: the K tile of a block (32 KB, 1024-aligned)
+constexpr uint32_t kPfVS = 131072;     // two V stages: V tile, K norms, V norms of a block
+constexpr uint32_t kPfVStage = kPfImgBytes - kPfImgV;    // 33792 bytes (1024-aligned)
+constexpr uint32_t kPfRed = kPfVS + 2 * kPfVStage;       // [2][2][128] floats: per-half row maxima
+constexpr uint32_t kPfBar = kPfRed + 2048;               // 17 mbarriers
+constexpr uint32_t kPfMisc = kPfBar + 144;               // tensor-memory base, abort flag
+constexpr uint32_t kPfQX = kPfMisc + 16;                 // the rows' power-of-two query scales (128 floats)
+constexpr uint32_t kPfEnd = kPfQX + 512;
+constexpr uint32_t kPfSmem = kPfEnd + 1024;              // plus alignment slack
+static_assert(kPfSmem <= 232448, "shared memory per CTA");
+constexpr int kPfStatusWait = 51;      // an MMA, copy or softmax wait gave up
+constexpr int kPfStatusRange = 52;     // q_start[b] + T exceeds the cache capacity, or q_start < 0
+constexpr float kPfRescale = 8.f;      // move the reference max when the row max grows by more (log2)
+
+__device__ __forceinline__ float pf_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Barrier among the softmax warps (named barrier 1).
+__device__ __forceinline__ void pf_softmax_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kPfSoftmax) : "memory");
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`.  Gives up at once
+// if the CTA's abort flag is set; a wait that runs out of time sets it and
+// the status word.  Returns false if it gave up.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, int parity, volatile int* abort_f, int* status) {
+    if (mbar_try_wait(bar, (uint32_t)parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, (uint32_t)parity)) {
+        if (*abort_f) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_f = 1;
+            report_timeout(status, kPfStatusWait);
+            return false;
+        }
+    }
+    return true;
+}
+
+// 2^e for -126 <= e <= 127, from the exponent field.
+__device__ __forceinline__ float pf_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// One warp rotates one query row for the tensor cores, as the decode
+// attention does: q~ = s2 . H (s . q) / sqrt(d) (s2 only with two-sided
+// signs) times the plan's query multiplier, over a power of two 2^e that
+// keeps it below 2^14, as fp16 high and low parts.  Lane l holds elements
+// 4 l .. 4 l + 3: the butterflies over index bits 0 and 1 are in registers,
+// those over bits 2-6 between lanes, in the order len = 1, 2, .., 64.  `raw`
+// is the lane's four bf16 elements; the parts go to row r of the swizzled Q
+// tiles (8 bytes per lane); returns 2^e.
+__device__ __forceinline__ float pf_rotate_row(uint2 raw, unsigned char* qh, unsigned char* ql, int r, int lane,
+                                               const AttnParams& P) {
+    float x[4];
     {
-        const float l = red[r] + red[128 + r] + red[256 + r] + red[384 + r];
-        const float sc = l > 0.f ? ldexpf(P.out_mul, E) / l : 0.f;
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = c.x;
+        x[3] = c.y;
+    }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float v = O[i] * sc;
-            O[i] = P.two_sided ? __uint_as_float(__float_as_uint(v) ^ P.sgn2[32 * cq + i]) : v;
+    for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(__float_as_uint(x[k]) ^ P.sgn[4 * lane + k]);
+    {
+        float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
+        x[0] = a0 + a2;
+        x[1] = a1 + a3;
+        x[2] = a0 - a2;
+        x[3] = a1 - a3;
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, x[k], m);
+            x[k] = upper ? o - x[k] : x[k] + o;  // (lo + hi, lo - hi)
         }
     }
-    fwht_reg<32>(O);
-    float* xs = reinterpret_cast<float*>(sm + kPfQH);
+    float a = 0.f;
 #pragma unroll
-    for (int bit = 1; bit <= 2; bit <<= 1) {  // quarter index bits: index bits 5 and 6
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xs[(cq * 32 + i) * 128 + r] = O[i];
-        __syncthreads();
-        const int pq = cq ^ bit;
-        const bool upper = (cq & bit) != 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float o = xs[(pq * 32 + i) * 128 + r];
-            O[i] = upper ? o - O[i] : O[i] + o;  // (lo + hi, lo - hi)
-        }
-        __syncthreads();
+    for (int k = 0; k < 4; ++k) {
+        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u)) * P.q_mul;
+        a = fmaxf(a, fabsf(x[k]));
     }
-    if (rvalid && !bad) {
-        float4* dst = reinterpret_cast<float4*>(out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128 + 32 * cq);
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+    int e = 0;
+    if (a > 0.f && a <= FLT_MAX) {
+        const int ex = (int)((__float_as_uint(a) >> 23) & 0xFFu) - 126;  // a in [2^(ex-1), 2^ex); subnormal: -126
+        e = min(100, max(-100, ex - 14));
+    }
+    const float inv = pf_pow2(-e);  // exact scaling by a power of two
+    uint32_t h[2], l[2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            const int j = 32 * cq + i;
-            float4 v;
-            v.x = __uint_as_float(__float_as_uint(O[i] * P.inv_sqrt_d) ^ P.sgn[j]);
-            v.y = __uint_as_float(__float_as_uint(O[i + 1] * P.inv_sqrt_d) ^ P.sgn[j + 1]);
-            v.z = __uint_as_float(__float_as_uint(O[i + 2] * P.inv_sqrt_d) ^ P.sgn[j + 2]);
-            v.w = __uint_as_float(__float_as_uint(O[i + 3] * P.inv_sqrt_d) ^ P.sgn[j + 3]);
-            dst[i / 4] = v;
+    for (int k = 0; k < 2; ++k) {
+        const float y0 = x[2 * k] * inv, y1 = x[2 * k + 1] * inv;
+        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
+        const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
+        h[k] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        l[k] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    }
+    const uint32_t off = pf_chunk(r, lane >> 1) + (lane & 1) * 8;
+    *reinterpret_cast<uint2*>(qh + off) = make_uint2(h[0], h[1]);
+    *reinterpret_cast<uint2*>(ql + off) = make_uint2(l[0], l[1]);
+    return pf_pow2(e);
+}
+
+// Tiles of a (sequence, KV head) are taken last first: with a causal mask the
+// last tiles read the most KV blocks, so the longest CTAs start first.
+__global__ void __launch_bounds__(kPfThreads, 1)
+k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restrict__ img, int nbmax, int Hq,
+               int Hkv, int T,
+               const int32_t* __restrict__ q_start, const float* __restrict__ bmax, int64_t cap,
+               float* __restrict__ out, int* status, const __grid_constant__ AttnParams P) {
+    extern __shared__ __align__(1024) unsigned char pf_raw[];
+    unsigned char* sm = pf_raw + ((1024u - (smem_addr(pf_raw) & 1023u)) & 1023u);
+    const uint32_t sa = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = Hq / Hkv, tpr = kPfRows / G;
+    const int bg = blockIdx.y, b = bg / Hkv, g = bg - b * Hkv;
+    const int mt = (int)(gridDim.x - 1 - blockIdx.x);
+    const int rows_total = T * G;
+    int64_t qs = __ldg(q_start + b);
+    const int last_tok = min(T, (mt + 1) * tpr) - 1;
+    if (qs < 0 || qs + T > cap) {  // nothing sensible to read: report and write zeros
+        if (tid == 0) report_timeout(status, kPfStatusRange);
+        qs = -1;
+    }
+    const int64_t kv_end = qs < 0 ? 0 : qs + last_tok + 1;  // positions this CTA reads
+    const int nblk = (int)((kv_end + kPfBlock - 1) / kPfBlock);
+    // Block j: K stage and V stage j % 2, tensor-memory buffer j % 3 (S, then
+    // P over it), output in columns 384-511.
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPfBar);
+    uint64_t* kfull = bars;         // [2] the K tile of the stage's block has landed
+    uint64_t* vfull = bars + 2;     // [2] its V tile and norms have landed
+    uint64_t* s_full = bars + 4;    // [3] S of the buffer's block is done (its K stage is free)
+    uint64_t* p_full = bars + 7;    // [3] the eight softmax warps wrote P over it
+    uint64_t* pv_done = bars + 10;  // [3] its PV product completed: buffer free, O current
+    uint64_t* vfree = bars + 13;    // [2] the PV product of the stage's block completed
+    uint64_t* q_full = bars + 15;   // the softmax warps rotated the query tile
+    uint64_t* drain = bars + 16;    // the MMA thread's products in flight, on the abort path
+    uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
+    volatile int* abort_f = reinterpret_cast<volatile int*>(sm + kPfMisc + 4);
+    float* red = reinterpret_cast<float*>(sm + kPfRed);
+    float* qx_s = reinterpret_cast<float*>(sm + kPfQX);
+
+    if (tid == 0) {
+        for (int i = 0; i < 17; ++i) mbar_init(&bars[i], ((i >= 7 && i < 10) || i == 15) ? 8u : 1u);
+        *abort_f = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc<512>(slot);  // S/P buffers at 0, 128, 256; O at 384
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    constexpr uint32_t idesc = umma_idesc_f16(128, 128, false);
+
+    if (warp == 0 || warp == 10) {
+        // ---- copies: warp 0 the K tile of block j into K stage j % 2 once S of
+        // block j - 2 is done, warp 10 the V tile and norms into V stage j % 2
+        // once the PV product of block j - 2 is
+        if (lane == 0) {
+            const bool kside = warp == 0;
+            uint64_t* fb = kside ? kfull : vfull;
+            int issued = 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j & 1;
+                if (j >= 2) {
+                    const int jo = j - 2;
+                    uint64_t* rel = kside ? &s_full[jo % 3] : &vfree[s];
+                    if (!pf_wait(rel, kside ? (jo / 3) & 1 : (jo >> 1) & 1, abort_f, status)) break;
+                }
+                const unsigned char* src = img + ((int64_t)bg * nbmax + j) * kPfImgBytes;
+                if (kside) {
+                    mbar_arrive_expect_tx(&kfull[s], 32768);
+                    bulk_load(sa + kPfKS + s * 32768, src + kPfImgK, 32768, &kfull[s]);
+                } else {
+                    mbar_arrive_expect_tx(&vfull[s], kPfVStage);
+                    bulk_load(sa + kPfVS + s * kPfVStage, src + kPfImgV, 32768, &vfull[s]);
+                    bulk_load(sa + kPfVS + s * kPfVStage + 32768, src + kPfImgKN, kPfImgBytes - kPfImgKN, &vfull[s]);
+                }
+                issued = j + 1;
+            }
+            // the copies issued have landed before the CTA leaves (bounded;
+            // regardless of the abort flag)
+            for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j) mbar_wait(&fb[j & 1], (j >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ---- MMAs: S of block j, then the PV product of block j - 1
+        if (lane == 0) {
+            bool ok = pf_wait(q_full, 0, abort_f, status);
+            int sb = 0, sph = 0;  // buffer and phase of the next S
+            int pb = 0, pph = 0;  // buffer and phase of the next PV product
+            for (int j = 0; ok && j <= nblk; ++j) {
+                if (j < nblk) {
+                    const int s = j & 1;
+                    // buffer sb last held P of block j - 3 (phase sph ^ 1)
+                    ok = pf_wait(&kfull[s], (j >> 1) & 1, abort_f, status) &&
+                         (j < 3 || pf_wait(&pv_done[sb], sph ^ 1, abort_f, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kt = sa + kPfKS + s * 32768;
+                    const uint32_t d = tmem + 128 * sb;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_f16(d, umma_desc_sw128(sa + kPfQH + off), umma_desc_sw128(kt + off), idesc,
+                                 kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_f16(d, umma_desc_sw128(sa + kPfQL + off), umma_desc_sw128(kt + off), idesc, 1u);
+                    }
+                    umma_commit(&s_full[sb]);
+                    if (++sb == 3) {
+                        sb = 0;
+                        sph ^= 1;
+                    }
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, s = jj & 1;
+                    ok = pf_wait(&vfull[s], (jj >> 1) & 1, abort_f, status) &&
+                         pf_wait(&p_full[pb], pph, abort_f, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vt = sa + kPfVS + s * kPfVStage;
+                    // P of positions 16 kk .. 16 kk + 15: high parts at column
+                    // 64 (kk / 4) + 8 (kk % 4) of the buffer, low parts 32 further
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t a = tmem + 128 * pb + 64 * (kk >> 2) + 8 * (kk & 3);
+                        umma_f16_ts(tmem + 384, a, umma_desc_sw128(vt + off), idesc, (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t a = tmem + 128 * pb + 64 * (kk >> 2) + 8 * (kk & 3) + 32;
+                        umma_f16_ts(tmem + 384, a, umma_desc_sw128(vt + off), idesc, 1u);
+                    }
+                    umma_commit(&pv_done[pb]);
+                    umma_commit(&vfree[s]);
+                    if (++pb == 3) {
+                        pb = 0;
+                        pph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // the products in flight finish before the tensor memory is freed (bounded)
+                umma_commit(drain);
+                mbar_wait(drain, 0);
+            }
+        }
+    } else {
+        // ---- softmax (warps 2-9): row r of the tile, columns 64 hf .. 64 hf + 63
+        const int qd = warp & 3, hf = (warp - 2) >> 2;
+        const int r = 32 * qd + lane;
+        const int grow = mt * kPfRows + r;  // the row within (b, g)
+        const bool rvalid = grow < rows_total;
+        const int tok = rvalid ? grow / G : 0, hh = rvalid ? grow - tok * G : 0;
+        // E: the largest V norm this CTA reads is below 2^E (from the blocks' maxima)
+        int E = 0;
+        {
+            float vm = 0.f;
+            for (int t = lane; t < nblk; t += 32) vm = fmaxf(vm, __ldg(bmax + (int64_t)bg * nbmax + t));
+            for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+            if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
+        }
+        // Q tile: warp w rotates rows 16 (w - 2) .. + 15 (zero rows past the
+        // chunk's last token), every row's load in flight before the first
+        // rotation; the tile goes to the tensor cores through q_full
+        {
+            uint2 raw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int gr = mt * kPfRows + 16 * (warp - 2) + i;
+                raw[i] = make_uint2(0u, 0u);
+                if (gr < rows_total) {
+                    const int tk = gr / G, hd = gr - tk * G;
+                    raw[i] = __ldg(reinterpret_cast<const uint2*>(q + (((int64_t)b * T + tk) * Hq + g * G + hd) * 128) +
+                                   lane);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int rr = 16 * (warp - 2) + i;
+                const float sc = pf_rotate_row(raw[i], sm + kPfQH, sm + kPfQL, rr, lane, P);
+                if (lane == 0) qx_s[rr] = mt * kPfRows + rr < rows_total ? sc : 0.f;
+            }
+        }
+        fence_proxy_async_smem();
+        pf_softmax_sync();
+        if (lane == 0) mbar_arrive(q_full);
+        const float qx = qx_s[r];
+
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
+        const int64_t pos = qs + tok;  // this row attends [0, pos]
+        const float qxs = rvalid ? qx : 1.f;
+        const float inv2E = ldexpf(1.f, -E);
+        const F2 QX = f2(qxs, qxs), IE = f2(inv2E, inv2E);
+        float m = -INFINITY, l = 0.f;  // reference max (s' units) and this half's sum
+        int bb = 0, bph = 0;           // tensor-memory buffer of block j and its phase
+        for (int j = 0; j < nblk; ++j) {
+            const int s = j & 1;
+            const int64_t t0 = (int64_t)j * kPfBlock;
+            const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
+            pf_wait(&vfull[s], (j >> 1) & 1, abort_f, status);  // the norms of the block
+            pf_wait(&s_full[bb], bph, abort_f, status);
+            __syncwarp();
+            tc_fence_after();
+            const unsigned char* stg = sm + kPfVS + s * kPfVStage - kPfImgV;  // image offsets
+            const float* kn = reinterpret_cast<const float*>(stg + kPfImgKN) + 64 * hf;
+            const float2* vn2 = reinterpret_cast<const float2*>(stg + kPfImgVN) + 32 * hf;
+            const uint32_t t_buf = t_lane + 128 * bb + 64 * hf;
+            // s' = S |k| per column; the row's scores in log2 units are s' qx
+            // (qx > 0), so the max is kept in s' units and p = exp2(s' qx - m qx).
+            // Columns inside the row's range for the whole half skip the mask.
+            float sv[64];
+            float mx = -INFINITY;
+            {
+                uint32_t sr0[32], sr1[32];
+                tmem_ld32(t_buf, sr0);
+                tmem_ld32(t_buf + 32, sr1);
+                tmem_wait_ld();
+                const bool whole = rvalid && 64 * hf + 63 < nv && t0 + 64 * hf + 63 <= pos;
+                if (whole) {
+                    const float4* kn4 = reinterpret_cast<const float4*>(kn);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 kk = kn4[i];
+                        const uint32_t* sr = i < 8 ? sr0 + 4 * i : sr1 + 4 * (i - 8);
+                        f2_split(f2_mul(f2(__uint_as_float(sr[0]), __uint_as_float(sr[1])), f2(kk.x, kk.y)),
+                                 sv[4 * i], sv[4 * i + 1]);
+                        f2_split(f2_mul(f2(__uint_as_float(sr[2]), __uint_as_float(sr[3])), f2(kk.z, kk.w)),
+                                 sv[4 * i + 2], sv[4 * i + 3]);
+                        mx = fmaxf(mx, fmaxf(fmaxf(sv[4 * i], sv[4 * i + 1]), fmaxf(sv[4 * i + 2], sv[4 * i + 3])));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int k = 64 * hf + i;
+                        const bool valid = rvalid && k < nv && t0 + k <= pos;
+                        const uint32_t raw = i < 32 ? sr0[i] : sr1[i - 32];
+                        sv[i] = valid ? __uint_as_float(raw) * kn[i] : -INFINITY;
+                        mx = fmaxf(mx, sv[i]);
+                    }
+                }
+            }
+            red[(s * 2 + hf) * 128 + r] = mx;
+            pf_softmax_sync();
+            const float m_new = fmaxf(m, fmaxf(red[(s * 2) * 128 + r], red[(s * 2 + 1) * 128 + r]));
+            // both threads of a row take the same decisions (same inputs)
+            const bool move = m == -INFINITY || (m_new - m) * qxs > kPfRescale;
+            const bool rescale = move && m != -INFINITY;  // O holds earlier blocks: scale it
+            if (__any_sync(0xFFFFFFFFu, rescale)) {
+                // the PV product of block j - 1 is the last one that wrote O
+                const int jp = j - 1;
+                pf_wait(&pv_done[jp % 3], (jp / 3) & 1, abort_f, status);
+                __syncwarp();
+                tc_fence_after();
+                const float alpha = rescale ? pf_exp2((m - m_new) * qxs) : 1.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_lane + 384 + 64 * hf + 32 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_lane + 384 + 64 * hf + 32 * c, o);
+                }
+                if (rescale) l *= alpha;
+            }
+            if (move) m = m_new;
+            const float nmq = m == -INFINITY ? 0.f : -m * qxs;  // masked columns: exp2(-inf) = 0
+            const F2 NMQ = f2(nmq, nmq);
+            F2 LB = f2(0.f, 0.f);
+            uint32_t hi[32], lo[32];  // P of positions 64 hf + 2 u, + 1 as fp16 pairs
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                float a0, a1;
+                f2_split(f2_fma(f2(sv[2 * u], sv[2 * u + 1]), QX, NMQ), a0, a1);
+                const F2 pp = f2(pf_exp2(a0), pf_exp2(a1));
+                LB = f2_add(LB, pp);
+                const float2 vv = vn2[u];
+                float w0, w1;
+                f2_split(f2_mul(pp, f2_mul(f2(vv.x, vv.y), IE)), w0, w1);
+                const __half2 hh2 = __floats2half2_rn(w0, w1);
+                const float2 hf2 = __half22float2(hh2);
+                const __half2 ll2 = __floats2half2_rn(w0 - hf2.x, w1 - hf2.y);
+                hi[u] = *reinterpret_cast<const uint32_t*>(&hh2);
+                lo[u] = *reinterpret_cast<const uint32_t*>(&ll2);
+            }
+            tmem_st32(t_buf, hi);
+            tmem_st32(t_buf + 32, lo);
+            tmem_wait_st();
+            {
+                float lb0, lb1;
+                f2_split(LB, lb0, lb1);
+                l += lb0 + lb1;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[bb]);
+            if (++bb == 3) {
+                bb = 0;
+                bph ^= 1;
+            }
+        }
+
+        // ---- epilogue: normalise (the row's sum over its two halves) and
+        // rotate back, s . H (s2 . o) / sqrt(d): H over the 7 index bits of a
+        // row is the butterflies over bits 0-5 (a thread's half, in
+        // registers) and over bit 6 (between the two threads of the row,
+        // through shared memory laid out [half][element / 4][row] in float4;
+        // the Q region, free once the last product is done).
+        float O[64];
+        if (nblk > 0) {
+            const int jl = nblk - 1;
+            pf_wait(&pv_done[jl % 3], (jl / 3) & 1, abort_f, status);
+            __syncwarp();
+            tc_fence_after();
+            uint32_t o0[32], o1[32];
+            tmem_ld32(t_lane + 384 + 64 * hf, o0);
+            tmem_ld32(t_lane + 384 + 64 * hf + 32, o1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                O[i] = __uint_as_float(o0[i]);
+                O[32 + i] = __uint_as_float(o1[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) O[i] = 0.f;
+        }
+        float* lsum = red + ((nblk & 1) * 2) * 128;  // the buffer block nblk - 1 did not use
+        lsum[hf * 128 + r] = l;
+        pf_softmax_sync();
+        const float lt = lsum[r] + lsum[128 + r];
+        const float sc = lt > 0.f ? ldexpf(P.out_mul, E) / lt * P.inv_sqrt_d : 0.f;
+        if (P.two_sided) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) O[i] = __uint_as_float(__float_as_uint(O[i]) ^ P.sgn2[64 * hf + i]);
+        }
+        fwht_reg2<64>(O);
+        float4* xs = reinterpret_cast<float4*>(sm + kPfQH);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xs[(hf * 16 + i) * 128 + r] = make_float4(O[4 * i], O[4 * i + 1], O[4 * i + 2], O[4 * i + 3]);
+        pf_softmax_sync();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 o = xs[((hf ^ 1) * 16 + i) * 128 + r];
+            const float oo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) O[4 * i + k] = hf ? oo[k] - O[4 * i + k] : O[4 * i + k] + oo[k];  // (lo + hi, lo - hi)
+        }
+        if (rvalid && *abort_f == 0) {
+            float4* dst = reinterpret_cast<float4*>(out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128 + 64 * hf);
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+                const int jd = 64 * hf + i;
+                float4 v;
+                v.x = __uint_as_float(__float_as_uint(O[i] * sc) ^ P.sgn[jd]);
+                v.y = __uint_as_float(__float_as_uint(O[i + 1] * sc) ^ P.sgn[jd + 1]);
+                v.z = __uint_as_float(__float_as_uint(O[i + 2] * sc) ^ P.sgn[jd + 2]);
+                v.w = __uint_as_float(__float_as_uint(O[i + 3] * sc) ^ P.sgn[jd + 3]);
+                dst[i / 4] = v;
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<512>(tmem);
     }
 }
 
-// Query rotation for the prefill: block (b, t, h) rotates q[b][t][h] into
-// row (t G + h % G) of (b, h / G) in the layout the prefill kernel reads.
-static __global__ void __launch_bounds__(128) k_prefill_q(const __nv_bfloat16* __restrict__ q,
-                                                          __half* __restrict__ q16, float* __restrict__ qexp,
-                                                          int T, int Hq, int Hkv,
-                                                          const __grid_constant__ AttnParams P) {
-    const int64_t i = blockIdx.x;  // (b T + t) Hq + h
-    const int h = (int)(i % Hq);
-    const int64_t bt = i / Hq;
-    const int t = (int)(bt % T);
-    const int64_t b = bt / T;
-    const int G = Hq / Hkv;
-    const int64_t row = (b * Hkv + h / G) * ((int64_t)T * G) + (int64_t)t * G + h % G;
-    rotate_q_row(q + i * 128, q16 + row * 256, qexp + row, P);
+#endif  // TQ_UNIT_KB == 4
+
+static cudaError_t set_smem_once(const void* fn, int bytes, int* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+    return e;
 }
 
 template <int KB, int VB>
-cudaError_t prefill_launch(const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
-                           const tq_cache_view& cache, float* out, void* ws, const AttnParams& P, cudaStream_t s) {
-    __half* q16 = static_cast<__half*>(ws);
-    float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * T * Hq * 512);
-    k_prefill_q<<<(unsigned)((int64_t)B * T * Hq), 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, T,
-                                                               Hq, Hkv, P);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    auto fn = k_attn_prefill<KB, VB>;
+cudaError_t prefill_expand(int B, int T, int Hkv, const int32_t* q_start, const tq_cache_view& cache,
+                           unsigned char* img, const AttnParams& P, cudaStream_t s) {
+    float* bmax = reinterpret_cast<float*>(img + attn_prefill_img_bytes(B, Hkv, cache.cap));
+    auto fn = k_prefill_expand<KB, VB>;
     static int attr_done[64] = {};
-    int dev = 0;
-    e = cudaGetDevice(&dev);
+    cudaError_t e = set_smem_once((const void*)fn, (int)kPxSmem, attr_done);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev] = 1;
-    }
-    const int G = Hq / Hkv;
-    const dim3 grid((unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows), (unsigned)(B * Hkv));
-    fn<<<grid, kPfThreads, kPfSmem, s>>>(q16, qexp, Hq, Hkv, T, q_start, cache, out, status_word(), P);
+    const int nbmax = (int)((cache.cap + kPfBlock - 1) / kPfBlock);
+    const int groups = B * Hkv;
+    int x = 608 / groups;  // about four CTAs per SM in all
+    x = x < 1 ? 1 : (x > nbmax ? nbmax : x);
+    fn<<<dim3((unsigned)x, (unsigned)groups), kPxThreads, kPxSmem, s>>>(q_start, T, Hkv, cache, nbmax, img, bmax, P);
     return cudaGetLastError();
 }
 
 }  // namespace dev
 
+#if TQ_UNIT_KB == 4
+cudaError_t launch_prefill_attention(const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
+                                     const tq_cache_view& cache, float* out, void* workspace,
+                                     const AttnParams& P, cudaStream_t s) {
+    using namespace dev;
+    const unsigned char* img = static_cast<const unsigned char*>(workspace);
+    static int attr_done[64] = {};
+    cudaError_t e = set_smem_once((const void*)k_attn_prefill, (int)kPfSmem, attr_done);
+    if (e != cudaSuccess) return e;
+    const int G = Hq / Hkv;
+    const int nbmax = (int)((cache.cap + kPfBlock - 1) / kPfBlock);
+    const dim3 grid((unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows), (unsigned)(B * Hkv));
+    const float* bmax = reinterpret_cast<const float*>(img + attn_prefill_img_bytes(B, Hkv, cache.cap));
+    k_attn_prefill<<<grid, kPfThreads, kPfSmem, s>>>(static_cast<const __nv_bfloat16*>(q), img, nbmax, Hq, Hkv, T,
+                                                     q_start, bmax, cache.cap, out, status_word(), P);
+    return cudaGetLastError();
+}
+#endif
+
 template <int KB>
 cudaError_t launch_attn_prefill(int v_bits, const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
                                 const tq_cache_view& cache, float* out, void* workspace, const AttnParams& P,
                                 cudaStream_t s) {
+    unsigned char* img = static_cast<unsigned char*>(workspace);
+    cudaError_t e;
     switch (v_bits) {
-        case 2: return dev::prefill_launch<KB, 2>(q, B, T, Hq, Hkv, q_start, cache, out, workspace, P, s);
-        case 3: return dev::prefill_launch<KB, 3>(q, B, T, Hq, Hkv, q_start, cache, out, workspace, P, s);
-        default: return dev::prefill_launch<KB, 4>(q, B, T, Hq, Hkv, q_start, cache, out, workspace, P, s);
+        case 2: e = dev::prefill_expand<KB, 2>(B, T, Hkv, q_start, cache, img, P, s); break;
+        case 3: e = dev::prefill_expand<KB, 3>(B, T, Hkv, q_start, cache, img, P, s); break;
+        default: e = dev::prefill_expand<KB, 4>(B, T, Hkv, q_start, cache, img, P, s); break;
     }
+    if (e != cudaSuccess) return e;
+    return launch_prefill_attention(q, B, T, Hq, Hkv, q_start, cache, out, workspace, P, s);
 }
 
-#if !defined(TQ_UNIT_KB)
-#error "compile once per K width with -DTQ_UNIT_KB=<bits>"
-#endif
 template cudaError_t launch_attn_prefill<TQ_UNIT_KB>(int, const void*, int, int, int, int, const int32_t*,
                                                      const tq_cache_view&, float*, void*, const AttnParams&,
                                                      cudaStream_t);
