@@ -169,15 +169,18 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
                                  const PagedArgs& pa, cudaStream_t s, const AttnAppend* app = nullptr);
 // Prefill (multi-query, causal) attention, d = 128 (tq_prefill.cu, one unit
-// per K width).  workspace: one expanded tile image of kPfImgBytes per block
-// of 128 cache positions per (sequence, KV head), then each block's largest
-// V norm (a float).
+// per K width).  workspace: the query rotation as a 128 x 128 bf16 matrix
+// (kPfRotBytes), one expanded tile image of kPfImgBytes per block of 128
+// cache positions per (sequence, KV head), then each block's largest V norm
+// (a float).
 constexpr size_t kPfImgBytes = 66560;
+constexpr size_t kPfRotBytes = 32768;
 inline size_t attn_prefill_img_bytes(int B, int Hkv, int64_t cap) {
     return (size_t)B * Hkv * (size_t)((cap + 127) / 128) * kPfImgBytes;
 }
 inline size_t attn_prefill_ws_bytes(int B, int Hkv, int64_t cap) {
-    return attn_prefill_img_bytes(B, Hkv, cap) + ((size_t)B * Hkv * (size_t)((cap + 127) / 128) * 4 + 15) / 16 * 16;
+    return kPfRotBytes + attn_prefill_img_bytes(B, Hkv, cap) +
+           ((size_t)B * Hkv * (size_t)((cap + 127) / 128) * 4 + 15) / 16 * 16;
 }
 template <int KB>
 cudaError_t launch_attn_prefill(int v_bits, const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,

@@ -17,29 +17,37 @@
 //     centroids [dim][position] as fp16, both in the 128-byte-swizzled
 //     K-major layout the tensor cores read, then the 128 K norms and the
 //     128 V norms (65 KB; norms past the sequence's last position are zero,
-//     centroids there c[0]).
+//     centroids there c[0]), and the block's largest V norm.  One block also
+//     writes the query rotation s2 . H . s as a bf16 matrix of +-1.
 //   k_attn_prefill  takes 128 query rows of one (sequence, KV head): 128 / G
 //     consecutive tokens times the G query heads of the group (row r = token
 //     r / G, head r % G), with warp roles:
-//       warp 0    streams the tile images into two stages (bulk copies);
-//       warp 1    issues S = Q_hi K^T + Q_lo K^T into one of two tensor-memory
-//                 buffers (the rotated query split into fp16 high and low
-//                 parts keeps about 22 significant bits) and, once the
-//                 softmax has written P over it, O += P_hi V + P_lo V (A read
-//                 from tensor memory);
-//       warps 2-9 two threads per query row, 64 columns each: scores times
-//                 the K norms and the query's power-of-two scale, the causal
-//                 mask, the row max merged through shared memory; P = exp2(s
-//                 - m) times the V norm over 2^E (E fixed per CTA from the
-//                 largest V norm it reads) as fp16 high and low parts,
-//                 stored over the thread's own S columns.
+//       warp 0    streams the K tile of block j into K stage j % 2 once S of
+//                 block j - 2 is done (bulk copies);
+//       warp 10   streams the V tile and norms into V stage j % 2 once the PV
+//                 product of block j - 2 is done;
+//       warp 1    issues the query rotation (bf16 rows times the +-1 matrix,
+//                 exact products, fp32 sums), then per block S = Q_hi K^T +
+//                 Q_lo K^T into tensor-memory buffer j % 3 (the rotated query
+//                 split into fp16 high and low parts keeps about 22
+//                 significant bits) and the PV product of block j - 1, O += P V
+//                 with P read from tensor memory;
+//       warps 2-9 two threads per query row, 64 columns each: the query tile
+//                 from the rotated rows, then per block the scores times the
+//                 K norms and the query's power-of-two scale, the causal mask,
+//                 the row max merged through shared memory, and P = exp2(s -
+//                 m) times the V norm over 2^E (E fixed per CTA from the
+//                 largest V norm it reads) as fp16 over the thread's own S
+//                 columns.
 //     The output accumulates in tensor memory.  The reference max m of a row
 //     moves only when a block raises the row max by more than 8 (log2 units),
-//     so P stays below 2^8; when it moves, the softmax threads rescale their
-//     output columns in tensor memory after the previous PV product is done.
-//     At the end the rows are divided by the denominator, scaled by 2^E / s_v
-//     and rotated back (s . H (s2 . o) / sqrt(d)): butterflies over a
-//     thread's 64 columns in registers, the last one through shared memory.
+//     so P stays below 2^8 (fp16: relative rounding at most 2^-12 per
+//     weight; the denominator sums the fp32 weights).  When it moves, the
+//     softmax threads rescale their output columns in tensor memory after the
+//     previous PV product is done.  At the end the rows are divided by the
+//     denominator, scaled by 2^E / s_v and rotated back (s . H (s2 . o) /
+//     sqrt(d)): butterflies over a thread's 64 columns in registers, the last
+//     one through shared memory.
 //
 // Every wait on an mbarrier is bounded (2 s); a wait that gives up sets the
 // device status word and a flag that ends every other wait of the CTA, the
@@ -104,17 +112,42 @@ __device__ __forceinline__ uint32_t pf_pack_half2(float a, float b) {
 
 // Block (x, bg) expands blocks x, x + gridDim.x, .. of (sequence, KV head) bg
 // into img + (bg nbmax + j) kPfImgBytes, and the block's largest |V norm|
-// into bmax[bg nbmax + j].  Blocks at or past the sequence's last position
+// into bmax[bg nbmax + j]; block (0, 0) also writes the query rotation matrix.  Blocks at or past the sequence's last position
 // q_start[b] + T are not read; a sequence whose range is invalid is skipped
 // (the attention kernel reports it).
 template <int KB, int VB>
 __global__ void __launch_bounds__(kPxThreads, 2)
 k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_view cache, int nbmax,
-                 unsigned char* __restrict__ img, float* __restrict__ bmax, const __grid_constant__ AttnParams P) {
+                 unsigned char* __restrict__ img, float* __restrict__ bmax, uint4* __restrict__ rot,
+                 const __grid_constant__ AttnParams P) {
     extern __shared__ __align__(16) unsigned char px_raw[];
     unsigned char* sm = px_raw;
     const int tid = threadIdx.x, lane = tid & 31;
     const int bg = blockIdx.y, b = bg / Hkv;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        // the query rotation as a bf16 matrix R[j][i] = s2_j H_ji s_i (entries
+        // +-1, H_ji = (-1)^popcount(i & j)), rows j in the 128-byte-swizzled
+        // K-major layout: 16-byte chunk c holds row j = (c / 8) % 128, elements
+        // 64 (c / 1024) + 8 ((c % 8) ^ (j % 8)) + 0 .. 7
+        for (int c = tid; c < 2048; c += kPxThreads) {
+            const int j = (c >> 3) & 127;
+            const int i0 = 64 * (c >> 10) + 8 * ((c & 7) ^ (j & 7));
+            const uint32_t s2 = P.two_sided ? P.sgn2[j] : 0u;
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t h2 = 0;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = i0 + 2 * k + u;
+                    const uint32_t sg = ((P.sgn[i] ^ s2) >> 16) ^ ((__popc(i & j) & 1) ? 0x8000u : 0u);
+                    h2 |= (0x3F80u | (sg & 0x8000u)) << (16 * u);
+                }
+                w[k] = h2;
+            }
+            rot[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
     const int64_t qs = __ldg(q_start + b);
     if (qs < 0 || qs + T > cache.cap) return;
     const int64_t kv_end = qs + T;
@@ -239,8 +272,8 @@ constexpr uint32_t kPfKS = 65536;      // two K stages: the K tile of a block (3
 constexpr uint32_t kPfVS = 131072;     // two V stages: V tile, K norms, V norms of a block
 constexpr uint32_t kPfVStage = kPfImgBytes - kPfImgV;    // 33792 bytes (1024-aligned)
 constexpr uint32_t kPfRed = kPfVS + 2 * kPfVStage;       // [2][2][128] floats: per-half row maxima
-constexpr uint32_t kPfBar = kPfRed + 2048;               // 17 mbarriers
-constexpr uint32_t kPfMisc = kPfBar + 144;               // tensor-memory base, abort flag
+constexpr uint32_t kPfBar = kPfRed + 2048;               // 19 mbarriers
+constexpr uint32_t kPfMisc = kPfBar + 160;               // tensor-memory base, abort flag
 constexpr uint32_t kPfQX = kPfMisc + 16;                 // the rows' power-of-two query scales (128 floats)
 constexpr uint32_t kPfEnd = kPfQX + 512;
 constexpr uint32_t kPfSmem = kPfEnd + 1024;              // plus alignment slack
@@ -280,76 +313,11 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, int parity, volatile int*
 // 2^e for -126 <= e <= 127, from the exponent field.
 __device__ __forceinline__ float pf_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// One warp rotates one query row for the tensor cores, as the decode
-// attention does: q~ = s2 . H (s . q) / sqrt(d) (s2 only with two-sided
-// signs) times the plan's query multiplier, over a power of two 2^e that
-// keeps it below 2^14, as fp16 high and low parts.  Lane l holds elements
-// 4 l .. 4 l + 3: the butterflies over index bits 0 and 1 are in registers,
-// those over bits 2-6 between lanes, in the order len = 1, 2, .., 64.  `raw`
-// is the lane's four bf16 elements; the parts go to row r of the swizzled Q
-// tiles (8 bytes per lane); returns 2^e.
-__device__ __forceinline__ float pf_rotate_row(uint2 raw, unsigned char* qh, unsigned char* ql, int r, int lane,
-                                               const AttnParams& P) {
-    float x[4];
-    {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        x[0] = a.x;
-        x[1] = a.y;
-        x[2] = c.x;
-        x[3] = c.y;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(__float_as_uint(x[k]) ^ P.sgn[4 * lane + k]);
-    {
-        float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
-        x[0] = a0 + a2;
-        x[1] = a1 + a3;
-        x[2] = a0 - a2;
-        x[3] = a1 - a3;
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float o = __shfl_xor_sync(0xFFFFFFFFu, x[k], m);
-            x[k] = upper ? o - x[k] : x[k] + o;  // (lo + hi, lo - hi)
-        }
-    }
-    float a = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u)) * P.q_mul;
-        a = fmaxf(a, fabsf(x[k]));
-    }
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-    int e = 0;
-    if (a > 0.f && a <= FLT_MAX) {
-        const int ex = (int)((__float_as_uint(a) >> 23) & 0xFFu) - 126;  // a in [2^(ex-1), 2^ex); subnormal: -126
-        e = min(100, max(-100, ex - 14));
-    }
-    const float inv = pf_pow2(-e);  // exact scaling by a power of two
-    uint32_t h[2], l[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float y0 = x[2 * k] * inv, y1 = x[2 * k + 1] * inv;
-        const __half h0 = __float2half_rn(y0), h1 = __float2half_rn(y1);
-        const __half l0 = __float2half_rn(y0 - __half2float(h0)), l1 = __float2half_rn(y1 - __half2float(h1));
-        h[k] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-        l[k] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
-    }
-    const uint32_t off = pf_chunk(r, lane >> 1) + (lane & 1) * 8;
-    *reinterpret_cast<uint2*>(qh + off) = make_uint2(h[0], h[1]);
-    *reinterpret_cast<uint2*>(ql + off) = make_uint2(l[0], l[1]);
-    return pf_pow2(e);
-}
-
 // Tiles of a (sequence, KV head) are taken last first: with a causal mask the
 // last tiles read the most KV blocks, so the longest CTAs start first.
 __global__ void __launch_bounds__(kPfThreads, 1)
-k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restrict__ img, int nbmax, int Hq,
-               int Hkv, int T,
+k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restrict__ rot,
+               const unsigned char* __restrict__ img, int nbmax, int Hq, int Hkv, int T,
                const int32_t* __restrict__ q_start, const float* __restrict__ bmax, int64_t cap,
                float* __restrict__ out, int* status, const __grid_constant__ AttnParams P) {
     extern __shared__ __align__(1024) unsigned char pf_raw[];
@@ -377,15 +345,17 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
     uint64_t* p_full = bars + 7;    // [3] the eight softmax warps wrote P over it
     uint64_t* pv_done = bars + 10;  // [3] its PV product completed: buffer free, O current
     uint64_t* vfree = bars + 13;    // [2] the PV product of the stage's block completed
-    uint64_t* q_full = bars + 15;   // the softmax warps rotated the query tile
+    uint64_t* q_full = bars + 15;   // the softmax warps wrote the query tile (fp16 high and low parts)
     uint64_t* drain = bars + 16;    // the MMA thread's products in flight, on the abort path
+    uint64_t* q_in = bars + 17;     // the bf16 query rows and the rotation matrix are in shared memory
+    uint64_t* rot_done = bars + 18; // the rotated rows are in tensor memory (columns 384-511)
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
     volatile int* abort_f = reinterpret_cast<volatile int*>(sm + kPfMisc + 4);
     float* red = reinterpret_cast<float*>(sm + kPfRed);
     float* qx_s = reinterpret_cast<float*>(sm + kPfQX);
 
     if (tid == 0) {
-        for (int i = 0; i < 17; ++i) mbar_init(&bars[i], ((i >= 7 && i < 10) || i == 15) ? 8u : 1u);
+        for (int i = 0; i < 19; ++i) mbar_init(&bars[i], ((i >= 7 && i < 10) || i == 15) ? 8u : (i == 17 ? 9u : 1u));
         *abort_f = 0;
         mbar_fence_init();
     }
@@ -403,6 +373,10 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
         if (lane == 0) {
             const bool kside = warp == 0;
             uint64_t* fb = kside ? kfull : vfull;
+            if (kside) {  // the rotation matrix, B operand of the query rotation
+                mbar_arrive_expect_tx(q_in, 32768);
+                bulk_load(sa + kPfQL, rot, 32768, q_in);
+            }
             int issued = 0;
             for (int j = 0; j < nblk; ++j) {
                 const int s = j & 1;
@@ -425,11 +399,25 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             // the copies issued have landed before the CTA leaves (bounded;
             // regardless of the abort flag)
             for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j) mbar_wait(&fb[j & 1], (j >> 1) & 1);
+            if (kside) mbar_wait(q_in, 0);
         }
     } else if (warp == 1) {
         // ---- MMAs: S of block j, then the PV product of block j - 1
         if (lane == 0) {
-            bool ok = pf_wait(q_full, 0, abort_f, status);
+            // the query rotation: rows (bf16, A) times the rotation matrix (B)
+            bool ok = pf_wait(q_in, 0, abort_f, status);
+            if (ok) {
+                tc_fence_after();
+                constexpr uint32_t idesc_bf = umma_idesc_f16(128, 128, true);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_f16(tmem + 384, umma_desc_sw128(sa + kPfQH + off), umma_desc_sw128(sa + kPfQL + off),
+                             idesc_bf, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(rot_done);
+                ok = pf_wait(q_full, 0, abort_f, status);
+            }
             int sb = 0, sph = 0;  // buffer and phase of the next S
             int pb = 0, pph = 0;  // buffer and phase of the next PV product
             for (int j = 0; ok && j <= nblk; ++j) {
@@ -466,19 +454,13 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vt = sa + kPfVS + s * kPfVStage;
-                    // P of positions 16 kk .. 16 kk + 15: high parts at column
-                    // 64 (kk / 4) + 8 (kk % 4) of the buffer, low parts 32 further
+                    // P of positions 16 kk .. 16 kk + 15 at column 64 (kk / 4) + 8 (kk % 4)
+                    // of the buffer
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                         const uint32_t a = tmem + 128 * pb + 64 * (kk >> 2) + 8 * (kk & 3);
                         umma_f16_ts(tmem + 384, a, umma_desc_sw128(vt + off), idesc, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t a = tmem + 128 * pb + 64 * (kk >> 2) + 8 * (kk & 3) + 32;
-                        umma_f16_ts(tmem + 384, a, umma_desc_sw128(vt + off), idesc, 1u);
                     }
                     umma_commit(&pv_done[pb]);
                     umma_commit(&vfree[s]);
@@ -508,9 +490,11 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
             if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
         }
-        // Q tile: warp w rotates rows 16 (w - 2) .. + 15 (zero rows past the
-        // chunk's last token), every row's load in flight before the first
-        // rotation; the tile goes to the tensor cores through q_full
+        // Q tile: warp w stages rows 16 (w - 2) .. + 15 as bf16 (zero rows past
+        // the chunk's last token) for the rotation product; from the rotated
+        // rows each thread then writes its 64 columns as fp16 high and low parts
+        // over a power of two 2^e per row that keeps them below 2^14, and the
+        // tile goes to the tensor cores through q_full
         {
             uint2 raw[16];
 #pragma unroll
@@ -524,11 +508,56 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int rr = 16 * (warp - 2) + i;
-                const float sc = pf_rotate_row(raw[i], sm + kPfQH, sm + kPfQL, rr, lane, P);
-                if (lane == 0) qx_s[rr] = mt * kPfRows + rr < rows_total ? sc : 0.f;
+            for (int i = 0; i < 16; ++i)
+                *reinterpret_cast<uint2*>(sm + kPfQH + pf_chunk(16 * (warp - 2) + i, lane >> 1) + (lane & 1) * 8) =
+                    raw[i];
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_in);
+        {
+            const uint32_t t_q = tmem + ((uint32_t)(32 * qd) << 16) + 384 + 64 * hf;
+            pf_wait(rot_done, 0, abort_f, status);
+            __syncwarp();
+            tc_fence_after();
+            uint32_t y0[32], y1[32];
+            tmem_ld32(t_q, y0);
+            tmem_ld32(t_q + 32, y1);
+            tmem_wait_ld();
+            float y[64];
+            float a = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                y[i] = __uint_as_float(y0[i]) * P.q_mul;
+                y[32 + i] = __uint_as_float(y1[i]) * P.q_mul;
+                a = fmaxf(a, fmaxf(fabsf(y[i]), fabsf(y[32 + i])));
             }
+            red[hf * 128 + r] = a;
+            pf_softmax_sync();  // every thread's rows are read, and the product is done: the Q region is free
+            a = fmaxf(red[r], red[128 + r]);
+            int e = 0;
+            if (a > 0.f && a <= FLT_MAX) {
+                const int ex = (int)((__float_as_uint(a) >> 23) & 0xFFu) - 126;  // a in [2^(ex-1), 2^ex)
+                e = min(100, max(-100, ex - 14));
+            }
+            const float inv = pf_pow2(-e);  // exact scaling by a power of two
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float v0 = y[8 * c + 2 * k] * inv, v1 = y[8 * c + 2 * k + 1] * inv;
+                    const __half2 hh2 = __floats2half2_rn(v0, v1);
+                    const float2 hf2 = __half22float2(hh2);
+                    const __half2 ll2 = __floats2half2_rn(v0 - hf2.x, v1 - hf2.y);
+                    h[k] = *reinterpret_cast<const uint32_t*>(&hh2);
+                    l[k] = *reinterpret_cast<const uint32_t*>(&ll2);
+                }
+                const uint32_t off = pf_chunk(r, 8 * hf + c);
+                *reinterpret_cast<uint4*>(sm + kPfQH + off) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(sm + kPfQL + off) = make_uint4(l[0], l[1], l[2], l[3]);
+            }
+            if (hf == 0) qx_s[r] = rvalid ? pf_pow2(e) : 0.f;
         }
         fence_proxy_async_smem();
         pf_softmax_sync();
@@ -616,7 +645,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             const float nmq = m == -INFINITY ? 0.f : -m * qxs;  // masked columns: exp2(-inf) = 0
             const F2 NMQ = f2(nmq, nmq);
             F2 LB = f2(0.f, 0.f);
-            uint32_t hi[32], lo[32];  // P of positions 64 hf + 2 u, + 1 as fp16 pairs
+            uint32_t ph[32];  // P of positions 64 hf + 2 u, + 1 as fp16 pairs
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 float a0, a1;
@@ -627,13 +656,9 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                 float w0, w1;
                 f2_split(f2_mul(pp, f2_mul(f2(vv.x, vv.y), IE)), w0, w1);
                 const __half2 hh2 = __floats2half2_rn(w0, w1);
-                const float2 hf2 = __half22float2(hh2);
-                const __half2 ll2 = __floats2half2_rn(w0 - hf2.x, w1 - hf2.y);
-                hi[u] = *reinterpret_cast<const uint32_t*>(&hh2);
-                lo[u] = *reinterpret_cast<const uint32_t*>(&ll2);
+                ph[u] = *reinterpret_cast<const uint32_t*>(&hh2);
             }
-            tmem_st32(t_buf, hi);
-            tmem_st32(t_buf + 32, lo);
+            tmem_st32(t_buf, ph);
             tmem_wait_st();
             {
                 float lb0, lb1;
@@ -731,7 +756,8 @@ static cudaError_t set_smem_once(const void* fn, int bytes, int* done) {
 
 template <int KB, int VB>
 cudaError_t prefill_expand(int B, int T, int Hkv, const int32_t* q_start, const tq_cache_view& cache,
-                           unsigned char* img, const AttnParams& P, cudaStream_t s) {
+                           unsigned char* ws, const AttnParams& P, cudaStream_t s) {
+    unsigned char* img = ws + kPfRotBytes;
     float* bmax = reinterpret_cast<float*>(img + attn_prefill_img_bytes(B, Hkv, cache.cap));
     auto fn = k_prefill_expand<KB, VB>;
     static int attr_done[64] = {};
@@ -741,7 +767,8 @@ cudaError_t prefill_expand(int B, int T, int Hkv, const int32_t* q_start, const 
     const int groups = B * Hkv;
     int x = 608 / groups;  // about four CTAs per SM in all
     x = x < 1 ? 1 : (x > nbmax ? nbmax : x);
-    fn<<<dim3((unsigned)x, (unsigned)groups), kPxThreads, kPxSmem, s>>>(q_start, T, Hkv, cache, nbmax, img, bmax, P);
+    fn<<<dim3((unsigned)x, (unsigned)groups), kPxThreads, kPxSmem, s>>>(q_start, T, Hkv, cache, nbmax, img, bmax,
+                                                                          reinterpret_cast<uint4*>(ws), P);
     return cudaGetLastError();
 }
 
@@ -752,7 +779,8 @@ cudaError_t launch_prefill_attention(const void* q, int B, int T, int Hq, int Hk
                                      const tq_cache_view& cache, float* out, void* workspace,
                                      const AttnParams& P, cudaStream_t s) {
     using namespace dev;
-    const unsigned char* img = static_cast<const unsigned char*>(workspace);
+    const unsigned char* rot = static_cast<const unsigned char*>(workspace);
+    const unsigned char* img = rot + kPfRotBytes;
     static int attr_done[64] = {};
     cudaError_t e = set_smem_once((const void*)k_attn_prefill, (int)kPfSmem, attr_done);
     if (e != cudaSuccess) return e;
@@ -760,8 +788,8 @@ cudaError_t launch_prefill_attention(const void* q, int B, int T, int Hq, int Hk
     const int nbmax = (int)((cache.cap + kPfBlock - 1) / kPfBlock);
     const dim3 grid((unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows), (unsigned)(B * Hkv));
     const float* bmax = reinterpret_cast<const float*>(img + attn_prefill_img_bytes(B, Hkv, cache.cap));
-    k_attn_prefill<<<grid, kPfThreads, kPfSmem, s>>>(static_cast<const __nv_bfloat16*>(q), img, nbmax, Hq, Hkv, T,
-                                                     q_start, bmax, cache.cap, out, status_word(), P);
+    k_attn_prefill<<<grid, kPfThreads, kPfSmem, s>>>(static_cast<const __nv_bfloat16*>(q), rot, img, nbmax, Hq, Hkv,
+                                                     T, q_start, bmax, cache.cap, out, status_word(), P);
     return cudaGetLastError();
 }
 #endif
@@ -770,12 +798,12 @@ template <int KB>
 cudaError_t launch_attn_prefill(int v_bits, const void* q, int B, int T, int Hq, int Hkv, const int32_t* q_start,
                                 const tq_cache_view& cache, float* out, void* workspace, const AttnParams& P,
                                 cudaStream_t s) {
-    unsigned char* img = static_cast<unsigned char*>(workspace);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
     cudaError_t e;
     switch (v_bits) {
-        case 2: e = dev::prefill_expand<KB, 2>(B, T, Hkv, q_start, cache, img, P, s); break;
-        case 3: e = dev::prefill_expand<KB, 3>(B, T, Hkv, q_start, cache, img, P, s); break;
-        default: e = dev::prefill_expand<KB, 4>(B, T, Hkv, q_start, cache, img, P, s); break;
+        case 2: e = dev::prefill_expand<KB, 2>(B, T, Hkv, q_start, cache, ws, P, s); break;
+        case 3: e = dev::prefill_expand<KB, 3>(B, T, Hkv, q_start, cache, ws, P, s); break;
+        default: e = dev::prefill_expand<KB, 4>(B, T, Hkv, q_start, cache, ws, P, s); break;
     }
     if (e != cudaSuccess) return e;
     return launch_prefill_attention(q, B, T, Hq, Hkv, q_start, cache, out, workspace, P, s);
