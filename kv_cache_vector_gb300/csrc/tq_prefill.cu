@@ -61,6 +61,7 @@
 #include "tq_async.cuh"
 #include "tq_device.cuh"
 #include "tq_umma.cuh"
+#include "tq_tmem.cuh"
 
 #if !defined(TQ_UNIT_KB)
 #error "compile once per K width with -DTQ_UNIT_KB=<bits>"
