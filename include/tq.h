@@ -319,7 +319,8 @@ size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int Hkv, int64_t ca
  *   workspace: tq_attn_prefill_workspace_bytes(B, T, Hq, Hkv, cache.cap, 128)
  *     bytes; the prefix of every sequence is expanded there once into fp16
  *     centroid tiles, then read by every query tile of its KV head.
- * Errors: TQ_ERR_UNSUPPORTED (d, group size, bits), TQ_ERR_RANGE (cap < T),
+ * Errors: TQ_ERR_UNSUPPORTED (d, group size, bits; B * Hkv > 65535 or
+ * T * Hq / Hkv > 65535 * 128), TQ_ERR_RANGE (cap < T),
  * TQ_ERR_INVALID_ARG, TQ_ERR_ALIGNMENT, TQ_ERR_WORKSPACE. */
 tq_status tq_attn_prefill(const tq_plan *plan, const void *q, int B, int T, int Hq, int Hkv,
                           tq_cache_view cache, const int32_t *q_start, int k_bits, int v_bits,

@@ -661,7 +661,9 @@ tq_status tq_attn_prefill(const tq_plan* plan, const void* q, int B, int T, int 
     if (!std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
     if (cache.cap < T) return TQ_ERR_RANGE;
     if (B == 0) return TQ_OK;
-    if ((int64_t)B * Hkv > 65535 || (int64_t)B * T * Hq > INT32_MAX) return TQ_ERR_UNSUPPORTED;
+    // grid limits: (sequence, KV head) pairs and 128-row query tiles per pair
+    if ((int64_t)B * Hkv > 65535 || (int64_t)B * T * Hq > INT32_MAX || (int64_t)T * G > 65535LL * 128)
+        return TQ_ERR_UNSUPPORTED;
     if (!q || !out || !q_start || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
         return TQ_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned16(cache.k_packed) ||

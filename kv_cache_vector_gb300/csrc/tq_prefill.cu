@@ -80,11 +80,13 @@ static_assert(kPfImgVN + 512 == kPfImgBytes, "tile image layout");
 
 // ---- expansion kernel
 constexpr int kPxThreads = 256;
-constexpr uint32_t kPxSK = kPfImgBytes;      // staged packed K rows, 64-byte stride
-constexpr uint32_t kPxSV = kPxSK + 8192;     // staged packed V rows
-constexpr uint32_t kPxTK = kPxSV + 8192;     // K pair table, 4 copies (up to 256 x 4 words)
+constexpr uint32_t kPxStage = kPfImgBytes;   // two stages of packed rows: K (8 KB) then V (8 KB)
+constexpr uint32_t kPxStageBytes = 16384;
+constexpr uint32_t kPxTK = kPxStage + 2 * kPxStageBytes;  // K pair table, 4 copies (up to 256 x 4 words)
 constexpr uint32_t kPxTV = kPxTK + 4096;     // V pair table, 4 copies
-constexpr uint32_t kPxSmem = kPxTV + 4096;
+constexpr uint32_t kPxBar = kPxTV + 4096;    // two mbarriers, a flag
+constexpr uint32_t kPxSmem = kPxBar + 32;
+constexpr int kPxStatusWait = 53;            // a staging wait of the expansion gave up
 constexpr int kPfCopies = 4;                 // table copies: lane l reads copy l % 4 (fewer bank conflicts)
 
 // Offset of the 16-byte chunk holding elements [8 k8, 8 k8 + 8) of `row` in a
@@ -111,21 +113,35 @@ __device__ __forceinline__ uint32_t pf_pack_half2(float a, float b) {
 
 // ------------------------------------------------------------------ expansion
 
-// Block (x, bg) expands blocks x, x + gridDim.x, .. of (sequence, KV head) bg
-// into img + (bg nbmax + j) kPfImgBytes, and the block's largest |V norm|
-// into bmax[bg nbmax + j]; block (0, 0) also writes the query rotation matrix.  Blocks at or past the sequence's last position
-// q_start[b] + T are not read; a sequence whose range is invalid is skipped
-// (the attention kernel reports it).
+// 1-D bulk copy of `bytes` bytes from shared address `src` to global memory
+// (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
+__device__ __forceinline__ void px_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// Block (x, bg), x < gridDim.x - 1, expands blocks x, x + gridDim.x - 1, ..
+// of (sequence, KV head) bg into img + (bg nbmax + j) kPfImgBytes, and the
+// block's largest |V norm| into bmax[bg nbmax + j]; block (gridDim.x - 1, 0)
+// writes the query rotation matrix.
+// Blocks at or past the sequence's last position q_start[b] + T are not
+// read; a sequence whose range is invalid is skipped (the attention kernel
+// reports it).  Thread 0 fetches the packed rows of the next block (one bulk
+// copy per side, rows below the capacity only) while the block builds the
+// current image, and sends each image out with one bulk store.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kPxThreads, 2)
 k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_view cache, int nbmax,
                  unsigned char* __restrict__ img, float* __restrict__ bmax, uint4* __restrict__ rot,
-                 const __grid_constant__ AttnParams P) {
+                 int* status, const __grid_constant__ AttnParams P) {
     extern __shared__ __align__(16) unsigned char px_raw[];
     unsigned char* sm = px_raw;
+    const uint32_t sa = smem_addr(sm);
     const int tid = threadIdx.x, lane = tid & 31;
     const int bg = blockIdx.y, b = bg / Hkv;
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
+    const int nx = gridDim.x - 1;  // blocks per (sequence, KV head); the last column has one job
+    if ((int)blockIdx.x == nx) {
+        if (blockIdx.y != 0) return;
         // the query rotation as a bf16 matrix R[j][i] = s2_j H_ji s_i (entries
         // +-1, H_ji = (-1)^popcount(i & j)), rows j in the 128-byte-swizzled
         // K-major layout: 16-byte chunk c holds row j = (c / 8) % 128, elements
@@ -148,6 +164,7 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
             }
             rot[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        return;
     }
     const int64_t qs = __ldg(q_start + b);
     if (qs < 0 || qs + T > cache.cap) return;
@@ -157,6 +174,8 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
     const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
     uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPxTK);
     uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPxTV);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPxBar);  // [2] the stage's rows have landed
+    volatile int* okf = reinterpret_cast<volatile int*>(sm + kPxBar + 16);
     // pair tables: entry e = (c[e % 2^b], c[e / 2^b]) as two fp16 halves, copy
     // c of entry e at word 4 e + c
     for (int i = tid; i < (kPfCopies << (2 * KB)); i += kPxThreads) {
@@ -169,43 +188,68 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
     }
     const uint32_t* tkl = tk + (lane & (kPfCopies - 1));  // this lane's copy
     const uint32_t* tvl = tv + (lane & (kPfCopies - 1));
+    // rows of block j that exist in the cache (at least the n of the sequence)
+    auto rows_of = [&](int j) {
+        const int64_t t0 = (int64_t)j * kPfBlock;
+        return cache.cap - t0 < kPfBlock ? (int)(cache.cap - t0) : kPfBlock;
+    };
+    auto stage = [&](int j, int s) {  // thread 0: the packed rows of block j into stage s
+        const int64_t t0 = (int64_t)j * kPfBlock;
+        const uint32_t nr = (uint32_t)rows_of(j);
+        const uint32_t dst = sa + kPxStage + s * kPxStageBytes;
+        mbar_arrive_expect_tx(&bars[s], nr * 16 * (KB + VB));
+        bulk_load(dst, cache.k_packed + (crow0 + t0) * (16 * KB), nr * 16 * KB, &bars[s]);
+        bulk_load(dst + 8192, cache.v_packed + (crow0 + t0) * (16 * VB), nr * 16 * VB, &bars[s]);
+    };
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_fence_init();
+        *okf = 1;
+        stage(blockIdx.x, 0);
+    }
+    __syncthreads();
 
-    for (int j = blockIdx.x; j < nb; j += gridDim.x) {
+    int k = 0, pre = 0;  // items started, and whether the next one's rows were requested
+    for (int j = blockIdx.x; j < nb; j += nx, ++k) {
+        const int s = k & 1;
         const int64_t t0 = (int64_t)j * kPfBlock;
         const int n = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
-        // packed rows (one contiguous run of the cache) and norms; zeros past n
-        for (int i = tid; i < kPfBlock * KB; i += kPxThreads) {
-            const int row = i / KB, part = i - row * KB;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < n)
-                v = __ldg(reinterpret_cast<const uint4*>(cache.k_packed + (crow0 + t0 + row) * (16 * KB)) + part);
-            *reinterpret_cast<uint4*>(sm + kPxSK + row * 64 + part * 16) = v;
-        }
-        for (int i = tid; i < kPfBlock * VB; i += kPxThreads) {
-            const int row = i / VB, part = i - row * VB;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (row < n)
-                v = __ldg(reinterpret_cast<const uint4*>(cache.v_packed + (crow0 + t0 + row) * (16 * VB)) + part);
-            *reinterpret_cast<uint4*>(sm + kPxSV + row * 64 + part * 16) = v;
-        }
-        {
-            const int k = tid & 127;
-            const float* nrm = tid < 128 ? cache.k_norm : cache.v_norm;
-            reinterpret_cast<float*>(sm + (tid < 128 ? kPfImgKN : kPfImgVN))[k] =
-                k < n ? __ldg(nrm + crow0 + t0 + k) : 0.f;
+        const int nr = rows_of(j);
+        if (tid == 0) {
+            // the next block's rows into the other stage (free: the block that
+            // used it was built before the last barrier), then wait for this
+            // block's rows (bounded) and for the last image store to have read
+            // shared memory
+            pre = j + nx < nb;
+            if (pre) stage(j + nx, s ^ 1);
+            const bool ok = mbar_wait(&bars[s], (k >> 1) & 1);
+            if (!ok) report_timeout(status, kPxStatusWait);
+            bulk_wait_read<0>();
+            *okf = ok ? 1 : 0;
         }
         __syncthreads();
+        if (!*okf) break;
+        const unsigned char* sk = sm + kPxStage + s * kPxStageBytes;
+        const unsigned char* sv = sk + 8192;
+        {  // norms; zeros past n
+            const int kk = tid & 127;
+            const float* nrm = tid < 128 ? cache.k_norm : cache.v_norm;
+            reinterpret_cast<float*>(sm + (tid < 128 ? kPfImgKN : kPfImgVN))[kk] =
+                kk < n ? __ldg(nrm + crow0 + t0 + kk) : 0.f;
+        }
         // K tile: lanes take the 16 chunks of 8 dims of a row (consecutive words
         // of the staged row, conflict-free tile stores); rows (tid / 16) + 16 i;
-        // 4 pair lookups per chunk
+        // 4 pair lookups per chunk; rows past the capacity read index 0
         {
             const int k8 = tid & 15;
             constexpr uint32_t M = (1u << (2 * KB)) - 1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = (tid >> 4) + 16 * i;
-                const uint32_t f =
-                    pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sm + kPxSK + t * 64), k8 * 8 * KB);
+                const uint32_t f = t < nr ? pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sk + t * (16 * KB)),
+                                                            k8 * 8 * KB)
+                                          : 0u;
                 uint4 c;
                 c.x = tkl[kPfCopies * (f & M)];
                 c.y = tkl[kPfCopies * ((f >> (2 * KB)) & M)];
@@ -226,8 +270,9 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
                 uint32_t f[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    f[u] = pf_bits<2 * VB>(reinterpret_cast<const uint32_t*>(sm + kPxSV + (8 * t8 + u) * 64),
-                                           2 * jp * VB);
+                    f[u] = 8 * t8 + u < nr ? pf_bits<2 * VB>(reinterpret_cast<const uint32_t*>(sv + (8 * t8 + u) * (16 * VB)),
+                                                             2 * jp * VB)
+                                           : 0u;
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
                     uint32_t c[4];
@@ -242,6 +287,7 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
                 }
             }
         }
+        fence_proxy_async_smem();  // the image goes out through the async proxy
         __syncthreads();
         if (tid >= 128 && tid < 160) {  // the block's largest |V norm|
             const float* vn = reinterpret_cast<const float*>(sm + kPfImgVN);
@@ -249,12 +295,17 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
             if (lane == 0) bmax[(int64_t)bg * nbmax + j] = v;
         }
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(sm);
-            uint4* dst = reinterpret_cast<uint4*>(img + ((int64_t)bg * nbmax + j) * kPfImgBytes);
-            for (int i = tid; i < (int)(kPfImgBytes / 16); i += kPxThreads) dst[i] = src[i];
+        if (tid == 0) {
+            px_bulk_store(img + ((int64_t)bg * nbmax + j) * kPfImgBytes, sa, kPfImgBytes);
+            bulk_commit();
         }
-        __syncthreads();
+    }
+    if (tid == 0) {
+        bulk_wait<0>();  // the image stores are complete before the block leaves
+        if (!*okf) {  // after a wait that gave up: the staging copies in flight land first (bounded)
+            mbar_wait(&bars[k & 1], (k >> 1) & 1);
+            if (pre) mbar_wait(&bars[(k + 1) & 1], ((k + 1) >> 1) & 1);
+        }
     }
 }
 
@@ -314,8 +365,9 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, int parity, volatile int*
 // 2^e for -126 <= e <= 127, from the exponent field.
 __device__ __forceinline__ float pf_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// Tiles of a (sequence, KV head) are taken last first: with a causal mask the
-// last tiles read the most KV blocks, so the longest CTAs start first.
+// Block (bg, y) takes query tile gridDim.y - 1 - y of (sequence, KV head) bg:
+// blocks start in x-fastest order, so the last tiles of every head, which
+// read the most KV blocks under the causal mask, start first.
 __global__ void __launch_bounds__(kPfThreads, 1)
 k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restrict__ rot,
                const unsigned char* __restrict__ img, int nbmax, int Hq, int Hkv, int T,
@@ -326,8 +378,8 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
     const uint32_t sa = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hq / Hkv, tpr = kPfRows / G;
-    const int bg = blockIdx.y, b = bg / Hkv, g = bg - b * Hkv;
-    const int mt = (int)(gridDim.x - 1 - blockIdx.x);
+    const int bg = blockIdx.x, b = bg / Hkv, g = bg - b * Hkv;
+    const int mt = (int)(gridDim.y - 1 - blockIdx.y);
     const int rows_total = T * G;
     int64_t qs = __ldg(q_start + b);
     const int last_tok = min(T, (mt + 1) * tpr) - 1;
@@ -768,8 +820,8 @@ cudaError_t prefill_expand(int B, int T, int Hkv, const int32_t* q_start, const 
     const int groups = B * Hkv;
     int x = 608 / groups;  // about four CTAs per SM in all
     x = x < 1 ? 1 : (x > nbmax ? nbmax : x);
-    fn<<<dim3((unsigned)x, (unsigned)groups), kPxThreads, kPxSmem, s>>>(q_start, T, Hkv, cache, nbmax, img, bmax,
-                                                                          reinterpret_cast<uint4*>(ws), P);
+    fn<<<dim3((unsigned)x + 1, (unsigned)groups), kPxThreads, kPxSmem, s>>>(q_start, T, Hkv, cache, nbmax, img, bmax,
+                                                                          reinterpret_cast<uint4*>(ws), status_word(), P);
     return cudaGetLastError();
 }
 
@@ -787,7 +839,7 @@ cudaError_t launch_prefill_attention(const void* q, int B, int T, int Hq, int Hk
     if (e != cudaSuccess) return e;
     const int G = Hq / Hkv;
     const int nbmax = (int)((cache.cap + kPfBlock - 1) / kPfBlock);
-    const dim3 grid((unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows), (unsigned)(B * Hkv));
+    const dim3 grid((unsigned)(B * Hkv), (unsigned)(((int64_t)T * G + kPfRows - 1) / kPfRows));
     const float* bmax = reinterpret_cast<const float*>(img + attn_prefill_img_bytes(B, Hkv, cache.cap));
     k_attn_prefill<<<grid, kPfThreads, kPfSmem, s>>>(static_cast<const __nv_bfloat16*>(q), rot, img, nbmax, Hq, Hkv,
                                                      T, q_start, bmax, cache.cap, out, status_word(), P);

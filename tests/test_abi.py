@@ -250,6 +250,8 @@ def test_prefill_call_validation_before_launch(L):
     assert L.tq_attn_prefill(p64.handle, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 2
     assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 5, 3, f(1.0), A, A, W, None) == 2
     assert L.tq_attn_prefill(h, A, 1, 300, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 4    # cap < T
+    big = abi.CacheView(A, A, A, A, 1 << 23)
+    assert L.tq_attn_prefill(h, A, 1, 2_100_000, 8, 2, big, A, 4, 3, f(1.0), A, A, W, None) == 2  # tiles > 65535
     assert L.tq_attn_prefill(h, A + 8, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, W, None) == 3
     assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, 16, None) == 5
     assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(float("nan")), A, A, W, None) == 1
