@@ -333,11 +333,20 @@ static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kPfStatusWait = 51;      // an MMA, copy or softmax wait gave up
 constexpr int kPfStatusRange = 52;     // q_start[b] + T exceeds the cache capacity, or q_start < 0
 constexpr float kPfRescale = 8.f;      // move the reference max when the row max grows by more (log2)
+constexpr uint32_t kPfOutStride = 528;  // output tile row stride in shared memory at the end
+static_assert(128 * kPfOutStride <= kPfKS + 32768, "the output tile fits the Q region and K stage 0");
 
 __device__ __forceinline__ float pf_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 1-D bulk copy of `bytes` bytes from shared address `src` to global memory
+// (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
+__device__ __forceinline__ void pf_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
 }
 
 // Barrier among the softmax warps (named barrier 1).
@@ -534,15 +543,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
         const int r = 32 * qd + lane;
         const int grow = mt * kPfRows + r;  // the row within (b, g)
         const bool rvalid = grow < rows_total;
-        const int tok = rvalid ? grow / G : 0, hh = rvalid ? grow - tok * G : 0;
-        // E: the largest V norm this CTA reads is below 2^E (from the blocks' maxima)
-        int E = 0;
-        {
-            float vm = 0.f;
-            for (int t = lane; t < nblk; t += 32) vm = fmaxf(vm, __ldg(bmax + (int64_t)bg * nbmax + t));
-            for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
-            if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
-        }
+        const int tok = rvalid ? grow / G : 0;
         // Q tile: warp w stages rows 16 (w - 2) .. + 15 as bf16 (zero rows past
         // the chunk's last token) for the rotation product; from the rotated
         // rows each thread then writes its 64 columns as fp16 high and low parts
@@ -568,6 +569,14 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_in);
+        // E: the largest V norm this CTA reads is below 2^E (from the blocks' maxima)
+        int E = 0;
+        {
+            float vm = 0.f;
+            for (int t = lane; t < nblk; t += 32) vm = fmaxf(vm, __ldg(bmax + (int64_t)bg * nbmax + t));
+            for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+            if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
+        }
         {
             const uint32_t t_q = tmem + ((uint32_t)(32 * qd) << 16) + 384 + 64 * hf;
             pf_wait(rot_done, 0, abort_f, status);
@@ -773,17 +782,35 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
 #pragma unroll
             for (int k = 0; k < 4; ++k) O[4 * i + k] = hf ? oo[k] - O[4 * i + k] : O[4 * i + k] + oo[k];  // (lo + hi, lo - hi)
         }
-        if (rvalid && *abort_f == 0) {
-            float4* dst = reinterpret_cast<float4*>(out + (((int64_t)b * T + tok) * Hq + g * G + hh) * 128 + 64 * hf);
+        pf_softmax_sync();  // the exchange is read: the Q region takes the output tile
+        // The output tile, row-major with rows kPfOutStride bytes apart (512
+        // bytes of data and 16 of padding, so the per-row writes hit distinct
+        // banks), from the start of shared memory: the Q region and the K
+        // stages are free once the last product is done.  Lanes 0-15 of each
+        // softmax warp then send 16 rows with one bulk store each, and wait only
+        // until shared memory has been read.
+        unsigned char* ot = sm + kPfQH;
 #pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-                const int jd = 64 * hf + i;
-                float4 v;
-                v.x = __uint_as_float(__float_as_uint(O[i] * sc) ^ P.sgn[jd]);
-                v.y = __uint_as_float(__float_as_uint(O[i + 1] * sc) ^ P.sgn[jd + 1]);
-                v.z = __uint_as_float(__float_as_uint(O[i + 2] * sc) ^ P.sgn[jd + 2]);
-                v.w = __uint_as_float(__float_as_uint(O[i + 3] * sc) ^ P.sgn[jd + 3]);
-                dst[i / 4] = v;
+        for (int i = 0; i < 64; i += 4) {
+            const int jd = 64 * hf + i;
+            float4 v;
+            v.x = __uint_as_float(__float_as_uint(O[i] * sc) ^ P.sgn[jd]);
+            v.y = __uint_as_float(__float_as_uint(O[i + 1] * sc) ^ P.sgn[jd + 1]);
+            v.z = __uint_as_float(__float_as_uint(O[i + 2] * sc) ^ P.sgn[jd + 2]);
+            v.w = __uint_as_float(__float_as_uint(O[i + 3] * sc) ^ P.sgn[jd + 3]);
+            *reinterpret_cast<float4*>(ot + r * kPfOutStride + jd * 4) = v;
+        }
+        fence_proxy_async_smem();
+        pf_softmax_sync();
+        if (lane < 16 && *abort_f == 0) {
+            const int rr = 16 * (warp - 2) + lane;
+            const int gr = mt * kPfRows + rr;
+            if (gr < rows_total) {
+                const int tk = gr / G, hd = gr - tk * G;
+                pf_bulk_store(out + (((int64_t)b * T + tk) * Hq + g * G + hd) * 128, sa + kPfQH + rr * kPfOutStride,
+                              512);
+                bulk_commit();
+                bulk_wait_read<0>();
             }
         }
     }
