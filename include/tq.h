@@ -297,8 +297,8 @@ tq_status tq_attn_decode_append_paged(const tq_plan *plan, const void *q, const 
                                       size_t workspace_bytes, tq_stream_t stream);
 
 /* Workspace bytes tq_attn_prefill needs for a cache of capacity `cap`: 32 KB
- * for the query rotation matrix, then the expanded K/V tiles, 66564 bytes per
- * 128 cache positions per sequence and KV head (about 4.3 times the packed
+ * for the query rotation matrix, then the expanded K/V tiles, 99332 bytes per
+ * 128 cache positions per sequence and KV head (about 6.5 times the packed
  * K4/V3 cache they expand); 0 for
  * invalid sizes, cap < T or d != 128.  B, T, Hq are checked only. */
 size_t tq_attn_prefill_workspace_bytes(int B, int T, int Hq, int Hkv, int64_t cap, int d);

@@ -289,6 +289,7 @@ void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, fl
     A.sparse_thr = sparse_thr;
     const double ks = P.hscale[k_bits] > 0.0f ? P.hscale[k_bits] : 1.0;
     const double vs = P.hscale[v_bits] > 0.0f ? P.hscale[v_bits] : 1.0;
+    for (int i = 0; i < 16; ++i) A.kcen_l[i] = (float)((double)P.c32[k_bits][i] * ks - (double)P.hcen[k_bits][i]);
     A.q_mul = (float)((double)scale * 1.4426950408889634 / (sd * ks));
     A.out_mul = (float)(1.0 / vs);
 }

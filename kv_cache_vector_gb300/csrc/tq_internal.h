@@ -35,11 +35,15 @@ struct AttnParams {
     float inv_sqrt_d;
     float scale;       // softmax scale applied to q . k
     float sparse_thr;  // 0 = dense
-    // d = 128 tensor-core kernels: fp16 values of c * s_k and c * s_v (exact
-    // in fp16), the query multiplier scale * log2(e) / (sqrt(d) * s_k) and the
-    // output multiplier 1 / s_v.
+    // d = 128 tensor-core kernels: the fp16 values nearest c * s_k and c * s_v
+    // (s per width makes every one of them close: within 8.3e-5 relative at 4
+    // bits, 2.2e-5 at 3), the query multiplier scale * log2(e) / (sqrt(d) *
+    // s_k) and the output multiplier 1 / s_v; kcen_l is the rest of c * s_k,
+    // c * s_k - kcen_h (fp16 holds it to 2^-11 of itself), for the prefill's
+    // key low part.
     float kcen_h[16];
     float vcen_h[16];
+    float kcen_l[16];
     float q_mul;
     float out_mul;
     int two_sided;  // as RowParams
@@ -173,7 +177,7 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
 // (kPfRotBytes), one expanded tile image of kPfImgBytes per block of 128
 // cache positions per (sequence, KV head), then each block's largest V norm
 // (a float).
-constexpr size_t kPfImgBytes = 66560;
+constexpr size_t kPfImgBytes = 99328;
 constexpr size_t kPfRotBytes = 32768;
 inline size_t attn_prefill_img_bytes(int B, int Hkv, int64_t cap) {
     return (size_t)B * Hkv * (size_t)((cap + 127) / 128) * kPfImgBytes;

@@ -9,50 +9,61 @@
 // output) with many queries per KV head, which turns both contractions into
 // dense matrix products.
 //
+// Precision.  The products run on fp16 operands with fp32 accumulation, and
+// every operand whose rounding the output can see is carried in two fp16
+// parts: the rotated query (high and low), the key centroids (the fp16
+// value nearest c * s_k and the fp16 rest c * s_k - that), and P (high and
+// low), so S = Q_hi K^T + Q_lo K^T + Q_hi Dk^T and O = P_hi V + P_lo V.  Only
+// the V centroids stay single (fp16 nearest c * s_v, within 2.2e-5 relative
+// at 3 bits): early causal tokens average few rows, so their outputs are
+// nearly raw V values, and the 2e-3 absolute bound has to hold on them.
+//
 // Two kernels.  Every (sequence, KV head) has many query tiles, and each of
 // them reads the whole prefix, so the packed rows are expanded once, not once
 // per tile:
 //   k_prefill_expand  turns each block of 128 cached positions into a tile
-//     image in the workspace: the K centroids [position][dim] and the V
-//     centroids [dim][position] as fp16, both in the 128-byte-swizzled
-//     K-major layout the tensor cores read, then the 128 K norms and the
-//     128 V norms (65 KB; norms past the sequence's last position are zero,
-//     centroids there c[0]), and the block's largest V norm.  One block also
-//     writes the query rotation s2 . H . s as a bf16 matrix of +-1.
+//     image in the workspace: the K centroid high and low parts
+//     [position][dim] and the V centroids [dim][position] as fp16, all in the
+//     128-byte-swizzled K-major layout the tensor cores read, then the 128 K
+//     norms and the 128 V norms (97 KB; norms past the sequence's last
+//     position are zero, centroids there c[0]), and the block's largest V
+//     norm.  One extra block writes the query rotation s2 . H . s as a bf16
+//     matrix of +-1.
 //   k_attn_prefill  takes 128 query rows of one (sequence, KV head): 128 / G
 //     consecutive tokens times the G query heads of the group (row r = token
 //     r / G, head r % G), with warp roles:
-//       warp 0    streams the K tile of block j into K stage j % 2 once S of
-//                 block j - 2 is done (bulk copies);
+//       warp 0    streams the K tiles (high and low) of block j into K stage
+//                 j % 2 once S of block j - 2 is done (bulk copies);
 //       warp 10   streams the V tile and norms into V stage j % 2 once the PV
 //                 product of block j - 2 is done;
 //       warp 1    issues the query rotation (bf16 rows times the +-1 matrix,
-//                 exact products, fp32 sums), then per block S = Q_hi K^T +
-//                 Q_lo K^T into tensor-memory buffer j % 3 (the rotated query
-//                 split into fp16 high and low parts keeps about 22
-//                 significant bits) and the PV product of block j - 1, O += P V
-//                 with P read from tensor memory;
-//       warps 2-9 two threads per query row, 64 columns each: the query tile
-//                 from the rotated rows, then per block the scores times the
-//                 K norms and the query's power-of-two scale, the causal mask,
-//                 the row max merged through shared memory, and P = exp2(s -
-//                 m) times the V norm over 2^E (E fixed per CTA from the
-//                 largest V norm it reads) as fp16 over the thread's own S
-//                 columns.
-//     The output accumulates in tensor memory.  The reference max m of a row
-//     moves only when a block raises the row max by more than 8 (log2 units),
-//     so P stays below 2^8 (fp16: relative rounding at most 2^-12 per
-//     weight; the denominator sums the fp32 weights).  When it moves, the
-//     softmax threads rescale their output columns in tensor memory after the
-//     previous PV product is done.  At the end the rows are divided by the
-//     denominator, scaled by 2^E / s_v and rotated back (s . H (s2 . o) /
-//     sqrt(d)): butterflies over a thread's 64 columns in registers, the last
-//     one through shared memory.
+//                 exact products, fp32 sums), then per block S into
+//                 tensor-memory buffer j % 2 (24 MMAs, the query read from
+//                 tensor memory) and the PV product of block j - 1 (16 MMAs,
+//                 P read from tensor memory);
+//       warps 2-9 two threads per query row, 64 columns each: the query's
+//                 high and low parts (under a power-of-two scale per row)
+//                 into tensor memory from the rotated rows, then per block
+//                 the scores times the K norms and the query's scale, the
+//                 causal mask, the row max merged through shared memory, and
+//                 P = exp2(s - m) times the V norm over 2^E (E fixed per CTA
+//                 from the largest V norm it reads) as fp16 high and low
+//                 parts over the thread's own S columns.
+//     Tensor memory: S/P buffers at columns 0 and 128, the output at 256, the
+//     query's high parts at 384 and low parts at 448.  The output
+//     accumulates in tensor memory.  The reference max m of a row moves only
+//     when a block raises the row max by more than 8 (log2 units), so P
+//     stays below 2^8; when it moves, the softmax threads rescale their
+//     output columns in tensor memory after the previous PV product is done.
+//     At the end the rows are divided by the denominator, scaled by 2^E / s_v
+//     and rotated back (s . H (s2 . o) / sqrt(d)): butterflies over a
+//     thread's 64 columns in registers, the last one through shared memory,
+//     and the rows leave through bulk stores.
 //
 // Every wait on an mbarrier is bounded (2 s); a wait that gives up sets the
 // device status word and a flag that ends every other wait of the CTA, the
-// MMA thread waits (bounded) for its products in flight, the copy thread for
-// its copies, and the CTA frees its tensor memory and returns.
+// MMA thread waits (bounded) for its products in flight, the copy threads for
+// their copies, and the CTA frees its tensor memory and returns.
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -72,18 +83,22 @@ namespace dev {
 
 constexpr int kPfBlock = 128;    // KV positions per block
 // tile image of one block, offsets within it
-constexpr uint32_t kPfImgK = 0;        // K centroids, 128 x 128 fp16, [position][dim]
-constexpr uint32_t kPfImgV = 32768;    // V centroids, [dim][position]
-constexpr uint32_t kPfImgKN = 65536;   // K norms (128 floats)
-constexpr uint32_t kPfImgVN = 66048;   // V norms
+constexpr uint32_t kPfImgK = 0;        // K centroid high parts, 128 x 128 fp16, [position][dim]
+constexpr uint32_t kPfImgD = 32768;    // K centroid low parts, the same layout
+constexpr uint32_t kPfImgV = 65536;    // V centroids, [dim][position]
+constexpr uint32_t kPfImgKN = 98304;   // K norms (128 floats)
+constexpr uint32_t kPfImgVN = 98816;   // V norms
 static_assert(kPfImgVN + 512 == kPfImgBytes, "tile image layout");
 
-// ---- expansion kernel
+// ---- expansion kernel: the image is built in two halves in one 64 KB buffer
+// (the K tiles, then the V tile and norms)
 constexpr int kPxThreads = 256;
-constexpr uint32_t kPxStage = kPfImgBytes;   // two stages of packed rows: K (8 KB) then V (8 KB)
+constexpr uint32_t kPxBuf = 0;
+constexpr uint32_t kPxStage = 65536;         // two stages of packed rows: K (8 KB) then V (8 KB)
 constexpr uint32_t kPxStageBytes = 16384;
-constexpr uint32_t kPxTK = kPxStage + 2 * kPxStageBytes;  // K pair table, 4 copies (up to 256 x 4 words)
-constexpr uint32_t kPxTV = kPxTK + 4096;     // V pair table, 4 copies
+constexpr uint32_t kPxTK = kPxStage + 2 * kPxStageBytes;  // K high-part pair table, 4 copies (256 x 4 words)
+constexpr uint32_t kPxTD = kPxTK + 4096;     // K low-part pair table
+constexpr uint32_t kPxTV = kPxTD + 4096;     // V pair table
 constexpr uint32_t kPxBar = kPxTV + 4096;    // two mbarriers, a flag
 constexpr uint32_t kPxSmem = kPxBar + 32;
 constexpr int kPxStatusWait = 53;            // a staging wait of the expansion gave up
@@ -111,24 +126,24 @@ __device__ __forceinline__ uint32_t pf_pack_half2(float a, float b) {
     return (uint32_t)__half_as_ushort(__float2half_rn(a)) | ((uint32_t)__half_as_ushort(__float2half_rn(b)) << 16);
 }
 
-// ------------------------------------------------------------------ expansion
-
 // 1-D bulk copy of `bytes` bytes from shared address `src` to global memory
 // (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
-__device__ __forceinline__ void px_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+__device__ __forceinline__ void pf_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                  : "memory");
 }
 
+// ------------------------------------------------------------------ expansion
+
 // Block (x, bg), x < gridDim.x - 1, expands blocks x, x + gridDim.x - 1, ..
 // of (sequence, KV head) bg into img + (bg nbmax + j) kPfImgBytes, and the
 // block's largest |V norm| into bmax[bg nbmax + j]; block (gridDim.x - 1, 0)
-// writes the query rotation matrix.
-// Blocks at or past the sequence's last position q_start[b] + T are not
-// read; a sequence whose range is invalid is skipped (the attention kernel
-// reports it).  Thread 0 fetches the packed rows of the next block (one bulk
-// copy per side, rows below the capacity only) while the block builds the
-// current image, and sends each image out with one bulk store.
+// writes the query rotation matrix.  Blocks at or past the sequence's last
+// position q_start[b] + T are not read; a sequence whose range is invalid is
+// skipped (the attention kernel reports it).  Thread 0 fetches the packed
+// rows of the next block (one bulk copy per side, rows below the capacity
+// only) while the block builds the current image, and sends each half of the
+// image out with one bulk store.
 template <int KB, int VB>
 __global__ void __launch_bounds__(kPxThreads, 2)
 k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_view cache, int nbmax,
@@ -173,6 +188,7 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
     if ((int)blockIdx.x >= nb) return;
     const int64_t crow0 = (int64_t)bg * cache.cap;  // cache row of position 0
     uint32_t* tk = reinterpret_cast<uint32_t*>(sm + kPxTK);
+    uint32_t* td = reinterpret_cast<uint32_t*>(sm + kPxTD);
     uint32_t* tv = reinterpret_cast<uint32_t*>(sm + kPxTV);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPxBar);  // [2] the stage's rows have landed
     volatile int* okf = reinterpret_cast<volatile int*>(sm + kPxBar + 16);
@@ -181,12 +197,14 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
     for (int i = tid; i < (kPfCopies << (2 * KB)); i += kPxThreads) {
         const int e = i / kPfCopies;
         tk[i] = pf_pack_half2(P.kcen_h[e & ((1 << KB) - 1)], P.kcen_h[e >> KB]);
+        td[i] = pf_pack_half2(P.kcen_l[e & ((1 << KB) - 1)], P.kcen_l[e >> KB]);
     }
     for (int i = tid; i < (kPfCopies << (2 * VB)); i += kPxThreads) {
         const int e = i / kPfCopies;
         tv[i] = pf_pack_half2(P.vcen_h[e & ((1 << VB) - 1)], P.vcen_h[e >> VB]);
     }
     const uint32_t* tkl = tk + (lane & (kPfCopies - 1));  // this lane's copy
+    const uint32_t* tdl = td + (lane & (kPfCopies - 1));
     const uint32_t* tvl = tv + (lane & (kPfCopies - 1));
     // rows of block j that exist in the cache (at least the n of the sequence)
     auto rows_of = [&](int j) {
@@ -216,6 +234,7 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
         const int64_t t0 = (int64_t)j * kPfBlock;
         const int n = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
         const int nr = rows_of(j);
+        unsigned char* dsti = img + ((int64_t)bg * nbmax + j) * kPfImgBytes;
         if (tid == 0) {
             // the next block's rows into the other stage (free: the block that
             // used it was built before the last barrier), then wait for this
@@ -232,15 +251,10 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
         if (!*okf) break;
         const unsigned char* sk = sm + kPxStage + s * kPxStageBytes;
         const unsigned char* sv = sk + 8192;
-        {  // norms; zeros past n
-            const int kk = tid & 127;
-            const float* nrm = tid < 128 ? cache.k_norm : cache.v_norm;
-            reinterpret_cast<float*>(sm + (tid < 128 ? kPfImgKN : kPfImgVN))[kk] =
-                kk < n ? __ldg(nrm + crow0 + t0 + kk) : 0.f;
-        }
-        // K tile: lanes take the 16 chunks of 8 dims of a row (consecutive words
-        // of the staged row, conflict-free tile stores); rows (tid / 16) + 16 i;
-        // 4 pair lookups per chunk; rows past the capacity read index 0
+        // K tiles, high and low parts: lanes take the 16 chunks of 8 dims of a
+        // row (consecutive words of the staged row, conflict-free tile stores);
+        // rows (tid / 16) + 16 i; 4 pair lookups per chunk and part; rows past
+        // the capacity read index 0
         {
             const int k8 = tid & 15;
             constexpr uint32_t M = (1u << (2 * KB)) - 1;
@@ -250,13 +264,27 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
                 const uint32_t f = t < nr ? pf_bits<8 * KB>(reinterpret_cast<const uint32_t*>(sk + t * (16 * KB)),
                                                             k8 * 8 * KB)
                                           : 0u;
-                uint4 c;
-                c.x = tkl[kPfCopies * (f & M)];
-                c.y = tkl[kPfCopies * ((f >> (2 * KB)) & M)];
-                c.z = tkl[kPfCopies * ((f >> (4 * KB)) & M)];
-                c.w = tkl[kPfCopies * ((f >> (6 * KB)) & M)];
-                *reinterpret_cast<uint4*>(sm + kPfImgK + pf_chunk(t, k8)) = c;
+                const uint32_t e0 = f & M, e1 = (f >> (2 * KB)) & M, e2 = (f >> (4 * KB)) & M, e3 = (f >> (6 * KB)) & M;
+                const uint32_t off = pf_chunk(t, k8);
+                *reinterpret_cast<uint4*>(sm + kPxBuf + off) =
+                    make_uint4(tkl[kPfCopies * e0], tkl[kPfCopies * e1], tkl[kPfCopies * e2], tkl[kPfCopies * e3]);
+                *reinterpret_cast<uint4*>(sm + kPxBuf + kPfImgD + off) =
+                    make_uint4(tdl[kPfCopies * e0], tdl[kPfCopies * e1], tdl[kPfCopies * e2], tdl[kPfCopies * e3]);
             }
+        }
+        fence_proxy_async_smem();  // the image goes out through the async proxy
+        __syncthreads();
+        if (tid == 0) {
+            pf_bulk_store(dsti + kPfImgK, sa + kPxBuf, 65536);
+            bulk_commit();
+            bulk_wait_read<0>();  // the buffer takes the second half
+        }
+        __syncthreads();
+        {  // norms (after the V tile in the buffer); zeros past n
+            const int kk = tid & 127;
+            const float* nrm = tid < 128 ? cache.k_norm : cache.v_norm;
+            reinterpret_cast<float*>(sm + kPxBuf + (tid < 128 ? kPfImgKN : kPfImgVN) - kPfImgV)[kk] =
+                kk < n ? __ldg(nrm + crow0 + t0 + kk) : 0.f;
         }
         // V tile: lanes take consecutive dim pairs (2 jp, 2 jp + 1) of the same
         // rows; thread = (dim pair tid % 64, groups (tid / 64) + 4 i of 8
@@ -282,21 +310,21 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
                         const uint32_t bb = (f[2 * pp + 1] >> (jj * VB)) & M;
                         c[pp] = tvl[kPfCopies * (a | (bb << VB))];
                     }
-                    *reinterpret_cast<uint4*>(sm + kPfImgV + pf_chunk(2 * jp + jj, t8)) =
+                    *reinterpret_cast<uint4*>(sm + kPxBuf + pf_chunk(2 * jp + jj, t8)) =
                         make_uint4(c[0], c[1], c[2], c[3]);
                 }
             }
         }
-        fence_proxy_async_smem();  // the image goes out through the async proxy
+        fence_proxy_async_smem();
         __syncthreads();
         if (tid >= 128 && tid < 160) {  // the block's largest |V norm|
-            const float* vn = reinterpret_cast<const float*>(sm + kPfImgVN);
+            const float* vn = reinterpret_cast<const float*>(sm + kPxBuf + kPfImgVN - kPfImgV);
             float v = fmaxf(fmaxf(fabsf(vn[lane]), fabsf(vn[lane + 32])), fmaxf(fabsf(vn[lane + 64]), fabsf(vn[lane + 96])));
             for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
             if (lane == 0) bmax[(int64_t)bg * nbmax + j] = v;
         }
         if (tid == 0) {
-            px_bulk_store(img + ((int64_t)bg * nbmax + j) * kPfImgBytes, sa, kPfImgBytes);
+            pf_bulk_store(dsti + kPfImgV, sa + kPxBuf, kPfImgBytes - kPfImgV);
             bulk_commit();
         }
     }
@@ -318,35 +346,34 @@ k_prefill_expand(const int32_t* __restrict__ q_start, int T, int Hkv, tq_cache_v
 constexpr int kPfRows = 128;           // query rows per CTA
 constexpr int kPfThreads = 352;        // warp 0 K copies, warp 1 MMAs, warps 2-9 softmax, warp 10 V copies
 constexpr int kPfSoftmax = 256;
-constexpr uint32_t kPfQH = 0;          // Q high parts, 128 x 128 fp16 (the output exchange at the end)
-constexpr uint32_t kPfQL = 32768;      // Q low parts
-constexpr uint32_t kPfKS = 65536;      // two K stages: the K tile of a block (32 KB, 1024-aligned)
-constexpr uint32_t kPfVS = 131072;     // two V stages: V tile, K norms, V norms of a block
-constexpr uint32_t kPfVStage = kPfImgBytes - kPfImgV;    // 33792 bytes (1024-aligned)
-constexpr uint32_t kPfRed = kPfVS + 2 * kPfVStage;       // [2][2][128] floats: per-half row maxima
-constexpr uint32_t kPfBar = kPfRed + 2048;               // 19 mbarriers
-constexpr uint32_t kPfMisc = kPfBar + 160;               // tensor-memory base, abort flag
-constexpr uint32_t kPfQX = kPfMisc + 16;                 // the rows' power-of-two query scales (128 floats)
+constexpr uint32_t kPfKStage = 65536;  // a K stage: the high and low K tiles of a block
+constexpr uint32_t kPfKS = 0;          // two K stages (1024-aligned); the exchange and output tiles at the end
+constexpr uint32_t kPfQB = kPfKS + kPfKStage;         // prologue, in K stage 1: the bf16 query rows
+constexpr uint32_t kPfRot = kPfQB + 32768;            // and the rotation matrix
+constexpr uint32_t kPfVS = kPfKS + 2 * kPfKStage;     // two V stages: V tile, K norms, V norms of a block
+constexpr uint32_t kPfVStage = kPfImgBytes - kPfImgV;  // 33792 bytes (1024-aligned)
+constexpr uint32_t kPfRed = kPfVS + 2 * kPfVStage;     // [2][2][128] floats: per-half row maxima
+constexpr uint32_t kPfBar = kPfRed + 2048;             // 15 mbarriers
+constexpr uint32_t kPfMisc = kPfBar + 128;             // tensor-memory base, abort flag
+constexpr uint32_t kPfQX = kPfMisc + 16;               // the rows' power-of-two query scales (128 floats)
 constexpr uint32_t kPfEnd = kPfQX + 512;
-constexpr uint32_t kPfSmem = kPfEnd + 1024;              // plus alignment slack
+constexpr uint32_t kPfSmem = kPfEnd + 1024;            // plus alignment slack
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
+constexpr uint32_t kPfTO = 256;        // tensor-memory column of the output (and of the rotated rows first)
+constexpr uint32_t kPfTQ = 384;        // of the query's high parts; the low parts 64 further
 constexpr int kPfStatusWait = 51;      // an MMA, copy or softmax wait gave up
 constexpr int kPfStatusRange = 52;     // q_start[b] + T exceeds the cache capacity, or q_start < 0
 constexpr float kPfRescale = 8.f;      // move the reference max when the row max grows by more (log2)
 constexpr uint32_t kPfOutStride = 528;  // output tile row stride in shared memory at the end
-static_assert(128 * kPfOutStride <= kPfKS + 32768, "the output tile fits the Q region and K stage 0");
+static_assert(128 * kPfOutStride <= 2 * kPfKStage, "the output tile fits the K stages");
+
+// 2^e for -126 <= e <= 127, from the exponent field.
+__device__ __forceinline__ float pf_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 __device__ __forceinline__ float pf_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 1-D bulk copy of `bytes` bytes from shared address `src` to global memory
-// (both 16-byte aligned, bytes % 16 == 0), in this thread's bulk group.
-__device__ __forceinline__ void pf_bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
 }
 
 // Barrier among the softmax warps (named barrier 1).
@@ -370,9 +397,6 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, int parity, volatile int*
     }
     return true;
 }
-
-// 2^e for -126 <= e <= 127, from the exponent field.
-__device__ __forceinline__ float pf_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 // Block (bg, y) takes query tile gridDim.y - 1 - y of (sequence, KV head) bg:
 // blocks start in x-fastest order, so the last tiles of every head, which
@@ -398,30 +422,28 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
     }
     const int64_t kv_end = qs < 0 ? 0 : qs + last_tok + 1;  // positions this CTA reads
     const int nblk = (int)((kv_end + kPfBlock - 1) / kPfBlock);
-    // Block j: K stage and V stage j % 2, tensor-memory buffer j % 3 (S, then
-    // P over it), output in columns 384-511.
+    // Block j: K stage, V stage and tensor-memory S/P buffer j % 2.
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPfBar);
-    uint64_t* kfull = bars;         // [2] the K tile of the stage's block has landed
+    uint64_t* kfull = bars;         // [2] the K tiles of the stage's block have landed
     uint64_t* vfull = bars + 2;     // [2] its V tile and norms have landed
-    uint64_t* s_full = bars + 4;    // [3] S of the buffer's block is done (its K stage is free)
-    uint64_t* p_full = bars + 7;    // [3] the eight softmax warps wrote P over it
-    uint64_t* pv_done = bars + 10;  // [3] its PV product completed: buffer free, O current
-    uint64_t* vfree = bars + 13;    // [2] the PV product of the stage's block completed
-    uint64_t* q_full = bars + 15;   // the softmax warps wrote the query tile (fp16 high and low parts)
-    uint64_t* drain = bars + 16;    // the MMA thread's products in flight, on the abort path
-    uint64_t* q_in = bars + 17;     // the bf16 query rows and the rotation matrix are in shared memory
-    uint64_t* rot_done = bars + 18; // the rotated rows are in tensor memory (columns 384-511)
+    uint64_t* s_full = bars + 4;    // [2] S of the block is done (its K stage is free)
+    uint64_t* p_full = bars + 6;    // [2] the eight softmax warps wrote P over it
+    uint64_t* pv_done = bars + 8;   // [2] its PV product completed: V stage and buffer free, O current
+    uint64_t* q_in = bars + 10;     // the bf16 query rows and the rotation matrix are in shared memory
+    uint64_t* rot_done = bars + 11; // the rotated rows are in tensor memory (the output columns)
+    uint64_t* q_full = bars + 12;   // the softmax warps wrote the query's parts to tensor memory
+    uint64_t* drain = bars + 13;    // the MMA thread's products in flight, on the abort path
     uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kPfMisc);
     volatile int* abort_f = reinterpret_cast<volatile int*>(sm + kPfMisc + 4);
     float* red = reinterpret_cast<float*>(sm + kPfRed);
     float* qx_s = reinterpret_cast<float*>(sm + kPfQX);
 
     if (tid == 0) {
-        for (int i = 0; i < 19; ++i) mbar_init(&bars[i], ((i >= 7 && i < 10) || i == 15) ? 8u : (i == 17 ? 9u : 1u));
+        for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 6 || i == 7 || i == 12) ? 8u : (i == 10 ? 9u : 1u));
         *abort_f = 0;
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc<512>(slot);  // S/P buffers at 0, 128, 256; O at 384
+    if (warp == 1) tmem_alloc<512>(slot);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -429,32 +451,31 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
     constexpr uint32_t idesc = umma_idesc_f16(128, 128, false);
 
     if (warp == 0 || warp == 10) {
-        // ---- copies: warp 0 the K tile of block j into K stage j % 2 once S of
-        // block j - 2 is done, warp 10 the V tile and norms into V stage j % 2
-        // once the PV product of block j - 2 is
+        // ---- copies: warp 0 the K tiles of block j into K stage j % 2 once S
+        // of block j - 2 is done (block 1 once the rotation has read the
+        // prologue's operands there), warp 10 the V tile and norms into V stage
+        // j % 2 once the PV product of block j - 2 is
         if (lane == 0) {
             const bool kside = warp == 0;
             uint64_t* fb = kside ? kfull : vfull;
             if (kside) {  // the rotation matrix, B operand of the query rotation
                 mbar_arrive_expect_tx(q_in, 32768);
-                bulk_load(sa + kPfQL, rot, 32768, q_in);
+                bulk_load(sa + kPfRot, rot, 32768, q_in);
             }
             int issued = 0;
             for (int j = 0; j < nblk; ++j) {
                 const int s = j & 1;
-                if (j >= 2) {
-                    const int jo = j - 2;
-                    uint64_t* rel = kside ? &s_full[jo % 3] : &vfree[s];
-                    if (!pf_wait(rel, kside ? (jo / 3) & 1 : (jo >> 1) & 1, abort_f, status)) break;
-                }
+                bool ok = true;
+                if (kside && j == 1) ok = pf_wait(rot_done, 0, abort_f, status);
+                if (ok && j >= 2) ok = pf_wait(kside ? &s_full[s] : &pv_done[s], ((j - 2) >> 1) & 1, abort_f, status);
+                if (!ok) break;
                 const unsigned char* src = img + ((int64_t)bg * nbmax + j) * kPfImgBytes;
                 if (kside) {
-                    mbar_arrive_expect_tx(&kfull[s], 32768);
-                    bulk_load(sa + kPfKS + s * 32768, src + kPfImgK, 32768, &kfull[s]);
+                    mbar_arrive_expect_tx(&kfull[s], kPfKStage);
+                    bulk_load(sa + kPfKS + s * kPfKStage, src + kPfImgK, kPfKStage, &kfull[s]);
                 } else {
                     mbar_arrive_expect_tx(&vfull[s], kPfVStage);
-                    bulk_load(sa + kPfVS + s * kPfVStage, src + kPfImgV, 32768, &vfull[s]);
-                    bulk_load(sa + kPfVS + s * kPfVStage + 32768, src + kPfImgKN, kPfImgBytes - kPfImgKN, &vfull[s]);
+                    bulk_load(sa + kPfVS + s * kPfVStage, src + kPfImgV, kPfVStage, &vfull[s]);
                 }
                 issued = j + 1;
             }
@@ -464,7 +485,8 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             if (kside) mbar_wait(q_in, 0);
         }
     } else if (warp == 1) {
-        // ---- MMAs: S of block j, then the PV product of block j - 1
+        // ---- MMAs: the query rotation, then S of block j and the PV product
+        // of block j - 1
         if (lane == 0) {
             // the query rotation: rows (bf16, A) times the rotation matrix (B)
             bool ok = pf_wait(q_in, 0, abort_f, status);
@@ -474,62 +496,63 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_f16(tmem + 384, umma_desc_sw128(sa + kPfQH + off), umma_desc_sw128(sa + kPfQL + off),
+                    umma_f16(tmem + kPfTO, umma_desc_sw128(sa + kPfQB + off), umma_desc_sw128(sa + kPfRot + off),
                              idesc_bf, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(rot_done);
                 ok = pf_wait(q_full, 0, abort_f, status);
             }
-            int sb = 0, sph = 0;  // buffer and phase of the next S
-            int pb = 0, pph = 0;  // buffer and phase of the next PV product
             for (int j = 0; ok && j <= nblk; ++j) {
                 if (j < nblk) {
                     const int s = j & 1;
-                    // buffer sb last held P of block j - 3 (phase sph ^ 1)
+                    // the buffer last held P of block j - 2
                     ok = pf_wait(&kfull[s], (j >> 1) & 1, abort_f, status) &&
-                         (j < 3 || pf_wait(&pv_done[sb], sph ^ 1, abort_f, status));
+                         (j < 2 || pf_wait(&pv_done[s], ((j - 2) >> 1) & 1, abort_f, status));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t kt = sa + kPfKS + s * 32768;
-                    const uint32_t d = tmem + 128 * sb;
+                    const uint32_t kt = sa + kPfKS + s * kPfKStage;
+                    const uint32_t d = tmem + 128 * s;
+                    // S = Q_hi K_hi^T + Q_lo K_hi^T + Q_hi K_lo^T; dims 16 kk ..
+                    // 16 kk + 15 of the query at column 8 kk of its part
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_f16(d, umma_desc_sw128(sa + kPfQH + off), umma_desc_sw128(kt + off), idesc,
-                                 kk > 0 ? 1u : 0u);
+                        umma_f16_ts(d, tmem + kPfTQ + 8 * kk, umma_desc_sw128(kt + off), idesc, kk > 0 ? 1u : 0u);
                     }
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_f16(d, umma_desc_sw128(sa + kPfQL + off), umma_desc_sw128(kt + off), idesc, 1u);
+                        umma_f16_ts(d, tmem + kPfTQ + 64 + 8 * kk, umma_desc_sw128(kt + off), idesc, 1u);
                     }
-                    umma_commit(&s_full[sb]);
-                    if (++sb == 3) {
-                        sb = 0;
-                        sph ^= 1;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_f16_ts(d, tmem + kPfTQ + 8 * kk, umma_desc_sw128(kt + kPfImgD + off), idesc, 1u);
                     }
+                    umma_commit(&s_full[s]);
                 }
                 if (j >= 1) {
                     const int jj = j - 1, s = jj & 1;
                     ok = pf_wait(&vfull[s], (jj >> 1) & 1, abort_f, status) &&
-                         pf_wait(&p_full[pb], pph, abort_f, status);
+                         pf_wait(&p_full[s], (jj >> 1) & 1, abort_f, status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vt = sa + kPfVS + s * kPfVStage;
-                    // P of positions 16 kk .. 16 kk + 15 at column 64 (kk / 4) + 8 (kk % 4)
-                    // of the buffer
+                    // P of positions 16 kk .. 16 kk + 15: high parts at column
+                    // 64 (kk / 4) + 8 (kk % 4) of the buffer, low parts 32 further
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint32_t a = tmem + 128 * pb + 64 * (kk >> 2) + 8 * (kk & 3);
-                        umma_f16_ts(tmem + 384, a, umma_desc_sw128(vt + off), idesc, (jj > 0 || kk > 0) ? 1u : 0u);
+                        const uint32_t a = tmem + 128 * s + 64 * (kk >> 2) + 8 * (kk & 3);
+                        umma_f16_ts(tmem + kPfTO, a, umma_desc_sw128(vt + off), idesc, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(&pv_done[pb]);
-                    umma_commit(&vfree[s]);
-                    if (++pb == 3) {
-                        pb = 0;
-                        pph ^= 1;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t a = tmem + 128 * s + 64 * (kk >> 2) + 8 * (kk & 3) + 32;
+                        umma_f16_ts(tmem + kPfTO, a, umma_desc_sw128(vt + off), idesc, 1u);
                     }
+                    umma_commit(&pv_done[s]);
                 }
             }
             if (!ok) {  // the products in flight finish before the tensor memory is freed (bounded)
@@ -544,11 +567,13 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
         const int grow = mt * kPfRows + r;  // the row within (b, g)
         const bool rvalid = grow < rows_total;
         const int tok = rvalid ? grow / G : 0;
-        // Q tile: warp w stages rows 16 (w - 2) .. + 15 as bf16 (zero rows past
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
+        // Query: warp w stages rows 16 (w - 2) .. + 15 as bf16 (zero rows past
         // the chunk's last token) for the rotation product; from the rotated
         // rows each thread then writes its 64 columns as fp16 high and low parts
-        // over a power of two 2^e per row that keeps them below 2^14, and the
-        // tile goes to the tensor cores through q_full
+        // over a power of two 2^e per row that keeps them below 2^14, into the
+        // query's tensor-memory columns, and the MMA thread takes them through
+        // q_full
         {
             uint2 raw[16];
 #pragma unroll
@@ -563,7 +588,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                *reinterpret_cast<uint2*>(sm + kPfQH + pf_chunk(16 * (warp - 2) + i, lane >> 1) + (lane & 1) * 8) =
+                *reinterpret_cast<uint2*>(sm + kPfQB + pf_chunk(16 * (warp - 2) + i, lane >> 1) + (lane & 1) * 8) =
                     raw[i];
         }
         fence_proxy_async_smem();
@@ -578,13 +603,12 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             if (vm > 0.f && vm <= FLT_MAX) frexpf(vm, &E);  // vm < 2^E
         }
         {
-            const uint32_t t_q = tmem + ((uint32_t)(32 * qd) << 16) + 384 + 64 * hf;
             pf_wait(rot_done, 0, abort_f, status);
             __syncwarp();
             tc_fence_after();
             uint32_t y0[32], y1[32];
-            tmem_ld32(t_q, y0);
-            tmem_ld32(t_q + 32, y1);
+            tmem_ld32(t_lane + kPfTO + 64 * hf, y0);
+            tmem_ld32(t_lane + kPfTO + 64 * hf + 32, y1);
             tmem_wait_ld();
             float y[64];
             float a = 0.f;
@@ -595,7 +619,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                 a = fmaxf(a, fmaxf(fabsf(y[i]), fabsf(y[32 + i])));
             }
             red[hf * 128 + r] = a;
-            pf_softmax_sync();  // every thread's rows are read, and the product is done: the Q region is free
+            pf_softmax_sync();
             a = fmaxf(red[r], red[128 + r]);
             int e = 0;
             if (a > 0.f && a <= FLT_MAX) {
@@ -603,48 +627,43 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                 e = min(100, max(-100, ex - 14));
             }
             const float inv = pf_pow2(-e);  // exact scaling by a power of two
+            uint32_t qh[32], ql[32];  // dims 64 hf + 2 u, + 1 as fp16 pairs
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t h[4], l[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float v0 = y[8 * c + 2 * k] * inv, v1 = y[8 * c + 2 * k + 1] * inv;
-                    const __half2 hh2 = __floats2half2_rn(v0, v1);
-                    const float2 hf2 = __half22float2(hh2);
-                    const __half2 ll2 = __floats2half2_rn(v0 - hf2.x, v1 - hf2.y);
-                    h[k] = *reinterpret_cast<const uint32_t*>(&hh2);
-                    l[k] = *reinterpret_cast<const uint32_t*>(&ll2);
-                }
-                const uint32_t off = pf_chunk(r, 8 * hf + c);
-                *reinterpret_cast<uint4*>(sm + kPfQH + off) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(sm + kPfQL + off) = make_uint4(l[0], l[1], l[2], l[3]);
+            for (int u = 0; u < 32; ++u) {
+                const float v0 = y[2 * u] * inv, v1 = y[2 * u + 1] * inv;
+                const __half2 hh2 = __floats2half2_rn(v0, v1);
+                const float2 hf2 = __half22float2(hh2);
+                const __half2 ll2 = __floats2half2_rn(v0 - hf2.x, v1 - hf2.y);
+                qh[u] = *reinterpret_cast<const uint32_t*>(&hh2);
+                ql[u] = *reinterpret_cast<const uint32_t*>(&ll2);
             }
+            tmem_st32(t_lane + kPfTQ + 32 * hf, qh);
+            tmem_st32(t_lane + kPfTQ + 64 + 32 * hf, ql);
+            tmem_wait_st();
             if (hf == 0) qx_s[r] = rvalid ? pf_pow2(e) : 0.f;
         }
-        fence_proxy_async_smem();
+        tc_fence_before();
         pf_softmax_sync();
         if (lane == 0) mbar_arrive(q_full);
         const float qx = qx_s[r];
 
-        const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
         const int64_t pos = qs + tok;  // this row attends [0, pos]
         const float qxs = rvalid ? qx : 1.f;
         const float inv2E = ldexpf(1.f, -E);
         const F2 QX = f2(qxs, qxs), IE = f2(inv2E, inv2E);
         float m = -INFINITY, l = 0.f;  // reference max (s' units) and this half's sum
-        int bb = 0, bph = 0;           // tensor-memory buffer of block j and its phase
         for (int j = 0; j < nblk; ++j) {
-            const int s = j & 1;
+            const int s = j & 1, ph = (j >> 1) & 1;
             const int64_t t0 = (int64_t)j * kPfBlock;
             const int nv = kv_end - t0 < kPfBlock ? (int)(kv_end - t0) : kPfBlock;
-            pf_wait(&vfull[s], (j >> 1) & 1, abort_f, status);  // the norms of the block
-            pf_wait(&s_full[bb], bph, abort_f, status);
+            pf_wait(&vfull[s], ph, abort_f, status);  // the norms of the block
+            pf_wait(&s_full[s], ph, abort_f, status);
             __syncwarp();
             tc_fence_after();
             const unsigned char* stg = sm + kPfVS + s * kPfVStage - kPfImgV;  // image offsets
             const float* kn = reinterpret_cast<const float*>(stg + kPfImgKN) + 64 * hf;
             const float2* vn2 = reinterpret_cast<const float2*>(stg + kPfImgVN) + 32 * hf;
-            const uint32_t t_buf = t_lane + 128 * bb + 64 * hf;
+            const uint32_t t_buf = t_lane + 128 * s + 64 * hf;
             // s' = S |k| per column; the row's scores in log2 units are s' qx
             // (qx > 0), so the max is kept in s' units and p = exp2(s' qx - m qx).
             // Columns inside the row's range for the whole half skip the mask.
@@ -687,19 +706,18 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             const bool rescale = move && m != -INFINITY;  // O holds earlier blocks: scale it
             if (__any_sync(0xFFFFFFFFu, rescale)) {
                 // the PV product of block j - 1 is the last one that wrote O
-                const int jp = j - 1;
-                pf_wait(&pv_done[jp % 3], (jp / 3) & 1, abort_f, status);
+                pf_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_f, status);
                 __syncwarp();
                 tc_fence_after();
                 const float alpha = rescale ? pf_exp2((m - m_new) * qxs) : 1.f;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(t_lane + 384 + 64 * hf + 32 * c, o);
+                    tmem_ld32(t_lane + kPfTO + 64 * hf + 32 * c, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(t_lane + 384 + 64 * hf + 32 * c, o);
+                    tmem_st32(t_lane + kPfTO + 64 * hf + 32 * c, o);
                 }
                 if (rescale) l *= alpha;
             }
@@ -707,7 +725,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             const float nmq = m == -INFINITY ? 0.f : -m * qxs;  // masked columns: exp2(-inf) = 0
             const F2 NMQ = f2(nmq, nmq);
             F2 LB = f2(0.f, 0.f);
-            uint32_t ph[32];  // P of positions 64 hf + 2 u, + 1 as fp16 pairs
+            uint32_t ph2[32], pl2[32];  // P of positions 64 hf + 2 u, + 1 as fp16 pairs
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 float a0, a1;
@@ -718,9 +736,13 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
                 float w0, w1;
                 f2_split(f2_mul(pp, f2_mul(f2(vv.x, vv.y), IE)), w0, w1);
                 const __half2 hh2 = __floats2half2_rn(w0, w1);
-                ph[u] = *reinterpret_cast<const uint32_t*>(&hh2);
+                const float2 hf2 = __half22float2(hh2);
+                const __half2 ll2 = __floats2half2_rn(w0 - hf2.x, w1 - hf2.y);
+                ph2[u] = *reinterpret_cast<const uint32_t*>(&hh2);
+                pl2[u] = *reinterpret_cast<const uint32_t*>(&ll2);
             }
-            tmem_st32(t_buf, ph);
+            tmem_st32(t_buf, ph2);
+            tmem_st32(t_buf + 32, pl2);
             tmem_wait_st();
             {
                 float lb0, lb1;
@@ -729,11 +751,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[bb]);
-            if (++bb == 3) {
-                bb = 0;
-                bph ^= 1;
-            }
+            if (lane == 0) mbar_arrive(&p_full[s]);
         }
 
         // ---- epilogue: normalise (the row's sum over its two halves) and
@@ -741,16 +759,16 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
         // row is the butterflies over bits 0-5 (a thread's half, in
         // registers) and over bit 6 (between the two threads of the row,
         // through shared memory laid out [half][element / 4][row] in float4;
-        // the Q region, free once the last product is done).
+        // the K stages, free once the last product is done).
         float O[64];
         if (nblk > 0) {
             const int jl = nblk - 1;
-            pf_wait(&pv_done[jl % 3], (jl / 3) & 1, abort_f, status);
+            pf_wait(&pv_done[jl & 1], (jl >> 1) & 1, abort_f, status);
             __syncwarp();
             tc_fence_after();
             uint32_t o0[32], o1[32];
-            tmem_ld32(t_lane + 384 + 64 * hf, o0);
-            tmem_ld32(t_lane + 384 + 64 * hf + 32, o1);
+            tmem_ld32(t_lane + kPfTO + 64 * hf, o0);
+            tmem_ld32(t_lane + kPfTO + 64 * hf + 32, o1);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -771,7 +789,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             for (int i = 0; i < 64; ++i) O[i] = __uint_as_float(__float_as_uint(O[i]) ^ P.sgn2[64 * hf + i]);
         }
         fwht_reg2<64>(O);
-        float4* xs = reinterpret_cast<float4*>(sm + kPfQH);
+        float4* xs = reinterpret_cast<float4*>(sm + kPfKS);
 #pragma unroll
         for (int i = 0; i < 16; ++i) xs[(hf * 16 + i) * 128 + r] = make_float4(O[4 * i], O[4 * i + 1], O[4 * i + 2], O[4 * i + 3]);
         pf_softmax_sync();
@@ -782,14 +800,12 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
 #pragma unroll
             for (int k = 0; k < 4; ++k) O[4 * i + k] = hf ? oo[k] - O[4 * i + k] : O[4 * i + k] + oo[k];  // (lo + hi, lo - hi)
         }
-        pf_softmax_sync();  // the exchange is read: the Q region takes the output tile
+        pf_softmax_sync();  // the exchange is read: the K stages take the output tile
         // The output tile, row-major with rows kPfOutStride bytes apart (512
         // bytes of data and 16 of padding, so the per-row writes hit distinct
-        // banks), from the start of shared memory: the Q region and the K
-        // stages are free once the last product is done.  Lanes 0-15 of each
-        // softmax warp then send 16 rows with one bulk store each, and wait only
-        // until shared memory has been read.
-        unsigned char* ot = sm + kPfQH;
+        // banks).  Lanes 0-15 of each softmax warp then send 16 rows with one
+        // bulk store each, and wait only until shared memory has been read.
+        unsigned char* ot = sm + kPfKS;
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
             const int jd = 64 * hf + i;
@@ -807,7 +823,7 @@ k_attn_prefill(const __nv_bfloat16* __restrict__ q, const unsigned char* __restr
             const int gr = mt * kPfRows + rr;
             if (gr < rows_total) {
                 const int tk = gr / G, hd = gr - tk * G;
-                pf_bulk_store(out + (((int64_t)b * T + tk) * Hq + g * G + hd) * 128, sa + kPfQH + rr * kPfOutStride,
+                pf_bulk_store(out + (((int64_t)b * T + tk) * Hq + g * G + hd) * 128, sa + kPfKS + rr * kPfOutStride,
                               512);
                 bulk_commit();
                 bulk_wait_read<0>();

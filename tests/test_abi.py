@@ -256,9 +256,9 @@ def test_prefill_call_validation_before_launch(L):
     assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(1.0), A, A, 16, None) == 5
     assert L.tq_attn_prefill(h, A, 1, 8, 8, 2, cv, A, 4, 3, f(float("nan")), A, A, W, None) == 1
     assert L.tq_attn_prefill(h, None, 0, 8, 8, 2, cv, None, 4, 3, f(1.0), None, None, 0, None) == 0
-    # the 32 KB rotation matrix, then a 66560-byte tile image and a float per 128 positions per
+    # the 32 KB rotation matrix, then a 99328-byte tile image and a float per 128 positions per
     # (sequence, KV head), 16-byte rounded
-    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 300, 128) == 32768 + 2 * 2 * 3 * 66560 + 48
-    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 256, 128) == 32768 + 2 * 2 * 2 * 66560 + 32
+    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 300, 128) == 32768 + 2 * 2 * 3 * 99328 + 48
+    assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 256, 128) == 32768 + 2 * 2 * 2 * 99328 + 32
     assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 300, 64) == 0
     assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 9, 128) == 0   # cap < T

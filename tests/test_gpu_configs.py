@@ -121,6 +121,45 @@ def test_long_context_dense_and_sparse_full_size():
     print("long context", res)
 
 
+@pytest.mark.parametrize("B,T,q_start", [(1, 2048, 0), (4, 512, 4096)])
+def test_prefill_attention_full_size(B, T, q_start):
+    """Prefill attention at the sizes the bench times: 32 query / 8 KV heads,
+    d 128, K4/V3, rows low-rank + diag drawn as the bench draws them; a fresh
+    2048-token prompt, and 4 x 512 tokens after 4096 cached.  For two
+    sampled (sequence, KV head) groups the oracle encodes the raw rows it
+    reads back and computes every token of the chunk for the group's query
+    heads."""
+    d, Hq, Hkv, kb, vb = 128, 32, 8, 4, 3
+    G = Hq // Hkv
+    cap = q_start + T
+    plan = abi.Plan(d, 42)
+    s = O.signs(42, d)
+    cache = abi.Cache.empty(B, Hkv, cap, d, kb, vb)
+    rows = B * Hkv * cap
+    raw = {}
+    for side, bits, pk, nm, stream in (("k", kb, cache.k_packed, cache.k_norm, 40000),
+                                       ("v", vb, cache.v_packed, cache.v_norm, 41000)):
+        x = synth.lowrank_rows(95, rows, d, stream=stream, device="cuda")
+        raw[side] = x.view(B, Hkv, cap, d)
+        abi.tq_encode(plan, bits, x, pk.view(-1, d * bits // 8), nm.view(-1))
+    q = synth.device_normal(96, (B, T, Hq, d))
+    qs = torch.full((B,), q_start, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    out = abi.tq_attn_prefill(plan, q, cache, qs, scale)
+    torch.cuda.synchronize()
+    assert abi.tq_device_status(reset=True) == 0
+    worst = 0.0
+    for b, h in [(0, 0), (B - 1, Hkv - 1)]:
+        kp, kn = O.encode(s, kb, raw["k"][b, h].double().cpu().numpy())
+        vp, vn = O.encode(s, vb, raw["v"][b, h].double().cpu().numpy())
+        qq = q[b:b + 1, :, h * G:(h + 1) * G].double().cpu().numpy()
+        want = O.attention_prefill(s, qq, kp[None, None], kn[None, None], vp[None, None], vn[None, None], kb, vb,
+                                   np.array([q_start], np.int32), scale)
+        got = out[b:b + 1, :, h * G:(h + 1) * G].cpu().numpy()
+        worst = max(worst, compare_attention(got, want)["max_abs_err"])
+    print("prefill", B, T, q_start, "max abs err", worst)
+
+
 def test_gemma_window_encode_and_append_loop():
     """34 layers x 4 KV heads x d 256: full 512-token window written with
     tq_append (512 new rows per head) and tq_encode, then 50 single-token
