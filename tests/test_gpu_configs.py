@@ -160,6 +160,41 @@ def test_prefill_attention_full_size(B, T, q_start):
     print("prefill", B, T, q_start, "max abs err", worst)
 
 
+def test_decode_attention_moderate_context_outliers():
+    """Decode attention (batch 1, 32 query / 8 KV heads, K4/V3) on the
+    bench's low-rank rows with x8 outlier channels, at contexts from 17 to
+    2048: few rows per softmax, so the outputs stay close to raw V values
+    and the keys' fp16 rounding is least averaged.  Four queries per context,
+    all eight groups, against the oracle's own encoding of the raw rows."""
+    d, Hq, Hkv, kb, vb, cap = 128, 32, 8, 4, 3, 2048
+    G = Hq // Hkv
+    plan = abi.Plan(d, 42)
+    s = O.signs(42, d)
+    cache = abi.Cache.empty(1, Hkv, cap, d, kb, vb)
+    enc = {}
+    for side, bits, pk, nm, stream in (("k", kb, cache.k_packed, cache.k_norm, 40000),
+                                       ("v", vb, cache.v_packed, cache.v_norm, 41000)):
+        x = synth.lowrank_rows(95, Hkv * cap, d, stream=stream, device="cuda")
+        abi.tq_encode(plan, bits, x, pk.view(-1, d * bits // 8), nm.view(-1))
+        xs = x.view(Hkv, cap, d)
+        for h in range(Hkv):
+            enc[(side, h)] = O.encode(s, bits, xs[h].double().cpu().numpy())
+    worst = 0.0
+    for ctx in (17, 100, 300, 700, 1184, 1600, 2048):
+        for trial in range(4):
+            q = synth.device_normal(500 + trial, (1, Hq, d))
+            out = abi.tq_attn_decode(plan, q, cache, ctx, 1.0 / math.sqrt(d), 0.0)
+            torch.cuda.synchronize()
+            for h in range(Hkv):
+                (kp, kn), (vp, vn) = enc[("k", h)], enc[("v", h)]
+                qq = q[:, h * G:(h + 1) * G].double().cpu().numpy()
+                want = O.attention(s, qq, kp[None, None], kn[None, None], vp[None, None], vn[None, None], kb, vb,
+                                   ctx, 1.0 / math.sqrt(d), 0.0)
+                got = out[:, h * G:(h + 1) * G].cpu().numpy()
+                worst = max(worst, compare_attention(got, want)["max_abs_err"])
+    print("decode moderate contexts, outliers: max abs err", worst)
+
+
 def test_gemma_window_encode_and_append_loop():
     """34 layers x 4 KV heads x d 256: full 512-token window written with
     tq_append (512 new rows per head) and tq_encode, then 50 single-token
