@@ -1096,65 +1096,80 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 }
 
 // Merge the partials of one (batch, query head) (m in log2 units), normalise
-// and rotate back: out = s . (H o) / sqrt(d).  Thread j owns dim j.  The
-// partials' maxima and weights are computed 128 at a time in parallel and
-// kept in shared memory, so the accumulation issues independent, coalesced
-// loads instead of a dependent chain per partial.
-__device__ __forceinline__ float block128_max(float v, float* red) {
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-}
-__device__ __forceinline__ float block128_sum(float v, float* red) {
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    return (red[0] + red[1]) + (red[2] + red[3]);
-}
-
-static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_splits,
+// and rotate back: out = s . H (s2 . o) / sqrt(d).  One warp per (batch,
+// query head), eight per block; lane l owns dims 2l, 2l + 1, 64 + 2l and
+// 65 + 2l (8-byte loads: a partial row is 130 floats).  The butterflies
+// over index bits 0 and 6 are in registers, those over bits 1-5 between
+// lanes, in the order len = 1, 2, .., 64.
+static __global__ void __launch_bounds__(256) k_attn3_combine(const float* __restrict__ part, int n_splits,
                                                               int grid, int64_t n_items, int Hq, int Hkv,
-                                                              float* __restrict__ out,
+                                                              int64_t n_bh, float* __restrict__ out,
                                                               const __grid_constant__ AttnParams P,
                                                               bool paged, const A3Meta meta) {
-    __shared__ float o[128];
-    __shared__ float f[128];
-    __shared__ float red[4];
-    const int bh = blockIdx.x, j = threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (bh >= n_bh) return;  // past the last (batch, query head): the whole warp
     // partials of this (batch, query head): one per CTA whose items reach its KV head
-    const int64_t bhk = (int64_t)(bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
+    const int64_t bhk = (bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
     const int n_parts = paged ? meta.slot_base[meta.clast[bhk]] - meta.slot_base[meta.c0[bhk]] + 1
                               : attn3_cta_of((bhk + 1) * n_splits - 1, grid, n_items) -
                                     attn3_cta_of(bhk * n_splits, grid, n_items) + 1;
-    const float* base = part + (int64_t)bh * n_splits * 130;
+    const float* base = part + bh * n_splits * 130;
     float M = -INFINITY;
-    for (int s = j; s < n_parts; s += 128) M = fmaxf(M, base[s * 130 + 128]);
-    M = block128_max(M, red);
-    float a = 0.f, lsum = 0.f;
-    for (int s0 = 0; s0 < n_parts; s0 += 128) {
-        const int s = s0 + j;
-        float w = 0.f;
-        if (s < n_parts) {
-            const float ms = base[s * 130 + 128];
-            w = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-            lsum = fmaf(w, base[s * 130 + 129], lsum);
-        }
-        f[j] = w;
-        __syncthreads();
-        const int cnt = min(128, n_parts - s0);
-        const float* col = base + (int64_t)s0 * 130 + j;
+    for (int s = lane; s < n_parts; s += 32) M = fmaxf(M, __ldg(base + s * 130 + 128));
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
-        for (int k = 0; k < cnt; ++k) a = fmaf(f[k], col[k * 130], a);
-        __syncthreads();
+    for (int s = 0; s < n_parts; ++s) {  // unrolled: the loads of several partials in flight
+        const float* row = base + s * 130;
+        const float ms = __ldg(row + 128);
+        const float w = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
+        L = fmaf(w, __ldg(row + 129), L);
+        const float2 x = __ldg(reinterpret_cast<const float2*>(row) + lane);
+        const float2 y = __ldg(reinterpret_cast<const float2*>(row + 64) + lane);
+        a0 = fmaf(w, x.x, a0);
+        a1 = fmaf(w, x.y, a1);
+        a2 = fmaf(w, y.x, a2);
+        a3 = fmaf(w, y.y, a3);
     }
-    const float L = block128_sum(lsum, red);
-    o[j] = L > 0.f ? a / L : 0.f;  // an empty context (paged, length 0) gives zeros
-    if (P.two_sided) o[j] = __uint_as_float(__float_as_uint(o[j]) ^ P.sgn2[j]);
-    fwht_smem<128>(o, 1);
-    out[(int64_t)bh * 128 + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
+    // an empty context (paged, length 0) gives zeros
+    float v[4] = {L > 0.f ? a0 / L : 0.f, L > 0.f ? a1 / L : 0.f, L > 0.f ? a2 / L : 0.f, L > 0.f ? a3 / L : 0.f};
+    const int dim[4] = {2 * lane, 2 * lane + 1, 64 + 2 * lane, 65 + 2 * lane};
+    if (P.two_sided) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = __uint_as_float(__float_as_uint(v[k]) ^ P.sgn2[dim[k]]);
+    }
+    {  // index bit 0
+        const float p0 = v[0] + v[1], p1 = v[0] - v[1], p2 = v[2] + v[3], p3 = v[2] - v[3];
+        v[0] = p0;
+        v[1] = p1;
+        v[2] = p2;
+        v[3] = p3;
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {  // index bits 1-5: lane bits 0-4
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[k], m);
+            v[k] = upper ? o - v[k] : v[k] + o;  // (lo + hi, lo - hi)
+        }
+    }
+    {  // index bit 6
+        const float p0 = v[0] + v[2], p2 = v[0] - v[2], p1 = v[1] + v[3], p3 = v[1] - v[3];
+        v[0] = p0;
+        v[1] = p1;
+        v[2] = p2;
+        v[3] = p3;
+    }
+    float* o = out + bh * 128;
+    float2 r0, r1;
+    r0.x = __uint_as_float(__float_as_uint(v[0] * P.inv_sqrt_d) ^ P.sgn[dim[0]]);
+    r0.y = __uint_as_float(__float_as_uint(v[1] * P.inv_sqrt_d) ^ P.sgn[dim[1]]);
+    r1.x = __uint_as_float(__float_as_uint(v[2] * P.inv_sqrt_d) ^ P.sgn[dim[2]]);
+    r1.y = __uint_as_float(__float_as_uint(v[3] * P.inv_sqrt_d) ^ P.sgn[dim[3]]);
+    reinterpret_cast<float2*>(o)[lane] = r0;
+    reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }
 
 template <int KB, int VB, int NG, bool PAGED>
@@ -1244,7 +1259,8 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
         e = attn3_split_launch<KB, VB, 2, PAGED>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P,
                                                  pa, meta, s);
     if (e != cudaSuccess) return e;
-    k_attn3_combine<<<B * Hq, 128, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv, out, P, PAGED, meta);
+    k_attn3_combine<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv,
+                                                                           (int64_t)B * Hq, out, P, PAGED, meta);
     return cudaGetLastError();
 }
 
