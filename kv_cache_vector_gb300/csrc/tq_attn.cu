@@ -413,11 +413,73 @@ __device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__
     rotate_q_row(q + bh * 128, q16 + bh * 256, qexp + bh, P);
 }
 
-static __global__ void __launch_bounds__(128) k_attn3_q(const __nv_bfloat16* __restrict__ q,
+// The same rotation with one warp per (batch, head), eight per block: lane l
+// holds elements 4 l .. 4 l + 3, the butterflies over index bits 0 and 1 are
+// in registers and those over bits 2-6 between lanes, in the order len = 1,
+// 2, .., 64, and the scale and the fp16 parts are those of rotate_q_row.
+static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __restrict__ q,
                                                         __half* __restrict__ q16,
                                                         float* __restrict__ qexp,
-                                                        const __grid_constant__ AttnParams P) {
-    attn3_rotate_q(q, q16, qexp, P);
+                                                        const __grid_constant__ AttnParams P, int64_t n_rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (bh >= n_rows) return;  // the whole warp
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + bh * 128) + lane);
+    float x[4];
+    {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = c.x;
+        x[3] = c.y;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(__float_as_uint(x[k]) ^ P.sgn[4 * lane + k]);
+    {
+        const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
+        x[0] = a0 + a2;
+        x[1] = a1 + a3;
+        x[2] = a0 - a2;
+        x[3] = a1 - a3;
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, x[k], m);
+            x[k] = upper ? o - x[k] : x[k] + o;  // (lo + hi, lo - hi)
+        }
+    }
+    float M = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u)) * P.q_mul;
+        M = fmaxf(M, fabsf(x[k]));
+    }
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    int e = 0;
+    if (M > 0.f && M <= FLT_MAX) {
+        int ex = 0;
+        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
+        e = min(100, max(-100, ex - 14));
+    }
+    __half hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float ys = ldexpf(x[k], -e);
+        hi[k] = __float2half_rn(ys);
+        lo[k] = __float2half_rn(ys - __half2float(hi[k]));
+    }
+    __half* row = q16 + bh * 256;
+    *reinterpret_cast<uint2*>(row + 4 * lane) =
+        make_uint2((uint32_t)__half_as_ushort(hi[0]) | ((uint32_t)__half_as_ushort(hi[1]) << 16),
+                   (uint32_t)__half_as_ushort(hi[2]) | ((uint32_t)__half_as_ushort(hi[3]) << 16));
+    *reinterpret_cast<uint2*>(row + 128 + 4 * lane) =
+        make_uint2((uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16),
+                   (uint32_t)__half_as_ushort(lo[2]) | ((uint32_t)__half_as_ushort(lo[3]) << 16));
+    if (lane == 0) qexp[bh] = ldexpf(1.f, e);
 }
 
 // The query rotation of the paged attention with the decode step's append
@@ -1227,7 +1289,8 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
                                                           *app->PK, *app->PV, KB, VB, len1, status_word());
         pa.lens = len1;
     } else {
-        k_attn3_q<<<B * Hq, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16, qexp, P);
+        k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16,
+                                                                       qexp, P, (int64_t)B * Hq);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
