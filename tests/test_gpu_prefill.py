@@ -109,3 +109,54 @@ def test_prefill_out_of_range_start():
     want = O.attention_prefill(s, q[:1].double().numpy(), *(a[:1] for a in arrs), kb, vb,
                                np.array([10], np.int32), 0.09)
     compare_attention(got[:1], want)
+
+
+def _sweep_cases(n, seed):
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for _ in range(n):
+        B = rng.choice([1, 2, 3])
+        G = rng.choice([1, 2, 4, 8])
+        Hkv = rng.choice([1, 2]) if G == 8 else rng.choice([1, 2, 4])
+        T = rng.choice([1, 7, 33, 128, 129, 255, 300])
+        starts = [rng.choice([0, 1, 63, 127, 128, 200, 400]) for _ in range(B)]
+        cap = max(starts) + T + rng.choice([0, 1, 5, 130])
+        flags = rng.choice([0, 0, abi.PLAN_TWO_SIDED_SIGNS, abi.PLAN_GAUSSIAN_CODEBOOK | abi.PLAN_TWO_SIDED_SIGNS])
+        cases.append((B, T, G * Hkv, Hkv, starts, cap, rng.choice([2, 3, 4]), rng.choice([2, 3, 4]), flags,
+                      rng.random() < 0.5))
+    return cases
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,q_start,cap,kb,vb,flags,lowrank", _sweep_cases(10, 1234))
+def test_prefill_seeded_sweep(B, T, Hq, Hkv, q_start, cap, kb, vb, flags, lowrank):
+    """Seeded draws over batch, chunk length, group size, start positions
+    (including a last position at the capacity), bit widths, format variants,
+    and N(0,1) or low-rank rows with x8 outlier channels."""
+    d = 128
+    plan = abi.Plan(d, 42, flags)
+    s = O.signs(42, d)
+    s2 = O.signs2(42, d) if flags & abi.PLAN_TWO_SIDED_SIGNS else None
+    kind = "gauss" if flags & abi.PLAN_GAUSSIAN_CODEBOOK else "sphere"
+    n = B * Hkv * cap
+    seed = 700 + T + cap
+    if lowrank:
+        kx = synth.lowrank_rows(seed, n, d, stream=1).double().numpy()
+        vx = synth.lowrank_rows(seed, n, d, stream=2).double().numpy()
+    else:
+        kx = synth.normal_rows(seed, n, d, torch.bfloat16, stream=1).double().numpy()
+        vx = synth.normal_rows(seed, n, d, torch.bfloat16, stream=2).double().numpy()
+    kp, kn = O.encode(s, kb, kx, s2=s2, kind=kind)
+    vp, vn = O.encode(s, vb, vx, s2=s2, kind=kind)
+    shp = (B, Hkv, cap)
+    arrs = (kp.reshape(*shp, -1), kn.reshape(shp), vp.reshape(*shp, -1), vn.reshape(shp))
+    cache = abi.Cache(*(torch.from_numpy(a).cuda() for a in arrs), kb, vb)
+    q = synth.normal_rows(seed + 1, B * T * Hq, d, torch.bfloat16, stream=3).reshape(B, T, Hq, d)
+    qs = torch.tensor(q_start, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    out = abi.tq_attn_prefill(plan, q.cuda(), cache, qs, scale)
+    torch.cuda.synchronize()
+    assert abi.tq_device_status(reset=True) == 0
+    want = O.attention_prefill(s, q.double().numpy(), *arrs, kb, vb, np.array(q_start, np.int32), scale, s2=s2,
+                               kind=kind)
+    compare_attention(out.cpu().numpy(), want)
