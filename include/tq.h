@@ -198,13 +198,18 @@ tq_status tq_attn_decode(const tq_plan *plan, const void *q, int B, int Hq, int 
  * counterpart of it.
  *   Scratch: a fixed device array of 8 MiB inside the library (every GPU
  *   that loads the library holds it until the process exits).  If the split-K
- *   partials for these sizes need more than that (compare
- *   tq_attn_workspace_bytes with 8388608), the call returns TQ_ERR_WORKSPACE
- *   and launches nothing.  No part of the scratch needs to start at zero:
- *   each call writes every partial before it reads it.
+ *   partials for these sizes and bit widths need more than that, the call
+ *   returns TQ_ERR_WORKSPACE and launches nothing.  tq_attn_workspace_bytes
+ *   is an upper bound over all bit widths: a result <= 8388608 guarantees
+ *   the sizes fit; a larger one may still fit for the widths of the call.
+ *   No part of the scratch needs to start at zero: each call writes every
+ *   partial before it reads it.
  *   Set-up: the first call on a device looks up the array's device address
- *   (with that device current) and caches it; make that first call before
- *   any stream capture on that device.
+ *   (with that device current) and caches it for the life of the process;
+ *   make that first call before any stream capture on that device.  A
+ *   cudaDeviceReset reloads the library's device code and leaves that cached
+ *   address (and the one of the tq_device_status word) stale: make no call
+ *   of this library on a device after resetting it.
  *   All calls on a device share the one array: calls whose kernels overlap on
  *   the GPU (different streams, or concurrent host threads) race and produce
  *   wrong results.  Serialise them, e.g. on one stream.

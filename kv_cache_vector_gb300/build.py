@@ -62,7 +62,7 @@ def _compile(unit, verbose: bool) -> str:
            "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
     for k, v in defs.items():
         cmd.insert(1, f"-DTQ_UNIT_{k}={v}")
-    # implementation selectors, e.g. TQ_NVCC_DEFINES="TQ_ENCODE_TCGEN05=1"
+    # extra preprocessor definitions, space separated (TQ_NVCC_DEFINES="A=1 B")
     for d in os.environ.get("TQ_NVCC_DEFINES", "").split():
         cmd.insert(1, f"-D{d}")
     if src.endswith(".cu"):

@@ -294,6 +294,51 @@ void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, fl
     A.out_mul = (float)(1.0 / vs);
 }
 
+tq_status tq::check_attn_decode_args(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                                     const tq_cache_view& cache, int64_t ctx_len, int k_bits, int v_bits,
+                                     float scale, float sparse_v_threshold, const float* out, bool* nothing) {
+    *nothing = false;
+    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0) return TQ_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return TQ_ERR_INVALID_ARG;
+    if (!valid_bits(k_bits) || !valid_bits(v_bits)) return TQ_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 8) return TQ_ERR_UNSUPPORTED;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (P->d < 32) return TQ_ERR_UNSUPPORTED;
+    if (!(std::isfinite(scale)) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
+        return TQ_ERR_INVALID_ARG;
+    if (ctx_len < 1 || ctx_len > cache.cap) return TQ_ERR_RANGE;
+    if (B == 0) {
+        *nothing = true;
+        return TQ_OK;
+    }
+    if (!q || !out || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
+        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
+        return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(cache.k_packed) ||
+        !device_accessible(cache.v_packed) || !device_accessible(cache.k_norm) ||
+        !device_accessible(cache.v_norm))
+        return TQ_ERR_INVALID_ARG;
+    return TQ_OK;
+}
+
+cudaError_t tq::launch_attn_decode(const Plan& P, const void* q, int B, int Hq, int Hkv,
+                                   const tq_cache_view& cache, int64_t ctx_len, int k_bits, int v_bits,
+                                   float scale, float sparse_v_threshold, float* out, void* workspace,
+                                   const AttnGeometry& g, cudaStream_t st) {
+    tq::AttnParams A;
+    tq::fill_attn_params(P, k_bits, v_bits, scale, sparse_v_threshold, A);
+    return dispatch_attn_d(P.d, [&](auto D) {
+        constexpr int d = decltype(D)::value;
+        switch (k_bits) {
+            case 2: return tq::launch_attn_dk<d, 2>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+            case 3: return tq::launch_attn_dk<d, 3>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+            default: return tq::launch_attn_dk<d, 4>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
+        }
+    });
+}
+
 extern "C" {
 
 tq_status tq_codebook_init(int d, int bits, double* centroids, double* boundaries) {
@@ -460,40 +505,18 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
                          tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
                          float scale, float sparse_v_threshold, float* out, void* workspace,
                          size_t workspace_bytes, tq_stream_t stream) {
-    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0) return TQ_ERR_INVALID_ARG;
-    if (Hq % Hkv != 0) return TQ_ERR_INVALID_ARG;
-    if (!valid_bits(k_bits) || !valid_bits(v_bits)) return TQ_ERR_UNSUPPORTED;
-    if (Hq / Hkv > 8) return TQ_ERR_UNSUPPORTED;
+    bool nothing = false;
+    tq_status st = tq::check_attn_decode_args(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale,
+                                              sparse_v_threshold, out, &nothing);
+    if (st != TQ_OK || nothing) return st;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
-    if (P->d < 32) return TQ_ERR_UNSUPPORTED;
-    if (!(std::isfinite(scale)) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
-        return TQ_ERR_INVALID_ARG;
-    if (ctx_len < 1 || ctx_len > cache.cap) return TQ_ERR_RANGE;
-    if (B == 0) return TQ_OK;
-    if (!q || !out || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
-        return TQ_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
-        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
-        return TQ_ERR_ALIGNMENT;
-    tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
-    size_t need = tq::attn_workspace_bytes(B, Hq, P->d, g);
-    if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
+    if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
-    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(workspace) ||
-        !device_accessible(cache.k_packed) || !device_accessible(cache.v_packed) ||
-        !device_accessible(cache.k_norm) || !device_accessible(cache.v_norm))
-        return TQ_ERR_INVALID_ARG;
-    tq::AttnParams A;
-    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
-    cudaError_t e = dispatch_attn_d(P->d, [&](auto D) {
-        constexpr int d = decltype(D)::value;
-        auto st = reinterpret_cast<cudaStream_t>(stream);
-        switch (k_bits) {
-            case 2: return tq::launch_attn_dk<d, 2>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
-            case 3: return tq::launch_attn_dk<d, 3>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
-            default: return tq::launch_attn_dk<d, 4>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, A, st);
-        }
-    });
+    if (!device_accessible(workspace)) return TQ_ERR_INVALID_ARG;
+    const cudaError_t e = tq::launch_attn_decode(*P, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale,
+                                                 sparse_v_threshold, out, workspace, g,
+                                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 

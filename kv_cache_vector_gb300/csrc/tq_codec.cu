@@ -13,16 +13,6 @@
 #include "tq_device.cuh"
 #include "tq_umma.cuh"
 
-// The d = 128 bf16 encode runs its Walsh-Hadamard transform on the tensor
-// cores (tcgen05) when this is 1, on CUDA cores (TMA-fed kernel) when 0.
-#ifndef TQ_ENCODE_TCGEN05
-#define TQ_ENCODE_TCGEN05 1
-#endif
-// Likewise for the d = 128 bf16-output decode.
-#ifndef TQ_DECODE_TCGEN05
-#define TQ_DECODE_TCGEN05 0
-#endif
-
 namespace tq {
 namespace dev {
 
@@ -924,224 +914,6 @@ k_decode3(const uint8_t* __restrict__ packed, const float* __restrict__ norms, i
     if (lane == 0) bulk_wait<0>();
 }
 
-// ------------------------------------------- decode on tcgen05 (d = 128)
-//
-// X_hat = (C H) * diag(s) * n / sqrt(d) for a tile of 128 rows: C (centroid
-// values, row-major) times the +-1 Hadamard matrix on the tensor cores.  The
-// fp32 centroids (scaled by 64 so that the low part stays a normal fp16) are
-// split as hi + lo fp16, two MMAs per k-step, so C H carries ~22 bits.  Warp
-// roles: 0 = MMA issuer and tensor-memory owner, 1-4 = builders (one row per
-// thread: unpack, table lookup, write the hi/lo operand tiles), 5-8 =
-// epilogue (tensor memory -> scale, sign, bf16 -> swizzled staging -> 2-D TMA
-// store).
-
-constexpr int kDuRows = 128;
-constexpr int kDuStages = 2;
-constexpr int kDuThreads = 9 * 32;
-constexpr int kDuTile = kDuRows * 128 * 2;            // one fp16 operand tile
-constexpr int kDuSmemBytes = 1024 + kDuStages * 2 * kDuTile + kDuTile /*H*/ + 4 * 8192 /*staging*/ +
-                             (2 * kDuStages + 4) * 8 + 16;
-constexpr float kDuScale = 64.0f;
-
-template <int BITS>
-__global__ void __launch_bounds__(kDuThreads, 1)
-k_decode_umma(const uint8_t* __restrict__ packed, const float* __restrict__ norms, int64_t n_rows,
-              const __grid_constant__ CUtensorMap ymap, int* status, const __grid_constant__ RowParams P) {
-    constexpr int RB = 128 * BITS / 8, NW = RB / 4;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ uint32_t cen2[16];  // (hi | lo << 16) fp16 halves of 64 * centroid
-    unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    unsigned char* as = base;                                  // stages: [hi 32 KB][lo 32 KB]
-    unsigned char* hb = as + kDuStages * 2 * kDuTile;           // H, K-major
-    unsigned char* stage_out = hb + kDuTile;                    // 4 x 8 KB
-    uint64_t* afull = reinterpret_cast<uint64_t*>(stage_out + 4 * 8192);
-    uint64_t* aempty = afull + kDuStages;
-    uint64_t* accf = aempty + kDuStages;
-    uint64_t* acce = accf + 2;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(acce + 2);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x < 16) {
-        const float c = P.cen[threadIdx.x] * kDuScale;
-        const __half hi = __float2half_rn(c);
-        const __half lo = __float2half_rn(c - __half2float(hi));
-        cen2[threadIdx.x] = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
-    }
-    for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
-        const int n = i >> 7, k = i & 127;
-        const bool neg = (__popc(n & k) & 1) != 0;
-        const int off = (k >> 6) * 16384 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
-        *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBC00u : 0x3C00u;
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kDuStages; ++i) {
-            mbar_init(&afull[i], 4);
-            mbar_init(&aempty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&accf[i], 1);
-            mbar_init(&acce[i], 4);
-        }
-        mbar_fence_init();
-    }
-    fence_proxy_async_smem();
-    if (warp == 0) tmem_alloc<256>(slot);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *slot;
-    const int64_t n_tiles = (n_rows + kDuRows - 1) / kDuRows;
-
-    if (warp == 0) {  // ---- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16(128, 128, false);
-            const uint32_t as_a = smem_addr(as), hb_a = smem_addr(hb);
-            int it = 0;
-            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-                const int s = it % kDuStages, a = it & 1;
-                if (!mbar_wait(&afull[s], (it / kDuStages) & 1)) {
-                    report_timeout(status, 21);
-                    break;
-                }
-                if (it >= 2 && !mbar_wait(&acce[a], ((it >> 1) - 1) & 1)) {
-                    report_timeout(status, 22);
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t bd = umma_desc_sw128(hb_a + off);
-                    umma_f16(tmem + a * 128, umma_desc_sw128(as_a + s * 2 * kDuTile + off), bd, idesc,
-                             kk > 0 ? 1u : 0u);
-                    umma_f16(tmem + a * 128, umma_desc_sw128(as_a + s * 2 * kDuTile + kDuTile + off), bd,
-                             idesc, 1u);
-                }
-                umma_commit(&aempty[s]);
-                umma_commit(&accf[a]);
-            }
-            for (int j = (it > 2 ? it - 2 : 0); j < it; ++j)
-                if (!mbar_wait(&accf[j & 1], (j >> 1) & 1)) {
-                    report_timeout(status, 23);
-                    break;
-                }
-        }
-    } else if (warp <= 4) {  // ---- builders: one row per thread
-        const int r = 32 * (warp - 1) + lane;
-        const char* cb = reinterpret_cast<const char*>(cen2);
-        int it = 0;
-        uint32_t wn[NW];
-        auto fetch = [&](int64_t tl) {
-            const int64_t row = tl * kDuRows + r;
-            if (tl < n_tiles && row < n_rows) load_bytes<RB>(packed + row * RB, wn);
-            else
-#pragma unroll
-                for (int k = 0; k < NW; ++k) wn[k] = 0;
-        };
-        fetch(blockIdx.x);
-        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-            const int s = it % kDuStages;
-            uint32_t w[NW];
-#pragma unroll
-            for (int k = 0; k < NW; ++k) w[k] = wn[k];
-            fetch(tile + gridDim.x);
-            if (it >= kDuStages && !mbar_wait(&aempty[s], ((it / kDuStages) - 1) & 1)) {
-                report_timeout(status, 24);
-                break;
-            }
-            unsigned char* hi_t = as + s * 2 * kDuTile;
-            unsigned char* lo_t = hi_t + kDuTile;
-            // 16 chunks of 8 columns: entries (hi | lo << 16) -> 4 hi pairs, 4 lo pairs
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint32_t e[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int i = 8 * c + m;
-                    const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
-                    uint32_t x;
-                    if (sh + BITS <= 32) x = w[wi] >> sh;
-                    else x = __funnelshift_r(w[wi], w[wi + 1], sh);
-                    e[m] = *reinterpret_cast<const uint32_t*>(cb + ((x << 2) & (((1u << BITS) - 1) << 2)));
-                    if (P.two_sided && P.sgn2[i]) e[m] ^= 0x80008000u;  // both fp16 halves
-                }
-                uint4 h, l;
-                h.x = __byte_perm(e[0], e[1], 0x5410); l.x = __byte_perm(e[0], e[1], 0x7632);
-                h.y = __byte_perm(e[2], e[3], 0x5410); l.y = __byte_perm(e[2], e[3], 0x7632);
-                h.z = __byte_perm(e[4], e[5], 0x5410); l.z = __byte_perm(e[4], e[5], 0x7632);
-                h.w = __byte_perm(e[6], e[7], 0x5410); l.w = __byte_perm(e[6], e[7], 0x7632);
-                const int off = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4*>(hi_t + off) = h;
-                *reinterpret_cast<uint4*>(lo_t + off) = l;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[s]);
-        }
-    } else {  // ---- epilogue warps 5-8: tensor-memory lane quarter q = warp & 3
-        const int q = warp & 3;
-        const int r = 32 * q + lane;
-        unsigned char* st = stage_out + q * 8192;
-        int it = 0;
-        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-            const int a = it & 1;
-            const int64_t row = tile * kDuRows + r;
-            const float nrm = row < n_rows ? __ldg(norms + row) : 0.f;
-            const float scs = nrm * P.inv_sqrt_d * (1.0f / kDuScale);
-            const F2 sc = f2(scs, scs);
-            if (!mbar_wait(&accf[a], (it >> 1) & 1)) {
-                report_timeout(status, 25);
-                break;
-            }
-            tc_fence_after();
-            if (lane == 0) bulk_wait_read<0>();  // staging free again
-            __syncwarp();
-            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + a * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t y[32];
-                tmem_ld32(ta + 32 * c, y);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k8 = 0; k8 < 4; ++k8) {  // 16-byte output chunk = 8 columns
-                    uint32_t qv[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int j = 8 * k8 + 2 * m;  // column within this 32-column slice
-                        const int col = 32 * c + j;
-                        float ax, ay;
-                        f2_split(f2_mul(f2(__uint_as_float(y[j]), __uint_as_float(y[j + 1])), sc), ax, ay);
-                        __nv_bfloat162 hv = __floats2bfloat162_rn(ax, ay);
-                        qv[m] = *reinterpret_cast<uint32_t*>(&hv) ^ ((P.sgn[col] >> 16) | P.sgn[col + 1]);
-                    }
-                    const int chunk = 4 * c + k8, half = chunk >> 3, cc = chunk & 7;
-                    *reinterpret_cast<uint4*>(st + half * 4096 + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
-                        make_uint4(qv[0], qv[1], qv[2], qv[3]);
-                }
-            }
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&acce[a]);
-                const int64_t row0 = tile * kDuRows + 32 * q;
-                if (row0 < n_rows) {
-                    tma_store_2d(&ymap, 0, (int)row0, st);
-                    tma_store_2d(&ymap, 64, (int)row0, st + 4096);
-                }
-                bulk_commit();
-            }
-        }
-        if (lane == 0) bulk_wait<0>();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc<256>(tmem);
-    }
-}
-
 }  // namespace dev
 
 // ---------------------------------------------------------------- launchers
@@ -1193,14 +965,18 @@ cudaError_t enc_umma(const void* x, int64_t n, uint8_t* pk, float* nm, const Row
 
 template <int D, int BITS, typename T>
 cudaError_t enc(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
-#if TQ_ENCODE_TCGEN05
-    if constexpr (D == 128 && sizeof(T) == 2) return enc_umma<BITS>(x, n, pk, nm, P, s);
-#endif
-    if constexpr ((D == 64 || D == 128) && sizeof(T) == 2) return enc_tma<D, BITS>(x, n, pk, nm, P, s);
-    auto fn = dev::k_encode<D, BITS, T>;
-    unsigned g = grid_for((const void*)fn, dev::kBlock, n * dev::RowShape<D>::R);
-    fn<<<g, dev::kBlock, 0, s>>>(static_cast<const T*>(x), n, pk, nm, P);
-    return cudaGetLastError();
+    // d = 128 bf16: the transform on the tensor cores; d = 64 bf16: TMA-fed
+    // CUDA-core butterflies; other shapes: one thread per row (two at d = 256)
+    if constexpr (D == 128 && sizeof(T) == 2) {
+        return enc_umma<BITS>(x, n, pk, nm, P, s);
+    } else if constexpr (D == 64 && sizeof(T) == 2) {
+        return enc_tma<D, BITS>(x, n, pk, nm, P, s);
+    } else {
+        auto fn = dev::k_encode<D, BITS, T>;
+        unsigned g = grid_for((const void*)fn, dev::kBlock, n * dev::RowShape<D>::R);
+        fn<<<g, dev::kBlock, 0, s>>>(static_cast<const T*>(x), n, pk, nm, P);
+        return cudaGetLastError();
+    }
 }
 
 template <int BITS>
@@ -1225,26 +1001,8 @@ cudaError_t dec3(const uint8_t* pk, const float* nm, int64_t n, void* y, const R
     return cudaGetLastError();
 }
 
-template <int BITS>
-cudaError_t dec_umma(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
-    CUtensorMap map;
-    cudaError_t e = make_rows_map(&map, y, 2, 128, (uint64_t)n, 32);
-    if (e != cudaSuccess) return e;
-    auto fn = dev::k_decode_umma<BITS>;
-    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kDuSmemBytes);
-    if (e != cudaSuccess) return e;
-    const int64_t tiles = (n + dev::kDuRows - 1) / dev::kDuRows;
-    int64_t grid = num_sms();
-    if (grid > tiles) grid = tiles;
-    fn<<<(unsigned)grid, dev::kDuThreads, dev::kDuSmemBytes, s>>>(pk, nm, n, map, status_word(), P);
-    return cudaGetLastError();
-}
-
 template <int D, int BITS, typename TO>
 cudaError_t dec(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
-#if TQ_DECODE_TCGEN05
-    if constexpr (D == 128 && sizeof(TO) == 2) return dec_umma<BITS>(pk, nm, n, y, P, s);
-#endif
     if constexpr (D == 128 && sizeof(TO) == 2) return dec3<BITS>(pk, nm, n, y, P, s);
     if constexpr (D == 64 || D == 128) {
         auto fn2 = dev::k_decode2<D, BITS, TO>;

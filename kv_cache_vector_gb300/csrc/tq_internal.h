@@ -68,6 +68,21 @@ struct Plan {
 void fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, float sparse_thr,
                       AttnParams& A);
 
+// Argument checks of the contiguous decode attention, shared by
+// tq_attn_decode and tq_attn_decode_noalloc: everything but the workspace,
+// including that every buffer is one the device can dereference.  TQ_OK with
+// *nothing = true when B == 0 (nothing to launch).
+tq_status check_attn_decode_args(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                                 const tq_cache_view& cache, int64_t ctx_len, int k_bits, int v_bits,
+                                 float scale, float sparse_v_threshold, const float* out, bool* nothing);
+// Launch of the contiguous decode attention on checked arguments, with the
+// workspace `workspace` (geometry g) and the head-dimension dispatch of
+// tq_attn_decode.
+struct AttnGeometry;
+cudaError_t launch_attn_decode(const Plan& P, const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
+                               int64_t ctx_len, int k_bits, int v_bits, float scale, float sparse_v_threshold,
+                               float* out, void* workspace, const AttnGeometry& g, cudaStream_t st);
+
 // Bucketing lookup table geometry (encode): cell g covers the normalised
 // coordinate w with rint(w * kLutScale) = g - kLutCenter, i.e. the closed
 // interval [(g - kLutCenter - 0.5) / kLutScale, (g - kLutCenter + 0.5) / kLutScale].

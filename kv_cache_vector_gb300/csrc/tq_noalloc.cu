@@ -47,20 +47,6 @@ cudaError_t scratch_for_current_device(void** out) {
     return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
-template <int D>
-cudaError_t launch_d(int kb, int vb, const void* q, int B, int Hq, int Hkv, const tq_cache_view& c,
-                     int64_t ctx, float* out, void* ws, const tq::AttnGeometry& g,
-                     const tq::AttnParams& A, cudaStream_t st) {
-    switch (kb) {
-        case 2: return tq::launch_attn_dk<D, 2>(vb, q, B, Hq, Hkv, c, ctx, out, ws, g, A, st);
-        case 3: return tq::launch_attn_dk<D, 3>(vb, q, B, Hq, Hkv, c, ctx, out, ws, g, A, st);
-        default: return tq::launch_attn_dk<D, 4>(vb, q, B, Hq, Hkv, c, ctx, out, ws, g, A, st);
-    }
-}
-
 }  // namespace
 
 extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, int B, int Hq,
@@ -68,38 +54,21 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, 
                                             int k_bits, int v_bits, float scale,
                                             float sparse_v_threshold, float* out,
                                             tq_stream_t stream) {
-    if (!plan || B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return TQ_ERR_INVALID_ARG;
-    if (k_bits < 2 || k_bits > 4 || v_bits < 2 || v_bits > 4 || Hq / Hkv > 8)
-        return TQ_ERR_UNSUPPORTED;
+    // the same checks as tq_attn_decode, bar the caller's workspace
+    bool nothing = false;
+    tq_status st = tq::check_attn_decode_args(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale,
+                                              sparse_v_threshold, out, &nothing);
+    if (st != TQ_OK || nothing) return st;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
-    if (P->d < 32) return TQ_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
-        return TQ_ERR_INVALID_ARG;
-    if (ctx_len < 1 || ctx_len > cache.cap) return TQ_ERR_RANGE;
-    if (B == 0) return TQ_OK;
-    if (!q || !out || !cache.k_packed || !cache.k_norm || !cache.v_packed || !cache.v_norm)
-        return TQ_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k_packed) ||
-        !aligned16(cache.v_packed) || !aligned4(cache.k_norm) || !aligned4(cache.v_norm))
-        return TQ_ERR_ALIGNMENT;
     const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
     if (tq::attn_workspace_bytes(B, Hq, P->d, g) > kScratchBytes) return TQ_ERR_WORKSPACE;
     void* ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
+    if (e == cudaSuccess)
+        e = tq::launch_attn_decode(*P, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale, sparse_v_threshold,
+                                   out, ws, g, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
-        tq::set_last_cuda_error(e);
-        return TQ_ERR_CUDA;
-    }
-    tq::AttnParams A;
-    tq::fill_attn_params(*P, k_bits, v_bits, scale, sparse_v_threshold, A);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    switch (P->d) {
-        case 32: e = launch_d<32>(k_bits, v_bits, q, B, Hq, Hkv, cache, ctx_len, out, ws, g, A, st); break;
-        case 64: e = launch_d<64>(k_bits, v_bits, q, B, Hq, Hkv, cache, ctx_len, out, ws, g, A, st); break;
-        case 128: e = launch_d<128>(k_bits, v_bits, q, B, Hq, Hkv, cache, ctx_len, out, ws, g, A, st); break;
-        default: e = launch_d<256>(k_bits, v_bits, q, B, Hq, Hkv, cache, ctx_len, out, ws, g, A, st); break;
-    }
-    if (e != cudaSuccess) {
+        cudaGetLastError();  // leave no stale error for the caller's next launch check
         tq::set_last_cuda_error(e);
         return TQ_ERR_CUDA;
     }
