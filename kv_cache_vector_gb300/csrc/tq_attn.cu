@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
 // k_attn3_combine merges a (batch, head)'s partials.
 
 constexpr int kA3Chunk = 32;
-constexpr int kA3MergeStride = 132;  // floats per (warp, head) row of the merge buffer
+constexpr int kA3MergeStride = kAttn3MergeRow / 4;  // floats per (warp, head) row of the merge buffer
 constexpr float kLazy = 8.0f;        // log2 units
 // Shared memory is addressed by absolute shared-window address.  The pair
 // table starts at 128 KiB: entry e of lane l's column is at
@@ -266,18 +266,22 @@ constexpr int kA3StatusLayout = 32;  // dynamic shared memory starts above kA3Ri
 constexpr int kA3StatusPage = 33;    // a paged cache's block table names a page out of range
 constexpr int kA3StatusAppend = 42;  // an appended row's position or page is out of range (as the append)
 
-// Warps and ring stages per CTA (attn3_warps, attn3_stages): up to 16 x 2
-// for up to four query heads per KV head, 8 x 3 for up to eight.
+// Warps, ring stages and the shared-memory plan per CTA (attn3_plan): up to
+// 16 warps x 2 stages for up to four query heads per KV head, 8 x 3 for up to
+// eight.
 template <int KB, int VB, int NG>
 struct A3Shape {
-    static constexpr int kWarps = attn3_warps(4 * NG, KB, VB);
-    static constexpr int kStages = attn3_stages(4 * NG);
+    static constexpr Attn3Plan kPlan = attn3_plan(4 * NG, KB, VB);
+    static constexpr int kWarps = kPlan.warps;
+    static constexpr int kStages = kPlan.stages;
     static constexpr int kThreads = 32 * kWarps;
+    static_assert(kWarps > 0, "no shared-memory plan");
 };
 
 template <int KB, int VB, int NG>
 struct A3Layout {
-    static constexpr int kWarps = A3Shape<KB, VB, NG>::kWarps, kStages = A3Shape<KB, VB, NG>::kStages;
+    static constexpr Attn3Plan kPlan = A3Shape<KB, VB, NG>::kPlan;
+    static constexpr int kWarps = kPlan.warps, kStages = kPlan.stages;
     static constexpr int kKRow = 16 * KB, kVRow = 16 * VB;  // bytes of a d = 128 row
     static constexpr int kVOff = kA3Chunk * kKRow;
     static constexpr int kKnOff = kA3Chunk * (kKRow + kVRow);
@@ -286,12 +290,17 @@ struct A3Layout {
     static_assert(kStage == attn3_stage_bytes(KB, VB), "stage size");
     static constexpr int kEntries = 256;  // rows of the pair table (one byte of index)
     static constexpr int kHeads = 4 * NG;
-    static constexpr uint32_t kMergeAt = kA3TableAt + 256u * kEntries;
-    static constexpr uint32_t kBarAt = kMergeAt + 4u * kWarps * kHeads * kA3MergeStride;
-    static constexpr uint32_t kEnd = kBarAt + 8u * kWarps * kStages;
+    // keys that carry their rest: 8-byte key entries (high and low fp16
+    // pairs), 16 columns shared by lanes l and l + 16
+    static constexpr bool kRest = attn3_key_rest(KB);
+    static constexpr int kMergeHeads = kPlan.merge_heads;
+    static constexpr uint32_t kMergeAt = (uint32_t)kPlan.merge;
+    static constexpr uint32_t kBarAt = (uint32_t)kPlan.bars;
+    static constexpr uint32_t kEnd = (uint32_t)kPlan.end;
     static_assert(kStage % 16 == 0, "stage alignment");
     static_assert(kA3RingAt + kWarps * kStages * kStage <= kA3TableAt, "ring overlaps the table");
-    static_assert(kEnd <= 232448, "more than 227 KiB of shared memory");
+    static_assert(kBarAt % 8 == 0 && kMergeAt % 16 == 0, "alignment");
+    static_assert(kEnd <= (uint32_t)kAttn3SmemTop, "more than 227 KiB of shared memory");
 };
 
 __device__ __forceinline__ uint32_t h2u(float lo, float hi) {
@@ -324,6 +333,12 @@ __host__ __device__ __forceinline__ int attn3_cta_of(int64_t i, int grid, int64_
 __device__ __forceinline__ uint32_t lds_tab(uint32_t addr) {
     uint32_t v;
     asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+// Both fp16 parts of a key pair (x: the values nearest c * s_k, y: their rests).
+__device__ __forceinline__ uint2 lds_tab2(uint32_t addr) {
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
 }
 // Loads of ring data: volatile, so that they stay after the stage's wait.
@@ -709,13 +724,18 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     }
     auto gptr = [&](uint32_t abs) { return a3_smem + (abs - base); };
 
-    // ---- pair tables (K columns, V columns) and the per-warp barriers
+    // ---- pair tables and the per-warp barriers
     {
         constexpr int MK = (1 << KB) - 1, MV = (1 << VB) - 1;
         for (int i = threadIdx.x; i < L::kEntries * 64; i += T) {
             const int e = i >> 6, s = i & 63;  // row e holds the pair e mod 2^(2 bits)
-            const uint32_t v = s < 32 ? h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK])
-                                      : h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
+            uint32_t v;
+            if (s >= 32)
+                v = h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
+            else if (L::kRest && (s & 1))  // words 2c, 2c + 1 of column c: high and low key parts
+                v = h2u(P.kcen_l[e & MK], P.kcen_l[(e >> KB) & MK]);
+            else
+                v = h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK]);
             *reinterpret_cast<uint32_t*>(gptr(kA3TableAt + 256u * e + 4u * s)) = v;
         }
     }
@@ -729,7 +749,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 
     const int g = lane >> 2, t = lane & 3;
     const int G = Hq / Hkv;
-    const uint32_t kslot = kA3TableAt + 4u * lane, vslot = kslot + 128u;
+    const uint32_t kslot = kA3TableAt + (L::kRest ? 8u * (lane & 15) : 4u * lane);
+    const uint32_t vslot = kA3TableAt + 128u + 4u * lane;
     const uint32_t ring = kA3RingAt + (uint32_t)(warp * S * L::kStage);
     float* merge = reinterpret_cast<float*>(gptr(L::kMergeAt));
     const int64_t i_begin = PAGED ? (int64_t)meta.cta_begin[blockIdx.x] : n_items * blockIdx.x / gridDim.x;
@@ -854,28 +875,39 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     auto chunk = [&](uint32_t sb, int n, auto full_tag) {
         constexpr bool FULL = decltype(full_tag)::value;
         const uint32_t sK = sb, sV = sb + L::kVOff;
-        // ---- scores
+        // ---- scores, one 16-position sub-tile at a time (fewer live registers)
         float sacc[2][NG][4];
-        uint32_t kw[2][2][KB];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
+            uint32_t kw[2][KB];
 #pragma unroll
             for (int hg = 0; hg < NG; ++hg) sacc[u][hg][0] = sacc[u][hg][1] = sacc[u][hg][2] = sacc[u][hg][3] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[u][h]);
-        }
+                load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[h]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < 8; ++kk) {
+                if constexpr (L::kRest) {
+                    // S = (K_hi + K_lo) (Q_hi + Q_lo): the keys' fp16 rests as a
+                    // second MMA into the same accumulators
+                    const uint2 a0 = lds_tab2(pair_addr<KB>(kw[0], 2 * kk, kslot));
+                    const uint2 a2 = lds_tab2(pair_addr<KB>(kw[0], 2 * kk + 1, kslot));
+                    const uint2 a1 = lds_tab2(pair_addr<KB>(kw[1], 2 * kk, kslot));
+                    const uint2 a3 = lds_tab2(pair_addr<KB>(kw[1], 2 * kk + 1, kslot));
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint32_t a0 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk, kslot));
-                const uint32_t a2 = lds_tab(pair_addr<KB>(kw[u][0], 2 * kk + 1, kslot));
-                const uint32_t a1 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk, kslot));
-                const uint32_t a3 = lds_tab(pair_addr<KB>(kw[u][1], 2 * kk + 1, kslot));
+                    for (int hg = 0; hg < NG; ++hg) {
+                        mma16816(sacc[u][hg], a0.x, a1.x, a2.x, a3.x, qb[hg][kk][0], qb[hg][kk][1]);
+                        mma16816(sacc[u][hg], a0.y, a1.y, a2.y, a3.y, qb[hg][kk][0], qb[hg][kk][1]);
+                    }
+                } else {
+                    const uint32_t a0 = lds_tab(pair_addr<KB>(kw[0], 2 * kk, kslot));
+                    const uint32_t a2 = lds_tab(pair_addr<KB>(kw[0], 2 * kk + 1, kslot));
+                    const uint32_t a1 = lds_tab(pair_addr<KB>(kw[1], 2 * kk, kslot));
+                    const uint32_t a3 = lds_tab(pair_addr<KB>(kw[1], 2 * kk + 1, kslot));
 #pragma unroll
-                for (int hg = 0; hg < NG; ++hg)
-                    mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
+                    for (int hg = 0; hg < NG; ++hg)
+                        mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
+                }
             }
         }
         // lane (g, t): positions 16u + 8h + g of head 4hg + t
@@ -1012,55 +1044,66 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     // first CTA whose items reach run_bh.
     auto publish = [&](int64_t run_bh) {
         const float mul = ldexpf(P.out_mul, vexp);
+        float lsum[NG];
 #pragma unroll
         for (int hg = 0; hg < NG; ++hg) {
             float l = l_run[hg];
             l += __shfl_xor_sync(kAll, l, 4);
             l += __shfl_xor_sync(kAll, l, 8);
             l += __shfl_xor_sync(kAll, l, 16);
-            if (hok[hg]) {
-                float* row = merge + (warp * L::kHeads + 4 * hg + t) * kA3MergeStride;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float4 v;
-                    v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
-                    v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
-                    v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
-                    v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
-                    *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
-                }
-                if (g == 0) {
-                    row[128] = m_run[hg];
-                    row[129] = l;
-                }
-            }
+            lsum[hg] = l;
         }
-        __syncthreads();
         const int64_t b = run_bh / Hkv;
         const int gh = (int)(run_bh % Hkv);
         const int slot = PAGED ? meta.slot_base[blockIdx.x] - meta.slot_base[meta.c0[run_bh]]
                                : (int)blockIdx.x - attn3_cta_of(run_bh * n_splits, gridDim.x, n_items);
-        for (int i = threadIdx.x; i < G * 128; i += T) {
-            const int h = i >> 7, dim = i & 127;
-            float M = -INFINITY;
+        // the merge buffer holds MH heads of every warp: heads h0 .. h0 + MH - 1 per pass
+        constexpr int MH = L::kMergeHeads;
+        for (int h0 = 0; h0 < G; h0 += MH) {
 #pragma unroll
-            for (int w = 0; w < W; ++w) M = fmaxf(M, merge[(w * L::kHeads + h) * kA3MergeStride + 128]);
-            float Ls = 0.f, A = 0.f;
+            for (int hg = 0; hg < NG; ++hg) {
+                const int hh = 4 * hg + t;
+                if (hok[hg] && hh >= h0 && hh < h0 + MH) {
+                    float* row = merge + (warp * MH + (hh - h0)) * kA3MergeStride;
 #pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float* row = merge + (w * L::kHeads + h) * kA3MergeStride;
-                const float f = row[128] == -INFINITY ? 0.f : fast_exp2(row[128] - M);
-                Ls = fmaf(f, row[129], Ls);
-                A = fmaf(f, row[dim], A);
+                    for (int i = 0; i < 4; ++i) {
+                        float4 v;
+                        v.x = (O[hg][2 * i][0] + O[hg][2 * i][1]) * mul;
+                        v.y = (O[hg][2 * i][2] + O[hg][2 * i][3]) * mul;
+                        v.z = (O[hg][2 * i + 1][0] + O[hg][2 * i + 1][1]) * mul;
+                        v.w = (O[hg][2 * i + 1][2] + O[hg][2 * i + 1][3]) * mul;
+                        *reinterpret_cast<float4*>(row + 16 * g + 4 * i) = v;
+                    }
+                    if (g == 0) {
+                        row[128] = m_run[hg];
+                        row[129] = lsum[hg];
+                    }
+                }
             }
-            float* o = part + ((b * Hq + gh * G + h) * n_splits + slot) * 130;
-            o[dim] = A;
-            if (dim == 0) {
-                o[128] = M;
-                o[129] = Ls;
+            __syncthreads();
+            const int nh = G - h0 < MH ? G - h0 : MH;
+            for (int i = threadIdx.x; i < nh * 128; i += T) {
+                const int h = i >> 7, dim = i & 127;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < W; ++w) M = fmaxf(M, merge[(w * MH + h) * kA3MergeStride + 128]);
+                float Ls = 0.f, A = 0.f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    const float* row = merge + (w * MH + h) * kA3MergeStride;
+                    const float f = row[128] == -INFINITY ? 0.f : fast_exp2(row[128] - M);
+                    Ls = fmaf(f, row[129], Ls);
+                    A = fmaf(f, row[dim], A);
+                }
+                float* o = part + ((b * Hq + gh * G + h0 + h) * n_splits + slot) * 130;
+                o[dim] = A;
+                if (dim == 0) {
+                    o[128] = M;
+                    o[129] = Ls;
+                }
             }
+            __syncthreads();
         }
-        __syncthreads();
     };
 
     // Items of one (batch, KV head) are consecutive: the warps accumulate

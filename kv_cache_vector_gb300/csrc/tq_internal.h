@@ -105,21 +105,62 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
                             const tq_cache_view& cache, int64_t pos, const RowParams& PK,
                             const RowParams& PV, cudaStream_t s);
 
-// Shape of the d = 128 attention kernel.  Each warp streams 32-position
-// chunks (packed K and V rows plus two fp32 norms each) through its own ring
-// of stages in shared memory below kAttn3TableAt.  Up to four query heads
-// per KV head: 2 stages and as many warps (at most 16) as the ring holds; up
-// to eight: 8 warps and 3 stages.
+// Shared-memory plan of the d = 128 attention kernel, in absolute
+// shared-window addresses (the dynamic block starts at or below
+// kAttn3RingAt).  Each warp streams 32-position chunks (packed K and V rows
+// plus two fp32 norms each) through its own ring of `stages` stages starting
+// at kAttn3RingAt.  The centroid-pair table sits at kAttn3TableAt, 64 KiB
+// aligned, so that a lookup address is one byte permute: row e (256 bytes)
+// holds the pair of levels e, keys in bytes 0..127 and values in 128..255.
+// A value entry is one fp16 pair per lane (32 columns of 4 bytes).  A key
+// entry is one fp16 pair per lane, or, for widths that carry the rest of
+// each centroid (attn3_key_rest), the pair of values nearest c * s_k and the
+// pair of their rests, 8 bytes read by one 64-bit load: such a load is served
+// a half-warp at a time, so lanes l and l + 16 share a column without a bank
+// conflict (16 columns of 8 bytes).  The merge buffer holds `merge_heads`
+// query heads of every warp at a time (merge passes = heads / merge_heads).
+// Up to four query heads per KV head: 2 stages and as many warps (at most
+// TQ_ATTN3_WARP_CAP) as fit; up to eight: 3 stages and at most 8 warps.
 constexpr int kAttn3RingAt = 2048;
 constexpr int kAttn3TableAt = 131072;
+constexpr int kAttn3SmemTop = 232448;    // 227 KiB, the most a block may use
+constexpr int kAttn3MergeRow = 132 * 4;  // bytes per (warp, head) row of the merge buffer
+// Tuning parameters: the most warps per CTA for up to four query heads per
+// KV head, and the smallest key width whose centroids carry their fp16 rest.
+#ifndef TQ_ATTN3_WARP_CAP
+#define TQ_ATTN3_WARP_CAP 16
+#endif
+#ifndef TQ_ATTN3_REST_MIN_BITS
+#define TQ_ATTN3_REST_MIN_BITS 3
+#endif
 constexpr int attn3_stage_bytes(int kb, int vb) { return 32 * (16 * kb + 16 * vb + 8); }
-constexpr int attn3_stages(int G) { return G <= 4 ? 2 : 3; }
-constexpr int attn3_warps(int G, int kb, int vb) {
-    return G > 4 ? 8
-                 : ((kAttn3TableAt - kAttn3RingAt) / (2 * attn3_stage_bytes(kb, vb)) < 16
-                        ? (kAttn3TableAt - kAttn3RingAt) / (2 * attn3_stage_bytes(kb, vb))
-                        : 16);
+constexpr bool attn3_key_rest(int kb) { return kb >= TQ_ATTN3_REST_MIN_BITS; }
+
+struct Attn3Plan {
+    int warps, stages, merge_heads;
+    int merge;  // merge buffer
+    int bars;   // one 8-byte mbarrier per (warp, stage)
+    int end;    // bytes of dynamic shared memory to ask for
+};
+
+constexpr Attn3Plan attn3_plan(int G, int kb, int vb) {
+    const int heads = G <= 4 ? 4 : 8;
+    const int stages = G <= 4 ? 2 : 3;
+    const int high = kAttn3TableAt + 65536;  // first byte above the table
+    for (int w = (G <= 4 ? TQ_ATTN3_WARP_CAP : 8); w >= 1; --w) {
+        const int ring_end = kAttn3RingAt + w * stages * attn3_stage_bytes(kb, vb);
+        if (ring_end > kAttn3TableAt) continue;
+        const int bars_bytes = 8 * w * stages;
+        for (int mh = heads; mh >= 1; mh /= 2) {
+            const int mb = w * mh * kAttn3MergeRow;
+            // merge and barriers above the table, else in the gap below it
+            if (high + mb + bars_bytes <= kAttn3SmemTop) return Attn3Plan{w, stages, mh, high, high + mb, high + mb + bars_bytes};
+            if (ring_end + mb + bars_bytes <= kAttn3TableAt) return Attn3Plan{w, stages, mh, ring_end, ring_end + mb, high};
+        }
+    }
+    return Attn3Plan{0, 0, 0, 0, 0, 0};
 }
+constexpr int attn3_warps(int G, int kb, int vb) { return attn3_plan(G, kb, vb).warps; }
 
 struct AttnGeometry {
     int n_splits;

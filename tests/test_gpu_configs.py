@@ -237,3 +237,43 @@ def test_gemma_window_encode_and_append_loop():
             rows = torch.cat([win[l, 0], new[:, l, 0, :, 0].permute(1, 0, 2)], dim=1)  # [Hkv, cap, d]
             compare_encode(s, 4, rows.reshape(-1, d).double().cpu().numpy(),
                            pk_t[0].reshape(-1, d // 2).cpu().numpy(), nm_t[0].reshape(-1).cpu().numpy())
+
+
+@pytest.mark.parametrize("bits,in_dtype,out_dtype", [(4, torch.bfloat16, torch.bfloat16),
+                                                     (2, torch.bfloat16, torch.bfloat16),
+                                                     (3, torch.float32, torch.float32)])
+def test_codec_ragged_large(bits, in_dtype, out_dtype):
+    """1,000,003 rows of d 128 (a multiple of neither 128 nor 32): the
+    persistent encoder and decoder take several tiles per CTA, so their
+    stage and accumulator phases wrap, and the last tile is ragged (the
+    tensor-map load past the end fills zeros, the tensor-map store clips).
+    Encode, then decode; 2048 sampled rows and the last 200 rows against the
+    oracle."""
+    d, n = 128, 1_000_003
+    plan = abi.Plan(d, 42)
+    s = O.signs(42, d)
+    x = synth.lowrank_rows(1234, n, d, dtype=in_dtype, stream=bits, device="cuda")
+    pk, nm = abi.tq_encode(plan, bits, x)
+    y = abi.tq_decode(plan, bits, pk, nm, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    idx = torch.cat([_sample_rows(n - 200, 2048, 11 + bits), torch.arange(n - 200, n)]).cuda()
+    xs = x[idx].double().cpu().numpy()
+    st = compare_encode(s, bits, xs, pk[idx].cpu().numpy(), nm[idx].cpu().numpy())
+    opk, onm = O.encode(s, bits, xs)
+    same = np.all(opk == pk[idx].cpu().numpy(), axis=1)
+    compare_decode(s, bits, opk[same], onm[same], y[idx].float().cpu().numpy()[same],
+                   bf16=out_dtype == torch.bfloat16)
+    print("ragged codec", bits, st)
+
+
+def test_decode_attention_ragged_large_context():
+    """Batch 3, 32 query / 8 KV heads, context 70,001 (not a multiple of a
+    chunk, a warp slice or a split), K4/V3, rows drawn like the prefill; three
+    sampled (batch, KV head) groups checked."""
+    B, Hq, Hkv, ctx = 3, 32, 8, 70001
+
+    def gen(h, side):
+        return synth.lowrank_rows(2100, B * ctx, 128, stream=(0 if side == "k" else 100) + h, device="cuda")
+
+    res = _attention_case(B, Hq, Hkv, ctx, 4, 3, gen, gen, 4, [(0, 0), (1, 3), (2, Hkv - 1)], [0.0])
+    print("ragged decode attention", res)
