@@ -483,18 +483,27 @@ def extra_codec_roundtrip(peak):
             "config": "4096 x d128 fp32 N(0,1) seed 0, signs seed 42, 4 bits; L2-resident (launch-bound)"}
 
 
-def extra_long_context(peak):
+def extra_long_context(peak, with_oracle=True):
     """Batch 1, 32 query / 8 KV heads, d 128, context 131072, K3/V2; keys
     N(0,1) with 2 outlier channels x8, values N(0,1); dense and sparse-V
-    (threshold 1e-4); L2 flushed before every timed call."""
+    (threshold 1e-4); L2 flushed before every timed call (200 calls each).
+    The sparse call's V rows read per KV head come from tq_attn_decode_ex;
+    beside them, the fraction of rows the oracle keeps per query head.  With
+    these random queries the softmax is flat (score std about 1.4) and nearly
+    every 32-position chunk holds a row some head keeps; the `sharpened`
+    variant scales the scores by 4 (as a larger query norm would), where
+    most chunks fall below the threshold."""
+    import numpy as np
     import torch
     from kv_cache_vector_gb300 import abi, synth
     B, Hq, Hkv, ctx, kb, vb = 1, 32, 8, 131072, 3, 2
     plan = abi.Plan(D, 42)
     cache = abi.Cache.empty(B, Hkv, ctx, D, kb, vb)
+    raw = []
     for h in range(Hkv):
         k = synth.outlier_rows(3000, B * ctx, D, 2, stream=h, device="cuda")
         v = synth.device_normal(3100 + h, (B * ctx, D))
+        raw.append((k, v))
         p2, n2 = abi.tq_encode(plan, kb, k)
         cache.k_packed[:, h] = p2.view(B, ctx, -1)
         cache.k_norm[:, h] = n2.view(B, ctx)
@@ -503,19 +512,50 @@ def extra_long_context(peak):
         cache.v_norm[:, h] = n2.view(B, ctx)
     q = synth.device_normal(5, (B, Hq, D))
     out = torch.empty(B, Hq, D, device="cuda")
+    rows = torch.empty(B, Hkv, dtype=torch.int32, device="cuda")
     ws = torch.empty(abi.tq_attn_workspace_bytes(B, Hq, Hkv, D, ctx), dtype=torch.uint8, device="cuda")
     buf = torch.zeros(4 * 129 * 2 ** 20 // 4, device="cuda")
-    res = {}
     nbytes = B * Hkv * ctx * (D * (kb + vb) // 8 + 8)
-    for name, thr in (("dense", 0.0), ("sparse_v_1e-4", 1e-4)):
-        f = lambda: abi.tq_attn_decode(plan, q, cache, ctx, 1.0 / math.sqrt(D), thr, out=out, workspace=ws)
-        for _ in range(5):
-            f()
-        ms = time_events(f, 200, lambda: flush_l2(buf))
-        res[name] = {"us": round(ms * 1e3, 2), "GBps_dense_bytes": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
-                     "frac_nominal": round(nbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4), "repeats": 200}
-    res["config"] = "B1 Hq32/Hkv8 d128 ctx131072 K3/V2, 2 outlier key channels x8, L2 flushed"
+    oracle_kept = {}
+    if with_oracle:  # the oracle's kept rows per query head, from its own encoding of the raw rows
+        from oracle import oracle as O
+        s = O.signs(42, D)
+        enc = []
+        for k, v in raw:
+            kp, kn = O.encode(s, kb, k.double().cpu().numpy())
+            vp, vn = O.encode(s, vb, v.double().cpu().numpy())
+            enc.append((kp, kn, vp, vn))
+        G = Hq // Hkv
+        for tag, mul in (("default", 1.0), ("sharpened", 4.0)):
+            kept = []
+            for h, (kp, kn, vp, vn) in enumerate(enc):
+                qq = q[:, h * G:(h + 1) * G].double().cpu().numpy()
+                _, kh = O.attention(s, qq, kp[None, None], kn[None, None], vp[None, None], vn[None, None],
+                                    kb, vb, ctx, mul / math.sqrt(D), 1e-4, want_kept=True)
+                kept += [round(float(x) / ctx, 4) for x in kh[0]]
+            oracle_kept[tag] = kept
+    del raw
+    res = {}
+    for tag, mul in (("default", 1.0), ("sharpened", 4.0)):
+        r = {}
+        for name, thr in (("dense", 0.0), ("sparse_v_1e-4", 1e-4)):
+            f = lambda: abi.tq_attn_decode_ex(plan, q, cache, ctx, mul / math.sqrt(D), thr, out=out,
+                                              v_rows_read=rows, workspace=ws)
+            for _ in range(5):
+                f()
+            ms = time_events(f, 200, lambda: flush_l2(buf))
+            rd = rows.cpu().numpy().reshape(-1)
+            r[name] = {"us": round(ms * 1e3, 2), "GBps_dense_bytes": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                       "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+                       "frac_nominal": round(nbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4), "repeats": 200,
+                       "v_rows_skipped_per_kv_head": [round(1.0 - float(x) / ctx, 4) for x in rd]}
+        if tag in oracle_kept:
+            r["oracle_kept_fraction_per_query_head"] = oracle_kept[tag]
+        res[tag] = r
+    res["dense"] = res["default"]["dense"]
+    res["sparse_v_1e-4"] = res["default"]["sparse_v_1e-4"]
+    res["config"] = ("B1 Hq32/Hkv8 d128 ctx131072 K3/V2, 2 outlier key channels x8, L2 flushed; "
+                     "sharpened: scale 4/sqrt(128)")
     return res
 
 

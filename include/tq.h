@@ -188,6 +188,25 @@ tq_status tq_attn_decode(const tq_plan *plan, const void *q, int B, int Hq, int 
                          float scale, float sparse_v_threshold, float *out, void *workspace,
                          size_t workspace_bytes, tq_stream_t stream);
 
+/* tq_attn_decode, also reporting how many cached rows' V bytes each (batch,
+ * KV head) read ("CITATIONS", Sparse V dequant: the gate saves the V loads
+ * and the dequantisation of rows no query head needs).
+ *   v_rows_read: [B][Hkv] int32, device, 4-byte aligned, or NULL; the call
+ *     writes it (no initial contents needed).  A dense call reads every row,
+ *     ctx_len per entry.  With sparse_v_threshold > 0 and d = 128 the kernel
+ *     copies the V rows of a 32-position chunk only when, for some query head
+ *     of the group, some row of the chunk has exp(sigma_t - m) >= threshold
+ *     (m that head's running maximum at the time, so no row the method keeps
+ *     is skipped); ctx_len - v_rows_read[b][g] rows of V were skipped.  Other
+ *     head dimensions gate row by row.
+ * tq_attn_decode is this call with v_rows_read = NULL; arguments, workspace
+ * and errors are otherwise the same (TQ_ERR_ALIGNMENT for a misaligned
+ * v_rows_read). */
+tq_status tq_attn_decode_ex(const tq_plan *plan, const void *q, int B, int Hq, int Hkv,
+                            tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                            float scale, float sparse_v_threshold, float *out, int32_t *v_rows_read,
+                            void *workspace, size_t workspace_bytes, tq_stream_t stream);
+
 /* Decode attention that allocates nothing, for callers that are not allowed
  * to allocate device memory while they run -- a plugin inside a framework
  * that owns every device allocation through its own memory planner, or a

@@ -26,7 +26,7 @@ STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_E
 EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_signs",
            "tq_plan_codebook", "tq_encode", "tq_decode", "tq_append", "tq_attn_workspace_bytes", "tq_attn_paged_workspace_bytes",
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
-           "tq_attn_decode_noalloc", "tq_append_paged", "tq_attn_decode_paged",
+           "tq_attn_decode_noalloc", "tq_attn_decode_ex", "tq_append_paged", "tq_attn_decode_paged",
            "tq_attn_decode_append_paged", "tq_plan_create_ex", "tq_plan_signs2", "tq_codebook_init_gaussian",
            "tq_attn_prefill_workspace_bytes", "tq_attn_prefill")
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t, vp]),
         ("tq_attn_decode_noalloc", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32,
                                          vp, vp]),
+        ("tq_attn_decode_ex", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32, vp, vp, vp,
+                                    ctypes.c_size_t, vp]),
         ("tq_append_paged", i32, [vp, i32, i32, vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, vp]),
         ("tq_attn_decode_paged", i32, [vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, i64, i32, i32,
                                        f32, f32, vp, vp, ctypes.c_size_t, vp]),
@@ -271,6 +273,32 @@ def tq_attn_decode(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scal
         ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(),
         workspace.data_ptr(), workspace.numel(), _stream(q)))
     return out
+
+
+def tq_attn_decode_ex(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scale: float,
+                      sparse_v_threshold: float = 0.0, out: torch.Tensor | None = None,
+                      v_rows_read: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None):
+    """tq_attn_decode that also returns, per (batch, KV head), how many cached
+    rows' V bytes the call read: (out [B, Hq, d] fp32, v_rows_read [B, Hkv] int32)."""
+    B, Hq, d = q.shape
+    Hkv = cache.k_norm.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    if v_rows_read is None:
+        v_rows_read = torch.empty(B, Hkv, dtype=torch.int32, device=q.device)
+    need = tq_attn_workspace_bytes(B, Hq, Hkv, d, ctx_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(q, out, workspace, v_rows_read)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    _i32(v_rows_read, "v_rows_read")
+    _check("tq_attn_decode_ex", lib().tq_attn_decode_ex(
+        plan.handle, q.data_ptr(), B, Hq, Hkv, cache.view(), ctx_len, cache.k_bits, cache.v_bits,
+        ctypes.c_float(scale), ctypes.c_float(sparse_v_threshold), out.data_ptr(), v_rows_read.data_ptr(),
+        workspace.data_ptr(), workspace.numel(), _stream(q)))
+    return out, v_rows_read
 
 
 def tq_attn_decode_noalloc(plan: Plan, q: torch.Tensor, cache: Cache, ctx_len: int, scale: float,

@@ -292,6 +292,7 @@ void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, fl
     for (int i = 0; i < 16; ++i) A.kcen_l[i] = (float)((double)P.c32[k_bits][i] * ks - (double)P.hcen[k_bits][i]);
     A.q_mul = (float)((double)scale * 1.4426950408889634 / (sd * ks));
     A.out_mul = (float)(1.0 / vs);
+    A.v_rows = nullptr;
 }
 
 tq_status tq::check_attn_decode_args(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
@@ -325,10 +326,15 @@ tq_status tq::check_attn_decode_args(const tq_plan* plan, const void* q, int B, 
 
 cudaError_t tq::launch_attn_decode(const Plan& P, const void* q, int B, int Hq, int Hkv,
                                    const tq_cache_view& cache, int64_t ctx_len, int k_bits, int v_bits,
-                                   float scale, float sparse_v_threshold, float* out, void* workspace,
-                                   const AttnGeometry& g, cudaStream_t st) {
+                                   float scale, float sparse_v_threshold, float* out, int32_t* v_rows,
+                                   void* workspace, const AttnGeometry& g, cudaStream_t st) {
     tq::AttnParams A;
     tq::fill_attn_params(P, k_bits, v_bits, scale, sparse_v_threshold, A);
+    if (v_rows) {  // counted by the split kernels, one add per warp and (batch, KV head) run
+        const cudaError_t e = cudaMemsetAsync(v_rows, 0, sizeof(int32_t) * (size_t)B * Hkv, st);
+        if (e != cudaSuccess) return e;
+        A.v_rows = v_rows;
+    }
     return dispatch_attn_d(P.d, [&](auto D) {
         constexpr int d = decltype(D)::value;
         switch (k_bits) {
@@ -501,23 +507,34 @@ size_t tq_attn_paged_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t max_
     return tq::attn_paged_workspace_bound(B, Hq, Hkv, max_ctx, tq::num_sms());
 }
 
-tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
-                         tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
-                         float scale, float sparse_v_threshold, float* out, void* workspace,
-                         size_t workspace_bytes, tq_stream_t stream) {
+tq_status tq_attn_decode_ex(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                            tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                            float scale, float sparse_v_threshold, float* out, int32_t* v_rows_read,
+                            void* workspace, size_t workspace_bytes, tq_stream_t stream) {
     bool nothing = false;
     tq_status st = tq::check_attn_decode_args(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale,
                                               sparse_v_threshold, out, &nothing);
     if (st != TQ_OK || nothing) return st;
+    if (v_rows_read && (!aligned4(v_rows_read))) return TQ_ERR_ALIGNMENT;
+    if (v_rows_read && !device_accessible(v_rows_read)) return TQ_ERR_INVALID_ARG;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
-    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits,
+                                                 sparse_v_threshold > 0.0f);
     if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
     if (!device_accessible(workspace)) return TQ_ERR_INVALID_ARG;
     const cudaError_t e = tq::launch_attn_decode(*P, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale,
-                                                 sparse_v_threshold, out, workspace, g,
+                                                 sparse_v_threshold, out, v_rows_read, workspace, g,
                                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
+                         tq_cache_view cache, int64_t ctx_len, int k_bits, int v_bits,
+                         float scale, float sparse_v_threshold, float* out, void* workspace,
+                         size_t workspace_bytes, tq_stream_t stream) {
+    return tq_attn_decode_ex(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale, sparse_v_threshold,
+                             out, nullptr, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------ paged cache

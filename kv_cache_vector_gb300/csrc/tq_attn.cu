@@ -148,12 +148,14 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
     const float thr = P.sparse_thr;
+    int nread = 0;  // rows whose V this warp reads
     for (int t = warp; t < len; t += kAttnWarps) {
         float pm = 0.f;
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h)
             if (h < G) pm = fmaxf(pm, sc[h * split_len + t]);
         if (pm < thr) continue;  // warp-uniform
+        ++nread;
         const uint8_t* vr = cache.v_packed + (row0 + t) * VRB;
         const int bit0 = lane * LBITS;
         const uint32_t* vw = reinterpret_cast<const uint32_t*>(vr);
@@ -169,6 +171,7 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
                 if (h < G) acc[h][e] = fmaf(sc[h * split_len + t], c, acc[h][e]);
         }
     }
+    if (P.v_rows && lane == 0 && nread > 0) atomicAdd(P.v_rows + (int64_t)b * Hkv + g, nread);
     // fixed-order cross-warp reduction
     for (int w = 0; w < kAttnWarps; ++w) {
         if (warp == w) {
@@ -269,25 +272,27 @@ constexpr int kA3StatusAppend = 42;  // an appended row's position or page is ou
 // Warps, ring stages and the shared-memory plan per CTA (attn3_plan): up to
 // 16 warps x 2 stages for up to four query heads per KV head, 8 x 3 for up to
 // eight.
-template <int KB, int VB, int NG>
+template <int KB, int VB, int NG, bool SP = false>
 struct A3Shape {
-    static constexpr Attn3Plan kPlan = attn3_plan(4 * NG, KB, VB);
+    static constexpr Attn3Plan kPlan = attn3_plan(4 * NG, KB, VB, SP);
     static constexpr int kWarps = kPlan.warps;
     static constexpr int kStages = kPlan.stages;
     static constexpr int kThreads = 32 * kWarps;
     static_assert(kWarps > 0, "no shared-memory plan");
 };
 
-template <int KB, int VB, int NG>
+template <int KB, int VB, int NG, bool SP = false>
 struct A3Layout {
-    static constexpr Attn3Plan kPlan = A3Shape<KB, VB, NG>::kPlan;
+    static constexpr Attn3Plan kPlan = A3Shape<KB, VB, NG, SP>::kPlan;
     static constexpr int kWarps = kPlan.warps, kStages = kPlan.stages;
     static constexpr int kKRow = 16 * KB, kVRow = 16 * VB;  // bytes of a d = 128 row
-    static constexpr int kVOff = kA3Chunk * kKRow;
-    static constexpr int kKnOff = kA3Chunk * (kKRow + kVRow);
+    static constexpr int kVOff = kA3Chunk * kKRow;  // V rows in the stage (not SP)
+    static constexpr int kKnOff = kA3Chunk * (kKRow + (SP ? 0 : kVRow));
     static constexpr int kVnOff = kKnOff + 4 * kA3Chunk;
     static constexpr int kStage = kVnOff + 4 * kA3Chunk;
-    static_assert(kStage == attn3_stage_bytes(KB, VB), "stage size");
+    static constexpr int kVBuf = kA3Chunk * kVRow;  // SP: one chunk's V rows; two per warp after its stages
+    static constexpr int kWarpRing = kPlan.stages * kStage + (SP ? 2 * kVBuf : 0);
+    static_assert(kWarpRing == attn3_warp_ring_bytes(KB, VB, kPlan.stages, SP), "ring size");
     static constexpr int kEntries = 256;  // rows of the pair table (one byte of index)
     static constexpr int kHeads = 4 * NG;
     // keys that carry their rest: 8-byte key entries (high and low fp16
@@ -298,7 +303,7 @@ struct A3Layout {
     static constexpr uint32_t kBarAt = (uint32_t)kPlan.bars;
     static constexpr uint32_t kEnd = (uint32_t)kPlan.end;
     static_assert(kStage % 16 == 0, "stage alignment");
-    static_assert(kA3RingAt + kWarps * kStages * kStage <= kA3TableAt, "ring overlaps the table");
+    static_assert(kA3RingAt + kWarps * kWarpRing <= kA3TableAt, "ring overlaps the table");
     static_assert(kBarAt % 8 == 0 && kMergeAt % 16 == 0, "alignment");
     static_assert(kEnd <= (uint32_t)kAttn3SmemTop, "more than 227 KiB of shared memory");
 };
@@ -306,6 +311,15 @@ struct A3Layout {
 __device__ __forceinline__ uint32_t h2u(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Unsigned keys that order as the floats do (for an integer atomic maximum).
+__device__ __forceinline__ uint32_t f2ord(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -432,13 +446,16 @@ __device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__
 // holds elements 4 l .. 4 l + 3, the butterflies over index bits 0 and 1 are
 // in registers and those over bits 2-6 between lanes, in the order len = 1,
 // 2, .., 64, and the scale and the fp16 parts are those of rotate_q_row.
+// gmax (sparse V, or nullptr): the split kernel's running maxima, cleared here.
 static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __restrict__ q,
                                                         __half* __restrict__ q16,
                                                         float* __restrict__ qexp,
-                                                        const __grid_constant__ AttnParams P, int64_t n_rows) {
+                                                        const __grid_constant__ AttnParams P, int64_t n_rows,
+                                                        uint32_t* __restrict__ gmax) {
     const int lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (bh >= n_rows) return;  // the whole warp
+    if (gmax && lane == 0) gmax[bh] = 0u;  // below every score's key
     const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + bh * 128) + lane);
     float x[4];
     {
@@ -552,6 +569,7 @@ struct A3Meta {
     int32_t* slot_base;
     int32_t* c0;
     int32_t* clast;
+    uint32_t* gmax;  // sparse V: largest score per (batch, query head) so far, zeroed by the query rotation
 };
 // Weights of the work partition, in rows of the busiest warp: an item that
 // holds rows costs its busiest warp's rows plus kA3ItemCost, an empty item
@@ -707,14 +725,20 @@ static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __res
 // length (at most ctx_len) and CTA ranges come from k_attn3_plan; otherwise
 // rows are [B][Hkv][cap], every sequence attends over ctx_len and CTA c takes
 // items [n_items c / grid, n_items (c + 1) / grid).
-template <int KB, int VB, int NG, bool PAGED>
-__global__ void __launch_bounds__(A3Shape<KB, VB, NG>::kThreads, 1)
+// SP (contiguous cache, sparse-V threshold > 0): the producer copies a
+// chunk's K rows and norms; the V rows are copied only after the chunk's
+// scores, when some query head keeps one of its rows ("CITATIONS", Sparse V
+// dequant), and their product is taken one chunk later, with the chunk's
+// weights rescaled if the running maximum moves in between.
+template <int KB, int VB, int NG, bool PAGED, bool SP>
+__global__ void __launch_bounds__(A3Shape<KB, VB, NG, SP>::kThreads, 1)
 k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv,
               tq_cache_view cache, int64_t ctx_len, int warp_len, int n_splits, int64_t n_items,
               float* __restrict__ part, int* status, const __grid_constant__ AttnParams P,
               const PagedArgs pa, const A3Meta meta) {
-    using L = A3Layout<KB, VB, NG>;
-    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG>::kThreads;
+    static_assert(!(SP && PAGED), "sparse-V copies are for the contiguous cache");
+    using L = A3Layout<KB, VB, NG, SP>;
+    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG, SP>::kThreads;
     constexpr uint32_t kAll = 0xFFFFFFFFu;
     extern __shared__ __align__(16) unsigned char a3_smem[];
     const uint32_t base = smem_addr(a3_smem);
@@ -741,8 +765,13 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t* bars = reinterpret_cast<uint64_t*>(gptr(L::kBarAt)) + warp * S;
+    uint64_t* vbars = reinterpret_cast<uint64_t*>(gptr(L::kBarAt)) + W * S + warp * 2;  // SP: the V buffers
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + s, 32);
+        if constexpr (SP) {
+            mbar_init(vbars, 1);
+            mbar_init(vbars + 1, 1);
+        }
         mbar_fence_init();
     }
     __syncthreads();
@@ -751,7 +780,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     const int G = Hq / Hkv;
     const uint32_t kslot = kA3TableAt + (L::kRest ? 8u * (lane & 15) : 4u * lane);
     const uint32_t vslot = kA3TableAt + 128u + 4u * lane;
-    const uint32_t ring = kA3RingAt + (uint32_t)(warp * S * L::kStage);
+    const uint32_t ring = kA3RingAt + (uint32_t)(warp * L::kWarpRing);
+    const uint32_t vbuf = ring + (uint32_t)(S * L::kStage);  // SP: V buffers 0 and 1
     float* merge = reinterpret_cast<float*>(gptr(L::kMergeAt));
     const int64_t i_begin = PAGED ? (int64_t)meta.cta_begin[blockIdx.x] : n_items * blockIdx.x / gridDim.x;
     const int64_t i_end = PAGED ? (int64_t)meta.cta_begin[blockIdx.x + 1] : n_items * (blockIdx.x + 1) / gridDim.x;
@@ -830,9 +860,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         if (ok) {
             if (lane == 0) {
                 fence_async_smem();  // earlier generic reads of this stage come first
-                mbar_expect_tx(bar, (uint32_t)(n * (L::kKRow + L::kVRow)));
+                mbar_expect_tx(bar, (uint32_t)(n * (L::kKRow + (SP ? 0 : L::kVRow))));
                 bulk_load(sb, cache.k_packed + row * L::kKRow, (uint32_t)(n * L::kKRow), bar);
-                bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
+                if constexpr (!SP)
+                    bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
             }
             // lanes past the end copy nothing (source size 0) from a valid row
             const int64_t r = row + (lane < n ? lane : n - 1);
@@ -871,10 +902,35 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
     const bool odd = (g & 1) != 0;
 
-    // One chunk of 32 positions at shared address sb; FULL: all 32 valid.
-    auto chunk = [&](uint32_t sb, int n, auto full_tag) {
+    // SP: the kept chunk whose V product is still to come (its V buffer,
+    // weights, V norms and valid rows); V buffers with a copy in flight; V
+    // barrier phases
+    bool pend = false;
+    int pvi = 0;
+    float pp[NG][2][2], pvn[2][2];
+    bool pok[2][2];
+    uint32_t pkeep = 0u;  // SP: sub-tiles of the pending chunk that some head keeps (bits u)
+    // SP: the largest score of the lane's head seen anywhere in the grid so far
+    // (log2 units; meta.gmax, one order-preserving key per (batch, query head)),
+    // as this warp last read or raised it, and that head's slot
+    float m_ref[NG];
+    uint32_t* gslot[NG];
+    const float lthr = SP ? __log2f(thr) : 0.f;
+    uint32_t vfl = 0u, vph = 0u;
+    int vcount = 0;  // rows whose V this warp read in the current (batch, KV head) run
+
+    // Scores of one chunk of 32 positions at shared address sb (FULL: all 32
+    // valid): the weights p relative to the running maximum, the V norms and
+    // the valid rows; updates the running maximum and denominators.
+    auto scores = [&](uint32_t sb, int n, auto full_tag, float (&p)[NG][2][2], float (&vn)[2][2],
+                      bool (&ok)[2][2], uint32_t& ukeep) {
         constexpr bool FULL = decltype(full_tag)::value;
-        const uint32_t sK = sb, sV = sb + L::kVOff;
+        const uint32_t sK = sb;
+        uint32_t gseen[NG];  // SP: the grid's maximum, loaded now and used after the MMAs
+        if constexpr (SP) {
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) gseen[hg] = *reinterpret_cast<volatile uint32_t*>(gslot[hg]);
+        }
         // ---- scores, one 16-position sub-tile at a time (fewer live registers)
         float sacc[2][NG][4];
 #pragma unroll
@@ -911,8 +967,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             }
         }
         // lane (g, t): positions 16u + 8h + g of head 4hg + t
-        float sc[NG][2][2], vn[2][2];
-        bool ok[2][2];
+        float sc[NG][2][2];
         float nvl = 0.f;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -941,6 +996,29 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             tmax[hg] = mx;
             need = need || mx > m_run[hg] + kLazy;
         }
+        if constexpr (SP) {
+            // Gate against the largest score of the head seen anywhere in the
+            // grid so far (at most the global maximum, so every row the
+            // method keeps is kept): a sub-tile's V is needed when some valid
+            // row of some head has sigma - m >= log2(threshold).  The warp
+            // raises the grid's value only when it holds a new maximum.
+            ukeep = 0u;
+#pragma unroll
+            for (int hg = 0; hg < NG; ++hg) {
+                if (hok[hg]) {
+                    m_ref[hg] = fmaxf(m_ref[hg], ord2f(gseen[hg]));
+                    if (tmax[hg] > m_ref[hg]) {
+                        m_ref[hg] = tmax[hg];
+                        if (g == 0) atomicMax(gslot[hg], f2ord(tmax[hg]));
+                    }
+                    const float gate = m_ref[hg] + lthr;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if ((ok[u][0] && sc[hg][u][0] >= gate) || (ok[u][1] && sc[hg][u][1] >= gate)) ukeep |= 1u << u;
+                }
+            }
+            ukeep = __reduce_or_sync(kAll, ukeep);
+        }
         // rare: the running maximum moves, or a V norm would take p * n_v
         // (p <= 2^kLazy) past the fp16 range in units of 2^vexp
         if (__any_sync(kAll, need || nvl > vlim)) {
@@ -957,6 +1035,14 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 }
                 l_run[hg] *= al;
                 m_run[hg] = mn;
+                if constexpr (SP) {  // the pending chunk's weights follow the new maximum
+                    if (pend) {
+                        pp[hg][0][0] *= al;
+                        pp[hg][0][1] *= al;
+                        pp[hg][1][0] *= al;
+                        pp[hg][1][1] *= al;
+                    }
+                }
             }
             float w = nvl;
 #pragma unroll
@@ -979,7 +1065,6 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 vsc = ldexpf(1.f, -en);
             }
         }
-        float p[NG][2][2];
 #pragma unroll
         for (int hg = 0; hg < NG; ++hg)
 #pragma unroll
@@ -989,11 +1074,16 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                     p[hg][u][h] = fast_exp2(sc[hg][u][h] - m_run[hg]);
                     l_run[hg] += p[hg][u][h];
                 }
+    };
 
-        // ---- O^T += V^T P, per sub-tile
+    // O^T += V^T P over the chunk whose V rows are at shared address sV, per sub-tile.
+    auto pv = [&](uint32_t sV, const float (&p)[NG][2][2], const float (&vn)[2][2], const bool (&ok)[2][2],
+                  uint32_t ukeep) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            if (sparse) {  // skip when every head is below the threshold
+            if constexpr (SP) {
+                if (!(ukeep & (1u << u))) continue;
+            } else if (sparse) {  // skip when every head is below the threshold
                 bool keep = false;
 #pragma unroll
                 for (int hg = 0; hg < NG; ++hg)
@@ -1039,10 +1129,32 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         }
     };
 
+    // SP: take the pending chunk's V product once its V rows have landed in
+    // its buffer.
+    auto flush = [&]() {
+        if constexpr (SP) {
+            if (!pend) return;
+            pend = false;
+            if (!bad) {
+                const bool okw = mbar_wait(vbars + pvi, (vph >> pvi) & 1u);
+                if (!__all_sync(kAll, okw)) {
+                    if (lane == 0) report_timeout(status, kA3StatusWait);
+                    bad = true;  // the copy stays in vfl: waited for again before exit
+                } else {
+                    vph ^= 1u << pvi;
+                    vfl &= ~(1u << pvi);
+                    pv(vbuf + (uint32_t)(pvi * L::kVBuf), pp, pvn, pok, pkeep);
+                }
+            }
+        }
+    };
+
     // Merge the warps' running partials of the (batch, KV head) run_bh into
     // one partial per query head; its slot is this CTA's offset from the
     // first CTA whose items reach run_bh.
     auto publish = [&](int64_t run_bh) {
+        if (P.v_rows && lane == 0 && vcount > 0) atomicAdd(P.v_rows + run_bh, vcount);
+        vcount = 0;
         const float mul = ldexpf(P.out_mul, vexp);
         float lsum[NG];
 #pragma unroll
@@ -1113,6 +1225,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     int64_t bh = i_begin / n_splits;
     for (int64_t item = i_begin; item <= i_end; ++item) {
         if (item == i_end || bh != cur_bh) {
+            flush();
             if (cur_bh >= 0) publish(cur_bh);
             if (item == i_end) break;
             cur_bh = bh;
@@ -1152,6 +1265,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 }
                 hok[hg] = 4 * hg + t < G;
                 qx[hg] = hok[hg] ? __ldg(qexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
+                if constexpr (SP) {
+                    m_ref[hg] = -INFINITY;
+                    gslot[hg] = meta.gmax + (b * Hq + gh * G + (hok[hg] ? 4 * hg + t : 0));
+                }
             }
         }
 
@@ -1160,7 +1277,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             const int64_t rem = ctx_run - pos;
             if (rem <= 0) break;  // this slot and the item's later ones hold no rows
             const int n = rem >= kA3Chunk ? kA3Chunk : (int)rem;
-            seek();
+            if constexpr (!SP) seek();  // paged: the page id loads while this chunk computes
             if (!bad) {
                 const bool ok = mbar_wait(bars + cst, cph);
                 if (!__all_sync(kAll, ok)) {
@@ -1170,13 +1287,61 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                     --inflight;
                 }
             }
+            bool release = true;  // SP refills the K stage itself, right after the scores
             if (!bad) {
                 const uint32_t sb = ring + (uint32_t)(cst * L::kStage);
-                if (n == kA3Chunk) chunk(sb, n, std::true_type{});
-                else chunk(sb, n, std::false_type{});
+                float p[NG][2][2], vn[2][2];
+                bool ok[2][2];
+                uint32_t ukeep = 3u;
+                if (n == kA3Chunk) scores(sb, n, std::true_type{}, p, vn, ok, ukeep);
+                else scores(sb, n, std::false_type{}, p, vn, ok, ukeep);
+                if constexpr (SP) {
+                    const bool keep = ukeep != 0u;  // warp-uniform
+                    const int vi = pend ? (pvi ^ 1) : 0;  // the buffer the pending chunk does not hold
+                    if (keep && lane == 0) {
+                        uint64_t* vb = vbars + vi;
+                        fence_async_smem();  // earlier generic reads of the buffer come first
+                        mbar_arrive_expect_tx(vb, (uint32_t)(n * L::kVRow));
+                        bulk_load(vbuf + (uint32_t)(vi * L::kVBuf),
+                                  cache.v_packed + (cur_bh * cache.cap + pos) * L::kVRow, (uint32_t)(n * L::kVRow), vb);
+                    }
+                    if (keep) vfl |= 1u << vi;
+                    // the K stage is done with: the producer refills it now
+                    __syncwarp();
+                    seek();
+                    issue();
+                    release = false;
+                    flush();  // the previous kept chunk's V product, while this chunk's V loads
+                    if (keep) {
+                        pend = true;
+                        pvi = vi;
+#pragma unroll
+                        for (int hg = 0; hg < NG; ++hg)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                pp[hg][u][0] = p[hg][u][0];
+                                pp[hg][u][1] = p[hg][u][1];
+                            }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            pvn[u][0] = vn[u][0];
+                            pvn[u][1] = vn[u][1];
+                            pok[u][0] = ok[u][0];
+                            pok[u][1] = ok[u][1];
+                        }
+                        pkeep = ukeep;
+                        vcount += n;
+                    }
+                } else {
+                    pv(sb + L::kVOff, p, vn, ok, 3u);
+                    vcount += n;
+                }
             }
-            __syncwarp();
-            issue();
+            if (release) {
+                __syncwarp();
+                if constexpr (SP) seek();
+                issue();
+            }
             if (!bad && ++cst == S) {
                 cst = 0;
                 cph ^= 1u;
@@ -1196,6 +1361,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 cst = 0;
                 cph ^= 1u;
             }
+        }
+        if constexpr (SP) {
+            for (int s = 0; s < 2; ++s)
+                if (vfl & (1u << s)) mbar_wait(vbars + s, (vph >> s) & 1u);
         }
     }
 }
@@ -1277,13 +1446,13 @@ static __global__ void __launch_bounds__(256) k_attn3_combine(const float* __res
     reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }
 
-template <int KB, int VB, int NG, bool PAGED>
+template <int KB, int VB, int NG, bool PAGED, bool SP>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
                                int64_t items, int grid, float* part, const AttnParams& P,
                                const PagedArgs& pa, const A3Meta& meta, cudaStream_t s) {
-    using L = A3Layout<KB, VB, NG>;
-    auto fn = k_attn3_split<KB, VB, NG, PAGED>;
+    using L = A3Layout<KB, VB, NG, SP>;
+    auto fn = k_attn3_split<KB, VB, NG, PAGED, SP>;
     // The kernel addresses shared memory from window address 0, so it asks
     // for kEnd bytes (the dynamic block starts at or below kA3RingAt).
     static int attr_done[64] = {};
@@ -1295,7 +1464,7 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    fn<<<(unsigned)grid, A3Shape<KB, VB, NG>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len,
+    fn<<<(unsigned)grid, A3Shape<KB, VB, NG, SP>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len,
                                                                       geo.warp_len, geo.n_splits, items,
                                                                       part, status_word(), P, pa, meta);
     return cudaGetLastError();
@@ -1315,6 +1484,7 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     meta.slot_base = meta.cta_begin + (sms + 1);
     meta.c0 = meta.slot_base + (sms + 1);
     meta.clast = meta.c0 + (size_t)B * Hq;
+    meta.gmax = reinterpret_cast<uint32_t*>(meta.clast + (size_t)B * Hq + B);
     PagedArgs pa = pa_in;
     cudaError_t e;
     if (PAGED && app) {
@@ -1332,8 +1502,9 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
                                                           *app->PK, *app->PV, KB, VB, len1, status_word());
         pa.lens = len1;
     } else {
-        k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(q), q16,
-                                                                       qexp, P, (int64_t)B * Hq);
+        k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(q), q16, qexp, P, (int64_t)B * Hq,
+            (!PAGED && P.sparse_thr > 0.f) ? meta.gmax : nullptr);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1358,12 +1529,19 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    // contiguous cache with a sparse-V threshold: the variant that copies V
+    // only for the chunks some head keeps
+    const bool sp = !PAGED && P.sparse_thr > 0.f;
     if (Hq / Hkv <= 4)
-        e = attn3_split_launch<KB, VB, 1, PAGED>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P,
-                                                 pa, meta, s);
+        e = sp ? attn3_split_launch<KB, VB, 1, false, true>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid,
+                                                            part, P, pa, meta, s)
+               : attn3_split_launch<KB, VB, 1, PAGED, false>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items,
+                                                             grid, part, P, pa, meta, s);
     else
-        e = attn3_split_launch<KB, VB, 2, PAGED>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid, part, P,
-                                                 pa, meta, s);
+        e = sp ? attn3_split_launch<KB, VB, 2, false, true>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid,
+                                                            part, P, pa, meta, s)
+               : attn3_split_launch<KB, VB, 2, PAGED, false>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items,
+                                                             grid, part, P, pa, meta, s);
     if (e != cudaSuccess) return e;
     k_attn3_combine<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv,
                                                                            (int64_t)B * Hq, out, P, PAGED, meta);

@@ -48,6 +48,9 @@ struct AttnParams {
     float out_mul;
     int two_sided;  // as RowParams
     uint32_t sgn2[kMaxD];
+    // [B][Hkv] rows whose V bytes the call read (zeroed before the launch),
+    // or nullptr
+    int32_t* v_rows;
 };
 
 // Host plan (the public tq_plan).
@@ -79,9 +82,11 @@ tq_status check_attn_decode_args(const tq_plan* plan, const void* q, int B, int 
 // workspace `workspace` (geometry g) and the head-dimension dispatch of
 // tq_attn_decode.
 struct AttnGeometry;
+// v_rows: the [B][Hkv] row counts of tq_attn_decode_ex, or nullptr.
 cudaError_t launch_attn_decode(const Plan& P, const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
                                int64_t ctx_len, int k_bits, int v_bits, float scale, float sparse_v_threshold,
-                               float* out, void* workspace, const AttnGeometry& g, cudaStream_t st);
+                               float* out, int32_t* v_rows, void* workspace, const AttnGeometry& g,
+                               cudaStream_t st);
 
 // Bucketing lookup table geometry (encode): cell g covers the normalised
 // coordinate w with rint(w * kLutScale) = g - kLutCenter, i.e. the closed
@@ -121,6 +126,10 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
 // query heads of every warp at a time (merge passes = heads / merge_heads).
 // Up to four query heads per KV head: 2 stages and as many warps (at most
 // TQ_ATTN3_WARP_CAP) as fit; up to eight: 3 stages and at most 8 warps.
+// The sparse-V variant (contiguous cache) copies a chunk's V rows only after
+// its scores and takes their product one chunk later: its stages hold K rows
+// and norms only, and each warp has two V buffers of one chunk after its
+// stages, each with its own barrier.
 constexpr int kAttn3RingAt = 2048;
 constexpr int kAttn3TableAt = 131072;
 constexpr int kAttn3SmemTop = 232448;    // 227 KiB, the most a block may use
@@ -134,23 +143,27 @@ constexpr int kAttn3MergeRow = 132 * 4;  // bytes per (warp, head) row of the me
 #define TQ_ATTN3_REST_MIN_BITS 3
 #endif
 constexpr int attn3_stage_bytes(int kb, int vb) { return 32 * (16 * kb + 16 * vb + 8); }
+// Ring bytes of one warp: its stages, and with sparse V its two V buffers.
+constexpr int attn3_warp_ring_bytes(int kb, int vb, int stages, bool sparse) {
+    return sparse ? stages * 32 * (16 * kb + 8) + 2 * 32 * 16 * vb : stages * attn3_stage_bytes(kb, vb);
+}
 constexpr bool attn3_key_rest(int kb) { return kb >= TQ_ATTN3_REST_MIN_BITS; }
 
 struct Attn3Plan {
     int warps, stages, merge_heads;
     int merge;  // merge buffer
-    int bars;   // one 8-byte mbarrier per (warp, stage)
+    int bars;   // 8-byte mbarriers: one per (warp, stage), then two per warp for sparse V
     int end;    // bytes of dynamic shared memory to ask for
 };
 
-constexpr Attn3Plan attn3_plan(int G, int kb, int vb) {
+constexpr Attn3Plan attn3_plan(int G, int kb, int vb, bool sparse = false) {
     const int heads = G <= 4 ? 4 : 8;
     const int stages = G <= 4 ? 2 : 3;
     const int high = kAttn3TableAt + 65536;  // first byte above the table
     for (int w = (G <= 4 ? TQ_ATTN3_WARP_CAP : 8); w >= 1; --w) {
-        const int ring_end = kAttn3RingAt + w * stages * attn3_stage_bytes(kb, vb);
+        const int ring_end = kAttn3RingAt + w * attn3_warp_ring_bytes(kb, vb, stages, sparse);
         if (ring_end > kAttn3TableAt) continue;
-        const int bars_bytes = 8 * w * stages;
+        const int bars_bytes = 8 * w * (stages + (sparse ? 2 : 0));
         for (int mh = heads; mh >= 1; mh /= 2) {
             const int mb = w * mh * kAttn3MergeRow;
             // merge and barriers above the table, else in the gap below it
@@ -160,7 +173,7 @@ constexpr Attn3Plan attn3_plan(int G, int kb, int vb) {
     }
     return Attn3Plan{0, 0, 0, 0, 0, 0};
 }
-constexpr int attn3_warps(int G, int kb, int vb) { return attn3_plan(G, kb, vb).warps; }
+constexpr int attn3_warps(int G, int kb, int vb, bool sparse = false) { return attn3_plan(G, kb, vb, sparse).warps; }
 
 struct AttnGeometry {
     int n_splits;
@@ -169,13 +182,16 @@ struct AttnGeometry {
     int warp_len;     // d = 128: positions per warp and split
     bool q16;         // the workspace starts with the rotated fp16 queries
 };
+// `sparse`: the call has a sparse-V threshold (the d = 128 kernel then runs
+// its sparse variant, with its own warp count).
 AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d, int kb,
-                           int vb);
+                           int vb, bool sparse = false);
 // d = 128, paged cache with a length per sequence: shorter warp slices, so a
 // sequence's last, partly filled split wastes little of a CTA's time.
 AttnGeometry attn_geometry_paged(int B, int Hq, int Hkv, int64_t max_ctx, int num_sms, int kb, int vb);
 size_t attn_paged_workspace_bound(int B, int Hq, int Hkv, int64_t max_ctx, int num_sms);
-// Workspace that covers every K/V width pair (the public size query takes none).
+// Workspace that covers every K/V width pair and both the dense and the
+// sparse-V kernel (the public size query takes neither).
 size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
@@ -183,9 +199,11 @@ size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // d = 128, paged attention: the work partition written by the planning
 // kernel after the partials: int32 CTA range starts [sms + 1], slot bases
 // [sms + 1], first and last CTA per (batch, KV head) [B * Hq] each (Hq bounds
-// Hkv), rounded up to 256 bytes.
+// Hkv), the attended lengths of the fused append [B]; then, for the sparse-V
+// kernel, the largest score seen so far per (batch, query head) [B * Hq] as
+// order-preserving uint32 keys; rounded up to 256 bytes.
 inline size_t attn3_meta_bytes(int B, int Hq, int sms) {
-    return ((size_t)4 * (2 * ((size_t)sms + 1) + 2 * (size_t)B * Hq + (size_t)B) + 255) / 256 * 256;
+    return ((size_t)4 * (2 * ((size_t)sms + 1) + 3 * (size_t)B * Hq + (size_t)B) + 255) / 256 * 256;
 }
 inline size_t attn3_partial_bytes(int B, int Hq, int n_splits) {
     return ((size_t)4 * B * Hq * n_splits * 130 + 255) / 256 * 256;

@@ -67,12 +67,12 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
 // (256 down to 32 positions) whose work items fill the last wave of CTAs to
 // at least 90%, else the one that fills it best.  Otherwise the longest split
 // (<= 512 positions) that still gives two CTAs per SM.
-AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d, int kb, int vb) {
+AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d, int kb, int vb, bool sparse) {
     AttnGeometry g;
     const int64_t pairs = (int64_t)B * Hkv;
     if (d == 128) {
         const int64_t cap = sms > 0 ? sms : 1;
-        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb);
+        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb, sparse);
         int best = 256;
         double best_eff = -1.0;
         for (int wl = 256; wl >= 32; wl /= 2) {
@@ -140,10 +140,12 @@ size_t attn_paged_workspace_bound(int B, int Hq, int Hkv, int64_t max_ctx, int s
 size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d) {
     size_t most = 0;
     for (int kb = 2; kb <= 4; ++kb)
-        for (int vb = 2; vb <= 4; ++vb) {
-            const size_t w = attn_workspace_bytes(B, Hq, d, attn_geometry(B, Hq, Hkv, ctx_len, sms, d, kb, vb));
-            if (w > most) most = w;
-        }
+        for (int vb = 2; vb <= 4; ++vb)
+            for (int sp = 0; sp < 2; ++sp) {
+                const size_t w =
+                    attn_workspace_bytes(B, Hq, d, attn_geometry(B, Hq, Hkv, ctx_len, sms, d, kb, vb, sp != 0));
+                if (w > most) most = w;
+            }
     return most;
 }
 

@@ -60,13 +60,14 @@ extern "C" tq_status tq_attn_decode_noalloc(const tq_plan* plan, const void* q, 
                                               sparse_v_threshold, out, &nothing);
     if (st != TQ_OK || nothing) return st;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
-    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits);
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), P->d, k_bits, v_bits,
+                                                 sparse_v_threshold > 0.0f);
     if (tq::attn_workspace_bytes(B, Hq, P->d, g) > kScratchBytes) return TQ_ERR_WORKSPACE;
     void* ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
     if (e == cudaSuccess)
         e = tq::launch_attn_decode(*P, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale, sparse_v_threshold,
-                                   out, ws, g, reinterpret_cast<cudaStream_t>(stream));
+                                   out, nullptr, ws, g, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();  // leave no stale error for the caller's next launch check
         tq::set_last_cuda_error(e);

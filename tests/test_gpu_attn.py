@@ -93,6 +93,38 @@ def test_sparse_v(B, Hq, Hkv, d, ctx, cap, kb, vb):
     assert kept.min() < ctx  # the oracle did drop rows
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,d,ctx,kb,vb", [(1, 32, 8, 128, 20000, 3, 2), (2, 8, 2, 128, 3001, 4, 3),
+                                                  (1, 4, 1, 64, 3001, 3, 2)])
+def test_sparse_v_skips_value_rows(B, Hq, Hkv, d, ctx, kb, vb):
+    """A sharpened softmax (query x 6, keys with two x8 outlier channels): the
+    sparse-V call reads the V rows of at most the context (at context 20000
+    well under 80% of them), as tq_attn_decode_ex counts them per (batch, KV
+    head), never fewer than any head of the group keeps in the oracle, and its
+    output stays within the tolerance of both the sparse and the dense oracle.
+    A dense call reads every row."""
+    s, q, host, cache = make_case(11 + ctx, B, Hq, Hkv, d, ctx, kb, vb, n_outliers=2)
+    plan = abi.Plan(d, 42)
+    scale = 1.0 / math.sqrt(d)
+    q = (q.float() * 6).to(torch.bfloat16)
+    out_d, rows_d = abi.tq_attn_decode_ex(plan, q.cuda(), cache, ctx, scale, 0.0)
+    out_s, rows_s = abi.tq_attn_decode_ex(plan, q.cuda(), cache, ctx, scale, 1e-4)
+    torch.cuda.synchronize()
+    rows_d, rows_s = rows_d.cpu().numpy(), rows_s.cpu().numpy()
+    assert np.all(rows_d == ctx)
+    assert np.all(rows_s <= ctx), rows_s
+    if ctx >= 20000:  # enough chunks per CTA for the shared running maximum to settle
+        assert rows_s.sum() < 0.8 * rows_s.size * ctx, rows_s
+    want_sparse, kept = oracle_out(s, q, host, kb, vb, ctx, scale, 1e-4, kept=True)
+    want_dense = oracle_out(s, q, host, kb, vb, ctx, scale)
+    compare_attention(out_s.cpu().numpy(), want_sparse)
+    compare_attention(out_s.cpu().numpy(), want_dense)
+    compare_attention(out_d.cpu().numpy(), want_dense)
+    G = Hq // Hkv
+    assert np.all(kept.reshape(B, Hkv, G).max(axis=2) <= rows_s)
+    print(f"sparse V, d {d} ctx {ctx}: V rows read {rows_s.tolist()} of {ctx}; oracle keeps per head "
+          f"{kept.tolist()}")
+
+
 def test_attention_errors():
     s, q, host, cache = make_case(3, 1, 4, 2, 128, 64, 4, 2)
     plan = abi.Plan(128, 42)
