@@ -308,6 +308,9 @@ tq_status tq::check_attn_decode_args(const tq_plan* plan, const void* q, int B, 
     if (!(std::isfinite(scale)) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
         return TQ_ERR_INVALID_ARG;
     if (ctx_len < 1 || ctx_len > cache.cap) return TQ_ERR_RANGE;
+    // the d = 128 kernel counts work items and positions in 32 bits
+    if (ctx_len > (int64_t(1) << 30) || (int64_t)B * Hkv * ((ctx_len + 31) / 32) > INT32_MAX)
+        return TQ_ERR_UNSUPPORTED;
     if (B == 0) {
         *nothing = true;
         return TQ_OK;
@@ -612,6 +615,7 @@ tq_status tq_attn_decode_paged(const tq_plan* plan, const void* q, int B, int Hq
     if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
         return TQ_ERR_INVALID_ARG;
     if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
+    if (max_ctx > (int64_t(1) << 30)) return TQ_ERR_UNSUPPORTED;  // positions are counted in 32 bits
     if (B == 0) return TQ_OK;
     if (!q || !out || !block_table || !ctx_lens || !paged_pointers_ok(cache)) return TQ_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned4(block_table) || !aligned4(ctx_lens) ||
@@ -654,6 +658,7 @@ tq_status tq_attn_decode_append_paged(const tq_plan* plan, const void* q, const 
     if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
         return TQ_ERR_INVALID_ARG;
     if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
+    if (max_ctx > (int64_t(1) << 30)) return TQ_ERR_UNSUPPORTED;  // positions are counted in 32 bits
     if (B == 0) return TQ_OK;
     if (!q || !k_new || !v_new || !out || !block_table || !positions || !paged_pointers_ok(cache))
         return TQ_ERR_INVALID_ARG;

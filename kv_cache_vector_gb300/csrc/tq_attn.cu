@@ -783,11 +783,14 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     const uint32_t ring = kA3RingAt + (uint32_t)(warp * L::kWarpRing);
     const uint32_t vbuf = ring + (uint32_t)(S * L::kStage);  // SP: V buffers 0 and 1
     float* merge = reinterpret_cast<float*>(gptr(L::kMergeAt));
-    const int64_t i_begin = PAGED ? (int64_t)meta.cta_begin[blockIdx.x] : n_items * blockIdx.x / gridDim.x;
-    const int64_t i_end = PAGED ? (int64_t)meta.cta_begin[blockIdx.x + 1] : n_items * (blockIdx.x + 1) / gridDim.x;
+    // Work items, (batch, KV head) pairs and positions fit in 32 bits (the
+    // host checks it); only cache row indices take 64.
+    const int i_begin = PAGED ? meta.cta_begin[blockIdx.x] : (int)(n_items * blockIdx.x / gridDim.x);
+    const int i_end = PAGED ? meta.cta_begin[blockIdx.x + 1] : (int)(n_items * (blockIdx.x + 1) / gridDim.x);
     const int nC = warp_len / kA3Chunk;
-    const int64_t seg = (int64_t)W * warp_len;
-    const int64_t wofs = (int64_t)warp * kA3Chunk;  // first chunk of the warp in a segment
+    const int seg = W * warp_len;
+    const int wofs = warp * kA3Chunk;  // first chunk of the warp in a segment
+    const int ctx32 = (int)ctx_len;
     constexpr int kStride = W * kA3Chunk;             // from one of its chunks to the next
     bool bad = false;  // warp-uniform: a wait gave up; compute is skipped from then on
     int inflight = 0;  // stages issued and not yet waited for
@@ -797,12 +800,11 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     // same row counts, so both sides skip the empty slots and take stages and
     // phases in the same order, and the producer stays S non-empty slots
     // ahead.  Position and cache row advance by additions.
-    int64_t p_item = i_begin, p_bh = i_begin / n_splits;
-    int p_c = 0, p_split = (int)(i_begin % n_splits), p_st = 0;
-    int64_t p_pos = (int64_t)p_split * seg + wofs;
-    int64_t p_row = p_bh * cache.cap + p_pos;
+    int p_item = i_begin, p_bh = i_begin / n_splits;
+    int p_c = 0, p_split = i_begin % n_splits, p_st = 0;
+    int p_pos = p_split * seg + wofs;
     // paged: the sequence, head and context length of p_bh, cached per pair
-    int64_t p_ctx = ctx_len, p_cbh = -1, p_b = 0;
+    int p_ctx = ctx32, p_cbh = -1, p_b = 0;
     int p_h = 0;
     auto next_item = [&]() {
         p_c = 0;
@@ -811,8 +813,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             p_split = 0;
             ++p_bh;
         }
-        p_pos = (int64_t)p_split * seg + wofs;
-        p_row = p_bh * cache.cap + p_pos;
+        p_pos = p_split * seg + wofs;
     };
     // seek() moves the cursor to the next slot that holds rows (or to the end
     // of the range), finds its row count and, paged, loads its page id.  It
@@ -827,32 +828,32 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 if (p_bh != p_cbh) {
                     p_cbh = p_bh;
                     p_b = p_bh / Hkv;
-                    p_h = (int)(p_bh - p_b * Hkv);
-                    const int64_t len = __ldg(pa.lens + p_b);
-                    p_ctx = len < 0 ? 0 : (len < ctx_len ? len : ctx_len);
+                    p_h = p_bh - p_b * Hkv;
+                    const int len = __ldg(pa.lens + p_b);
+                    p_ctx = len < 0 ? 0 : (len < ctx32 ? len : ctx32);
                 }
             }
-            const int64_t rem = p_ctx - p_pos;
+            const int rem = p_ctx - p_pos;
             if (rem <= 0) {  // the item's later slots of this warp lie further out
                 next_item();
                 continue;
             }
-            q_n = rem >= kA3Chunk ? kA3Chunk : (int)rem;
-            if constexpr (PAGED) q_page = __ldg(pa.bt + p_b * pa.max_pages + (p_pos >> pa.page_shift));
+            q_n = rem >= kA3Chunk ? kA3Chunk : rem;
+            if constexpr (PAGED) q_page = __ldg(pa.bt + (int64_t)p_b * pa.max_pages + (p_pos >> pa.page_shift));
             return;
         }
     };
     auto issue = [&]() {
         if (q_n == 0 || bad) return;
         const int n = q_n;
-        int64_t row = p_row;
+        int64_t row = (int64_t)p_bh * cache.cap + p_pos;
         bool ok = true;
         if constexpr (PAGED) {
             if (q_page < 0 || q_page >= pa.n_pages) {
                 if (lane == 0) report_timeout(status, kA3StatusPage);
                 ok = false;
             } else {
-                row = (((int64_t)q_page * Hkv + p_h) << pa.page_shift) + (p_pos & ((int64_t(1) << pa.page_shift) - 1));
+                row = (((int64_t)q_page * Hkv + p_h) << pa.page_shift) + (p_pos & ((1 << pa.page_shift) - 1));
             }
         }
         uint64_t* bar = bars + p_st;
@@ -865,11 +866,14 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 if constexpr (!SP)
                     bulk_load(sb + L::kVOff, cache.v_packed + row * L::kVRow, (uint32_t)(n * L::kVRow), bar);
             }
-            // lanes past the end copy nothing (source size 0) from a valid row
+            // lanes past the end copy nothing (source size 0) from a valid row;
+            // position l's norms go to slot 4 (l % 8) + l / 8, so that lane
+            // (g, t) finds positions g, g + 8, g + 16, g + 24 in one 16-byte load
             const int64_t r = row + (lane < n ? lane : n - 1);
             const uint32_t sz = lane < n ? 4u : 0u;
-            cp_async4(sb + L::kKnOff + 4u * lane, cache.k_norm + r, sz);
-            cp_async4(sb + L::kVnOff + 4u * lane, cache.v_norm + r, sz);
+            const uint32_t slot = 4u * (4u * (lane & 7) + (lane >> 3));
+            cp_async4(sb + L::kKnOff + slot, cache.k_norm + r, sz);
+            cp_async4(sb + L::kVnOff + slot, cache.v_norm + r, sz);
             cp_async_arrive(bar);
         } else {
             mbar_arrive(bar);  // a bad page: nothing is copied, the chunk's result is undefined
@@ -878,7 +882,6 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             next_item();
         } else {
             p_pos += kStride;
-            p_row += kStride;
         }
         if (++p_st == S) p_st = 0;
         ++inflight;
@@ -895,8 +898,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     bool hok[NG];
     int vexp = 0;  // the V accumulators are in units of 2^vexp
     float vlim = 128.f, vsc = 1.f;
-    int64_t cur_bh = -1;
-    int64_t ctx_run = ctx_len;  // context length of the current (batch, KV head) run
+    int cur_bh = -1;
+    int ctx_run = ctx32;  // context length of the current (batch, KV head) run
     const float thr = P.sparse_thr;
     const bool sparse = thr > 0.f;
     const int srcA = 8 * t + (g >> 1), srcB = srcA + 4;
@@ -966,17 +969,20 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 }
             }
         }
-        // lane (g, t): positions 16u + 8h + g of head 4hg + t
+        // lane (g, t): positions 16u + 8h + g of head 4hg + t; their norms are
+        // the 4 consecutive slots 4g + 2u + h
         float sc[NG][2][2];
         float nvl = 0.f;
+        const uint4 kn4 = lds_v4(sb + L::kKnOff + 16u * g), vn4 = lds_v4(sb + L::kVnOff + 16u * g);
+        const uint32_t knw[4] = {kn4.x, kn4.y, kn4.z, kn4.w}, vnw[4] = {vn4.x, vn4.y, vn4.z, vn4.w};
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int r = 16 * u + 8 * h + g;
                 ok[u][h] = FULL || r < n;
-                const float kn = lds_f32(sb + L::kKnOff + 4u * r);
-                vn[u][h] = lds_f32(sb + L::kVnOff + 4u * r);
+                const float kn = __uint_as_float(knw[2 * u + h]);
+                vn[u][h] = __uint_as_float(vnw[2 * u + h]);
                 if (FULL) nvl = fmaxf(nvl, vn[u][h]);
                 else if (ok[u][h]) nvl = fmaxf(nvl, vn[u][h]);
 #pragma unroll
@@ -1220,10 +1226,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 
     // Items of one (batch, KV head) are consecutive: the warps accumulate
     // across them and publish when the pair changes and at the end.
-    int split = (int)(i_begin % n_splits), cst = 0;
+    int split = i_begin % n_splits, cst = 0;
     uint32_t cph = 0;
-    int64_t bh = i_begin / n_splits;
-    for (int64_t item = i_begin; item <= i_end; ++item) {
+    int bh = i_begin / n_splits;
+    for (int item = i_begin; item <= i_end; ++item) {
         if (item == i_end || bh != cur_bh) {
             flush();
             if (cur_bh >= 0) publish(cur_bh);
@@ -1242,8 +1248,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             const int64_t b = bh / Hkv;
             const int gh = (int)(bh % Hkv);
             if constexpr (PAGED) {
-                const int64_t len = __ldg(pa.lens + b);
-                ctx_run = len < 0 ? 0 : (len < ctx_len ? len : ctx_len);
+                const int len = __ldg(pa.lens + b);
+                ctx_run = len < 0 ? 0 : (len < ctx32 ? len : ctx32);
             }
 #pragma unroll
             for (int hg = 0; hg < NG; ++hg) {
@@ -1272,11 +1278,11 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             }
         }
 
-        int64_t pos = (int64_t)split * seg + wofs;
+        int pos = split * seg + wofs;
         for (int c = 0; c < nC; ++c, pos += kStride) {
-            const int64_t rem = ctx_run - pos;
+            const int rem = ctx_run - pos;
             if (rem <= 0) break;  // this slot and the item's later ones hold no rows
-            const int n = rem >= kA3Chunk ? kA3Chunk : (int)rem;
+            const int n = rem >= kA3Chunk ? kA3Chunk : rem;
             if constexpr (!SP) seek();  // paged: the page id loads while this chunk computes
             if (!bad) {
                 const bool ok = mbar_wait(bars + cst, cph);
@@ -1303,7 +1309,8 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                         fence_async_smem();  // earlier generic reads of the buffer come first
                         mbar_arrive_expect_tx(vb, (uint32_t)(n * L::kVRow));
                         bulk_load(vbuf + (uint32_t)(vi * L::kVBuf),
-                                  cache.v_packed + (cur_bh * cache.cap + pos) * L::kVRow, (uint32_t)(n * L::kVRow), vb);
+                                  cache.v_packed + ((int64_t)cur_bh * cache.cap + pos) * L::kVRow,
+                                  (uint32_t)(n * L::kVRow), vb);
                     }
                     if (keep) vfl |= 1u << vi;
                     // the K stage is done with: the producer refills it now
