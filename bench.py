@@ -682,45 +682,86 @@ def extra_prefill(peak_hbm):
     return res
 
 
+def time_graph(g, iters, flush=None):
+    """Median device time of replays of the CUDA graph g (no host gaps between
+    its launches), flushing L2 before each replay if asked."""
+    return time_events(g.replay, iters, flush)
+
+
 def extra_gemma(peak):
-    """34 layers x 4 KV heads x d 256 x 512 tokens bf16 N(0,1), K4/V4: window
-    encode GB/s (L2 flushed), then the append-only decode step: one tq_append
-    per layer (4 K + 4 V rows), the 34-layer step replayed from a CUDA graph."""
+    """34 layers x 4 KV heads x d 256 x 512 tokens bf16 N(0,1), K4/V4:
+    window encode and window decode (to bf16) GB/s, each the K and V calls of
+    all 34 layers' window replayed from a CUDA graph with L2 flushed before
+    every replay (200 replays); then the append-only decode step, one
+    tq_append per layer (4 K + 4 V rows), and the decode attention of one
+    token per layer (batch 1, 8 query / 4 KV heads, context 513), each
+    34-layer step replayed from a CUDA graph."""
     import torch
     from kv_cache_vector_gb300 import abi, synth
-    L, Hkv, d, T, steps = 34, 4, 256, 512, 50
+    L, Hkv, Hq, d, T, steps = 34, 4, 8, 256, 512, 50
     plan = abi.Plan(d, 42)
-    win = synth.device_normal(4000, (2, L * Hkv * T, d))
-    pk = torch.empty(L * Hkv * T, d // 2, dtype=torch.uint8, device="cuda")
-    nm = torch.empty(L * Hkv * T, device="cuda")
+    rows = L * Hkv * T
+    win = synth.device_normal(4000, (2, rows, d))
+    pk = torch.empty(2, rows, d // 2, dtype=torch.uint8, device="cuda")
+    nm = torch.empty(2, rows, device="cuda")
+    dec = torch.empty(2, rows, d, dtype=torch.bfloat16, device="cuda")
     buf = torch.zeros(4 * 129 * 2 ** 20 // 4, device="cuda")
-    f = lambda: (abi.tq_encode(plan, 4, win[0], pk, nm), abi.tq_encode(plan, 4, win[1], pk, nm))
-    for _ in range(3):
-        f()
-    ms = time_events(f, 200, lambda: flush_l2(buf))
-    wbytes = 2 * L * Hkv * T * (d * 2 + d // 2 + 4)
+    stream = torch.cuda.Stream()
+
+    def graph_of(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    enc = graph_of(lambda: (abi.tq_encode(plan, 4, win[0], pk[0], nm[0]), abi.tq_encode(plan, 4, win[1], pk[1], nm[1])))
+    ms = time_graph(enc, 200, lambda: flush_l2(buf))
+    decg = graph_of(lambda: (abi.tq_decode(plan, 4, pk[0], nm[0], out=dec[0]),
+                             abi.tq_decode(plan, 4, pk[1], nm[1], out=dec[1])))
+    dms = time_graph(decg, 200, lambda: flush_l2(buf))
+    wbytes = 2 * rows * (d * 2 + d // 2 + 4)
     caches = [abi.Cache.empty(1, Hkv, T + steps, d, 4, 4) for _ in range(L)]
+    for l in range(L):
+        caches[l].k_packed[0, :, :T] = pk[0].view(L, Hkv, T, -1)[l]
+        caches[l].k_norm[0, :, :T] = nm[0].view(L, Hkv, T)[l]
+        caches[l].v_packed[0, :, :T] = pk[1].view(L, Hkv, T, -1)[l]
+        caches[l].v_norm[0, :, :T] = nm[1].view(L, Hkv, T)[l]
     nk = synth.device_normal(4002, (L, 1, Hkv, 1, d))
     nv = synth.device_normal(4003, (L, 1, Hkv, 1, d))
     one = lambda: abi.tq_append(plan, caches[0], nk[0], nv[0], T)
     for _ in range(3):
         one()
     append_ms = time_events(one, 50)
-    stream = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for l in range(L):
-            abi.tq_append(plan, caches[l], nk[l], nv[l], T)
-    for _ in range(3):
-        g.replay()
-    step_ms = time_events(g.replay, 50)
+    app = graph_of(lambda: [abi.tq_append(plan, caches[l], nk[l], nv[l], T) for l in range(L)])
+    step_ms = time_graph(app, 50)
+    q = synth.device_normal(4004, (L, 1, Hq, d))
+    out = torch.empty(L, 1, Hq, d, device="cuda")
+    wss = [torch.empty(abi.tq_attn_workspace_bytes(1, Hq, Hkv, d, T + 1), dtype=torch.uint8, device="cuda")
+           for _ in range(L)]
+    att = graph_of(lambda: [abi.tq_attn_decode(plan, q[l], caches[l], T + 1, 1.0 / math.sqrt(d), out=out[l],
+                                               workspace=wss[l]) for l in range(L)])
+    att_ms = time_graph(att, 50)
+    abytes = L * Hkv * (T + 1) * (d * 8 // 8 + 8)
     return {"window_encode": {"ms": round(ms, 4), "GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
                               "frac": round(wbytes / (ms * 1e-3) / 1e9 / peak, 4),
                               "frac_nominal": round(wbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
-                              "repeats": 200},
+                              "repeats": 200, "timing": "graph replay of the K and V calls, L2 flushed"},
+            "window_decode_bf16": {"ms": round(dms, 4), "GBps": round(wbytes / (dms * 1e-3) / 1e9, 1),
+                                   "frac": round(wbytes / (dms * 1e-3) / 1e9 / peak, 4),
+                                   "frac_nominal": round(wbytes / (dms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                                   "repeats": 200, "timing": "graph replay of the K and V calls, L2 flushed"},
             "append_us_per_call": round(append_ms * 1e3, 2),
             "append_step_us_34_layers_graph": round(step_ms * 1e3, 2),
-            "config": "34L x 4Hkv x d256 x 512 tokens bf16, K4/V4, then 1-token appends (B1)"}
+            "attn_step_us_34_layers_graph": round(att_ms * 1e3, 2),
+            "attn_GBps": round(abytes / (att_ms * 1e-3) / 1e9, 1),
+            "config": "34L x 4Hkv x d256 x 512 tokens bf16, K4/V4; 1-token appends (B1); decode attention "
+                      "B1 Hq8/Hkv4 ctx513 per layer"}
 
 
 # ------------------------------------------------------- oracle timing

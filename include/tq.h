@@ -158,8 +158,8 @@ tq_status tq_append(const tq_plan *plan, int k_bits, int v_bits, const void *k_n
 size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len);
 
 /* Workspace bytes tq_attn_decode_paged needs for these sizes on the current
- * device (split-K partials and the work partition).  0 for invalid sizes or
- * d != 128. */
+ * device (split-K partials, and for d = 128 the work partition).  0 for
+ * invalid sizes or d not in {32, 64, 128, 256}. */
 size_t tq_attn_paged_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t max_ctx);
 
 /* Decode attention over the packed cache, one query token per sequence
@@ -278,7 +278,8 @@ tq_status tq_append_paged(const tq_plan *plan, int k_bits, int v_bits, const voi
 /* Decode attention over a paged cache with a context length per sequence:
  * for sequence b and query head h, the tq_attn_decode result over positions
  * [0, min(ctx_lens[b], max_ctx)) of sequence b (an empty context gives a zero
- * output row).  d = 128 only.
+ * output row).  d in {32, 64, 128, 256}: the tensor-core kernel at d = 128,
+ * the CUDA-core one otherwise.
  *   q:   [B][Hq][d] bf16, device;  out: [B][Hq][d] fp32, device
  *   block_table: [B][max_pages] int32, device;  ctx_lens: [B] int32, device
  *   max_ctx: an upper bound of the lengths, <= max_pages * page_size; it sizes
@@ -286,9 +287,9 @@ tq_status tq_append_paged(const tq_plan *plan, int k_bits, int v_bits, const voi
  *     tq_attn_paged_workspace_bytes(B, Hq, Hkv, 128, max_ctx) bytes.
  * A page id outside [0, n_pages) is not read; the device status word is set
  * to 33 and that chunk's result is undefined.
- * Errors: as tq_attn_decode; TQ_ERR_UNSUPPORTED also for d != 128 or a
- * page_size that is not a power of two >= 32; TQ_ERR_RANGE if max_ctx < 1 or
- * max_ctx > max_pages * page_size. */
+ * Errors: as tq_attn_decode; TQ_ERR_UNSUPPORTED also for d not in {32, 64,
+ * 128, 256}, B > 65535, max_ctx > 2^30 or a page_size that is not a power of
+ * two >= 32; TQ_ERR_RANGE if max_ctx < 1 or max_ctx > max_pages * page_size. */
 tq_status tq_attn_decode_paged(const tq_plan *plan, const void *q, int B, int Hq, int Hkv,
                                tq_paged_cache cache, const int32_t *block_table, int max_pages,
                                const int32_t *ctx_lens, int64_t max_ctx, int k_bits, int v_bits,
@@ -301,8 +302,9 @@ tq_status tq_attn_decode_paged(const tq_plan *plan, const void *q, int B, int Hq
  * and the cached K and V are read for attention).  For sequence b the new
  * rows are written at position positions[b], exactly as tq_append_paged
  * writes them, and the output is the tq_attn_decode_paged result over
- * positions [0, min(positions[b] + 1, max_ctx)).  The append rides on the
- * attention's first launch; no launch is added.  d = 128 only.
+ * positions [0, min(positions[b] + 1, max_ctx)).  At d = 128 the append rides
+ * on the attention's first launch (no launch is added); at d in {32, 64, 256}
+ * the append is its own launch before the attention.
  *   q:      [B][Hq][d] bf16, device;  out: [B][Hq][d] fp32, device
  *   k_new, v_new: [B][Hkv][d] (kv_dtype), device
  *   block_table: [B][max_pages] int32, device;  positions: [B] int32, device

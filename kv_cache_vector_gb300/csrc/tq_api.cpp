@@ -506,8 +506,10 @@ size_t tq_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
 }
 
 size_t tq_attn_paged_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t max_ctx) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_ctx < 1 || d != 128) return 0;
-    return tq::attn_paged_workspace_bound(B, Hq, Hkv, max_ctx, tq::num_sms());
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_ctx < 1) return 0;
+    if (d == 128) return tq::attn_paged_workspace_bound(B, Hq, Hkv, max_ctx, tq::num_sms());
+    if (d != 32 && d != 64 && d != 256) return 0;
+    return tq::attn_workspace_bound(B, Hq, Hkv, max_ctx, tq::num_sms(), d);
 }
 
 tq_status tq_attn_decode_ex(const tq_plan* plan, const void* q, int B, int Hq, int Hkv,
@@ -569,6 +571,38 @@ tq_cache_view paged_as_view(const tq_paged_cache& c) {
     v.cap = 0;  // unused on the paged paths
     return v;
 }
+
+// Paged attention for d != 128 (the generic kernel), after the common checks:
+// sequence b attends over lens[b] + len_plus positions, clamped to max_ctx.
+tq_status generic_paged(const tq::Plan& P, const void* q, int B, int Hq, int Hkv, const tq_paged_cache& cache,
+                        const int32_t* block_table, int max_pages, const int32_t* lens, int len_plus,
+                        int64_t max_ctx, int shift, int k_bits, int v_bits, float scale, float sparse_v_threshold,
+                        float* out, void* workspace, size_t workspace_bytes, tq_stream_t stream) {
+    const tq::AttnGeometry g = tq::attn_geometry(B, Hq, Hkv, max_ctx, tq::num_sms(), P.d, k_bits, v_bits);
+    if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P.d, g)) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(q) || !device_accessible(out) || !device_accessible(workspace) ||
+        !device_accessible(block_table) || !device_accessible(lens) || !paged_accessible(cache))
+        return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    tq::fill_attn_params(P, k_bits, v_bits, scale, sparse_v_threshold, A);
+    const tq::PagedArgs pa{block_table, lens, cache.n_pages, max_pages, shift};
+    const tq_cache_view view = paged_as_view(cache);
+    auto st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = dispatch_attn_d(P.d, [&](auto D) -> cudaError_t {
+        constexpr int d = decltype(D)::value;
+        if constexpr (d == 128) {
+            return cudaErrorInvalidValue;  // the d = 128 kernel has its own paged path
+        } else {
+            switch (k_bits) {
+                case 2: return tq::launch_attn_generic_paged<d, 2>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, len_plus, st);
+                case 3: return tq::launch_attn_generic_paged<d, 3>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, len_plus, st);
+                default: return tq::launch_attn_generic_paged<d, 4>(v_bits, q, B, Hq, Hkv, view, max_ctx, out, workspace, g, A, pa, len_plus, st);
+            }
+        }
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
 }  // namespace
 
 tq_status tq_append_paged(const tq_plan* plan, int k_bits, int v_bits, const void* k_new,
@@ -611,16 +645,19 @@ tq_status tq_attn_decode_paged(const tq_plan* plan, const void* q, int B, int Hq
     if (!valid_bits(k_bits) || !valid_bits(v_bits) || Hq / Hkv > 8) return TQ_ERR_UNSUPPORTED;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
     const int shift = page_shift_of(cache.page_size);
-    if (P->d != 128 || shift < 0) return TQ_ERR_UNSUPPORTED;
+    if ((P->d != 128 && P->d != 32 && P->d != 64 && P->d != 256) || shift < 0) return TQ_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
         return TQ_ERR_INVALID_ARG;
     if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
-    if (max_ctx > (int64_t(1) << 30)) return TQ_ERR_UNSUPPORTED;  // positions are counted in 32 bits
+    if (max_ctx > (int64_t(1) << 30) || B > 65535) return TQ_ERR_UNSUPPORTED;  // 32-bit positions; grid
     if (B == 0) return TQ_OK;
     if (!q || !out || !block_table || !ctx_lens || !paged_pointers_ok(cache)) return TQ_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || !aligned4(block_table) || !aligned4(ctx_lens) ||
         !paged_aligned(cache))
         return TQ_ERR_ALIGNMENT;
+    if (P->d != 128)
+        return generic_paged(*P, q, B, Hq, Hkv, cache, block_table, max_pages, ctx_lens, 0, max_ctx, shift, k_bits,
+                             v_bits, scale, sparse_v_threshold, out, workspace, workspace_bytes, stream);
     tq::AttnGeometry g = tq::attn_geometry_paged(B, Hq, Hkv, max_ctx, tq::num_sms(), k_bits, v_bits);
     if ((int64_t)B * Hkv * g.n_splits > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // work items are int32
     if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
@@ -654,17 +691,34 @@ tq_status tq_attn_decode_append_paged(const tq_plan* plan, const void* q, const 
         return TQ_ERR_UNSUPPORTED;
     const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
     const int shift = page_shift_of(cache.page_size);
-    if (P->d != 128 || shift < 0) return TQ_ERR_UNSUPPORTED;
+    if ((P->d != 128 && P->d != 32 && P->d != 64 && P->d != 256) || shift < 0) return TQ_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !(sparse_v_threshold >= 0.0f) || !std::isfinite(sparse_v_threshold))
         return TQ_ERR_INVALID_ARG;
     if (max_ctx < 1 || max_ctx > ((int64_t)max_pages << shift)) return TQ_ERR_RANGE;
-    if (max_ctx > (int64_t(1) << 30)) return TQ_ERR_UNSUPPORTED;  // positions are counted in 32 bits
+    if (max_ctx > (int64_t(1) << 30) || B > 65535) return TQ_ERR_UNSUPPORTED;  // 32-bit positions; grid
     if (B == 0) return TQ_OK;
     if (!q || !k_new || !v_new || !out || !block_table || !positions || !paged_pointers_ok(cache))
         return TQ_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || !aligned4(block_table) ||
         !aligned4(positions) || !paged_aligned(cache))
         return TQ_ERR_ALIGNMENT;
+    if (P->d != 128) {
+        // the append, then the attention over positions[b] + 1 rows: two launches
+        if (!device_accessible(k_new) || !device_accessible(v_new)) return TQ_ERR_INVALID_ARG;
+        tq::RowParams PK, PV;
+        fill_row_params(*P, k_bits, PK);
+        fill_row_params(*P, v_bits, PV);
+        const tq::PagedArgs pa{block_table, positions, cache.n_pages, max_pages, shift};
+        const tq_cache_view view = paged_as_view(cache);
+        const cudaError_t e = dispatch_d(P->d, [&](auto D) {
+            return tq::launch_append_paged_d<decltype(D)::value>(k_bits, v_bits, kv_dtype, k_new, v_new, B, Hkv,
+                                                                 view, pa, PK, PV,
+                                                                 reinterpret_cast<cudaStream_t>(stream));
+        });
+        if (e != cudaSuccess) return cuda_fail(e);
+        return generic_paged(*P, q, B, Hq, Hkv, cache, block_table, max_pages, positions, 1, max_ctx, shift, k_bits,
+                             v_bits, scale, sparse_v_threshold, out, workspace, workspace_bytes, stream);
+    }
     tq::AttnGeometry g = tq::attn_geometry_paged(B, Hq, Hkv, max_ctx, tq::num_sms(), k_bits, v_bits);
     if ((int64_t)B * Hkv * g.n_splits > INT32_MAX) return TQ_ERR_UNSUPPORTED;  // work items are int32
     if (!workspace || workspace_bytes < tq::attn_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;

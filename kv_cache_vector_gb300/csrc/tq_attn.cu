@@ -24,24 +24,59 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxGroup = 8;
 
-template <int BITS, int D>
-__device__ __forceinline__ void load_packed_row(const uint8_t* p, uint32_t (&w)[(D * BITS + 31) / 32]) {
-    load_bytes<D * BITS / 8>(p, w);
+// Cache row of position p of (sequence b, KV head g): contiguous, or through
+// the block table (-1 for a page id out of range, which is not read).
+template <bool PAGED>
+__device__ __forceinline__ int64_t attn_row(const tq_cache_view& cache, const PagedArgs& pa, int Hkv, int b, int g,
+                                            int64_t p) {
+    if constexpr (PAGED) {
+        const int page = __ldg(pa.bt + (int64_t)b * pa.max_pages + (p >> pa.page_shift));
+        if (page < 0 || page >= pa.n_pages) return -1;
+        return (((int64_t)page * Hkv + g) << pa.page_shift) + (p & ((int64_t(1) << pa.page_shift) - 1));
+    } else {
+        return ((int64_t)b * Hkv + g) * cache.cap + p;
+    }
 }
 
-template <int D, int KB, int VB>
+// The lane's LB <= 32 bits of a packed row starting at bit LB * lane.
+template <int LB>
+__device__ __forceinline__ uint32_t lane_bits(const uint8_t* row, int lane) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
+    const int bit0 = lane * LB, wi = bit0 / 32, sh = bit0 % 32;
+    uint32_t x = __ldg(w + wi) >> sh;
+    if (sh + LB > 32) x |= __ldg(w + wi + 1) << (32 - sh);
+    return x;
+}
+
+// Head dimensions other than 128 (CUDA cores, fp32 centroids).  CTA (split,
+// KV head, sequence) takes positions [split * split_len, ..) of the
+// sequence's length: ctx_len (contiguous), or, PAGED, lens[b] + len_plus
+// clamped to [0, ctx_len] (len_plus = 1 when lens holds the positions just
+// appended).  The group's queries are rotated into shared memory; the scores
+// take a warp per position (lane l holds dims [l D/32, (l+1) D/32) of the key,
+// the query in a transposed copy so that lanes read consecutive words), then
+// the exponentials, then the V product a warp per position.  A split with no
+// positions writes an empty partial (m = -FLT_MAX, l = 0).
+template <int D, int KB, int VB, bool PAGED>
 __global__ void __launch_bounds__(kAttnThreads)
 k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view cache,
              int64_t ctx_len, int split_len, int n_splits, float* __restrict__ ws,
-             const __grid_constant__ AttnParams P) {
+             const __grid_constant__ AttnParams P, const PagedArgs pa, int len_plus, int* status) {
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = Hq / Hkv;
+    int64_t Ls = ctx_len;
+    if constexpr (PAGED) {
+        const int64_t l = (int64_t)__ldg(pa.lens + b) + len_plus;
+        Ls = l < 0 ? 0 : (l < ctx_len ? l : ctx_len);
+    }
     const int64_t t0 = (int64_t)split * split_len;
-    const int len = (int)min((int64_t)split_len, ctx_len - t0);
+    const int len = (int)(Ls - t0 < 0 ? 0 : (Ls - t0 < split_len ? Ls - t0 : split_len));
+    constexpr int EPL = D / 32;  // dims per lane
 
     extern __shared__ float smem[];
     float* qrot = smem;                          // [G][D]
-    float* sc = qrot + kMaxGroup * D;            // [G][split_len]: scores, then exp
+    float* qT = qrot + kMaxGroup * D;            // [G * EPL][32]: dim l EPL + e of head h at (h EPL + e) 32 + l
+    float* sc = qT + kMaxGroup * D;              // [G][split_len]: scores, then exp
     float* accs = sc + kMaxGroup * split_len;    // [G][D] cross-warp sum
     float* red = accs + kMaxGroup * D;           // [kAttnWarps][kMaxGroup]
     float* mh = red + kAttnWarps * kMaxGroup;    // [kMaxGroup] max per head
@@ -50,6 +85,13 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
     float* vcen = kcen + 16;                     // [16]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (len == 0) {  // block-uniform: an empty partial
+        for (int i = tid; i < G * (D + 2); i += blockDim.x) {
+            const int h = i / (D + 2), j = i % (D + 2);
+            ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = j == D ? -FLT_MAX : 0.f;
+        }
+        return;
+    }
     if (tid < 16) {
         kcen[tid] = P.kcen[tid];
         vcen[tid] = P.vcen[tid];
@@ -66,35 +108,50 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
     }
     __syncthreads();
+    for (int i = tid; i < G * D; i += blockDim.x) {
+        const int h = i / D, j = i % D;
+        qT[(h * EPL + j % EPL) * 32 + j / EPL] = qrot[i];
+    }
+    __syncthreads();
 
-    const int64_t row0 = ((int64_t)b * Hkv + g) * cache.cap + t0;
     constexpr int KRB = D * KB / 8, VRB = D * VB / 8;
+    constexpr int KLB = EPL * KB, VLB = EPL * VB;  // bits per lane (<= 32)
 
-    // ---- pass 1: scores sigma = n_k * (qrot . c_k) for every position
+    // ---- pass 1: sigma = n_k * (qrot . c_k), a warp per position
     float mloc[kMaxGroup];
 #pragma unroll
     for (int h = 0; h < kMaxGroup; ++h) mloc[h] = -FLT_MAX;
-    for (int t = tid; t < len; t += blockDim.x) {
-        uint32_t w[(D * KB + 31) / 32];
-        load_packed_row<KB, D>(cache.k_packed + (row0 + t) * KRB, w);
-        const float nk = __ldg(cache.k_norm + row0 + t);
-        float acc[kMaxGroup];
+    for (int t = warp; t < len; t += kAttnWarps) {
+        const int64_t row = attn_row<PAGED>(cache, pa, Hkv, b, g, t0 + t);
+        if (row < 0) {  // warp-uniform: a page id out of range, nothing read
+            if (lane == 0) {
+                report_timeout(status, 33);
+                for (int h = 0; h < G; ++h) sc[h * split_len + t] = -FLT_MAX;
+            }
+            continue;
+        }
+        const uint32_t bits = lane_bits<KLB>(cache.k_packed + row * KRB, lane);
+        const float nk = __ldg(cache.k_norm + row);
+        float part[kMaxGroup];
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) acc[h] = 0.f;
+        for (int h = 0; h < kMaxGroup; ++h) part[h] = 0.f;
 #pragma unroll
-        for (int j = 0; j < D; ++j) {
-            const float c = kcen[unpack_one<KB>(w, j)];
+        for (int e = 0; e < EPL; ++e) {
+            const float c = kcen[(bits >> (e * KB)) & ((1u << KB) - 1)];
 #pragma unroll
             for (int h = 0; h < kMaxGroup; ++h)
-                if (h < G) acc[h] = fmaf(qrot[h * D + j], c, acc[h]);
+                if (h < G) part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
         }
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
+        for (int h = 0; h < kMaxGroup; ++h) {
             if (h < G) {
-                const float s = acc[h] * nk;
-                sc[h * split_len + t] = s;
+                float s = part[h];
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                s *= nk;
+                if (lane == 0) sc[h * split_len + t] = s;
                 mloc[h] = fmaxf(mloc[h], s);
             }
+        }
     }
     // block max per head
 #pragma unroll
@@ -140,8 +197,6 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
 
     // ---- pass 2: acc += p_t * n_v * c_v in the rotated domain.  A warp takes
     // one position at a time; lane l owns elements [l*EPL, (l+1)*EPL).
-    constexpr int EPL = D / 32;
-    constexpr int LBITS = EPL * VB;  // bits per lane per row (<= 32)
     float acc[kMaxGroup][EPL];
 #pragma unroll
     for (int h = 0; h < kMaxGroup; ++h)
@@ -155,14 +210,11 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         for (int h = 0; h < kMaxGroup; ++h)
             if (h < G) pm = fmaxf(pm, sc[h * split_len + t]);
         if (pm < thr) continue;  // warp-uniform
+        const int64_t row = attn_row<PAGED>(cache, pa, Hkv, b, g, t0 + t);
+        if (row < 0) continue;  // warp-uniform: a page id out of range
         ++nread;
-        const uint8_t* vr = cache.v_packed + (row0 + t) * VRB;
-        const int bit0 = lane * LBITS;
-        const uint32_t* vw = reinterpret_cast<const uint32_t*>(vr);
-        const int wi = bit0 / 32, sh = bit0 % 32;
-        uint32_t bitsv = __ldg(vw + wi) >> sh;
-        if (sh + LBITS > 32) bitsv |= __ldg(vw + wi + 1) << (32 - sh);
-        const float nv = __ldg(cache.v_norm + row0 + t);
+        const uint32_t bitsv = lane_bits<VLB>(cache.v_packed + row * VRB, lane);
+        const float nv = __ldg(cache.v_norm + row);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
             const float c = vcen[(bitsv >> (e * VB)) & ((1u << VB) - 1)] * nv;
@@ -208,7 +260,8 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
         L = fmaf(f, base[s * (D + 2) + D + 1], L);
         a = fmaf(f, base[s * (D + 2) + j], a);
     }
-    o[j] = __uint_as_float(__float_as_uint(a / L) ^ (P.two_sided ? P.sgn2[j] : 0u));
+    const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
+    o[j] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? P.sgn2[j] : 0u));
     fwht_smem<D>(o, 1);
     out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
 }
@@ -1555,16 +1608,18 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     return cudaGetLastError();
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool PAGED = false>
 cudaError_t attn_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
                         int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
-                        const AttnParams& P, cudaStream_t s) {
-    auto fn = k_attn_split<D, KB, VB>;
-    const size_t smem = sizeof(float) * (kMaxGroup * D * 2 + (size_t)kMaxGroup * geo.split_len +
+                        const AttnParams& P, cudaStream_t s, const PagedArgs& pa = PagedArgs{},
+                        int len_plus = 0) {
+    auto fn = k_attn_split<D, KB, VB, PAGED>;
+    const size_t smem = sizeof(float) * (kMaxGroup * D * 3 + (size_t)kMaxGroup * geo.split_len +
                                          kAttnWarps * kMaxGroup + 2 * kMaxGroup + 32);
     dim3 grid(geo.n_splits, Hkv, B);
     fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
-                                       geo.split_len, geo.n_splits, static_cast<float*>(ws), P);
+                                       geo.split_len, geo.n_splits, static_cast<float*>(ws), P, pa, len_plus,
+                                       status_word());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k_attn_combine<D><<<B * Hq, D, 0, s>>>(static_cast<const float*>(ws), geo.n_splits, out, P);
@@ -1614,6 +1669,26 @@ template cudaError_t launch_attn128_paged<TQ_UNIT_KB>(int, const void*, int, int
                                                       int64_t, float*, void*, const AttnGeometry&,
                                                       const AttnParams&, const PagedArgs&, cudaStream_t,
                                                       const AttnAppend*);
+#endif
+
+#if TQ_UNIT_D != 128
+// Head dimensions other than 128, paged cache: the generic kernel with the
+// block table; len_plus = 1 when pa.lens holds the positions just appended.
+template <int D, int KB>
+cudaError_t launch_attn_generic_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
+                                      const tq_cache_view& pages, int64_t max_ctx, float* out, void* workspace,
+                                      const AttnGeometry& g, const AttnParams& P, const PagedArgs& pa,
+                                      int len_plus, cudaStream_t s) {
+    switch (v_bits) {
+        case 2: return dev::attn_launch<D, KB, 2, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
+        case 3: return dev::attn_launch<D, KB, 3, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
+        default: return dev::attn_launch<D, KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
+    }
+}
+template cudaError_t launch_attn_generic_paged<TQ_UNIT_D, TQ_UNIT_KB>(int, const void*, int, int, int,
+                                                                       const tq_cache_view&,
+                                                           int64_t, float*, void*, const AttnGeometry&,
+                                                           const AttnParams&, const PagedArgs&, int, cudaStream_t);
 #endif
 
 #if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB)

@@ -466,7 +466,9 @@ constexpr uint32_t kUmBarAt = kUmHbAt + 128 * 128 * 2;          // barriers, TME
 constexpr uint32_t kUmRepAt = 65536;                            // replicated window (64 KB)
 constexpr uint32_t kUmXsAt = 131072;                            // X stages
 constexpr uint32_t kUmEnd = kUmXsAt + kUmStages * kUmStageBytes;
-static_assert(kUmBarAt + (2 * kUmStages + 2 * kUmAcc) * 8 + 16 <= kUmRepAt, "layout");
+constexpr uint32_t kUmSgnAt = kUmBarAt + 256;  // s and s2 masks (1 KB), read when building D H
+static_assert(kUmBarAt + (2 * kUmStages + 2 * kUmAcc) * 8 + 16 <= kUmSgnAt, "layout");
+static_assert(kUmSgnAt + 1024 <= kUmRepAt, "layout");
 static_assert(kUmEnd <= 232448, "shared memory");
 // The window: cells k = rint(w * kLutScale) in [-128, 128), i.e. |w| < 0.5.
 constexpr int kRepCells = 256;
@@ -516,10 +518,18 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
 
     // B operand: element (n, k) = s2_n * (-1)^popcount(n & k) * s_k (s2 all
     // +1 unless the signs are two-sided), stored like a TMA 128-byte-swizzled
-    // K-major tile (two 64-column halves of 16 KB).
+    // K-major tile (two 64-column halves of 16 KB).  The sign masks are staged
+    // in shared memory first: indexed reads of the parameter bank with a
+    // different index per lane would be serialised.
+    uint32_t* sg = reinterpret_cast<uint32_t*>(at(kUmSgnAt));
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        sg[i] = P.sgn[i];
+        sg[128 + i] = P.sgn2[i];
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
         const int n = i >> 7, k = i & 127;
-        const bool neg = (((__popc(n & k) & 1) != 0) != (P.sgn[k] != 0u)) != (P.sgn2[n] != 0u);
+        const bool neg = (((__popc(n & k) & 1) != 0) != (sg[k] != 0u)) != (sg[128 + n] != 0u);
         const int off = (k >> 6) * 16384 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
         *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBF80u : 0x3F80u;
     }
@@ -711,6 +721,316 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<kUmAcc * 128>(tmem);
+    }
+}
+
+// ------------------------------------------- encode on tcgen05 (d = 256)
+//
+// H_256 = [[H, H], [H, -H]] (Sylvester order), so for a row x = [x0, x1] of
+// 2 x 128 elements, y = H_256 (s . x) = [A0 + A1, A0 - A1] with
+// A_p = H (s_p . x_p).  For a tile of 128 rows both A_p are tensor-core GEMMs
+// against the constant +-1 matrices D_p H, as in the d = 128 encoder: X is
+// TMA-loaded in 32 KB halves (columns 0..127, then 128..255) through three
+// stages, and half p goes to accumulator columns 128 p of the tile's
+// 256-column pair.  The epilogue forms A0 +- A1, the norm (||y||^2 =
+// 2 (||A0||^2 + ||A1||^2) = d ||x||^2), the second signs when the plan has
+// them (they differ between the two output halves, so they are not folded
+// into D_p H), buckets and packs.  The bucketing table is the d = 128 one
+// with 16 columns of 8 bytes (a 64-bit load is served a half-warp at a time,
+// so lanes l and l + 16 share a column) at cell stride 128 bytes.
+
+constexpr int kU2Rows = 128;
+constexpr int kU2Stages = 3;               // X halves of 32 KB
+constexpr int kU2Acc = 2;                  // accumulator pairs of 2 x 128 columns
+constexpr int kU2Threads = 10 * 32;
+constexpr int kU2HalfBytes = kU2Rows * 128 * 2;
+constexpr uint32_t kU2HbAt = 2048;                                 // D0 H, D1 H (2 x 32 KB)
+constexpr uint32_t kU2XsAt = kU2HbAt + 2 * 32768;                  // X stages (1024-aligned)
+constexpr uint32_t kU2BarAt = kU2XsAt + kU2Stages * kU2HalfBytes;  // barriers, TMEM slot
+constexpr uint32_t kU2RepAt = 196608;                              // bucketing table (32 KB)
+constexpr uint32_t kU2End = kU2RepAt + kRepCells * 128;
+static_assert(kU2XsAt % 1024 == 0, "swizzle atoms");
+constexpr uint32_t kU2SgnAt = kU2BarAt + 256;  // the sign masks s, then s2 (2 x 1 KB)
+static_assert(kU2BarAt + (2 * kU2Stages + 2 * kU2Acc) * 8 + 16 <= kU2SgnAt, "layout");
+static_assert(kU2SgnAt + 2048 <= kU2RepAt, "layout");
+static_assert((kU2RepAt & 0x7F80u) == 0, "table base: cell bits free");
+static_assert(kU2End <= 232448, "shared memory");
+
+template <int BITS>
+__global__ void __launch_bounds__(kU2Threads, 1)
+k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* __restrict__ packed,
+                 float* __restrict__ norms, int* status, const __grid_constant__ RowParams P) {
+    constexpr int RB = 256 * BITS / 8, HB = RB / 2;  // bytes per row and per output half
+    constexpr int NW = 128 * BITS / 32;              // packed words per output half
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t sbase = smem_addr(smem_raw);
+    if (sbase > kU2HbAt) {  // the layout assumes dynamic memory starts lower
+        if (threadIdx.x == 0) report_timeout(status, 67);
+        return;
+    }
+    auto at = [&](uint32_t a) { return smem_raw + (a - sbase); };
+    unsigned char* xs = at(kU2XsAt);
+    unsigned char* hb = at(kU2HbAt);
+    uint64_t* full = reinterpret_cast<uint64_t*>(at(kU2BarAt));
+    uint64_t* empty = full + kU2Stages;
+    uint64_t* accf = empty + kU2Stages;
+    uint64_t* acce = accf + kU2Acc;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(acce + kU2Acc);
+    uint32_t* sg = reinterpret_cast<uint32_t*>(at(kU2SgnAt));
+    const uint32_t* sg2 = sg + 256;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the sign masks, once per thread from the parameter bank (indexed reads
+    // of it with a different index per lane would be serialised)
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        sg[i] = P.sgn[i];
+        sg[256 + i] = P.sgn2[i];
+    }
+
+    // Barriers first: the producer starts loading X while the other warps
+    // build the operands and the table (a named barrier among warps 1-9).
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kU2Stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < kU2Acc; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], 4);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t tmem = 0;
+    if (warp > 0) {
+        // B operands: D_p H, element (n, k) = (-1)^popcount(n & k) * s_{128 p + k},
+        // each stored like a 128-byte-swizzled K-major tile of two 64-column
+        // halves; 8 consecutive k per 16-byte store
+        for (int i = threadIdx.x - 32; i < 2 * 128 * 16; i += blockDim.x - 32) {
+            const int p = i >> 11, n = (i >> 4) & 127, k8 = i & 15;
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t h2 = 0;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 8 * k8 + 2 * j + e;
+                    const bool neg = ((__popc(n & k) & 1) != 0) != (sg[128 * p + k] != 0u);
+                    h2 |= (neg ? 0xBF80u : 0x3F80u) << (16 * e);
+                }
+                w[j] = h2;
+            }
+            const int off = p * 32768 + (k8 >> 3) * 16384 + n * 128 + (((k8 & 7) ^ (n & 7)) << 4);
+            *reinterpret_cast<uint4*>(hb + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // bucketing table: one cell per thread, written to its 16 columns
+        for (int c = threadIdx.x - 32; c < kRepCells; c += blockDim.x - 32) {
+            const LutEntry e = lut_cell(P.bnd, (1 << BITS) - 1, c - kRepCells / 2);
+            LutEntry* row = reinterpret_cast<LutEntry*>(at(kU2RepAt + 128u * c));
+#pragma unroll
+            for (int col = 0; col < 16; ++col) row[col] = e;
+        }
+        fence_proxy_async_smem();  // the operands are read by the tensor cores
+        if (warp == 1) tmem_alloc<kU2Acc * 256>(slot);
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(kU2Threads - 32) : "memory");
+        tc_fence_after();
+        tmem = *slot;
+    }
+    const int64_t n_tiles = (n_rows + kU2Rows - 1) / kU2Rows;
+
+    if (warp == 0) {  // ---- TMA producer: half h = 2 * (tile iteration) + p
+        if (lane == 0) {
+            tma_prefetch_desc(&xmap);
+            int h = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                for (int p = 0; p < 2; ++p, ++h) {
+                    const int s = h % kU2Stages;
+                    if (h >= kU2Stages && !mbar_wait(&empty[s], ((h / kU2Stages) - 1) & 1)) {
+                        report_timeout(status, 61);
+                        goto drain;
+                    }
+                    mbar_arrive_expect_tx(&full[s], kU2HalfBytes);
+                    tma_load_2d(xs + s * kU2HalfBytes, &xmap, 128 * p, (int)(tile * kU2Rows), &full[s]);
+                    tma_load_2d(xs + s * kU2HalfBytes + 16384, &xmap, 128 * p + 64, (int)(tile * kU2Rows), &full[s]);
+                }
+            }
+        drain:
+            for (int j = (h > kU2Stages ? h - kU2Stages : 0); j < h; ++j)
+                if (!mbar_wait(&full[j % kU2Stages], (j / kU2Stages) & 1)) {
+                    report_timeout(status, 62);
+                    break;
+                }
+        }
+    } else if (warp == 1) {  // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16(128, 128, true);
+            const uint32_t xs_a = smem_addr(xs), hb_a = smem_addr(hb);
+            int it = 0, h = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+                const int a = it % kU2Acc;
+                if (it >= kU2Acc && !mbar_wait(&acce[a], ((it / kU2Acc) - 1) & 1)) {
+                    report_timeout(status, 63);
+                    break;
+                }
+                bool ok = true;
+                for (int p = 0; p < 2; ++p, ++h) {
+                    const int s = h % kU2Stages;
+                    if (!mbar_wait(&full[s], (h / kU2Stages) & 1)) {
+                        report_timeout(status, 64);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_f16(tmem + a * 256 + p * 128, umma_desc_sw128(xs_a + s * kU2HalfBytes + off),
+                                 umma_desc_sw128(hb_a + p * 32768 + off), idesc, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&accf[a]);
+            }
+            // the last accumulators must be complete before tensor memory is freed
+            for (int j = (it > kU2Acc ? it - kU2Acc : 0); j < it; ++j)
+                if (!mbar_wait(&accf[j % kU2Acc], (j / kU2Acc) & 1)) {
+                    report_timeout(status, 65);
+                    break;
+                }
+        }
+    } else {  // ---- epilogue: warps 2-5 take even tiles, 6-9 odd tiles
+        const int wg = (warp - 2) >> 2, q = warp & 3;
+        const int r = 32 * q + lane;
+        constexpr float kMagic = 12582912.0f + (float)(kRepCells / 2);
+        const F2 M2 = f2(kMagic, kMagic);
+        const uint32_t rep_slot = kU2RepAt + 8u * (lane & 15);
+        int it = wg;
+        for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < n_tiles;
+             tile += 2 * (int64_t)gridDim.x, it += 2) {
+            const int a = it % kU2Acc;
+            if (!mbar_wait(&accf[a], (it / kU2Acc) & 1)) {
+                report_timeout(status, 66);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + a * 256;
+            // The chunk loops stay rolled: the whole row unrolled does not fit
+            // the instruction cache.
+            F2 sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {  // columns of A0 then A1
+                uint32_t y[32];
+                tmem_ld32(ta + 32 * c, y);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const F2 p0 = f2(__uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+                    const F2 p1 = f2(__uint_as_float(y[i + 2]), __uint_as_float(y[i + 3]));
+                    sa = f2_fma(p0, p0, sa);
+                    sb = f2_fma(p1, p1, sb);
+                }
+            }
+            float s0, s1, s2, s3;
+            f2_split(sa, s0, s1);
+            f2_split(sb, s2, s3);
+            const float ss = 2.0f * ((s0 + s1) + (s2 + s3));  // = ||y||^2 = d ||x||^2
+            const float n = __fsqrt_rn(ss * (1.0f / 256.0f));
+            const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // u = y * inv
+            const float ks = inv * (float)kLutScale;
+            const F2 K2 = f2(ks, ks);
+            const int64_t row = tile * kU2Rows + r;
+            const bool valid = row < n_rows;
+            uint8_t* dst = packed + row * RB;
+            // chunk c holds output dims 32c.. (low half) and 128 + 32c.. (high half):
+            // 32 indices, CW words, per half
+            constexpr int CW = BITS;
+            auto put = [&](uint32_t (&w)[CW], int i, int id) {
+                const int pos = i * BITS, wi = pos / 32, sh = pos % 32;
+                w[wi] += (uint32_t)id << sh;
+                if (sh + BITS > 32) w[wi + 1] += (uint32_t)id >> (32 - sh);
+            };
+            auto store = [&](int c, const uint32_t (&wl)[CW], const uint32_t (&wh)[CW]) {
+                if (!valid) return;
+                uint32_t* lo = reinterpret_cast<uint32_t*>(dst + 4 * BITS * c);
+                uint32_t* hi = reinterpret_cast<uint32_t*>(dst + HB + 4 * BITS * c);
+#pragma unroll
+                for (int k = 0; k < CW; ++k) {
+                    lo[k] = wl[k];
+                    hi[k] = wh[k];
+                }
+            };
+            auto halves = [&](const uint32_t (&a0)[32], const uint32_t (&a1)[32], int i, int c, float& ylo,
+                              float& yhi) {
+                ylo = __uint_as_float(a0[i]) + __uint_as_float(a1[i]);
+                yhi = __uint_as_float(a0[i]) - __uint_as_float(a1[i]);
+                if (P.two_sided) {
+                    ylo = __uint_as_float(__float_as_uint(ylo) ^ sg2[32 * c + i]);
+                    yhi = __uint_as_float(__float_as_uint(yhi) ^ sg2[128 + 32 * c + i]);
+                }
+            };
+            uint32_t out = 0u;  // bits outside the table's cell byte: some |u| >= 0.5, or not finite
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a0[32], a1[32];
+                tmem_ld32(ta + 32 * c, a0);
+                tmem_ld32(ta + 128 + 32 * c, a1);
+                tmem_wait_ld();
+                uint32_t wl[CW], wh[CW];
+#pragma unroll
+                for (int k = 0; k < CW; ++k) wl[k] = wh[k] = 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float ylo, yhi;
+                    halves(a0, a1, i, c, ylo, yhi);
+                    float fx, fy;
+                    f2_split(f2_fma(f2(ylo, yhi), K2, M2), fx, fy);
+                    const uint32_t bx = __float_as_uint(fx), by = __float_as_uint(fy);
+                    out |= (bx ^ kRepMagicBits) | (by ^ kRepMagicBits);
+                    const LutEntry e0 = lds_entry(((bx << 7) & 0x7F80u) | rep_slot);
+                    const LutEntry e1 = lds_entry(((by << 7) & 0x7F80u) | rep_slot);
+                    put(wl, i, e0.lo + (fmaf(ylo, inv, -e0.thr) >= 0.0f ? 1 : 0));
+                    put(wh, i, e1.lo + (fmaf(yhi, inv, -e1.thr) >= 0.0f ? 1 : 0));
+                }
+                store(c, wl, wh);
+            }
+            // rows with a coordinate outside the table's window: exact binary
+            // search over the boundaries, written over the fast path's bytes
+            // (the tensor-memory loads are warp-wide)
+            const bool slow = (out & ~0xFFu) != 0u;
+            if (__any_sync(0xFFFFFFFFu, slow)) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t a0[32], a1[32];
+                    tmem_ld32(ta + 32 * c, a0);
+                    tmem_ld32(ta + 128 + 32 * c, a1);
+                    tmem_wait_ld();
+                    if (slow) {
+                        uint32_t wl[CW], wh[CW];
+#pragma unroll
+                        for (int k = 0; k < CW; ++k) wl[k] = wh[k] = 0;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float ylo, yhi;
+                            halves(a0, a1, i, c, ylo, yhi);
+                            put(wl, i, bucket_search<BITS>(P.bnd, ylo, inv));
+                            put(wh, i, bucket_search<BITS>(P.bnd, yhi, inv));
+                        }
+                        store(c, wl, wh);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[a]);
+            if (valid) norms[row] = n;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<kU2Acc * 256>(tmem);
     }
 }
 
@@ -963,12 +1283,30 @@ cudaError_t enc_umma(const void* x, int64_t n, uint8_t* pk, float* nm, const Row
     return cudaGetLastError();
 }
 
+template <int BITS>
+cudaError_t enc_umma256(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
+    CUtensorMap map;
+    cudaError_t e = make_rows_map(&map, x, 2, 256, (uint64_t)n, dev::kU2Rows);
+    if (e != cudaSuccess) return e;
+    auto fn = dev::k_encode_umma256<BITS>;
+    // absolute layout: ask for kU2End bytes (the dynamic block starts below kU2HbAt)
+    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev::kU2End);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (n + dev::kU2Rows - 1) / dev::kU2Rows;
+    int64_t grid = num_sms();
+    if (grid > tiles) grid = tiles;
+    fn<<<(unsigned)grid, dev::kU2Threads, dev::kU2End, s>>>(map, n, pk, nm, status_word(), P);
+    return cudaGetLastError();
+}
+
 template <int D, int BITS, typename T>
 cudaError_t enc(const void* x, int64_t n, uint8_t* pk, float* nm, const RowParams& P, cudaStream_t s) {
-    // d = 128 bf16: the transform on the tensor cores; d = 64 bf16: TMA-fed
-    // CUDA-core butterflies; other shapes: one thread per row (two at d = 256)
+    // d = 128 and 256 bf16: the transform on the tensor cores; d = 64 bf16:
+    // TMA-fed CUDA-core butterflies; other shapes: one thread per row (two at d = 256)
     if constexpr (D == 128 && sizeof(T) == 2) {
         return enc_umma<BITS>(x, n, pk, nm, P, s);
+    } else if constexpr (D == 256 && sizeof(T) == 2) {
+        return enc_umma256<BITS>(x, n, pk, nm, P, s);
     } else if constexpr (D == 64 && sizeof(T) == 2) {
         return enc_tma<D, BITS>(x, n, pk, nm, P, s);
     } else {

@@ -246,6 +246,14 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
                                  const tq_cache_view& pages, int64_t max_ctx, float* out,
                                  void* workspace, const AttnGeometry& g, const AttnParams& P,
                                  const PagedArgs& pa, cudaStream_t s, const AttnAppend* app = nullptr);
+// Paged attention for head dimensions other than 128 (tq_attn.cu, compiled
+// in the d units other than 128): the generic kernel over the block table,
+// lengths pa.lens[b] + len_plus.
+template <int D, int KB>
+cudaError_t launch_attn_generic_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
+                                      const tq_cache_view& pages, int64_t max_ctx, float* out, void* workspace,
+                                      const AttnGeometry& g, const AttnParams& P, const PagedArgs& pa,
+                                      int len_plus, cudaStream_t s);
 // Prefill (multi-query, causal) attention, d = 128 (tq_prefill.cu, one unit
 // per K width).  workspace: the query rotation as a 128 x 128 bf16 matrix
 // (kPfRotBytes), one expanded tile image of kPfImgBytes per block of 128

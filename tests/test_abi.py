@@ -135,7 +135,8 @@ def test_hot_call_validation_before_launch(L):
     assert L.tq_attn_decode(h, A, 1, 8, 2, cv, 8, 4, 2, f(1.0), f(-1.0), A, A, 1 << 20, s) == 1
     assert L.tq_attn_workspace_bytes(1, 6, 4, 128, 8) == 0
     assert L.tq_attn_paged_workspace_bytes(1, 6, 4, 128, 8) == 0
-    assert L.tq_attn_paged_workspace_bytes(1, 8, 2, 64, 8) == 0
+    assert L.tq_attn_paged_workspace_bytes(1, 8, 2, 64, 8) > 0    # d = 64: the generic kernel
+    assert L.tq_attn_paged_workspace_bytes(1, 8, 2, 16, 8) == 0   # no attention below d = 32
     p.close()
 
 
@@ -208,7 +209,10 @@ def test_paged_call_validation_before_launch(L):
     W = 1 << 24
     assert L.tq_attn_decode_paged(h, A, 1, 6, 4, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
     assert L.tq_attn_decode_paged(h, A, 1, 32, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2
-    assert L.tq_attn_decode_paged(p64.handle, A, 1, 8, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W,
+    # d = 64 runs the generic kernel: its workspace check still comes before any launch
+    assert L.tq_attn_decode_paged(p64.handle, A, 1, 8, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, 16,
+                                  s) == 5
+    assert L.tq_attn_decode_paged(p16.handle, A, 1, 8, 2, pc(), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A, A, W,
                                   s) == 2
     assert L.tq_attn_decode_paged(h, A, 1, 8, 2, pc(page_size=100), A, 4, A, 100, 4, 3, f(1.0), f(0.0), A,
                                   A, W, s) == 2
@@ -226,7 +230,7 @@ def test_paged_call_validation_before_launch(L):
     assert fa(None, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 1
     assert fa(h, A, A, A, 7, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2  # dtype
     assert fa(h, A, A, A, 1, 1, 32, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2  # GQA 16
-    assert fa(p64.handle, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2
+    assert fa(p16.handle, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 2
     assert fa(h, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 257, 4, 3, f(1.0), f(0.0), A, A, W, s) == 4
     assert fa(h, A, A, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, 16, s) == 5
     assert fa(h, A, A + 8, A, 1, 1, 8, 2, pc(), A, 4, A, 256, 4, 3, f(1.0), f(0.0), A, A, W, s) == 3

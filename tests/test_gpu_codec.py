@@ -80,13 +80,13 @@ def test_encode_edge_rows(d):
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_encode_spiky_rotated_rows_bf16(d, bits):
     """bf16 rows whose rotated, normalised coordinates reach |u| = 1 or sit
     near |u| = 0.5: a sign-flipped column of the Hadamard matrix, scaled, plus
-    seeded noise.  The d = 128 encoder buckets |u| < 0.5 through a windowed
-    table and redoes any other row by binary search; both must agree with the
-    oracle."""
+    seeded noise.  The d = 128 and d = 256 encoders bucket |u| < 0.5 through a
+    windowed table and redo any other row by binary search; both must agree
+    with the oracle."""
     s = O.signs(42, d)
     noise = synth.normal_rows(4242 + d, 64, d).double().numpy()
     j = np.arange(d)

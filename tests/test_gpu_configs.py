@@ -239,20 +239,21 @@ def test_gemma_window_encode_and_append_loop():
                            pk_t[0].reshape(-1, d // 2).cpu().numpy(), nm_t[0].reshape(-1).cpu().numpy())
 
 
-@pytest.mark.parametrize("bits,in_dtype,out_dtype", [(4, torch.bfloat16, torch.bfloat16),
-                                                     (2, torch.bfloat16, torch.bfloat16),
-                                                     (3, torch.float32, torch.float32)])
-def test_codec_ragged_large(bits, in_dtype, out_dtype):
-    """1,000,003 rows of d 128 (a multiple of neither 128 nor 32): the
-    persistent encoder and decoder take several tiles per CTA, so their
-    stage and accumulator phases wrap, and the last tile is ragged (the
-    tensor-map load past the end fills zeros, the tensor-map store clips).
-    Encode, then decode; 2048 sampled rows and the last 200 rows against the
-    oracle."""
-    d, n = 128, 1_000_003
+@pytest.mark.parametrize("d,bits,in_dtype,out_dtype", [(128, 4, torch.bfloat16, torch.bfloat16),
+                                                       (128, 2, torch.bfloat16, torch.bfloat16),
+                                                       (128, 3, torch.float32, torch.float32),
+                                                       (256, 4, torch.bfloat16, torch.bfloat16),
+                                                       (256, 3, torch.bfloat16, torch.float32)])
+def test_codec_ragged_large(d, bits, in_dtype, out_dtype):
+    """1,000,003 rows (a multiple of neither 128 nor 32): the persistent
+    encoders and decoders take several tiles per CTA, so their stage and
+    accumulator phases wrap, and the last tile is ragged (the tensor-map load
+    past the end fills zeros, the tensor-map store clips).  Encode, then
+    decode; 2048 sampled rows and the last 200 rows against the oracle."""
+    n = 1_000_003
     plan = abi.Plan(d, 42)
     s = O.signs(42, d)
-    x = synth.lowrank_rows(1234, n, d, dtype=in_dtype, stream=bits, device="cuda")
+    x = synth.lowrank_rows(1234 + d, n, d, dtype=in_dtype, stream=bits, device="cuda")
     pk, nm = abi.tq_encode(plan, bits, x)
     y = abi.tq_decode(plan, bits, pk, nm, out_dtype=out_dtype)
     torch.cuda.synchronize()
@@ -263,7 +264,7 @@ def test_codec_ragged_large(bits, in_dtype, out_dtype):
     same = np.all(opk == pk[idx].cpu().numpy(), axis=1)
     compare_decode(s, bits, opk[same], onm[same], y[idx].float().cpu().numpy()[same],
                    bf16=out_dtype == torch.bfloat16)
-    print("ragged codec", bits, st)
+    print("ragged codec", d, bits, st)
 
 
 def test_decode_attention_ragged_large_context():

@@ -89,9 +89,10 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64, 256])
 @pytest.mark.parametrize("lens,Hq,Hkv,page,kb,vb", CASES)
-def test_paged_attention_parity(lens, Hq, Hkv, page, kb, vb):
-    d = 128
+def test_paged_attention_parity(lens, Hq, Hkv, page, kb, vb, d):
+    """The tensor-core kernel at d = 128, the generic one at 64 and 256."""
     plan = abi.Plan(d, 42)
     s, q, seqs, cache, bt, max_pages = make_paged(11, lens, Hq, Hkv, d, page, kb, vb)
     scale = 1.0 / math.sqrt(d)
@@ -209,13 +210,15 @@ def test_paged_append_then_attend():
         compare_attention(got[b][None], oracle_seq(s, q[b], seq, kb, vb, L + 1, scale)[None])
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("kv_dtype", [torch.bfloat16, torch.float32])
-def test_fused_append_attend_matches_two_calls(kv_dtype):
+def test_fused_append_attend_matches_two_calls(kv_dtype, d):
     """tq_attn_decode_append_paged writes the same cache bytes as
     tq_append_paged and returns what tq_attn_decode_paged returns over the
-    lengths + 1; both agree with the oracle over the grown sequences."""
+    lengths + 1; both agree with the oracle over the grown sequences (one
+    launch sequence at d = 128, the append and then the generic kernel at
+    d = 256)."""
     lens, Hq, Hkv, page, kb, vb = [63, 64, 10, 1, 300], 8, 2, 64, 4, 3
-    d = 128
     plan = abi.Plan(d, 42)
     s, q, seqs, cache, bt, max_pages = make_paged(15, lens, Hq, Hkv, d, page, kb, vb, extra_slot=True)
     B = len(lens)
