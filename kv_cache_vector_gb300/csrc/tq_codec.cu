@@ -736,8 +736,8 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
 // 2 (||A0||^2 + ||A1||^2) = d ||x||^2), the second signs when the plan has
 // them (they differ between the two output halves, so they are not folded
 // into D_p H), buckets and packs.  The bucketing table is the d = 128 one
-// with 16 columns of 8 bytes (a 64-bit load is served a half-warp at a time,
-// so lanes l and l + 16 share a column) at cell stride 128 bytes.
+// (count of boundaries below the cell, the boundary inside it) with 16
+// lane-replicated columns of 8 bytes at cell stride 128 bytes.
 
 constexpr int kU2Rows = 128;
 constexpr int kU2Stages = 3;               // X halves of 32 KB
@@ -748,11 +748,12 @@ constexpr uint32_t kU2HbAt = 2048;                                 // D0 H, D1 H
 constexpr uint32_t kU2XsAt = kU2HbAt + 2 * 32768;                  // X stages (1024-aligned)
 constexpr uint32_t kU2BarAt = kU2XsAt + kU2Stages * kU2HalfBytes;  // barriers, TMEM slot
 constexpr uint32_t kU2RepAt = 196608;                              // bucketing table (32 KB)
-constexpr uint32_t kU2End = kU2RepAt + kRepCells * 128;
+constexpr uint32_t kU2End = kU2RepAt + kRepCells * 128;  // 16 columns of 8 bytes per cell
 static_assert(kU2XsAt % 1024 == 0, "swizzle atoms");
-constexpr uint32_t kU2SgnAt = kU2BarAt + 256;  // the sign masks s, then s2 (2 x 1 KB)
+constexpr uint32_t kU2SgnAt = kU2BarAt + 256;    // the sign masks s, then s2 (2 x 1 KB)
+constexpr uint32_t kU2CellAt = kU2SgnAt + 2048;  // the table's cells, once each (2 KB)
 static_assert(kU2BarAt + (2 * kU2Stages + 2 * kU2Acc) * 8 + 16 <= kU2SgnAt, "layout");
-static_assert(kU2SgnAt + 2048 <= kU2RepAt, "layout");
+static_assert(kU2CellAt + 8 * kRepCells <= kU2RepAt, "layout");
 static_assert((kU2RepAt & 0x7F80u) == 0, "table base: cell bits free");
 static_assert(kU2End <= 232448, "shared memory");
 
@@ -784,6 +785,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
         sg[i] = P.sgn[i];
         sg[256 + i] = P.sgn2[i];
+        reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2);
     }
 
     // Barriers first: the producer starts loading X while the other warps
@@ -822,13 +824,11 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
             const int off = p * 32768 + (k8 >> 3) * 16384 + n * 128 + (((k8 & 7) ^ (n & 7)) << 4);
             *reinterpret_cast<uint4*>(hb + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        // bucketing table: one cell per thread, written to its 16 columns
-        for (int c = threadIdx.x - 32; c < kRepCells; c += blockDim.x - 32) {
-            const LutEntry e = lut_cell(P.bnd, (1 << BITS) - 1, c - kRepCells / 2);
-            LutEntry* row = reinterpret_cast<LutEntry*>(at(kU2RepAt + 128u * c));
-#pragma unroll
-            for (int col = 0; col < 16; ++col) row[col] = e;
-        }
+        // bucketing table: the cells, replicated into 16 columns (consecutive
+        // lanes write consecutive columns: no bank conflict)
+        const LutEntry* cells = reinterpret_cast<const LutEntry*>(at(kU2CellAt));
+        for (int i = threadIdx.x - 32; i < kRepCells * 16; i += blockDim.x - 32)
+            *reinterpret_cast<LutEntry*>(at(kU2RepAt + 8u * i)) = cells[i >> 4];
         fence_proxy_async_smem();  // the operands are read by the tensor cores
         if (warp == 1) tmem_alloc<kU2Acc * 256>(slot);
         tc_fence_before();
@@ -915,14 +915,10 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
             }
             tc_fence_after();
             const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + a * 256;
-            // The chunk loops stay rolled: the whole row unrolled does not fit
-            // the instruction cache.
+            // The rare slow path below stays rolled over its chunks: with it
+            // unrolled too, the code outgrows the instruction cache.
             F2 sa = f2(0.f, 0.f), sb = f2(0.f, 0.f);
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {  // columns of A0 then A1
-                uint32_t y[32];
-                tmem_ld32(ta + 32 * c, y);
-                tmem_wait_ld();
+            auto sumsq = [&](const uint32_t (&y)[32]) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const F2 p0 = f2(__uint_as_float(y[i]), __uint_as_float(y[i + 1]));
@@ -930,6 +926,13 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     sa = f2_fma(p0, p0, sa);
                     sb = f2_fma(p1, p1, sb);
                 }
+            };
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // columns of A0 then A1
+                uint32_t y[32];
+                tmem_ld32(ta + 32 * c, y);
+                tmem_wait_ld();
+                sumsq(y);
             }
             float s0, s1, s2, s3;
             f2_split(sa, s0, s1);
@@ -970,12 +973,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 }
             };
             uint32_t out = 0u;  // bits outside the table's cell byte: some |u| >= 0.5, or not finite
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                uint32_t a0[32], a1[32];
-                tmem_ld32(ta + 32 * c, a0);
-                tmem_ld32(ta + 128 + 32 * c, a1);
-                tmem_wait_ld();
+            auto bucket_chunk = [&](const uint32_t (&a0)[32], const uint32_t (&a1)[32], int c) {
                 uint32_t wl[CW], wh[CW];
 #pragma unroll
                 for (int k = 0; k < CW; ++k) wl[k] = wh[k] = 0;
@@ -993,6 +991,16 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     put(wh, i, e1.lo + (fmaf(yhi, inv, -e1.thr) >= 0.0f ? 1 : 0));
                 }
                 store(c, wl, wh);
+            };
+            // the common path unrolled (as the d = 128 epilogue): independent
+            // elements across the whole row for the scheduler to overlap
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t a0[32], a1[32];
+                tmem_ld32(ta + 32 * c, a0);
+                tmem_ld32(ta + 128 + 32 * c, a1);
+                tmem_wait_ld();
+                bucket_chunk(a0, a1, c);
             }
             // rows with a coordinate outside the table's window: exact binary
             // search over the boundaries, written over the fast path's bytes
