@@ -74,6 +74,15 @@ def _lib():
         _i8p, _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
         ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _f32p, _u8p, _f32p, ctypes.c_int, _f32p, _u8p, _f32p,
         _f64p, ctypes.c_double, _f64p]
+    L.orc_qjl_matrix.argtypes = [ctypes.c_uint64, ctypes.c_int, _f64p]
+    L.orc_encode_qjl.argtypes = [_i8p, _i8p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _f64p, _f64p,
+                                 ctypes.c_int64, _u8p, _f32p, _f32p, _f64p]
+    L.orc_decode_qjl.argtypes = [_i8p, _i8p, ctypes.c_int, ctypes.c_int, _f32p, _f64p, _u8p, _f32p, _f32p,
+                                 ctypes.c_int64, _f64p]
+    L.orc_attention_qjl.argtypes = [
+        _i8p, _i8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int, _f32p, _f64p, _u8p, _f32p, _f32p, ctypes.c_int, _f32p, _u8p, _f32p, _f64p,
+        ctypes.c_double, _f64p]
     return L
 
 
@@ -262,4 +271,75 @@ def attention_prefill(s, q, k_packed, k_norm, v_packed, v_norm, k_bits, v_bits, 
                                  _p(kc, _f32p), _p(k_packed, _u8p), _p(k_norm, _f32p),
                                  v_bits, _p(vc, _f32p), _p(v_packed, _u8p), _p(v_norm, _f32p),
                                  _p(q, _f64p), float(scale), _p(out, _f64p))
+    return out
+
+
+# ------------------------------------------------------------ QJL residual keys
+# Reading ("CITATIONS", Google TurboQuant entry; "TurboQuant KV Cache
+# Compression -- Spec", Why not QJL?): b bits = a (b - 1)-bit MSE index per
+# coordinate plus one sign of a Gaussian projection of the rotated residual per
+# coordinate; the residual norm gamma rides beside the row norm.  Full
+# statement in tq_oracle.h.
+
+def qjl_matrix(seed: int, d: int) -> np.ndarray:
+    """The d x d Gaussian projection S drawn from the plan seed's stream."""
+    S = np.empty((d, d), np.float64)
+    _lib().orc_qjl_matrix(ctypes.c_uint64(seed), d, _p(S, _f64p))
+    return S
+
+
+def encode_qjl(s: np.ndarray, bits: int, x: np.ndarray, S: np.ndarray, s2: np.ndarray | None = None,
+               kind: str = "sphere", want_proj: bool = False):
+    """x: [n, d]. Returns packed [n, d*bits/8] uint8, norms [n] and gamma [n]
+    (float32), and with want_proj the projections S r [n, d] in double."""
+    x = np.ascontiguousarray(x, np.float64)
+    n, d = x.shape
+    assert 2 <= bits and (d * (bits - 1)) % 8 == 0
+    cen, bnd = codebook_f32(d, bits - 1, kind)
+    S = np.ascontiguousarray(S, np.float64)
+    packed = np.empty((n, d * bits // 8), np.uint8)
+    norms = np.empty(n, np.float32)
+    rnorms = np.empty(n, np.float32)
+    proj = np.empty((n, d), np.float64) if want_proj else None
+    _lib().orc_encode_qjl(_p(s, _i8p), _s2p(s2), d, bits, _p(cen, _f32p), _p(bnd, _f32p), _p(S, _f64p),
+                          _p(x, _f64p), n, _p(packed, _u8p), _p(norms, _f32p), _p(rnorms, _f32p),
+                          _p(proj, _f64p) if want_proj else None)
+    return (packed, norms, rnorms, proj) if want_proj else (packed, norms, rnorms)
+
+
+def decode_qjl(s: np.ndarray, bits: int, packed: np.ndarray, norms: np.ndarray, rnorms: np.ndarray,
+               S: np.ndarray, s2: np.ndarray | None = None, kind: str = "sphere") -> np.ndarray:
+    packed = np.ascontiguousarray(packed, np.uint8)
+    norms = np.ascontiguousarray(norms, np.float32)
+    rnorms = np.ascontiguousarray(rnorms, np.float32)
+    n = norms.shape[0]
+    d = packed.shape[-1] * 8 // bits
+    cen, _ = codebook_f32(d, bits - 1, kind)
+    S = np.ascontiguousarray(S, np.float64)
+    out = np.empty((n, d), np.float64)
+    _lib().orc_decode_qjl(_p(s, _i8p), _s2p(s2), d, bits, _p(cen, _f32p), _p(S, _f64p), _p(packed, _u8p),
+                          _p(norms, _f32p), _p(rnorms, _f32p), n, _p(out, _f64p))
+    return out
+
+
+def attention_qjl(s, q, k_packed, k_norm, k_rnorm, S, v_packed, v_norm, k_bits, v_bits, ctx_len, scale,
+                  s2=None, kind="sphere"):
+    """Dense decode attention with QJL keys. q: [B, Hq, d]; k_packed:
+    [B, Hkv, cap, d*kb/8]; k_norm, k_rnorm: [B, Hkv, cap]; values plain."""
+    q = np.ascontiguousarray(q, np.float64)
+    B, Hq, d = q.shape
+    Hkv, cap = k_norm.shape[1], k_norm.shape[2]
+    kc, _ = codebook_f32(d, k_bits - 1, kind)
+    vc, _ = codebook_f32(d, v_bits, kind)
+    k_packed = np.ascontiguousarray(k_packed, np.uint8)
+    v_packed = np.ascontiguousarray(v_packed, np.uint8)
+    k_norm = np.ascontiguousarray(k_norm, np.float32)
+    k_rnorm = np.ascontiguousarray(k_rnorm, np.float32)
+    v_norm = np.ascontiguousarray(v_norm, np.float32)
+    S = np.ascontiguousarray(S, np.float64)
+    out = np.empty((B, Hq, d), np.float64)
+    _lib().orc_attention_qjl(_p(s, _i8p), _s2p(s2), d, B, Hq, Hkv, cap, ctx_len, k_bits, _p(kc, _f32p),
+                             _p(S, _f64p), _p(k_packed, _u8p), _p(k_norm, _f32p), _p(k_rnorm, _f32p),
+                             v_bits, _p(vc, _f32p), _p(v_packed, _u8p), _p(v_norm, _f32p), _p(q, _f64p),
+                             float(scale), _p(out, _f64p))
     return out

@@ -504,3 +504,123 @@ void orc_attention_prefill(const int8_t *s, const int8_t *s2, int d, int B, int 
         free(sig);
     }
 }
+
+/* ------------------------------------------------------ QJL residual keys */
+
+/* The Gaussian projection of the QJL stage (reading in tq_oracle.h). */
+void orc_qjl_matrix(uint64_t seed, int d, double *S) {
+    uint64_t state = seed;
+    for (int i = 0; i < 2 * d; ++i) orc_splitmix64_next(&state); /* s1, s2 */
+    const double two53 = 9007199254740992.0;
+    for (int64_t k = 0; k < (int64_t)d * d; ++k) {
+        double u1 = (double)(orc_splitmix64_next(&state) >> 11) / two53;
+        double u2 = (double)(orc_splitmix64_next(&state) >> 11) / two53;
+        S[k] = sqrt(-2.0 * log(1.0 - u1)) * cos(2.0 * M_PI * u2);
+    }
+}
+
+void orc_encode_qjl(const int8_t *s, const int8_t *s2, int d, int bits, const float *c_mse,
+                    const float *b_mse, const double *S, const double *x, int64_t n_rows,
+                    uint8_t *packed, float *norms, float *rnorms, double *proj_out) {
+    int rb = d * bits / 8, ib = d * (bits - 1) / 8;
+    double *y = (double *)malloc(sizeof(double) * d);
+    double *r = (double *)malloc(sizeof(double) * d);
+    uint8_t *idx = (uint8_t *)malloc((size_t)d);
+    uint8_t *sg = (uint8_t *)malloc((size_t)d);
+    for (int64_t row = 0; row < n_rows; ++row) {
+        const double *xr = x + row * d;
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += xr[i] * xr[i];
+        double n = sqrt(ss);
+        orc_rotate(s, s2, d, xr, y);
+        norms[row] = (float)n;
+        /* MSE stage on b - 1 bits, then the residual of the normalised row */
+        double rr = 0.0;
+        for (int i = 0; i < d; ++i) {
+            double u = (n > 0.0) ? y[i] / n : 0.0;
+            idx[i] = (uint8_t)orc_bucket((float)u, bits - 1, b_mse);
+            r[i] = u - (double)c_mse[idx[i]];
+            rr += r[i] * r[i];
+        }
+        rnorms[row] = (float)(n * sqrt(rr));
+        /* QJL stage: the signs of S r */
+        for (int k = 0; k < d; ++k) {
+            double p = 0.0;
+            for (int j = 0; j < d; ++j) p += S[(int64_t)k * d + j] * r[j];
+            if (proj_out) proj_out[row * d + k] = p;
+            sg[k] = p >= 0.0 ? 1 : 0;
+        }
+        orc_pack(idx, d, bits - 1, packed + row * rb);
+        orc_pack(sg, d, 1, packed + row * rb + ib);
+    }
+    free(y);
+    free(r);
+    free(idx);
+    free(sg);
+}
+
+void orc_decode_qjl(const int8_t *s, const int8_t *s2, int d, int bits, const float *c_mse,
+                    const double *S, const uint8_t *packed, const float *norms, const float *rnorms,
+                    int64_t n_rows, double *out) {
+    int rb = d * bits / 8, ib = d * (bits - 1) / 8;
+    double *yr = (double *)malloc(sizeof(double) * d);
+    uint8_t *idx = (uint8_t *)malloc((size_t)d);
+    uint8_t *sg = (uint8_t *)malloc((size_t)d);
+    const double kappa = sqrt(M_PI / 2.0) / (double)d;
+    for (int64_t row = 0; row < n_rows; ++row) {
+        orc_unpack(packed + row * rb, d, bits - 1, idx);
+        orc_unpack(packed + row * rb + ib, d, 1, sg);
+        double n = (double)norms[row], g = (double)rnorms[row];
+        for (int i = 0; i < d; ++i) {
+            double t = 0.0;
+            for (int k = 0; k < d; ++k) t += S[(int64_t)k * d + i] * (sg[k] ? 1.0 : -1.0);
+            yr[i] = n * (double)c_mse[idx[i]] + kappa * g * t;
+        }
+        orc_unrotate(s, s2, d, yr, out + row * d);
+    }
+    free(yr);
+    free(idx);
+    free(sg);
+}
+
+void orc_attention_qjl(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int Hkv, int64_t cap,
+                       int64_t ctx_len, int k_bits, const float *k_c_mse, const double *S,
+                       const uint8_t *k_packed, const float *k_norm, const float *k_rnorm, int v_bits,
+                       const float *v_centroids, const uint8_t *v_packed, const float *v_norm,
+                       const double *q, double scale, double *out) {
+    int G = Hq / Hkv;
+    int rbk = d * k_bits / 8, rbv = d * v_bits / 8;
+    double *kh = (double *)malloc(sizeof(double) * (size_t)(ctx_len * d + 1));
+    double *vh = (double *)malloc(sizeof(double) * (size_t)(ctx_len * d + 1));
+    double *sig = (double *)malloc(sizeof(double) * (size_t)(ctx_len + 1));
+    for (int b = 0; b < B; ++b) {
+        for (int g = 0; g < Hkv; ++g) {
+            int64_t row0 = ((int64_t)b * Hkv + g) * cap;
+            orc_decode_qjl(s, s2, d, k_bits, k_c_mse, S, k_packed + row0 * rbk, k_norm + row0,
+                           k_rnorm + row0, ctx_len, kh);
+            orc_decode(s, s2, d, v_bits, v_centroids, v_packed + row0 * rbv, v_norm + row0, ctx_len, vh);
+            for (int hh = 0; hh < G; ++hh) {
+                int h = g * G + hh;
+                const double *qh = q + ((int64_t)b * Hq + h) * d;
+                double *o = out + ((int64_t)b * Hq + h) * d;
+                double m = -INFINITY;
+                for (int64_t t = 0; t < ctx_len; ++t) {
+                    double dot = 0.0;
+                    for (int j = 0; j < d; ++j) dot += qh[j] * kh[t * d + j];
+                    sig[t] = scale * dot;
+                    if (sig[t] > m) m = sig[t];
+                }
+                double l = 0.0;
+                for (int64_t t = 0; t < ctx_len; ++t) l += exp(sig[t] - m);
+                for (int j = 0; j < d; ++j) o[j] = 0.0;
+                for (int64_t t = 0; t < ctx_len; ++t) {
+                    double p = exp(sig[t] - m) / l;
+                    for (int j = 0; j < d; ++j) o[j] += p * vh[t * d + j];
+                }
+            }
+        }
+    }
+    free(kh);
+    free(vh);
+    free(sig);
+}

@@ -136,6 +136,48 @@ void orc_attention_prefill(const int8_t *s, const int8_t *s2, int d, int B, int 
                            int v_bits, const float *v_centroids, const uint8_t *v_packed,
                            const float *v_norm, const double *q, double scale, double *out);
 
+/* ------------------------------------------------------ QJL residual keys
+ * "CITATIONS" (Atlas), Google TurboQuant entry: for inner products, an
+ * MSE-optimal quantiser followed by a 1-bit quantised Johnson-Lindenstrauss
+ * transform of the residual removes the bias ("TurboQuant KV Cache
+ * Compression -- Spec", Why not QJL?; "Implementation specification ...",
+ * TurboQuant path: residual / QJL-style correction).  The pages print no
+ * formula; the reading taken here:
+ *  - b bits per coordinate: the first b - 1 are the MSE codec's index, on the
+ *    (b - 1)-bit codebook; then one sign bit per projection, d projections.
+ *    Row layout: the d indices of b - 1 bits (dense LSB-first), then the d
+ *    signs (bit k = 1 iff projection k >= 0), d*b/8 bytes.
+ *  - the residual of the rotated normalised row, r = u - c[idx] (u as the
+ *    encoder computes it, c the fp32 centroids), is projected by S (d x d,
+ *    i.i.d. N(0,1)); gamma = n * ||r|| is stored beside the norm n.
+ *  - decode (rotated domain): n c[idx] + sqrt(pi/2)/d * gamma * S^T sgn,
+ *    sgn_k = +-1; E over S of the second term is n r (E[sign(s.r) s] =
+ *    sqrt(2/pi) r/||r|| for a standard Gaussian s), so inner products with
+ *    the decoded row are unbiased.
+ *  - S_ij: Box-Muller, sqrt(-2 ln(1 - U1)) cos(2 pi U2), on the outputs
+ *    o = 2d + 2k and 2d + 2k + 1 (k = i d + j) of the splitmix64 stream of
+ *    `seed` (the stream whose first 2d outputs give s1 and s2), U = (out >>
+ *    11) / 2^53. */
+void orc_qjl_matrix(uint64_t seed, int d, double *S);
+
+/* packed: [n_rows][d*bits/8] as above; norms, rnorms: [n_rows] fp32 (n and
+ * gamma).  c_mse / b_mse: the (bits-1)-bit codebook (fp32).  proj_out
+ * (optional): [n_rows][d] the projections S r in double. */
+void orc_encode_qjl(const int8_t *s, const int8_t *s2, int d, int bits, const float *c_mse,
+                    const float *b_mse, const double *S, const double *x, int64_t n_rows,
+                    uint8_t *packed, float *norms, float *rnorms, double *proj_out);
+/* x_hat = unrotate(n c[idx] + sqrt(pi/2)/d * gamma * S^T sgn), in double. */
+void orc_decode_qjl(const int8_t *s, const int8_t *s2, int d, int bits, const float *c_mse,
+                    const double *S, const uint8_t *packed, const float *norms, const float *rnorms,
+                    int64_t n_rows, double *out);
+/* orc_attention with keys in the QJL format (k_rnorm [B][Hkv][cap] holds
+ * gamma) and values in the plain format; dense. */
+void orc_attention_qjl(const int8_t *s, const int8_t *s2, int d, int B, int Hq, int Hkv, int64_t cap,
+                       int64_t ctx_len, int k_bits, const float *k_c_mse, const double *S,
+                       const uint8_t *k_packed, const float *k_norm, const float *k_rnorm, int v_bits,
+                       const float *v_centroids, const uint8_t *v_packed, const float *v_norm,
+                       const double *q, double scale, double *out);
+
 #ifdef __cplusplus
 }
 #endif
