@@ -354,6 +354,47 @@ tq_status tq_attn_prefill(const tq_plan *plan, const void *q, int B, int T, int 
                           tq_stream_t stream);
 
 /* Text for a status code (static storage). */
+/* ------------------------------------------------------ QJL residual keys
+ * "CITATIONS" (Atlas), Google TurboQuant entry: an MSE-optimal quantiser
+ * followed by a 1-bit quantised Johnson-Lindenstrauss transform of the
+ * residual gives unbiased inner products ("TurboQuant KV Cache Compression --
+ * Spec", Why not QJL?, which keeps MSE-only for softmax attention).  The
+ * pages print no formula; the format here, for d in {32, 64, 128} and
+ * b = bits in {2, 3, 4}:
+ *   row bytes d*b/8: the d indices of the (b-1)-bit codec (same rotation,
+ *   norm and bucketing, (b-1)-bit codebook of the plan), packed as tq_encode
+ *   packs them, then d sign bits (stream bit k = 1 iff (S r)_k >= 0) where
+ *   r = u - c[idx] is the residual of the rotated normalised row u;
+ *   norms[i] = n = ||x_i||, rnorms[i] = gamma = n * ||r|| (fp32);
+ *   decode: x_hat = s1 . H (s2 . (n c[idx] + sqrt(pi/2)/d * gamma * S^T sgn))
+ *   / sqrt(d), sgn_k = +-1.  Over Gaussian S, E[<y, x_hat>] = <y, x>.
+ * S is [d][d] fp32, row-major, caller-owned device memory (16-byte aligned),
+ * filled by tq_qjl_matrix: S_ij = sqrt(-2 ln(1 - U1)) cos(2 pi U2) with
+ * U = (out >> 11) / 2^53 on outputs 2d + 2k and 2d + 2k + 1 (k = i d + j) of
+ * the plan seed's splitmix64 stream, in double, rounded to fp32.
+ * Errors: TQ_ERR_UNSUPPORTED for other d, bits or dtypes; otherwise as
+ * tq_encode / tq_decode / tq_attn_decode. */
+tq_status tq_qjl_matrix(const tq_plan *plan, float *S, tq_stream_t stream);
+/* x [n_rows][d] fp32 or bf16 -> packed [n_rows][d*bits/8], norms, rnorms [n_rows]. */
+tq_status tq_encode_qjl(const tq_plan *plan, int bits, const float *S, const void *x, tq_dtype x_dtype,
+                        int64_t n_rows, uint8_t *packed, float *norms, float *rnorms, tq_stream_t stream);
+/* packed, norms, rnorms as tq_encode_qjl writes them -> y [n_rows][d]. */
+tq_status tq_decode_qjl(const tq_plan *plan, int bits, const float *S, const uint8_t *packed,
+                        const float *norms, const float *rnorms, int64_t n_rows, void *y, tq_dtype y_dtype,
+                        tq_stream_t stream);
+/* Decode attention (dense) over a contiguous cache whose K rows are in the
+ * QJL format of k_bits (cache.k_packed [B][Hkv][cap][d*k_bits/8], cache.k_norm
+ * the norms, k_rnorm [B][Hkv][cap] the gammas) and whose V rows are plain
+ * tq_encode rows of v_bits: out = softmax(scale * q . K_hat) V_hat per query
+ * head, with q [B][Hq][d] bf16 and out [B][Hq][d] fp32.  The scores are
+ * n <R q, c[idx]> + sqrt(pi/2)/d * gamma <S R q, sgn>: S meets only the query.
+ * workspace: at least tq_attn_qjl_workspace_bytes(B, Hq, Hkv, d, ctx_len). */
+size_t tq_attn_qjl_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len);
+tq_status tq_attn_decode_qjl(const tq_plan *plan, const float *S, const void *q, int B, int Hq, int Hkv,
+                             tq_cache_view cache, const float *k_rnorm, int64_t ctx_len, int k_bits,
+                             int v_bits, float scale, float *out, void *workspace, size_t workspace_bytes,
+                             tq_stream_t stream);
+
 const char *tq_status_string(tq_status status);
 
 /* The cudaError_t value behind the most recent TQ_ERR_CUDA of this thread. */

@@ -28,7 +28,8 @@ EXPORTS = ("tq_codebook_init", "tq_plan_create", "tq_plan_destroy", "tq_plan_sig
            "tq_attn_decode", "tq_status_string", "tq_last_cuda_error", "tq_device_status",
            "tq_attn_decode_noalloc", "tq_attn_decode_ex", "tq_append_paged", "tq_attn_decode_paged",
            "tq_attn_decode_append_paged", "tq_plan_create_ex", "tq_plan_signs2", "tq_codebook_init_gaussian",
-           "tq_attn_prefill_workspace_bytes", "tq_attn_prefill")
+           "tq_attn_prefill_workspace_bytes", "tq_attn_prefill", "tq_qjl_matrix", "tq_encode_qjl",
+           "tq_decode_qjl", "tq_attn_qjl_workspace_bytes", "tq_attn_decode_qjl")
 
 
 class TQError(RuntimeError):
@@ -79,6 +80,12 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t, vp]),
         ("tq_attn_decode_noalloc", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32,
                                          vp, vp]),
+        ("tq_qjl_matrix", i32, [vp, vp, vp]),
+        ("tq_encode_qjl", i32, [vp, i32, vp, vp, i32, i64, vp, vp, vp, vp]),
+        ("tq_decode_qjl", i32, [vp, i32, vp, vp, vp, vp, i64, vp, i32, vp]),
+        ("tq_attn_qjl_workspace_bytes", ctypes.c_size_t, [i32, i32, i32, i32, i64]),
+        ("tq_attn_decode_qjl", i32, [vp, vp, vp, i32, i32, i32, CacheView, vp, i64, i32, i32, f32, vp, vp,
+                                     ctypes.c_size_t, vp]),
         ("tq_attn_decode_ex", i32, [vp, vp, i32, i32, i32, CacheView, i64, i32, i32, f32, f32, vp, vp, vp,
                                     ctypes.c_size_t, vp]),
         ("tq_append_paged", i32, [vp, i32, i32, vp, vp, i32, i32, i32, PagedCacheView, vp, i32, vp, vp]),
@@ -465,3 +472,65 @@ def tq_device_status(reset: bool = False) -> int:
     st = ctypes.c_int(0)
     _check("tq_device_status", lib().tq_device_status(int(reset), ctypes.byref(st)))
     return st.value
+
+
+# ------------------------------------------------------------ QJL residual keys
+
+def tq_qjl_matrix(plan: Plan, device="cuda", out: torch.Tensor | None = None) -> torch.Tensor:
+    """The plan's QJL projection S [d, d] fp32, drawn on the device."""
+    if out is None:
+        out = torch.empty(plan.d, plan.d, dtype=torch.float32, device=device)
+    _cuda(out)
+    _check("tq_qjl_matrix", lib().tq_qjl_matrix(plan.handle, out.data_ptr(), _stream(out)))
+    return out
+
+
+def tq_encode_qjl(plan: Plan, bits: int, S: torch.Tensor, x: torch.Tensor):
+    """x: [n, d] fp32/bf16 -> (packed [n, d*bits/8] uint8, norms [n], rnorms [n] fp32)."""
+    x2 = x.reshape(-1, plan.d)
+    n = x2.shape[0]
+    packed = torch.empty(n, plan.d * bits // 8, dtype=torch.uint8, device=x.device)
+    norms = torch.empty(n, dtype=torch.float32, device=x.device)
+    rnorms = torch.empty(n, dtype=torch.float32, device=x.device)
+    _cuda(S, x2, packed, norms, rnorms)
+    _check("tq_encode_qjl", lib().tq_encode_qjl(plan.handle, bits, S.data_ptr(), x2.data_ptr(), _dt(x2), n,
+                                                packed.data_ptr(), norms.data_ptr(), rnorms.data_ptr(),
+                                                _stream(x2)))
+    return packed, norms, rnorms
+
+
+def tq_decode_qjl(plan: Plan, bits: int, S: torch.Tensor, packed: torch.Tensor, norms: torch.Tensor,
+                  rnorms: torch.Tensor, out_dtype=torch.float32) -> torch.Tensor:
+    n = norms.numel()
+    out = torch.empty(n, plan.d, dtype=out_dtype, device=packed.device)
+    _cuda(S, packed, norms, rnorms, out)
+    _check("tq_decode_qjl", lib().tq_decode_qjl(plan.handle, bits, S.data_ptr(), packed.data_ptr(),
+                                                norms.data_ptr(), rnorms.data_ptr(), n, out.data_ptr(),
+                                                _dt(out), _stream(out)))
+    return out
+
+
+def tq_attn_qjl_workspace_bytes(B: int, Hq: int, Hkv: int, d: int, ctx_len: int) -> int:
+    return int(lib().tq_attn_qjl_workspace_bytes(B, Hq, Hkv, d, ctx_len))
+
+
+def tq_attn_decode_qjl(plan: Plan, S: torch.Tensor, q: torch.Tensor, cache: Cache, k_rnorm: torch.Tensor,
+                       ctx_len: int, scale: float, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """q: [B, Hq, d] bf16; cache.k_* in the QJL format of cache.k_bits with
+    k_rnorm [B, Hkv, cap] the gammas -> out [B, Hq, d] fp32."""
+    B, Hq, d = q.shape
+    Hkv = cache.k_norm.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    need = tq_attn_qjl_workspace_bytes(B, Hq, Hkv, d, ctx_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _cuda(S, q, k_rnorm, out, workspace)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bf16")
+    _check("tq_attn_decode_qjl", lib().tq_attn_decode_qjl(
+        plan.handle, S.data_ptr(), q.data_ptr(), B, Hq, Hkv, cache.view(), k_rnorm.data_ptr(), ctx_len,
+        cache.k_bits, cache.v_bits, ctypes.c_float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel(), _stream(q)))
+    return out

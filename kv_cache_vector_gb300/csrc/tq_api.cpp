@@ -263,6 +263,19 @@ cudaError_t dispatch_attn_d(int d, F&& f) {
     return cudaErrorInvalidValue;
 }
 
+// QJL residual keys: head dimensions whose matrix fits in shared memory.
+bool qjl_d(int d) { return d == 32 || d == 64 || d == 128; }
+
+template <typename F>
+cudaError_t dispatch_qjl_d(int d, F&& f) {
+    switch (d) {
+        case 32: return f(IntC<32>{});
+        case 64: return f(IntC<64>{});
+        case 128: return f(IntC<128>{});
+    }
+    return cudaErrorInvalidValue;
+}
+
 bool valid_bits(int b) { return b >= 2 && b <= 4; }
 bool valid_dtype(tq_dtype t) { return t == TQ_F32 || t == TQ_BF16; }
 
@@ -540,6 +553,97 @@ tq_status tq_attn_decode(const tq_plan* plan, const void* q, int B, int Hq, int 
                          size_t workspace_bytes, tq_stream_t stream) {
     return tq_attn_decode_ex(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale, sparse_v_threshold,
                              out, nullptr, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------ QJL residual keys
+
+tq_status tq_qjl_matrix(const tq_plan* plan, float* S, tq_stream_t stream) {
+    if (!plan || !S) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (!qjl_d(P->d)) return TQ_ERR_UNSUPPORTED;
+    if (!aligned16(S)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(S)) return TQ_ERR_INVALID_ARG;
+    const cudaError_t e = tq::launch_qjl_matrix(P->seed, P->d, S, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_encode_qjl(const tq_plan* plan, int bits, const float* S, const void* x, tq_dtype x_dtype,
+                        int64_t n_rows, uint8_t* packed, float* norms, float* rnorms, tq_stream_t stream) {
+    if (!plan || n_rows < 0) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (!valid_bits(bits) || !valid_dtype(x_dtype) || !qjl_d(P->d)) return TQ_ERR_UNSUPPORTED;
+    if (n_rows == 0) return TQ_OK;
+    if (!S || !x || !packed || !norms || !rnorms) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(x) || !aligned16(packed) || !aligned4(norms) || !aligned4(rnorms))
+        return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(S) || !device_accessible(x) || !device_accessible(packed) ||
+        !device_accessible(norms) || !device_accessible(rnorms))
+        return TQ_ERR_INVALID_ARG;
+    tq::RowParams R;
+    fill_row_params(*P, bits - 1, R);
+    cudaError_t e = dispatch_qjl_d(P->d, [&](auto D) {
+        return tq::launch_encode_qjl_d<decltype(D)::value>(bits, x_dtype, x, n_rows, S, packed, norms, rnorms, R,
+                                                           reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+tq_status tq_decode_qjl(const tq_plan* plan, int bits, const float* S, const uint8_t* packed, const float* norms,
+                        const float* rnorms, int64_t n_rows, void* y, tq_dtype y_dtype, tq_stream_t stream) {
+    if (!plan || n_rows < 0) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (!valid_bits(bits) || !valid_dtype(y_dtype) || !qjl_d(P->d)) return TQ_ERR_UNSUPPORTED;
+    if (n_rows == 0) return TQ_OK;
+    if (!S || !y || !packed || !norms || !rnorms) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned16(y) || !aligned16(packed) || !aligned4(norms) || !aligned4(rnorms))
+        return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(S) || !device_accessible(y) || !device_accessible(packed) ||
+        !device_accessible(norms) || !device_accessible(rnorms))
+        return TQ_ERR_INVALID_ARG;
+    tq::RowParams R;
+    fill_row_params(*P, bits - 1, R);
+    cudaError_t e = dispatch_qjl_d(P->d, [&](auto D) {
+        return tq::launch_decode_qjl_d<decltype(D)::value>(bits, y_dtype, packed, norms, rnorms, n_rows, S, y, R,
+                                                           reinterpret_cast<cudaStream_t>(stream));
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
+}
+
+size_t tq_attn_qjl_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !qjl_d(d)) return 0;
+    return tq::attn_qjl_workspace_bytes(B, Hq, d, tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms()));
+}
+
+tq_status tq_attn_decode_qjl(const tq_plan* plan, const float* S, const void* q, int B, int Hq, int Hkv,
+                             tq_cache_view cache, const float* k_rnorm, int64_t ctx_len, int k_bits, int v_bits,
+                             float scale, float* out, void* workspace, size_t workspace_bytes,
+                             tq_stream_t stream) {
+    if (!plan) return TQ_ERR_INVALID_ARG;
+    const tq::Plan* P = reinterpret_cast<const tq::Plan*>(plan);
+    if (!qjl_d(P->d)) return TQ_ERR_UNSUPPORTED;
+    bool nothing = false;
+    tq_status st = tq::check_attn_decode_args(plan, q, B, Hq, Hkv, cache, ctx_len, k_bits, v_bits, scale, 0.0f,
+                                              out, &nothing);
+    if (st != TQ_OK || nothing) return st;
+    if (!S || !k_rnorm) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(S) || !aligned4(k_rnorm)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(S) || !device_accessible(k_rnorm)) return TQ_ERR_INVALID_ARG;
+    const tq::AttnGeometry g = tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms());
+    if (!workspace || workspace_bytes < tq::attn_qjl_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
+    if (!device_accessible(workspace)) return TQ_ERR_INVALID_ARG;
+    tq::AttnParams A;
+    tq::fill_attn_params(*P, k_bits - 1, v_bits, scale, 0.0f, A);
+    cudaError_t e = dispatch_qjl_d(P->d, [&](auto D) {
+        constexpr int d = decltype(D)::value;
+        const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        switch (k_bits) {
+            case 2: return tq::launch_attn_qjl<d, 2>(v_bits, q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, A, s);
+            case 3: return tq::launch_attn_qjl<d, 3>(v_bits, q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, A, s);
+            default: return tq::launch_attn_qjl<d, 4>(v_bits, q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, A, s);
+        }
+    });
+    return e == cudaSuccess ? TQ_OK : cuda_fail(e);
 }
 
 // ------------------------------------------------------------ paged cache

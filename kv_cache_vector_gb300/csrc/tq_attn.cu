@@ -57,11 +57,18 @@ __device__ __forceinline__ uint32_t lane_bits(const uint8_t* row, int lane) {
 // the query in a transposed copy so that lanes read consecutive words), then
 // the exponentials, then the V product a warp per position.  A split with no
 // positions writes an empty partial (m = -FLT_MAX, l = 0).
-template <int D, int KB, int VB, bool PAGED>
+//
+// QJL: keys in the QJL residual format of KB bits (a (KB - 1)-bit index per
+// coordinate, then d sign bits of the projected residual; k_rnorm holds
+// gamma).  The score is n <q~, c[idx]> + gamma <q', sgn> with q~ the rotated
+// scaled query and q' = sqrt(pi/2)/d * S q~, both read from qpre (written by
+// k_qjl_query) instead of rotating q here: S then never meets the keys.
+template <int D, int KB, int VB, bool PAGED, bool QJL = false>
 __global__ void __launch_bounds__(kAttnThreads)
 k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view cache,
              int64_t ctx_len, int split_len, int n_splits, float* __restrict__ ws,
-             const __grid_constant__ AttnParams P, const PagedArgs pa, int len_plus, int* status) {
+             const __grid_constant__ AttnParams P, const PagedArgs pa, int len_plus, int* status,
+             const float* __restrict__ qpre, const float* __restrict__ k_rnorm) {
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = Hq / Hkv;
     int64_t Ls = ctx_len;
@@ -96,16 +103,27 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         kcen[tid] = P.kcen[tid];
         vcen[tid] = P.vcen[tid];
     }
-    // ---- rotate the group's queries: qrot = H (s . q) / sqrt(d), times scale
-    for (int i = tid; i < G * D; i += blockDim.x) {
-        const int h = i / D, j = i % D;
-        const float x = __bfloat162float(q[((int64_t)b * Hq + g * G + h) * D + j]);
-        qrot[i] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
-    }
-    fwht_smem<D>(qrot, G);
-    for (int i = tid; i < G * D; i += blockDim.x) {
-        const uint32_t m = P.two_sided ? P.sgn2[i % D] : 0u;
-        qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
+    if constexpr (QJL) {
+        // rotated queries and their projections; the projections wait in the
+        // cross-warp sum buffer, which pass 2 clears only after pass 1
+        for (int i = tid; i < G * D; i += blockDim.x) {
+            const int h = i / D, j = i % D;
+            const float* src = qpre + ((int64_t)b * Hq + g * G + h) * 2 * D;
+            qrot[i] = src[j];
+            accs[i] = src[D + j];
+        }
+    } else {
+        // ---- rotate the group's queries: qrot = H (s . q) / sqrt(d), times scale
+        for (int i = tid; i < G * D; i += blockDim.x) {
+            const int h = i / D, j = i % D;
+            const float x = __bfloat162float(q[((int64_t)b * Hq + g * G + h) * D + j]);
+            qrot[i] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
+        }
+        fwht_smem<D>(qrot, G);
+        for (int i = tid; i < G * D; i += blockDim.x) {
+            const uint32_t m = P.two_sided ? P.sgn2[i % D] : 0u;
+            qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
+        }
     }
     __syncthreads();
     for (int i = tid; i < G * D; i += blockDim.x) {
@@ -130,24 +148,49 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
             }
             continue;
         }
-        const uint32_t bits = lane_bits<KLB>(cache.k_packed + row * KRB, lane);
         const float nk = __ldg(cache.k_norm + row);
         float part[kMaxGroup];
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h) part[h] = 0.f;
+        if constexpr (QJL) {
+            constexpr int MB = KB - 1, KIB = D * MB / 8;  // index bits per coordinate, index bytes
+            const uint8_t* krow = cache.k_packed + row * KRB;
+            const uint32_t bits = lane_bits<EPL * MB>(krow, lane);
+            const uint32_t* sw = reinterpret_cast<const uint32_t*>(krow + KIB);
+            float sp[kMaxGroup];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float c = kcen[(bits >> (e * KB)) & ((1u << KB) - 1)];
+            for (int h = 0; h < kMaxGroup; ++h) sp[h] = 0.f;
 #pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h)
-                if (h < G) part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
+            for (int e = 0; e < EPL; ++e) {
+                const float c = kcen[(bits >> (e * MB)) & ((1u << MB) - 1)];
+                // projection k = 32 e + lane: its sign is bit `lane` of word e
+                const uint32_t neg = (~__ldg(sw + e) >> lane) << 31;
+#pragma unroll
+                for (int h = 0; h < kMaxGroup; ++h)
+                    if (h < G) {
+                        part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
+                        sp[h] += __uint_as_float(__float_as_uint(accs[h * D + 32 * e + lane]) ^ neg);
+                    }
+            }
+            const float gk = __ldg(k_rnorm + row);
+#pragma unroll
+            for (int h = 0; h < kMaxGroup; ++h) part[h] = fmaf(nk, part[h], gk * sp[h]);
+        } else {
+            const uint32_t bits = lane_bits<KLB>(cache.k_packed + row * KRB, lane);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const float c = kcen[(bits >> (e * KB)) & ((1u << KB) - 1)];
+#pragma unroll
+                for (int h = 0; h < kMaxGroup; ++h)
+                    if (h < G) part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
+            }
         }
 #pragma unroll
         for (int h = 0; h < kMaxGroup; ++h) {
             if (h < G) {
                 float s = part[h];
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-                s *= nk;
+                if constexpr (!QJL) s *= nk;
                 if (lane == 0) sc[h * split_len + t] = s;
                 mloc[h] = fmaxf(mloc[h], s);
             }
@@ -264,6 +307,32 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
     o[j] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? P.sgn2[j] : 0u));
     fwht_smem<D>(o, 1);
     out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
+}
+
+// QJL keys: the rotated query of one (batch, query head), times the softmax
+// scale, and its projection by the QJL matrix times sqrt(pi/2)/d, written to
+// qpre[bh][0, D) and [D, 2D).  One block of D threads per head; thread k
+// forms projection k from row k of S.
+template <int D>
+__global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict__ q,
+                                                 const float* __restrict__ S, float* __restrict__ qpre,
+                                                 const __grid_constant__ AttnParams P, float kappa) {
+    __shared__ float v[D];
+    const int bh = blockIdx.x, j = threadIdx.x;
+    const float x = __bfloat162float(q[(int64_t)bh * D + j]);
+    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
+    fwht_smem<D>(v, 1);
+    const uint32_t m = P.two_sided ? P.sgn2[j] : 0u;
+    const float r = __uint_as_float(__float_as_uint(v[j]) ^ m) * (P.inv_sqrt_d * P.scale);
+    __syncthreads();
+    v[j] = r;
+    __syncthreads();
+    float p = 0.f;
+    const float* row = S + (int64_t)j * D;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) p = fmaf(__ldg(row + i), v[i], p);
+    qpre[(int64_t)bh * 2 * D + j] = r;
+    qpre[(int64_t)bh * 2 * D + D + j] = p * kappa;
 }
 
 // ============================================================ d = 128
@@ -1619,10 +1688,35 @@ cudaError_t attn_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_vi
     dim3 grid(geo.n_splits, Hkv, B);
     fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
                                        geo.split_len, geo.n_splits, static_cast<float*>(ws), P, pa, len_plus,
-                                       status_word());
+                                       status_word(), nullptr, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k_attn_combine<D><<<B * Hq, D, 0, s>>>(static_cast<const float*>(ws), geo.n_splits, out, P);
+    return cudaGetLastError();
+}
+
+// QJL keys (contiguous cache): the query prologue, the split kernel with QJL
+// scoring over the workspace after the prologue's qpre, and the combine.
+template <int D, int KB, int VB>
+cudaError_t attn_qjl_launch(const void* q, const float* S, int B, int Hq, int Hkv, const tq_cache_view& cache,
+                            const float* k_rnorm, int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
+                            const AttnParams& P, cudaStream_t s) {
+    float* qpre = static_cast<float*>(ws);
+    float* part = qpre + attn_qjl_prefix_floats(B, Hq, D);
+    k_qjl_query<D><<<B * Hq, D, 0, s>>>(static_cast<const __nv_bfloat16*>(q), S, qpre, P,
+                                        (float)(1.2533141373155003 / D));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto fn = k_attn_split<D, KB, VB, false, true>;
+    const size_t smem = sizeof(float) * (kMaxGroup * D * 3 + (size_t)kMaxGroup * geo.split_len +
+                                         kAttnWarps * kMaxGroup + 2 * kMaxGroup + 32);
+    dim3 grid(geo.n_splits, Hkv, B);
+    fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
+                                       geo.split_len, geo.n_splits, part, P, PagedArgs{}, 0, status_word(), qpre,
+                                       k_rnorm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_attn_combine<D><<<B * Hq, D, 0, s>>>(part, geo.n_splits, out, P);
     return cudaGetLastError();
 }
 
@@ -1689,6 +1783,23 @@ template cudaError_t launch_attn_generic_paged<TQ_UNIT_D, TQ_UNIT_KB>(int, const
                                                                        const tq_cache_view&,
                                                            int64_t, float*, void*, const AttnGeometry&,
                                                            const AttnParams&, const PagedArgs&, int, cudaStream_t);
+#endif
+
+#if TQ_UNIT_D <= 128
+template <int D, int KB>
+cudaError_t launch_attn_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
+                            const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
+                            void* workspace, const AttnGeometry& g, const AttnParams& P, cudaStream_t s) {
+    switch (v_bits) {
+        case 2: return dev::attn_qjl_launch<D, KB, 2>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
+        case 3: return dev::attn_qjl_launch<D, KB, 3>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
+        default: return dev::attn_qjl_launch<D, KB, 4>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
+    }
+}
+template cudaError_t launch_attn_qjl<TQ_UNIT_D, TQ_UNIT_KB>(int, const void*, const float*, int, int, int,
+                                                            const tq_cache_view&, const float*, int64_t, float*,
+                                                            void*, const AttnGeometry&, const AttnParams&,
+                                                            cudaStream_t);
 #endif
 
 #if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB)

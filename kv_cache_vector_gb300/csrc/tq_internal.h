@@ -110,6 +110,31 @@ cudaError_t launch_append_d(int k_bits, int v_bits, tq_dtype dt, const void* k_n
                             const tq_cache_view& cache, int64_t pos, const RowParams& PK,
                             const RowParams& PV, cudaStream_t s);
 
+// QJL residual keys (d = 32, 64, 128): the seeded Gaussian matrix S [d][d]
+// (fp32, row-major), encode and decode with P the (bits - 1)-bit row
+// parameters, and the decode attention over a contiguous cache whose keys are
+// in that format (P from fill_attn_params with k_bits - 1).  The attention
+// workspace is the prefix of rotated and projected queries (2 d floats per
+// query head, rounded up to 64 floats) followed by the split partials of the
+// generic geometry (attn_qjl_geometry).
+cudaError_t launch_qjl_matrix(uint64_t seed, int d, float* S, cudaStream_t s);
+template <int D>
+cudaError_t launch_encode_qjl_d(int bits, tq_dtype dt, const void* x, int64_t n_rows, const float* S,
+                                uint8_t* packed, float* norms, float* rnorms, const RowParams& P,
+                                cudaStream_t s);
+template <int D>
+cudaError_t launch_decode_qjl_d(int bits, tq_dtype dt, const uint8_t* packed, const float* norms,
+                                const float* rnorms, int64_t n_rows, const float* S, void* y, const RowParams& P,
+                                cudaStream_t s);
+struct AttnGeometry;
+template <int D, int KB>
+cudaError_t launch_attn_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
+                            const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
+                            void* workspace, const AttnGeometry& g, const AttnParams& P, cudaStream_t s);
+inline size_t attn_qjl_prefix_floats(int B, int Hq, int d) {
+    return ((size_t)B * Hq * 2 * d + 63) / 64 * 64;
+}
+
 // Shared-memory plan of the d = 128 attention kernel, in absolute
 // shared-window addresses (the dynamic block starts at or below
 // kAttn3RingAt).  Each warp streams 32-position chunks (packed K and V rows
@@ -194,6 +219,10 @@ size_t attn_paged_workspace_bound(int B, int Hq, int Hkv, int64_t max_ctx, int n
 // sparse-V kernel (the public size query takes neither).
 size_t attn_workspace_bound(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int d);
 size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
+// QJL keys: the generic (CUDA-core) split geometry at any d, and the bytes of
+// its workspace (query prefix and partials).
+AttnGeometry attn_qjl_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms);
+size_t attn_qjl_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
 // their power-of-two scales (4 bytes per head), rounded up to 256 bytes.
 // d = 128, paged attention: the work partition written by the planning

@@ -108,6 +108,15 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
     return g;
 }
 
+AttnGeometry attn_qjl_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms) {
+    // the generic kernel's geometry (any d other than 128 takes that branch)
+    return attn_geometry(B, Hq, Hkv, ctx_len, sms, 64, 2, 2, false);
+}
+
+size_t attn_qjl_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g) {
+    return sizeof(float) * (attn_qjl_prefix_floats(B, Hq, d) + (size_t)B * Hq * g.n_splits * g.parts * (d + 2));
+}
+
 AttnGeometry attn_geometry_paged(int B, int Hq, int Hkv, int64_t max_ctx, int sms, int kb, int vb) {
     // The CTAs' shares are balanced on the device from the actual lengths;
     // here only the slice length is chosen: the longest one that stays under

@@ -1,0 +1,386 @@
+// tq_qjl.cu -- QJL residual keys: the Gaussian projection, encode and decode.
+//
+// "CITATIONS" (Atlas), Google TurboQuant entry: an MSE-optimal quantiser
+// followed by a 1-bit quantised Johnson-Lindenstrauss transform of the
+// residual makes inner products unbiased ("TurboQuant KV Cache Compression --
+// Spec", Why not QJL?).  The pages give no formula; the format implemented
+// here, for b bits per coordinate:
+//   * the first b - 1 bits are the row codec's index on the (b - 1)-bit
+//     codebook (the same rotation, norm and bucketing);
+//   * r = u - c[idx] is the residual of the rotated normalised row u; its
+//     projections p = S r by a d x d matrix S of i.i.d. N(0, 1) entries give
+//     one sign bit each (bit k = 1 iff p_k >= 0), packed after the indices:
+//     d * b / 8 bytes per row;
+//   * gamma = n ||r|| (fp32) is stored beside the norm n;
+//   * decode, in the rotated domain: n c[idx] + sqrt(pi/2)/d * gamma * S^T sgn
+//     (sgn_k = +-1), then the inverse rotation.  E[sign(s.r) s] =
+//     sqrt(2/pi) r / ||r|| for a standard Gaussian row s, so the correction
+//     has expectation n r over S and <y, x_hat> is unbiased.
+// S is drawn from the plan seed's splitmix64 stream (Vigna's published
+// generator), after the 2d outputs of the sign vectors: entry k = i d + j is
+// Box-Muller, sqrt(-2 ln(1 - U1)) cos(2 pi U2), on outputs 2d + 2k and
+// 2d + 2k + 1, U = (out >> 11) / 2^53, computed in double and stored fp32.
+//
+// Work layout (d = 32, 64, 128): a warp takes four rows at a time; lane l
+// holds the E = d/32 coordinates l E .. l E + E - 1 through the transform and
+// the projections k = l + 32 e, so that the sign bits of projection word e
+// are one warp ballot.  The block keeps S in shared memory, row-major with a
+// stride of d + 4 floats: lane reads of four consecutive floats of 32
+// different rows (encode) and of one row (decode) are both free of bank
+// conflicts.  Each S load feeds the four rows of the warp.
+#include <cuda_bf16.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+namespace dev {
+
+constexpr int kQjlWarps = 8;
+constexpr int kQjlRows = 4;  // rows per warp at a time
+
+template <int D>
+struct QjlSmem {
+    static constexpr int kStride = D + 4;                       // floats per row of S
+    static constexpr int kS = D * kStride * 4;                  // bytes of S
+    static constexpr int kR = kQjlWarps * kQjlRows * D * 4;     // residuals (encode) / rows (decode)
+    static constexpr int kI = kQjlWarps * kQjlRows * D;         // index bytes (encode)
+    static constexpr int kBytes = kS + kR + kI + 2 * D * 4;     // + sign masks
+};
+
+#if TQ_UNIT_D == 128  // the matrix kernel is built once
+// Output i (0-based) of splitmix64 seeded with `seed`: the state after i + 1
+// increments of the golden-ratio constant, through the published mix.
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__global__ void __launch_bounds__(256) k_qjl_matrix(uint64_t seed, int d, float* __restrict__ S) {
+    const int64_t n = (int64_t)d * d;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t o = 2 * (uint64_t)d + 2 * (uint64_t)k;
+        const double u1 = (double)(splitmix64_at(seed, o) >> 11) * 0x1p-53;
+        const double u2 = (double)(splitmix64_at(seed, o + 1) >> 11) * 0x1p-53;
+        S[k] = (float)(sqrt(-2.0 * log(1.0 - u1)) * cos(6.283185307179586 * u2));
+    }
+}
+#endif
+
+// Copy S [D][D] (global, row-major) into shared memory with row stride D + 4.
+template <int D>
+__device__ __forceinline__ void stage_matrix(const float* __restrict__ S, float* Ss) {
+    constexpr int kStride = QjlSmem<D>::kStride;
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) {
+        const int k = (4 * i) / D, j = (4 * i) % D;
+        *reinterpret_cast<float4*>(Ss + k * kStride + j) = __ldg(reinterpret_cast<const float4*>(S) + i);
+    }
+}
+
+// The in-warp transform: the E registers of each lane, then across lanes
+// (element e of lane l is coordinate l E + e), unnormalised.
+template <int E>
+__device__ __forceinline__ void warp_fwht(float (&v)[E], int lane) {
+    fwht_reg<E>(v);
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
+            v[e] = (lane & b) ? o - v[e] : v[e] + o;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    return s;
+}
+
+// Encode: BITS total bits per coordinate (2..4), T the input type.  P holds
+// the (BITS - 1)-bit codebook.
+template <int D, int BITS, typename T>
+__global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restrict__ x, int64_t n_rows,
+                                                               const float* __restrict__ S,
+                                                               uint8_t* __restrict__ packed,
+                                                               float* __restrict__ norms, float* __restrict__ rnorms,
+                                                               const __grid_constant__ RowParams P) {
+    constexpr int E = D / 32, MB = BITS - 1, NB = (1 << MB) - 1;
+    constexpr int RB = D * BITS / 8, IB = D * MB / 8;
+    constexpr int kStride = QjlSmem<D>::kStride;
+    extern __shared__ __align__(16) unsigned char qjl_smem[];
+    float* Ss = reinterpret_cast<float*>(qjl_smem);
+    float* rbuf = reinterpret_cast<float*>(qjl_smem + QjlSmem<D>::kS);
+    uint8_t* ibuf = qjl_smem + QjlSmem<D>::kS + QjlSmem<D>::kR;
+    uint32_t* sg = reinterpret_cast<uint32_t*>(ibuf + QjlSmem<D>::kI);
+    uint32_t* sg2 = sg + D;
+    stage_matrix<D>(S, Ss);
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        sg[i] = P.sgn[i];
+        sg2[i] = P.sgn2[i];
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* rw = rbuf + warp * kQjlRows * D;
+    uint8_t* iw = ibuf + warp * kQjlRows * D;
+    for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
+         r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
+        float nrm[kQjlRows], gam[kQjlRows];
+        // ---- MSE stage and residual of each row (rows past the end: zeros)
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q) {
+            float v[E];
+            if (r0 + q < n_rows) {
+                load_lane<E, T>(x + (r0 + q) * D, lane, sg, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[e] = 0.f;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+            ss = warp_sum(ss);
+            warp_fwht<E>(v, lane);
+            if (P.two_sided) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
+            }
+            const float n = __fsqrt_rn(ss);
+            const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+            float rr = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                int id = 0;
+#pragma unroll
+                for (int j = 0; j < NB; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
+                const float r = fmaf(v[e], inv, -P.cen[id]);
+                rr = fmaf(r, r, rr);
+                iw[q * D + lane * E + e] = (uint8_t)id;
+                rw[q * D + lane * E + e] = r;
+            }
+            rr = warp_sum(rr);
+            nrm[q] = n;
+            gam[q] = n * __fsqrt_rn(rr);
+        }
+        __syncwarp();
+        // ---- projections p_k = sum_j S[k][j] r_j, k = lane + 32 e
+        float acc[kQjlRows][E];
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[q][e] = 0.f;
+#pragma unroll 4
+        for (int j = 0; j < D; j += 4) {
+            float4 rv[kQjlRows];
+#pragma unroll
+            for (int q = 0; q < kQjlRows; ++q) rv[q] = *reinterpret_cast<const float4*>(rw + q * D + j);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float4 s = *reinterpret_cast<const float4*>(Ss + (lane + 32 * e) * kStride + j);
+#pragma unroll
+                for (int q = 0; q < kQjlRows; ++q) {
+                    acc[q][e] = fmaf(s.x, rv[q].x, acc[q][e]);
+                    acc[q][e] = fmaf(s.y, rv[q].y, acc[q][e]);
+                    acc[q][e] = fmaf(s.z, rv[q].z, acc[q][e]);
+                    acc[q][e] = fmaf(s.w, rv[q].w, acc[q][e]);
+                }
+            }
+        }
+        // ---- store: indices, sign words, norm and gamma
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q) {
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint32_t w = __ballot_sync(0xFFFFFFFFu, acc[q][e] >= 0.f);
+                if (lane == e) mine = w;
+            }
+            if (r0 + q < n_rows) {  // warp-uniform
+                uint8_t* dst = packed + (r0 + q) * RB;
+                warp_pack_row<D>(iw + q * D, lane, MB, dst);
+                if (lane < E) reinterpret_cast<uint32_t*>(dst + IB)[lane] = mine;
+                if (lane == 0) {
+                    norms[r0 + q] = nrm[q];
+                    rnorms[r0 + q] = gam[q];
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Decode: y = s1 . H (s2 . (n c[idx] + kappa gamma S^T sgn)) / sqrt(d), kappa =
+// sqrt(pi/2)/d; lane l computes coordinates l E .. l E + E - 1.
+template <int D, int BITS, typename TO>
+__global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __restrict__ packed,
+                                                               const float* __restrict__ norms,
+                                                               const float* __restrict__ rnorms, int64_t n_rows,
+                                                               const float* __restrict__ S, TO* __restrict__ y,
+                                                               const __grid_constant__ RowParams P, float kappa) {
+    constexpr int E = D / 32, MB = BITS - 1;
+    constexpr int RB = D * BITS / 8, IB = D * MB / 8;
+    constexpr int kStride = QjlSmem<D>::kStride;
+    extern __shared__ __align__(16) unsigned char qjl_smem[];
+    float* Ss = reinterpret_cast<float*>(qjl_smem);
+    stage_matrix<D>(S, Ss);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
+         r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
+        uint32_t sw[kQjlRows][E];  // sign words of each row (every lane holds all)
+        uint32_t ib[kQjlRows];     // the lane's E indices
+        float nrm[kQjlRows], gk[kQjlRows];
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q) {
+            const bool ok = r0 + q < n_rows;
+            const uint8_t* row = packed + (ok ? r0 + q : 0) * RB;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(row + IB);
+#pragma unroll
+            for (int e = 0; e < E; ++e) sw[q][e] = ok ? __ldg(w + e) : 0u;
+            // bits [lane E MB, (lane + 1) E MB) of the index stream
+            const int bit0 = lane * E * MB, wi = bit0 / 32, sh = bit0 % 32;
+            const uint32_t* iwp = reinterpret_cast<const uint32_t*>(row);
+            uint32_t v = ok ? __ldg(iwp + wi) >> sh : 0u;
+            if (ok && sh + E * MB > 32) v |= __ldg(iwp + wi + 1) << (32 - sh);
+            ib[q] = v;
+            nrm[q] = ok ? __ldg(norms + r0 + q) : 0.f;
+            gk[q] = ok ? __ldg(rnorms + r0 + q) * kappa : 0.f;
+        }
+        // t_i = sum_k sgn_k S[k][i]
+        float t[kQjlRows][E];
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q)
+#pragma unroll
+            for (int e = 0; e < E; ++e) t[q][e] = 0.f;
+#pragma unroll
+        for (int kw = 0; kw < E; ++kw) {
+#pragma unroll 8
+            for (int b = 0; b < 32; ++b) {
+                const int k = 32 * kw + b;
+                float s[E];
+                if constexpr (E == 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(Ss + k * kStride + lane * 4);
+                    s[0] = f.x; s[1] = f.y; s[2] = f.z; s[3] = f.w;
+                } else if constexpr (E == 2) {
+                    const float2 f = *reinterpret_cast<const float2*>(Ss + k * kStride + lane * 2);
+                    s[0] = f.x; s[1] = f.y;
+                } else {
+                    s[0] = Ss[k * kStride + lane];
+                }
+#pragma unroll
+                for (int q = 0; q < kQjlRows; ++q) {
+                    const uint32_t neg = (~sw[q][kw] >> b) << 31;  // sign bit set for sgn_k = -1
+#pragma unroll
+                    for (int e = 0; e < E; ++e) t[q][e] += __uint_as_float(__float_as_uint(s[e]) ^ neg);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q) {
+            if (r0 + q >= n_rows) break;  // warp-uniform
+            float v[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float c = P.cen[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
+                v[e] = fmaf(gk[q], t[q][e], nrm[q] * c);
+                if (P.two_sided) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ P.sgn2[lane * E + e]);
+            }
+            warp_fwht<E>(v, lane);
+            TO* dst = y + (r0 + q) * D + lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float o = __uint_as_float(__float_as_uint(v[e] * P.inv_sqrt_d) ^ P.sgn[lane * E + e]);
+                if constexpr (sizeof(TO) == 2) dst[e] = __float2bfloat16_rn(o);
+                else dst[e] = o;
+            }
+        }
+    }
+}
+
+}  // namespace dev
+
+namespace {
+
+template <typename K>
+unsigned qjl_grid(K fn, int64_t n_rows, int smem) {
+    const int64_t per_block = (int64_t)dev::kQjlWarps * dev::kQjlRows;
+    int64_t g = (n_rows + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kQjlWarps, smem);
+    if (g > cap) g = cap;
+    return (unsigned)(g < 1 ? 1 : g);
+}
+
+template <int D, int BITS, typename T>
+cudaError_t enc_qjl(const void* x, int64_t n, const float* S, uint8_t* pk, float* nm, float* rn,
+                    const RowParams& P, cudaStream_t s) {
+    auto fn = dev::k_encode_qjl<D, BITS, T>;
+    constexpr int smem = dev::QjlSmem<D>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fn<<<qjl_grid(fn, n, smem), 32 * dev::kQjlWarps, smem, s>>>(static_cast<const T*>(x), n, S, pk, nm, rn, P);
+    return cudaGetLastError();
+}
+
+template <int D, int BITS, typename TO>
+cudaError_t dec_qjl(const uint8_t* pk, const float* nm, const float* rn, int64_t n, const float* S, void* y,
+                    const RowParams& P, cudaStream_t s) {
+    auto fn = dev::k_decode_qjl<D, BITS, TO>;
+    constexpr int smem = dev::QjlSmem<D>::kS;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const float kappa = (float)(1.2533141373155003 / D);  // sqrt(pi / 2) / d
+    fn<<<qjl_grid(fn, n, smem), 32 * dev::kQjlWarps, smem, s>>>(pk, nm, rn, n, S, static_cast<TO*>(y), P, kappa);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+template <int D>
+cudaError_t launch_encode_qjl_d(int bits, tq_dtype dt, const void* x, int64_t n_rows, const float* S,
+                                uint8_t* packed, float* norms, float* rnorms, const RowParams& P,
+                                cudaStream_t s) {
+    auto go = [&](auto tag) {
+        using T = decltype(tag);
+        switch (bits) {
+            case 2: return enc_qjl<D, 2, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+            case 3: return enc_qjl<D, 3, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+            default: return enc_qjl<D, 4, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+        }
+    };
+    return dt == TQ_BF16 ? go(__nv_bfloat16{}) : go(float{});
+}
+
+template <int D>
+cudaError_t launch_decode_qjl_d(int bits, tq_dtype dt, const uint8_t* packed, const float* norms,
+                                const float* rnorms, int64_t n_rows, const float* S, void* y, const RowParams& P,
+                                cudaStream_t s) {
+    auto go = [&](auto tag) {
+        using TO = decltype(tag);
+        switch (bits) {
+            case 2: return dec_qjl<D, 2, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+            case 3: return dec_qjl<D, 3, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+            default: return dec_qjl<D, 4, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+        }
+    };
+    return dt == TQ_BF16 ? go(__nv_bfloat16{}) : go(float{});
+}
+
+#if TQ_UNIT_D == 128
+cudaError_t launch_qjl_matrix(uint64_t seed, int d, float* S, cudaStream_t s) {
+    const int64_t n = (int64_t)d * d;
+    dev::k_qjl_matrix<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(seed, d, S);
+    return cudaGetLastError();
+}
+#endif
+
+#if !defined(TQ_UNIT_D)
+#error "compile once per head dimension with -DTQ_UNIT_D=<d>"
+#endif
+template cudaError_t launch_encode_qjl_d<TQ_UNIT_D>(int, tq_dtype, const void*, int64_t, const float*, uint8_t*,
+                                                    float*, float*, const RowParams&, cudaStream_t);
+template cudaError_t launch_decode_qjl_d<TQ_UNIT_D>(int, tq_dtype, const uint8_t*, const float*, const float*,
+                                                    int64_t, const float*, void*, const RowParams&, cudaStream_t);
+
+}  // namespace tq

@@ -266,3 +266,51 @@ def test_prefill_call_validation_before_launch(L):
     assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 256, 128) == 32768 + 2 * 2 * 2 * 99328 + 32
     assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 300, 64) == 0
     assert L.tq_attn_prefill_workspace_bytes(2, 10, 8, 2, 9, 128) == 0   # cap < T
+
+
+def test_qjl_call_validation_before_launch(L):
+    """The QJL entry points check their arguments on the host before any
+    launch: d outside {32, 64, 128}, bits outside 2..4, null and misaligned
+    pointers, and the attention workspace size."""
+    p128, p256, p16 = abi.Plan(128, 42), abi.Plan(256, 42), abi.Plan(16, 42)
+    h = p128.handle
+    A = 1 << 20
+    f = ctypes.c_float
+    assert L.tq_qjl_matrix(None, A, None) == 1
+    assert L.tq_qjl_matrix(h, None, None) == 1
+    assert L.tq_qjl_matrix(p256.handle, A, None) == 2
+    assert L.tq_qjl_matrix(p16.handle, A, None) == 2
+    assert L.tq_qjl_matrix(h, A + 4, None) == 3
+    # tq_encode_qjl(plan, bits, S, x, dtype, n, packed, norms, rnorms, stream)
+    assert L.tq_encode_qjl(h, 1, A, A, 0, 4, A, A, A, None) == 2
+    assert L.tq_encode_qjl(h, 5, A, A, 0, 4, A, A, A, None) == 2
+    assert L.tq_encode_qjl(h, 3, A, A, 7, 4, A, A, A, None) == 2
+    assert L.tq_encode_qjl(p256.handle, 3, A, A, 0, 4, A, A, A, None) == 2
+    assert L.tq_encode_qjl(h, 3, A, A, 0, -1, A, A, A, None) == 1
+    assert L.tq_encode_qjl(h, 3, None, None, 0, 0, None, None, None, None) == 0
+    assert L.tq_encode_qjl(h, 3, None, A, 0, 4, A, A, A, None) == 1
+    assert L.tq_encode_qjl(h, 3, A, A, 0, 4, A, A, None, None) == 1
+    assert L.tq_encode_qjl(h, 3, A + 4, A, 0, 4, A, A, A, None) == 3
+    assert L.tq_encode_qjl(h, 3, A, A, 0, 4, A, A, A + 2, None) == 3
+    # tq_decode_qjl(plan, bits, S, packed, norms, rnorms, n, y, dtype, stream)
+    assert L.tq_decode_qjl(h, 1, A, A, A, A, 4, A, 0, None) == 2
+    assert L.tq_decode_qjl(p16.handle, 3, A, A, A, A, 4, A, 0, None) == 2
+    assert L.tq_decode_qjl(h, 3, A, A, A, None, 4, A, 0, None) == 1
+    assert L.tq_decode_qjl(h, 3, A, A + 8, A, A, 4, A, 0, None) == 3
+    assert L.tq_decode_qjl(h, 3, None, None, None, None, 0, None, 0, None) == 0
+    # workspace: rotated and projected queries (2 d floats per query head, in
+    # 64-float units) then (d + 2) floats per query head and split
+    assert L.tq_attn_qjl_workspace_bytes(1, 8, 2, 256, 1000) == 0
+    assert L.tq_attn_qjl_workspace_bytes(1, 12, 8, 128, 1000) == 0  # Hq % Hkv
+    n = L.tq_attn_qjl_workspace_bytes(1, 8, 2, 128, 1000)
+    assert n >= 4 * (2048 + 8 * 130) and (n - 4 * 2048) % (4 * 8 * 130) == 0
+    cv = abi.CacheView(A, A, A, A, 256)
+    W = 1 << 24
+    # tq_attn_decode_qjl(plan, S, q, B, Hq, Hkv, cache, k_rnorm, ctx, kb, vb, scale, out, ws, ws_bytes, s)
+    assert L.tq_attn_decode_qjl(None, A, A, 1, 8, 2, cv, A, 100, 3, 3, f(1.0), A, A, W, None) == 1
+    assert L.tq_attn_decode_qjl(p256.handle, A, A, 1, 8, 2, cv, A, 100, 3, 3, f(1.0), A, A, W, None) == 2
+    assert L.tq_attn_decode_qjl(h, A, A, 1, 8, 2, cv, A, 100, 5, 3, f(1.0), A, A, W, None) == 2
+    assert L.tq_attn_decode_qjl(h, A, A, 1, 36, 2, cv, A, 100, 3, 3, f(1.0), A, A, W, None) == 2  # group 18
+    assert L.tq_attn_decode_qjl(h, A, A, 1, 8, 2, cv, A, 300, 3, 3, f(1.0), A, A, W, None) == 4  # ctx > cap
+    assert L.tq_attn_decode_qjl(h, A, A + 8, 1, 8, 2, cv, A, 100, 3, 3, f(1.0), A, A, W, None) == 3
+    assert L.tq_attn_decode_qjl(h, A, A, 0, 8, 2, cv, A, 100, 3, 3, f(1.0), A, A, W, None) == 0  # B = 0
