@@ -25,7 +25,8 @@ CODEC_DIMS = (8, 16, 32, 64, 128, 256)
 ATTN_DIMS = (32, 64, 128, 256)
 UNITS = ([("tq_api.cpp", {}), ("tq_launch.cu", {}), ("tq_noalloc.cu", {})]
          + [("tq_codec.cu", {"D": d}) for d in CODEC_DIMS]
-         + [("tq_attn.cu", {"D": d, "KB": kb}) for d in ATTN_DIMS for kb in (2, 3, 4)]
+         + [("tq_attn.cu", {"D": 128, "KB": kb}) for kb in (2, 3, 4)]
+         + [("tq_attn_generic.cu", {"D": d, "KB": kb}) for d in ATTN_DIMS for kb in (2, 3, 4)]
          + [("tq_prefill.cu", {"KB": kb}) for kb in (2, 3, 4)]
          + [("tq_qjl.cu", {"D": d}) for d in (32, 64, 128)])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

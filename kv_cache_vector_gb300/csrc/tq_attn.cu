@@ -1,14 +1,12 @@
-// tq_attn.cu -- decode attention over the packed cache, in the rotated domain.
+// tq_attn.cu -- decode attention over the packed cache at d = 128, on the
+// tensor cores (the other head dimensions and QJL keys: tq_attn_generic.cu).
 //
 // "TurboQuant KV Cache Compression -- Spec", Optimization: Fused dequant-dot:
 // rotate q once, score each cached position against its centroids
 // ((Rq).(Rk) = q.k), accumulate V in the rotated domain, rotate the output
-// back once.  Split-K flash-decode: CTA (split, kv head, batch) handles a
-// contiguous range of positions for all Hq/Hkv query heads of the GQA group
-// and writes fp32 partials (running max m, denominator l, accumulator acc[d]);
-// a second kernel merges the splits by log-sum-exp, normalises and
-// un-rotates.  "CITATIONS", Sparse V dequant: a V row is skipped when every
-// head's exp(sigma - m) is below the threshold; it still counts in l.
+// back once.  Split-K flash-decode with fp32 partials merged by log-sum-exp.
+// "CITATIONS", Sparse V dequant: a V row is skipped when every head's
+// exp(sigma - m) is below the threshold; it still counts in l.
 #include <cfloat>
 #include <type_traits>
 
@@ -19,321 +17,6 @@
 
 namespace tq {
 namespace dev {
-
-constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kMaxGroup = 8;
-
-// Cache row of position p of (sequence b, KV head g): contiguous, or through
-// the block table (-1 for a page id out of range, which is not read).
-template <bool PAGED>
-__device__ __forceinline__ int64_t attn_row(const tq_cache_view& cache, const PagedArgs& pa, int Hkv, int b, int g,
-                                            int64_t p) {
-    if constexpr (PAGED) {
-        const int page = __ldg(pa.bt + (int64_t)b * pa.max_pages + (p >> pa.page_shift));
-        if (page < 0 || page >= pa.n_pages) return -1;
-        return (((int64_t)page * Hkv + g) << pa.page_shift) + (p & ((int64_t(1) << pa.page_shift) - 1));
-    } else {
-        return ((int64_t)b * Hkv + g) * cache.cap + p;
-    }
-}
-
-// The lane's LB <= 32 bits of a packed row starting at bit LB * lane.
-template <int LB>
-__device__ __forceinline__ uint32_t lane_bits(const uint8_t* row, int lane) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
-    const int bit0 = lane * LB, wi = bit0 / 32, sh = bit0 % 32;
-    uint32_t x = __ldg(w + wi) >> sh;
-    if (sh + LB > 32) x |= __ldg(w + wi + 1) << (32 - sh);
-    return x;
-}
-
-// Head dimensions other than 128 (CUDA cores, fp32 centroids).  CTA (split,
-// KV head, sequence) takes positions [split * split_len, ..) of the
-// sequence's length: ctx_len (contiguous), or, PAGED, lens[b] + len_plus
-// clamped to [0, ctx_len] (len_plus = 1 when lens holds the positions just
-// appended).  The group's queries are rotated into shared memory; the scores
-// take a warp per position (lane l holds dims [l D/32, (l+1) D/32) of the key,
-// the query in a transposed copy so that lanes read consecutive words), then
-// the exponentials, then the V product a warp per position.  A split with no
-// positions writes an empty partial (m = -FLT_MAX, l = 0).
-//
-// QJL: keys in the QJL residual format of KB bits (a (KB - 1)-bit index per
-// coordinate, then d sign bits of the projected residual; k_rnorm holds
-// gamma).  The score is n <q~, c[idx]> + gamma <q', sgn> with q~ the rotated
-// scaled query and q' = sqrt(pi/2)/d * S q~, both read from qpre (written by
-// k_qjl_query) instead of rotating q here: S then never meets the keys.
-template <int D, int KB, int VB, bool PAGED, bool QJL = false>
-__global__ void __launch_bounds__(kAttnThreads)
-k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view cache,
-             int64_t ctx_len, int split_len, int n_splits, float* __restrict__ ws,
-             const __grid_constant__ AttnParams P, const PagedArgs pa, int len_plus, int* status,
-             const float* __restrict__ qpre, const float* __restrict__ k_rnorm) {
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int G = Hq / Hkv;
-    int64_t Ls = ctx_len;
-    if constexpr (PAGED) {
-        const int64_t l = (int64_t)__ldg(pa.lens + b) + len_plus;
-        Ls = l < 0 ? 0 : (l < ctx_len ? l : ctx_len);
-    }
-    const int64_t t0 = (int64_t)split * split_len;
-    const int len = (int)(Ls - t0 < 0 ? 0 : (Ls - t0 < split_len ? Ls - t0 : split_len));
-    constexpr int EPL = D / 32;  // dims per lane
-
-    extern __shared__ float smem[];
-    float* qrot = smem;                          // [G][D]
-    float* qT = qrot + kMaxGroup * D;            // [G * EPL][32]: dim l EPL + e of head h at (h EPL + e) 32 + l
-    float* sc = qT + kMaxGroup * D;              // [G][split_len]: scores, then exp
-    float* accs = sc + kMaxGroup * split_len;    // [G][D] cross-warp sum
-    float* red = accs + kMaxGroup * D;           // [kAttnWarps][kMaxGroup]
-    float* mh = red + kAttnWarps * kMaxGroup;    // [kMaxGroup] max per head
-    float* lh = mh + kMaxGroup;                  // [kMaxGroup] denominators
-    float* kcen = lh + kMaxGroup;                // [16]
-    float* vcen = kcen + 16;                     // [16]
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (len == 0) {  // block-uniform: an empty partial
-        for (int i = tid; i < G * (D + 2); i += blockDim.x) {
-            const int h = i / (D + 2), j = i % (D + 2);
-            ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = j == D ? -FLT_MAX : 0.f;
-        }
-        return;
-    }
-    if (tid < 16) {
-        kcen[tid] = P.kcen[tid];
-        vcen[tid] = P.vcen[tid];
-    }
-    if constexpr (QJL) {
-        // rotated queries and their projections; the projections wait in the
-        // cross-warp sum buffer, which pass 2 clears only after pass 1
-        for (int i = tid; i < G * D; i += blockDim.x) {
-            const int h = i / D, j = i % D;
-            const float* src = qpre + ((int64_t)b * Hq + g * G + h) * 2 * D;
-            qrot[i] = src[j];
-            accs[i] = src[D + j];
-        }
-    } else {
-        // ---- rotate the group's queries: qrot = H (s . q) / sqrt(d), times scale
-        for (int i = tid; i < G * D; i += blockDim.x) {
-            const int h = i / D, j = i % D;
-            const float x = __bfloat162float(q[((int64_t)b * Hq + g * G + h) * D + j]);
-            qrot[i] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
-        }
-        fwht_smem<D>(qrot, G);
-        for (int i = tid; i < G * D; i += blockDim.x) {
-            const uint32_t m = P.two_sided ? P.sgn2[i % D] : 0u;
-            qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += blockDim.x) {
-        const int h = i / D, j = i % D;
-        qT[(h * EPL + j % EPL) * 32 + j / EPL] = qrot[i];
-    }
-    __syncthreads();
-
-    constexpr int KRB = D * KB / 8, VRB = D * VB / 8;
-    constexpr int KLB = EPL * KB, VLB = EPL * VB;  // bits per lane (<= 32)
-
-    // ---- pass 1: sigma = n_k * (qrot . c_k), a warp per position
-    float mloc[kMaxGroup];
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) mloc[h] = -FLT_MAX;
-    for (int t = warp; t < len; t += kAttnWarps) {
-        const int64_t row = attn_row<PAGED>(cache, pa, Hkv, b, g, t0 + t);
-        if (row < 0) {  // warp-uniform: a page id out of range, nothing read
-            if (lane == 0) {
-                report_timeout(status, 33);
-                for (int h = 0; h < G; ++h) sc[h * split_len + t] = -FLT_MAX;
-            }
-            continue;
-        }
-        const float nk = __ldg(cache.k_norm + row);
-        float part[kMaxGroup];
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) part[h] = 0.f;
-        if constexpr (QJL) {
-            constexpr int MB = KB - 1, KIB = D * MB / 8;  // index bits per coordinate, index bytes
-            const uint8_t* krow = cache.k_packed + row * KRB;
-            const uint32_t bits = lane_bits<EPL * MB>(krow, lane);
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(krow + KIB);
-            float sp[kMaxGroup];
-#pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h) sp[h] = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                const float c = kcen[(bits >> (e * MB)) & ((1u << MB) - 1)];
-                // projection k = 32 e + lane: its sign is bit `lane` of word e
-                const uint32_t neg = (~__ldg(sw + e) >> lane) << 31;
-#pragma unroll
-                for (int h = 0; h < kMaxGroup; ++h)
-                    if (h < G) {
-                        part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
-                        sp[h] += __uint_as_float(__float_as_uint(accs[h * D + 32 * e + lane]) ^ neg);
-                    }
-            }
-            const float gk = __ldg(k_rnorm + row);
-#pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h) part[h] = fmaf(nk, part[h], gk * sp[h]);
-        } else {
-            const uint32_t bits = lane_bits<KLB>(cache.k_packed + row * KRB, lane);
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                const float c = kcen[(bits >> (e * KB)) & ((1u << KB) - 1)];
-#pragma unroll
-                for (int h = 0; h < kMaxGroup; ++h)
-                    if (h < G) part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-            if (h < G) {
-                float s = part[h];
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-                if constexpr (!QJL) s *= nk;
-                if (lane == 0) sc[h * split_len + t] = s;
-                mloc[h] = fmaxf(mloc[h], s);
-            }
-        }
-    }
-    // block max per head
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-        float m = mloc[h];
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) red[warp * kMaxGroup + h] = m;
-    }
-    __syncthreads();
-    if (tid < kMaxGroup) {
-        float m = -FLT_MAX;
-        for (int w = 0; w < kAttnWarps; ++w) m = fmaxf(m, red[w * kMaxGroup + tid]);
-        mh[tid] = m;
-    }
-    __syncthreads();
-    // ---- exp and denominators
-    float lloc[kMaxGroup];
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) lloc[h] = 0.f;
-    for (int t = tid; t < len; t += blockDim.x) {
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
-            if (h < G) {
-                const float e = __expf(sc[h * split_len + t] - mh[h]);
-                sc[h * split_len + t] = e;
-                lloc[h] += e;
-            }
-    }
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-        float l = lloc[h];
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-        if (lane == 0) red[warp * kMaxGroup + h] = l;
-    }
-    __syncthreads();
-    if (tid < kMaxGroup) {
-        float l = 0.f;
-        for (int w = 0; w < kAttnWarps; ++w) l += red[w * kMaxGroup + tid];
-        lh[tid] = l;
-    }
-    for (int i = tid; i < G * D; i += blockDim.x) accs[i] = 0.f;
-    __syncthreads();
-
-    // ---- pass 2: acc += p_t * n_v * c_v in the rotated domain.  A warp takes
-    // one position at a time; lane l owns elements [l*EPL, (l+1)*EPL).
-    float acc[kMaxGroup][EPL];
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
-    const float thr = P.sparse_thr;
-    int nread = 0;  // rows whose V this warp reads
-    for (int t = warp; t < len; t += kAttnWarps) {
-        float pm = 0.f;
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
-            if (h < G) pm = fmaxf(pm, sc[h * split_len + t]);
-        if (pm < thr) continue;  // warp-uniform
-        const int64_t row = attn_row<PAGED>(cache, pa, Hkv, b, g, t0 + t);
-        if (row < 0) continue;  // warp-uniform: a page id out of range
-        ++nread;
-        const uint32_t bitsv = lane_bits<VLB>(cache.v_packed + row * VRB, lane);
-        const float nv = __ldg(cache.v_norm + row);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const float c = vcen[(bitsv >> (e * VB)) & ((1u << VB) - 1)] * nv;
-#pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h)
-                if (h < G) acc[h][e] = fmaf(sc[h * split_len + t], c, acc[h][e]);
-        }
-    }
-    if (P.v_rows && lane == 0 && nread > 0) atomicAdd(P.v_rows + (int64_t)b * Hkv + g, nread);
-    // fixed-order cross-warp reduction
-    for (int w = 0; w < kAttnWarps; ++w) {
-        if (warp == w) {
-#pragma unroll
-            for (int h = 0; h < kMaxGroup; ++h)
-                if (h < G)
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) accs[h * D + lane * EPL + e] += acc[h][e];
-        }
-        __syncthreads();
-    }
-    // ---- partials: ws[b][h][split][D + 2] = acc..., m, l
-    for (int i = tid; i < G * (D + 2); i += blockDim.x) {
-        const int h = i / (D + 2), j = i % (D + 2);
-        const float v = j < D ? accs[h * D + j] : (j == D ? mh[h] : lh[h]);
-        ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = v;
-    }
-}
-
-// Merge the splits of one (batch, query head) by log-sum-exp, normalise and
-// rotate back: out = s . (H o_rot) / sqrt(d).
-template <int D>
-__global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws, int n_splits,
-                                                    float* __restrict__ out,
-                                                    const __grid_constant__ AttnParams P) {
-    __shared__ float o[D];
-    const int bh = blockIdx.x, j = threadIdx.x;
-    const float* base = ws + (int64_t)bh * n_splits * (D + 2);
-    float M = -FLT_MAX;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, base[s * (D + 2) + D]);
-    float L = 0.f, a = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-        const float f = __expf(base[s * (D + 2) + D] - M);
-        L = fmaf(f, base[s * (D + 2) + D + 1], L);
-        a = fmaf(f, base[s * (D + 2) + j], a);
-    }
-    const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
-    o[j] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? P.sgn2[j] : 0u));
-    fwht_smem<D>(o, 1);
-    out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ P.sgn[j]);
-}
-
-// QJL keys: the rotated query of one (batch, query head), times the softmax
-// scale, and its projection by the QJL matrix times sqrt(pi/2)/d, written to
-// qpre[bh][0, D) and [D, 2D).  One block of D threads per head; thread k
-// forms projection k from row k of S.
-template <int D>
-__global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict__ q,
-                                                 const float* __restrict__ S, float* __restrict__ qpre,
-                                                 const __grid_constant__ AttnParams P, float kappa) {
-    __shared__ float v[D];
-    const int bh = blockIdx.x, j = threadIdx.x;
-    const float x = __bfloat162float(q[(int64_t)bh * D + j]);
-    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
-    fwht_smem<D>(v, 1);
-    const uint32_t m = P.two_sided ? P.sgn2[j] : 0u;
-    const float r = __uint_as_float(__float_as_uint(v[j]) ^ m) * (P.inv_sqrt_d * P.scale);
-    __syncthreads();
-    v[j] = r;
-    __syncthreads();
-    float p = 0.f;
-    const float* row = S + (int64_t)j * D;
-#pragma unroll 8
-    for (int i = 0; i < D; ++i) p = fmaf(__ldg(row + i), v[i], p);
-    qpre[(int64_t)bh * 2 * D + j] = r;
-    qpre[(int64_t)bh * 2 * D + D + j] = p * kappa;
-}
 
 // ============================================================ d = 128
 //
@@ -1677,77 +1360,27 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     return cudaGetLastError();
 }
 
-template <int D, int KB, int VB, bool PAGED = false>
-cudaError_t attn_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
-                        int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
-                        const AttnParams& P, cudaStream_t s, const PagedArgs& pa = PagedArgs{},
-                        int len_plus = 0) {
-    auto fn = k_attn_split<D, KB, VB, PAGED>;
-    const size_t smem = sizeof(float) * (kMaxGroup * D * 3 + (size_t)kMaxGroup * geo.split_len +
-                                         kAttnWarps * kMaxGroup + 2 * kMaxGroup + 32);
-    dim3 grid(geo.n_splits, Hkv, B);
-    fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
-                                       geo.split_len, geo.n_splits, static_cast<float*>(ws), P, pa, len_plus,
-                                       status_word(), nullptr, nullptr);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_attn_combine<D><<<B * Hq, D, 0, s>>>(static_cast<const float*>(ws), geo.n_splits, out, P);
-    return cudaGetLastError();
-}
-
-// QJL keys (contiguous cache): the query prologue, the split kernel with QJL
-// scoring over the workspace after the prologue's qpre, and the combine.
-template <int D, int KB, int VB>
-cudaError_t attn_qjl_launch(const void* q, const float* S, int B, int Hq, int Hkv, const tq_cache_view& cache,
-                            const float* k_rnorm, int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
-                            const AttnParams& P, cudaStream_t s) {
-    float* qpre = static_cast<float*>(ws);
-    float* part = qpre + attn_qjl_prefix_floats(B, Hq, D);
-    k_qjl_query<D><<<B * Hq, D, 0, s>>>(static_cast<const __nv_bfloat16*>(q), S, qpre, P,
-                                        (float)(1.2533141373155003 / D));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    auto fn = k_attn_split<D, KB, VB, false, true>;
-    const size_t smem = sizeof(float) * (kMaxGroup * D * 3 + (size_t)kMaxGroup * geo.split_len +
-                                         kAttnWarps * kMaxGroup + 2 * kMaxGroup + 32);
-    dim3 grid(geo.n_splits, Hkv, B);
-    fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
-                                       geo.split_len, geo.n_splits, part, P, PagedArgs{}, 0, status_word(), qpre,
-                                       k_rnorm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_attn_combine<D><<<B * Hq, D, 0, s>>>(part, geo.n_splits, out, P);
-    return cudaGetLastError();
-}
-
-template <int D, int KB>
-cudaError_t attn_vb(int vb, const void* q, int B, int Hq, int Hkv, const tq_cache_view& c,
-                    int64_t ctx, float* out, void* ws, const AttnGeometry& geo, const AttnParams& P,
-                    cudaStream_t s) {
-    if constexpr (D == 128) {
-        switch (vb) {
-            case 2: return attn3_launch<KB, 2>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-            case 3: return attn3_launch<KB, 3>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-            default: return attn3_launch<KB, 4>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-        }
-    }
-    switch (vb) {
-        case 2: return attn_launch<D, KB, 2>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-        case 3: return attn_launch<D, KB, 3>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-        default: return attn_launch<D, KB, 4>(q, B, Hq, Hkv, c, ctx, out, ws, geo, P, s);
-    }
-}
-
 }  // namespace dev
 
-template <int D, int KB>
-cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv,
-                           const tq_cache_view& cache, int64_t ctx_len, float* out, void* workspace,
-                           const AttnGeometry& g, const AttnParams& P, cudaStream_t s) {
-    return dev::attn_vb<D, KB>(v_bits, q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, P, s);
-}
+#if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB) || TQ_UNIT_D != 128
+#error "compile for d = 128, once per K width, with -DTQ_UNIT_D=128 -DTQ_UNIT_KB=<bits>"
+#endif
 
-#if TQ_UNIT_D == 128
+template <int D, int KB>
+cudaError_t launch_attn_dk(int v_bits, const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache,
+                           int64_t ctx_len, float* out, void* workspace, const AttnGeometry& g, const AttnParams& P,
+                           cudaStream_t s) {
+    static_assert(D == 128, "the tensor-core kernel is d = 128 only");
+    switch (v_bits) {
+        case 2: return dev::attn3_launch<KB, 2>(q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, P, s);
+        case 3: return dev::attn3_launch<KB, 3>(q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, P, s);
+        default: return dev::attn3_launch<KB, 4>(q, B, Hq, Hkv, cache, ctx_len, out, workspace, g, P, s);
+    }
+}
+template cudaError_t launch_attn_dk<128, TQ_UNIT_KB>(int, const void*, int, int, int, const tq_cache_view&, int64_t,
+                                                     float*, void*, const AttnGeometry&, const AttnParams&,
+                                                     cudaStream_t);
+
 template <int KB>
 cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
                                  const tq_cache_view& pages, int64_t max_ctx, float* out,
@@ -1763,51 +1396,5 @@ template cudaError_t launch_attn128_paged<TQ_UNIT_KB>(int, const void*, int, int
                                                       int64_t, float*, void*, const AttnGeometry&,
                                                       const AttnParams&, const PagedArgs&, cudaStream_t,
                                                       const AttnAppend*);
-#endif
-
-#if TQ_UNIT_D != 128
-// Head dimensions other than 128, paged cache: the generic kernel with the
-// block table; len_plus = 1 when pa.lens holds the positions just appended.
-template <int D, int KB>
-cudaError_t launch_attn_generic_paged(int v_bits, const void* q, int B, int Hq, int Hkv,
-                                      const tq_cache_view& pages, int64_t max_ctx, float* out, void* workspace,
-                                      const AttnGeometry& g, const AttnParams& P, const PagedArgs& pa,
-                                      int len_plus, cudaStream_t s) {
-    switch (v_bits) {
-        case 2: return dev::attn_launch<D, KB, 2, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
-        case 3: return dev::attn_launch<D, KB, 3, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
-        default: return dev::attn_launch<D, KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, len_plus);
-    }
-}
-template cudaError_t launch_attn_generic_paged<TQ_UNIT_D, TQ_UNIT_KB>(int, const void*, int, int, int,
-                                                                       const tq_cache_view&,
-                                                           int64_t, float*, void*, const AttnGeometry&,
-                                                           const AttnParams&, const PagedArgs&, int, cudaStream_t);
-#endif
-
-#if TQ_UNIT_D <= 128
-template <int D, int KB>
-cudaError_t launch_attn_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
-                            const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
-                            void* workspace, const AttnGeometry& g, const AttnParams& P, cudaStream_t s) {
-    switch (v_bits) {
-        case 2: return dev::attn_qjl_launch<D, KB, 2>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
-        case 3: return dev::attn_qjl_launch<D, KB, 3>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
-        default: return dev::attn_qjl_launch<D, KB, 4>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, s);
-    }
-}
-template cudaError_t launch_attn_qjl<TQ_UNIT_D, TQ_UNIT_KB>(int, const void*, const float*, int, int, int,
-                                                            const tq_cache_view&, const float*, int64_t, float*,
-                                                            void*, const AttnGeometry&, const AttnParams&,
-                                                            cudaStream_t);
-#endif
-
-#if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB)
-#error "compile once per head dimension and K width with -DTQ_UNIT_D=<d> -DTQ_UNIT_KB=<bits>"
-#endif
-template cudaError_t launch_attn_dk<TQ_UNIT_D, TQ_UNIT_KB>(int, const void*, int, int, int,
-                                                           const tq_cache_view&, int64_t, float*,
-                                                           void*, const AttnGeometry&,
-                                                           const AttnParams&, cudaStream_t);
 
 }  // namespace tq

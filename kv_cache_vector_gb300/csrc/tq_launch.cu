@@ -97,7 +97,9 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
         g.q16 = true;
         return g;
     }
-    int split = 512;
+    // the generic kernel stages its whole range in shared memory: at most 512
+    // positions (256 at d = 256) keep two CTAs per SM
+    int split = d > 128 ? 256 : 512;
     const int64_t want = 2LL * (sms > 0 ? sms : 1);
     while (split > 64 && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
     g.split_len = split;
