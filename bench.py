@@ -48,7 +48,8 @@ def args_():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["encode", "decode", "attn", "append"], default=None,
                     help="run just one kernel per step (profiling of one kernel)")
-    ap.add_argument("--extra", choices=["codec_roundtrip", "long_context", "gemma_cache", "paged_varlen", "prefill"],
+    ap.add_argument("--extra", choices=["codec_roundtrip", "long_context", "gemma_cache", "paged_varlen", "prefill",
+                                        "qjl"],
                     default=None,
                     help="run just one of the extra measurements and print its result (profiling)")
     return ap.parse_args()
@@ -559,6 +560,93 @@ def extra_long_context(peak, with_oracle=True):
     return res
 
 
+def fp32_alu_peak_tflops():
+    """FP32 FMA peak: 152 SMs x 128 lanes x 2 flops per clock at the maximum
+    SM clock of MEASURED_PEAKS.json (2070 MHz): 80.5 TFLOP/s."""
+    mhz = 2070.0
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def extra_qjl(peak, small=False):
+    """QJL residual keys at d = 128, 4 bits (3-bit MSE index + 1 sign per
+    coordinate).  Codec: 1,048,576 bf16 low-rank rows with outlier channels
+    (one layer of the Llama-8B-shaped prefill: 8 KV heads x 16 x 8192), encode
+    and decode, inputs above L2 (256 MB), 20 calls each; bound by the fp32
+    projection (2 d^2 flops per row).  Attention: the decode-attention
+    workload (B32, Hq32/Hkv8, ctx 32768) with QJL K4 keys and plain V3 values,
+    20 calls over a 1.07 GB cache; parity sample: the oracle's attention of
+    one (batch, KV head) group from its own encoding of the raw rows.
+    small (profiling): 1/8 of the codec rows and batch 8 (a 260 MB cache)."""
+    import numpy as np
+    import torch
+    from kv_cache_vector_gb300 import abi, synth
+    bits, n = 4, 8 * 16 * 8192 // (8 if small else 1)
+    plan = abi.Plan(D, 42)
+    S = abi.tq_qjl_matrix(plan)
+    x = torch.cat([synth.lowrank_rows(77, n // 8, D, stream=h, device="cuda") for h in range(8)])
+    pk, nm, rn = abi.tq_encode_qjl(plan, bits, S, x)
+    y = abi.tq_decode_qjl(plan, bits, S, pk, nm, rn, torch.bfloat16)
+    alu = fp32_alu_peak_tflops()
+    res = {"config": "d128 K4 (3-bit index + QJL signs); codec 1048576 bf16 rows; attention B32 Hq32/Hkv8 "
+                     "ctx32768 K4(QJL)/V3, scale 1/sqrt(128)", "alu_peak_tflops": round(alu, 1)}
+    cb = n * (D * 2 + D * bits // 8 + 8)
+    for name, fn in (("encode", lambda: abi.tq_encode_qjl(plan, bits, S, x)),
+                     ("decode", lambda: abi.tq_decode_qjl(plan, bits, S, pk, nm, rn, torch.bfloat16))):
+        for _ in range(3):
+            fn()
+        ms = time_events(fn, 20)
+        gbps = cb / (ms * 1e-3) / 1e9
+        tf = n * 2 * D * D / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 4), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4),
+                     "projection_tflops": round(tf, 2), "frac_alu": round(tf / alu, 4), "repeats": 20}
+    del x, y, pk, nm, rn
+    B, Hq, Hkv, ctx, kb, vb = (8 if small else 32), 32, 8, 32768, 4, 3
+    if small:
+        res["config"] = res["config"].replace("1048576", str(n)).replace("B32", "B8")
+    cache = abi.Cache.empty(B, Hkv, ctx, D, kb, vb)
+    k_rn = torch.empty(B, Hkv, ctx, device="cuda")
+    raw = {}
+    for h in range(Hkv):
+        k = synth.lowrank_rows(91, B * ctx, D, stream=10000 + h, device="cuda")
+        v = synth.lowrank_rows(91, B * ctx, D, stream=20000 + h, device="cuda")
+        if h == 0:
+            raw = (k[:ctx].clone(), v[:ctx].clone())  # batch 0, KV head 0
+        p2, n2, g2 = abi.tq_encode_qjl(plan, kb, S, k)
+        cache.k_packed[:, h] = p2.view(B, ctx, -1)
+        cache.k_norm[:, h] = n2.view(B, ctx)
+        k_rn[:, h] = g2.view(B, ctx)
+        p2, n2 = abi.tq_encode(plan, vb, v)
+        cache.v_packed[:, h] = p2.view(B, ctx, -1)
+        cache.v_norm[:, h] = n2.view(B, ctx)
+        del k, v
+    q = synth.device_normal(93, (B, Hq, D))
+    out = torch.empty(B, Hq, D, device="cuda")
+    ws = torch.empty(abi.tq_attn_qjl_workspace_bytes(B, Hq, Hkv, D, ctx), dtype=torch.uint8, device="cuda")
+    f = lambda: abi.tq_attn_decode_qjl(plan, S, q, cache, k_rn, ctx, 1.0 / math.sqrt(D), out=out, workspace=ws)
+    for _ in range(3):
+        f()
+    ms = time_events(f, 20)
+    ab = B * Hkv * ctx * (D * (kb + vb) // 8 + 12) + B * Hq * D * (2 + 4)
+    res["attention"] = {"us": round(ms * 1e3, 2), "GBps": round(ab / (ms * 1e-3) / 1e9, 1),
+                        "frac": round(ab / (ms * 1e-3) / 1e9 / peak, 4),
+                        "frac_nominal": round(ab / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                        "bytes": ab, "repeats": 20}
+    from oracle import oracle as O
+    s = O.signs(42, D)
+    S64 = O.qjl_matrix(42, D)
+    kp, kn, kg = O.encode_qjl(s, kb, raw[0].double().cpu().numpy(), S64)
+    vp, vn = O.encode(s, vb, raw[1].double().cpu().numpy())
+    G = Hq // Hkv
+    want = O.attention_qjl(s, q[:1, :G].double().cpu().numpy(), kp[None, None], kn[None, None], kg[None, None],
+                           S64, vp[None, None], vn[None, None], kb, vb, ctx, 1.0 / math.sqrt(D))
+    res["attention"]["parity_max_abs_err_b0_g0"] = float(np.abs(out[:1, :G].cpu().numpy() - want).max())
+    return res
+
+
 def extra_paged(peak):
     """Paged cache with a length per sequence (serving-style decode): batch 32,
     32 query / 8 KV heads, d 128, K4/V3, pages of 256 positions in a shuffled
@@ -853,8 +941,10 @@ def main():
     if a.extra:
         if rank == 0:
             fn = {"codec_roundtrip": extra_codec_roundtrip, "long_context": extra_long_context,
-                  "gemma_cache": extra_gemma, "paged_varlen": extra_paged, "prefill": extra_prefill}
-            print(json.dumps({"extra": a.extra, **fn[a.extra](measured_peak()[0])}))
+                  "gemma_cache": extra_gemma, "paged_varlen": extra_paged, "prefill": extra_prefill,
+                  "qjl": extra_qjl}
+            kw = {"small": True} if a.small and a.extra == "qjl" else {}
+            print(json.dumps({"extra": a.extra, **fn[a.extra](measured_peak()[0], **kw)}))
         barrier(world)
         return
     S = make_state(W, rank)
@@ -939,6 +1029,7 @@ def main():
         out["gemma_cache"] = extra_gemma(peak)
         out["paged_varlen"] = extra_paged(peak)
         out["prefill"] = extra_prefill(peak)
+        out["qjl"] = extra_qjl(peak)
     print(json.dumps(out))
     barrier(world)
 

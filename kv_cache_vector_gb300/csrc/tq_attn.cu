@@ -257,6 +257,7 @@ static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __r
                                                         float* __restrict__ qexp,
                                                         const __grid_constant__ AttnParams P, int64_t n_rows,
                                                         uint32_t* __restrict__ gmax) {
+    griddep_launch();  // the split kernel may start its table build now
     const int lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (bh >= n_rows) return;  // the whole warp
@@ -339,6 +340,7 @@ static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat
                                                                int v_bits, int32_t* __restrict__ len1, int* status) {
     __shared__ uint32_t sg[128], sg2[128];
     __shared__ uint8_t ib[2][128];
+    griddep_launch();
     const int j = threadIdx.x;
     sg[j] = P.sgn[j];
     sg2[j] = P.sgn2[j];
@@ -449,6 +451,7 @@ static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __res
     extern __shared__ __align__(16) unsigned char plan_smem[];
     __shared__ int64_t wsum[32];
     __shared__ int32_t cb[1025];
+    griddep_launch();
     const int tid = threadIdx.x;
     const int W = (int)(seg / warp_len), nC = warp_len / kA3Chunk;
     // exclusive prefix weight of each pair: shared memory, or the c0/clast
@@ -546,6 +549,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG, SP>::kThreads;
     constexpr uint32_t kAll = 0xFFFFFFFFu;
     extern __shared__ __align__(16) unsigned char a3_smem[];
+    griddep_launch();  // the combine may be scheduled; it waits for this grid
     const uint32_t base = smem_addr(a3_smem);
     if (base > kA3RingAt) {  // the layout below assumes dynamic memory starts lower
         if (threadIdx.x == 0) report_timeout(status, kA3StatusLayout);
@@ -580,6 +584,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         mbar_fence_init();
     }
     __syncthreads();
+    // everything above depends on the parameters only; from here on the
+    // rotated queries (and, paged, the work partition and appended rows) of
+    // the previous kernels are read
+    griddep_wait();
 
     const int g = lane >> 2, t = lane & 3;
     const int G = Hq / Hkv;
@@ -1187,14 +1195,15 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 // 65 + 2l (8-byte loads: a partial row is 130 floats).  The butterflies
 // over index bits 0 and 6 are in registers, those over bits 1-5 between
 // lanes, in the order len = 1, 2, .., 64.
-static __global__ void __launch_bounds__(256) k_attn3_combine(const float* __restrict__ part, int n_splits,
+static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __restrict__ part, int n_splits,
                                                               int grid, int64_t n_items, int Hq, int Hkv,
                                                               int64_t n_bh, float* __restrict__ out,
                                                               const __grid_constant__ AttnParams P,
                                                               bool paged, const A3Meta meta) {
-    const int lane = threadIdx.x & 31;
-    const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (bh >= n_bh) return;  // past the last (batch, query head): the whole warp
+    griddep_wait();  // the partials of the split kernel
+    __shared__ float red[3][132];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t bh = blockIdx.x;
     // partials of this (batch, query head): one per CTA whose items reach its KV head
     const int64_t bhk = (bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
     const int n_parts = paged ? meta.slot_base[meta.clast[bhk]] - meta.slot_base[meta.c0[bhk]] + 1
@@ -1202,21 +1211,37 @@ static __global__ void __launch_bounds__(256) k_attn3_combine(const float* __res
                                     attn3_cta_of(bhk * n_splits, grid, n_items) + 1;
     const float* base = part + bh * n_splits * 130;
     float M = -INFINITY;
-    for (int s = lane; s < n_parts; s += 32) M = fmaxf(M, __ldg(base + s * 130 + 128));
+    for (int s = lane; s < n_parts; s += 32) M = fmaxf(M, __ldcg(base + s * 130 + 128));
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    // the four warps take every fourth partial
     float L = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < n_parts; ++s) {  // unrolled: the loads of several partials in flight
+#pragma unroll 4
+    for (int s = w; s < n_parts; s += 4) {  // unrolled: the loads of several partials in flight
         const float* row = base + s * 130;
-        const float ms = __ldg(row + 128);
-        const float w = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
-        L = fmaf(w, __ldg(row + 129), L);
-        const float2 x = __ldg(reinterpret_cast<const float2*>(row) + lane);
-        const float2 y = __ldg(reinterpret_cast<const float2*>(row + 64) + lane);
-        a0 = fmaf(w, x.x, a0);
-        a1 = fmaf(w, x.y, a1);
-        a2 = fmaf(w, y.x, a2);
-        a3 = fmaf(w, y.y, a3);
+        const float ms = __ldcg(row + 128);
+        const float wt = ms == -INFINITY ? 0.f : fast_exp2(ms - M);
+        L = fmaf(wt, __ldcg(row + 129), L);
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(row) + lane);
+        const float2 y = __ldcg(reinterpret_cast<const float2*>(row + 64) + lane);
+        a0 = fmaf(wt, x.x, a0);
+        a1 = fmaf(wt, x.y, a1);
+        a2 = fmaf(wt, y.x, a2);
+        a3 = fmaf(wt, y.y, a3);
+    }
+    if (w > 0) {
+        *reinterpret_cast<float4*>(&red[w - 1][4 * lane]) = make_float4(a0, a1, a2, a3);
+        if (lane == 0) red[w - 1][128] = L;
+    }
+    __syncthreads();
+    if (w > 0) return;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {  // fixed order
+        const float4 r = *reinterpret_cast<const float4*>(&red[k][4 * lane]);
+        a0 += r.x;
+        a1 += r.y;
+        a2 += r.z;
+        a3 += r.w;
+        L += red[k][128];
     }
     // an empty context (paged, length 0) gives zeros
     float v[4] = {L > 0.f ? a0 / L : 0.f, L > 0.f ? a1 / L : 0.f, L > 0.f ? a2 / L : 0.f, L > 0.f ? a3 / L : 0.f};
@@ -1258,6 +1283,25 @@ static __global__ void __launch_bounds__(256) k_attn3_combine(const float* __res
     reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous one in the stream runs, and waits for it (griddep_wait)
+// before reading what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int KB, int VB, int NG, bool PAGED, bool SP>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
@@ -1276,10 +1320,8 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    fn<<<(unsigned)grid, A3Shape<KB, VB, NG, SP>::kThreads, L::kEnd, s>>>(q16, qexp, Hq, Hkv, cache, ctx_len,
-                                                                      geo.warp_len, geo.n_splits, items,
-                                                                      part, status_word(), P, pa, meta);
-    return cudaGetLastError();
+    return launch_pdl(fn, dim3((unsigned)grid), dim3(A3Shape<KB, VB, NG, SP>::kThreads), L::kEnd, s, q16, qexp, Hq,
+                      Hkv, cache, ctx_len, geo.warp_len, geo.n_splits, items, part, status_word(), P, pa, meta);
 }
 
 template <int KB, int VB, bool PAGED = false>
@@ -1355,9 +1397,8 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
                : attn3_split_launch<KB, VB, 2, PAGED, false>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items,
                                                              grid, part, P, pa, meta, s);
     if (e != cudaSuccess) return e;
-    k_attn3_combine<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(part, geo.n_splits, grid, items, Hq, Hkv,
-                                                                           (int64_t)B * Hq, out, P, PAGED, meta);
-    return cudaGetLastError();
+    return launch_pdl(k_attn3_combine, dim3((unsigned)(B * Hq)), dim3(128), 0, s, (const float*)part, geo.n_splits,
+                      grid, items, Hq, Hkv, (int64_t)B * Hq, out, P, PAGED, meta);
 }
 
 }  // namespace dev

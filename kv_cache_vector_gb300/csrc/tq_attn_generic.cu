@@ -231,7 +231,26 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- pass 1: sigma = n_k (q~ . c_k) (+ gamma q' . sgn), a warp per position
+    // ---- pass 1: sigma = n_k (q~ . c_k) (+ gamma q' . sgn), a warp per position.
+    // The lane's query values (and projections) are the same for every
+    // position: held in registers where they fit (the score stores into the
+    // same shared array would otherwise force a reload per position).
+    constexpr bool HOIST = (QJL ? 2 : 1) * GP * EPL <= 48;
+    float qreg[HOIST ? GP : 1][HOIST ? EPL : 1];
+    float preg[HOIST && QJL ? GP : 1][HOIST && QJL ? EPL : 1];
+    if constexpr (HOIST) {
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                qreg[h][e] = qT[(h * EPL + e) * 32 + lane];
+                if constexpr (QJL) preg[h][e] = accs[h * D + 32 * e + lane];
+            }
+    }
+    auto qv = [&](int h, int e) { if constexpr (HOIST) return qreg[h][e]; else return qT[(h * EPL + e) * 32 + lane]; };
+    auto pv = [&](int h, int e) {
+        if constexpr (HOIST && QJL) return preg[h][e]; else return accs[h * D + 32 * e + lane];
+    };
     const int myh = head_of<GP>(lane);
     const bool writer = (lane & (32 / GP - 1)) == 0;
     float mloc = -FLT_MAX;
@@ -254,10 +273,17 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         for (int e = 0; e < EPL; ++e) {
             const float c = kcen[(bits >> (e * MB)) & ((1u << MB) - 1)];
 #pragma unroll
-            for (int h = 0; h < GP; ++h) part[h] = fmaf(qT[(h * EPL + e) * 32 + lane], c, part[h]);
+            for (int h = 0; h < GP; ++h) part[h] = fmaf(qv(h, e), c, part[h]);
         }
         if constexpr (QJL) {
-            const uint32_t* sw = reinterpret_cast<const uint32_t*>(krow + KIB);
+            uint32_t sw[EPL];
+            if constexpr (EPL == 4 && KIB % 16 == 0) {
+                const uint4 w = *reinterpret_cast<const uint4*>(krow + KIB);
+                sw[0] = w.x; sw[1] = w.y; sw[2] = w.z; sw[3] = w.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) sw[e] = reinterpret_cast<const uint32_t*>(krow + KIB)[e];
+            }
             float sp[GP];
 #pragma unroll
             for (int h = 0; h < GP; ++h) sp[h] = 0.f;
@@ -266,8 +292,7 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
                 // projection k = 32 e + lane: its sign is bit `lane` of word e
                 const uint32_t neg = (~sw[e] >> lane) << 31;
 #pragma unroll
-                for (int h = 0; h < GP; ++h)
-                    sp[h] += __uint_as_float(__float_as_uint(accs[h * D + 32 * e + lane]) ^ neg);
+                for (int h = 0; h < GP; ++h) sp[h] += __uint_as_float(__float_as_uint(pv(h, e)) ^ neg);
             }
             const float nk = kn[t], gk = kg[t];
 #pragma unroll
