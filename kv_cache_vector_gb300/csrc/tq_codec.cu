@@ -1242,6 +1242,92 @@ k_decode3(const uint8_t* __restrict__ packed, const float* __restrict__ norms, i
     if (lane == 0) bulk_wait<0>();
 }
 
+// d = 256 with bf16 output: as k_decode3, two threads per row (lanes 2j and
+// 2j + 1 hold the row's two "split" parts, see RowShape), so a warp tile is
+// 16 rows; the transform ends with the cross-thread stage, leaving part p
+// with output dims 128p .. 128p + 127.  The tile (16 rows of 512 B) is staged
+// as four 128-byte-swizzled 64-column blocks and leaves as four 2-D TMA
+// stores.
+constexpr int kDec3bWarps = 4;
+constexpr int kDec3bSmem = kDec3bWarps * 2 * 8192 + 1024;
+
+template <int BITS>
+__global__ void __launch_bounds__(32 * kDec3bWarps, 2)
+k_decode3_256(const uint8_t* __restrict__ packed, const float* __restrict__ norms, int64_t n_rows,
+              const __grid_constant__ CUtensorMap ymap, const __grid_constant__ RowParams P) {
+    constexpr int D = 256, E = 128, RB = D * BITS / 8, HB = E / 2 * BITS / 8, NW = E * BITS / 32;
+    __shared__ float cen_s[16];
+    extern __shared__ __align__(1024) unsigned char dsm[];
+    unsigned char* base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rr = lane >> 1, p = lane & 1;  // row of the tile, part of the row
+    unsigned char* buf = base + warp * 2 * 8192;
+    const int64_t n_tiles = (n_rows + 15) / 16;
+    const int64_t wstride = (int64_t)gridDim.x * kDec3bWarps;
+    int64_t tile = (int64_t)blockIdx.x * kDec3bWarps + warp;
+    uint32_t wn[NW];
+    float nn = 0.f;
+    auto fetch = [&](int64_t tl) {
+        const int64_t row = tl * 16 + rr;
+        if (tl < n_tiles && row < n_rows) {
+            const uint8_t* src = packed + row * RB;
+            load_bytes<HB>(src + p * HB, wn);
+            load_bytes<HB>(src + 2 * HB + p * HB, wn + HB / 4);
+            nn = __ldg(norms + row);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NW; ++k) wn[k] = 0;
+            nn = 0.f;
+        }
+    };
+    fetch(tile);
+    int it = 0;
+    for (; tile < n_tiles; tile += wstride, ++it) {
+        uint32_t w[NW];
+#pragma unroll
+        for (int k = 0; k < NW; ++k) w[k] = wn[k];
+        const float norm = nn;
+        fetch(tile + wstride);
+        float v[E];
+        centroids_of<BITS, E>(w, cen_s, v);
+        if (P.two_sided) flip_rotated<D>(v, p, P.sgn2);
+        fwht_reg2<E>(v);
+        fwht_cross<E>(v, p);  // split -> contiguous: dims 128p + j
+        const float scs = norm * P.inv_sqrt_d;
+        const F2 sc = f2(scs, scs);
+        const uint32_t* sg = P.sgn + p * E;
+        unsigned char* b = buf + (it & 1) * 8192;
+        // the stores that last read this buffer (two tiles ago) must be done
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {  // 16-byte chunk c = dims 128p + 8c .. + 7
+            uint32_t q[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int k = 8 * c + 2 * m;
+                float ax, ay;
+                f2_split(f2_mul(f2(v[k], v[k + 1]), sc), ax, ay);
+                __nv_bfloat162 h = __floats2bfloat162_rn(ax, ay);
+                q[m] = *reinterpret_cast<uint32_t*>(&h) ^ ((sg[k] >> 16) | sg[k + 1]);
+            }
+            const int blk = 2 * p + (c >> 3), cc = c & 7;
+            *reinterpret_cast<uint4*>(b + blk * 2048 + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
+                make_uint4(q[0], q[1], q[2], q[3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) tma_store_2d(&ymap, 64 * blk, (int)(tile * 16), b + blk * 2048);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) bulk_wait<0>();
+}
+
 }  // namespace dev
 
 // ---------------------------------------------------------------- launchers
@@ -1347,9 +1433,27 @@ cudaError_t dec3(const uint8_t* pk, const float* nm, int64_t n, void* y, const R
     return cudaGetLastError();
 }
 
+template <int BITS>
+cudaError_t dec3_256(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
+    CUtensorMap map;
+    cudaError_t e = make_rows_map(&map, y, 2, 256, (uint64_t)n, 16);
+    if (e != cudaSuccess) return e;
+    auto fn = dev::k_decode3_256<BITS>;
+    e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kDec3bSmem);
+    if (e != cudaSuccess) return e;
+    const int per_sm = blocks_per_sm((const void*)fn, 32 * dev::kDec3bWarps, dev::kDec3bSmem);
+    const int64_t warp_tiles = (n + 15) / 16;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    const int64_t need = (warp_tiles + dev::kDec3bWarps - 1) / dev::kDec3bWarps;
+    if (grid > need) grid = need;
+    fn<<<(unsigned)grid, 32 * dev::kDec3bWarps, dev::kDec3bSmem, s>>>(pk, nm, n, map, P);
+    return cudaGetLastError();
+}
+
 template <int D, int BITS, typename TO>
 cudaError_t dec(const uint8_t* pk, const float* nm, int64_t n, void* y, const RowParams& P, cudaStream_t s) {
     if constexpr (D == 128 && sizeof(TO) == 2) return dec3<BITS>(pk, nm, n, y, P, s);
+    if constexpr (D == 256 && sizeof(TO) == 2) return dec3_256<BITS>(pk, nm, n, y, P, s);
     if constexpr (D == 64 || D == 128) {
         auto fn2 = dev::k_decode2<D, BITS, TO>;
         unsigned g = grid_for((const void*)fn2, 128, n);
