@@ -159,5 +159,24 @@ __device__ __forceinline__ void report_timeout(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous one in the stream runs, and waits for it (griddep_wait)
+// before reading what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace dev
 }  // namespace tq

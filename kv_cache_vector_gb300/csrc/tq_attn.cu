@@ -1283,25 +1283,6 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
     reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }
 
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous one in the stream runs, and waits for it (griddep_wait)
-// before reading what it wrote.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
 template <int KB, int VB, int NG, bool PAGED, bool SP>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,

@@ -142,6 +142,10 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
              int split_len, int n_splits, float* __restrict__ ws, const __grid_constant__ AttnParams P,
              const PagedArgs pa, int len_plus, int* status, const float* __restrict__ qpre,
              const float* __restrict__ k_rnorm) {
+    // the previous kernel in the stream may have written the cache or the
+    // queries: wait for it, then let the combine be scheduled
+    griddep_wait();
+    griddep_launch();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = Hq / Hkv;
     int64_t Ls = ctx_len;
@@ -407,11 +411,15 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
                                                     float* __restrict__ out,
                                                     const __grid_constant__ AttnParams P) {
     __shared__ float o[D];
+    griddep_wait();  // the split kernel's partials
+    griddep_launch();
     const int bh = blockIdx.x, j = threadIdx.x;
     const float* base = ws + (int64_t)bh * n_splits * (D + 2);
     float M = -FLT_MAX;
+#pragma unroll 4
     for (int s = 0; s < n_splits; ++s) M = fmaxf(M, base[s * (D + 2) + D]);
     float L = 0.f, a = 0.f;
+#pragma unroll 4  // several partials' loads in flight
     for (int s = 0; s < n_splits; ++s) {
         const float f = __expf(base[s * (D + 2) + D] - M);
         L = fmaf(f, base[s * (D + 2) + D + 1], L);
@@ -432,6 +440,8 @@ __global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict
                                                  const float* __restrict__ S, float* __restrict__ qpre,
                                                  const __grid_constant__ AttnParams P, float kappa) {
     __shared__ float v[D];
+    griddep_wait();
+    griddep_launch();
     const int bh = blockIdx.x, j = threadIdx.x;
     const float x = __bfloat162float(q[(int64_t)bh * D + j]);
     v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
@@ -467,10 +477,9 @@ cudaError_t split_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     auto go = [&](auto fn) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        fn<<<grid, kAttnThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, cache, ctx_len,
-                                           geo.split_len, geo.n_splits, part, P, pa, len_plus, status_word(),
-                                           qpre, k_rnorm);
-        return cudaGetLastError();
+        return launch_pdl(fn, grid, dim3(kAttnThreads), smem, s, static_cast<const __nv_bfloat16*>(q), Hq, Hkv,
+                          cache, ctx_len, geo.split_len, geo.n_splits, part, P, pa, len_plus, status_word(), qpre,
+                          k_rnorm);
     };
     if (G <= 2) return go(k_attn_split<D, KB, VB, PAGED, QJL, 2>);
     if (G <= 4) return go(k_attn_split<D, KB, VB, PAGED, QJL, 4>);
@@ -486,8 +495,7 @@ cudaError_t attn_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_vi
     cudaError_t e = split_launch<D, KB, VB, PAGED, false>(q, B, Hq, Hkv, cache, ctx_len, part, geo, P, s, pa,
                                                           len_plus, nullptr, nullptr);
     if (e != cudaSuccess) return e;
-    k_attn_combine<D><<<B * Hq, D, 0, s>>>(part, geo.n_splits, out, P);
-    return cudaGetLastError();
+    return launch_pdl(k_attn_combine<D>, dim3(B * Hq), dim3(D), 0, s, (const float*)part, geo.n_splits, out, P);
 }
 
 // QJL keys (contiguous cache): the query prologue, the split kernel with QJL
@@ -498,15 +506,13 @@ cudaError_t attn_qjl_launch(const void* q, const float* S, int B, int Hq, int Hk
                             const AttnParams& P, cudaStream_t s) {
     float* qpre = static_cast<float*>(ws);
     float* part = qpre + attn_qjl_prefix_floats(B, Hq, D);
-    k_qjl_query<D><<<B * Hq, D, 0, s>>>(static_cast<const __nv_bfloat16*>(q), S, qpre, P,
-                                        (float)(1.2533141373155003 / D));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_qjl_query<D>, dim3(B * Hq), dim3(D), 0, s, static_cast<const __nv_bfloat16*>(q), S,
+                               qpre, P, (float)(1.2533141373155003 / D));
     if (e != cudaSuccess) return e;
     e = split_launch<D, KB, VB, false, true>(q, B, Hq, Hkv, cache, ctx_len, part, geo, P, s, PagedArgs{}, 0, qpre,
                                              k_rnorm);
     if (e != cudaSuccess) return e;
-    k_attn_combine<D><<<B * Hq, D, 0, s>>>(part, geo.n_splits, out, P);
-    return cudaGetLastError();
+    return launch_pdl(k_attn_combine<D>, dim3(B * Hq), dim3(D), 0, s, (const float*)part, geo.n_splits, out, P);
 }
 
 }  // namespace dev
