@@ -973,8 +973,14 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 }
             };
             uint32_t out = 0u;  // bits outside the table's cell byte: some |u| >= 0.5, or not finite
+            // The row's packed words, low and high output halves (4 CW words
+            // each), kept in registers over the chunks and written as whole
+            // 16-byte vectors: per-chunk 4-byte stores of 32 rows 128 bytes
+            // apart sent 8x the output through the L1 write path.
+            uint32_t row_w[2][4 * CW];
             auto bucket_chunk = [&](const uint32_t (&a0)[32], const uint32_t (&a1)[32], int c) {
-                uint32_t wl[CW], wh[CW];
+                uint32_t (&wl)[CW] = *reinterpret_cast<uint32_t (*)[CW]>(&row_w[0][CW * c]);
+                uint32_t (&wh)[CW] = *reinterpret_cast<uint32_t (*)[CW]>(&row_w[1][CW * c]);
 #pragma unroll
                 for (int k = 0; k < CW; ++k) wl[k] = wh[k] = 0;
 #pragma unroll
@@ -990,7 +996,6 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     put(wl, i, e0.lo + (fmaf(ylo, inv, -e0.thr) >= 0.0f ? 1 : 0));
                     put(wh, i, e1.lo + (fmaf(yhi, inv, -e1.thr) >= 0.0f ? 1 : 0));
                 }
-                store(c, wl, wh);
             };
             // the common path unrolled (as the d = 128 epilogue): independent
             // elements across the whole row for the scheduler to overlap
@@ -1001,6 +1006,15 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 tmem_ld32(ta + 128 + 32 * c, a1);
                 tmem_wait_ld();
                 bucket_chunk(a0, a1, c);
+            }
+            if (valid) {  // HB = 16 CW bytes per half, 16-byte aligned (RB = 32 CW)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int k = 0; k < CW; ++k)
+                        reinterpret_cast<uint4*>(dst + hh * HB)[k] =
+                            make_uint4(row_w[hh][4 * k], row_w[hh][4 * k + 1], row_w[hh][4 * k + 2],
+                                       row_w[hh][4 * k + 3]);
             }
             // rows with a coordinate outside the table's window: exact binary
             // search over the boundaries, written over the fast path's bytes
