@@ -973,14 +973,30 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 }
             };
             uint32_t out = 0u;  // bits outside the table's cell byte: some |u| >= 0.5, or not finite
-            // The row's packed words, low and high output halves (4 CW words
-            // each), kept in registers over the chunks and written as whole
-            // 16-byte vectors: per-chunk 4-byte stores of 32 rows 128 bytes
-            // apart sent 8x the output through the L1 write path.
-            uint32_t row_w[2][4 * CW];
+            // A chunk's packed words (CW per output half) leave as one vector
+            // store per half where the width allows (16 bytes at 4 bits, 8 at 2):
+            // 4-byte stores of 32 rows 128 bytes apart sent 8x the output
+            // through the L1 write path.
+            auto store_vec = [&](int c, const uint32_t (&wl)[CW], const uint32_t (&wh)[CW]) {
+                if (!valid) return;
+                uint8_t* lo = dst + 4 * BITS * c;
+                uint8_t* hi = dst + HB + 4 * BITS * c;
+                if constexpr (CW == 4) {
+                    *reinterpret_cast<uint4*>(lo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                    *reinterpret_cast<uint4*>(hi) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                } else if constexpr (CW == 2) {
+                    *reinterpret_cast<uint2*>(lo) = make_uint2(wl[0], wl[1]);
+                    *reinterpret_cast<uint2*>(hi) = make_uint2(wh[0], wh[1]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < CW; ++k) {
+                        reinterpret_cast<uint32_t*>(lo)[k] = wl[k];
+                        reinterpret_cast<uint32_t*>(hi)[k] = wh[k];
+                    }
+                }
+            };
             auto bucket_chunk = [&](const uint32_t (&a0)[32], const uint32_t (&a1)[32], int c) {
-                uint32_t (&wl)[CW] = *reinterpret_cast<uint32_t (*)[CW]>(&row_w[0][CW * c]);
-                uint32_t (&wh)[CW] = *reinterpret_cast<uint32_t (*)[CW]>(&row_w[1][CW * c]);
+                uint32_t wl[CW], wh[CW];
 #pragma unroll
                 for (int k = 0; k < CW; ++k) wl[k] = wh[k] = 0;
 #pragma unroll
@@ -996,25 +1012,17 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     put(wl, i, e0.lo + (fmaf(ylo, inv, -e0.thr) >= 0.0f ? 1 : 0));
                     put(wh, i, e1.lo + (fmaf(yhi, inv, -e1.thr) >= 0.0f ? 1 : 0));
                 }
+                store_vec(c, wl, wh);
             };
-            // the common path unrolled (as the d = 128 epilogue): independent
-            // elements across the whole row for the scheduler to overlap
-#pragma unroll
+            // the common path rolled over the chunks (32 independent elements
+            // each): unrolled, the code outgrew the instruction cache
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t a0[32], a1[32];
                 tmem_ld32(ta + 32 * c, a0);
                 tmem_ld32(ta + 128 + 32 * c, a1);
                 tmem_wait_ld();
                 bucket_chunk(a0, a1, c);
-            }
-            if (valid) {  // HB = 16 CW bytes per half, 16-byte aligned (RB = 32 CW)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int k = 0; k < CW; ++k)
-                        reinterpret_cast<uint4*>(dst + hh * HB)[k] =
-                            make_uint4(row_w[hh][4 * k], row_w[hh][4 * k + 1], row_w[hh][4 * k + 2],
-                                       row_w[hh][4 * k + 3]);
             }
             // rows with a coordinate outside the table's window: exact binary
             // search over the boundaries, written over the fast path's bytes
