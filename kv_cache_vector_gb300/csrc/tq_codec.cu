@@ -769,6 +769,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
         if (threadIdx.x == 0) report_timeout(status, 67);
         return;
     }
+    griddep_launch();
     auto at = [&](uint32_t a) { return smem_raw + (a - sbase); };
     unsigned char* xs = at(kU2XsAt);
     unsigned char* hb = at(kU2HbAt);
@@ -836,6 +837,9 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
         tc_fence_after();
         tmem = *slot;
     }
+    // the prologue above reads the parameters only; the rows and the outputs
+    // may belong to the previous kernel in the stream
+    griddep_wait();
     const int64_t n_tiles = (n_rows + kU2Rows - 1) / kU2Rows;
 
     if (warp == 0) {  // ---- TMA producer: half h = 2 * (tile iteration) + p
@@ -1281,8 +1285,10 @@ k_decode3_256(const uint8_t* __restrict__ packed, const float* __restrict__ norm
     __shared__ float cen_s[16];
     extern __shared__ __align__(1024) unsigned char dsm[];
     unsigned char* base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+    griddep_launch();
     if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
+    griddep_wait();  // the packed rows and the output may belong to the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rr = lane >> 1, p = lane & 1;  // row of the tile, part of the row
     unsigned char* buf = base + warp * 2 * 8192;
@@ -1411,8 +1417,8 @@ cudaError_t enc_umma256(const void* x, int64_t n, uint8_t* pk, float* nm, const 
     const int64_t tiles = (n + dev::kU2Rows - 1) / dev::kU2Rows;
     int64_t grid = num_sms();
     if (grid > tiles) grid = tiles;
-    fn<<<(unsigned)grid, dev::kU2Threads, dev::kU2End, s>>>(map, n, pk, nm, status_word(), P);
-    return cudaGetLastError();
+    return dev::launch_pdl(fn, dim3((unsigned)grid), dim3(dev::kU2Threads), dev::kU2End, s, map, n, pk, nm,
+                           status_word(), P);
 }
 
 template <int D, int BITS, typename T>
@@ -1468,8 +1474,8 @@ cudaError_t dec3_256(const uint8_t* pk, const float* nm, int64_t n, void* y, con
     int64_t grid = (int64_t)num_sms() * per_sm;
     const int64_t need = (warp_tiles + dev::kDec3bWarps - 1) / dev::kDec3bWarps;
     if (grid > need) grid = need;
-    fn<<<(unsigned)grid, 32 * dev::kDec3bWarps, dev::kDec3bSmem, s>>>(pk, nm, n, map, P);
-    return cudaGetLastError();
+    return dev::launch_pdl(fn, dim3((unsigned)grid), dim3(32 * dev::kDec3bWarps), dev::kDec3bSmem, s, pk, nm, n, map,
+                           P);
 }
 
 template <int D, int BITS, typename TO>
