@@ -506,6 +506,7 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
         if (threadIdx.x == 0) report_timeout(status, 17);
         return;
     }
+    griddep_launch();
     auto at = [&](uint32_t a) { return smem_raw + (a - sbase); };
     unsigned char* xs = at(kUmXsAt);                            // stages of X
     unsigned char* hb = at(kUmHbAt);                            // D H, K-major
@@ -556,6 +557,9 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *slot;
+    // the prologue above reads the parameters only; the rows and the outputs
+    // may belong to the previous kernel in the stream
+    griddep_wait();
     const int64_t n_tiles = (n_rows + kUmRows - 1) / kUmRows;
 
     if (warp == 0) {  // ---- TMA producer
@@ -1204,8 +1208,10 @@ k_decode3(const uint8_t* __restrict__ packed, const float* __restrict__ norms, i
     __shared__ float cen_s[16];
     extern __shared__ __align__(1024) unsigned char dsm[];
     unsigned char* base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
+    griddep_launch();
     if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
+    griddep_wait();  // the packed rows and the output may belong to the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* buf = base + warp * 2 * 8192;
     const int64_t n_tiles = (n_rows + 31) / 32;
@@ -1401,8 +1407,8 @@ cudaError_t enc_umma(const void* x, int64_t n, uint8_t* pk, float* nm, const Row
     const int64_t tiles = (n + dev::kUmRows - 1) / dev::kUmRows;
     int64_t grid = num_sms();
     if (grid > tiles) grid = tiles;
-    fn<<<(unsigned)grid, dev::kUmThreads, dev::kUmEnd, s>>>(map, n, pk, nm, status_word(), P);
-    return cudaGetLastError();
+    return dev::launch_pdl(fn, dim3((unsigned)grid), dim3(dev::kUmThreads), dev::kUmEnd, s, map, n, pk, nm,
+                           status_word(), P);
 }
 
 template <int BITS>
@@ -1457,8 +1463,8 @@ cudaError_t dec3(const uint8_t* pk, const float* nm, int64_t n, void* y, const R
     int64_t grid = (int64_t)num_sms() * per_sm;
     const int64_t need = (warp_tiles + dev::kDec3Warps - 1) / dev::kDec3Warps;
     if (grid > need) grid = need;
-    fn<<<(unsigned)grid, 32 * dev::kDec3Warps, dev::kDec3Smem, s>>>(pk, nm, n, map, P);
-    return cudaGetLastError();
+    return dev::launch_pdl(fn, dim3((unsigned)grid), dim3(32 * dev::kDec3Warps), dev::kDec3Smem, s, pk, nm, n, map,
+                           P);
 }
 
 template <int BITS>
