@@ -611,7 +611,16 @@ tq_status tq_decode_qjl(const tq_plan* plan, int bits, const float* S, const uin
 
 size_t tq_attn_qjl_workspace_bytes(int B, int Hq, int Hkv, int d, int64_t ctx_len) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || ctx_len < 1 || !qjl_d(d)) return 0;
-    return tq::attn_qjl_workspace_bytes(B, Hq, d, tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms()));
+    size_t most = tq::attn_qjl_workspace_bytes(B, Hq, d, tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms()));
+    if (d == 128 && Hq / Hkv <= 8) {  // 3- and 4-bit keys: the tensor-core kernel
+        for (int kb = 3; kb <= 4; ++kb)
+            for (int vb = 2; vb <= 4; ++vb) {
+                const size_t w = tq::attn_qjl128_workspace_bytes(
+                    B, Hq, tq::attn_qjl128_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), kb, vb));
+                if (w > most) most = w;
+            }
+    }
+    return most;
 }
 
 tq_status tq_attn_decode_qjl(const tq_plan* plan, const float* S, const void* q, int B, int Hq, int Hkv,
@@ -628,12 +637,27 @@ tq_status tq_attn_decode_qjl(const tq_plan* plan, const float* S, const void* q,
     if (!S || !k_rnorm) return TQ_ERR_INVALID_ARG;
     if (!aligned16(S) || !aligned4(k_rnorm)) return TQ_ERR_ALIGNMENT;
     if (!device_accessible(S) || !device_accessible(k_rnorm)) return TQ_ERR_INVALID_ARG;
-    const tq::AttnGeometry g = tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms());
-    if (!workspace || workspace_bytes < tq::attn_qjl_workspace_bytes(B, Hq, P->d, g)) return TQ_ERR_WORKSPACE;
+    // 3- and 4-bit keys at d = 128 run on the tensor cores, the rest on the CUDA cores
+    const bool tc = P->d == 128 && k_bits >= 3;
+    const tq::AttnGeometry g = tc ? tq::attn_qjl128_geometry(B, Hq, Hkv, ctx_len, tq::num_sms(), k_bits, v_bits)
+                                  : tq::attn_qjl_geometry(B, Hq, Hkv, ctx_len, tq::num_sms());
+    const size_t need = tc ? tq::attn_qjl128_workspace_bytes(B, Hq, g) : tq::attn_qjl_workspace_bytes(B, Hq, P->d, g);
+    if (!workspace || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TQ_ERR_ALIGNMENT;
     if (!device_accessible(workspace)) return TQ_ERR_INVALID_ARG;
     tq::AttnParams A;
     tq::fill_attn_params(*P, k_bits - 1, v_bits, scale, 0.0f, A);
+    if (tc) {
+        // q' = scale log2(e) sqrt(pi/2) / (d sqrt(d)) S y, y the unnormalised rotated query
+        const float proj_mul = (float)((double)scale * 1.4426950408889634 * 1.2533141373155003 / (128.0 * std::sqrt(128.0)));
+        const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+        const cudaError_t e3 =
+            k_bits == 3 ? tq::launch_attn3_qjl<3>(v_bits, q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, A,
+                                                  proj_mul, s)
+                        : tq::launch_attn3_qjl<4>(v_bits, q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, A,
+                                                  proj_mul, s);
+        return e3 == cudaSuccess ? TQ_OK : cuda_fail(e3);
+    }
     cudaError_t e = dispatch_qjl_d(P->d, [&](auto D) {
         constexpr int d = decltype(D)::value;
         const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -77,32 +77,38 @@ constexpr int kA3StatusAppend = 42;  // an appended row's position or page is ou
 // Warps, ring stages and the shared-memory plan per CTA (attn3_plan): up to
 // 16 warps x 2 stages for up to four query heads per KV head, 8 x 3 for up to
 // eight.
-template <int KB, int VB, int NG, bool SP = false>
+// QJL: keys in the QJL residual format, KB bits in total (a KB - 1 bit index
+// per coordinate, then the 128 sign bits of the projected residual).
+template <int KB, int VB, int NG, bool SP = false, bool QJL = false>
 struct A3Shape {
-    static constexpr Attn3Plan kPlan = attn3_plan(4 * NG, KB, VB, SP);
+    static constexpr Attn3Plan kPlan = attn3_plan(4 * NG, KB, VB, SP, QJL);
     static constexpr int kWarps = kPlan.warps;
     static constexpr int kStages = kPlan.stages;
     static constexpr int kThreads = 32 * kWarps;
     static_assert(kWarps > 0, "no shared-memory plan");
 };
 
-template <int KB, int VB, int NG, bool SP = false>
+template <int KB, int VB, int NG, bool SP = false, bool QJL = false>
 struct A3Layout {
-    static constexpr Attn3Plan kPlan = A3Shape<KB, VB, NG, SP>::kPlan;
+    static_assert(!(SP && QJL), "QJL keys run dense");
+    static constexpr Attn3Plan kPlan = A3Shape<KB, VB, NG, SP, QJL>::kPlan;
     static constexpr int kWarps = kPlan.warps, kStages = kPlan.stages;
+    static constexpr int kMB = QJL ? KB - 1 : KB;            // index bits per key coordinate
+    static constexpr int kSignOff = 16 * kMB;                 // QJL: the sign words of a key row
     static constexpr int kKRow = 16 * KB, kVRow = 16 * VB;  // bytes of a d = 128 row
     static constexpr int kVOff = kA3Chunk * kKRow;  // V rows in the stage (not SP)
     static constexpr int kKnOff = kA3Chunk * (kKRow + (SP ? 0 : kVRow));
     static constexpr int kVnOff = kKnOff + 4 * kA3Chunk;
-    static constexpr int kStage = kVnOff + 4 * kA3Chunk;
+    static constexpr int kGnOff = kVnOff + 4 * kA3Chunk;      // QJL: the keys' gammas
+    static constexpr int kStage = (QJL ? kGnOff : kVnOff) + 4 * kA3Chunk;
     static constexpr int kVBuf = kA3Chunk * kVRow;  // SP: one chunk's V rows; two per warp after its stages
     static constexpr int kWarpRing = kPlan.stages * kStage + (SP ? 2 * kVBuf : 0);
-    static_assert(kWarpRing == attn3_warp_ring_bytes(KB, VB, kPlan.stages, SP), "ring size");
+    static_assert(kWarpRing == attn3_warp_ring_bytes(KB, VB, kPlan.stages, SP, QJL), "ring size");
     static constexpr int kEntries = 256;  // rows of the pair table (one byte of index)
     static constexpr int kHeads = 4 * NG;
     // keys that carry their rest: 8-byte key entries (high and low fp16
     // pairs), 16 columns shared by lanes l and l + 16
-    static constexpr bool kRest = attn3_key_rest(KB);
+    static constexpr bool kRest = attn3_key_rest(kMB);
     static constexpr int kMergeHeads = kPlan.merge_heads;
     static constexpr uint32_t kMergeAt = (uint32_t)kPlan.merge;
     static constexpr uint32_t kBarAt = (uint32_t)kPlan.bars;
@@ -377,6 +383,11 @@ struct A3Meta {
     int32_t* c0;
     int32_t* clast;
     uint32_t* gmax;  // sparse V: largest score per (batch, query head) so far, zeroed by the query rotation
+    // QJL keys: the projected queries (fp16 high and low parts, [B Hq][2][128])
+    // and their powers of two, and the keys' gammas [B][Hkv][cap]
+    const __half* qp16;
+    const float* qpexp;
+    const float* k_rnorm;
 };
 // Weights of the work partition, in rows of the busiest warp: an item that
 // holds rows costs its busiest warp's rows plus kA3ItemCost, an empty item
@@ -538,15 +549,17 @@ static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __res
 // scores, when some query head keeps one of its rows ("CITATIONS", Sparse V
 // dequant), and their product is taken one chunk later, with the chunk's
 // weights rescaled if the running maximum moves in between.
-template <int KB, int VB, int NG, bool PAGED, bool SP>
-__global__ void __launch_bounds__(A3Shape<KB, VB, NG, SP>::kThreads, 1)
+template <int KB, int VB, int NG, bool PAGED, bool SP, bool QJL = false>
+__global__ void __launch_bounds__(A3Shape<KB, VB, NG, SP, QJL>::kThreads, 1)
 k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, int Hq, int Hkv,
               tq_cache_view cache, int64_t ctx_len, int warp_len, int n_splits, int64_t n_items,
               float* __restrict__ part, int* status, const __grid_constant__ AttnParams P,
               const PagedArgs pa, const A3Meta meta) {
     static_assert(!(SP && PAGED), "sparse-V copies are for the contiguous cache");
-    using L = A3Layout<KB, VB, NG, SP>;
-    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG, SP>::kThreads;
+    static_assert(!(QJL && PAGED), "QJL keys: contiguous cache");
+    using L = A3Layout<KB, VB, NG, SP, QJL>;
+    constexpr int W = L::kWarps, S = L::kStages, T = A3Shape<KB, VB, NG, SP, QJL>::kThreads;
+    constexpr int MB = L::kMB;  // index bits of a key coordinate
     constexpr uint32_t kAll = 0xFFFFFFFFu;
     extern __shared__ __align__(16) unsigned char a3_smem[];
     griddep_launch();  // the combine may be scheduled; it waits for this grid
@@ -559,16 +572,16 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 
     // ---- pair tables and the per-warp barriers
     {
-        constexpr int MK = (1 << KB) - 1, MV = (1 << VB) - 1;
+        constexpr int MK = (1 << MB) - 1, MV = (1 << VB) - 1;
         for (int i = threadIdx.x; i < L::kEntries * 64; i += T) {
             const int e = i >> 6, s = i & 63;  // row e holds the pair e mod 2^(2 bits)
             uint32_t v;
             if (s >= 32)
                 v = h2u(P.vcen_h[e & MV], P.vcen_h[(e >> VB) & MV]);
             else if (L::kRest && (s & 1))  // words 2c, 2c + 1 of column c: high and low key parts
-                v = h2u(P.kcen_l[e & MK], P.kcen_l[(e >> KB) & MK]);
+                v = h2u(P.kcen_l[e & MK], P.kcen_l[(e >> MB) & MK]);
             else
-                v = h2u(P.kcen_h[e & MK], P.kcen_h[(e >> KB) & MK]);
+                v = h2u(P.kcen_h[e & MK], P.kcen_h[(e >> MB) & MK]);
             *reinterpret_cast<uint32_t*>(gptr(kA3TableAt + 256u * e + 4u * s)) = v;
         }
     }
@@ -687,6 +700,7 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             const uint32_t slot = 4u * (4u * (lane & 7) + (lane >> 3));
             cp_async4(sb + L::kKnOff + slot, cache.k_norm + r, sz);
             cp_async4(sb + L::kVnOff + slot, cache.v_norm + r, sz);
+            if constexpr (QJL) cp_async4(sb + L::kGnOff + slot, meta.k_rnorm + r, sz);
             cp_async_arrive(bar);
         } else {
             mbar_arrive(bar);  // a bad page: nothing is copied, the chunk's result is undefined
@@ -708,6 +722,9 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
     float O[NG][8][4];
     float m_run[NG], l_run[NG], qx[NG];
     uint32_t qb[NG][8][2];
+    // QJL: the projected query's B fragments and powers of two
+    uint32_t qpb[QJL ? NG : 1][QJL ? 8 : 1][2];
+    float qpx[QJL ? NG : 1];
     bool hok[NG];
     int vexp = 0;  // the V accumulators are in units of 2^vexp
     float vlim = 128.f, vsc = 1.f;
@@ -749,36 +766,58 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         }
         // ---- scores, one 16-position sub-tile at a time (fewer live registers)
         float sacc[2][NG][4];
+        float ssg[QJL ? 2 : 1][QJL ? NG : 1][4];  // QJL: the sign part, its own accumulators
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            uint32_t kw[2][KB];
+            uint32_t kw[2][MB];
 #pragma unroll
             for (int hg = 0; hg < NG; ++hg) sacc[u][hg][0] = sacc[u][hg][1] = sacc[u][hg][2] = sacc[u][hg][3] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                load_kfield<KB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * KB * t), kw[h]);
+                load_kfield<MB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * MB * t), kw[h]);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 if constexpr (L::kRest) {
                     // S = (K_hi + K_lo) (Q_hi + Q_lo): the keys' fp16 rests as a
                     // second MMA into the same accumulators
-                    const uint2 a0 = lds_tab2(pair_addr<KB>(kw[0], 2 * kk, kslot));
-                    const uint2 a2 = lds_tab2(pair_addr<KB>(kw[0], 2 * kk + 1, kslot));
-                    const uint2 a1 = lds_tab2(pair_addr<KB>(kw[1], 2 * kk, kslot));
-                    const uint2 a3 = lds_tab2(pair_addr<KB>(kw[1], 2 * kk + 1, kslot));
+                    const uint2 a0 = lds_tab2(pair_addr<MB>(kw[0], 2 * kk, kslot));
+                    const uint2 a2 = lds_tab2(pair_addr<MB>(kw[0], 2 * kk + 1, kslot));
+                    const uint2 a1 = lds_tab2(pair_addr<MB>(kw[1], 2 * kk, kslot));
+                    const uint2 a3 = lds_tab2(pair_addr<MB>(kw[1], 2 * kk + 1, kslot));
 #pragma unroll
                     for (int hg = 0; hg < NG; ++hg) {
                         mma16816(sacc[u][hg], a0.x, a1.x, a2.x, a3.x, qb[hg][kk][0], qb[hg][kk][1]);
                         mma16816(sacc[u][hg], a0.y, a1.y, a2.y, a3.y, qb[hg][kk][0], qb[hg][kk][1]);
                     }
                 } else {
-                    const uint32_t a0 = lds_tab(pair_addr<KB>(kw[0], 2 * kk, kslot));
-                    const uint32_t a2 = lds_tab(pair_addr<KB>(kw[0], 2 * kk + 1, kslot));
-                    const uint32_t a1 = lds_tab(pair_addr<KB>(kw[1], 2 * kk, kslot));
-                    const uint32_t a3 = lds_tab(pair_addr<KB>(kw[1], 2 * kk + 1, kslot));
+                    const uint32_t a0 = lds_tab(pair_addr<MB>(kw[0], 2 * kk, kslot));
+                    const uint32_t a2 = lds_tab(pair_addr<MB>(kw[0], 2 * kk + 1, kslot));
+                    const uint32_t a1 = lds_tab(pair_addr<MB>(kw[1], 2 * kk, kslot));
+                    const uint32_t a3 = lds_tab(pair_addr<MB>(kw[1], 2 * kk + 1, kslot));
 #pragma unroll
                     for (int hg = 0; hg < NG; ++hg)
                         mma16816(sacc[u][hg], a0, a1, a2, a3, qb[hg][kk][0], qb[hg][kk][1]);
+                }
+            }
+            if constexpr (QJL) {
+                // <q', sgn>: A = +-1 from the sign bits (bit set: +1).  Lane t
+                // reads sign word t of its rows (projections 32t .. 32t + 31), in
+                // the k-slot order of the index dims above, so B is the projected
+                // query's fragments laid out as the query's.
+                uint32_t sw[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    sw[h] = lds_u32(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + L::kSignOff + 4 * t));
+#pragma unroll
+                for (int hg = 0; hg < NG; ++hg) ssg[u][hg][0] = ssg[u][hg][1] = ssg[u][hg][2] = ssg[u][hg][3] = 0.f;
+                auto pm1 = [](uint32_t x) { return 0xBC00BC00u ^ ((x & 1u) << 15) ^ ((x & 2u) << 30); };
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a0 = pm1(sw[0] >> (4 * kk)), a2 = pm1(sw[0] >> (4 * kk + 2));
+                    const uint32_t a1 = pm1(sw[1] >> (4 * kk)), a3 = pm1(sw[1] >> (4 * kk + 2));
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg)
+                        mma16816(ssg[u][hg], a0, a1, a2, a3, qpb[hg][kk][0], qpb[hg][kk][1]);
                 }
             }
         }
@@ -788,6 +827,14 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
         float nvl = 0.f;
         const uint4 kn4 = lds_v4(sb + L::kKnOff + 16u * g), vn4 = lds_v4(sb + L::kVnOff + 16u * g);
         const uint32_t knw[4] = {kn4.x, kn4.y, kn4.z, kn4.w}, vnw[4] = {vn4.x, vn4.y, vn4.z, vn4.w};
+        uint32_t gnw[4] = {0u, 0u, 0u, 0u};  // QJL: the keys' gammas, the same slots
+        if constexpr (QJL) {
+            const uint4 gn4 = lds_v4(sb + L::kGnOff + 16u * g);
+            gnw[0] = gn4.x;
+            gnw[1] = gn4.y;
+            gnw[2] = gn4.z;
+            gnw[3] = gn4.w;
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -800,7 +847,10 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
                 else if (ok[u][h]) nvl = fmaxf(nvl, vn[u][h]);
 #pragma unroll
                 for (int hg = 0; hg < NG; ++hg) {
-                    const float v = (sacc[u][hg][2 * h] + sacc[u][hg][2 * h + 1]) * (kn * qx[hg]);
+                    float v = (sacc[u][hg][2 * h] + sacc[u][hg][2 * h + 1]) * (kn * qx[hg]);
+                    if constexpr (QJL)
+                        v = fmaf(ssg[u][hg][2 * h] + ssg[u][hg][2 * h + 1],
+                                 __uint_as_float(gnw[2 * u + h]) * qpx[hg], v);
                     sc[hg][u][h] = ok[u][h] ? v : -INFINITY;
                 }
             }
@@ -1082,8 +1132,26 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) qb[hg][kk][0] = qb[hg][kk][1] = 0u;
                 }
+                if constexpr (QJL) {  // the same fragment layout over the projections
+                    if (hc < G) {
+                        const uint4* qpp = reinterpret_cast<const uint4*>(
+                            meta.qp16 + ((b * Hq + gh * G + hc) * 2 + (g & 1)) * 128 + 32 * t);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 u = __ldg(qpp + i);
+                            qpb[hg][2 * i][0] = u.x;
+                            qpb[hg][2 * i][1] = u.y;
+                            qpb[hg][2 * i + 1][0] = u.z;
+                            qpb[hg][2 * i + 1][1] = u.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) qpb[hg][kk][0] = qpb[hg][kk][1] = 0u;
+                    }
+                }
                 hok[hg] = 4 * hg + t < G;
                 qx[hg] = hok[hg] ? __ldg(qexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
+                if constexpr (QJL) qpx[hg] = hok[hg] ? __ldg(meta.qpexp + b * Hq + gh * G + 4 * hg + t) : 0.f;
                 if constexpr (SP) {
                     m_ref[hg] = -INFINITY;
                     gslot[hg] = meta.gmax + (b * Hq + gh * G + (hok[hg] ? 4 * hg + t : 0));
@@ -1283,13 +1351,13 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
     reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }
 
-template <int KB, int VB, int NG, bool PAGED, bool SP>
+template <int KB, int VB, int NG, bool PAGED, bool SP, bool QJL = false>
 cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int Hkv,
                                const tq_cache_view& cache, int64_t ctx_len, const AttnGeometry& geo,
                                int64_t items, int grid, float* part, const AttnParams& P,
                                const PagedArgs& pa, const A3Meta& meta, cudaStream_t s) {
-    using L = A3Layout<KB, VB, NG, SP>;
-    auto fn = k_attn3_split<KB, VB, NG, PAGED, SP>;
+    using L = A3Layout<KB, VB, NG, SP, QJL>;
+    auto fn = k_attn3_split<KB, VB, NG, PAGED, SP, QJL>;
     // The kernel addresses shared memory from window address 0, so it asks
     // for kEnd bytes (the dynamic block starts at or below kA3RingAt).
     static int attr_done[64] = {};
@@ -1301,7 +1369,7 @@ cudaError_t attn3_split_launch(const __half* q16, const float* qexp, int Hq, int
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = 1;
     }
-    return launch_pdl(fn, dim3((unsigned)grid), dim3(A3Shape<KB, VB, NG, SP>::kThreads), L::kEnd, s, q16, qexp, Hq,
+    return launch_pdl(fn, dim3((unsigned)grid), dim3(A3Shape<KB, VB, NG, SP, QJL>::kThreads), L::kEnd, s, q16, qexp, Hq,
                       Hkv, cache, ctx_len, geo.warp_len, geo.n_splits, items, part, status_word(), P, pa, meta);
 }
 
@@ -1314,7 +1382,7 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
     float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * Hq * 512);
     float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + attn3_prefix_bytes(B, Hq));
     const int sms = num_sms();
-    A3Meta meta;
+    A3Meta meta{};
     meta.cta_begin = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(part) + attn3_partial_bytes(B, Hq, geo.n_splits));
     meta.slot_base = meta.cta_begin + (sms + 1);
     meta.c0 = meta.slot_base + (sms + 1);
@@ -1382,6 +1450,96 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
                       grid, items, Hq, Hkv, (int64_t)B * Hq, out, P, PAGED, meta);
 }
 
+// QJL keys: the projected query of one (batch, query head) for the sign
+// part of the scores.  y = s2 . H (s . q) (unnormalised, as k_attn3_q), then
+// q' = proj_mul * S y with proj_mul = scale * log2(e) * sqrt(pi/2) / (d sqrt(d)),
+// so that gamma <q', sgn> is the sign part of the score in log2 units, as
+// fp16 high and low parts of q' / 2^e (|q' / 2^e| < 2^14) at qp16[bh][2][128]
+// in projection order, and 2^e at qpexp[bh].  One block of 128 threads per
+// head; thread k forms projection k from row k of S.
+static __global__ void __launch_bounds__(128) k_attn3_qjl_q(const __nv_bfloat16* __restrict__ q,
+                                                            const float* __restrict__ S, __half* __restrict__ qp16,
+                                                            float* __restrict__ qpexp,
+                                                            const __grid_constant__ AttnParams P, float proj_mul) {
+    __shared__ float v[128];
+    __shared__ float wmax[4];
+    griddep_launch();
+    const int bh = blockIdx.x, j = threadIdx.x;
+    const float x = __bfloat162float(q[(int64_t)bh * 128 + j]);
+    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
+    fwht_smem<128>(v, 1);
+    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u));
+    __syncthreads();
+    v[j] = y;
+    __syncthreads();
+    float p = 0.f;
+    const float* row = S + (int64_t)j * 128;
+#pragma unroll 8
+    for (int i = 0; i < 128; ++i) p = fmaf(__ldg(row + i), v[i], p);
+    p *= proj_mul;
+    float M = fabsf(p);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    if ((j & 31) == 0) wmax[j >> 5] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    int e = 0;
+    if (M > 0.f && M <= FLT_MAX) {
+        int ex = 0;
+        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
+        e = min(100, max(-100, ex - 14));
+    }
+    const float ps = ldexpf(p, -e);
+    const __half hi = __float2half_rn(ps);
+    const __half lo = __float2half_rn(ps - __half2float(hi));
+    qp16[(int64_t)bh * 256 + j] = hi;
+    qp16[(int64_t)bh * 256 + 128 + j] = lo;
+    if (j == 0) qpexp[bh] = ldexpf(1.f, e);
+}
+
+// QJL keys (KB bits in total, contiguous cache): the query rotation, the
+// projected query, the split kernel with the QJL scores, the combine.  The
+// workspace is the d = 128 layout with the projected queries' prefix after
+// the rotated queries'.
+template <int KB, int VB>
+cudaError_t attn3_qjl_launch(const void* q, const float* S, int B, int Hq, int Hkv, const tq_cache_view& cache,
+                             const float* k_rnorm, int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
+                             const AttnParams& P, float proj_mul, cudaStream_t s) {
+    __half* q16 = static_cast<__half*>(ws);
+    float* qexp = reinterpret_cast<float*>(static_cast<char*>(ws) + (size_t)B * Hq * 512);
+    char* pre2 = static_cast<char*>(ws) + attn3_prefix_bytes(B, Hq);
+    __half* qp16 = reinterpret_cast<__half*>(pre2);
+    float* qpexp = reinterpret_cast<float*>(pre2 + (size_t)B * Hq * 512);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + 2 * attn3_prefix_bytes(B, Hq));
+    const int sms = num_sms();
+    A3Meta meta{};
+    meta.cta_begin = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(part) + attn3_partial_bytes(B, Hq, geo.n_splits));
+    meta.slot_base = meta.cta_begin + (sms + 1);
+    meta.c0 = meta.slot_base + (sms + 1);
+    meta.clast = meta.c0 + (size_t)B * Hq;
+    meta.gmax = nullptr;
+    meta.qp16 = qp16;
+    meta.qpexp = qpexp;
+    meta.k_rnorm = k_rnorm;
+    const auto qb = static_cast<const __nv_bfloat16*>(q);
+    k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(qb, q16, qexp, P, (int64_t)B * Hq, nullptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_attn3_qjl_q<<<(unsigned)(B * Hq), 128, 0, s>>>(qb, S, qp16, qpexp, P, proj_mul);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)B * Hkv * geo.n_splits;
+    const int grid = (int)(items < sms ? items : sms);  // one CTA per SM
+    if (Hq / Hkv <= 4)
+        e = attn3_split_launch<KB, VB, 1, false, false, true>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid,
+                                                              part, P, PagedArgs{}, meta, s);
+    else
+        e = attn3_split_launch<KB, VB, 2, false, false, true>(q16, qexp, Hq, Hkv, cache, ctx_len, geo, items, grid,
+                                                              part, P, PagedArgs{}, meta, s);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_attn3_combine, dim3((unsigned)(B * Hq)), dim3(128), 0, s, (const float*)part, geo.n_splits,
+                      grid, items, Hq, Hkv, (int64_t)B * Hq, out, P, false, meta);
+}
+
 }  // namespace dev
 
 #if !defined(TQ_UNIT_D) || !defined(TQ_UNIT_KB) || TQ_UNIT_D != 128
@@ -1414,6 +1572,23 @@ cudaError_t launch_attn128_paged(int v_bits, const void* q, int B, int Hq, int H
         default: return dev::attn3_launch<KB, 4, true>(q, B, Hq, Hkv, pages, max_ctx, out, workspace, g, P, s, pa, app);
     }
 }
+#if TQ_UNIT_KB >= 3
+// QJL keys of TQ_UNIT_KB bits in total (a TQ_UNIT_KB - 1 bit index).
+template <int KB>
+cudaError_t launch_attn3_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
+                             const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
+                             void* workspace, const AttnGeometry& g, const AttnParams& P, float proj_mul,
+                             cudaStream_t s) {
+    switch (v_bits) {
+        case 2: return dev::attn3_qjl_launch<KB, 2>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, proj_mul, s);
+        case 3: return dev::attn3_qjl_launch<KB, 3>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, proj_mul, s);
+        default: return dev::attn3_qjl_launch<KB, 4>(q, S, B, Hq, Hkv, cache, k_rnorm, ctx_len, out, workspace, g, P, proj_mul, s);
+    }
+}
+template cudaError_t launch_attn3_qjl<TQ_UNIT_KB>(int, const void*, const float*, int, int, int, const tq_cache_view&,
+                                                  const float*, int64_t, float*, void*, const AttnGeometry&,
+                                                  const AttnParams&, float, cudaStream_t);
+#endif
 template cudaError_t launch_attn128_paged<TQ_UNIT_KB>(int, const void*, int, int, int, const tq_cache_view&,
                                                       int64_t, float*, void*, const AttnGeometry&,
                                                       const AttnParams&, const PagedArgs&, cudaStream_t,

@@ -127,6 +127,11 @@ cudaError_t launch_decode_qjl_d(int bits, tq_dtype dt, const uint8_t* packed, co
                                 const float* rnorms, int64_t n_rows, const float* S, void* y, const RowParams& P,
                                 cudaStream_t s);
 struct AttnGeometry;
+template <int KB>
+cudaError_t launch_attn3_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
+                             const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
+                             void* workspace, const AttnGeometry& g, const AttnParams& P, float proj_mul,
+                             cudaStream_t s);
 template <int D, int KB>
 cudaError_t launch_attn_qjl(int v_bits, const void* q, const float* S, int B, int Hq, int Hkv,
                             const tq_cache_view& cache, const float* k_rnorm, int64_t ctx_len, float* out,
@@ -167,10 +172,12 @@ constexpr int kAttn3MergeRow = 132 * 4;  // bytes per (warp, head) row of the me
 #ifndef TQ_ATTN3_REST_MIN_BITS
 #define TQ_ATTN3_REST_MIN_BITS 3
 #endif
-constexpr int attn3_stage_bytes(int kb, int vb) { return 32 * (16 * kb + 16 * vb + 8); }
+// QJL keys (qjl): kb is the row's total width and a stage also holds each
+// position's gamma (4 more bytes per position).
+constexpr int attn3_stage_bytes(int kb, int vb, bool qjl = false) { return 32 * (16 * kb + 16 * vb + (qjl ? 12 : 8)); }
 // Ring bytes of one warp: its stages, and with sparse V its two V buffers.
-constexpr int attn3_warp_ring_bytes(int kb, int vb, int stages, bool sparse) {
-    return sparse ? stages * 32 * (16 * kb + 8) + 2 * 32 * 16 * vb : stages * attn3_stage_bytes(kb, vb);
+constexpr int attn3_warp_ring_bytes(int kb, int vb, int stages, bool sparse, bool qjl = false) {
+    return sparse ? stages * 32 * (16 * kb + 8) + 2 * 32 * 16 * vb : stages * attn3_stage_bytes(kb, vb, qjl);
 }
 constexpr bool attn3_key_rest(int kb) { return kb >= TQ_ATTN3_REST_MIN_BITS; }
 
@@ -181,12 +188,16 @@ struct Attn3Plan {
     int end;    // bytes of dynamic shared memory to ask for
 };
 
-constexpr Attn3Plan attn3_plan(int G, int kb, int vb, bool sparse = false) {
+// The QJL-key kernel carries the projected query and a second set of score
+// accumulators: at most 12 warps (170 registers per thread).
+constexpr int kAttn3QjlWarpCap = 12;
+
+constexpr Attn3Plan attn3_plan(int G, int kb, int vb, bool sparse = false, bool qjl = false) {
     const int heads = G <= 4 ? 4 : 8;
     const int stages = G <= 4 ? 2 : 3;
     const int high = kAttn3TableAt + 65536;  // first byte above the table
-    for (int w = (G <= 4 ? TQ_ATTN3_WARP_CAP : 8); w >= 1; --w) {
-        const int ring_end = kAttn3RingAt + w * attn3_warp_ring_bytes(kb, vb, stages, sparse);
+    for (int w = (G <= 4 ? (qjl ? kAttn3QjlWarpCap : TQ_ATTN3_WARP_CAP) : 8); w >= 1; --w) {
+        const int ring_end = kAttn3RingAt + w * attn3_warp_ring_bytes(kb, vb, stages, sparse, qjl);
         if (ring_end > kAttn3TableAt) continue;
         const int bars_bytes = 8 * w * (stages + (sparse ? 2 : 0));
         for (int mh = heads; mh >= 1; mh /= 2) {
@@ -198,7 +209,9 @@ constexpr Attn3Plan attn3_plan(int G, int kb, int vb, bool sparse = false) {
     }
     return Attn3Plan{0, 0, 0, 0, 0, 0};
 }
-constexpr int attn3_warps(int G, int kb, int vb, bool sparse = false) { return attn3_plan(G, kb, vb, sparse).warps; }
+constexpr int attn3_warps(int G, int kb, int vb, bool sparse = false, bool qjl = false) {
+    return attn3_plan(G, kb, vb, sparse, qjl).warps;
+}
 
 struct AttnGeometry {
     int n_splits;
@@ -223,6 +236,11 @@ size_t attn_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
 // its workspace (query prefix and partials).
 AttnGeometry attn_qjl_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms);
 size_t attn_qjl_workspace_bytes(int B, int Hq, int d, const AttnGeometry& g);
+// QJL keys of 3 and 4 bits at d = 128: the tensor-core kernel.  Its workspace
+// is the d = 128 layout with a second query prefix (the projected query,
+// fp16 high and low parts, and its powers of two) after the first.
+AttnGeometry attn_qjl128_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int num_sms, int kb, int vb);
+size_t attn_qjl128_workspace_bytes(int B, int Hq, const AttnGeometry& g);
 // d = 128: rotated queries (fp16 high and low parts, 512 bytes per head) and
 // their power-of-two scales (4 bytes per head), rounded up to 256 bytes.
 // d = 128, paged attention: the work partition written by the planning

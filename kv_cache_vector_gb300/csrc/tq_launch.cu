@@ -62,41 +62,54 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
     return (unsigned)(want < 1 ? 1 : want);
 }
 
+namespace {
+// d = 128: the longest per-warp range (256 down to 32 positions) whose work
+// items fill the last wave of one-CTA-per-SM grids to at least 90%, else the
+// one that fills it best; W warps per CTA.
+AttnGeometry attn3_geometry(int64_t pairs, int64_t ctx_len, int sms, int W) {
+    AttnGeometry g;
+    const int64_t cap = sms > 0 ? sms : 1;
+    int best = 256;
+    double best_eff = -1.0;
+    for (int wl = 256; wl >= 32; wl /= 2) {
+        const int64_t seg = (int64_t)W * wl;
+        const int64_t items = pairs * ((ctx_len + seg - 1) / seg);
+        const int64_t grid = items < cap ? (items > 0 ? items : 1) : cap;
+        const int64_t rounds = (items + grid - 1) / grid;
+        const double eff = rounds > 0 ? (double)items / (double)(rounds * grid) : 1.0;
+        if (eff >= 0.9) {
+            best = wl;
+            break;
+        }
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = wl;
+        }
+    }
+    g.warp_len = best;
+    g.split_len = W * best;
+    g.n_splits = (int)((ctx_len + g.split_len - 1) / g.split_len);
+    g.parts = 1;
+    g.q16 = true;
+    return g;
+}
+}  // namespace
+
+AttnGeometry attn_qjl128_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int kb, int vb) {
+    return attn3_geometry((int64_t)B * Hkv, ctx_len, sms, attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb, false, true));
+}
+
+size_t attn_qjl128_workspace_bytes(int B, int Hq, const AttnGeometry& g) {
+    return 2 * attn3_prefix_bytes(B, Hq) + attn3_partial_bytes(B, Hq, g.n_splits) + attn3_meta_bytes(B, Hq, num_sms());
+}
+
 // Split-K geometry of the decode attention.  d = 128 (tensor-core kernel,
-// one CTA of attn3_warps(G, kb, vb) warps per SM): the longest per-warp range
-// (256 down to 32 positions) whose work items fill the last wave of CTAs to
-// at least 90%, else the one that fills it best.  Otherwise the longest split
-// (<= 512 positions) that still gives two CTAs per SM.
+// one CTA of attn3_warps(G, kb, vb) warps per SM): attn3_geometry.  Otherwise
+// the longest split (<= 512 positions) that still gives two CTAs per SM.
 AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int d, int kb, int vb, bool sparse) {
     AttnGeometry g;
     const int64_t pairs = (int64_t)B * Hkv;
-    if (d == 128) {
-        const int64_t cap = sms > 0 ? sms : 1;
-        const int W = attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb, sparse);
-        int best = 256;
-        double best_eff = -1.0;
-        for (int wl = 256; wl >= 32; wl /= 2) {
-            const int64_t seg = (int64_t)W * wl;
-            const int64_t items = pairs * ((ctx_len + seg - 1) / seg);
-            const int64_t grid = items < cap ? (items > 0 ? items : 1) : cap;
-            const int64_t rounds = (items + grid - 1) / grid;
-            const double eff = rounds > 0 ? (double)items / (double)(rounds * grid) : 1.0;
-            if (eff >= 0.9) {
-                best = wl;
-                break;
-            }
-            if (eff > best_eff + 1e-9) {
-                best_eff = eff;
-                best = wl;
-            }
-        }
-        g.warp_len = best;
-        g.split_len = W * best;
-        g.n_splits = (int)((ctx_len + g.split_len - 1) / g.split_len);
-        g.parts = 1;
-        g.q16 = true;
-        return g;
-    }
+    if (d == 128) return attn3_geometry(pairs, ctx_len, sms, attn3_warps(Hkv > 0 ? Hq / Hkv : 1, kb, vb, sparse));
     // the generic kernel stages its whole range in shared memory: at most 512
     // positions (256 at d = 256) keep two CTAs per SM
     int split = d > 128 ? 256 : 512;

@@ -298,12 +298,15 @@ def test_qjl_call_validation_before_launch(L):
     assert L.tq_decode_qjl(h, 3, A, A, A, None, 4, A, 0, None) == 1
     assert L.tq_decode_qjl(h, 3, A, A + 8, A, A, 4, A, 0, None) == 3
     assert L.tq_decode_qjl(h, 3, None, None, None, None, 0, None, 0, None) == 0
-    # workspace: rotated and projected queries (2 d floats per query head, in
-    # 64-float units) then (d + 2) floats per query head and split
+    # workspace of the CUDA-core kernel (d = 64): rotated and projected
+    # queries (2 d floats per query head, in 64-float units) then (d + 2)
+    # floats per query head and split; at d = 128 also the tensor-core
+    # kernel's (two fp16 query prefixes, partials, work partition)
     assert L.tq_attn_qjl_workspace_bytes(1, 8, 2, 256, 1000) == 0
     assert L.tq_attn_qjl_workspace_bytes(1, 12, 8, 128, 1000) == 0  # Hq % Hkv
-    n = L.tq_attn_qjl_workspace_bytes(1, 8, 2, 128, 1000)
-    assert n >= 4 * (2048 + 8 * 130) and (n - 4 * 2048) % (4 * 8 * 130) == 0
+    n = L.tq_attn_qjl_workspace_bytes(1, 8, 2, 64, 1000)
+    assert n >= 4 * (1024 + 8 * 66) and (n - 4 * 1024) % (4 * 8 * 66) == 0
+    assert L.tq_attn_qjl_workspace_bytes(1, 8, 2, 128, 1000) >= 4 * (2048 + 8 * 130)
     cv = abi.CacheView(A, A, A, A, 256)
     W = 1 << 24
     # tq_attn_decode_qjl(plan, S, q, B, Hq, Hkv, cache, k_rnorm, ctx, kb, vb, scale, out, ws, ws_bytes, s)
