@@ -801,20 +801,22 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
             }
             if constexpr (QJL) {
                 // <q', sgn>: A = +-1 from the sign bits (bit set: +1).  Lane t
-                // reads sign word t of its rows (projections 32t .. 32t + 31), in
-                // the k-slot order of the index dims above, so B is the projected
-                // query's fragments laid out as the query's.
+                // reads sign word t of its rows (projections 32t .. 32t + 31).
+                // For MMA kk its fp16 pairs are bits (kk, kk + 16) (a0, a1) and
+                // (kk + 8, kk + 24) (a2, a3): one constant shift puts both bits
+                // of a pair on the fp16 sign positions (bits 15 and 31).  The
+                // projected query is stored in the same order (k_attn3_qjl_q).
                 uint32_t sw[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
                     sw[h] = lds_u32(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + L::kSignOff + 4 * t));
 #pragma unroll
                 for (int hg = 0; hg < NG; ++hg) ssg[u][hg][0] = ssg[u][hg][1] = ssg[u][hg][2] = ssg[u][hg][3] = 0.f;
-                auto pm1 = [](uint32_t x) { return 0xBC00BC00u ^ ((x & 1u) << 15) ^ ((x & 2u) << 30); };
+                auto pm1 = [](uint32_t z) { return (z & 0x80008000u) ^ 0xBC00BC00u; };
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t a0 = pm1(sw[0] >> (4 * kk)), a2 = pm1(sw[0] >> (4 * kk + 2));
-                    const uint32_t a1 = pm1(sw[1] >> (4 * kk)), a3 = pm1(sw[1] >> (4 * kk + 2));
+                    const uint32_t a0 = pm1(sw[0] << (15 - kk)), a2 = pm1(sw[0] << (7 - kk));
+                    const uint32_t a1 = pm1(sw[1] << (15 - kk)), a3 = pm1(sw[1] << (7 - kk));
 #pragma unroll
                     for (int hg = 0; hg < NG; ++hg)
                         mma16816(ssg[u][hg], a0, a1, a2, a3, qpb[hg][kk][0], qpb[hg][kk][1]);
@@ -1454,9 +1456,11 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
 // part of the scores.  y = s2 . H (s . q) (unnormalised, as k_attn3_q), then
 // q' = proj_mul * S y with proj_mul = scale * log2(e) * sqrt(pi/2) / (d sqrt(d)),
 // so that gamma <q', sgn> is the sign part of the score in log2 units, as
-// fp16 high and low parts of q' / 2^e (|q' / 2^e| < 2^14) at qp16[bh][2][128]
-// in projection order, and 2^e at qpexp[bh].  One block of 128 threads per
-// head; thread k forms projection k from row k of S.
+// fp16 high and low parts of q' / 2^e (|q' / 2^e| < 2^14) at qp16[bh][2][128],
+// and 2^e at qpexp[bh].  Projection 32t + j sits at 32t + 4 (j mod 8) + m,
+// m = 0, 2, 1, 3 for j in [0, 8), [8, 16), [16, 24), [24, 32): the order in
+// which the split kernel's sign fragments pair the bits.  One block of 128
+// threads per head; thread k forms projection k from row k of S.
 static __global__ void __launch_bounds__(128) k_attn3_qjl_q(const __nv_bfloat16* __restrict__ q,
                                                             const float* __restrict__ S, __half* __restrict__ qp16,
                                                             float* __restrict__ qpexp,
@@ -1491,8 +1495,10 @@ static __global__ void __launch_bounds__(128) k_attn3_qjl_q(const __nv_bfloat16*
     const float ps = ldexpf(p, -e);
     const __half hi = __float2half_rn(ps);
     const __half lo = __float2half_rn(ps - __half2float(hi));
-    qp16[(int64_t)bh * 256 + j] = hi;
-    qp16[(int64_t)bh * 256 + 128 + j] = lo;
+    const int r = j & 31, slot = (int)((0x3120u >> (4 * (r >> 3))) & 0xFu);  // 0, 2, 1, 3
+    const int at = (j & ~31) + 4 * (r & 7) + slot;
+    qp16[(int64_t)bh * 256 + at] = hi;
+    qp16[(int64_t)bh * 256 + 128 + at] = lo;
     if (j == 0) qpexp[bh] = ldexpf(1.f, e);
 }
 
