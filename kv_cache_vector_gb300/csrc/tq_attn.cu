@@ -257,17 +257,11 @@ __device__ __forceinline__ void attn3_rotate_q(const __nv_bfloat16* __restrict__
 // holds elements 4 l .. 4 l + 3, the butterflies over index bits 0 and 1 are
 // in registers and those over bits 2-6 between lanes, in the order len = 1,
 // 2, .., 64, and the scale and the fp16 parts are those of rotate_q_row.
-// gmax (sparse V, or nullptr): the split kernel's running maxima, cleared here.
-static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __restrict__ q,
-                                                        __half* __restrict__ q16,
-                                                        float* __restrict__ qexp,
-                                                        const __grid_constant__ AttnParams P, int64_t n_rows,
-                                                        uint32_t* __restrict__ gmax) {
-    griddep_launch();  // the split kernel may start its table build now
-    const int lane = threadIdx.x & 31;
-    const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (bh >= n_rows) return;  // the whole warp
-    if (gmax && lane == 0) gmax[bh] = 0u;  // below every score's key
+// y_out (or nullptr): the lane's four elements of s2 . H (s . q) before the
+// scale, for the QJL projection.
+__device__ __forceinline__ void attn3_q_warp(const __nv_bfloat16* __restrict__ q, __half* __restrict__ q16,
+                                             float* __restrict__ qexp, const AttnParams& P, int64_t bh, int lane,
+                                             float* y_out) {
     const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + bh * 128) + lane);
     float x[4];
     {
@@ -299,7 +293,9 @@ static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __r
     float M = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u)) * P.q_mul;
+        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u));
+        if (y_out) y_out[k] = x[k];
+        x[k] *= P.q_mul;
         M = fmaxf(M, fabsf(x[k]));
     }
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
@@ -324,6 +320,20 @@ static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __r
         make_uint2((uint32_t)__half_as_ushort(lo[0]) | ((uint32_t)__half_as_ushort(lo[1]) << 16),
                    (uint32_t)__half_as_ushort(lo[2]) | ((uint32_t)__half_as_ushort(lo[3]) << 16));
     if (lane == 0) qexp[bh] = ldexpf(1.f, e);
+}
+
+// gmax (sparse V, or nullptr): the split kernel's running maxima, cleared here.
+static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __restrict__ q,
+                                                        __half* __restrict__ q16,
+                                                        float* __restrict__ qexp,
+                                                        const __grid_constant__ AttnParams P, int64_t n_rows,
+                                                        uint32_t* __restrict__ gmax) {
+    griddep_launch();  // the split kernel may start its table build now
+    const int lane = threadIdx.x & 31;
+    const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (bh >= n_rows) return;  // the whole warp
+    if (gmax && lane == 0) gmax[bh] = 0u;  // below every score's key
+    attn3_q_warp(q, q16, qexp, P, bh, lane, nullptr);
 }
 
 // The query rotation of the paged attention with the decode step's append
@@ -455,13 +465,18 @@ struct A3PairCost {
 // starts at the first item with P_i >= ceil(c total / grid), found by a
 // binary search over the pairs' prefix weights and one within the pair.  A
 // CTA's range thus runs through consecutive splits of one (batch, KV head)
-// at a time.
+// at a time.  The kernel runs beside the query rotation launched before it
+// (programmatic dependent launch) and waits for it at the end, so that the
+// split kernel, which waits for this one, sees the rotated queries too;
+// lens_from_prev: lens is written by that launch, so wait for it first.
 static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __restrict__ lens, int Hkv,
                                                             int n_splits, int64_t seg, int warp_len,
-                                                            int64_t max_ctx, int n_pairs, int grid, A3Meta m) {
+                                                            int64_t max_ctx, int n_pairs, int grid, A3Meta m,
+                                                            bool lens_from_prev) {
     extern __shared__ __align__(16) unsigned char plan_smem[];
     __shared__ int64_t wsum[32];
     __shared__ int32_t cb[1025];
+    if (lens_from_prev) griddep_wait();
     griddep_launch();
     const int tid = threadIdx.x;
     const int W = (int)(seg / warp_len), nC = warp_len / kA3Chunk;
@@ -538,6 +553,7 @@ static __global__ void __launch_bounds__(1024) k_attn3_plan(const int32_t* __res
         m.c0[bh] = a;
         m.clast[bh] = z;
     }
+    griddep_wait();  // the query rotation has completed
 }
 
 // PAGED: the cache is paged (PagedArgs), each sequence attends over its own
@@ -1429,9 +1445,8 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) plan_attr[dev] = 1;
         }
-        k_attn3_plan<<<1, 1024, plan_smem, s>>>(pa.lens, Hkv, geo.n_splits, (int64_t)geo.split_len, geo.warp_len,
-                                                ctx_len, n_pairs, grid, meta);
-        e = cudaGetLastError();
+        e = launch_pdl(k_attn3_plan, dim3(1), dim3(1024), plan_smem, s, (const int32_t*)pa.lens, Hkv, geo.n_splits,
+                       (int64_t)geo.split_len, geo.warp_len, ctx_len, n_pairs, grid, meta, app != nullptr);
         if (e != cudaSuccess) return e;
     }
     // contiguous cache with a sparse-V threshold: the variant that copies V
@@ -1452,58 +1467,97 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
                       grid, items, Hq, Hkv, (int64_t)B * Hq, out, P, PAGED, meta);
 }
 
-// QJL keys: the projected query of one (batch, query head) for the sign
-// part of the scores.  y = s2 . H (s . q) (unnormalised, as k_attn3_q), then
-// q' = proj_mul * S y with proj_mul = scale * log2(e) * sqrt(pi/2) / (d sqrt(d)),
-// so that gamma <q', sgn> is the sign part of the score in log2 units, as
-// fp16 high and low parts of q' / 2^e (|q' / 2^e| < 2^14) at qp16[bh][2][128],
-// and 2^e at qpexp[bh].  Projection 32t + j sits at 32t + 4 (j mod 8) + m,
-// m = 0, 2, 1, 3 for j in [0, 8), [8, 16), [16, 24), [24, 32): the order in
-// which the split kernel's sign fragments pair the bits.  One block of 128
-// threads per head; thread k forms projection k from row k of S.
-static __global__ void __launch_bounds__(128) k_attn3_qjl_q(const __nv_bfloat16* __restrict__ q,
-                                                            const float* __restrict__ S, __half* __restrict__ qp16,
+// QJL keys: the rotated and the projected queries of eight (batch, query
+// head) rows per block of 256 threads.  Warp w rotates row 8 blockIdx.x + w
+// as k_attn3_q does (q16, qexp) and keeps y = s2 . H (s . q) (unnormalised)
+// in shared memory.  The projection is q' = proj_mul * S y with proj_mul =
+// scale * log2(e) * sqrt(pi/2) / (d sqrt(d)), so that gamma <q', sgn> is the
+// sign part of the score in log2 units.  S (row k = projection k) passes
+// through shared memory in two halves of 64 columns with a row stride of 65
+// floats, so that the 32 lanes reading one column of 32 rows hit distinct
+// banks; thread (h4, k) forms projection k of rows 4 h4 .. 4 h4 + 3.  Each
+// row is stored as fp16 high and low parts of q' / 2^e (|q' / 2^e| < 2^14) at
+// qp16[bh][2][128] and 2^e at qpexp[bh].  Projection 32t + j sits at 32t +
+// 4 (j mod 8) + m, m = 0, 2, 1, 3 for j in [0, 8), [8, 16), [16, 24), [24,
+// 32): the order in which the split kernel's sign fragments pair the bits.
+static __global__ void __launch_bounds__(256) k_attn3_qjl_q(const __nv_bfloat16* __restrict__ q,
+                                                            const float* __restrict__ S, __half* __restrict__ q16,
+                                                            float* __restrict__ qexp, __half* __restrict__ qp16,
                                                             float* __restrict__ qpexp,
-                                                            const __grid_constant__ AttnParams P, float proj_mul) {
-    __shared__ float v[128];
-    __shared__ float wmax[4];
+                                                            const __grid_constant__ AttnParams P, float proj_mul,
+                                                            int64_t n_rows) {
+    __shared__ __align__(16) float ys[8][128];
+    __shared__ float ss[128 * 65];
+    __shared__ float wmax[8][4];
     griddep_launch();
-    const int bh = blockIdx.x, j = threadIdx.x;
-    const float x = __bfloat162float(q[(int64_t)bh * 128 + j]);
-    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
-    fwht_smem<128>(v, 1);
-    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u));
-    __syncthreads();
-    v[j] = y;
-    __syncthreads();
-    float p = 0.f;
-    const float* row = S + (int64_t)j * 128;
-#pragma unroll 8
-    for (int i = 0; i < 128; ++i) p = fmaf(__ldg(row + i), v[i], p);
-    p *= proj_mul;
-    float M = fabsf(p);
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    if ((j & 31) == 0) wmax[j >> 5] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-    int e = 0;
-    if (M > 0.f && M <= FLT_MAX) {
-        int ex = 0;
-        frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
-        e = min(100, max(-100, ex - 14));
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t row0 = (int64_t)blockIdx.x * 8;
+    {
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row0 + w < n_rows) attn3_q_warp(q, q16, qexp, P, row0 + w, lane, y);
+        *reinterpret_cast<float4*>(&ys[w][4 * lane]) = make_float4(y[0], y[1], y[2], y[3]);
     }
-    const float ps = ldexpf(p, -e);
-    const __half hi = __float2half_rn(ps);
-    const __half lo = __float2half_rn(ps - __half2float(hi));
-    const int r = j & 31, slot = (int)((0x3120u >> (4 * (r >> 3))) & 0xFu);  // 0, 2, 1, 3
-    const int at = (j & ~31) + 4 * (r & 7) + slot;
-    qp16[(int64_t)bh * 256 + at] = hi;
-    qp16[(int64_t)bh * 256 + 128 + at] = lo;
-    if (j == 0) qpexp[bh] = ldexpf(1.f, e);
+    const int k = tid & 127, h4 = tid >> 7;
+    float p[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int half = 0; half < 2; ++half) {
+        __syncthreads();  // ys written; the previous half's reads of ss done
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {  // 128 rows x 16 float4 of this half
+            const int f = tid + 256 * r, sr = f >> 4, c4 = f & 15;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(S + sr * 128 + 64 * half) + c4);
+            float* d = ss + sr * 65 + 4 * c4;
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        }
+        __syncthreads();
+        const float* srow = ss + k * 65;
+#pragma unroll 4
+        for (int i = 0; i < 64; i += 4) {
+            const float s0 = srow[i], s1 = srow[i + 1], s2 = srow[i + 2], s3 = srow[i + 3];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float4 y = *reinterpret_cast<const float4*>(&ys[4 * h4 + h][64 * half + i]);
+                p[h] = fmaf(s0, y.x, p[h]);
+                p[h] = fmaf(s1, y.y, p[h]);
+                p[h] = fmaf(s2, y.z, p[h]);
+                p[h] = fmaf(s3, y.w, p[h]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        p[h] *= proj_mul;
+        float M = fabsf(p[h]);
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        if (lane == 0) wmax[w][h] = M;
+    }
+    __syncthreads();
+    const int r = k & 31, slot = (int)((0x3120u >> (4 * (r >> 3))) & 0xFu);  // 0, 2, 1, 3
+    const int at = (k & ~31) + 4 * (r & 7) + slot;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int64_t bh = row0 + 4 * h4 + h;
+        if (bh >= n_rows) break;
+        const float M = fmaxf(fmaxf(wmax[4 * h4][h], wmax[4 * h4 + 1][h]), fmaxf(wmax[4 * h4 + 2][h], wmax[4 * h4 + 3][h]));
+        int e = 0;
+        if (M > 0.f && M <= FLT_MAX) {
+            int ex = 0;
+            frexpf(M, &ex);  // M in [2^(ex-1), 2^ex)
+            e = min(100, max(-100, ex - 14));
+        }
+        const float ps = ldexpf(p[h], -e);
+        const __half hi = __float2half_rn(ps);
+        const __half lo = __float2half_rn(ps - __half2float(hi));
+        qp16[bh * 256 + at] = hi;
+        qp16[bh * 256 + 128 + at] = lo;
+        if (k == 0) qpexp[bh] = ldexpf(1.f, e);
+    }
 }
 
-// QJL keys (KB bits in total, contiguous cache): the query rotation, the
-// projected query, the split kernel with the QJL scores, the combine.  The
+// QJL keys (KB bits in total, contiguous cache): the rotated and projected
+// queries, the split kernel with the QJL scores, the combine.  The
 // workspace is the d = 128 layout with the projected queries' prefix after
 // the rotated queries'.
 template <int KB, int VB>
@@ -1527,11 +1581,9 @@ cudaError_t attn3_qjl_launch(const void* q, const float* S, int B, int Hq, int H
     meta.qpexp = qpexp;
     meta.k_rnorm = k_rnorm;
     const auto qb = static_cast<const __nv_bfloat16*>(q);
-    k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(qb, q16, qexp, P, (int64_t)B * Hq, nullptr);
+    k_attn3_qjl_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(qb, S, q16, qexp, qp16, qpexp, P, proj_mul,
+                                                                         (int64_t)B * Hq);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_attn3_qjl_q<<<(unsigned)(B * Hq), 128, 0, s>>>(qb, S, qp16, qpexp, P, proj_mul);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
     const int grid = (int)(items < sms ? items : sms);  // one CTA per SM

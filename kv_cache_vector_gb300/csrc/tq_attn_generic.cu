@@ -434,12 +434,15 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
 // QJL keys: the rotated query of one (batch, query head), times the softmax
 // scale, and its projection by the QJL matrix times sqrt(pi/2)/d, written to
 // qpre[bh][0, D) and [D, 2D).  One block of D threads per head; thread k
-// forms projection k from row k of S.
+// forms projection k from row k of S, which passes through shared memory 32
+// columns at a time (read coalesced, row stride 33 floats, so that the lanes
+// reading one column of 32 rows hit distinct banks).
 template <int D>
 __global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict__ q,
                                                  const float* __restrict__ S, float* __restrict__ qpre,
                                                  const __grid_constant__ AttnParams P, float kappa) {
     __shared__ float v[D];
+    __shared__ float ss[D * 33];
     griddep_wait();
     griddep_launch();
     const int bh = blockIdx.x, j = threadIdx.x;
@@ -452,9 +455,14 @@ __global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict
     v[j] = r;
     __syncthreads();
     float p = 0.f;
-    const float* row = S + (int64_t)j * D;
+    for (int c = 0; c < D; c += 32) {
+        if (c > 0) __syncthreads();  // the previous columns' reads done
 #pragma unroll 8
-    for (int i = 0; i < D; ++i) p = fmaf(__ldg(row + i), v[i], p);
+        for (int f = j; f < D * 32; f += D) ss[(f >> 5) * 33 + (f & 31)] = __ldg(S + (f >> 5) * D + c + (f & 31));
+        __syncthreads();
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) p = fmaf(ss[j * 33 + i], v[c + i], p);
+    }
     qpre[(int64_t)bh * 2 * D + j] = r;
     qpre[(int64_t)bh * 2 * D + D + j] = p * kappa;
 }
