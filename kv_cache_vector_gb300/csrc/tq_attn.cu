@@ -791,21 +791,38 @@ k_attn3_split(const __half* __restrict__ q16, const float* __restrict__ qexp, in
 #pragma unroll
             for (int h = 0; h < 2; ++h)
                 load_kfield<MB>(sK + (uint32_t)((16 * u + 8 * h + g) * L::kKRow + 4 * MB * t), kw[h]);
+            if constexpr (L::kRest) {
+                // S = (K_hi + K_lo) (Q_hi + Q_lo) with the keys' fp16 rests:
+                // one MMA per 8 positions, whose A rows g and g + 8 are the
+                // high parts and the rests of the same position, so that one
+                // 8-byte table entry (high pair, rest pair) is two consecutive
+                // A registers; the two row halves are summed afterwards
+                float ra[2][NG][4];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                if constexpr (L::kRest) {
-                    // S = (K_hi + K_lo) (Q_hi + Q_lo): the keys' fp16 rests as a
-                    // second MMA into the same accumulators
-                    const uint2 a0 = lds_tab2(pair_addr<MB>(kw[0], 2 * kk, kslot));
-                    const uint2 a2 = lds_tab2(pair_addr<MB>(kw[0], 2 * kk + 1, kslot));
-                    const uint2 a1 = lds_tab2(pair_addr<MB>(kw[1], 2 * kk, kslot));
-                    const uint2 a3 = lds_tab2(pair_addr<MB>(kw[1], 2 * kk + 1, kslot));
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int hg = 0; hg < NG; ++hg) ra[h][hg][0] = ra[h][hg][1] = ra[h][hg][2] = ra[h][hg][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint2 e0 = lds_tab2(pair_addr<MB>(kw[h], 2 * kk, kslot));
+                        const uint2 e1 = lds_tab2(pair_addr<MB>(kw[h], 2 * kk + 1, kslot));
+#pragma unroll
+                        for (int hg = 0; hg < NG; ++hg)
+                            mma16816(ra[h][hg], e0.x, e0.y, e1.x, e1.y, qb[hg][kk][0], qb[hg][kk][1]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int hg = 0; hg < NG; ++hg) {
-                        mma16816(sacc[u][hg], a0.x, a1.x, a2.x, a3.x, qb[hg][kk][0], qb[hg][kk][1]);
-                        mma16816(sacc[u][hg], a0.y, a1.y, a2.y, a3.y, qb[hg][kk][0], qb[hg][kk][1]);
+                        sacc[u][hg][2 * h] = ra[h][hg][0] + ra[h][hg][2];
+                        sacc[u][hg][2 * h + 1] = ra[h][hg][1] + ra[h][hg][3];
                     }
-                } else {
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t a0 = lds_tab(pair_addr<MB>(kw[0], 2 * kk, kslot));
                     const uint32_t a2 = lds_tab(pair_addr<MB>(kw[0], 2 * kk + 1, kslot));
                     const uint32_t a1 = lds_tab(pair_addr<MB>(kw[1], 2 * kk, kslot));
