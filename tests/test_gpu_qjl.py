@@ -168,6 +168,7 @@ def _qjl_cache(seed, d, B, Hkv, cap, kb, vb, S32):
     (128, 2, 32, 8, 1100, 1037),   # several splits and a ragged tail
     (128, 1, 8, 8, 64, 1),         # one position: the V row
     (128, 1, 16, 2, 900, 777),     # eight query heads per KV head
+    (128, 3, 2, 1, 300, 211),      # six query rows: a part-filled block of the query kernel
     (64, 3, 16, 2, 700, 700),      # group of 8, the whole cache
     (32, 1, 4, 4, 300, 257),
 ])
