@@ -63,9 +63,14 @@ unsigned grid_for(const void* fn, int block_threads, int64_t items) {
 }
 
 namespace {
+// Tuning parameter: the share of the last wave the d = 128 split geometry
+// asks its work items to fill.
+#ifndef TQ_ATTN3_FILL
+#define TQ_ATTN3_FILL 0.97
+#endif
 // d = 128: the longest per-warp range (256 down to 32 positions) whose work
-// items fill the last wave of one-CTA-per-SM grids to at least 90%, else the
-// one that fills it best; W warps per CTA.
+// items fill the last wave of one-CTA-per-SM grids to at least TQ_ATTN3_FILL,
+// else the one that fills it best; W warps per CTA.
 AttnGeometry attn3_geometry(int64_t pairs, int64_t ctx_len, int sms, int W) {
     AttnGeometry g;
     const int64_t cap = sms > 0 ? sms : 1;
@@ -77,7 +82,7 @@ AttnGeometry attn3_geometry(int64_t pairs, int64_t ctx_len, int sms, int W) {
         const int64_t grid = items < cap ? (items > 0 ? items : 1) : cap;
         const int64_t rounds = (items + grid - 1) / grid;
         const double eff = rounds > 0 ? (double)items / (double)(rounds * grid) : 1.0;
-        if (eff >= 0.9) {
+        if (eff >= TQ_ATTN3_FILL) {
             best = wl;
             break;
         }
