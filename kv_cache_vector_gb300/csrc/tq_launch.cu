@@ -68,6 +68,10 @@ namespace {
 #ifndef TQ_ATTN3_FILL
 #define TQ_ATTN3_FILL 0.97
 #endif
+// Tuning parameter: the shortest split of the CUDA-core decode attention.
+#ifndef TQ_ATTN_MIN_SPLIT
+#define TQ_ATTN_MIN_SPLIT 64
+#endif
 // d = 128: the longest per-warp range (256 down to 32 positions) whose work
 // items fill the last wave of one-CTA-per-SM grids to at least TQ_ATTN3_FILL,
 // else the one that fills it best; W warps per CTA.
@@ -119,7 +123,7 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
     // positions (256 at d = 256) keep two CTAs per SM
     int split = d > 128 ? 256 : 512;
     const int64_t want = 2LL * (sms > 0 ? sms : 1);
-    while (split > 64 && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
+    while (split > TQ_ATTN_MIN_SPLIT && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
     g.split_len = split;
     g.n_splits = (int)((ctx_len + split - 1) / split);
     g.parts = 1;
