@@ -27,7 +27,8 @@
 // are one warp ballot.  The block keeps S in shared memory, row-major with a
 // stride of d + 4 floats: lane reads of four consecutive floats of 32
 // different rows (encode) and of one row (decode) are both free of bank
-// conflicts.  Each S load feeds the four rows of the warp.
+// conflicts.  Each S load feeds the four rows of the warp.  Blocks of 12
+// warps: two of them fit an SM by registers and by shared memory (S is 66 KB).
 #include <cuda_bf16.h>
 
 #include "tq_device.cuh"
@@ -35,8 +36,16 @@
 namespace tq {
 namespace dev {
 
-constexpr int kQjlWarps = 8;
-constexpr int kQjlRows = 4;  // rows per warp at a time
+// Tuning parameters: warps per block, and rows per warp at a time (each S
+// load feeds that many rows).
+#ifndef TQ_QJL_WARPS
+#define TQ_QJL_WARPS 12
+#endif
+constexpr int kQjlWarps = TQ_QJL_WARPS;
+#ifndef TQ_QJL_ROWS
+#define TQ_QJL_ROWS 4
+#endif
+constexpr int kQjlRows = TQ_QJL_ROWS;
 
 template <int D>
 struct QjlSmem {
@@ -128,16 +137,21 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
     for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
          r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
         float nrm[kQjlRows], gam[kQjlRows];
-        // ---- MSE stage and residual of each row (rows past the end: zeros)
+        // the rows' loads first, all in flight (rows past the end: zeros)
+        float vq[kQjlRows][E];
 #pragma unroll
         for (int q = 0; q < kQjlRows; ++q) {
-            float v[E];
             if (r0 + q < n_rows) {
-                load_lane<E, T>(x + (r0 + q) * D, lane, sg, v);
+                load_lane<E, T>(x + (r0 + q) * D, lane, sg, vq[q]);
             } else {
 #pragma unroll
-                for (int e = 0; e < E; ++e) v[e] = 0.f;
+                for (int e = 0; e < E; ++e) vq[q][e] = 0.f;
             }
+        }
+        // ---- MSE stage and residual of each row
+#pragma unroll
+        for (int q = 0; q < kQjlRows; ++q) {
+            float(&v)[E] = vq[q];
             float ss = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
@@ -212,7 +226,9 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
 }
 
 // Decode: y = s1 . H (s2 . (n c[idx] + kappa gamma S^T sgn)) / sqrt(d), kappa =
-// sqrt(pi/2)/d; lane l computes coordinates l E .. l E + E - 1.
+// sqrt(pi/2)/d; lane l computes coordinates l E .. l E + E - 1.  S^T sgn is
+// taken as 2 t - c, t the sum of the rows of S whose sign bit is set (one
+// predicated add per element) and c the column sums of S.
 template <int D, int BITS, typename TO>
 __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __restrict__ packed,
                                                                const float* __restrict__ norms,
@@ -224,9 +240,19 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
     constexpr int kStride = QjlSmem<D>::kStride;
     extern __shared__ __align__(16) unsigned char qjl_smem[];
     float* Ss = reinterpret_cast<float*>(qjl_smem);
+    __shared__ float csum[D];  // column sums of S
     stage_matrix<D>(S, Ss);
     __syncthreads();
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        float c = 0.f;
+        for (int k = 0; k < D; ++k) c += Ss[k * kStride + i];
+        csum[i] = c;
+    }
+    __syncthreads();
+    float cs[E];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int e = 0; e < E; ++e) cs[e] = csum[lane * E + e];
     for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
          r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
         uint32_t sw[kQjlRows][E];  // sign words of each row (every lane holds all)
@@ -248,7 +274,7 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
             nrm[q] = ok ? __ldg(norms + r0 + q) : 0.f;
             gk[q] = ok ? __ldg(rnorms + r0 + q) * kappa : 0.f;
         }
-        // t_i = sum_k sgn_k S[k][i]
+        // t_i = sum of S[k][i] over the projections k with sgn_k = +1
         float t[kQjlRows][E];
 #pragma unroll
         for (int q = 0; q < kQjlRows; ++q)
@@ -256,7 +282,7 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
             for (int e = 0; e < E; ++e) t[q][e] = 0.f;
 #pragma unroll
         for (int kw = 0; kw < E; ++kw) {
-#pragma unroll 8
+#pragma unroll
             for (int b = 0; b < 32; ++b) {
                 const int k = 32 * kw + b;
                 float s[E];
@@ -270,11 +296,11 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
                     s[0] = Ss[k * kStride + lane];
                 }
 #pragma unroll
-                for (int q = 0; q < kQjlRows; ++q) {
-                    const uint32_t neg = (~sw[q][kw] >> b) << 31;  // sign bit set for sgn_k = -1
+                for (int q = 0; q < kQjlRows; ++q)
+                    if (sw[q][kw] & (1u << b)) {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) t[q][e] += __uint_as_float(__float_as_uint(s[e]) ^ neg);
-                }
+                        for (int e = 0; e < E; ++e) t[q][e] += s[e];
+                    }
             }
         }
 #pragma unroll
@@ -284,7 +310,7 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
 #pragma unroll
             for (int e = 0; e < E; ++e) {
                 const float c = P.cen[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
-                v[e] = fmaf(gk[q], t[q][e], nrm[q] * c);
+                v[e] = fmaf(gk[q], fmaf(2.f, t[q][e], -cs[e]), nrm[q] * c);
                 if (P.two_sided) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ P.sgn2[lane * E + e]);
             }
             warp_fwht<E>(v, lane);
