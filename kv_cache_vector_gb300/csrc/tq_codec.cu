@@ -149,7 +149,9 @@ __global__ void __launch_bounds__(kBlock) k_append(const T* __restrict__ k_new,
 
 // Append for d >= 32, built for latency (a decode step appends a few rows):
 // one warp per row (warp_encode_indices, warp_pack_row), kAppWarps rows per
-// block.
+// block.  Launched with programmatic dependent launch: the sign tables are
+// set up while the previous kernel of the stream finishes, and the rows and
+// the cache are touched only after it has.
 constexpr int kAppWarps = 4;
 
 // PAGED: one new row per (sequence, KV head) (n_new = 1), written at position
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
         sg2[i] = P.sgn2[i];
     }
     __syncthreads();
+    griddep_wait();    // the new rows, and readers of the cache, of the previous kernel
+    griddep_launch();  // the next kernel may set itself up; it waits for this grid
     const int bits = is_v ? v_bits : k_bits;
     const int nb = (1 << bits) - 1;
     const T* src = is_v ? v_new : k_new;
@@ -1509,9 +1513,9 @@ cudaError_t app(const void* kn, const void* vn, int B, int Hkv, int64_t n_new, c
         int64_t g = (rows + dev::kAppWarps - 1) / dev::kAppWarps;
         const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kAppWarps, 0);
         if (g > cap) g = cap;
-        fn<<<dim3((unsigned)g, 2), 32 * dev::kAppWarps, 0, s>>>(static_cast<const T*>(kn),
-                                                                static_cast<const T*>(vn), rows, n_new, c,
-                                                                pos, kb, vb, PK, PV, PagedArgs{}, Hkv, nullptr);
+        return dev::launch_pdl(fn, dim3((unsigned)g, 2), dim3(32 * dev::kAppWarps), 0, s, static_cast<const T*>(kn),
+                               static_cast<const T*>(vn), rows, n_new, c, pos, kb, vb, PK, PV, PagedArgs{}, Hkv,
+                               (int*)nullptr);
     } else {
         auto fn = dev::k_append<D, T>;
         unsigned g = grid_for((const void*)fn, dev::kBlock, rows * dev::RowShape<D>::R);
@@ -1580,11 +1584,9 @@ cudaError_t launch_append_paged_d(int k_bits, int v_bits, tq_dtype dt, const voi
             int64_t g = (rows + dev::kAppWarps - 1) / dev::kAppWarps;
             const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kAppWarps, 0);
             if (g > cap) g = cap;
-            fn<<<dim3((unsigned)g, 2), 32 * dev::kAppWarps, 0, s>>>(static_cast<const T*>(k_new),
-                                                                    static_cast<const T*>(v_new), rows, 1,
-                                                                    pages, 0, k_bits, v_bits, PK, PV, pa, Hkv,
-                                                                    status_word());
-            return cudaGetLastError();
+            return dev::launch_pdl(fn, dim3((unsigned)g, 2), dim3(32 * dev::kAppWarps), 0, s,
+                                   static_cast<const T*>(k_new), static_cast<const T*>(v_new), rows, (int64_t)1,
+                                   pages, (int64_t)0, k_bits, v_bits, PK, PV, pa, Hkv, status_word());
         };
         return dt == TQ_BF16 ? launch(__nv_bfloat16{}) : launch(float{});
     } else {
