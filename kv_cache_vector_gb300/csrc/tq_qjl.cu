@@ -30,7 +30,9 @@
 // conflicts.  Each S load feeds the four rows of the warp.  Blocks of 12
 // warps: two of them fit an SM by registers and by shared memory (S is 66 KB).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
+#include "tq_async.cuh"
 #include "tq_device.cuh"
 
 namespace tq {
@@ -325,6 +327,305 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
     }
 }
 
+#if TQ_UNIT_D == 128
+// ---- d = 128: the projections on the tensor cores (mma.sync m16n8k16, fp16
+// operands, fp32 accumulation), a warp taking 16 rows at a time.
+//
+// Encode: the MSE stage is the CUDA-core kernel's, row by row, so indices,
+// norms and gammas are the same.  The residuals, times 2^10, go to shared
+// memory as fp16 high and low parts, and P = R S^T is taken as R_hi S_hi +
+// R_lo S_hi + R_hi S_lo: each operand carried to about 22 bits, so a sign can
+// differ from an exact projection's only within about 1e-6 ||r|| of zero.  The
+// sign bits come from four ballots per tile of 8 projections.
+// Decode: S^T sgn = SGN S with A = the signs as fp16 +-1 (exact), B = S as
+// fp16 high and low parts, then the CUDA-core kernel's epilogue per row.
+// S sits in shared memory as fp16 high and low parts in rows of 136 halves:
+// [projection][dim] for the encode, [dim][projection] for the decode, so that
+// each operand's ldmatrix reads 8 rows of 16 bytes from distinct banks.
+#ifndef TQ_QJL_TC_WARPS
+#define TQ_QJL_TC_WARPS 12
+#endif
+constexpr int kQtcWarps = TQ_QJL_TC_WARPS;
+constexpr int kQtcRow = 136;                                     // halves per row of an fp16 tile
+constexpr int kQtcS = 2 * 128 * kQtcRow * 2;                     // S high and low parts
+constexpr int kQtcEncWarp = 2 * 16 * kQtcRow * 2 + 16 * 128;     // residual parts, index bytes
+constexpr int kQtcEncSmem = kQtcS + kQtcWarps * kQtcEncWarp + 2 * 128 * 4;
+constexpr int kQtcDecWarp = 16 * kQtcRow * 4;                    // S^T sgn of 16 rows, fp32
+constexpr int kQtcDecSmem = kQtcS + kQtcWarps * kQtcDecWarp;
+
+__device__ __forceinline__ void qtc_mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void qtc_ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// x as fp16 high and low parts (x = hi + lo to about 22 bits), packed pairwise.
+__device__ __forceinline__ void qtc_split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+    const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+    hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+    lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+}
+// S (fp32 [projection][dim]) as fp16 high and low parts in rows of kQtcRow
+// halves, [projection][dim] or, TRANS, [dim][projection].
+template <bool TRANS>
+__device__ __forceinline__ void qtc_stage_s(const float* __restrict__ S, __half* sh, __half* sl) {
+    for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
+        const int k = i >> 7, j = i & 127;
+        const float v = __ldg(S + i);
+        const __half h = __float2half_rn(v);
+        const int at = TRANS ? j * kQtcRow + k : k * kQtcRow + j;
+        sh[at] = h;
+        sl[at] = __float2half_rn(v - __half2float(h));
+    }
+}
+// bits 0..3 of e to bits 0, 2, 4, 6
+__device__ __forceinline__ uint32_t qtc_spread4(uint32_t e) {
+    return (e & 1u) | ((e & 2u) << 1) | ((e & 4u) << 2) | ((e & 8u) << 3);
+}
+
+template <int BITS, typename T>
+__global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __restrict__ x, int64_t n_rows,
+                                                                  const float* __restrict__ S,
+                                                                  uint8_t* __restrict__ packed,
+                                                                  float* __restrict__ norms,
+                                                                  float* __restrict__ rnorms,
+                                                                  const __grid_constant__ RowParams P) {
+    constexpr int D = 128, E = 4, MB = BITS - 1, NB = (1 << MB) - 1;
+    constexpr int RB = D * BITS / 8, IB = D * MB / 8;
+    extern __shared__ __align__(16) unsigned char qtc_smem[];
+    __half* Sh = reinterpret_cast<__half*>(qtc_smem);
+    __half* Sl = Sh + 128 * kQtcRow;
+    uint32_t* sg = reinterpret_cast<uint32_t*>(qtc_smem + kQtcS + kQtcWarps * kQtcEncWarp);
+    uint32_t* sg2 = sg + D;
+    qtc_stage_s<false>(S, Sh, Sl);
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        sg[i] = P.sgn[i];
+        sg2[i] = P.sgn2[i];
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* wb = qtc_smem + kQtcS + warp * kQtcEncWarp;
+    uint32_t* Rh = reinterpret_cast<uint32_t*>(wb);                       // [16][kQtcRow / 2] half pairs
+    uint32_t* Rl = Rh + 16 * kQtcRow / 2;
+    uint8_t* iw = wb + 2 * 16 * kQtcRow * 2;                               // [16][128] index bytes
+    const uint32_t sRh = smem_addr(Rh), sRl = smem_addr(Rl), sSh = smem_addr(Sh), sSl = smem_addr(Sl);
+    for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
+         r0 += (int64_t)gridDim.x * kQtcWarps * 16) {
+        // ---- MSE stage and residual of each row, four rows at a time (their
+        // loads first; rows past the end: zeros)
+#pragma unroll 1
+        for (int q0 = 0; q0 < 16; q0 += 4) {
+            float vq[4][E];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (r0 + q0 + q < n_rows) {
+                    load_lane<E, T>(x + (r0 + q0 + q) * D, lane, sg, vq[q]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) vq[q][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int row = q0 + q;
+                float(&v)[E] = vq[q];
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+                ss = warp_sum(ss);
+                warp_fwht<E>(v, lane);
+                if (P.two_sided) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
+                }
+                const float n = __fsqrt_rn(ss);
+                const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+                float rr = 0.f, rs[E];
+                uint32_t ids = 0u;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    int id = 0;
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
+                    const float r = fmaf(v[e], inv, -P.cen[id]);
+                    rr = fmaf(r, r, rr);
+                    ids |= (uint32_t)id << (8 * e);
+                    rs[e] = r * 1024.f;  // exact; keeps the low parts out of the fp16 subnormals
+                }
+                reinterpret_cast<uint32_t*>(iw + row * D)[lane] = ids;
+                uint32_t h0, l0, h1, l1;
+                qtc_split2(rs[0], rs[1], h0, l0);
+                qtc_split2(rs[2], rs[3], h1, l1);
+                *reinterpret_cast<uint2*>(Rh + row * (kQtcRow / 2) + 2 * lane) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2*>(Rl + row * (kQtcRow / 2) + 2 * lane) = make_uint2(l0, l1);
+                rr = warp_sum(rr);
+                if (lane == 0 && r0 + row < n_rows) {
+                    norms[r0 + row] = n;
+                    rnorms[r0 + row] = n * __fsqrt_rn(rr);
+                }
+            }
+        }
+        __syncwarp();
+        // ---- P = R S^T: A fragments of the 8 k-steps (16 dims each), then
+        // tiles of 8 projections
+        uint32_t ah[8][4], al[8][4];
+        {
+            const uint32_t off = (uint32_t)(((lane & 15) * kQtcRow + (lane >> 4) * 8) * 2);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                qtc_ldsm4(sRh + off + 32u * kk, ah[kk]);
+                qtc_ldsm4(sRl + off + 32u * kk, al[kk]);
+            }
+        }
+        uint32_t wd[4] = {0u, 0u, 0u, 0u};  // lane r < 16: the sign words of row r
+        const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                uint32_t bh[4], bl[4];
+                const uint32_t off = boff + (uint32_t)((8 * nt * kQtcRow + 16 * kk) * 2);
+                qtc_ldsm4(sSh + off, bh);  // k-steps kk (regs 0, 1) and kk + 1 (regs 2, 3)
+                qtc_ldsm4(sSl + off, bl);
+                qtc_mma(c, ah[kk], bh[0], bh[1]);
+                qtc_mma(c, al[kk], bh[0], bh[1]);
+                qtc_mma(c, ah[kk], bl[0], bl[1]);
+                qtc_mma(c, ah[kk + 1], bh[2], bh[3]);
+                qtc_mma(c, al[kk + 1], bh[2], bh[3]);
+                qtc_mma(c, ah[kk + 1], bl[2], bl[3]);
+            }
+            // c: rows g, g + 8, projections 8 nt + 2t, 8 nt + 2t + 1 (lane 4g + t)
+            const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, c[0] >= 0.f), b1 = __ballot_sync(0xFFFFFFFFu, c[1] >= 0.f);
+            const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, c[2] >= 0.f), b3 = __ballot_sync(0xFFFFFFFFu, c[3] >= 0.f);
+            const uint32_t sh = 4u * (uint32_t)(lane & 7);
+            const uint32_t e0 = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, e1 = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
+            wd[nt >> 2] |= (qtc_spread4(e0) | (qtc_spread4(e1) << 1)) << (8 * (nt & 3));
+        }
+        // ---- stores: each row's indices, then its sign words
+#pragma unroll 1
+        for (int q = 0; q < 16; ++q) {
+            if (r0 + q >= n_rows) break;  // warp-uniform
+            warp_pack_row<D>(iw + q * D, lane, MB, packed + (r0 + q) * RB);
+        }
+        if (lane < 16 && r0 + lane < n_rows)
+            *reinterpret_cast<uint4*>(packed + (r0 + lane) * RB + IB) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        __syncwarp();
+    }
+}
+
+template <int BITS, typename TO>
+__global__ void __launch_bounds__(32 * kQtcWarps) k_decode_qjl_tc(const uint8_t* __restrict__ packed,
+                                                                  const float* __restrict__ norms,
+                                                                  const float* __restrict__ rnorms,
+                                                                  int64_t n_rows, const float* __restrict__ S,
+                                                                  TO* __restrict__ y,
+                                                                  const __grid_constant__ RowParams P, float kappa) {
+    constexpr int D = 128, E = 4, MB = BITS - 1;
+    constexpr int RB = D * BITS / 8, IB = D * MB / 8;
+    extern __shared__ __align__(16) unsigned char qtc_smem[];
+    __half* Sh = reinterpret_cast<__half*>(qtc_smem);  // [dim][projection]
+    __half* Sl = Sh + 128 * kQtcRow;
+    qtc_stage_s<true>(S, Sh, Sl);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float* Tb = reinterpret_cast<float*>(qtc_smem + kQtcS + warp * kQtcDecWarp);  // [16][kQtcRow]
+    const uint32_t sSh = smem_addr(Sh), sSl = smem_addr(Sl);
+    const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
+    for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
+         r0 += (int64_t)gridDim.x * kQtcWarps * 16) {
+        // sign words: lane r < 16 loads row r's, then each lane takes rows g and g + 8
+        uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+        if (lane < 16 && r0 + lane < n_rows) wv = __ldg(reinterpret_cast<const uint4*>(packed + (r0 + lane) * RB + IB));
+        const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t wg[4], wg8[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            wg[i] = __shfl_sync(0xFFFFFFFFu, w4[i], g);
+            wg8[i] = __shfl_sync(0xFFFFFFFFu, w4[i], g + 8);
+        }
+        // A: sgn_k as fp16 +1 (bit set) or -1; k-step kk is projections
+        // 16 kk .. 16 kk + 15, bits 16 (kk & 1) + .. of word kk / 2
+        auto pm = [](uint32_t z) { return 0x3C003C00u | ((~z & 1u) << 15) | ((~z & 2u) << 30); };
+        uint32_t a[8][4];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int b = 16 * (kk & 1) + 2 * t;
+            a[kk][0] = pm(wg[kk >> 1] >> b);
+            a[kk][1] = pm(wg8[kk >> 1] >> b);
+            a[kk][2] = pm(wg[kk >> 1] >> (b + 8));
+            a[kk][3] = pm(wg8[kk >> 1] >> (b + 8));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                uint32_t bh[4], bl[4];
+                const uint32_t off = boff + (uint32_t)((8 * nt * kQtcRow + 16 * kk) * 2);
+                qtc_ldsm4(sSh + off, bh);
+                qtc_ldsm4(sSl + off, bl);
+                qtc_mma(c, a[kk], bh[0], bh[1]);
+                qtc_mma(c, a[kk], bl[0], bl[1]);
+                qtc_mma(c, a[kk + 1], bh[2], bh[3]);
+                qtc_mma(c, a[kk + 1], bl[2], bl[3]);
+            }
+            // rows g, g + 8, dims 8 nt + 2t, + 1
+            *reinterpret_cast<float2*>(Tb + g * kQtcRow + 8 * nt + 2 * t) = make_float2(c[0], c[1]);
+            *reinterpret_cast<float2*>(Tb + (g + 8) * kQtcRow + 8 * nt + 2 * t) = make_float2(c[2], c[3]);
+        }
+        __syncwarp();
+        // ---- per row: n c[idx] + kappa gamma S^T sgn, then the inverse transform
+#pragma unroll 1
+        for (int q0 = 0; q0 < 16; q0 += 4) {
+            uint32_t ib[4];
+            float nrm[4], gk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool ok = r0 + q0 + q < n_rows;
+                const uint8_t* row = packed + (ok ? r0 + q0 + q : 0) * RB;
+                const int bit0 = lane * E * MB, wi = bit0 / 32, sh = bit0 % 32;
+                const uint32_t* iwp = reinterpret_cast<const uint32_t*>(row);
+                uint32_t v = ok ? __ldg(iwp + wi) >> sh : 0u;
+                if (ok && sh + E * MB > 32) v |= __ldg(iwp + wi + 1) << (32 - sh);
+                ib[q] = v;
+                nrm[q] = ok ? __ldg(norms + r0 + q0 + q) : 0.f;
+                gk[q] = ok ? __ldg(rnorms + r0 + q0 + q) * kappa : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (r0 + q0 + q >= n_rows) continue;  // warp-uniform
+                const float4 tv = *reinterpret_cast<const float4*>(Tb + (q0 + q) * kQtcRow + 4 * lane);
+                const float tt[E] = {tv.x, tv.y, tv.z, tv.w};
+                float v[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float c = P.cen[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
+                    v[e] = fmaf(gk[q], tt[e], nrm[q] * c);
+                    if (P.two_sided) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ P.sgn2[lane * E + e]);
+                }
+                warp_fwht<E>(v, lane);
+                TO* dst = y + (r0 + q0 + q) * D + lane * E;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float o = __uint_as_float(__float_as_uint(v[e] * P.inv_sqrt_d) ^ P.sgn[lane * E + e]);
+                    if constexpr (sizeof(TO) == 2) dst[e] = __float2bfloat16_rn(o);
+                    else dst[e] = o;
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+#endif
+
 }  // namespace dev
 
 namespace {
@@ -361,6 +662,40 @@ cudaError_t dec_qjl(const uint8_t* pk, const float* nm, const float* rn, int64_t
     return cudaGetLastError();
 }
 
+#if TQ_UNIT_D == 128
+template <int BITS, typename T>
+cudaError_t enc_qjl_tc(const void* x, int64_t n, const float* S, uint8_t* pk, float* nm, float* rn,
+                       const RowParams& P, cudaStream_t s) {
+    auto fn = dev::k_encode_qjl_tc<BITS, T>;
+    constexpr int smem = dev::kQtcEncSmem;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t per_block = (int64_t)dev::kQtcWarps * 16;
+    int64_t g = (n + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kQtcWarps, smem);
+    if (g > cap) g = cap;
+    fn<<<(unsigned)(g < 1 ? 1 : g), 32 * dev::kQtcWarps, smem, s>>>(static_cast<const T*>(x), n, S, pk, nm, rn, P);
+    return cudaGetLastError();
+}
+
+template <int BITS, typename TO>
+cudaError_t dec_qjl_tc(const uint8_t* pk, const float* nm, const float* rn, int64_t n, const float* S, void* y,
+                       const RowParams& P, cudaStream_t s) {
+    auto fn = dev::k_decode_qjl_tc<BITS, TO>;
+    constexpr int smem = dev::kQtcDecSmem;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t per_block = (int64_t)dev::kQtcWarps * 16;
+    int64_t g = (n + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)num_sms() * blocks_per_sm((const void*)fn, 32 * dev::kQtcWarps, smem);
+    if (g > cap) g = cap;
+    const float kappa = (float)(1.2533141373155003 / 128);  // sqrt(pi / 2) / d
+    fn<<<(unsigned)(g < 1 ? 1 : g), 32 * dev::kQtcWarps, smem, s>>>(pk, nm, rn, n, S, static_cast<TO*>(y), P,
+                                                                    kappa);
+    return cudaGetLastError();
+}
+#endif
+
 }  // namespace
 
 template <int D>
@@ -369,10 +704,21 @@ cudaError_t launch_encode_qjl_d(int bits, tq_dtype dt, const void* x, int64_t n_
                                 cudaStream_t s) {
     auto go = [&](auto tag) {
         using T = decltype(tag);
-        switch (bits) {
-            case 2: return enc_qjl<D, 2, T>(x, n_rows, S, packed, norms, rnorms, P, s);
-            case 3: return enc_qjl<D, 3, T>(x, n_rows, S, packed, norms, rnorms, P, s);
-            default: return enc_qjl<D, 4, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+#if TQ_UNIT_D == 128
+        if constexpr (D == 128) {  // the projections on the tensor cores
+            switch (bits) {
+                case 2: return enc_qjl_tc<2, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+                case 3: return enc_qjl_tc<3, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+                default: return enc_qjl_tc<4, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+            }
+        } else
+#endif
+        {
+            switch (bits) {
+                case 2: return enc_qjl<D, 2, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+                case 3: return enc_qjl<D, 3, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+                default: return enc_qjl<D, 4, T>(x, n_rows, S, packed, norms, rnorms, P, s);
+            }
         }
     };
     return dt == TQ_BF16 ? go(__nv_bfloat16{}) : go(float{});
@@ -384,10 +730,21 @@ cudaError_t launch_decode_qjl_d(int bits, tq_dtype dt, const uint8_t* packed, co
                                 cudaStream_t s) {
     auto go = [&](auto tag) {
         using TO = decltype(tag);
-        switch (bits) {
-            case 2: return dec_qjl<D, 2, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
-            case 3: return dec_qjl<D, 3, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
-            default: return dec_qjl<D, 4, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+#if TQ_UNIT_D == 128
+        if constexpr (D == 128) {  // the projections on the tensor cores
+            switch (bits) {
+                case 2: return dec_qjl_tc<2, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+                case 3: return dec_qjl_tc<3, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+                default: return dec_qjl_tc<4, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+            }
+        } else
+#endif
+        {
+            switch (bits) {
+                case 2: return dec_qjl<D, 2, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+                case 3: return dec_qjl<D, 3, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+                default: return dec_qjl<D, 4, TO>(packed, norms, rnorms, n_rows, S, y, P, s);
+            }
         }
     };
     return dt == TQ_BF16 ? go(__nv_bfloat16{}) : go(float{});
