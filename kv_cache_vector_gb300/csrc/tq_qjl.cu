@@ -127,11 +127,13 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
     uint8_t* ibuf = qjl_smem + QjlSmem<D>::kS + QjlSmem<D>::kR;
     uint32_t* sg = reinterpret_cast<uint32_t*>(ibuf + QjlSmem<D>::kI);
     uint32_t* sg2 = sg + D;
+    __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
     stage_matrix<D>(S, Ss);
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
         sg[i] = P.sgn[i];
         sg2[i] = P.sgn2[i];
     }
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float* rw = rbuf + warp * kQjlRows * D;
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
                 int id = 0;
 #pragma unroll
                 for (int j = 0; j < NB; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
-                const float r = fmaf(v[e], inv, -P.cen[id]);
+                const float r = fmaf(v[e], inv, -cen_s[id]);
                 rr = fmaf(r, r, rr);
                 iw[q * D + lane * E + e] = (uint8_t)id;
                 rw[q * D + lane * E + e] = r;
@@ -242,8 +244,10 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
     constexpr int kStride = QjlSmem<D>::kStride;
     extern __shared__ __align__(16) unsigned char qjl_smem[];
     float* Ss = reinterpret_cast<float*>(qjl_smem);
-    __shared__ float csum[D];  // column sums of S
+    __shared__ float csum[D];    // column sums of S
+    __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
     stage_matrix<D>(S, Ss);
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
         float c = 0.f;
@@ -252,9 +256,14 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
     }
     __syncthreads();
     float cs[E];
+    uint32_t sgl[E], sg2l[E];  // the lane's sign masks, read once (lane-varying parameter reads serialise)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-    for (int e = 0; e < E; ++e) cs[e] = csum[lane * E + e];
+    for (int e = 0; e < E; ++e) {
+        cs[e] = csum[lane * E + e];
+        sgl[e] = P.sgn[lane * E + e];
+        sg2l[e] = P.two_sided ? P.sgn2[lane * E + e] : 0u;
+    }
     for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
          r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
         uint32_t sw[kQjlRows][E];  // sign words of each row (every lane holds all)
@@ -311,15 +320,15 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
             float v[E];
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                const float c = P.cen[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
+                const float c = cen_s[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
                 v[e] = fmaf(gk[q], fmaf(2.f, t[q][e], -cs[e]), nrm[q] * c);
-                if (P.two_sided) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ P.sgn2[lane * E + e]);
+                v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2l[e]);
             }
             warp_fwht<E>(v, lane);
             TO* dst = y + (r0 + q) * D + lane * E;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                const float o = __uint_as_float(__float_as_uint(v[e] * P.inv_sqrt_d) ^ P.sgn[lane * E + e]);
+                const float o = __uint_as_float(__float_as_uint(v[e] * P.inv_sqrt_d) ^ sgl[e]);
                 if constexpr (sizeof(TO) == 2) dst[e] = __float2bfloat16_rn(o);
                 else dst[e] = o;
             }
@@ -389,9 +398,33 @@ __device__ __forceinline__ void qtc_stage_s(const float* __restrict__ S, __half*
 __device__ __forceinline__ uint32_t qtc_spread4(uint32_t e) {
     return (e & 1u) | ((e & 2u) << 1) | ((e & 4u) << 2) | ((e & 8u) << 3);
 }
+// warp_fwht and warp_sum on R rows side by side: each row's operations are
+// those of the one-row versions, and the rows' shuffles overlap.
+template <int R, int E>
+__device__ __forceinline__ void warp_fwht_rows(float (&v)[R][E], int lane) {
+#pragma unroll
+    for (int q = 0; q < R; ++q) fwht_reg<E>(v[q]);
+#pragma unroll
+    for (int b = 1; b < 32; b <<= 1) {
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float o = __shfl_xor_sync(0xFFFFFFFFu, v[q][e], b);
+                v[q][e] = (lane & b) ? o - v[q][e] : v[q][e] + o;
+            }
+    }
+}
+template <int R>
+__device__ __forceinline__ void warp_sum_rows(float (&s)[R]) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < R; ++q) s[q] += __shfl_xor_sync(0xFFFFFFFFu, s[q], o);
+}
 
 template <int BITS, typename T>
-__global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __restrict__ x, int64_t n_rows,
+__global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __restrict__ x, int64_t n_rows,
                                                                   const float* __restrict__ S,
                                                                   uint8_t* __restrict__ packed,
                                                                   float* __restrict__ norms,
@@ -404,11 +437,13 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __res
     __half* Sl = Sh + 128 * kQtcRow;
     uint32_t* sg = reinterpret_cast<uint32_t*>(qtc_smem + kQtcS + kQtcWarps * kQtcEncWarp);
     uint32_t* sg2 = sg + D;
+    __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
     qtc_stage_s<false>(S, Sh, Sl);
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
         sg[i] = P.sgn[i];
         sg2[i] = P.sgn2[i];
     }
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* wb = qtc_smem + kQtcS + warp * kQtcEncWarp;
@@ -432,30 +467,37 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __res
                     for (int e = 0; e < E; ++e) vq[q][e] = 0.f;
                 }
             }
+            float ss[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ss[q] = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) ss[q] = fmaf(vq[q][e], vq[q][e], ss[q]);
+            }
+            warp_sum_rows<4>(ss);
+            warp_fwht_rows<4, E>(vq, lane);
+            float rr[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int row = q0 + q;
                 float(&v)[E] = vq[q];
-                float ss = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
-                ss = warp_sum(ss);
-                warp_fwht<E>(v, lane);
                 if (P.two_sided) {
 #pragma unroll
                     for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
                 }
-                const float n = __fsqrt_rn(ss);
+                const float n = __fsqrt_rn(ss[q]);
+                ss[q] = n;
                 const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
-                float rr = 0.f, rs[E];
+                float rs[E];
                 uint32_t ids = 0u;
+                rr[q] = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     int id = 0;
 #pragma unroll
                     for (int j = 0; j < NB; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
-                    const float r = fmaf(v[e], inv, -P.cen[id]);
-                    rr = fmaf(r, r, rr);
+                    const float r = fmaf(v[e], inv, -cen_s[id]);
+                    rr[q] = fmaf(r, r, rr[q]);
                     ids |= (uint32_t)id << (8 * e);
                     rs[e] = r * 1024.f;  // exact; keeps the low parts out of the fp16 subnormals
                 }
@@ -465,11 +507,15 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __res
                 qtc_split2(rs[2], rs[3], h1, l1);
                 *reinterpret_cast<uint2*>(Rh + row * (kQtcRow / 2) + 2 * lane) = make_uint2(h0, h1);
                 *reinterpret_cast<uint2*>(Rl + row * (kQtcRow / 2) + 2 * lane) = make_uint2(l0, l1);
-                rr = warp_sum(rr);
-                if (lane == 0 && r0 + row < n_rows) {
-                    norms[r0 + row] = n;
-                    rnorms[r0 + row] = n * __fsqrt_rn(rr);
-                }
+            }
+            warp_sum_rows<4>(rr);
+            if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (r0 + q0 + q < n_rows) {
+                        norms[r0 + q0 + q] = ss[q];
+                        rnorms[r0 + q0 + q] = ss[q] * __fsqrt_rn(rr[q]);
+                    }
             }
         }
         __syncwarp();
@@ -522,7 +568,7 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_encode_qjl_tc(const T* __res
 }
 
 template <int BITS, typename TO>
-__global__ void __launch_bounds__(32 * kQtcWarps) k_decode_qjl_tc(const uint8_t* __restrict__ packed,
+__global__ void __launch_bounds__(32 * kQtcWarps, 1) k_decode_qjl_tc(const uint8_t* __restrict__ packed,
                                                                   const float* __restrict__ norms,
                                                                   const float* __restrict__ rnorms,
                                                                   int64_t n_rows, const float* __restrict__ S,
@@ -533,10 +579,18 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_decode_qjl_tc(const uint8_t*
     extern __shared__ __align__(16) unsigned char qtc_smem[];
     __half* Sh = reinterpret_cast<__half*>(qtc_smem);  // [dim][projection]
     __half* Sl = Sh + 128 * kQtcRow;
+    __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
     qtc_stage_s<true>(S, Sh, Sl);
+    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     float* Tb = reinterpret_cast<float*>(qtc_smem + kQtcS + warp * kQtcDecWarp);  // [16][kQtcRow]
+    uint32_t sgl[E], sg2l[E];  // the lane's sign masks, read once (lane-varying parameter reads serialise)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        sgl[e] = P.sgn[lane * E + e];
+        sg2l[e] = P.two_sided ? P.sgn2[lane * E + e] : 0u;
+    }
     const uint32_t sSh = smem_addr(Sh), sSl = smem_addr(Sl);
     const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
     for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
@@ -599,25 +653,33 @@ __global__ void __launch_bounds__(32 * kQtcWarps) k_decode_qjl_tc(const uint8_t*
                 nrm[q] = ok ? __ldg(norms + r0 + q0 + q) : 0.f;
                 gk[q] = ok ? __ldg(rnorms + r0 + q0 + q) * kappa : 0.f;
             }
+            float v[4][E];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 tv = *reinterpret_cast<const float4*>(Tb + (q0 + q) * kQtcRow + 4 * lane);
+                const float tt[E] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float c = cen_s[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
+                    v[q][e] = fmaf(gk[q], tt[e], nrm[q] * c);
+                    v[q][e] = __uint_as_float(__float_as_uint(v[q][e]) ^ sg2l[e]);
+                }
+            }
+            warp_fwht_rows<4, E>(v, lane);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (r0 + q0 + q >= n_rows) continue;  // warp-uniform
-                const float4 tv = *reinterpret_cast<const float4*>(Tb + (q0 + q) * kQtcRow + 4 * lane);
-                const float tt[E] = {tv.x, tv.y, tv.z, tv.w};
-                float v[E];
+                float o[E];
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float c = P.cen[(ib[q] >> (e * MB)) & ((1u << MB) - 1)];
-                    v[e] = fmaf(gk[q], tt[e], nrm[q] * c);
-                    if (P.two_sided) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ P.sgn2[lane * E + e]);
-                }
-                warp_fwht<E>(v, lane);
-                TO* dst = y + (r0 + q0 + q) * D + lane * E;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float o = __uint_as_float(__float_as_uint(v[e] * P.inv_sqrt_d) ^ P.sgn[lane * E + e]);
-                    if constexpr (sizeof(TO) == 2) dst[e] = __float2bfloat16_rn(o);
-                    else dst[e] = o;
+                for (int e = 0; e < E; ++e)
+                    o[e] = __uint_as_float(__float_as_uint(v[q][e] * P.inv_sqrt_d) ^ sgl[e]);
+                TO* dst = y + (r0 + q0 + q) * D + lane * E;  // 16-byte aligned rows
+                if constexpr (sizeof(TO) == 2) {
+                    const __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&a),
+                                                                *reinterpret_cast<const uint32_t*>(&b));
+                } else {
+                    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
                 }
             }
         }
