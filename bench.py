@@ -560,23 +560,15 @@ def extra_long_context(peak, with_oracle=True):
     return res
 
 
-def fp32_alu_peak_tflops():
-    """FP32 FMA peak: 152 SMs x 128 lanes x 2 flops per clock at the maximum
-    SM clock of MEASURED_PEAKS.json (2070 MHz): 80.5 TFLOP/s."""
-    mhz = 2070.0
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            mhz = float(json.load(f).get("sm_max_mhz", mhz))
-    return 152 * 128 * 2 * mhz * 1e6 / 1e12
-
-
 def extra_qjl(peak, small=False):
     """QJL residual keys at d = 128, 4 bits (3-bit MSE index + 1 sign per
     coordinate).  Codec: 1,048,576 bf16 low-rank rows with outlier channels
     (one layer of the Llama-8B-shaped prefill: 8 KV heads x 16 x 8192), encode
-    and decode, inputs above L2 (256 MB), 20 calls each; bound by the fp32
-    projection (2 d^2 flops per row).  Attention: the decode-attention
+    and decode, inputs above L2 (256 MB), 20 calls each.  The projections
+    (2 d^2 flops per row) run on the tensor cores in fp16 parts: three
+    products per tile for the encode, two for the decode; tensor_tflops counts
+    those, projection_tflops the useful 2 d^2, and frac_tensor is against the
+    measured dense bf16 (= fp16) peak.  Attention: the decode-attention
     workload (B32, Hq32/Hkv8, ctx 32768) with QJL K4 keys and plain V3 values,
     20 calls over a 1.07 GB cache; parity sample: the oracle's attention of
     one (batch, KV head) group from its own encoding of the raw rows.
@@ -590,19 +582,20 @@ def extra_qjl(peak, small=False):
     x = torch.cat([synth.lowrank_rows(77, n // 8, D, stream=h, device="cuda") for h in range(8)])
     pk, nm, rn = abi.tq_encode_qjl(plan, bits, S, x)
     y = abi.tq_decode_qjl(plan, bits, S, pk, nm, rn, torch.bfloat16)
-    alu = fp32_alu_peak_tflops()
+    tpeak, _ = measured_tensor_peak()
     res = {"config": "d128 K4 (3-bit index + QJL signs); codec 1048576 bf16 rows; attention B32 Hq32/Hkv8 "
-                     "ctx32768 K4(QJL)/V3, scale 1/sqrt(128)", "alu_peak_tflops": round(alu, 1)}
+                     "ctx32768 K4(QJL)/V3, scale 1/sqrt(128)", "tensor_peak_tflops": round(tpeak, 1)}
     cb = n * (D * 2 + D * bits // 8 + 8)
-    for name, fn in (("encode", lambda: abi.tq_encode_qjl(plan, bits, S, x)),
-                     ("decode", lambda: abi.tq_decode_qjl(plan, bits, S, pk, nm, rn, torch.bfloat16))):
+    for name, passes, fn in (("encode", 3, lambda: abi.tq_encode_qjl(plan, bits, S, x)),
+                             ("decode", 2, lambda: abi.tq_decode_qjl(plan, bits, S, pk, nm, rn, torch.bfloat16))):
         for _ in range(3):
             fn()
         ms = time_events(fn, 20)
         gbps = cb / (ms * 1e-3) / 1e9
         tf = n * 2 * D * D / (ms * 1e-3) / 1e12
         res[name] = {"ms": round(ms, 4), "GBps": round(gbps, 1), "frac_hbm": round(gbps / peak, 4),
-                     "projection_tflops": round(tf, 2), "frac_alu": round(tf / alu, 4), "repeats": 20}
+                     "projection_tflops": round(tf, 2), "tensor_tflops": round(passes * tf, 2),
+                     "frac_tensor": round(passes * tf / tpeak, 4), "repeats": 20}
     del x, y, pk, nm, rn
     B, Hq, Hkv, ctx, kb, vb = (8 if small else 32), 32, 8, 32768, 4, 3
     if small:

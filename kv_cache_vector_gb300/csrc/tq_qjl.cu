@@ -21,14 +21,15 @@
 // Box-Muller, sqrt(-2 ln(1 - U1)) cos(2 pi U2), on outputs 2d + 2k and
 // 2d + 2k + 1, U = (out >> 11) / 2^53, computed in double and stored fp32.
 //
-// Work layout (d = 32, 64, 128): a warp takes four rows at a time; lane l
-// holds the E = d/32 coordinates l E .. l E + E - 1 through the transform and
-// the projections k = l + 32 e, so that the sign bits of projection word e
-// are one warp ballot.  The block keeps S in shared memory, row-major with a
-// stride of d + 4 floats: lane reads of four consecutive floats of 32
-// different rows (encode) and of one row (decode) are both free of bank
-// conflicts.  Each S load feeds the four rows of the warp.  Blocks of 12
-// warps: two of them fit an SM by registers and by shared memory (S is 66 KB).
+// d = 128 runs the projections on the tensor cores (k_encode_qjl_tc,
+// k_decode_qjl_tc, below).  CUDA-core work layout (d = 32, 64): a warp takes
+// four rows at a time; lane l holds the E = d/32 coordinates l E .. l E + E -
+// 1 through the transform and the projections k = l + 32 e, so that the sign
+// bits of projection word e are one warp ballot.  The block keeps S in shared
+// memory, row-major with a stride of d + 4 floats: lane reads of four
+// consecutive floats of 32 different rows (encode) and of one row (decode)
+// are both free of bank conflicts.  Each S load feeds the four rows of the
+// warp.  Blocks of 12 warps.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -340,8 +341,9 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
 // ---- d = 128: the projections on the tensor cores (mma.sync m16n8k16, fp16
 // operands, fp32 accumulation), a warp taking 16 rows at a time.
 //
-// Encode: the MSE stage is the CUDA-core kernel's, row by row, so indices,
-// norms and gammas are the same.  The residuals, times 2^10, go to shared
+// Encode: the MSE stage computes what the CUDA-core kernel does, so indices,
+// norms and gammas are the same; the indices are packed by shuffles and
+// stored as soon as a row's are known.  The residuals, times 2^10, go to shared
 // memory as fp16 high and low parts, and P = R S^T is taken as R_hi S_hi +
 // R_lo S_hi + R_hi S_lo: each operand carried to about 22 bits, so a sign can
 // differ from an exact projection's only within about 1e-6 ||r|| of zero.  The
@@ -355,9 +357,14 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
 #define TQ_QJL_TC_WARPS 12
 #endif
 constexpr int kQtcWarps = TQ_QJL_TC_WARPS;
+// rows the encoder's MSE stage takes side by side
+#ifndef TQ_QJL_TC_SIDE
+#define TQ_QJL_TC_SIDE 4
+#endif
+constexpr int kQtcSide = TQ_QJL_TC_SIDE;
 constexpr int kQtcRow = 136;                                     // halves per row of an fp16 tile
 constexpr int kQtcS = 2 * 128 * kQtcRow * 2;                     // S high and low parts
-constexpr int kQtcEncWarp = 2 * 16 * kQtcRow * 2 + 16 * 128;     // residual parts, index bytes
+constexpr int kQtcEncWarp = 2 * 16 * kQtcRow * 2;                // residual parts
 constexpr int kQtcEncSmem = kQtcS + kQtcWarps * kQtcEncWarp + 2 * 128 * 4;
 constexpr int kQtcDecWarp = 16 * kQtcRow * 4;                    // S^T sgn of 16 rows, fp32
 constexpr int kQtcDecSmem = kQtcS + kQtcWarps * kQtcDecWarp;
@@ -398,6 +405,39 @@ __device__ __forceinline__ void qtc_stage_s(const float* __restrict__ S, __half*
 __device__ __forceinline__ uint32_t qtc_spread4(uint32_t e) {
     return (e & 1u) | ((e & 2u) << 1) | ((e & 4u) << 2) | ((e & 8u) << 3);
 }
+// The MB-bit indices of dims 4l .. 4l + 3, bytes of lane l's ids, into the
+// row's dense LSB-first stream at dst (16 MB bytes, 4-byte aligned): each
+// lane's 4 MB-bit field, concatenated with its neighbours' by shuffles.
+template <int MB>
+__device__ __forceinline__ void qtc_pack_indices(uint32_t ids, int lane, uint8_t* dst) {
+    const uint32_t f = (ids & 0xFFu) | (((ids >> 8) & 0xFFu) << MB) | (((ids >> 16) & 0xFFu) << (2 * MB)) |
+                       ((ids >> 24) << (3 * MB));
+    uint32_t* o = reinterpret_cast<uint32_t*>(dst);
+    if constexpr (MB == 1) {  // 4-bit fields: 8 lanes per word
+        uint32_t x = f;
+        x |= __shfl_down_sync(0xFFFFFFFFu, x, 1) << 4;
+        x |= __shfl_down_sync(0xFFFFFFFFu, x, 2) << 8;
+        x |= __shfl_down_sync(0xFFFFFFFFu, x, 4) << 16;
+        if ((lane & 7) == 0) o[lane >> 3] = x;
+    } else if constexpr (MB == 2) {  // 8-bit fields: 4 lanes per word
+        uint32_t x = f;
+        x |= __shfl_down_sync(0xFFFFFFFFu, x, 1) << 8;
+        x |= __shfl_down_sync(0xFFFFFFFFu, x, 2) << 16;
+        if ((lane & 3) == 0) o[lane >> 2] = x;
+    } else {  // 12-bit fields: 8 lanes per 3 words
+        const uint32_t p = f | (__shfl_down_sync(0xFFFFFFFFu, f, 1) << 12);  // 24 bits (even lanes)
+        const uint64_t q = (uint64_t)p | ((uint64_t)__shfl_down_sync(0xFFFFFFFFu, p, 2) << 24);  // 48 bits (lanes 4k)
+        const uint32_t plo = __shfl_down_sync(0xFFFFFFFFu, (uint32_t)q, 4);
+        const uint32_t phi = __shfl_down_sync(0xFFFFFFFFu, (uint32_t)(q >> 32), 4);
+        const uint64_t partner = ((uint64_t)phi << 32) | plo;  // lanes 4k + 4 .. 4k + 7
+        const uint64_t lo = q | (partner << 48);
+        if ((lane & 7) == 0) {
+            o[3 * (lane >> 3)] = (uint32_t)lo;
+            o[3 * (lane >> 3) + 1] = (uint32_t)(lo >> 32);
+            o[3 * (lane >> 3) + 2] = (uint32_t)(partner >> 16);
+        }
+    }
+}
 // warp_fwht and warp_sum on R rows side by side: each row's operations are
 // those of the one-row versions, and the rows' shuffles overlap.
 template <int R, int E>
@@ -437,29 +477,32 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
     __half* Sl = Sh + 128 * kQtcRow;
     uint32_t* sg = reinterpret_cast<uint32_t*>(qtc_smem + kQtcS + kQtcWarps * kQtcEncWarp);
     uint32_t* sg2 = sg + D;
-    __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
+    // centroids and boundaries by lane-varying index: shared memory, not the parameter bank
+    __shared__ float cen_s[16], bnd_s[16];
     qtc_stage_s<false>(S, Sh, Sl);
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
         sg[i] = P.sgn[i];
         sg2[i] = P.sgn2[i];
     }
-    if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
+    if (threadIdx.x < 16) {
+        cen_s[threadIdx.x] = P.cen[threadIdx.x];
+        bnd_s[threadIdx.x] = threadIdx.x < NB ? P.bnd[threadIdx.x] : 0.f;
+    }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char* wb = qtc_smem + kQtcS + warp * kQtcEncWarp;
     uint32_t* Rh = reinterpret_cast<uint32_t*>(wb);                       // [16][kQtcRow / 2] half pairs
     uint32_t* Rl = Rh + 16 * kQtcRow / 2;
-    uint8_t* iw = wb + 2 * 16 * kQtcRow * 2;                               // [16][128] index bytes
     const uint32_t sRh = smem_addr(Rh), sRl = smem_addr(Rl), sSh = smem_addr(Sh), sSl = smem_addr(Sl);
     for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
          r0 += (int64_t)gridDim.x * kQtcWarps * 16) {
-        // ---- MSE stage and residual of each row, four rows at a time (their
-        // loads first; rows past the end: zeros)
+        // ---- MSE stage and residual of each row, kQtcSide rows side by side
+        // (their loads first; rows past the end: zeros)
 #pragma unroll 1
-        for (int q0 = 0; q0 < 16; q0 += 4) {
-            float vq[4][E];
+        for (int q0 = 0; q0 < 16; q0 += kQtcSide) {
+            float vq[kQtcSide][E];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kQtcSide; ++q) {
                 if (r0 + q0 + q < n_rows) {
                     load_lane<E, T>(x + (r0 + q0 + q) * D, lane, sg, vq[q]);
                 } else {
@@ -467,18 +510,18 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
                     for (int e = 0; e < E; ++e) vq[q][e] = 0.f;
                 }
             }
-            float ss[4];
+            float ss[kQtcSide];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kQtcSide; ++q) {
                 ss[q] = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) ss[q] = fmaf(vq[q][e], vq[q][e], ss[q]);
             }
-            warp_sum_rows<4>(ss);
-            warp_fwht_rows<4, E>(vq, lane);
-            float rr[4];
+            warp_sum_rows<kQtcSide>(ss);
+            warp_fwht_rows<kQtcSide, E>(vq, lane);
+            float rr[kQtcSide];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kQtcSide; ++q) {
                 const int row = q0 + q;
                 float(&v)[E] = vq[q];
                 if (P.two_sided) {
@@ -493,25 +536,29 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
                 rr[q] = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
+                    // the number of boundaries at or below the coordinate; the
+                    // test is monotone in the boundary, so a binary search
+                    // finds the count
                     int id = 0;
 #pragma unroll
-                    for (int j = 0; j < NB; ++j) id += fmaf(v[e], inv, -P.bnd[j]) >= 0.0f ? 1 : 0;
+                    for (int step = (NB + 1) / 2; step >= 1; step >>= 1)
+                        if (fmaf(v[e], inv, -bnd_s[id + step - 1]) >= 0.0f) id += step;
                     const float r = fmaf(v[e], inv, -cen_s[id]);
                     rr[q] = fmaf(r, r, rr[q]);
                     ids |= (uint32_t)id << (8 * e);
                     rs[e] = r * 1024.f;  // exact; keeps the low parts out of the fp16 subnormals
                 }
-                reinterpret_cast<uint32_t*>(iw + row * D)[lane] = ids;
+                if (r0 + row < n_rows) qtc_pack_indices<MB>(ids, lane, packed + (r0 + row) * RB);  // warp-uniform
                 uint32_t h0, l0, h1, l1;
                 qtc_split2(rs[0], rs[1], h0, l0);
                 qtc_split2(rs[2], rs[3], h1, l1);
                 *reinterpret_cast<uint2*>(Rh + row * (kQtcRow / 2) + 2 * lane) = make_uint2(h0, h1);
                 *reinterpret_cast<uint2*>(Rl + row * (kQtcRow / 2) + 2 * lane) = make_uint2(l0, l1);
             }
-            warp_sum_rows<4>(rr);
+            warp_sum_rows<kQtcSide>(rr);
             if (lane == 0) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < kQtcSide; ++q)
                     if (r0 + q0 + q < n_rows) {
                         norms[r0 + q0 + q] = ss[q];
                         rnorms[r0 + q0 + q] = ss[q] * __fsqrt_rn(rr[q]);
@@ -530,39 +577,39 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
                 qtc_ldsm4(sRl + off + 32u * kk, al[kk]);
             }
         }
-        uint32_t wd[4] = {0u, 0u, 0u, 0u};  // lane r < 16: the sign words of row r
         const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < 8; kk += 2) {
-                uint32_t bh[4], bl[4];
-                const uint32_t off = boff + (uint32_t)((8 * nt * kQtcRow + 16 * kk) * 2);
-                qtc_ldsm4(sSh + off, bh);  // k-steps kk (regs 0, 1) and kk + 1 (regs 2, 3)
-                qtc_ldsm4(sSl + off, bl);
-                qtc_mma(c, ah[kk], bh[0], bh[1]);
-                qtc_mma(c, al[kk], bh[0], bh[1]);
-                qtc_mma(c, ah[kk], bl[0], bl[1]);
-                qtc_mma(c, ah[kk + 1], bh[2], bh[3]);
-                qtc_mma(c, al[kk + 1], bh[2], bh[3]);
-                qtc_mma(c, ah[kk + 1], bl[2], bl[3]);
-            }
-            // c: rows g, g + 8, projections 8 nt + 2t, 8 nt + 2t + 1 (lane 4g + t)
-            const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, c[0] >= 0.f), b1 = __ballot_sync(0xFFFFFFFFu, c[1] >= 0.f);
-            const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, c[2] >= 0.f), b3 = __ballot_sync(0xFFFFFFFFu, c[3] >= 0.f);
-            const uint32_t sh = 4u * (uint32_t)(lane & 7);
-            const uint32_t e0 = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, e1 = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
-            wd[nt >> 2] |= (qtc_spread4(e0) | (qtc_spread4(e1) << 1)) << (8 * (nt & 3));
-        }
-        // ---- stores: each row's indices, then its sign words
+        // sign word w of each row: projections 32 w .. 32 w + 31, four tiles
 #pragma unroll 1
-        for (int q = 0; q < 16; ++q) {
-            if (r0 + q >= n_rows) break;  // warp-uniform
-            warp_pack_row<D>(iw + q * D, lane, MB, packed + (r0 + q) * RB);
+        for (int w = 0; w < 4; ++w) {
+            uint32_t word = 0u;  // lane r < 16: row r's
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int nt = 4 * w + j;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < 8; kk += 2) {
+                    uint32_t bh[4], bl[4];
+                    const uint32_t off = boff + (uint32_t)((8 * nt * kQtcRow + 16 * kk) * 2);
+                    qtc_ldsm4(sSh + off, bh);  // k-steps kk (regs 0, 1) and kk + 1 (regs 2, 3)
+                    qtc_ldsm4(sSl + off, bl);
+                    qtc_mma(c, ah[kk], bh[0], bh[1]);
+                    qtc_mma(c, al[kk], bh[0], bh[1]);
+                    qtc_mma(c, ah[kk], bl[0], bl[1]);
+                    qtc_mma(c, ah[kk + 1], bh[2], bh[3]);
+                    qtc_mma(c, al[kk + 1], bh[2], bh[3]);
+                    qtc_mma(c, ah[kk + 1], bl[2], bl[3]);
+                }
+                // c: rows g, g + 8, projections 8 nt + 2t, 8 nt + 2t + 1 (lane 4g + t)
+                const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, c[0] >= 0.f);
+                const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, c[1] >= 0.f);
+                const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, c[2] >= 0.f);
+                const uint32_t b3 = __ballot_sync(0xFFFFFFFFu, c[3] >= 0.f);
+                const uint32_t sh = 4u * (uint32_t)(lane & 7);
+                const uint32_t e0 = ((lane < 8 ? b0 : b2) >> sh) & 0xFu, e1 = ((lane < 8 ? b1 : b3) >> sh) & 0xFu;
+                word |= (qtc_spread4(e0) | (qtc_spread4(e1) << 1)) << (8 * j);
+            }
+            if (lane < 16 && r0 + lane < n_rows) reinterpret_cast<uint32_t*>(packed + (r0 + lane) * RB + IB)[w] = word;
         }
-        if (lane < 16 && r0 + lane < n_rows)
-            *reinterpret_cast<uint4*>(packed + (r0 + lane) * RB + IB) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         __syncwarp();
     }
 }
