@@ -92,6 +92,31 @@ def test_encode_parity_ragged(d, bits, dtype):
                       rn.cpu().numpy())
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_codec_parity_several_grid_passes(bits):
+    """d = 128, 40,001 bf16 low-rank rows with outlier channels: more rows
+    than one pass of the persistent grid takes (152 blocks of 12 warps x 16
+    rows), with a ragged last group.  Encode against the oracle as above;
+    decode of the library's own encoding against the oracle's decode of the
+    same bytes."""
+    d, n = 128, 40001
+    plan = abi.Plan(d, 42)
+    S32 = _s32(42, d)
+    Sd = torch.from_numpy(S32).cuda()
+    x = synth.lowrank_rows(1500 + bits, n, d)
+    pk, nm, rn = abi.tq_encode_qjl(plan, bits, Sd, x.cuda())
+    torch.cuda.synchronize()
+    pk, nm, rn = pk.cpu().numpy(), nm.cpu().numpy(), rn.cpu().numpy()
+    s = O.signs(42, d)
+    _check_qjl_encode(s, bits, x.double().numpy(), S32, pk, nm, rn)
+    y = abi.tq_decode_qjl(plan, bits, Sd, torch.from_numpy(pk).cuda(), torch.from_numpy(nm).cuda(),
+                          torch.from_numpy(rn).cuda(), torch.float32)
+    torch.cuda.synchronize()
+    want = O.decode_qjl(s, bits, pk, nm, rn, S32.astype(np.float64))
+    tol = DECODE_REL * np.linalg.norm(want, axis=1, keepdims=True) / math.sqrt(d)
+    assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - want) <= tol)
+
+
 @pytest.mark.parametrize("flags", [abi.PLAN_TWO_SIDED_SIGNS, abi.PLAN_GAUSSIAN_CODEBOOK | abi.PLAN_TWO_SIDED_SIGNS])
 def test_encode_parity_format_variants(flags):
     d, bits = 128, 3
