@@ -24,6 +24,7 @@
 // log2(GP) shuffle steps halves the set of heads a lane carries, so the GP
 // sums cost GP - 1 + 5 - log2(GP) shuffles (6 for GP = 4) instead of 5 GP.
 #include <cfloat>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 
@@ -128,6 +129,28 @@ __device__ __forceinline__ int head_of(int lane) {
     else return ((lane >> 2) & 4) | ((lane >> 2) & 2) | ((lane >> 2) & 1);
 }
 
+// Thread-block clusters: the CTA's rank in its cluster, a shared-memory
+// address of another CTA of the cluster, a load from it, and a barrier of
+// every thread of the cluster (release / acquire).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The generic split kernel.  D: head dimension; KB, VB: K and V widths (for
 // QJL keys KB is the total width: a (KB - 1)-bit index per coordinate, then
 // d sign bits of the projected residual, with k_rnorm holding gamma; the score
@@ -136,12 +159,17 @@ __device__ __forceinline__ int head_of(int lane) {
 // positions through the block table; the sequence's length is lens[b] +
 // len_plus clamped to [0, ctx_len] (len_plus = 1 when lens holds the
 // positions just appended).  GP: the group size rounded up (2, 4 or 8).
-template <int D, int KB, int VB, bool PAGED, bool QJL, int GP>
+// CL: the splits of one (batch, KV head) form a thread-block cluster (at most
+// 8); after its partial each CTA waits at a cluster barrier, and the CTA of
+// rank 0 merges the partials straight from its peers' shared memory into
+// out, as k_attn_combine would from the workspace; a second barrier keeps
+// the peers' memory until it has.
+template <int D, int KB, int VB, bool PAGED, bool QJL, int GP, bool CL = false>
 __global__ void __launch_bounds__(kAttnThreads, 2)
 k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view cache, int64_t ctx_len,
              int split_len, int n_splits, float* __restrict__ ws, const __grid_constant__ AttnParams P,
              const PagedArgs pa, int len_plus, int* status, const float* __restrict__ qpre,
-             const float* __restrict__ k_rnorm) {
+             const float* __restrict__ k_rnorm, float* __restrict__ out) {
     // the previous kernel in the stream may have written the cache or the
     // queries: wait for it, then let the combine be scheduled
     griddep_wait();
@@ -178,7 +206,7 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
     uint8_t* keep = reinterpret_cast<uint8_t*>(kg + split_len);  // [split_len] (sparse V)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (len == 0) {  // block-uniform: an empty partial
+    if (!CL && len == 0) {  // block-uniform: an empty partial (in a cluster the body below gives it)
         for (int i = tid; i < G * (D + 2); i += blockDim.x) {
             const int h = i / (D + 2), j = i % (D + 2);
             ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = j == D ? -FLT_MAX : 0.f;
@@ -396,11 +424,53 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         }
         __syncthreads();
     }
-    // ---- partials: ws[b][h][split][D + 2] = acc..., m, l
-    for (int i = tid; i < G * (D + 2); i += blockDim.x) {
-        const int h = i / (D + 2), j = i % (D + 2);
-        const float v = j < D ? accs[h * D + j] : (j == D ? mh[h] : lh[h]);
-        ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = v;
+    if constexpr (!CL) {
+        // ---- partials: ws[b][h][split][D + 2] = acc..., m, l
+        for (int i = tid; i < G * (D + 2); i += blockDim.x) {
+            const int h = i / (D + 2), j = i % (D + 2);
+            const float v = j < D ? accs[h * D + j] : (j == D ? mh[h] : lh[h]);
+            ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = v;
+        }
+    } else {
+        // ---- merge in rank 0: the same arithmetic as k_attn_combine, the
+        // splits in rank order (rank = split)
+        __shared__ float cml[2][8][kMaxGroup];  // rank 0: every split's m and l
+        cluster_sync_all();  // every partial is in its CTA's shared memory
+        if (cluster_rank() == 0) {
+            const uint32_t a_accs = smem_addr(accs);
+            if (tid < G * n_splits) {
+                const int r = tid / G, h = tid % G;
+                cml[0][r][h] = ld_cluster_f32(cluster_map(smem_addr(mh + h), r));
+                cml[1][r][h] = ld_cluster_f32(cluster_map(smem_addr(lh + h), r));
+            }
+            __syncthreads();
+            float* o = qrot;  // [G][D], free since pass 1
+            for (int i = tid; i < G * D; i += blockDim.x) {
+                const int h = i / D, j = i % D;
+                float x[8];  // the splits' accumulators, loads all in flight
+#pragma unroll
+                for (int r = 0; r < 8; ++r) x[r] = r < n_splits ? ld_cluster_f32(cluster_map(a_accs + 4u * i, r)) : 0.f;
+                float M = -FLT_MAX;
+                for (int r = 0; r < n_splits; ++r) M = fmaxf(M, cml[0][r][h]);
+                float L = 0.f, a = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (r < n_splits) {
+                        const float f = __expf(cml[0][r][h] - M);
+                        L = fmaf(f, cml[1][r][h], L);
+                        a = fmaf(f, x[r], a);
+                    }
+                }
+                const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
+                o[i] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? P.sgn2[j] : 0u));
+            }
+            fwht_smem<D>(o, G);  // synchronises the CTA first
+            for (int i = tid; i < G * D; i += blockDim.x) {
+                const int h = i / D, j = i % D;
+                out[((int64_t)b * Hq + g * G + h) * D + j] = __uint_as_float(__float_as_uint(o[i] * P.inv_sqrt_d) ^ P.sgn[j]);
+            }
+        }
+        cluster_sync_all();  // the peers' memory stays until rank 0 has read it
     }
 }
 
@@ -475,23 +545,61 @@ constexpr size_t split_smem(int split_len) {
            (size_t)split_len * (D * KB / 8 + D * VB / 8 + 3 * sizeof(float) + 1);
 }
 
+// A launch with programmatic stream serialization and, cx > 0, clusters of
+// cx CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               unsigned cx, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cx;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cx > 0 ? 2 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The split kernel, then, unless its splits merge inside their cluster, the
+// combine.  A cluster launch that the device refuses (a cluster it cannot
+// place) is retried without clusters.
 template <int D, int KB, int VB, bool PAGED, bool QJL>
 cudaError_t split_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_view& cache, int64_t ctx_len,
-                         float* part, const AttnGeometry& geo, const AttnParams& P, cudaStream_t s,
+                         float* part, float* out, const AttnGeometry& geo, const AttnParams& P, cudaStream_t s,
                          const PagedArgs& pa, int len_plus, const float* qpre, const float* k_rnorm) {
     const int G = Hq / Hkv;
     const size_t smem = split_smem<D, KB, VB>(geo.split_len);
     dim3 grid(geo.n_splits, Hkv, B);
-    auto go = [&](auto fn) {
+    auto go = [&](auto fn, unsigned cx) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(fn, grid, dim3(kAttnThreads), smem, s, static_cast<const __nv_bfloat16*>(q), Hq, Hkv,
-                          cache, ctx_len, geo.split_len, geo.n_splits, part, P, pa, len_plus, status_word(), qpre,
-                          k_rnorm);
+        return launch_pdl_cluster(fn, grid, dim3(kAttnThreads), smem, s, cx, static_cast<const __nv_bfloat16*>(q),
+                                  Hq, Hkv, cache, ctx_len, geo.split_len, geo.n_splits, part, P, pa, len_plus,
+                                  status_word(), qpre, k_rnorm, out);
     };
-    if (G <= 2) return go(k_attn_split<D, KB, VB, PAGED, QJL, 2>);
-    if (G <= 4) return go(k_attn_split<D, KB, VB, PAGED, QJL, 4>);
-    return go(k_attn_split<D, KB, VB, PAGED, QJL, 8>);
+    auto pick = [&](auto cl) {
+        constexpr bool C = decltype(cl)::value;
+        const unsigned cx = C ? (unsigned)geo.n_splits : 0u;
+        if (G <= 2) return go(k_attn_split<D, KB, VB, PAGED, QJL, 2, C>, cx);
+        if (G <= 4) return go(k_attn_split<D, KB, VB, PAGED, QJL, 4, C>, cx);
+        return go(k_attn_split<D, KB, VB, PAGED, QJL, 8, C>, cx);
+    };
+    if (geo.cluster) {
+        const cudaError_t e = pick(std::true_type{});
+        if (e != cudaErrorInvalidClusterSize && e != cudaErrorLaunchOutOfResources) return e;
+        cudaGetLastError();  // not a sticky error: take the two-launch path
+    }
+    cudaError_t e = pick(std::false_type{});
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_attn_combine<D>, dim3(B * Hq), dim3(D), 0, s, (const float*)part, geo.n_splits, out, P);
 }
 
 template <int D, int KB, int VB, bool PAGED = false>
@@ -500,14 +608,13 @@ cudaError_t attn_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_vi
                         const AttnParams& P, cudaStream_t s, const PagedArgs& pa = PagedArgs{},
                         int len_plus = 0) {
     float* part = static_cast<float*>(ws);
-    cudaError_t e = split_launch<D, KB, VB, PAGED, false>(q, B, Hq, Hkv, cache, ctx_len, part, geo, P, s, pa,
-                                                          len_plus, nullptr, nullptr);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_attn_combine<D>, dim3(B * Hq), dim3(D), 0, s, (const float*)part, geo.n_splits, out, P);
+    return split_launch<D, KB, VB, PAGED, false>(q, B, Hq, Hkv, cache, ctx_len, part, out, geo, P, s, pa, len_plus,
+                                                 nullptr, nullptr);
 }
 
 // QJL keys (contiguous cache): the query prologue, the split kernel with QJL
-// scoring over the workspace after the prologue's qpre, and the combine.
+// scoring over the workspace after the prologue's qpre, and (without
+// clusters) the combine.
 template <int D, int KB, int VB>
 cudaError_t attn_qjl_launch(const void* q, const float* S, int B, int Hq, int Hkv, const tq_cache_view& cache,
                             const float* k_rnorm, int64_t ctx_len, float* out, void* ws, const AttnGeometry& geo,
@@ -517,10 +624,8 @@ cudaError_t attn_qjl_launch(const void* q, const float* S, int B, int Hq, int Hk
     cudaError_t e = launch_pdl(k_qjl_query<D>, dim3(B * Hq), dim3(D), 0, s, static_cast<const __nv_bfloat16*>(q), S,
                                qpre, P, (float)(1.2533141373155003 / D));
     if (e != cudaSuccess) return e;
-    e = split_launch<D, KB, VB, false, true>(q, B, Hq, Hkv, cache, ctx_len, part, geo, P, s, PagedArgs{}, 0, qpre,
-                                             k_rnorm);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_attn_combine<D>, dim3(B * Hq), dim3(D), 0, s, (const float*)part, geo.n_splits, out, P);
+    return split_launch<D, KB, VB, false, true>(q, B, Hq, Hkv, cache, ctx_len, part, out, geo, P, s, PagedArgs{}, 0,
+                                                qpre, k_rnorm);
 }
 
 }  // namespace dev

@@ -215,10 +215,11 @@ constexpr int attn3_warps(int G, int kb, int vb, bool sparse = false, bool qjl =
 
 struct AttnGeometry {
     int n_splits;
-    int split_len;    // positions per split
-    int parts;        // partials written per split
-    int warp_len;     // d = 128: positions per warp and split
-    bool q16;         // the workspace starts with the rotated fp16 queries
+    int split_len;         // positions per split
+    int parts;             // partials written per split
+    int warp_len;          // d = 128: positions per warp and split
+    bool q16;              // the workspace starts with the rotated fp16 queries
+    bool cluster = false;  // other d: the splits of a (batch, KV head) form one cluster (<= 8)
 };
 // `sparse`: the call has a sparse-V threshold (the d = 128 kernel then runs
 // its sparse variant, with its own warp count).

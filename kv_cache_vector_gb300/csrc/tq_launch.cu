@@ -123,9 +123,20 @@ AttnGeometry attn_geometry(int B, int Hq, int Hkv, int64_t ctx_len, int sms, int
     // positions (256 at d = 256) keep two CTAs per SM
     int split = d > 128 ? 256 : 512;
     const int64_t want = 2LL * (sms > 0 ? sms : 1);
+    const int cap = split;
     while (split > TQ_ATTN_MIN_SPLIT && pairs * ((ctx_len + split - 1) / split) < want) split /= 2;
     g.split_len = split;
     g.n_splits = (int)((ctx_len + split - 1) / split);
+    // At most 8 splits form one thread-block cluster and are merged inside it
+    // (no combine launch).  Just past 8, take 8 splits of up to 5/4 the length.
+    if (g.n_splits > 8) {
+        const int64_t s8 = (ctx_len + 7) / 8;
+        if (s8 <= cap && 4 * s8 <= 5 * (int64_t)split) {
+            g.split_len = (int)s8;
+            g.n_splits = (int)((ctx_len + s8 - 1) / s8);
+        }
+    }
+    g.cluster = g.n_splits <= 8;
     g.parts = 1;
     g.warp_len = 0;
     g.q16 = false;
