@@ -285,9 +285,12 @@ void tq::set_last_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
 void tq::fill_attn_params(const Plan& P, int k_bits, int v_bits, float scale, float sparse_thr,
                           AttnParams& A) {
+    for (int w = 0; w < kMaxD / 32; ++w) A.sgnb[w] = A.sgn2b[w] = 0u;
     for (int i = 0; i < kMaxD; ++i) {
         A.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
         A.sgn2[i] = (i < P.d && P.signs2[i] < 0) ? 0x80000000u : 0u;
+        if (A.sgn[i]) A.sgnb[i >> 5] |= 1u << (i & 31);
+        if (A.sgn2[i]) A.sgn2b[i >> 5] |= 1u << (i & 31);
     }
     A.two_sided = (P.flags & TQ_PLAN_TWO_SIDED_SIGNS) ? 1 : 0;
     for (int i = 0; i < 16; ++i) {

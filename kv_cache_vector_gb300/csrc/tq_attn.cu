@@ -273,7 +273,7 @@ __device__ __forceinline__ void attn3_q_warp(const __nv_bfloat16* __restrict__ q
         x[3] = c.y;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(__float_as_uint(x[k]) ^ P.sgn[4 * lane + k]);
+    for (int k = 0; k < 4; ++k) x[k] = __uint_as_float(__float_as_uint(x[k]) ^ sign_mask(P.sgnb, 4 * lane + k));
     {
         const float a0 = x[0] + x[1], a1 = x[0] - x[1], a2 = x[2] + x[3], a3 = x[2] - x[3];
         x[0] = a0 + a2;
@@ -293,7 +293,7 @@ __device__ __forceinline__ void attn3_q_warp(const __nv_bfloat16* __restrict__ q
     float M = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? P.sgn2[4 * lane + k] : 0u));
+        x[k] = __uint_as_float(__float_as_uint(x[k]) ^ (P.two_sided ? sign_mask(P.sgn2b, 4 * lane + k) : 0u));
         if (y_out) y_out[k] = x[k];
         x[k] *= P.q_mul;
         M = fmaxf(M, fabsf(x[k]));
@@ -358,8 +358,8 @@ static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat
     __shared__ uint8_t ib[2][128];
     griddep_launch();
     const int j = threadIdx.x;
-    sg[j] = P.sgn[j];
-    sg2[j] = P.sgn2[j];
+    sg[j] = sign_mask(P.sgnb, j);
+    sg2[j] = sign_mask(P.sgn2b, j);
     const int b = blockIdx.x / Hq, h = blockIdx.x - b * Hq, G = Hq / Hkv;
     const int64_t p = __ldg(pa.lens + b);
     if (h == 0 && j == 0) len1[b] = p < 0 ? 0 : (p >= INT32_MAX ? INT32_MAX : (int32_t)(p + 1));
@@ -1351,7 +1351,7 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
     const int dim[4] = {2 * lane, 2 * lane + 1, 64 + 2 * lane, 65 + 2 * lane};
     if (P.two_sided) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = __uint_as_float(__float_as_uint(v[k]) ^ P.sgn2[dim[k]]);
+        for (int k = 0; k < 4; ++k) v[k] = __uint_as_float(__float_as_uint(v[k]) ^ sign_mask(P.sgn2b, dim[k]));
     }
     {  // index bit 0
         const float p0 = v[0] + v[1], p1 = v[0] - v[1], p2 = v[2] + v[3], p3 = v[2] - v[3];
@@ -1378,10 +1378,10 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
     }
     float* o = out + bh * 128;
     float2 r0, r1;
-    r0.x = __uint_as_float(__float_as_uint(v[0] * P.inv_sqrt_d) ^ P.sgn[dim[0]]);
-    r0.y = __uint_as_float(__float_as_uint(v[1] * P.inv_sqrt_d) ^ P.sgn[dim[1]]);
-    r1.x = __uint_as_float(__float_as_uint(v[2] * P.inv_sqrt_d) ^ P.sgn[dim[2]]);
-    r1.y = __uint_as_float(__float_as_uint(v[3] * P.inv_sqrt_d) ^ P.sgn[dim[3]]);
+    r0.x = __uint_as_float(__float_as_uint(v[0] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, dim[0]));
+    r0.y = __uint_as_float(__float_as_uint(v[1] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, dim[1]));
+    r1.x = __uint_as_float(__float_as_uint(v[2] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, dim[2]));
+    r1.y = __uint_as_float(__float_as_uint(v[3] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, dim[3]));
     reinterpret_cast<float2*>(o)[lane] = r0;
     reinterpret_cast<float2*>(o + 64)[lane] = r1;
 }

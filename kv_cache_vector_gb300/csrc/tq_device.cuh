@@ -106,6 +106,12 @@ __device__ __forceinline__ void load_signed(const __nv_bfloat16* __restrict__ sr
 
 // ------------------------------------------------------------------ FWHT
 
+// The xor mask of sign j (0x80000000 for a negative sign) from its bit in
+// 32-bit words (AttnParams::sgnb / sgn2b).
+__device__ __forceinline__ uint32_t sign_mask(const uint32_t* bits, int j) {
+    return ((bits[j >> 5] >> (j & 31)) & 1u) << 31;
+}
+
 // Unnormalised butterfly over the E registers: stages len = 1 .. E/2,
 // (a, b) -> (a + b, a - b).  Every loop has a constant trip count (stage st,
 // butterfly q; the pair is (i, i + 2^st) with i = q with a zero bit inserted
@@ -475,9 +481,9 @@ __device__ __forceinline__ void rotate_q_row(const __nv_bfloat16* __restrict__ q
     __shared__ float wmax[4];
     const int j = threadIdx.x;
     const float x = __bfloat162float(q_row[j]);
-    v[j] = __uint_as_float(__float_as_uint(x) ^ P.sgn[j]);
+    v[j] = __uint_as_float(__float_as_uint(x) ^ sign_mask(P.sgnb, j));
     fwht_smem<128>(v, 1);
-    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? P.sgn2[j] : 0u)) * P.q_mul;
+    const float y = __uint_as_float(__float_as_uint(v[j]) ^ (P.two_sided ? sign_mask(P.sgn2b, j) : 0u)) * P.q_mul;
     float a = fabsf(y);
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
     if ((j & 31) == 0) wmax[j >> 5] = a;

@@ -48,6 +48,12 @@ struct AttnParams {
     float out_mul;
     int two_sided;  // as RowParams
     uint32_t sgn2[kMaxD];
+    // The same signs one bit each (bit j of word j / 32 set: element j
+    // negative).  A warp whose lanes take consecutive elements reads one or a
+    // few words, where a per-element array read would take one parameter-bank
+    // access per distinct lane address.
+    uint32_t sgnb[kMaxD / 32];
+    uint32_t sgn2b[kMaxD / 32];
     // [B][Hkv] rows whose V bytes the call read (zeroed before the launch),
     // or nullptr
     int32_t* v_rows;
