@@ -144,7 +144,9 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    // volatile: kept after the cluster barrier (also volatile); no memory
+    // clobber, so the loads of several ranks are issued back to back
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ void cluster_sync_all() {
@@ -447,9 +449,10 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
             float* o = qrot;  // [G][D], free since pass 1
             for (int i = tid; i < G * D; i += blockDim.x) {
                 const int h = i / D, j = i % D;
-                float x[8];  // the splits' accumulators, loads all in flight
+                float x[8];  // the splits' accumulators, loads all in flight (ranks past the last: the last)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) x[r] = r < n_splits ? ld_cluster_f32(cluster_map(a_accs + 4u * i, r)) : 0.f;
+                for (int r = 0; r < 8; ++r)
+                    x[r] = ld_cluster_f32(cluster_map(a_accs + 4u * i, (uint32_t)(r < n_splits ? r : n_splits - 1)));
                 float M = -FLT_MAX;
                 for (int r = 0; r < n_splits; ++r) M = fmaxf(M, cml[0][r][h]);
                 float L = 0.f, a = 0.f;
