@@ -149,6 +149,9 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -437,15 +440,13 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         // ---- merge in rank 0: the same arithmetic as k_attn_combine, the
         // splits in rank order (rank = split)
         __shared__ float cml[2][8][kMaxGroup];  // rank 0: every split's m and l
-        cluster_sync_all();  // every partial is in its CTA's shared memory
+        if (tid < G) {  // handed to rank 0 before the barrier (remote stores)
+            st_cluster_f32(cluster_map(smem_addr(&cml[0][split][tid]), 0), mh[tid]);
+            st_cluster_f32(cluster_map(smem_addr(&cml[1][split][tid]), 0), lh[tid]);
+        }
+        cluster_sync_all();  // every partial is in its CTA's shared memory, m and l in rank 0's
         if (cluster_rank() == 0) {
             const uint32_t a_accs = smem_addr(accs);
-            if (tid < G * n_splits) {
-                const int r = tid / G, h = tid % G;
-                cml[0][r][h] = ld_cluster_f32(cluster_map(smem_addr(mh + h), r));
-                cml[1][r][h] = ld_cluster_f32(cluster_map(smem_addr(lh + h), r));
-            }
-            __syncthreads();
             float* o = qrot;  // [G][D], free since pass 1
             for (int i = tid; i < G * D; i += blockDim.x) {
                 const int h = i / D, j = i % D;
