@@ -25,9 +25,6 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 // A pointer the GPU cannot dereference (pageable host memory on a system
 // without pageable-memory access) is turned into an error instead of a fault.
-// Unknown answers are let through.
-// A pointer the GPU cannot dereference (pageable host memory on a system
-// without pageable-memory access) is turned into an error instead of a fault.
 // Unknown answers are let through.  Where the device reads pageable memory
 // every pointer qualifies, so no per-pointer query is made (the answer is
 // cached per device).
@@ -191,9 +188,12 @@ bool lut_exact(const float* b32, int nb) {
 }
 
 void fill_row_params(const tq::Plan& P, int bits, tq::RowParams& R) {
+    for (int w = 0; w < tq::kMaxD / 32; ++w) R.sgnb[w] = R.sgn2b[w] = 0u;
     for (int i = 0; i < tq::kMaxD; ++i) {
         R.sgn[i] = (i < P.d && P.signs[i] < 0) ? 0x80000000u : 0u;
         R.sgn2[i] = (i < P.d && P.signs2[i] < 0) ? 0x80000000u : 0u;
+        if (R.sgn[i]) R.sgnb[i >> 5] |= 1u << (i & 31);
+        if (R.sgn2[i]) R.sgn2b[i >> 5] |= 1u << (i & 31);
     }
     R.two_sided = (P.flags & TQ_PLAN_TWO_SIDED_SIGNS) ? 1 : 0;
     for (int i = 0; i < 16; ++i) {

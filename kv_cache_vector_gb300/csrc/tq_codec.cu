@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(32 * kAppWarps) k_append_warp(const T* __restr
     const bool is_v = blockIdx.y == 1;
     const RowParams& P = is_v ? PV : PK;
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        sg[i] = P.sgn[i];
-        sg2[i] = P.sgn2[i];
+        sg[i] = sign_mask(P.sgnb, i);
+        sg2[i] = sign_mask(P.sgn2b, i);
     }
     __syncthreads();
     griddep_wait();    // the new rows, and readers of the cache, of the previous kernel
@@ -524,12 +524,13 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
     // B operand: element (n, k) = s2_n * (-1)^popcount(n & k) * s_k (s2 all
     // +1 unless the signs are two-sided), stored like a TMA 128-byte-swizzled
     // K-major tile (two 64-column halves of 16 KB).  The sign masks are staged
-    // in shared memory first: indexed reads of the parameter bank with a
-    // different index per lane would be serialised.
+    // in shared memory first, from the bit words (a warp reads one word):
+    // indexed reads of the parameter bank with a different index per lane
+    // would be serialised.
     uint32_t* sg = reinterpret_cast<uint32_t*>(at(kUmSgnAt));
     for (int i = threadIdx.x; i < 128; i += blockDim.x) {
-        sg[i] = P.sgn[i];
-        sg[128 + i] = P.sgn2[i];
+        sg[i] = sign_mask(P.sgnb, i);
+        sg[128 + i] = sign_mask(P.sgn2b, i);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
@@ -789,11 +790,11 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
     uint32_t* sg = reinterpret_cast<uint32_t*>(at(kU2SgnAt));
     const uint32_t* sg2 = sg + 256;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // the sign masks, once per thread from the parameter bank (indexed reads
+    // the sign masks, from the bit words of the parameter bank (indexed reads
     // of it with a different index per lane would be serialised)
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-        sg[i] = P.sgn[i];
-        sg[256 + i] = P.sgn2[i];
+        sg[i] = sign_mask(P.sgnb, i);
+        sg[256 + i] = sign_mask(P.sgn2b, i);
         reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2);
     }
 

@@ -25,6 +25,8 @@ struct RowParams {
     // applied after the forward transform and before the inverse one.
     int two_sided;
     uint32_t sgn2[kMaxD];
+    uint32_t sgnb[kMaxD / 32];   // the signs one bit each (as AttnParams::sgnb)
+    uint32_t sgn2b[kMaxD / 32];
 };
 
 // Constants of the attention kernels.

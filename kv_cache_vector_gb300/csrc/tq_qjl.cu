@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
     __shared__ float cen_s[16];  // centroids by lane-varying index: shared memory, not the parameter bank
     stage_matrix<D>(S, Ss);
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        sg[i] = P.sgn[i];
-        sg2[i] = P.sgn2[i];
+        sg[i] = sign_mask(P.sgnb, i);
+        sg2[i] = sign_mask(P.sgn2b, i);
     }
     if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
     __syncthreads();
@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         cs[e] = csum[lane * E + e];
-        sgl[e] = P.sgn[lane * E + e];
-        sg2l[e] = P.two_sided ? P.sgn2[lane * E + e] : 0u;
+        sgl[e] = sign_mask(P.sgnb, lane * E + e);
+        sg2l[e] = P.two_sided ? sign_mask(P.sgn2b, lane * E + e) : 0u;
     }
     for (int64_t r0 = ((int64_t)blockIdx.x * kQjlWarps + warp) * kQjlRows; r0 < n_rows;
          r0 += (int64_t)gridDim.x * kQjlWarps * kQjlRows) {
@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
     __shared__ float cen_s[16], bnd_s[16];
     qtc_stage_s<false>(S, Sh, Sl);
     for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        sg[i] = P.sgn[i];
-        sg2[i] = P.sgn2[i];
+        sg[i] = sign_mask(P.sgnb, i);
+        sg2[i] = sign_mask(P.sgn2b, i);
     }
     if (threadIdx.x < 16) {
         cen_s[threadIdx.x] = P.cen[threadIdx.x];
@@ -635,8 +635,8 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_decode_qjl_tc(const uint8
     uint32_t sgl[E], sg2l[E];  // the lane's sign masks, read once (lane-varying parameter reads serialise)
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        sgl[e] = P.sgn[lane * E + e];
-        sg2l[e] = P.two_sided ? P.sgn2[lane * E + e] : 0u;
+        sgl[e] = sign_mask(P.sgnb, lane * E + e);
+        sg2l[e] = P.two_sided ? sign_mask(P.sgn2b, lane * E + e) : 0u;
     }
     const uint32_t sSh = smem_addr(Sh), sSl = smem_addr(Sl);
     const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
