@@ -774,11 +774,12 @@ def extra_gemma(peak):
     window encode and window decode (to bf16) GB/s.  K and V have the same
     width, so a window is one call over its K and V rows; one CUDA graph holds
     the calls of 4 copies of the window (4 x 90 MB, more than L2, so each
-    window's input comes from HBM) and is replayed after an L2 flush, 50
+    window's input comes from HBM) and is replayed after an L2 flush, 200
     times.  Then the
     append-only decode step, one tq_append per layer (4 K + 4 V rows), and
     the decode attention of one token per layer (batch 1, 8 query / 4 KV
-    heads, context 513), each 34-layer step replayed from a CUDA graph."""
+    heads, context 513), each 34-layer step replayed from a CUDA graph, 200
+    times (the eager append call too)."""
     import torch
     from kv_cache_vector_gb300 import abi, synth
     L, Hkv, Hq, d, T, steps, NW = 34, 4, 8, 256, 512, 50, 4
@@ -806,10 +807,10 @@ def extra_gemma(peak):
     # K and V share the width (K4/V4), so a window is one call over its 2 x rows rows
     enc = graph_of(lambda: [abi.tq_encode(plan, 4, win[w].view(2 * rows, d), pk[w].view(2 * rows, -1), nm[w].view(-1))
                             for w in range(NW)])
-    ms = time_graph(enc, 50, lambda: flush_l2(buf)) / NW
+    ms = time_graph(enc, 200, lambda: flush_l2(buf)) / NW
     decg = graph_of(lambda: [abi.tq_decode(plan, 4, pk[w].view(2 * rows, -1), nm[w].view(-1),
                                            out=dec[w].view(2 * rows, d)) for w in range(NW)])
-    dms = time_graph(decg, 50, lambda: flush_l2(buf)) / NW
+    dms = time_graph(decg, 200, lambda: flush_l2(buf)) / NW
     pk, nm = pk[0], nm[0]
     del win, dec
     wbytes = 2 * rows * (d * 2 + d // 2 + 4)
@@ -824,29 +825,29 @@ def extra_gemma(peak):
     one = lambda: abi.tq_append(plan, caches[0], nk[0], nv[0], T)
     for _ in range(3):
         one()
-    append_ms = time_events(one, 50)
+    append_ms = time_events(one, 200)
     app = graph_of(lambda: [abi.tq_append(plan, caches[l], nk[l], nv[l], T) for l in range(L)])
-    step_ms = time_graph(app, 50)
+    step_ms = time_graph(app, 200)
     q = synth.device_normal(4004, (L, 1, Hq, d))
     out = torch.empty(L, 1, Hq, d, device="cuda")
     wss = [torch.empty(abi.tq_attn_workspace_bytes(1, Hq, Hkv, d, T + 1), dtype=torch.uint8, device="cuda")
            for _ in range(L)]
     att = graph_of(lambda: [abi.tq_attn_decode(plan, q[l], caches[l], T + 1, 1.0 / math.sqrt(d), out=out[l],
                                                workspace=wss[l]) for l in range(L)])
-    att_ms = time_graph(att, 50)
+    att_ms = time_graph(att, 200)
     abytes = L * Hkv * (T + 1) * (d * 8 // 8 + 8)
     return {"window_encode": {"ms": round(ms, 4), "GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
                               "frac": round(wbytes / (ms * 1e-3) / 1e9 / peak, 4),
                               "frac_nominal": round(wbytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
-                              "repeats": 50, "timing": "graph of 4 windows (one call per window over its K and V rows), L2 flushed per replay"},
+                              "repeats": 200, "timing": "graph of 4 windows (one call per window over its K and V rows), L2 flushed per replay"},
             "window_decode_bf16": {"ms": round(dms, 4), "GBps": round(wbytes / (dms * 1e-3) / 1e9, 1),
                                    "frac": round(wbytes / (dms * 1e-3) / 1e9 / peak, 4),
                                    "frac_nominal": round(wbytes / (dms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
-                                   "repeats": 50, "timing": "graph of 4 windows (one call per window over its K and V rows), L2 flushed per replay"},
+                                   "repeats": 200, "timing": "graph of 4 windows (one call per window over its K and V rows), L2 flushed per replay"},
             "append_us_per_call": round(append_ms * 1e3, 2),
             "append_step_us_34_layers_graph": round(step_ms * 1e3, 2),
             "attn_step_us_34_layers_graph": round(att_ms * 1e3, 2),
-            "attn_GBps": round(abytes / (att_ms * 1e-3) / 1e9, 1),
+            "attn_GBps": round(abytes / (att_ms * 1e-3) / 1e9, 1), "step_repeats": 200,
             "config": "34L x 4Hkv x d256 x 512 tokens bf16, K4/V4; 1-token appends (B1); decode attention "
                       "B1 Hq8/Hkv4 ctx513 per layer"}
 
