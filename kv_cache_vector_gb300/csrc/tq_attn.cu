@@ -328,6 +328,7 @@ static __global__ void __launch_bounds__(256) k_attn3_q(const __nv_bfloat16* __r
                                                         float* __restrict__ qexp,
                                                         const __grid_constant__ AttnParams P, int64_t n_rows,
                                                         uint32_t* __restrict__ gmax) {
+    griddep_wait();    // the queries, and readers of this call's workspace, of the previous kernel
     griddep_launch();  // the split kernel may start its table build now
     const int lane = threadIdx.x & 31;
     const int64_t bh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -356,10 +357,11 @@ static __global__ void __launch_bounds__(128) k_attn3_q_append(const __nv_bfloat
                                                                int v_bits, int32_t* __restrict__ len1, int* status) {
     __shared__ uint32_t sg[128], sg2[128];
     __shared__ uint8_t ib[2][128];
-    griddep_launch();
     const int j = threadIdx.x;
     sg[j] = sign_mask(P.sgnb, j);
     sg2[j] = sign_mask(P.sgn2b, j);
+    griddep_wait();  // the queries, new rows and cache, and readers of the workspace, of the previous kernel
+    griddep_launch();
     const int b = blockIdx.x / Hq, h = blockIdx.x - b * Hq, G = Hq / Hkv;
     const int64_t p = __ldg(pa.lens + b);
     if (h == 0 && j == 0) len1[b] = p < 0 ? 0 : (p >= INT32_MAX ? INT32_MAX : (int32_t)(p + 1));
@@ -1303,7 +1305,8 @@ static __global__ void __launch_bounds__(128) k_attn3_combine(const float* __res
                                                               int64_t n_bh, float* __restrict__ out,
                                                               const __grid_constant__ AttnParams P,
                                                               bool paged, const A3Meta meta) {
-    griddep_wait();  // the partials of the split kernel
+    griddep_wait();    // the partials of the split kernel
+    griddep_launch();  // a later kernel of the stream may set itself up; it waits for this grid
     __shared__ float red[3][132];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t bh = blockIdx.x;
@@ -1429,22 +1432,20 @@ cudaError_t attn3_launch(const void* q, int B, int Hq, int Hkv, const tq_cache_v
         int32_t* len1 = meta.clast + (size_t)B * Hq;  // attended lengths, written by the append launch
         auto qb = static_cast<const __nv_bfloat16*>(q);
         if (app->bf16)
-            k_attn3_q_append<__nv_bfloat16><<<B * Hq, 128, 0, s>>>(
-                qb, q16, qexp, P, Hq, Hkv, static_cast<const __nv_bfloat16*>(app->k_new),
-                static_cast<const __nv_bfloat16*>(app->v_new), cache, pa, *app->PK, *app->PV, KB, VB, len1,
-                status_word());
+            e = launch_pdl(k_attn3_q_append<__nv_bfloat16>, dim3(B * Hq), dim3(128), 0, s, qb, q16, qexp, P, Hq, Hkv,
+                           static_cast<const __nv_bfloat16*>(app->k_new),
+                           static_cast<const __nv_bfloat16*>(app->v_new), cache, pa, *app->PK, *app->PV, KB, VB,
+                           len1, status_word());
         else
-            k_attn3_q_append<float><<<B * Hq, 128, 0, s>>>(qb, q16, qexp, P, Hq, Hkv,
-                                                          static_cast<const float*>(app->k_new),
-                                                          static_cast<const float*>(app->v_new), cache, pa,
-                                                          *app->PK, *app->PV, KB, VB, len1, status_word());
+            e = launch_pdl(k_attn3_q_append<float>, dim3(B * Hq), dim3(128), 0, s, qb, q16, qexp, P, Hq, Hkv,
+                           static_cast<const float*>(app->k_new), static_cast<const float*>(app->v_new), cache, pa,
+                           *app->PK, *app->PV, KB, VB, len1, status_word());
         pa.lens = len1;
     } else {
-        k_attn3_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(q), q16, qexp, P, (int64_t)B * Hq,
-            (!PAGED && P.sparse_thr > 0.f) ? meta.gmax : nullptr);
+        e = launch_pdl(k_attn3_q, dim3((unsigned)(((int64_t)B * Hq + 7) / 8)), dim3(256), 0, s,
+                       static_cast<const __nv_bfloat16*>(q), q16, qexp, P, (int64_t)B * Hq,
+                       (!PAGED && P.sparse_thr > 0.f) ? meta.gmax : (uint32_t*)nullptr);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
     int grid = (int)(items < sms ? items : sms);  // one CTA per SM
@@ -1506,6 +1507,7 @@ static __global__ void __launch_bounds__(256) k_attn3_qjl_q(const __nv_bfloat16*
     __shared__ __align__(16) float ys[8][128];
     __shared__ float ss[128 * 65];
     __shared__ float wmax[8][4];
+    griddep_wait();  // the queries and S, and readers of the workspace, of the previous kernel
     griddep_launch();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int64_t row0 = (int64_t)blockIdx.x * 8;
@@ -1598,9 +1600,8 @@ cudaError_t attn3_qjl_launch(const void* q, const float* S, int B, int Hq, int H
     meta.qpexp = qpexp;
     meta.k_rnorm = k_rnorm;
     const auto qb = static_cast<const __nv_bfloat16*>(q);
-    k_attn3_qjl_q<<<(unsigned)(((int64_t)B * Hq + 7) / 8), 256, 0, s>>>(qb, S, q16, qexp, qp16, qpexp, P, proj_mul,
-                                                                         (int64_t)B * Hq);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_attn3_qjl_q, dim3((unsigned)(((int64_t)B * Hq + 7) / 8)), dim3(256), 0, s, qb, S, q16,
+                               qexp, qp16, qpexp, P, proj_mul, (int64_t)B * Hq);
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)B * Hkv * geo.n_splits;
     const int grid = (int)(items < sms ? items : sms);  // one CTA per SM
