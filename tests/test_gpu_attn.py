@@ -61,6 +61,10 @@ CASES = [
     (2, 32, 8, 128, 1000, 1000, 4, 3),
     (1, 4, 1, 128, 5000, 5003, 4, 4),   # several splits and a ragged last split
     (1, 16, 2, 64, 3001, 3001, 3, 2),
+    # d != 128 with at most 8 splits: merged inside a thread-block cluster
+    (1, 8, 2, 64, 200, 210, 4, 2),      # 4 splits of 64
+    (1, 4, 4, 256, 600, 600, 2, 3),     # 10 splits of 64 become 8 of 75
+    (2, 8, 4, 256, 700, 700, 4, 4),     # 11 splits stay (split and combine launches)
 ]
 
 
