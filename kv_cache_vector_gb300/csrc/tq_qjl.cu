@@ -97,10 +97,11 @@ __device__ __forceinline__ void warp_fwht(float (&v)[E], int lane) {
     fwht_reg<E>(v);
 #pragma unroll
     for (int b = 1; b < 32; b <<= 1) {
+        const float sgn = (lane & b) ? -1.f : 1.f;  // (lo + hi, lo - hi) = o + (+-1) v, one rounding
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             const float o = __shfl_xor_sync(0xFFFFFFFFu, v[e], b);
-            v[e] = (lane & b) ? o - v[e] : v[e] + o;
+            v[e] = fmaf(sgn, v[e], o);
         }
     }
 }
@@ -353,6 +354,12 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_decode_qjl(const uint8_t* __
 // S sits in shared memory as fp16 high and low parts in rows of 136 halves:
 // [projection][dim] for the encode, [dim][projection] for the decode, so that
 // each operand's ldmatrix reads 8 rows of 16 bytes from distinct banks.
+// Row data reaches a warp through its own staging buffer in shared memory,
+// filled by cp.async one tile ahead: the encoder's next 16 bf16 rows (4 KB,
+// issued once the current rows have been read, so the copy runs under the
+// projections), the decoder's next 16 packed rows with their norms and gammas
+// (two buffers, since a tile's rows are read until its end).  Bytes past the
+// last row are zero-filled.
 #ifndef TQ_QJL_TC_WARPS
 #define TQ_QJL_TC_WARPS 12
 #endif
@@ -365,9 +372,18 @@ constexpr int kQtcSide = TQ_QJL_TC_SIDE;
 constexpr int kQtcRow = 136;                                     // halves per row of an fp16 tile
 constexpr int kQtcS = 2 * 128 * kQtcRow * 2;                     // S high and low parts
 constexpr int kQtcEncWarp = 2 * 16 * kQtcRow * 2;                // residual parts
-constexpr int kQtcEncSmem = kQtcS + kQtcWarps * kQtcEncWarp + 2 * 128 * 4;
+constexpr int kQtcEncXb = 16 * 128 * 2;                          // staged bf16 rows of a tile
+constexpr int kQtcEncXbAt = kQtcS + kQtcWarps * kQtcEncWarp + 2 * 128 * 4;  // after the sign masks
+constexpr int kQtcEncSmem = kQtcEncXbAt + kQtcWarps * kQtcEncXb;
 constexpr int kQtcDecWarp = 16 * kQtcRow * 4;                    // S^T sgn of 16 rows, fp32
-constexpr int kQtcDecSmem = kQtcS + kQtcWarps * kQtcDecWarp;
+constexpr int kQtcDecXb = 16 * 64 + 2 * 16 * 4;                  // packed rows (at most 64 B), norms, gammas
+constexpr int kQtcDecXbAt = kQtcS + kQtcWarps * kQtcDecWarp;
+constexpr int kQtcDecSmem = kQtcDecXbAt + kQtcWarps * 2 * kQtcDecXb;
+static_assert(kQtcEncXbAt % 16 == 0 && kQtcDecXbAt % 16 == 0 && kQtcDecXb % 16 == 0, "16-byte copies");
+static_assert(kQtcEncSmem + 256 <= 232448 && kQtcDecSmem + 256 <= 232448, "shared memory per block");
+
+// All of this thread's cp.async groups but the last one committed have landed.
+__device__ __forceinline__ void qtc_cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ void qtc_mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -446,12 +462,15 @@ __device__ __forceinline__ void warp_fwht_rows(float (&v)[R][E], int lane) {
     for (int q = 0; q < R; ++q) fwht_reg<E>(v[q]);
 #pragma unroll
     for (int b = 1; b < 32; b <<= 1) {
+        // (lo + hi, lo - hi) as one fused multiply-add, o + (+-1) v: the
+        // product is exact, so the one rounding is that of the add
+        const float sgn = (lane & b) ? -1.f : 1.f;
 #pragma unroll
         for (int q = 0; q < R; ++q)
 #pragma unroll
             for (int e = 0; e < E; ++e) {
                 const float o = __shfl_xor_sync(0xFFFFFFFFu, v[q][e], b);
-                v[q][e] = (lane & b) ? o - v[q][e] : v[q][e] + o;
+                v[q][e] = fmaf(sgn, v[q][e], o);
             }
     }
 }
@@ -493,9 +512,33 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
     unsigned char* wb = qtc_smem + kQtcS + warp * kQtcEncWarp;
     uint32_t* Rh = reinterpret_cast<uint32_t*>(wb);                       // [16][kQtcRow / 2] half pairs
     uint32_t* Rl = Rh + 16 * kQtcRow / 2;
-    const uint32_t sRh = smem_addr(Rh), sRl = smem_addr(Rl), sSh = smem_addr(Sh), sSl = smem_addr(Sl);
-    for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
-         r0 += (int64_t)gridDim.x * kQtcWarps * 16) {
+    const uint32_t sRh = smem_addr(Rh), sSh = smem_addr(Sh), sSl = smem_addr(Sl);
+    const uint32_t sRl = smem_addr(Rl);
+    // bf16 rows come through the warp's staging buffer (fp32 rows, twice the
+    // bytes, are loaded directly)
+    constexpr bool kStaged = sizeof(T) == 2;
+    const unsigned char* xb = qtc_smem + kQtcEncXbAt + warp * kQtcEncXb;
+    const uint32_t sXb = smem_addr(xb);
+    auto stage = [&](int64_t t0) {  // tile t0 .. t0 + 15: 256 pieces of 16 bytes, 8 per lane
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(x + t0 * D);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int p = lane + 32 * k;  // row p / 16
+            const bool in = t0 + (p >> 4) < n_rows;
+            cp_async16(sXb + 16u * p, in ? src + 16 * p : src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    const int64_t r_step = (int64_t)gridDim.x * kQtcWarps * 16;
+    int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16;
+    if constexpr (kStaged) {
+        if (r0 < n_rows) stage(r0);
+    }
+    for (; r0 < n_rows; r0 += r_step) {
+        if constexpr (kStaged) {
+            cp_async_wait_all();
+            __syncwarp();
+        }
         // ---- MSE stage and residual of each row, kQtcSide rows side by side
         // (their loads first; rows past the end: zeros)
 #pragma unroll 1
@@ -504,7 +547,14 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
 #pragma unroll
             for (int q = 0; q < kQtcSide; ++q) {
                 if (r0 + q0 + q < n_rows) {
-                    load_lane<E, T>(x + (r0 + q0 + q) * D, lane, sg, vq[q]);
+                    if constexpr (kStaged) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(xb + (q0 + q) * 256 + 8 * lane);
+                        const uint32_t h[E] = {u.x << 16, u.x & 0xFFFF0000u, u.y << 16, u.y & 0xFFFF0000u};
+#pragma unroll
+                        for (int e = 0; e < E; ++e) vq[q][e] = __uint_as_float(h[e] ^ sg[lane * E + e]);
+                    } else {
+                        load_lane<E, T>(x + (r0 + q0 + q) * D, lane, sg, vq[q]);
+                    }
                 } else {
 #pragma unroll
                     for (int e = 0; e < E; ++e) vq[q][e] = 0.f;
@@ -566,6 +616,11 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
             }
         }
         __syncwarp();
+        // every lane has read the staged rows: the next tile's copy runs
+        // under this tile's projections
+        if constexpr (kStaged) {
+            if (r0 + r_step < n_rows) stage(r0 + r_step);
+        }
         // ---- P = R S^T: A fragments of the 8 k-steps (16 dims each), then
         // tiles of 8 projections
         uint32_t ah[8][4], al[8][4];
@@ -640,11 +695,37 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_decode_qjl_tc(const uint8
     }
     const uint32_t sSh = smem_addr(Sh), sSl = smem_addr(Sl);
     const uint32_t boff = (uint32_t)(((lane & 7) * kQtcRow + (lane >> 3) * 8) * 2);
-    for (int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16; r0 < n_rows;
-         r0 += (int64_t)gridDim.x * kQtcWarps * 16) {
-        // sign words: lane r < 16 loads row r's, then each lane takes rows g and g + 8
+    // staging buffer b of the warp: the tile's packed rows (16 RB bytes), then
+    // its 16 norms and 16 gammas
+    const unsigned char* xb0 = qtc_smem + kQtcDecXbAt + warp * 2 * kQtcDecXb;
+    const uint32_t sXb0 = smem_addr(xb0);
+    auto stage = [&](int64_t t0, int b) {  // always commits a group, empty past the end
+        if (t0 < n_rows) {
+            const uint32_t dst = sXb0 + (uint32_t)(b * kQtcDecXb);
+            const uint8_t* src = packed + t0 * RB;
+            const int64_t have = n_rows - t0;  // rows of the tile that exist (may exceed 16)
+            for (int p = lane; p < RB; p += 32) {  // RB pieces of 16 bytes, RB / 16 per row
+                const bool in = p / (RB / 16) < have;
+                cp_async16(dst + 16u * p, in ? src + 16 * p : src, in ? 16u : 0u);
+            }
+            const int r = lane & 15;
+            const bool in = r < have;
+            cp_async4(dst + 16u * RB + 4u * lane, (lane < 16 ? norms : rnorms) + t0 + (in ? r : 0), in ? 4u : 0u);
+        }
+        cp_async_commit();
+    };
+    const int64_t r_step = (int64_t)gridDim.x * kQtcWarps * 16;
+    int64_t r0 = ((int64_t)blockIdx.x * kQtcWarps + warp) * 16;
+    stage(r0, 0);
+    for (int it = 0; r0 < n_rows; r0 += r_step, ++it) {
+        stage(r0 + r_step, (it + 1) & 1);
+        qtc_cp_async_wait_prev();  // this tile's group
+        __syncwarp();
+        const unsigned char* xb = xb0 + (it & 1) * kQtcDecXb;
+        const float* xn = reinterpret_cast<const float*>(xb + 16 * RB);  // norms, then gammas
+        // sign words: lane r < 16 reads row r's, then each lane takes rows g and g + 8
         uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-        if (lane < 16 && r0 + lane < n_rows) wv = __ldg(reinterpret_cast<const uint4*>(packed + (r0 + lane) * RB + IB));
+        if (lane < 16) wv = *reinterpret_cast<const uint4*>(xb + lane * RB + IB);
         const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t wg[4], wg8[4];
 #pragma unroll
@@ -689,16 +770,14 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_decode_qjl_tc(const uint8
             uint32_t ib[4];
             float nrm[4], gk[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const bool ok = r0 + q0 + q < n_rows;
-                const uint8_t* row = packed + (ok ? r0 + q0 + q : 0) * RB;
+            for (int q = 0; q < 4; ++q) {  // rows past the end read the zero fill
                 const int bit0 = lane * E * MB, wi = bit0 / 32, sh = bit0 % 32;
-                const uint32_t* iwp = reinterpret_cast<const uint32_t*>(row);
-                uint32_t v = ok ? __ldg(iwp + wi) >> sh : 0u;
-                if (ok && sh + E * MB > 32) v |= __ldg(iwp + wi + 1) << (32 - sh);
+                const uint32_t* iwp = reinterpret_cast<const uint32_t*>(xb + (q0 + q) * RB);
+                uint32_t v = iwp[wi] >> sh;
+                if (sh + E * MB > 32) v |= iwp[wi + 1] << (32 - sh);
                 ib[q] = v;
-                nrm[q] = ok ? __ldg(norms + r0 + q0 + q) : 0.f;
-                gk[q] = ok ? __ldg(rnorms + r0 + q0 + q) * kappa : 0.f;
+                nrm[q] = xn[q0 + q];
+                gk[q] = xn[16 + q0 + q] * kappa;
             }
             float v[4][E];
 #pragma unroll
