@@ -766,7 +766,9 @@ static_assert(kU2CellAt + 8 * kRepCells <= kU2RepAt, "layout");
 static_assert((kU2RepAt & 0x7F80u) == 0, "table base: cell bits free");
 static_assert(kU2End <= 232448, "shared memory");
 
-template <int BITS>
+// TS: the plan's second signs (two-sided), fixed per instantiation so that
+// the per-element loop carries no test of it.
+template <int BITS, bool TS>
 __global__ void __launch_bounds__(kU2Threads, 1)
 k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* __restrict__ packed,
                  float* __restrict__ norms, int* status, const __grid_constant__ RowParams P) {
@@ -980,7 +982,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                               float& yhi) {
                 ylo = __uint_as_float(a0[i]) + __uint_as_float(a1[i]);
                 yhi = __uint_as_float(a0[i]) - __uint_as_float(a1[i]);
-                if (P.two_sided) {
+                if constexpr (TS) {
                     ylo = __uint_as_float(__float_as_uint(ylo) ^ sg2[32 * c + i]);
                     yhi = __uint_as_float(__float_as_uint(yhi) ^ sg2[128 + 32 * c + i]);
                 }
@@ -1421,7 +1423,7 @@ cudaError_t enc_umma256(const void* x, int64_t n, uint8_t* pk, float* nm, const 
     CUtensorMap map;
     cudaError_t e = make_rows_map(&map, x, 2, 256, (uint64_t)n, dev::kU2Rows);
     if (e != cudaSuccess) return e;
-    auto fn = dev::k_encode_umma256<BITS>;
+    auto fn = P.two_sided ? dev::k_encode_umma256<BITS, true> : dev::k_encode_umma256<BITS, false>;
     // absolute layout: ask for kU2End bytes (the dynamic block starts below kU2HbAt)
     e = cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev::kU2End);
     if (e != cudaSuccess) return e;
