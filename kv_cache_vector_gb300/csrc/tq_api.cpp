@@ -177,12 +177,12 @@ bool codebook(int d, int bits, double* cen, double* bnd, bool gaussian = false) 
     return true;
 }
 
-// The encode kernels bucket through a table of cells of width 1/kLutScale;
-// it is exact when no closed cell holds two boundaries.
-bool lut_exact(const float* b32, int nb) {
+// The encode kernels bucket through a table of cells of width 1/scale; it
+// is exact when no closed cell holds two boundaries.
+bool lut_exact(const float* b32, int nb, int scale) {
     for (int j = 0; j + 1 < nb; ++j) {
         double gap = (double)b32[j + 1] - (double)b32[j];
-        if (gap <= 1.0 / tq::kLutScale + 1e-12) return false;
+        if (gap <= 1.0 / scale + 1e-12) return false;
     }
     return true;
 }
@@ -408,7 +408,8 @@ tq_status tq_plan_create_ex(int d, uint64_t seed, uint32_t flags, tq_plan** out)
             P->b32[bits][i] = i < L - 1 ? (float)P->b64[bits][i]
                                         : std::numeric_limits<float>::infinity();
         }
-        if (bits >= 2 && !lut_exact(P->b32[bits], L - 1)) {
+        if (bits >= 2 && (!lut_exact(P->b32[bits], L - 1, tq::kLutScale) ||
+                          (d == 128 && !lut_exact(P->b32[bits], L - 1, tq::kUmLutScale)))) {
             delete P;
             return TQ_ERR_UNSUPPORTED;
         }

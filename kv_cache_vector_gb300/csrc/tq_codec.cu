@@ -7,6 +7,7 @@
 // norm / sqrt(d) -> sign -> store.  Rows are independent ("TurboQuantEngine --
 // Specification", 7 Non-goals: each row encoded independently), so the grid
 // simply strides over rows.
+#include <cfloat>
 #include <cuda_fp16.h>
 
 #include "tq_async.cuh"
@@ -474,7 +475,9 @@ constexpr uint32_t kUmSgnAt = kUmBarAt + 256;  // s and s2 masks (1 KB), read wh
 static_assert(kUmBarAt + (2 * kUmStages + 2 * kUmAcc) * 8 + 16 <= kUmSgnAt, "layout");
 static_assert(kUmSgnAt + 1024 <= kUmRepAt, "layout");
 static_assert(kUmEnd <= 232448, "shared memory");
-// The window: cells k = rint(w * kLutScale) in [-128, 128), i.e. |w| < 0.5.
+// d = 256: the window of cells k = rint(w * kLutScale) in [-128, 128), i.e.
+// |w| < 0.5; d = 128: cells k = rint(w * kUmLutScale) in [-64, 64], every
+// finite row.  Both indexed by one byte, k + 128.
 constexpr int kRepCells = 256;
 constexpr uint32_t kRepMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
 
@@ -484,10 +487,10 @@ __device__ __forceinline__ LutEntry lds_entry(uint32_t addr) {
     return e;
 }
 
-// Table entry of the cell k = rint(w * kLutScale) (same rule as build_lut).
-__device__ __forceinline__ LutEntry lut_cell(const float* bnd, int nb, int k) {
-    const float lo = (float)(k - 0.5) / (float)kLutScale;
-    const float hi = (float)(k + 0.5) / (float)kLutScale;
+// Table entry of the cell k = rint(w * scale) (same rule as build_lut).
+__device__ __forceinline__ LutEntry lut_cell(const float* bnd, int nb, int k, int scale) {
+    const float lo = (float)(k - 0.5) / (float)scale;
+    const float hi = (float)(k + 0.5) / (float)scale;
     LutEntry e;
     e.lo = 0;
     e.thr = __int_as_float(0x7F800000);
@@ -540,7 +543,7 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
         *reinterpret_cast<uint16_t*>(hb + off) = neg ? 0xBF80u : 0x3F80u;
     }
     for (int c = threadIdx.x; c < kRepCells; c += blockDim.x) {
-        const LutEntry e = lut_cell(P.bnd, (1 << BITS) - 1, c - kRepCells / 2);
+        const LutEntry e = lut_cell(P.bnd, (1 << BITS) - 1, c - kRepCells / 2, kUmLutScale);
         LutEntry* row = reinterpret_cast<LutEntry*>(at(kUmRepAt + 256u * c));
 #pragma unroll 4
         for (int l = 0; l < 32; ++l) row[l] = e;
@@ -656,16 +659,14 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
             const float ss = (s0 + s1) + (s2 + s3);  // = d * ||x||^2
             const float n = __fsqrt_rn(ss * (1.0f / 128.0f));
             const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // w = y / sqrt(ss) = u
-            const float ks = inv * (float)kLutScale;
+            const float ks = inv * (float)kUmLutScale;
             const F2 K2 = f2(ks, ks);
             uint32_t w[NW];
 #pragma unroll
             for (int k = 0; k < NW; ++k) w[k] = 0;
-            // Cells come from the replicated window (conflict-free: lane l
-            // reads only its own column); `out` collects every bit outside
-            // the window's low byte, non-zero iff some |w| >= 0.5 (or the row
-            // is not finite).
-            uint32_t out = 0u;
+            // Cells come from the replicated table (conflict-free: lane l
+            // reads only its own column).  A finite row has |w| <= 1, so its
+            // cells are 64 .. 192 and no coordinate needs a further check.
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t y[32];
@@ -677,7 +678,6 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
                     float fx, fy;
                     f2_split(f2_fma(f2(y0, y1), K2, M2), fx, fy);
                     const uint32_t bx = __float_as_uint(fx), by = __float_as_uint(fy);
-                    out |= (bx ^ kRepMagicBits) | (by ^ kRepMagicBits);
                     const LutEntry e0 = lds_entry(__byte_perm(bx, rep_slot, 0x7604));
                     const LutEntry e1 = lds_entry(__byte_perm(by, rep_slot, 0x7604));
                     const int id0 = e0.lo + (fmaf(y0, inv, -e0.thr) >= 0.0f ? 1 : 0);
@@ -691,9 +691,11 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
                     }
                 }
             }
-            // Rows with a coordinate outside the window: exact binary search
-            // over the boundaries (the tensor-memory loads are warp-wide).
-            const bool slow = (out & ~0xFFu) != 0u;
+            // Rows that are not finite (a NaN or infinite coordinate, or
+            // squares past the fp32 range): exact binary search over the
+            // boundaries, as the other encoders take it (the tensor-memory
+            // loads are warp-wide).
+            const bool slow = !(ss <= FLT_MAX);
             if (__any_sync(0xFFFFFFFFu, slow)) {
                 if (slow) {
 #pragma unroll
@@ -797,7 +799,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
         sg[i] = sign_mask(P.sgnb, i);
         sg[256 + i] = sign_mask(P.sgn2b, i);
-        reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2);
+        reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2, kLutScale);
     }
 
     // Barriers first: the producer starts loading X while the other warps

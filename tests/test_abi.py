@@ -140,11 +140,13 @@ def test_hot_call_validation_before_launch(L):
     p.close()
 
 
-def _emulate_table_bucket(bnd32: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """numpy restatement of the kernels' bucketing table: cell = rint(w*256)
+def _emulate_table_bucket(bnd32: np.ndarray, w: np.ndarray, S: int = 256, C: int = 512,
+                          N: int = 1024) -> np.ndarray:
+    """numpy restatement of the kernels' bucketing table: cell = rint(w*S)
     (round half even, exact), lo = #{beta < cell_lo}, thr = the boundary in the
-    closed cell, idx = lo + [w >= thr]."""
-    S, C, N = 256, 512, 1024
+    closed cell, idx = lo + [w >= thr].  Defaults: the 1024-cell table; the
+    d = 128 tensor-core encoder's is S = 64 with one byte of cell (C = 128,
+    N = 256)."""
     g = np.arange(N)
     lo = ((g - C - 0.5) / S).astype(np.float32).astype(np.float64)
     hi = ((g - C + 0.5) / S).astype(np.float32).astype(np.float64)
@@ -177,6 +179,30 @@ def test_bucketing_table_is_exact(L, d, bits):
         rng.uniform(-1, 1, 200000).astype(np.float32), np.array([0.0, -0.0, 1.0, -1.0], np.float32)])
     want = np.searchsorted(bnd, w, side="right")
     assert np.array_equal(_emulate_table_bucket(bnd, w), want)
+    p.close()
+
+
+@pytest.mark.parametrize("gauss", [False, True])
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_d128_tensor_core_table_is_exact(L, bits, gauss):
+    """The d = 128 tensor-core encoder's table (cells of width 1/64, one byte
+    of cell index, no window) gives #{j : w >= beta_j} for every fp32 w in
+    [-1, 1] plus rounding, with no cell index outside 64 .. 192."""
+    p = abi.Plan(128, 1, abi.PLAN_GAUSSIAN_CODEBOOK) if gauss else abi.Plan(128, 1)
+    _, bnd = p.codebook(bits)
+    rng = np.random.default_rng(128 + bits + gauss)
+    edges = ((np.arange(-64, 64) + 0.5) / 64).astype(np.float32)
+    w = np.concatenate([
+        bnd, np.nextafter(bnd, np.float32(-9)), np.nextafter(bnd, np.float32(9)),
+        edges, np.nextafter(edges, np.float32(-9)), np.nextafter(edges, np.float32(9)),
+        rng.normal(0, 1 / math.sqrt(128), 200000).astype(np.float32),
+        rng.uniform(-1, 1, 200000).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, np.nextafter(np.float32(1), np.float32(2)),
+                  np.nextafter(np.float32(-1), np.float32(-2))], np.float32)])
+    cell = np.rint(w.astype(np.float64) * 64).astype(np.int64) + 128
+    assert cell.min() >= 64 and cell.max() <= 192
+    want = np.searchsorted(bnd, w, side="right")
+    assert np.array_equal(_emulate_table_bucket(bnd, w, 64, 128, 256), want)
     p.close()
 
 
