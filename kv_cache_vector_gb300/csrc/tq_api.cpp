@@ -409,7 +409,7 @@ tq_status tq_plan_create_ex(int d, uint64_t seed, uint32_t flags, tq_plan** out)
                                         : std::numeric_limits<float>::infinity();
         }
         if (bits >= 2 && (!lut_exact(P->b32[bits], L - 1, tq::kLutScale) ||
-                          (d == 128 && !lut_exact(P->b32[bits], L - 1, tq::kUmLutScale)))) {
+                          ((d == 128 || d == 256) && !lut_exact(P->b32[bits], L - 1, tq::kUmLutScale)))) {
             delete P;
             return TQ_ERR_UNSUPPORTED;
         }

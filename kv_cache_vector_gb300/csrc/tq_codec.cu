@@ -475,11 +475,9 @@ constexpr uint32_t kUmSgnAt = kUmBarAt + 256;  // s and s2 masks (1 KB), read wh
 static_assert(kUmBarAt + (2 * kUmStages + 2 * kUmAcc) * 8 + 16 <= kUmSgnAt, "layout");
 static_assert(kUmSgnAt + 1024 <= kUmRepAt, "layout");
 static_assert(kUmEnd <= 232448, "shared memory");
-// d = 256: the window of cells k = rint(w * kLutScale) in [-128, 128), i.e.
-// |w| < 0.5; d = 128: cells k = rint(w * kUmLutScale) in [-64, 64], every
-// finite row.  Both indexed by one byte, k + 128.
+// The tensor-core encoders' tables: cells k = rint(w * kUmLutScale) in
+// [-64, 64], every finite row, indexed by one byte, k + 128.
 constexpr int kRepCells = 256;
-constexpr uint32_t kRepMagicBits = 0x4B400000u;  // bits of 1.5 * 2^23
 
 __device__ __forceinline__ LutEntry lds_entry(uint32_t addr) {
     LutEntry e;
@@ -799,7 +797,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
         sg[i] = sign_mask(P.sgnb, i);
         sg[256 + i] = sign_mask(P.sgn2b, i);
-        reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2, kLutScale);
+        reinterpret_cast<LutEntry*>(at(kU2CellAt))[i] = lut_cell(P.bnd, (1 << BITS) - 1, i - kRepCells / 2, kUmLutScale);
     }
 
     // Barriers first: the producer starts loading X while the other warps
@@ -957,7 +955,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
             const float ss = 2.0f * ((s0 + s1) + (s2 + s3));  // = ||y||^2 = d ||x||^2
             const float n = __fsqrt_rn(ss * (1.0f / 256.0f));
             const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // u = y * inv
-            const float ks = inv * (float)kLutScale;
+            const float ks = inv * (float)kUmLutScale;
             const F2 K2 = f2(ks, ks);
             const int64_t row = tile * kU2Rows + r;
             const bool valid = row < n_rows;
@@ -989,7 +987,6 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     yhi = __uint_as_float(__float_as_uint(yhi) ^ sg2[128 + 32 * c + i]);
                 }
             };
-            uint32_t out = 0u;  // bits outside the table's cell byte: some |u| >= 0.5, or not finite
             // A chunk's packed words (CW per output half) leave as one vector
             // store per half where the width allows (16 bytes at 4 bits, 8 at 2):
             // 4-byte stores of 32 rows 128 bytes apart sent 8x the output
@@ -1023,7 +1020,6 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     float fx, fy;
                     f2_split(f2_fma(f2(ylo, yhi), K2, M2), fx, fy);
                     const uint32_t bx = __float_as_uint(fx), by = __float_as_uint(fy);
-                    out |= (bx ^ kRepMagicBits) | (by ^ kRepMagicBits);
                     const LutEntry e0 = lds_entry(((bx << 7) & 0x7F80u) | rep_slot);
                     const LutEntry e1 = lds_entry(((by << 7) & 0x7F80u) | rep_slot);
                     put(wl, i, e0.lo + (fmaf(ylo, inv, -e0.thr) >= 0.0f ? 1 : 0));
@@ -1041,10 +1037,12 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 tmem_wait_ld();
                 bucket_chunk(a0, a1, c);
             }
-            // rows with a coordinate outside the table's window: exact binary
-            // search over the boundaries, written over the fast path's bytes
-            // (the tensor-memory loads are warp-wide)
-            const bool slow = (out & ~0xFFu) != 0u;
+            // rows that are not finite (a NaN or infinite coordinate, or
+            // squares past the fp32 range): exact binary search over the
+            // boundaries, written over the fast path's bytes (the
+            // tensor-memory loads are warp-wide); a finite row's cells are
+            // 64 .. 192, all in the table
+            const bool slow = !(ss <= FLT_MAX);
             if (__any_sync(0xFFFFFFFFu, slow)) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {

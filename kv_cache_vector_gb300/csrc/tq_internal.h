@@ -102,11 +102,11 @@ cudaError_t launch_attn_decode(const Plan& P, const void* q, int B, int Hq, int 
 constexpr int kLutScale = 256;
 constexpr int kLutCenter = 512;
 constexpr int kLutCells = 1024;  // covers w in [-2, 2); |w| <= 1 for finite rows
-// The d = 128 tensor-core encoder's table: cells of width 1/64 (a power of
-// two, so y * inv * 64 is the exact product), k = rint(w * 64) in [-64, 64]
-// for every finite row, indexed by one byte (k + 128).  Exact when no closed
-// cell holds two boundaries: every d = 128 codebook's boundaries are at least
-// 1.45 cells apart.
+// The tensor-core encoders' tables (d = 128 and 256): cells of width 1/64 (a
+// power of two, so y * inv * 64 is the exact product), k = rint(w * 64) in
+// [-64, 64] for every finite row, indexed by one byte (k + 128).  Exact when
+// no closed cell holds two boundaries: the codebooks' boundaries are at least
+// 1.45 (d = 128) and 1.03 (d = 256) cells apart; plan creation checks it.
 constexpr int kUmLutScale = 64;
 
 // Launchers, one explicit instantiation per head dimension D (each kernel

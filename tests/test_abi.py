@@ -184,18 +184,19 @@ def test_bucketing_table_is_exact(L, d, bits):
 
 @pytest.mark.parametrize("gauss", [False, True])
 @pytest.mark.parametrize("bits", [2, 3, 4])
-def test_d128_tensor_core_table_is_exact(L, bits, gauss):
-    """The d = 128 tensor-core encoder's table (cells of width 1/64, one byte
-    of cell index, no window) gives #{j : w >= beta_j} for every fp32 w in
-    [-1, 1] plus rounding, with no cell index outside 64 .. 192."""
-    p = abi.Plan(128, 1, abi.PLAN_GAUSSIAN_CODEBOOK) if gauss else abi.Plan(128, 1)
+@pytest.mark.parametrize("d", [128, 256])
+def test_tensor_core_encoder_table_is_exact(L, d, bits, gauss):
+    """The tensor-core encoders' table (d = 128 and 256: cells of width 1/64,
+    one byte of cell index, no window) gives #{j : w >= beta_j} for every fp32
+    w in [-1, 1] plus rounding, with no cell index outside 64 .. 192."""
+    p = abi.Plan(d, 1, abi.PLAN_GAUSSIAN_CODEBOOK) if gauss else abi.Plan(d, 1)
     _, bnd = p.codebook(bits)
-    rng = np.random.default_rng(128 + bits + gauss)
+    rng = np.random.default_rng(d + bits + gauss)
     edges = ((np.arange(-64, 64) + 0.5) / 64).astype(np.float32)
     w = np.concatenate([
         bnd, np.nextafter(bnd, np.float32(-9)), np.nextafter(bnd, np.float32(9)),
         edges, np.nextafter(edges, np.float32(-9)), np.nextafter(edges, np.float32(9)),
-        rng.normal(0, 1 / math.sqrt(128), 200000).astype(np.float32),
+        rng.normal(0, 1 / math.sqrt(d), 200000).astype(np.float32),
         rng.uniform(-1, 1, 200000).astype(np.float32),
         np.array([0.0, -0.0, 1.0, -1.0, np.nextafter(np.float32(1), np.float32(2)),
                   np.nextafter(np.float32(-1), np.float32(-2))], np.float32)])
