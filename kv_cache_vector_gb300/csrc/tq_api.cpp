@@ -195,6 +195,7 @@ void fill_row_params(const tq::Plan& P, int bits, tq::RowParams& R) {
         if (R.sgn[i]) R.sgnb[i >> 5] |= 1u << (i & 31);
         if (R.sgn2[i]) R.sgn2b[i >> 5] |= 1u << (i & 31);
     }
+    for (int j = 0; j < tq::kMaxD / 2; ++j) R.sgnh[j] = (R.sgn[2 * j] >> 16) | R.sgn[2 * j + 1];
     R.two_sided = (P.flags & TQ_PLAN_TWO_SIDED_SIGNS) ? 1 : 0;
     for (int i = 0; i < 16; ++i) {
         R.cen[i] = P.c32[bits][i];

@@ -1296,10 +1296,15 @@ k_decode3_256(const uint8_t* __restrict__ packed, const float* __restrict__ norm
               const __grid_constant__ CUtensorMap ymap, const __grid_constant__ RowParams P) {
     constexpr int D = 256, E = 128, RB = D * BITS / 8, HB = E / 2 * BITS / 8, NW = E * BITS / 32;
     __shared__ float cen_s[16];
+    // the output pairs' sign masks of part p at sgh_s[65 p ..]: the lanes of
+    // the two parts read different banks (a lane-varying index into the
+    // parameter bank would be serialised)
+    __shared__ uint32_t sgh_s[2 * 65];
     extern __shared__ __align__(1024) unsigned char dsm[];
     unsigned char* base = dsm + ((1024u - (smem_addr(dsm) & 1023u)) & 1023u);
     griddep_launch();
     if (threadIdx.x < 16) cen_s[threadIdx.x] = P.cen[threadIdx.x];
+    if (threadIdx.x < 128) sgh_s[threadIdx.x + (threadIdx.x >> 6)] = P.sgnh[threadIdx.x];
     __syncthreads();
     griddep_wait();  // the packed rows and the output may belong to the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1338,7 +1343,7 @@ k_decode3_256(const uint8_t* __restrict__ packed, const float* __restrict__ norm
         fwht_cross<E>(v, p);  // split -> contiguous: dims 128p + j
         const float scs = norm * P.inv_sqrt_d;
         const F2 sc = f2(scs, scs);
-        const uint32_t* sg = P.sgn + p * E;
+        const uint32_t* sgh = sgh_s + 65 * p;
         unsigned char* b = buf + (it & 1) * 8192;
         // the stores that last read this buffer (two tiles ago) must be done
         if (lane == 0) bulk_wait_read<1>();
@@ -1352,7 +1357,7 @@ k_decode3_256(const uint8_t* __restrict__ packed, const float* __restrict__ norm
                 float ax, ay;
                 f2_split(f2_mul(f2(v[k], v[k + 1]), sc), ax, ay);
                 __nv_bfloat162 h = __floats2bfloat162_rn(ax, ay);
-                q[m] = *reinterpret_cast<uint32_t*>(&h) ^ ((sg[k] >> 16) | sg[k + 1]);
+                q[m] = *reinterpret_cast<uint32_t*>(&h) ^ sgh[k >> 1];
             }
             const int blk = 2 * p + (c >> 3), cc = c & 7;
             *reinterpret_cast<uint4*>(b + blk * 2048 + rr * 128 + ((cc ^ (rr & 7)) << 4)) =

@@ -27,6 +27,9 @@ struct RowParams {
     uint32_t sgn2[kMaxD];
     uint32_t sgnb[kMaxD / 32];   // the signs one bit each (as AttnParams::sgnb)
     uint32_t sgn2b[kMaxD / 32];
+    // the signs of elements 2j and 2j + 1 on the sign bits of a bf16 pair
+    // (bits 15 and 31): one xor flips a packed output pair
+    uint32_t sgnh[kMaxD / 2];
 };
 
 // Constants of the attention kernels.
