@@ -101,7 +101,10 @@ tq_status tq_codebook_init_gaussian(int d, int bits, double *centroids, double *
 /* Build a plan for head dimension d (power of two, 8..256) and sign seed
  * (the pages' fa_tq_init(head_dim, config, seed)).  Computes the codebooks
  * for bits 2, 3, 4 and the sign diagonal.  *out receives a host object that
- * the caller releases with tq_plan_destroy. */
+ * the caller releases with tq_plan_destroy.
+ * Errors: TQ_ERR_INVALID_ARG (null out), TQ_ERR_UNSUPPORTED (d, or a codebook
+ * with two boundaries closer than the encoders' bucketing cells: 1/256, and
+ * 1/64 at d = 128 and 256 -- no codebook the library builds is), TQ_ERR_NOMEM. */
 tq_status tq_plan_create(int d, uint64_t seed, tq_plan **out);
 
 /* Format variants of the plan, for interoperability with caches written by
