@@ -45,9 +45,32 @@ __device__ __forceinline__ void encode_part(const T* __restrict__ row, uint8_t* 
     fwht_reg<E>(v);
     if constexpr (R == 2) fwht_cross<E>(v, p);
     if (P.two_sided) flip_rotated<D>(v, p, P.sgn2);
-    const float n = __fsqrt_rn(ss);
+    float n = __fsqrt_rn(ss);
     // w = y * inv is the normalised coordinate u = (H s x / sqrt(d)) / n
-    const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+    float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+    if (!ss_in_range(ss)) {  // both threads of a row (R = 2) agree: ss is shared
+        float m = 0.f;
+        bool nf = false;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const float a = fabsf(v[i]);
+            nf = nf || !(a <= FLT_MAX);
+            m = fmaxf(m, a);
+        }
+        if constexpr (R == 2) {
+            const unsigned am = __activemask();
+            m = fmaxf(m, __shfl_xor_sync(am, m, 1));
+            nf = __shfl_xor_sync(am, (int)nf, 1) != 0 || nf;
+        }
+        if (!nf && m > 0.f) {  // squares past fp32's range: the sums again on y S
+            const float S = pow2_scale(m);
+            float t = 0.f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) t = fmaf(v[i] * S, v[i] * S, t);
+            if constexpr (R == 2) t += __shfl_xor_sync(__activemask(), t, 1);
+            scaled_norm<D>(t, S, n, inv);
+        }
+    }
     const float inv_s = inv * (float)kLutScale;
 
     constexpr int NW = (E * BITS + 31) / 32;
@@ -413,8 +436,25 @@ k_encode_tma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t* 
         const float ss = (s0 + s1) + (s2 + s3);
         fwht_reg2<D>(v);
         if (P.two_sided) flip_rotated<D>(v, 0, P.sgn2);
-        const float n = __fsqrt_rn(ss);
-        const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+        float n = __fsqrt_rn(ss);
+        float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+        if (!ss_in_range(ss)) {
+            float m = 0.f;
+            bool nf = false;
+#pragma unroll
+            for (int i = 0; i < D; ++i) {
+                const float a = fabsf(v[i]);
+                nf = nf || !(a <= FLT_MAX);
+                m = fmaxf(m, a);
+            }
+            if (!nf && m > 0.f) {  // squares past fp32's range: the sums again on y S
+                const float S = pow2_scale(m);
+                float t = 0.f;
+#pragma unroll
+                for (int i = 0; i < D; ++i) t = fmaf(v[i] * S, v[i] * S, t);
+                scaled_norm<D>(t, S, n, inv);
+            }
+        }
         const float ks = inv * (float)kLutScale;
         const F2 K2 = f2(ks, ks);
         constexpr float kMagic = 12582912.0f + (float)kLutCenter;
@@ -655,8 +695,45 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
             f2_split(sa, s0, s1);
             f2_split(sb, s2, s3);
             const float ss = (s0 + s1) + (s2 + s3);  // = d * ||x||^2
-            const float n = __fsqrt_rn(ss * (1.0f / 128.0f));
-            const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // w = y / sqrt(ss) = u
+            float n = __fsqrt_rn(ss * (1.0f / 128.0f));
+            float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // w = y / sqrt(ss) = u
+            bool slow = false;  // a coordinate is not finite: binary search below
+            const bool odd = !ss_in_range(ss);
+            if (__any_sync(0xFFFFFFFFu, odd)) {
+                // squares past fp32's range (or a zero or non-finite row): the
+                // sums again on y S (rare; the tensor-memory loads are warp-wide)
+                float m = 0.f;
+                bool nf = false;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(ta + 32 * c, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float a = fabsf(__uint_as_float(y[i]));
+                        nf = nf || !(a <= FLT_MAX);
+                        m = fmaxf(m, a);
+                    }
+                }
+                const float S = (odd && !nf && m > 0.f) ? pow2_scale(m) : 1.f;
+                float t = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(ta + 32 * c, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float a = __uint_as_float(y[i]) * S;
+                        t = fmaf(a, a, t);
+                    }
+                }
+                if (odd) {
+                    if (nf) slow = true;
+                    else if (m > 0.f) scaled_norm<128>(t, S, n, inv);
+                }
+            }
             const float ks = inv * (float)kUmLutScale;
             const F2 K2 = f2(ks, ks);
             uint32_t w[NW];
@@ -689,11 +766,9 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
                     }
                 }
             }
-            // Rows that are not finite (a NaN or infinite coordinate, or
-            // squares past the fp32 range): exact binary search over the
-            // boundaries, as the other encoders take it (the tensor-memory
-            // loads are warp-wide).
-            const bool slow = !(ss <= FLT_MAX);
+            // Rows with a NaN or infinite coordinate: exact binary search over
+            // the boundaries, as the other encoders take it (the
+            // tensor-memory loads are warp-wide).
             if (__any_sync(0xFFFFFFFFu, slow)) {
                 if (slow) {
 #pragma unroll
@@ -953,8 +1028,45 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
             f2_split(sa, s0, s1);
             f2_split(sb, s2, s3);
             const float ss = 2.0f * ((s0 + s1) + (s2 + s3));  // = ||y||^2 = d ||x||^2
-            const float n = __fsqrt_rn(ss * (1.0f / 256.0f));
-            const float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // u = y * inv
+            float n = __fsqrt_rn(ss * (1.0f / 256.0f));
+            float inv = ss > 0.f ? __frcp_rn(__fsqrt_rn(ss)) : 0.f;  // u = y * inv
+            bool slow = false;  // a coordinate is not finite: binary search below
+            const bool odd = !ss_in_range(ss);
+            if (__any_sync(0xFFFFFFFFu, odd)) {
+                // squares past fp32's range (or a zero or non-finite row): the
+                // sums again on A S (rare; the tensor-memory loads are warp-wide)
+                float m = 0.f;
+                bool nf = false;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(ta + 32 * c, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float a = fabsf(__uint_as_float(y[i]));
+                        nf = nf || !(a <= FLT_MAX);
+                        m = fmaxf(m, a);
+                    }
+                }
+                const float S = (odd && !nf && m > 0.f) ? pow2_scale(m) : 1.f;
+                float t = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(ta + 32 * c, y);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float a = __uint_as_float(y[i]) * S;
+                        t = fmaf(a, a, t);
+                    }
+                }
+                if (odd) {
+                    if (nf) slow = true;
+                    else if (m > 0.f) scaled_norm<256>(2.0f * t, S, n, inv);
+                }
+            }
             const float ks = inv * (float)kUmLutScale;
             const F2 K2 = f2(ks, ks);
             const int64_t row = tile * kU2Rows + r;
@@ -1037,12 +1149,10 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                 tmem_wait_ld();
                 bucket_chunk(a0, a1, c);
             }
-            // rows that are not finite (a NaN or infinite coordinate, or
-            // squares past the fp32 range): exact binary search over the
-            // boundaries, written over the fast path's bytes (the
+            // rows with a NaN or infinite coordinate: exact binary search
+            // over the boundaries, written over the fast path's bytes (the
             // tensor-memory loads are warp-wide); a finite row's cells are
             // 64 .. 192, all in the table
-            const bool slow = !(ss <= FLT_MAX);
             if (__any_sync(0xFFFFFFFFu, slow)) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {

@@ -237,6 +237,29 @@ __device__ __forceinline__ void build_lut(LutEntry* lut, const float* bnd, int n
     }
 }
 
+// Rows whose sum of squares leaves fp32's range.  The encoders take a row's
+// norm from its sum of squares; for a row of finite norm that sum can still
+// overflow (norms above about 1.8e19) or underflow (below about 1e-19), and
+// the norm and every index would come out wrong.  Such a row -- and a zero or
+// non-finite one, which share the test -- is measured again on y S, S the
+// power of two that brings the row's largest |y| to [1, 4): an exact
+// scaling, so the normalised coordinates and the stored norm are the ones
+// the unscaled arithmetic would give had it the range.
+__device__ __forceinline__ bool ss_in_range(float ss) { return ss >= 0x1p-120f && ss <= 0x1p+120f; }
+// S = 2^(127 - e) for the biased exponent e of m (m > 0 finite; S <= 2^127).
+__device__ __forceinline__ float pow2_scale(float m) {
+    const uint32_t e = min((__float_as_uint(m) >> 23) & 0xFFu, 253u);
+    return __uint_as_float((254u - e) << 23);
+}
+// Norm and normaliser of a row from ss2 = sum of (y S)^2 over its D
+// coordinates (y = H s x, unnormalised): n = ||x|| = sqrt(ss2 / D) / S and
+// inv = 1 / (sqrt(D) n) = S / sqrt(ss2), so that y * inv = u.
+template <int D>
+__device__ __forceinline__ void scaled_norm(float ss2, float S, float& n, float& inv) {
+    n = __fdiv_rn(__fsqrt_rn(ss2 * (1.0f / (float)D)), S);
+    inv = __frcp_rn(__fsqrt_rn(ss2)) * S;
+}
+
 // Level index of w = y * inv (exact product), via the table.  The cell is
 // rint(w * kLutScale) + kLutCenter, read off the mantissa of a single FMA
 // with 1.5 * 2^23 (its unit in the last place is 1, so the FMA rounds the
@@ -421,8 +444,30 @@ __device__ __forceinline__ float warp_encode_indices(const T* __restrict__ row, 
 #pragma unroll
         for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
     }
-    const float n = __fsqrt_rn(ss);
-    const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+    float n = __fsqrt_rn(ss);
+    float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+    if (!ss_in_range(ss)) {  // warp-uniform: ss is the warp's sum
+        float m = 0.f;
+        bool nf = false;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float a = fabsf(v[e]);
+            nf = nf || !(a <= FLT_MAX);
+            m = fmaxf(m, a);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        nf = __any_sync(0xFFFFFFFFu, nf);
+        if (!nf && m > 0.f) {  // squares past fp32's range: the sums again on y S
+            const float S = pow2_scale(m);
+            float t = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) t = fmaf(v[e] * S, v[e] * S, t);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+            scaled_norm<D>(t, S, n, inv);
+        }
+    }
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         int id = 0;

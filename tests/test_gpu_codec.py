@@ -79,14 +79,60 @@ def test_encode_edge_rows(d):
         assert np.array_equal(idx[k], idx[8])
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [8, 64, 128, 256])
+def test_encode_rows_beyond_fp32_squares(d, dtype):
+    """Rows of finite norm whose sum of squares leaves fp32's range (scalings
+    by 2^+-70 and 2^+-100 of seeded rows), beside in-range ones and a zero
+    row: every encoder (thread per row, TMA-fed, tensor-core at d = 128 and
+    256, bf16 and fp32 rows) gives the oracle's indices, the indices of the
+    unscaled row, and the norm scaled by 2^k."""
+    bits = 4
+    plan = abi.Plan(d, 42)
+    base = synth.normal_rows(123 + d, 6, d).double()
+    ks = (-100, -70, 0, 70, 100)
+    rows = [base[j] * 2.0 ** k for j in range(6) for k in ks] + [torch.zeros(d, dtype=torch.float64)]
+    x = torch.stack(rows).to(dtype)
+    pk, nm = _encode(plan, bits, x)
+    s = O.signs(42, d)
+    compare_encode(s, bits, x.double().numpy(), pk, nm)
+    idx = O.unpack(pk, d, bits)
+    for j in range(6):
+        r0 = j * len(ks) + ks.index(0)
+        for i, k in enumerate(ks):
+            r = j * len(ks) + i
+            assert np.array_equal(idx[r], idx[r0])
+            assert abs(float(nm[r]) / 2.0 ** k / float(nm[r0]) - 1.0) < 1e-6
+    assert nm[-1] == 0.0 and np.all(idx[-1] == 8)
+
+
+def test_append_rows_beyond_fp32_squares():
+    """The append's warp-per-row encoder on rows scaled by 2^+-100."""
+    d, kb, vb, B, Hkv, cap = 128, 4, 2, 1, 2, 8
+    plan = abi.Plan(d, 42)
+    s = O.signs(42, d)
+    cache = abi.Cache.empty(B, Hkv, cap, d, kb, vb)
+    base = synth.normal_rows(77, B * Hkv * 2, d).double()
+    scale = torch.tensor([2.0 ** 100, 2.0 ** -100, 2.0 ** 100, 1.0], dtype=torch.float64)[:, None]
+    k = (base * scale).to(torch.bfloat16).reshape(B, Hkv, 2, d)
+    v = (base * scale.flip(0)).to(torch.bfloat16).reshape(B, Hkv, 2, d)
+    abi.tq_append(plan, cache, k.cuda(), v.cuda(), 3)
+    torch.cuda.synchronize()
+    for x, bits, pk_t, nm_t in ((k, kb, cache.k_packed, cache.k_norm), (v, vb, cache.v_packed, cache.v_norm)):
+        got_pk = pk_t.cpu().numpy()[:, :, 3:5].reshape(-1, d * bits // 8)
+        got_nm = nm_t.cpu().numpy()[:, :, 3:5].reshape(-1)
+        compare_encode(s, bits, x.double().numpy().reshape(-1, d), got_pk, got_nm)
+
+
 @pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_encode_spiky_rotated_rows_bf16(d, bits):
     """bf16 rows whose rotated, normalised coordinates reach |u| = 1 or sit
     near |u| = 0.5: a sign-flipped column of the Hadamard matrix, scaled, plus
-    seeded noise.  The d = 128 and d = 256 encoders bucket |u| < 0.5 through a
-    windowed table and redo any other row by binary search; both must agree
-    with the oracle."""
+    seeded noise.  The d = 128 and d = 256 encoders bucket every finite row
+    through their 1/64-cell table, cells -64 .. 64 included (they once had a
+    window |u| < 0.5 and a binary-search fallback); all must agree with the
+    oracle."""
     s = O.signs(42, d)
     noise = synth.normal_rows(4242 + d, 64, d).double().numpy()
     j = np.arange(d)
