@@ -259,6 +259,32 @@ __device__ __forceinline__ void scaled_norm(float ss2, float S, float& n, float&
     n = __fdiv_rn(__fsqrt_rn(ss2 * (1.0f / (float)D)), S);
     inv = __frcp_rn(__fsqrt_rn(ss2)) * S;
 }
+// The same for a row spread over a warp, E transformed coordinates per lane
+// (call warp-uniformly).  A zero row or one with a non-finite coordinate keeps
+// n and inv.
+template <int D, int E>
+__device__ __forceinline__ void warp_rescaled_norm(const float (&v)[E], float& n, float& inv) {
+    float m = 0.f;
+    bool nf = false;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float a = fabsf(v[e]);
+        nf = nf || !(a <= FLT_MAX);
+        m = fmaxf(m, a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    nf = __any_sync(0xFFFFFFFFu, nf);
+    if (!nf && m > 0.f) {
+        const float S = pow2_scale(m);
+        float t = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) t = fmaf(v[e] * S, v[e] * S, t);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        scaled_norm<D>(t, S, n, inv);
+    }
+}
 
 // Level index of w = y * inv (exact product), via the table.  The cell is
 // rint(w * kLutScale) + kLutCenter, read off the mantissa of a single FMA
@@ -446,28 +472,7 @@ __device__ __forceinline__ float warp_encode_indices(const T* __restrict__ row, 
     }
     float n = __fsqrt_rn(ss);
     float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
-    if (!ss_in_range(ss)) {  // warp-uniform: ss is the warp's sum
-        float m = 0.f;
-        bool nf = false;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float a = fabsf(v[e]);
-            nf = nf || !(a <= FLT_MAX);
-            m = fmaxf(m, a);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        nf = __any_sync(0xFFFFFFFFu, nf);
-        if (!nf && m > 0.f) {  // squares past fp32's range: the sums again on y S
-            const float S = pow2_scale(m);
-            float t = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) t = fmaf(v[e] * S, v[e] * S, t);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-            scaled_norm<D>(t, S, n, inv);
-        }
-    }
+    if (!ss_in_range(ss)) warp_rescaled_norm<D, E>(v, n, inv);  // warp-uniform: ss is the warp's sum
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         int id = 0;

@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(32 * kQjlWarps) k_encode_qjl(const T* __restri
 #pragma unroll
                 for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
             }
-            const float n = __fsqrt_rn(ss);
-            const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+            float n = __fsqrt_rn(ss);
+            float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+            if (!ss_in_range(ss)) warp_rescaled_norm<D, E>(v, n, inv);  // squares past fp32's range
             float rr = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
@@ -578,9 +579,10 @@ __global__ void __launch_bounds__(32 * kQtcWarps, 1) k_encode_qjl_tc(const T* __
 #pragma unroll
                     for (int e = 0; e < E; ++e) v[e] = __uint_as_float(__float_as_uint(v[e]) ^ sg2[lane * E + e]);
                 }
-                const float n = __fsqrt_rn(ss[q]);
+                float n = __fsqrt_rn(ss[q]);
+                float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
+                if (!ss_in_range(ss[q])) warp_rescaled_norm<D, E>(v, n, inv);  // squares past fp32's range
                 ss[q] = n;
-                const float inv = n > 0.f ? __fdiv_rn(P.inv_sqrt_d, n) : 0.f;
                 float rs[E];
                 uint32_t ids = 0u;
                 rr[q] = 0.f;

@@ -92,6 +92,24 @@ def test_encode_parity_ragged(d, bits, dtype):
                       rn.cpu().numpy())
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_encode_rows_beyond_fp32_squares(d, dtype):
+    """Rows of finite norm whose sum of squares leaves fp32's range (2^+-100
+    scalings) beside unscaled ones: indices, signs, norms and gammas as the
+    oracle's."""
+    bits = 4
+    plan = abi.Plan(d, 42)
+    S32 = _s32(42, d)
+    base = synth.normal_rows(4100 + d, 12, d).double()
+    scale = torch.tensor([2.0 ** 100, 2.0 ** -100, 1.0] * 4, dtype=torch.float64)[:, None]
+    x = (base * scale).to(dtype)
+    pk, nm, rn = abi.tq_encode_qjl(plan, bits, torch.from_numpy(S32).cuda(), x.cuda())
+    torch.cuda.synchronize()
+    _check_qjl_encode(O.signs(42, d), bits, x.double().numpy(), S32, pk.cpu().numpy(), nm.cpu().numpy(),
+                      rn.cpu().numpy())
+
+
 @pytest.mark.parametrize("bits", [2, 3, 4])
 def test_codec_parity_several_grid_passes(bits):
     """d = 128, 40,001 bf16 low-rank rows with outlier channels: more rows
