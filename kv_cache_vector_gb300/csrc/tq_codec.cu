@@ -820,8 +820,10 @@ k_encode_umma(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8_t*
 // 2 (||A0||^2 + ||A1||^2) = d ||x||^2), the second signs when the plan has
 // them (they differ between the two output halves, so they are not folded
 // into D_p H), buckets and packs.  The bucketing table is the d = 128 one
-// (count of boundaries below the cell, the boundary inside it) with 16
-// lane-replicated columns of 8 bytes at cell stride 128 bytes.
+// (count of boundaries below the cell, the boundary inside it), one column
+// of 8 bytes per lane at cell stride 256 bytes from a 64 KiB base, so an
+// entry's address is one byte permute; only the rows of finite rows' cells
+// (64 .. 192) are stored, between the barriers and the X stages.
 
 constexpr int kU2Rows = 128;
 constexpr int kU2Stages = 3;               // X halves of 32 KB
@@ -829,16 +831,20 @@ constexpr int kU2Acc = 2;                  // accumulator pairs of 2 x 128 colum
 constexpr int kU2Threads = 10 * 32;
 constexpr int kU2HalfBytes = kU2Rows * 128 * 2;
 constexpr uint32_t kU2HbAt = 2048;                                 // D0 H, D1 H (2 x 32 KB)
-constexpr uint32_t kU2XsAt = kU2HbAt + 2 * 32768;                  // X stages (1024-aligned)
-constexpr uint32_t kU2BarAt = kU2XsAt + kU2Stages * kU2HalfBytes;  // barriers, TMEM slot
-constexpr uint32_t kU2RepAt = 196608;                              // bucketing table (32 KB)
-constexpr uint32_t kU2End = kU2RepAt + kRepCells * 128;  // 16 columns of 8 bytes per cell
-static_assert(kU2XsAt % 1024 == 0, "swizzle atoms");
+constexpr uint32_t kU2BarAt = kU2HbAt + 2 * 32768;                 // barriers, TMEM slot
 constexpr uint32_t kU2SgnAt = kU2BarAt + 256;    // the sign masks s, then s2 (2 x 1 KB)
 constexpr uint32_t kU2CellAt = kU2SgnAt + 2048;  // the table's cells, once each (2 KB)
+constexpr uint32_t kU2RepAt = 65536;             // table row c at kU2RepAt + 256 c (rows 64 .. 192)
+constexpr int kU2RowLo = 64, kU2RowHi = 192;
+constexpr uint32_t kU2XsAt = 115712;             // X stages (1024-aligned), after the table's rows
+constexpr uint32_t kU2End = kU2XsAt + kU2Stages * kU2HalfBytes;
+static_assert(kU2XsAt % 1024 == 0, "swizzle atoms");
 static_assert(kU2BarAt + (2 * kU2Stages + 2 * kU2Acc) * 8 + 16 <= kU2SgnAt, "layout");
-static_assert(kU2CellAt + 8 * kRepCells <= kU2RepAt, "layout");
-static_assert((kU2RepAt & 0x7F80u) == 0, "table base: cell bits free");
+static_assert(kU2CellAt + 8 * kRepCells <= kU2RepAt + 256u * kU2RowLo, "layout");
+static_assert(kU2RepAt + 256u * (kU2RowHi + 1) <= kU2XsAt, "layout");
+static_assert((kU2RepAt & 0xFF00u) == 0, "table base: cell byte free");
+// a non-finite row's cell byte may name any row 0 .. 255: still inside the block's memory
+static_assert(kU2RepAt >= kU2HbAt && kU2RepAt + 256u * 256u <= kU2End, "table rows in range");
 static_assert(kU2End <= 232448, "shared memory");
 
 // TS: the plan's second signs (two-sided), fixed per instantiation so that
@@ -911,11 +917,13 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
             const int off = p * 32768 + (k8 >> 3) * 16384 + n * 128 + (((k8 & 7) ^ (n & 7)) << 4);
             *reinterpret_cast<uint4*>(hb + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        // bucketing table: the cells, replicated into 16 columns (consecutive
-        // lanes write consecutive columns: no bank conflict)
+        // bucketing table: the cells of finite rows, replicated into 32
+        // columns (consecutive threads write consecutive columns)
         const LutEntry* cells = reinterpret_cast<const LutEntry*>(at(kU2CellAt));
-        for (int i = threadIdx.x - 32; i < kRepCells * 16; i += blockDim.x - 32)
-            *reinterpret_cast<LutEntry*>(at(kU2RepAt + 8u * i)) = cells[i >> 4];
+        for (int i = threadIdx.x - 32; i < (kU2RowHi - kU2RowLo + 1) * 32; i += blockDim.x - 32) {
+            const int c = kU2RowLo + (i >> 5);
+            *reinterpret_cast<LutEntry*>(at(kU2RepAt + 256u * c + 8u * (i & 31))) = cells[c];
+        }
         fence_proxy_async_smem();  // the operands are read by the tensor cores
         if (warp == 1) tmem_alloc<kU2Acc * 256>(slot);
         tc_fence_before();
@@ -994,7 +1002,7 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
         const int r = 32 * q + lane;
         constexpr float kMagic = 12582912.0f + (float)(kRepCells / 2);
         const F2 M2 = f2(kMagic, kMagic);
-        const uint32_t rep_slot = kU2RepAt + 8u * (lane & 15);
+        const uint32_t rep_slot = kU2RepAt + 8u * lane;
         int it = wg;
         for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < n_tiles;
              tile += 2 * (int64_t)gridDim.x, it += 2) {
@@ -1132,8 +1140,8 @@ k_encode_umma256(const __grid_constant__ CUtensorMap xmap, int64_t n_rows, uint8
                     float fx, fy;
                     f2_split(f2_fma(f2(ylo, yhi), K2, M2), fx, fy);
                     const uint32_t bx = __float_as_uint(fx), by = __float_as_uint(fy);
-                    const LutEntry e0 = lds_entry(((bx << 7) & 0x7F80u) | rep_slot);
-                    const LutEntry e1 = lds_entry(((by << 7) & 0x7F80u) | rep_slot);
+                    const LutEntry e0 = lds_entry(__byte_perm(bx, rep_slot, 0x7604));
+                    const LutEntry e1 = lds_entry(__byte_perm(by, rep_slot, 0x7604));
                     put(wl, i, e0.lo + (fmaf(ylo, inv, -e0.thr) >= 0.0f ? 1 : 0));
                     put(wh, i, e1.lo + (fmaf(yhi, inv, -e1.thr) >= 0.0f ? 1 : 0));
                 }
