@@ -251,7 +251,7 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
             const float x = __bfloat162float(q[((int64_t)b * Hq + g * G + h) * D + j]);
             qrot[i] = __uint_as_float(__float_as_uint(x) ^ sign_mask(P.sgnb, j));
         }
-        fwht_smem<D>(qrot, G);
+        fwht_rows_warp<D>(qrot, G);
         for (int i = tid; i < G * D; i += blockDim.x) {
             const uint32_t m = P.two_sided ? sign_mask(P.sgn2b, i % D) : 0u;
             qrot[i] = __uint_as_float(__float_as_uint(qrot[i]) ^ m) * (P.inv_sqrt_d * P.scale);
@@ -468,7 +468,7 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
                 const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
                 o[i] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? sign_mask(P.sgn2b, j) : 0u));
             }
-            fwht_smem<D>(o, G);  // synchronises the CTA first
+            fwht_rows_warp<D>(o, G);  // synchronises the CTA first
             for (int i = tid; i < G * D; i += blockDim.x) {
                 const int h = i / D, j = i % D;
                 out[((int64_t)b * Hq + g * G + h) * D + j] = __uint_as_float(__float_as_uint(o[i] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, j));
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(D) k_attn_combine(const float* __restrict__ ws
     }
     const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
     o[j] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? sign_mask(P.sgn2b, j) : 0u));
-    fwht_smem<D>(o, 1);
+    fwht_rows_warp<D>(o, 1);
     out[(int64_t)bh * D + j] = __uint_as_float(__float_as_uint(o[j] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, j));
 }
 
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(D) k_qjl_query(const __nv_bfloat16* __restrict
     const int bh = blockIdx.x, j = threadIdx.x;
     const float x = __bfloat162float(q[(int64_t)bh * D + j]);
     v[j] = __uint_as_float(__float_as_uint(x) ^ sign_mask(P.sgnb, j));
-    fwht_smem<D>(v, 1);
+    fwht_rows_warp<D>(v, 1);
     const uint32_t m = P.two_sided ? sign_mask(P.sgn2b, j) : 0u;
     const float r = __uint_as_float(__float_as_uint(v[j]) ^ m) * (P.inv_sqrt_d * P.scale);
     __syncthreads();

@@ -519,6 +519,37 @@ __device__ void fwht_smem(float* v, int nvec) {
     __syncthreads();
 }
 
+// The same transform with a warp per row: lane l holds elements l E .. l E +
+// E - 1 (E = D / 32); the stages over the element bits run in registers and
+// those over the lane bits by shuffles, in the order len = 1, 2, .., D/2 and
+// with the same adds as fwht_smem, so the result is the same; two CTA
+// barriers instead of log2(D) + 1.  Rows r, r + warps, .. go to warp r.
+template <int D>
+__device__ void fwht_rows_warp(float* v, int nvec) {
+    constexpr int E = D / 32;
+    __syncthreads();  // the rows were written by other threads
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int r = warp; r < nvec; r += nw) {  // warp-uniform
+        float* x = v + r * D + lane * E;
+        float e[E];
+#pragma unroll
+        for (int k = 0; k < E; ++k) e[k] = x[k];
+        fwht_reg<E>(e);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                const float o = __shfl_xor_sync(0xFFFFFFFFu, e[k], m);
+                e[k] = upper ? o - e[k] : e[k] + o;  // (lo + hi, lo - hi)
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < E; ++k) x[k] = e[k];
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------- query rotation (d = 128)
 // One block of 128 threads rotates one query row for the tensor-core
 // attention: q~ = s2 . H (s . q) / sqrt(d) (s2 only with two-sided signs),
