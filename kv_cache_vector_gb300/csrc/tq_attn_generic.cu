@@ -418,16 +418,35 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
         }
     }
     if (P.v_rows && lane == 0 && nread > 0) atomicAdd(P.v_rows + (int64_t)b * Hkv + g, nread);
-    // fixed-order cross-warp reduction
-    for (int w = 0; w < kAttnWarps; ++w) {
-        if (warp == w) {
+    // fixed-order cross-warp reduction: accs = ((0 + acc_0) + acc_1) + ...
+    if (kAttnWarps * G <= 2 * kMaxGroup) {  // block-uniform: the warps' partials fit in qrot and qT
+        // (both free since pass 1): written side by side, then summed in warp
+        // order by every thread for its elements; two barriers instead of one per warp
+        float* part = qrot;  // [kAttnWarps][G][D]
 #pragma unroll
-            for (int h = 0; h < GP; ++h)
-                if (h < G)
+        for (int h = 0; h < GP; ++h)
+            if (h < G)
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) accs[h * D + lane * EPL + e] += acc[h][e];
+                for (int e = 0; e < EPL; ++e) part[(warp * G + h) * D + lane * EPL + e] = acc[h][e];
+        __syncthreads();
+        for (int i = tid; i < G * D; i += blockDim.x) {
+            float a = accs[i];
+#pragma unroll
+            for (int w = 0; w < kAttnWarps; ++w) a += part[w * G * D + i];
+            accs[i] = a;
         }
         __syncthreads();
+    } else {
+        for (int w = 0; w < kAttnWarps; ++w) {
+            if (warp == w) {
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+                    if (h < G)
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) accs[h * D + lane * EPL + e] += acc[h][e];
+            }
+            __syncthreads();
+        }
     }
     if constexpr (!CL) {
         // ---- partials: ws[b][h][split][D + 2] = acc..., m, l
