@@ -456,44 +456,50 @@ k_attn_split(const __nv_bfloat16* __restrict__ q, int Hq, int Hkv, tq_cache_view
             ws[(((int64_t)b * Hq + g * G + h) * n_splits + split) * (D + 2) + j] = v;
         }
     } else {
-        // ---- merge in rank 0: the same arithmetic as k_attn_combine, the
-        // splits in rank order (rank = split)
-        __shared__ float cml[2][8][kMaxGroup];  // rank 0: every split's m and l
-        if (tid < G) {  // handed to rank 0 before the barrier (remote stores)
-            st_cluster_f32(cluster_map(smem_addr(&cml[0][split][tid]), 0), mh[tid]);
-            st_cluster_f32(cluster_map(smem_addr(&cml[1][split][tid]), 0), lh[tid]);
-        }
-        cluster_sync_all();  // every partial is in its CTA's shared memory, m and l in rank 0's
-        if (cluster_rank() == 0) {
-            const uint32_t a_accs = smem_addr(accs);
-            float* o = qrot;  // [G][D], free since pass 1
-            for (int i = tid; i < G * D; i += blockDim.x) {
-                const int h = i / D, j = i % D;
-                float x[8];  // the splits' accumulators, loads all in flight (ranks past the last: the last)
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    x[r] = ld_cluster_f32(cluster_map(a_accs + 4u * i, (uint32_t)(r < n_splits ? r : n_splits - 1)));
-                float M = -FLT_MAX;
-                for (int r = 0; r < n_splits; ++r) M = fmaxf(M, cml[0][r][h]);
-                float L = 0.f, a = 0.f;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (r < n_splits) {
-                        const float f = __expf(cml[0][r][h] - M);
-                        L = fmaf(f, cml[1][r][h], L);
-                        a = fmaf(f, x[r], a);
-                    }
-                }
-                const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
-                o[i] = __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? sign_mask(P.sgn2b, j) : 0u));
+        // ---- merge: the same arithmetic as k_attn_combine, the splits in
+        // rank order (rank = split).  Every rank merges the elements i with
+        // i mod n_splits = its rank, reading the splits' accumulators from
+        // their shared memory, and stores the merged values into rank 0's
+        // buffer; rank 0 then rotates back and writes the output.
+        __shared__ float cml[2][8][kMaxGroup];  // every split's m and l, in every rank
+        if (tid < G) {  // handed to every rank before the barrier (remote stores)
+            for (int r = 0; r < n_splits; ++r) {
+                st_cluster_f32(cluster_map(smem_addr(&cml[0][split][tid]), (uint32_t)r), mh[tid]);
+                st_cluster_f32(cluster_map(smem_addr(&cml[1][split][tid]), (uint32_t)r), lh[tid]);
             }
+        }
+        cluster_sync_all();  // every partial is in its CTA's shared memory, m and l in every rank's
+        const int rank = (int)cluster_rank();
+        float* o = qrot;  // [G][D], free since the cross-warp sum
+        const uint32_t a_accs = smem_addr(accs), o0 = cluster_map(smem_addr(o), 0);
+        for (int i = rank + tid * n_splits; i < G * D; i += blockDim.x * n_splits) {
+            const int h = i / D, j = i % D;
+            float x[8];  // the splits' accumulators, loads all in flight (ranks past the last: the last)
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                x[r] = ld_cluster_f32(cluster_map(a_accs + 4u * i, (uint32_t)(r < n_splits ? r : n_splits - 1)));
+            float M = -FLT_MAX;
+            for (int r = 0; r < n_splits; ++r) M = fmaxf(M, cml[0][r][h]);
+            float L = 0.f, a = 0.f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (r < n_splits) {
+                    const float f = __expf(cml[0][r][h] - M);
+                    L = fmaf(f, cml[1][r][h], L);
+                    a = fmaf(f, x[r], a);
+                }
+            }
+            const float v = L > 0.f ? a / L : 0.f;  // a sequence with no positions gives zeros
+            st_cluster_f32(o0 + 4u * i, __uint_as_float(__float_as_uint(v) ^ (P.two_sided ? sign_mask(P.sgn2b, j) : 0u)));
+        }
+        cluster_sync_all();  // rank 0's buffer is complete; no rank reads another's memory after this
+        if (rank == 0) {
             fwht_rows_warp<D>(o, G);  // synchronises the CTA first
             for (int i = tid; i < G * D; i += blockDim.x) {
                 const int h = i / D, j = i % D;
                 out[((int64_t)b * Hq + g * G + h) * D + j] = __uint_as_float(__float_as_uint(o[i] * P.inv_sqrt_d) ^ sign_mask(P.sgnb, j));
             }
         }
-        cluster_sync_all();  // the peers' memory stays until rank 0 has read it
     }
 }
 
